@@ -1,0 +1,291 @@
+"""fp64 CPU oracle for decode-phase KV-cache attention (test infrastructure).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never does, and this
+package never imports the CUDA library: the two share no code.  The arithmetic
+lives in ``kvd_oracle.c`` (plain loops in double); this module only builds it
+with gcc and marshals arrays.
+
+Every function states what it computes and the page section it follows:
+
+* ``attend_masked`` -- "Intel NPU running LLMs" (OpenVINO community article
+  882), Part 1 "解决方案：预分配 + Attention Mask" and Part 3 "Attention 在 NPU
+  上的完整实现"; "FlashMLA на Huawei Ascend", "Математическая постановка".
+* ``append`` -- same article, Part 2 "NPUW 的核心设计" (update_kvcache_for).
+* ``gather_paged`` -- "PyPTO 实现 AscendC GatherPaKvCache（Norm/ND 分支）",
+  sections 3.1-3.3 and 7.
+* ``attend_paged`` -- gather (above) followed by ``attend_masked`` with an
+  all-ones mask.
+* ``combine`` -- the log-sum-exp merge of disjoint key ranges (Part 3, "Flash
+  SDPA 路径": tiles merged exactly through running max and sum).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kvd_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libkvd_oracle.so")
+
+BF16 = 0
+F32 = 1
+
+ERR_POS = 1
+ERR_BLOCK = 2
+ERR_COLS = 4
+ERR_SEQLENS = 8
+ERR_OFFSET = 16
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/libkvd_oracle.so`` with gcc.
+
+    No fast-math and no floating-point contraction, so the sums are evaluated
+    exactly in the order the C source writes them on every host.
+    """
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", "-std=c11", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = build()
+            L = ctypes.CDLL(path)
+            vp, i32p, dp, u8p = (ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32),
+                                 ctypes.POINTER(ctypes.c_double),
+                                 ctypes.POINTER(ctypes.c_uint8))
+            ci, cd = ctypes.c_int, ctypes.c_double
+            L.kvd_oracle_attend_masked.argtypes = [vp, vp, vp, u8p, ci, ci, ci, ci, ci, ci,
+                                                   cd, dp, dp, ci]
+            L.kvd_oracle_append.argtypes = [vp, vp, vp, vp, i32p, u8p, ci, ci, ci, ci, ci]
+            L.kvd_oracle_gather_paged.argtypes = [vp, vp, i32p, i32p, i32p, vp, vp] + [ci] * 10
+            L.kvd_oracle_attend_paged.argtypes = [vp, vp, vp, i32p, i32p, i32p] + [ci] * 8 + [
+                cd, dp, dp, ci]
+            L.kvd_oracle_combine.argtypes = [dp, dp, ci, ci, ci, dp, dp]
+            L.kvd_oracle_threads.argtypes = []
+            for f in (L.kvd_oracle_attend_masked, L.kvd_oracle_append,
+                      L.kvd_oracle_gather_paged, L.kvd_oracle_attend_paged,
+                      L.kvd_oracle_combine, L.kvd_oracle_threads):
+                f.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def threads() -> int:
+    """Threads the oracle's parallel loops use by default (OpenMP)."""
+    return lib().kvd_oracle_threads()
+
+
+# ---------------------------------------------------------------- marshalling
+
+def _storage(x):
+    """Return (contiguous numpy array holding the raw elements, dtype code).
+
+    Accepts torch CPU tensors (bfloat16 or float32) and numpy float32 arrays;
+    bf16 elements travel as their 16-bit patterns and are widened in C.
+    """
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            if x.dtype == torch.bfloat16:
+                return x.view(torch.int16).numpy().view(np.uint16), BF16
+            if x.dtype == torch.float32:
+                return x.numpy(), F32
+            raise TypeError(f"oracle: unsupported tensor dtype {x.dtype}")
+    except ImportError:  # pragma: no cover - torch is always present here
+        pass
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        return x, F32
+    if x.dtype == np.uint16:
+        return x, BF16
+    raise TypeError(f"oracle: unsupported array dtype {x.dtype}")
+
+
+def _bytes_view(x):
+    """Contiguous numpy view of the raw bytes of a tensor/array (for copies)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            return x.view(torch.uint8).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(x).view(np.uint8)
+
+
+def _i32(x):
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().to(torch.int32).contiguous().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(x, dtype=np.int32)
+
+
+def _u8(x):
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().to(torch.uint8).contiguous().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(x, dtype=np.uint8)
+
+
+def _p(a, t=None):
+    if t is None:
+        return a.ctypes.data_as(ctypes.c_void_p)
+    return a.ctypes.data_as(ctypes.POINTER(t))
+
+
+# ------------------------------------------------------------------ functions
+
+def attend_masked(q, k, v, mask, scale: float, nthreads: int = 0):
+    """Masked decode attention, fp64.
+
+    q [B, Hq, D]; k, v [B, Hkv, C, D]; mask [B, C] (nonzero = valid).
+    Returns (out [B, Hq, D] float64, lse [B, Hq] float64, natural log).
+    """
+    qa, dt = _storage(q)
+    ka, dk = _storage(k)
+    va, dv = _storage(v)
+    if not (dt == dk == dv):
+        raise TypeError("oracle: q, k, v must share one element type")
+    B, Hq, D = qa.shape
+    _, Hkv, C, Dk = ka.shape
+    if Dk != D or va.shape != ka.shape:
+        raise ValueError("oracle: shape mismatch")
+    m = _u8(mask).reshape(B, C) if C > 0 else np.zeros((B, 1), np.uint8)
+    out = np.zeros((B, Hq, D), np.float64)
+    lse = np.zeros((B, Hq), np.float64)
+    rc = lib().kvd_oracle_attend_masked(_p(qa), _p(ka), _p(va), _p(m, ctypes.c_uint8), dt,
+                                        B, Hq, Hkv, C, D, float(scale),
+                                        _p(out, ctypes.c_double), _p(lse, ctypes.c_double),
+                                        int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle attend_masked failed ({rc})")
+    return out, lse
+
+
+def append(k_cache, v_cache, k_new, v_new, pos, mask=None) -> int:
+    """KV append in place on numpy arrays (any element type, byte copy).
+
+    k_cache, v_cache [B, Hkv, C, D] (numpy, modified); k_new, v_new [B, Hkv, D];
+    pos [B]; mask [B, C] uint8 numpy (modified) or None.  Returns error bits.
+    """
+    if not (isinstance(k_cache, np.ndarray) and isinstance(v_cache, np.ndarray)):
+        raise TypeError("oracle.append works in place on numpy arrays")
+    B, Hkv, C, D = k_cache.shape
+    eb = k_cache.dtype.itemsize
+    kn = np.ascontiguousarray(_bytes_view(k_new))
+    vn = np.ascontiguousarray(_bytes_view(v_new))
+    if kn.size != B * Hkv * D * eb or vn.size != kn.size:
+        raise ValueError("oracle.append: new rows have the wrong size")
+    p = _i32(pos)
+    mp = None
+    if mask is not None:
+        if not (isinstance(mask, np.ndarray) and mask.dtype == np.uint8 and mask.flags.c_contiguous):
+            raise TypeError("oracle.append: mask must be a contiguous uint8 numpy array")
+        mp = _p(mask, ctypes.c_uint8)
+    return lib().kvd_oracle_append(_p(k_cache), _p(v_cache), _p(kn), _p(vn),
+                                   _p(p, ctypes.c_int32), mp, B, Hkv, C, D, eb)
+
+
+def gather_paged(key_cache, value_cache, block_tables, seq_lens, seq_offset=None,
+                 total_tokens=None):
+    """gather_pa_kv_cache on numpy arrays (byte copy).
+
+    key_cache [NB, BS, Hk, Dk], value_cache [NB, BS, Hv, Dv] numpy arrays of
+    one element type; block_tables [Q, cols]; seq_lens [Q+1] cumsum;
+    seq_offset [Q] or None.  Returns (key_out, value_out, error bits).
+    Rows that are not written (error cases) stay zero.
+    """
+    kc = np.ascontiguousarray(key_cache)
+    vc = np.ascontiguousarray(value_cache)
+    if kc.dtype != vc.dtype:
+        raise TypeError("oracle.gather_paged: caches must share one element type")
+    NB, BS, Hk, Dk = kc.shape
+    NBv, BSv, Hv, Dv = vc.shape
+    if (NB, BS) != (NBv, BSv):
+        raise ValueError("oracle.gather_paged: caches disagree on blocks")
+    bt = _i32(block_tables)
+    Q, cols = bt.shape
+    sl = _i32(seq_lens)
+    if sl.shape != (Q + 1,):
+        raise ValueError("oracle.gather_paged: only cumsum seq_lens [Q+1] is supported")
+    so = None if seq_offset is None else _i32(seq_offset)
+    T = int(sl[-1]) if total_tokens is None else int(total_tokens)
+    ko = np.zeros((max(T, 0), Hk, Dk), kc.dtype)
+    vo = np.zeros((max(T, 0), Hv, Dv), vc.dtype)
+    err = lib().kvd_oracle_gather_paged(_p(kc), _p(vc), _p(bt, ctypes.c_int32),
+                                        _p(sl, ctypes.c_int32),
+                                        None if so is None else _p(so, ctypes.c_int32),
+                                        _p(ko), _p(vo), Q, NB, BS, cols, Hk, Dk, Hv, Dv, T,
+                                        kc.dtype.itemsize)
+    return ko, vo, err
+
+
+def attend_paged(q, key_cache, value_cache, block_tables, seq_lens, seq_offset, scale: float,
+                 nthreads: int = 0):
+    """Paged decode attention, fp64: gather then attend with all-ones masks.
+
+    q [Q, Hq, D]; caches [NB, BS, Hkv, D]; returns (out [Q, Hq, D], lse [Q, Hq]).
+    """
+    qa, dt = _storage(q)
+    ka, dk = _storage(key_cache)
+    va, dv = _storage(value_cache)
+    if not (dt == dk == dv):
+        raise TypeError("oracle: q and caches must share one element type")
+    Q, Hq, D = qa.shape
+    NB, BS, Hkv, Dk = ka.shape
+    if Dk != D or va.shape != ka.shape:
+        raise ValueError("oracle: shape mismatch")
+    bt = _i32(block_tables)
+    cols = bt.shape[1]
+    sl = _i32(seq_lens)
+    so = None if seq_offset is None else _i32(seq_offset)
+    out = np.zeros((Q, Hq, D), np.float64)
+    lse = np.zeros((Q, Hq), np.float64)
+    rc = lib().kvd_oracle_attend_paged(_p(qa), _p(ka), _p(va), _p(bt, ctypes.c_int32),
+                                       _p(sl, ctypes.c_int32),
+                                       None if so is None else _p(so, ctypes.c_int32),
+                                       dt, Q, Hq, Hkv, NB, BS, cols, D, float(scale),
+                                       _p(out, ctypes.c_double), _p(lse, ctypes.c_double),
+                                       int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle attend_paged failed ({rc})")
+    return out, lse
+
+
+def combine(part_o, part_lse):
+    """Log-sum-exp combine: part_o [R, S, D], part_lse [R, S] -> (out [R, D], lse [R])."""
+    po = np.ascontiguousarray(part_o, dtype=np.float64)
+    pl = np.ascontiguousarray(part_lse, dtype=np.float64)
+    R, S, D = po.shape
+    if pl.shape != (R, S):
+        raise ValueError("oracle.combine: shape mismatch")
+    out = np.zeros((R, D), np.float64)
+    lse = np.zeros((R,), np.float64)
+    lib().kvd_oracle_combine(_p(po, ctypes.c_double), _p(pl, ctypes.c_double), R, S, D,
+                             _p(out, ctypes.c_double), _p(lse, ctypes.c_double))
+    return out, lse

@@ -1,0 +1,346 @@
+/*
+ * kvd_oracle.c -- plain, slow, fp64 CPU oracle for decode-phase KV-cache
+ * attention, KV append, paged gather, paged attention and the log-sum-exp
+ * combine.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may include, link,
+ * load or call this file.  Only the test suite, the smoke check of the graft
+ * entry point and the CPU-baseline leg of the benchmark use it.  It shares no
+ * code, header, constant or helper with the CUDA library; it has its own
+ * element decoding, its own index arithmetic and its own status bits.
+ *
+ * Every function is the direct definition, written out loop by loop: no
+ * blocking, no online softmax, no split of the sequence.  Floating point is
+ * carried in double; bf16 and fp32 inputs are widened exactly.
+ *
+ * Sources (page title, section):
+ *  [NPU-KV]   "Intel NPU running LLMs" (OpenVINO community article 882),
+ *             Part 1 "解决方案：预分配 + Attention Mask" (static buffer of
+ *             capacity MAX_PROMPT_LEN + MIN_RESPONSE_LEN, 0/1 mask, mask=0
+ *             positions set to -inf before the softmax); Part 2 "NPUW 的核心
+ *             设计" (update_kvcache_for writes only the new row at the next
+ *             empty slot); Part 3 "Attention 在 NPU 上的完整实现"
+ *             (decomposed SDPA: Q x K^T, x scale, + mask, softmax, x V);
+ *             Part 5 "当前限制" (over capacity is an error).
+ *  [FlashMLA] "FlashMLA на Huawei Ascend: ядро разреженного внимания
+ *             изнутри", section "Математическая постановка" (P = Q K^T,
+ *             S = softmax(P * sm_scale), out = S V; lse per row).
+ *  [PyPTO]    "PyPTO 实现 AscendC GatherPaKvCache（Norm/ND 分支）", sections
+ *             3.1 (tensor contract), 3.2 (gather semantics: logical_block =
+ *             t // block_size, slot = t % block_size, physical_block =
+ *             block_tables[q, table_offset(q) + logical_block], output row
+ *             seq_lens[q] + t), 3.3 (shape and value constraints), 7 (only
+ *             the cumsum form of seq_lens).
+ *
+ * Parity pins for every function live in tests/test_oracle_*.py (closed
+ * forms, invariants, a library cross-check and brute force on tiny inputs).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* element types of the storage */
+#define ORC_BF16 0
+#define ORC_F32 1
+
+/* error bits reported by the data-movement oracles (own numbering) */
+#define ORC_ERR_POS 1        /* append position outside [0, capacity) */
+#define ORC_ERR_BLOCK 2      /* block id outside [0, num_blocks) */
+#define ORC_ERR_COLS 4       /* table_offset + needed blocks > table columns */
+#define ORC_ERR_SEQLENS 8    /* cumsum not starting at 0, decreasing, or past total */
+#define ORC_ERR_OFFSET 16    /* seq_offset negative or not a multiple of block_size */
+
+/* Exact widening of one stored element to double.  bf16 is the upper half
+ * of an IEEE binary32, so shifting its 16 bits up gives the same number. */
+static double orc_elem(const void* base, size_t i, int dtype) {
+    if (dtype == ORC_BF16) {
+        uint16_t h = ((const uint16_t*)base)[i];
+        uint32_t w = ((uint32_t)h) << 16;
+        float f;
+        memcpy(&f, &w, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float*)base)[i];
+}
+
+int kvd_oracle_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Masked decode attention over a static buffer.
+ *   q    [B, Hq, D]          k, v [B, Hkv, C, D]        mask [B, C] (0 = padding)
+ *   out  [B, Hq, D] double   lse  [B, Hq] double (natural log), may be NULL
+ * Query head h reads kv head h / (Hq / Hkv) (contiguous GQA groups).
+ * Masked slots are excluded from the softmax by selection, which is the
+ * same as adding -inf to their scores for finite contents and stays exact
+ * when the padding holds inf or NaN.  A row with no valid slot gives out = 0
+ * and lse = -inf.
+ */
+int kvd_oracle_attend_masked(const void* q, const void* k, const void* v,
+                             const uint8_t* mask, int dtype, int B, int Hq,
+                             int Hkv, int C, int D, double scale, double* out,
+                             double* lse, int nthreads) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || C < 0 || D <= 0 || Hq % Hkv) return -1;
+    const int g = Hq / Hkv;
+    const long units = (long)B * Hq;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long u = 0; u < units; ++u) {
+        const int b = (int)(u / Hq), h = (int)(u % Hq), kvh = h / g;
+        double* s = (double*)malloc(sizeof(double) * (C > 0 ? C : 1));
+        double* num = (double*)malloc(sizeof(double) * D);
+        if (!s || !num) {
+            free(s);
+            free(num);
+#pragma omp atomic write
+            failed = 1;
+            continue;
+        }
+        const size_t qbase = ((size_t)b * Hq + h) * D;
+        const size_t kvbase = ((size_t)b * Hkv + kvh) * (size_t)C * D;
+        /* pass 1: scores of the valid slots and their maximum */
+        double m = -INFINITY;
+        long nvalid = 0;
+        for (int t = 0; t < C; ++t) {
+            if (!mask[(size_t)b * C + t]) continue;
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += orc_elem(q, qbase + d, dtype) *
+                       orc_elem(k, kvbase + (size_t)t * D + d, dtype);
+            s[t] = scale * dot;
+            if (s[t] > m) m = s[t];
+            ++nvalid;
+        }
+        double* o = out + qbase;
+        if (nvalid == 0) {
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            if (lse) lse[(size_t)b * Hq + h] = -INFINITY;
+            free(s);
+            free(num);
+            continue;
+        }
+        /* pass 2: softmax weights and the weighted sum of V rows */
+        double den = 0.0;
+        for (int d = 0; d < D; ++d) num[d] = 0.0;
+        for (int t = 0; t < C; ++t) {
+            if (!mask[(size_t)b * C + t]) continue;
+            const double w = exp(s[t] - m);
+            den += w;
+            for (int d = 0; d < D; ++d)
+                num[d] += w * orc_elem(v, kvbase + (size_t)t * D + d, dtype);
+        }
+        for (int d = 0; d < D; ++d) o[d] = num[d] / den;
+        if (lse) lse[(size_t)b * Hq + h] = m + log(den);
+        free(s);
+        free(num);
+    }
+    return failed ? -2 : 0;
+}
+
+/*
+ * KV append: row pos[b] of every kv head of k_cache / v_cache [B, Hkv, C, D]
+ * becomes k_new / v_new [B, Hkv, D]; if mask [B, C] is given its slot
+ * pos[b] becomes 1.  A position outside [0, C) writes nothing for that batch
+ * entry and sets ORC_ERR_POS.  Pure byte copy.
+ */
+int kvd_oracle_append(void* k_cache, void* v_cache, const void* k_new,
+                      const void* v_new, const int32_t* pos, uint8_t* mask,
+                      int B, int Hkv, int C, int D, int elem_bytes) {
+    int err = 0;
+    const size_t row = (size_t)D * elem_bytes;
+    for (int b = 0; b < B; ++b) {
+        const int p = pos[b];
+        if (p < 0 || p >= C) {
+            err |= ORC_ERR_POS;
+            continue;
+        }
+        for (int h = 0; h < Hkv; ++h) {
+            const size_t dst = (((size_t)b * Hkv + h) * C + p) * row;
+            const size_t src = ((size_t)b * Hkv + h) * row;
+            memcpy((char*)k_cache + dst, (const char*)k_new + src, row);
+            memcpy((char*)v_cache + dst, (const char*)v_new + src, row);
+        }
+        if (mask) mask[(size_t)b * C + p] = 1;
+    }
+    return err;
+}
+
+/*
+ * Paged gather (gather_pa_kv_cache, Norm/ND branch):
+ *   key_cache [NB, BS, Hk, Dk], value_cache [NB, BS, Hv, Dv]
+ *   block_tables [Q, cols], seq_lens [Q + 1] cumsum with seq_lens[0] = 0,
+ *   seq_offset [Q] or NULL (zeros)
+ *   key_out [total, Hk, Dk], value_out [total, Hv, Dv]
+ * For every sequence q and token t < seq_lens[q+1] - seq_lens[q]:
+ *   physical = block_tables[q, seq_offset[q] / BS + t / BS]
+ *   key_out[seq_lens[q] + t] = key_cache[physical, t % BS]   (same for value)
+ * Checks follow the page's constraints; a violating sequence (or token) is
+ * not written and its error bit is returned.
+ */
+int kvd_oracle_gather_paged(const void* key_cache, const void* value_cache,
+                            const int32_t* block_tables,
+                            const int32_t* seq_lens, const int32_t* seq_offset,
+                            void* key_out, void* value_out, int Q, int NB,
+                            int BS, int cols, int Hk, int Dk, int Hv, int Dv,
+                            int total_tokens, int elem_bytes) {
+    int err = 0;
+    const size_t krow = (size_t)Hk * Dk * elem_bytes;
+    const size_t vrow = (size_t)Hv * Dv * elem_bytes;
+    if (seq_lens[0] != 0) err |= ORC_ERR_SEQLENS;
+    for (int q = 0; q < Q; ++q) {
+        const long start = seq_lens[q], end = seq_lens[q + 1];
+        if (end < start || start < 0 || end > total_tokens) {
+            err |= ORC_ERR_SEQLENS;
+            continue;
+        }
+        const long len = end - start;
+        const long off = seq_offset ? seq_offset[q] : 0;
+        if (off < 0 || off % BS) {
+            err |= ORC_ERR_OFFSET;
+            continue;
+        }
+        const long first_col = off / BS;
+        const long nblocks = (len + BS - 1) / BS;
+        if (first_col + nblocks > cols) {
+            err |= ORC_ERR_COLS;
+            continue;
+        }
+        for (long t = 0; t < len; ++t) {
+            const long logical = t / BS, slot = t % BS;
+            const long phys = block_tables[(size_t)q * cols + first_col + logical];
+            if (phys < 0 || phys >= NB) {
+                err |= ORC_ERR_BLOCK;
+                continue;
+            }
+            memcpy((char*)key_out + (size_t)(start + t) * krow,
+                   (const char*)key_cache + ((size_t)phys * BS + slot) * krow, krow);
+            memcpy((char*)value_out + (size_t)(start + t) * vrow,
+                   (const char*)value_cache + ((size_t)phys * BS + slot) * vrow, vrow);
+        }
+    }
+    return err;
+}
+
+/*
+ * Paged decode attention: for sequence q, the keys and values are the rows
+ * the gather above produces for q (all of them valid), and the query
+ * q_in[q, h, :] attends over them with kv head h / (Hq / Hkv).
+ *   q_in [Q, Hq, D], caches [NB, BS, Hkv, D], out [Q, Hq, D], lse [Q, Hq]
+ * Written as the composition "gather, then masked attention with an
+ * all-ones mask", with no other arithmetic of its own.
+ */
+int kvd_oracle_attend_paged(const void* q_in, const void* key_cache,
+                            const void* value_cache,
+                            const int32_t* block_tables,
+                            const int32_t* seq_lens, const int32_t* seq_offset,
+                            int dtype, int Q, int Hq, int Hkv, int NB, int BS,
+                            int cols, int D, double scale, double* out,
+                            double* lse, int nthreads) {
+    const int eb = dtype == ORC_BF16 ? 2 : 4;
+    if (seq_lens[0] != 0) return ORC_ERR_SEQLENS;
+    const int total = seq_lens[Q];
+    for (int q = 0; q < Q; ++q)
+        if (seq_lens[q + 1] < seq_lens[q]) return ORC_ERR_SEQLENS;
+    const size_t row = (size_t)Hkv * D * eb;
+    char* kg = (char*)malloc(row * (size_t)(total > 0 ? total : 1));
+    char* vg = (char*)malloc(row * (size_t)(total > 0 ? total : 1));
+    if (!kg || !vg) {
+        free(kg);
+        free(vg);
+        return -2;
+    }
+    int err = kvd_oracle_gather_paged(key_cache, value_cache, block_tables,
+                                      seq_lens, seq_offset, kg, vg, Q, NB, BS,
+                                      cols, Hkv, D, Hkv, D, total, eb);
+    if (err) {
+        free(kg);
+        free(vg);
+        return err;
+    }
+    int rc = 0;
+    for (int q = 0; q < Q && rc == 0; ++q) {
+        const int len = seq_lens[q + 1] - seq_lens[q];
+        /* the gathered rows of q, viewed as a [1, len, Hkv, D] block, are
+         * re-laid as [1, Hkv, len, D] for the static-buffer oracle */
+        const size_t e = (size_t)eb;
+        char* kq = (char*)malloc((size_t)Hkv * (len > 0 ? len : 1) * D * e);
+        char* vq = (char*)malloc((size_t)Hkv * (len > 0 ? len : 1) * D * e);
+        uint8_t* ones = (uint8_t*)malloc(len > 0 ? len : 1);
+        if (!kq || !vq || !ones) {
+            free(kq);
+            free(vq);
+            free(ones);
+            rc = -2;
+            break;
+        }
+        for (int t = 0; t < len; ++t) {
+            ones[t] = 1;
+            for (int h = 0; h < Hkv; ++h) {
+                const size_t src = ((size_t)(seq_lens[q] + t) * Hkv + h) * D * e;
+                const size_t dst = ((size_t)h * len + t) * D * e;
+                memcpy(kq + dst, kg + src, D * e);
+                memcpy(vq + dst, vg + src, D * e);
+            }
+        }
+        rc = kvd_oracle_attend_masked((const char*)q_in + (size_t)q * Hq * D * e,
+                                      kq, vq, ones, dtype, 1, Hq, Hkv, len, D,
+                                      scale, out + (size_t)q * Hq * D,
+                                      lse ? lse + (size_t)q * Hq : NULL,
+                                      nthreads);
+        free(kq);
+        free(vq);
+        free(ones);
+    }
+    free(kg);
+    free(vg);
+    return rc;
+}
+
+/*
+ * Log-sum-exp combine of partial results over disjoint key ranges:
+ *   part_o [R, S, D] (each normalised within its range), part_lse [R, S]
+ *   LSE = log sum_s exp(lse_s),  out = sum_s exp(lse_s - LSE) * o_s.
+ * Ranges with lse = -inf carry weight 0; a row whose ranges are all empty
+ * gives out = 0 and LSE = -inf.
+ */
+int kvd_oracle_combine(const double* part_o, const double* part_lse, int R,
+                       int S, int D, double* out, double* lse) {
+    for (int r = 0; r < R; ++r) {
+        double m = -INFINITY;
+        for (int s = 0; s < S; ++s)
+            if (part_lse[(size_t)r * S + s] > m) m = part_lse[(size_t)r * S + s];
+        double* o = out + (size_t)r * D;
+        if (m == -INFINITY) {
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            if (lse) lse[r] = -INFINITY;
+            continue;
+        }
+        double sum = 0.0;
+        for (int s = 0; s < S; ++s) sum += exp(part_lse[(size_t)r * S + s] - m);
+        const double L = m + log(sum);
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        for (int s = 0; s < S; ++s) {
+            const double ls = part_lse[(size_t)r * S + s];
+            if (ls == -INFINITY) continue;
+            const double w = exp(ls - L);
+            for (int d = 0; d < D; ++d)
+                o[d] += w * part_o[((size_t)r * S + s) * D + d];
+        }
+        if (lse) lse[r] = L;
+    }
+    return 0;
+}
