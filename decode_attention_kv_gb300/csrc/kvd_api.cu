@@ -1,0 +1,411 @@
+// kvd_api.cu -- the C ABI of libkvd: argument validation, split planning,
+// tensor-map set-up and kernel launches.  Allocates nothing, never
+// synchronises; every launch goes to the caller's stream.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "attend_split.cuh"
+#include "kvd_internal.h"
+
+namespace kvd {
+cudaError_t launch_attend_bf16(int D, int G, bool paged, const AttendParams& p,
+                               const CUtensorMap* kmap, const CUtensorMap* vmap, dim3 grid,
+                               cudaStream_t stream);
+cudaError_t launch_attend_f32(int D, int G, bool paged, const AttendParams& p,
+                              const CUtensorMap* kmap, const CUtensorMap* vmap, dim3 grid,
+                              cudaStream_t stream);
+AttendGeom attend_geom_bf16(int D);
+AttendGeom attend_geom_f32(int D);
+}  // namespace kvd
+
+using namespace kvd;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+kvd_status fail(kvd_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+kvd_status ok() {
+    g_last_error[0] = '\0';
+    return KVD_OK;
+}
+
+kvd_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(KVD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int elem_size(kvd_dtype dt) { return dt == KVD_BF16 ? 2 : 4; }
+bool dtype_ok(kvd_dtype dt) { return dt == KVD_BF16 || dt == KVD_F32; }
+
+// ----------------------------------------------------------------- planning
+// Splits of the sequence axis.  The planner is a function of the sizes only
+// (not of the device), so that the workspace size queried ahead of a call
+// equals what the call needs.  It aims at about kTargetCtas CTAs per launch
+// (several waves on 152 SMs at two CTAs per SM), with splits of at least
+// kMinChunk slots so that the partial rows stay a small fraction of the
+// KV traffic.
+constexpr long long kTargetCtas = 2048;
+constexpr int kMinChunk = 128;
+
+struct Plan {
+    int G, HG;      // compile-time group width, head groups per kv head
+    int tile;       // tokens per ring stage
+    int chunk;      // tokens per split
+    int S;          // splits
+    size_t ws;      // workspace bytes (0 when S == 1)
+};
+
+int group_width(int g) {
+    int G = 1;
+    while (G < g && G < 8) G <<= 1;
+    return G;
+}
+
+long long gcd_ll(long long a, long long b) {
+    while (b) {
+        const long long t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+AttendGeom geom(kvd_dtype dt, int D) { return dt == KVD_BF16 ? attend_geom_bf16(D) : attend_geom_f32(D); }
+
+// rows: batch entries (or sequences); cap: most tokens a row can hold;
+// BS > 0 for the paged layout.
+Plan plan_attention(int rows, int Hq, int Hkv, int cap, int D, kvd_dtype dt, int BS,
+                    int num_splits) {
+    Plan pl{};
+    const int g = Hq / Hkv;
+    pl.G = group_width(g);
+    pl.HG = (g + pl.G - 1) / pl.G;
+    const int T = geom(dt, D).tile_max;
+    if (BS > 0) {
+        int t = T < BS ? T : BS;
+        while (BS % t) --t;  // largest divisor of BS not above T
+        pl.tile = t;
+    } else {
+        pl.tile = T;
+    }
+    const long long unit = (long long)pl.tile / gcd_ll(pl.tile, 32) * 32;  // lcm(tile, 32)
+    long long max_chunk = kMaxChunk / unit * unit;
+    if (BS > 0) {
+        const long long by_blocks = (long long)(kMaxBlocks - 2) * BS / unit * unit;
+        if (by_blocks < max_chunk) max_chunk = by_blocks;
+    }
+    if (max_chunk < unit) max_chunk = unit;
+    long long chunk;
+    if (num_splits > 0) {
+        chunk = ((long long)cap + num_splits - 1) / num_splits;
+    } else {
+        const long long ctas_per_split = (long long)rows * Hkv * pl.HG;
+        chunk = ((long long)cap * ctas_per_split + kTargetCtas - 1) / kTargetCtas;
+        if (chunk < kMinChunk) chunk = kMinChunk;
+    }
+    chunk = (chunk + unit - 1) / unit * unit;
+    if (chunk > max_chunk) chunk = max_chunk;
+    if (chunk < unit) chunk = unit;
+    pl.chunk = (int)chunk;
+    pl.S = (int)(((long long)cap + chunk - 1) / chunk);
+    if (pl.S < 1) pl.S = 1;
+    if (pl.S > 1) {
+        const size_t R = (size_t)rows * Hq;
+        const size_t po = R * pl.S * D * sizeof(float);
+        const size_t pls = R * pl.S * sizeof(float);
+        pl.ws = (po + 255) / 256 * 256 + pls;
+    }
+    return pl;
+}
+
+// ---------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+cudaError_t get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q != cudaDriverEntryPointSuccess)
+            g_encode_err = cudaErrorNotSupported;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode_err;
+}
+
+// Paged cache [NB, BS, Hkv, D] seen as a 3-D tensor (D, Hkv, NB*BS); one box
+// is one kv head of `tile` consecutive slots.
+kvd_status make_cache_map(CUtensorMap* map, const void* cache, kvd_dtype dt, int NB, int BS,
+                          int Hkv, int D, int tile) {
+    const cudaError_t e = get_encoder();
+    if (e != cudaSuccess || !g_encode) return cuda_fail(e, "cuTensorMapEncodeTiled lookup");
+    const int es = elem_size(dt);
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)NB * BS};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)Hkv * D * es};
+    const cuuint32_t box[3] = {(cuuint32_t)D, 1u, (cuuint32_t)tile};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = g_encode(map,
+                                dt == KVD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                                3, const_cast<void*>(cache), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KVD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return KVD_OK;
+}
+
+cudaError_t launch_attend(kvd_dtype dt, int D, int G, bool paged, const AttendParams& p,
+                          const CUtensorMap* kmap, const CUtensorMap* vmap, dim3 grid,
+                          cudaStream_t s) {
+    return dt == KVD_BF16 ? launch_attend_bf16(D, G, paged, p, kmap, vmap, grid, s)
+                          : launch_attend_f32(D, G, paged, p, kmap, vmap, grid, s);
+}
+
+kvd_status check_attention_shape(int Hq, int Hkv, int D, kvd_dtype dt) {
+    if (Hq < 1 || Hkv < 1) return fail(KVD_ERR_INVALID_ARG, "head counts must be >= 1");
+    if (Hq % Hkv) return fail(KVD_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", Hq, Hkv);
+    if (!dtype_ok(dt)) return fail(KVD_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+    if (D != 64 && D != 128) return fail(KVD_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", D);
+    return KVD_OK;
+}
+
+}  // namespace
+
+// ===================================================================== C ABI
+extern "C" {
+
+const char* kvd_status_string(kvd_status s) {
+    switch (s) {
+        case KVD_OK: return "KVD_OK";
+        case KVD_ERR_INVALID_ARG: return "KVD_ERR_INVALID_ARG";
+        case KVD_ERR_UNSUPPORTED: return "KVD_ERR_UNSUPPORTED";
+        case KVD_ERR_WORKSPACE: return "KVD_ERR_WORKSPACE";
+        case KVD_ERR_CUDA: return "KVD_ERR_CUDA";
+    }
+    return "KVD_ERR_UNKNOWN";
+}
+
+const char* kvd_last_error(void) { return g_last_error; }
+
+int kvd_version(void) { return 10000; }
+
+kvd_status kvd_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                      const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
+                      kvd_dtype dtype, int32_t* dev_status, kvd_stream_t stream) {
+    if (!k_cache || !v_cache || !k_new || !v_new || !pos)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_append: null pointer");
+    if (B < 1 || Hkv < 1 || C < 1 || D < 1)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_append: sizes must be >= 1");
+    if (!dtype_ok(dtype)) return fail(KVD_ERR_INVALID_ARG, "kvd_append: unknown dtype");
+    const long long row = (long long)D * elem_size(dtype);
+    if (row % 16) return fail(KVD_ERR_INVALID_ARG, "kvd_append: D*elem must be a multiple of 16 bytes");
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) ||
+        !aligned(pos, 4) || !aligned(dev_status, 4))
+        return fail(KVD_ERR_INVALID_ARG, "kvd_append: misaligned pointer");
+    if (B > 65535) return fail(KVD_ERR_UNSUPPORTED, "kvd_append: B > 65535");
+    const cudaError_t e = launch_append(k_cache, v_cache, k_new, v_new, pos, mask, B, Hkv, C,
+                                        (int)row, dev_status, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvd_append launch");
+    return ok();
+}
+
+size_t kvd_attend_masked_workspace_bytes(int B, int Hq, int Hkv, int C, int D, kvd_dtype dtype,
+                                         int num_splits) {
+    if (B < 1 || C < 1 || check_attention_shape(Hq, Hkv, D, dtype) != KVD_OK) return 0;
+    return plan_attention(B, Hq, Hkv, C, D, dtype, 0, num_splits).ws;
+}
+
+kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_cache,
+                             const uint8_t* mask, void* out, float* lse_out, int B, int Hq,
+                             int Hkv, int C, int D, float scale, kvd_dtype dtype, int num_splits,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             kvd_stream_t stream) {
+    kvd_status st = check_attention_shape(Hq, Hkv, D, dtype);
+    if (st != KVD_OK) return st;
+    if (B < 0 || C < 1) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked: B >= 0 and C >= 1 required");
+    if (B == 0) return ok();
+    if (!q || !k_cache || !v_cache || !mask || !out)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked: null pointer");
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(lse_out, 4) || !aligned(dev_status, 4))
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked: misaligned pointer");
+    if (B > 65535) return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_masked: B > 65535");
+    if (num_splits < 0) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked: num_splits < 0");
+    const Plan pl = plan_attention(B, Hq, Hkv, C, D, dtype, 0, num_splits);
+    if ((long long)Hkv * pl.HG > 65535) return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_masked: too many heads");
+    if (pl.S > 1) {
+        if (!workspace) return fail(KVD_ERR_WORKSPACE, "kvd_attend_masked: workspace required (%zu bytes)", pl.ws);
+        if (workspace_bytes < pl.ws)
+            return fail(KVD_ERR_WORKSPACE, "kvd_attend_masked: workspace %zu < %zu bytes", workspace_bytes, pl.ws);
+        if (!aligned(workspace, 256)) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked: workspace not 256-byte aligned");
+    }
+    AttendParams p{};
+    p.q = q;
+    p.k = k_cache;
+    p.v = v_cache;
+    p.mask = mask;
+    p.out = out;
+    p.lse_out = lse_out;
+    const size_t R = (size_t)B * Hq;
+    p.part_o = static_cast<float*>(workspace);
+    p.part_lse = pl.S > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                     (R * pl.S * D * sizeof(float) + 255) / 256 * 256)
+                          : nullptr;
+    p.dev_status = dev_status;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.g = Hq / Hkv;
+    p.HG = pl.HG;
+    p.C = C;
+    p.tile = pl.tile;
+    p.chunk = pl.chunk;
+    p.S = pl.S;
+    p.mask_vec = (C % 16 == 0) && aligned(mask, 16);
+    p.qscale = scale * kLog2e;
+    p.direct = pl.S == 1;
+    CUtensorMap dummy;
+    std::memset(&dummy, 0, sizeof dummy);
+    const dim3 grid(pl.S, Hkv * pl.HG, B);
+    cudaError_t e = launch_attend(dtype, D, pl.G, false, p, &dummy, &dummy, grid, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked split launch");
+    if (pl.S > 1) {
+        e = launch_combine(p.part_o, p.part_lse, out, lse_out, (int)R, pl.S, D, dtype, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked combine launch");
+    }
+    return ok();
+}
+
+size_t kvd_attend_paged_workspace_bytes(int Q, int Hq, int Hkv, int BS, int cols, int D,
+                                        kvd_dtype dtype, int num_splits) {
+    if (Q < 1 || BS < 1 || cols < 1 || check_attention_shape(Hq, Hkv, D, dtype) != KVD_OK) return 0;
+    return plan_attention(Q, Hq, Hkv, (int)((long long)cols * BS), D, dtype, BS, num_splits).ws;
+}
+
+kvd_status kvd_attend_paged(const void* q_in, const void* key_cache, const void* value_cache,
+                            const int32_t* block_tables, const int32_t* seq_lens,
+                            const int32_t* seq_offset, void* out, float* lse_out, int Q, int Hq,
+                            int Hkv, int NB, int BS, int cols, int D, float scale,
+                            kvd_dtype dtype, int num_splits, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, kvd_stream_t stream) {
+    kvd_status st = check_attention_shape(Hq, Hkv, D, dtype);
+    if (st != KVD_OK) return st;
+    if (Q < 0 || NB < 1 || BS < 1 || cols < 1)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_paged: Q >= 0, NB, BS, cols >= 1 required");
+    if (Q == 0) return ok();
+    if (!q_in || !key_cache || !value_cache || !block_tables || !seq_lens || !out)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_paged: null pointer");
+    if (!aligned(q_in, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+        !aligned(out, 16) || !aligned(lse_out, 4) || !aligned(block_tables, 4) ||
+        !aligned(seq_lens, 4) || !aligned(seq_offset, 4) || !aligned(dev_status, 4))
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_paged: misaligned pointer");
+    if ((long long)NB * BS >= (1ll << 31)) return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_paged: NB*BS >= 2^31");
+    if ((long long)cols * BS >= (1ll << 31)) return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_paged: cols*BS >= 2^31");
+    if (Q > 65535) return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_paged: Q > 65535");
+    if (num_splits < 0) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_paged: num_splits < 0");
+    const Plan pl = plan_attention(Q, Hq, Hkv, cols * BS, D, dtype, BS, num_splits);
+    if ((long long)Hkv * pl.HG > 65535) return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_paged: too many heads");
+    if (pl.S > 1) {
+        if (!workspace) return fail(KVD_ERR_WORKSPACE, "kvd_attend_paged: workspace required (%zu bytes)", pl.ws);
+        if (workspace_bytes < pl.ws)
+            return fail(KVD_ERR_WORKSPACE, "kvd_attend_paged: workspace %zu < %zu bytes", workspace_bytes, pl.ws);
+        if (!aligned(workspace, 256)) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_paged: workspace not 256-byte aligned");
+    }
+    CUtensorMap kmap, vmap;
+    st = make_cache_map(&kmap, key_cache, dtype, NB, BS, Hkv, D, pl.tile);
+    if (st != KVD_OK) return st;
+    st = make_cache_map(&vmap, value_cache, dtype, NB, BS, Hkv, D, pl.tile);
+    if (st != KVD_OK) return st;
+    AttendParams p{};
+    p.q = q_in;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.seq_offset = seq_offset;
+    p.out = out;
+    p.lse_out = lse_out;
+    const size_t R = (size_t)Q * Hq;
+    p.part_o = static_cast<float*>(workspace);
+    p.part_lse = pl.S > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                     (R * pl.S * D * sizeof(float) + 255) / 256 * 256)
+                          : nullptr;
+    p.dev_status = dev_status;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.g = Hq / Hkv;
+    p.HG = pl.HG;
+    p.BS = BS;
+    p.cols = cols;
+    p.NB = NB;
+    p.tile = pl.tile;
+    p.chunk = pl.chunk;
+    p.S = pl.S;
+    p.qscale = scale * kLog2e;
+    p.direct = pl.S == 1;
+    const dim3 grid(pl.S, Hkv * pl.HG, Q);
+    cudaError_t e = launch_attend(dtype, D, pl.G, true, p, &kmap, &vmap, grid, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_paged split launch");
+    if (pl.S > 1) {
+        e = launch_combine(p.part_o, p.part_lse, out, lse_out, (int)R, pl.S, D, dtype, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_paged combine launch");
+    }
+    return ok();
+}
+
+kvd_status kvd_gather_paged(const void* key_cache, const void* value_cache,
+                            const int32_t* block_tables, const int32_t* seq_lens,
+                            const int32_t* seq_offset, void* key_out, void* value_out, int Q,
+                            int NB, int BS, int cols, int Hk, int Dk, int Hv, int Dv,
+                            int total_tokens, int elem_bytes, int32_t* dev_status,
+                            kvd_stream_t stream) {
+    if (Q < 0 || NB < 1 || BS < 1 || cols < 1 || Hk < 1 || Dk < 1 || Hv < 1 || Dv < 1 ||
+        total_tokens < 0)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_gather_paged: bad sizes");
+    if (elem_bytes != 2 && elem_bytes != 4)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_gather_paged: elem_bytes must be 2 or 4");
+    if (Q == 0) return ok();
+    if (!key_cache || !value_cache || !block_tables || !seq_lens || (total_tokens > 0 && (!key_out || !value_out)))
+        return fail(KVD_ERR_INVALID_ARG, "kvd_gather_paged: null pointer");
+    if (!aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(key_out, 16) ||
+        !aligned(value_out, 16) || !aligned(block_tables, 4) || !aligned(seq_lens, 4) ||
+        !aligned(seq_offset, 4) || !aligned(dev_status, 4))
+        return fail(KVD_ERR_INVALID_ARG, "kvd_gather_paged: misaligned pointer");
+    if ((long long)Q * cols >= (1ll << 31)) return fail(KVD_ERR_UNSUPPORTED, "kvd_gather_paged: Q*cols >= 2^31");
+    const long long krow = (long long)Hk * Dk * elem_bytes, vrow = (long long)Hv * Dv * elem_bytes;
+    const cudaError_t e = launch_gather(key_cache, value_cache, block_tables, seq_lens, seq_offset,
+                                        key_out, value_out, Q, NB, BS, cols, krow, vrow,
+                                        total_tokens, dev_status, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvd_gather_paged launch");
+    return ok();
+}
+
+kvd_status kvd_combine(const float* part_o, const float* part_lse, void* out, float* lse_out,
+                       int R, int S, int D, kvd_dtype out_dtype, kvd_stream_t stream) {
+    if (R < 0 || S < 1 || D < 4 || D % 4 || D > 1024)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_combine: R >= 0, S >= 1, D % 4 == 0 and 4 <= D <= 1024 required");
+    if (!dtype_ok(out_dtype)) return fail(KVD_ERR_INVALID_ARG, "kvd_combine: unknown dtype");
+    if (R == 0) return ok();
+    if (!part_o || !part_lse || !out) return fail(KVD_ERR_INVALID_ARG, "kvd_combine: null pointer");
+    if (!aligned(part_o, 16) || !aligned(out, 16) || !aligned(part_lse, 4) || !aligned(lse_out, 4))
+        return fail(KVD_ERR_INVALID_ARG, "kvd_combine: misaligned pointer");
+    const cudaError_t e = launch_combine(part_o, part_lse, out, lse_out, R, S, D, out_dtype, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvd_combine launch");
+    return ok();
+}
+
+}  // extern "C"

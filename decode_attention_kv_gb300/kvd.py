@@ -1,0 +1,281 @@
+"""Thin ctypes binding of libkvd (argument marshalling only).
+
+Every function passes torch tensors' device pointers and sizes straight to the
+C entry point of the same name (``kvd_<name>``) on the current CUDA stream.
+All computation happens in libkvd's kernels; there is no other code path: if
+the library is not built, or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkvd.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = 0, 1, 2, 3, 4
+BF16, F32 = 0, 1
+
+DEV_POS_RANGE = 1
+DEV_BLOCK_RANGE = 2
+DEV_TABLE_COLS = 4
+DEV_SEQLENS = 8
+DEV_SEQ_OFFSET = 16
+DEV_TIMEOUT = 32
+
+# Entry points of include/kvd.h with their argument types.
+_vp, _sz, _i, _f = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+SIGNATURES = {
+    "kvd_append": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp], _i),
+    "kvd_attend_masked_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
+    "kvd_attend_masked": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz,
+                           _vp, _vp], _i),
+    "kvd_attend_paged_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i, _i], _sz),
+    "kvd_attend_paged": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
+                          _i, _i, _vp, _sz, _vp, _vp], _i),
+    "kvd_gather_paged": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp] + [_i] * 10 + [_vp, _vp], _i),
+    "kvd_combine": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
+    "kvd_status_string": ([_i], ctypes.c_char_p),
+    "kvd_last_error": ([], ctypes.c_char_p),
+    "kvd_version": ([], _i),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KvdError(RuntimeError):
+    def __init__(self, name, status, message):
+        super().__init__(f"{name} failed: {status} ({message})")
+        self.status = status
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libkvd.so (built in-tree by ``_build.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"libkvd.so not found at {p}: build it first "
+                                   "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(p)
+            for name, (args, res) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def _check(name, status):
+    if status != OK:
+        L = load()
+        msg = L.kvd_last_error().decode(errors="replace")
+        raise KvdError(name, L.kvd_status_string(status).decode(), msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(dev):
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _cuda_contig(name, t):
+    if not (t.is_cuda and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def status_tensor(device=None):
+    """A zeroed int32 device word for the kernels' error bits."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+# ------------------------------------------------------------------ append
+
+def append(k_cache, v_cache, k_new, v_new, pos, mask=None, dev_status=None):
+    """kvd_append: write the step's K/V rows at pos[b]; set mask[b, pos[b]]."""
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_new", k_new), ("v_new", v_new),
+                 ("pos", pos)):
+        _cuda_contig(n, t)
+    B, Hkv, C, D = k_cache.shape
+    if v_cache.shape != k_cache.shape or k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D):
+        raise ValueError("append: shape mismatch")
+    if pos.dtype != torch.int32 or pos.numel() != B:
+        raise ValueError("append: pos must be int32 [B]")
+    if mask is not None:
+        _cuda_contig("mask", mask)
+        if mask.dtype != torch.uint8 or mask.shape != (B, C):
+            raise ValueError("append: mask must be uint8 [B, C]")
+    dt = _dtype_code(k_cache)
+    st = load().kvd_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(pos),
+                           _ptr(mask), B, Hkv, C, D, dt, _ptr(dev_status), _stream(k_cache.device))
+    _check("kvd_append", st)
+
+
+# ------------------------------------------------------------------ attention
+
+def attend_masked_workspace_bytes(B, Hq, Hkv, C, D, dtype=torch.bfloat16, num_splits=0):
+    return load().kvd_attend_masked_workspace_bytes(B, Hq, Hkv, C, D,
+                                                    BF16 if dtype == torch.bfloat16 else F32,
+                                                    num_splits)
+
+
+def _workspace(nbytes, device, workspace):
+    if nbytes == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace smaller than {nbytes} bytes")
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def attend_masked(q, k_cache, v_cache, mask, scale=None, out=None, lse=None, num_splits=0,
+                  workspace=None, dev_status=None):
+    """kvd_attend_masked: decode attention over the static buffer.
+
+    q [B, Hq, D]; k_cache, v_cache [B, Hkv, C, D]; mask [B, C] uint8.
+    Returns out [B, Hq, D] (dtype of q); fills ``lse`` [B, Hq] fp32 if given.
+    """
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("mask", mask)):
+        _cuda_contig(n, t)
+    B, Hq, D = q.shape
+    Bk, Hkv, C, Dk = k_cache.shape
+    if Bk != B or Dk != D or v_cache.shape != k_cache.shape or mask.shape != (B, C):
+        raise ValueError("attend_masked: shape mismatch")
+    if mask.dtype != torch.uint8:
+        raise ValueError("attend_masked: mask must be uint8")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("attend_masked: q and caches must share a dtype")
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is not None:
+        _cuda_contig("lse", lse)
+    L = load()
+    need = L.kvd_attend_masked_workspace_bytes(B, Hq, Hkv, C, D, dt, num_splits)
+    ws, wsb = _workspace(need, q.device, workspace)
+    st = L.kvd_attend_masked(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(mask), _ptr(out),
+                             _ptr(lse), B, Hq, Hkv, C, D, float(scale), dt, num_splits, _ptr(ws),
+                             wsb, _ptr(dev_status), _stream(q.device))
+    _check("kvd_attend_masked", st)
+    return out
+
+
+def attend_paged_workspace_bytes(Q, Hq, Hkv, BS, cols, D, dtype=torch.bfloat16, num_splits=0):
+    return load().kvd_attend_paged_workspace_bytes(Q, Hq, Hkv, BS, cols, D,
+                                                   BF16 if dtype == torch.bfloat16 else F32,
+                                                   num_splits)
+
+
+def attend_paged(q, key_cache, value_cache, block_tables, seq_lens, seq_offset=None, scale=None,
+                 out=None, lse=None, num_splits=0, workspace=None, dev_status=None):
+    """kvd_attend_paged: decode attention over the paged cache.
+
+    q [Q, Hq, D]; caches [NB, BS, Hkv, D]; block_tables [Q, cols] int32;
+    seq_lens [Q + 1] int32 cumsum; seq_offset [Q] int32 or None.
+    """
+    for n, t in (("q", q), ("key_cache", key_cache), ("value_cache", value_cache),
+                 ("block_tables", block_tables), ("seq_lens", seq_lens)):
+        _cuda_contig(n, t)
+    Q, Hq, D = q.shape
+    NB, BS, Hkv, Dk = key_cache.shape
+    if Dk != D or value_cache.shape != key_cache.shape:
+        raise ValueError("attend_paged: shape mismatch")
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or block_tables.shape[0] != Q:
+        raise ValueError("attend_paged: block_tables must be int32 [Q, cols]")
+    if seq_lens.dtype != torch.int32 or seq_lens.shape != (Q + 1,):
+        raise ValueError("attend_paged: only cumsum seq_lens [Q+1] int32 is supported")
+    if seq_offset is not None:
+        _cuda_contig("seq_offset", seq_offset)
+        if seq_offset.dtype != torch.int32 or seq_offset.shape != (Q,):
+            raise ValueError("attend_paged: seq_offset must be int32 [Q]")
+    cols = block_tables.shape[1]
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    L = load()
+    need = L.kvd_attend_paged_workspace_bytes(Q, Hq, Hkv, BS, cols, D, dt, num_splits)
+    ws, wsb = _workspace(need, q.device, workspace)
+    st = L.kvd_attend_paged(_ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+                            _ptr(seq_lens), _ptr(seq_offset), _ptr(out), _ptr(lse), Q, Hq, Hkv,
+                            NB, BS, cols, D, float(scale), dt, num_splits, _ptr(ws), wsb,
+                            _ptr(dev_status), _stream(q.device))
+    _check("kvd_attend_paged", st)
+    return out
+
+
+# ------------------------------------------------------------------ gather
+
+def gather_paged(key_cache, value_cache, block_tables, seq_lens, seq_offset=None,
+                 key_out=None, value_out=None, total_tokens=None, dev_status=None):
+    """kvd_gather_paged (gather_pa_kv_cache): copy the pages of every sequence
+    into contiguous [total_tokens, H, D] outputs.  Allocates the outputs when
+    not given; ``total_tokens`` defaults to seq_lens[-1] (read once to size the
+    outputs when they are allocated here)."""
+    for n, t in (("key_cache", key_cache), ("value_cache", value_cache),
+                 ("block_tables", block_tables), ("seq_lens", seq_lens)):
+        _cuda_contig(n, t)
+    NB, BS, Hk, Dk = key_cache.shape
+    NBv, BSv, Hv, Dv = value_cache.shape
+    if (NB, BS) != (NBv, BSv) or key_cache.dtype != value_cache.dtype:
+        raise ValueError("gather_paged: caches disagree on blocks or dtype")
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2:
+        raise ValueError("gather_paged: block_tables must be int32 [Q, cols]")
+    Q, cols = block_tables.shape
+    if seq_lens.dtype != torch.int32 or seq_lens.shape != (Q + 1,):
+        raise ValueError("gather_paged: only cumsum seq_lens [Q+1] int32 is supported")
+    if seq_offset is not None:
+        _cuda_contig("seq_offset", seq_offset)
+    if total_tokens is None:
+        total_tokens = int(key_out.shape[0]) if key_out is not None else int(seq_lens[-1].item())
+    if key_out is None:
+        key_out = torch.empty((total_tokens, Hk, Dk), dtype=key_cache.dtype, device=key_cache.device)
+    if value_out is None:
+        value_out = torch.empty((total_tokens, Hv, Dv), dtype=value_cache.dtype,
+                                device=value_cache.device)
+    if key_out.shape != (total_tokens, Hk, Dk) or value_out.shape != (total_tokens, Hv, Dv):
+        raise ValueError("gather_paged: output shapes must be [total_tokens, H, D]")
+    st = load().kvd_gather_paged(_ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+                                 _ptr(seq_lens), _ptr(seq_offset), _ptr(key_out), _ptr(value_out),
+                                 Q, NB, BS, cols, Hk, Dk, Hv, Dv, total_tokens,
+                                 key_cache.element_size(), _ptr(dev_status),
+                                 _stream(key_cache.device))
+    _check("kvd_gather_paged", st)
+    return key_out, value_out
+
+
+# ------------------------------------------------------------------ combine
+
+def combine(part_o, part_lse, out=None, lse=None, out_dtype=torch.float32):
+    """kvd_combine: log-sum-exp merge of part_o [R, S, D] by part_lse [R, S]."""
+    _cuda_contig("part_o", part_o)
+    _cuda_contig("part_lse", part_lse)
+    R, S, D = part_o.shape
+    if part_lse.shape != (R, S) or part_o.dtype != torch.float32 or part_lse.dtype != torch.float32:
+        raise ValueError("combine: part_o [R,S,D] and part_lse [R,S] fp32 required")
+    if out is None:
+        out = torch.empty((R, D), dtype=out_dtype, device=part_o.device)
+    st = load().kvd_combine(_ptr(part_o), _ptr(part_lse), _ptr(out), _ptr(lse), R, S, D,
+                            _dtype_code(out), _stream(part_o.device))
+    _check("kvd_combine", st)
+    return out

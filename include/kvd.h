@@ -1,0 +1,195 @@
+/*
+ * kvd.h -- C ABI of libkvd: decode-phase KV-cache attention on GB300 (sm_103a).
+ *
+ * One new query token per head attends over a KV cache of fixed capacity,
+ * kept either as a static buffer with a 0/1 mask or as a paged cache
+ * addressed through block tables.  Sources (page title, section):
+ *
+ *  [NPU]    "Intel NPU running LLMs" (OpenVINO community article 882):
+ *           Part 1 "解决方案：预分配 + Attention Mask" -- static buffer of
+ *           capacity MAX_PROMPT_LEN + MIN_RESPONSE_LEN (default 1024 + 128 =
+ *           1152) with a 0/1 mask the length of the buffer, mask = 0 slots
+ *           set to -inf before the softmax; Part 2 "NPUW 的核心设计" --
+ *           update_kvcache_for writes only the new token's row at the next
+ *           empty slot and bumps num_stored_tokens; Part 3 "Attention 在 NPU
+ *           上的完整实现" -- decode is one query against N keys (incremental
+ *           SDPA), tiles along the sequence merged exactly through a running
+ *           output, max and sum (Flash SDPA path); Part 5 "当前限制" -- more
+ *           tokens than the capacity is an error.
+ *  [FlashMLA] "FlashMLA на Huawei Ascend: ядро разреженного внимания
+ *           изнутри", "Математическая постановка" -- out = softmax(Q K^T *
+ *           sm_scale) V per query token; "Ход вычислений" -- fp32 running
+ *           max / sum / output and a log-sum-exp per row.
+ *  [PyPTO]  "PyPTO 实现 AscendC GatherPaKvCache（Norm/ND 分支）" sections
+ *           3.1-3.3 -- key_cache [num_blocks, block_size, heads, dim],
+ *           int32 block_tables [Q, cols], cumsum seq_lens [Q+1] starting at
+ *           0, optional seq_offset [Q] (multiple of block_size, selects the
+ *           first table column), logical_block = t / block_size, slot =
+ *           t % block_size, output row seq_lens[q] + t; section 7 -- only the
+ *           cumsum form of seq_lens and int32 indices.
+ *
+ * Conventions for every entry point:
+ *  - Tensors are caller-owned device memory, contiguous, row-major, in the
+ *    layouts given per call.  The library never allocates, frees, copies to
+ *    the host or synchronises; every call is asynchronous on `stream`.
+ *  - Pointers to element data must be 16-byte aligned; byte masks and int32
+ *    index arrays need only their natural alignment.
+ *  - The return value reports errors the host can see (arguments, sizes,
+ *    launch failures).  Errors that depend on device-resident data set bits
+ *    in the optional caller-owned `dev_status` word (atomic OR, never cleared
+ *    by the library); the offending element is skipped, never written out of
+ *    bounds.  Nothing traps or aborts.
+ *  - Every wait inside a kernel is bounded (about one second); a wait that
+ *    runs out sets KVD_DEV_TIMEOUT and the kernel returns.
+ *  - The caches are plain inputs/outputs of the calls: the caller owns them,
+ *    starts a conversation by zeroing them and appends through kvd_append.
+ */
+#ifndef KVD_H
+#define KVD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* kvd_stream_t;
+
+typedef enum {
+    KVD_OK = 0,
+    KVD_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, bad combination */
+    KVD_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head_dim, dtype, group) */
+    KVD_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+    KVD_ERR_CUDA = 4          /* a CUDA runtime/driver call failed (see kvd_last_error) */
+} kvd_status;
+
+typedef enum { KVD_BF16 = 0, KVD_F32 = 1 } kvd_dtype;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define KVD_DEV_POS_RANGE 1u     /* append position outside [0, capacity) */
+#define KVD_DEV_BLOCK_RANGE 2u   /* block table entry outside [0, num_blocks) */
+#define KVD_DEV_TABLE_COLS 4u    /* seq_offset/BS + ceil(len/BS) > table columns */
+#define KVD_DEV_SEQLENS 8u       /* seq_lens not starting at 0, decreasing, or past total */
+#define KVD_DEV_SEQ_OFFSET 16u   /* seq_offset negative or not a multiple of block_size */
+#define KVD_DEV_TIMEOUT 32u      /* a bounded in-kernel wait ran out */
+
+/*
+ * kvd_append -- [NPU] Part 2, update_kvcache_for: for every batch entry b
+ * and kv head h, row pos[b] of k_cache[b, h] and v_cache[b, h] becomes
+ * k_new[b, h] and v_new[b, h]; if `mask` is given, mask[b, pos[b]] = 1.
+ *   k_cache, v_cache  [B, Hkv, C, D] of `dtype`          (in/out)
+ *   k_new, v_new      [B, Hkv, D] of `dtype`             (in)
+ *   pos               [B] int32, device                  (in)
+ *   mask              [B, C] uint8 or NULL               (in/out)
+ * A byte copy.  pos[b] outside [0, C) writes nothing for b and sets
+ * KVD_DEV_POS_RANGE ([NPU] Part 5: over capacity is an error).
+ * Errors: INVALID_ARG for null pointers, sizes < 1, D*elem not a multiple of
+ * 16 bytes, misaligned data pointers.
+ */
+kvd_status kvd_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                      const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
+                      kvd_dtype dtype, int32_t* dev_status, kvd_stream_t stream);
+
+/*
+ * kvd_attend_masked -- decode attention over the static buffer ([NPU] Part 1
+ * and Part 3; [FlashMLA] "Математическая постановка"):
+ *   out[b, h, :] = sum_t w_t v[b, h/g, t, :] / sum_t w_t,
+ *   w_t = exp(scale * q[b, h, :] . k[b, h/g, t, :] - max), over t with
+ *   mask[b, t] != 0, g = Hq / Hkv (query head h reads kv head h / g).
+ *   lse[b, h] = log sum_t exp(scale * q.k_t) (natural log).
+ *   q         [B, Hq, D] of `dtype`
+ *   k_cache   [B, Hkv, C, D], v_cache [B, Hkv, C, D] of `dtype`
+ *   mask      [B, C] uint8, nonzero = valid; any content in mask = 0 slots
+ *             (inf, NaN) is ignored; all-zero mask tiles are not read
+ *   out       [B, Hq, D] of `dtype` (fp32 result rounded to nearest even)
+ *   lse_out   [B, Hq] float or NULL
+ * A row with no valid slot gives out = 0 and lse = -inf.
+ * The sequence axis is split across CTAs (num_splits; 0 = planned by the
+ * library from the sizes); each split keeps an fp32 running max / sum /
+ * output, and splits are merged by log-sum-exp (kvd_combine).  When more
+ * than one split is used the call needs `workspace` of at least
+ * kvd_attend_masked_workspace_bytes(...) bytes (any contents, 256-byte
+ * aligned); with one split it may be NULL.
+ * Supported: D in {64, 128}; dtype bf16 or f32; any Hq multiple of Hkv.
+ */
+size_t kvd_attend_masked_workspace_bytes(int B, int Hq, int Hkv, int C, int D, kvd_dtype dtype,
+                                         int num_splits);
+kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_cache,
+                             const uint8_t* mask, void* out, float* lse_out, int B, int Hq,
+                             int Hkv, int C, int D, float scale, kvd_dtype dtype, int num_splits,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             kvd_stream_t stream);
+
+/*
+ * kvd_attend_paged -- decode attention over the paged cache: for sequence q
+ * the keys/values are the rows kvd_gather_paged would produce for q
+ * ([PyPTO] 3.2), all valid, and q_in[q, h] attends over them with kv head
+ * h / (Hq / Hkv).  The block-table indirection is resolved in the kernel.
+ *   q_in         [Q, Hq, D] of `dtype`
+ *   key_cache    [NB, BS, Hkv, D], value_cache [NB, BS, Hkv, D] of `dtype`
+ *   block_tables [Q, cols] int32
+ *   seq_lens     [Q + 1] int32, cumsum starting at 0
+ *   seq_offset   [Q] int32 or NULL (zeros); first table column = seq_offset[q] / BS
+ *   out          [Q, Hq, D] of `dtype`;  lse_out [Q, Hq] float or NULL
+ * Device-detected errors (KVD_DEV_SEQLENS, SEQ_OFFSET, TABLE_COLS) make the
+ * sequence empty (out = 0, lse = -inf); an out-of-range block id
+ * (KVD_DEV_BLOCK_RANGE) drops that block's tokens.  A sequence of length 0
+ * gives out = 0, lse = -inf.  Workspace as for kvd_attend_masked.
+ * Supported: D in {64, 128}; bf16 or f32; BS*Hkv*D*elem addressable by a
+ * TMA tensor map (NB*BS < 2^31).
+ */
+size_t kvd_attend_paged_workspace_bytes(int Q, int Hq, int Hkv, int BS, int cols, int D,
+                                        kvd_dtype dtype, int num_splits);
+kvd_status kvd_attend_paged(const void* q_in, const void* key_cache, const void* value_cache,
+                            const int32_t* block_tables, const int32_t* seq_lens,
+                            const int32_t* seq_offset, void* out, float* lse_out, int Q, int Hq,
+                            int Hkv, int NB, int BS, int cols, int D, float scale,
+                            kvd_dtype dtype, int num_splits, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, kvd_stream_t stream);
+
+/*
+ * kvd_gather_paged -- gather_pa_kv_cache, Norm/ND branch ([PyPTO] 3.2):
+ * for every sequence q and t < seq_lens[q+1] - seq_lens[q]:
+ *   phys = block_tables[q, seq_offset[q] / BS + t / BS]
+ *   key_out[seq_lens[q] + t] = key_cache[phys, t % BS]   (all Hk x Dk)
+ *   value_out[seq_lens[q] + t] = value_cache[phys, t % BS] (all Hv x Dv)
+ *   key_cache [NB, BS, Hk, Dk], value_cache [NB, BS, Hv, Dv], elem_bytes 2 or 4
+ *   key_out [total_tokens, Hk, Dk], value_out [total_tokens, Hv, Dv]
+ * A byte copy (bit-exact).  total_tokens must equal seq_lens[Q] and is
+ * passed from the host.  Device-detected errors (SEQLENS, SEQ_OFFSET,
+ * TABLE_COLS) skip the whole sequence; BLOCK_RANGE skips that block's rows;
+ * skipped rows are left untouched.  Rows must be whole multiples of 2 bytes.
+ */
+kvd_status kvd_gather_paged(const void* key_cache, const void* value_cache,
+                            const int32_t* block_tables, const int32_t* seq_lens,
+                            const int32_t* seq_offset, void* key_out, void* value_out, int Q,
+                            int NB, int BS, int cols, int Hk, int Dk, int Hv, int Dv,
+                            int total_tokens, int elem_bytes, int32_t* dev_status,
+                            kvd_stream_t stream);
+
+/*
+ * kvd_combine -- log-sum-exp merge of partial results over disjoint key
+ * ranges ([NPU] Part 3, Flash SDPA path: tiles merged exactly):
+ *   LSE[r] = log sum_s exp(part_lse[r, s]),
+ *   out[r, :] = sum_s exp(part_lse[r, s] - LSE[r]) * part_o[r, s, :]
+ *   part_o [R, S, D] float (each normalised over its range), part_lse [R, S]
+ *   float (natural log, -inf = empty range whose part_o is not read)
+ *   out [R, D] of out_dtype;  lse_out [R] float or NULL
+ * All ranges empty: out = 0, LSE = -inf.  D a multiple of 4, at most 1024.
+ */
+kvd_status kvd_combine(const float* part_o, const float* part_lse, void* out, float* lse_out,
+                       int R, int S, int D, kvd_dtype out_dtype, kvd_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* kvd_status_string(kvd_status status);
+/* Description of the last error returned on the calling thread (static per thread). */
+const char* kvd_last_error(void);
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int kvd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVD_H */

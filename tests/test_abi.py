@@ -1,0 +1,101 @@
+"""CPU checks of the C ABI: the library builds for sm_103a, loads, exports
+every entry point include/kvd.h declares, and rejects bad arguments on the
+host before any CUDA call (no GPU needed for these paths)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from decode_attention_kv_gb300 import _build, kvd
+    _build.build()
+    return kvd.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "kvd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvd_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    syms = declared_symbols()
+    assert len(syms) >= 10
+    from decode_attention_kv_gb300 import kvd
+    for s in syms:
+        assert hasattr(lib, s), f"{s} not exported"
+        assert s in kvd.SIGNATURES, f"{s} has no binding signature"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.kvd_version() == 10000
+    assert lib.kvd_status_string(0) == b"KVD_OK"
+    assert lib.kvd_status_string(3) == b"KVD_ERR_WORKSPACE"
+
+
+def _masked(lib, q=1, k=1, v=1, m=1, out=1, B=2, Hq=8, Hkv=2, C=64, D=128, dt=0, ns=0, ws=None,
+            wsb=0):
+    P = lambda x: None if x is None else ctypes.c_void_p(x * 4096)  # noqa: E731 (aligned fakes)
+    return lib.kvd_attend_masked(P(q), P(k), P(v), P(m), P(out), None, B, Hq, Hkv, C, D, 0.1, dt,
+                                 ns, P(ws), wsb, None, None)
+
+
+def test_masked_host_validation(lib):
+    assert _masked(lib, Hq=6, Hkv=4) == 1            # Hq not a multiple of Hkv
+    assert _masked(lib, D=96) == 2                   # unsupported head_dim
+    assert _masked(lib, dt=7) == 1                   # unknown dtype
+    assert _masked(lib, q=None) == 1                 # null pointer
+    assert _masked(lib, B=0, q=None) == 0            # empty batch: nothing to do
+    assert _masked(lib, C=0) == 1
+    assert _masked(lib, C=4096, ns=4) == 3           # splits need a workspace
+    need = lib.kvd_attend_masked_workspace_bytes(2, 8, 2, 4096, 128, 0, 4)
+    assert need > 0
+    assert _masked(lib, C=4096, ns=4, ws=1, wsb=need - 1) == 3
+    msg = lib.kvd_last_error().decode()
+    assert "workspace" in msg
+    misaligned = lib.kvd_attend_masked(ctypes.c_void_p(4096 + 8), ctypes.c_void_p(4096),
+                                       ctypes.c_void_p(4096), ctypes.c_void_p(4096),
+                                       ctypes.c_void_p(4096), None, 1, 4, 4, 64, 128, 0.1, 0, 0,
+                                       None, 0, None, None)
+    assert misaligned == 1
+
+
+def test_workspace_sizes_follow_the_plan(lib):
+    """Workspace = partial rows + their log-sum-exps for S splits; one split
+    needs none.  The plan depends on the sizes only."""
+    # 16 x 32 heads over capacity 8192: 512 rows
+    ws = lib.kvd_attend_masked_workspace_bytes(16, 32, 8, 8192, 128, 0, 0)
+    R = 16 * 32
+    S = None
+    for s in range(1, 65):
+        po = (R * s * 128 * 4 + 255) // 256 * 256
+        if po + R * s * 4 == ws:
+            S = s
+    assert S is not None and S > 1
+    assert lib.kvd_attend_masked_workspace_bytes(1, 4, 4, 32, 64, 1, 0) == 0  # tiny: one split
+    assert lib.kvd_attend_masked_workspace_bytes(1, 32, 32, 32768, 128, 0, 16) == \
+        (32 * 16 * 128 * 4 + 255) // 256 * 256 + 32 * 16 * 4
+    assert lib.kvd_attend_paged_workspace_bytes(64, 32, 8, 128, 32, 128, 0, 0) > 0
+    assert lib.kvd_attend_masked_workspace_bytes(1, 4, 3, 32, 64, 0, 0) == 0  # invalid -> 0
+
+
+def test_other_entry_points_validate(lib):
+    P = lambda x: ctypes.c_void_p(x * 4096)  # noqa: E731
+    # append: D*elem not a multiple of 16 bytes
+    assert lib.kvd_append(P(1), P(1), P(1), P(1), P(1), None, 1, 1, 8, 6, 0, None, None) == 1
+    # gather: elem_bytes must be 2 or 4
+    assert lib.kvd_gather_paged(P(1), P(1), P(1), P(1), None, P(1), P(1), 1, 4, 16, 2, 1, 64, 1,
+                                64, 10, 8, None, None) == 1
+    assert lib.kvd_gather_paged(P(1), P(1), P(1), P(1), None, P(1), P(1), 0, 4, 16, 2, 1, 64, 1,
+                                64, 0, 2, None, None) == 0  # no sequences
+    # combine: D must be a multiple of 4
+    assert lib.kvd_combine(P(1), P(1), P(1), None, 4, 2, 6, 1, None) == 1
+    assert lib.kvd_combine(P(1), P(1), P(1), None, 0, 2, 8, 1, None) == 0
+    # paged: NB*BS beyond the tensor-map range
+    assert lib.kvd_attend_paged(P(1), P(1), P(1), P(1), P(1), None, P(1), None, 1, 4, 4,
+                                1 << 24, 256, 4, 128, 0.1, 0, 0, None, 0, None, None) == 2

@@ -1,0 +1,30 @@
+"""CPU checks of the benchmark's algorithmic-byte accounting against the
+sizing figures the pages print."""
+import bench
+
+
+def test_kv_bytes_per_layer_llama7b_4096():
+    """A LLaMA-7B layer (32 heads x 128, fp16/bf16) at 4096 tokens holds 64 MB
+    of K and V (PD-disaggregation article, opening paragraph: 64 MB per layer,
+    2 GB per token over 32 layers)."""
+    kv = bench.masked_attend_bytes([4096], 32, 32, 4096, 128, 2)
+    extra = 4096 + 2 * 32 * 128 * 2  # mask row, q and out
+    assert kv - extra == 64 * 2**20
+    assert 32 * (kv - extra) == 2 * 2**30
+
+
+def test_copy_kvcache_volume():
+    """Prefill -> generate copy of 32 layers x (K, V) x 32 heads x 1024 x 128
+    x 2 bytes is 512 MB ("Intel NPU running LLMs", Part 5 '当前限制'); one
+    append row moves read + write of that volume / 1024 per row."""
+    per_row = bench.append_bytes(1, 32, 128, 2)  # read + write, K and V, one layer
+    assert 32 * 1024 * per_row // 2 == 512 * 2**20
+
+
+def test_paged_and_gather_accounting():
+    lengths = [1, 128, 129]
+    rows = sum(lengths)
+    a = bench.paged_attend_bytes(lengths, 32, 8, 128, 2, 128)
+    assert a == rows * 8 * 128 * 2 * 2 + (1 + 1 + 2) * 4 + 4 * 4 + 2 * 3 * 32 * 128 * 2
+    g = bench.gather_bytes(lengths, 8, 128, 1, 64, 2, 128)
+    assert g == 2 * rows * (8 * 128 + 64) * 2 + 4 * 4 + 4 * 4

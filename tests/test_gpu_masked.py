@@ -1,0 +1,209 @@
+"""GPU parity of the static-buffer path (append + masked split-KV attention +
+combine) against the fp64 oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from parity_util import assert_attention_close, assert_lse_close, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvd():
+    from decode_attention_kv_gb300 import kvd as _kvd
+    _kvd.load()
+    return _kvd
+
+
+def _run_masked(kvd, q, k, v, mask, scale, num_splits=0):
+    dev = "cuda"
+    qd, kd, vd, md = (t.to(dev).contiguous() for t in (q, k, v, mask))
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    status = kvd.status_tensor(dev)
+    out = kvd.attend_masked(qd, kd, vd, md, scale, lse=lse, num_splits=num_splits,
+                            dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return out, lse
+
+
+def test_tiny_workload_fp32(kvd):
+    """4-token prompt, appends at 4, 5, 6 with +-1e3 garbage in the padding
+    (fp32, head_dim 64, capacity 32): append bit-exact, attention within the
+    fp32 tolerance after every step."""
+    k, v, mask, steps, scale = W.tiny()
+    kd, vd, md = k.cuda(), v.cuda(), mask.cuda()
+    kh, vh, mh = k.numpy().copy(), v.numpy().copy(), mask.numpy().copy()
+    status = kvd.status_tensor()
+    for st in steps:
+        kvd.append(kd, vd, st["k_new"].cuda(), st["v_new"].cuda(), st["pos"].cuda(), md, status)
+        assert oracle.append(kh, vh, st["k_new"], st["v_new"], st["pos"], mh) == 0
+        torch.cuda.synchronize()
+        assert np.array_equal(host(kd).numpy(), kh) and np.array_equal(host(vd).numpy(), vh)
+        assert np.array_equal(host(md).numpy(), mh)
+        lse = torch.empty(1, 4, device="cuda")
+        out = kvd.attend_masked(st["q"].cuda(), kd, vd, md, scale, lse=lse, dev_status=status)
+        ref, ref_lse = oracle.attend_masked(st["q"], torch.from_numpy(kh), torch.from_numpy(vh),
+                                            torch.from_numpy(mh), scale)
+        assert_attention_close(out, ref, torch.float32, f"tiny step pos={int(st['pos'])}")
+        assert_lse_close(lse, ref_lse)
+    assert int(status.item()) == 0
+
+
+CASES = [
+    # dtype, B, Hq, Hkv, C, D, lengths, num_splits
+    (torch.bfloat16, 3, 8, 2, 1000, 128, [1000, 517, 1], 0),
+    (torch.bfloat16, 2, 32, 8, 2048, 128, [2048, 777], 3),
+    (torch.bfloat16, 2, 4, 4, 300, 64, [300, 33], 0),
+    (torch.bfloat16, 1, 6, 2, 4100, 128, [4099], 0),
+    (torch.float32, 2, 4, 1, 200, 64, [200, 65], 2),
+    (torch.float32, 2, 8, 8, 96, 128, [96, 40], 0),
+    (torch.bfloat16, 1, 16, 1, 640, 128, [639], 5),
+    (torch.bfloat16, 2, 48, 3, 512, 64, [512, 100], 0),
+]
+
+
+@pytest.mark.parametrize("dtype,B,Hq,Hkv,C,D,lengths,num_splits", CASES)
+def test_masked_parity(kvd, dtype, B, Hq, Hkv, C, D, lengths, num_splits):
+    """Several tiles, ragged tails, several splits, group sizes 1..16."""
+    g = W.generator(100 + C + Hq)
+    q = W.randn(g, (B, Hq, D), dtype)
+    k = W.randn(g, (B, Hkv, C, D), dtype)
+    v = W.randn(g, (B, Hkv, C, D), dtype)
+    mask = W.prefix_mask(lengths, C)
+    scale = 1.0 / math.sqrt(D)
+    out, lse = _run_masked(kvd, q, k, v, mask, scale, num_splits)
+    ref, ref_lse = oracle.attend_masked(q, k, v, mask, scale)
+    assert_attention_close(out, ref, dtype, "masked")
+    assert_lse_close(lse, ref_lse, "masked lse")
+
+
+def test_non_prefix_masks_and_skipped_tiles(kvd):
+    """Random sparse masks, a history + current-slot mask, empty rows and
+    mask runs that leave whole tiles empty."""
+    B, Hq, Hkv, C, D = 5, 8, 2, 1500, 128
+    g = W.generator(7)
+    q = W.randn(g, (B, Hq, D))
+    k = W.randn(g, (B, Hkv, C, D))
+    v = W.randn(g, (B, Hkv, C, D))
+    mask = torch.zeros(B, C, dtype=torch.uint8)
+    mask[0] = (torch.rand(C, generator=g) < 0.05).to(torch.uint8)
+    mask[1, :3] = 1
+    mask[1, C - 1] = 1                       # history at the front, current slot last
+    mask[2, 100:140] = 1
+    mask[2, 1300:1301] = 1                   # tiles in between are all zero
+    # row 3 stays empty
+    mask[4] = 1
+    out, lse = _run_masked(kvd, q, k, v, mask, 0.09)
+    ref, ref_lse = oracle.attend_masked(q, k, v, mask, 0.09)
+    assert_attention_close(out, ref, torch.bfloat16, "sparse masks")
+    assert_lse_close(lse, ref_lse)
+    assert torch.all(out[3] == 0) and torch.all(torch.isneginf(lse[3]))
+
+
+@pytest.mark.parametrize("fill", [float("inf"), float("nan"), 1e3])
+def test_garbage_padding_is_ignored(kvd, fill):
+    """inf / NaN / large values in mask = 0 slots leave the GPU result
+    bit-identical to zero padding, and equal to the oracle within tolerance."""
+    B, Hq, Hkv, C, D = 2, 8, 4, 700, 128
+    g = W.generator(8)
+    q = W.randn(g, (B, Hq, D))
+    k = W.randn(g, (B, Hkv, C, D))
+    v = W.randn(g, (B, Hkv, C, D))
+    mask = W.prefix_mask([650, 37], C)
+    mask[0, 10] = 0
+    pad = (mask == 0).view(B, 1, C, 1)
+    out0, lse0 = _run_masked(kvd, q, k.masked_fill(pad, 0), v.masked_fill(pad, 0), mask, 0.1)
+    out1, lse1 = _run_masked(kvd, q, k.masked_fill(pad, fill), v.masked_fill(pad, -fill), mask, 0.1)
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
+    ref, _ = oracle.attend_masked(q, k.masked_fill(pad, fill), v.masked_fill(pad, fill), mask, 0.1)
+    assert_attention_close(out1, ref, torch.bfloat16, "garbage")
+
+
+def test_single_valid_position_is_exact(kvd):
+    B, Hq, Hkv, C, D = 2, 4, 2, 300, 128
+    g = W.generator(9)
+    q = W.randn(g, (B, Hq, D))
+    k = W.randn(g, (B, Hkv, C, D))
+    v = W.randn(g, (B, Hkv, C, D))
+    mask = torch.zeros(B, C, dtype=torch.uint8)
+    mask[0, 0] = 1
+    mask[1, 299] = 1
+    for ns in (0, 3):
+        out, _ = _run_masked(kvd, q, k, v, mask, 0.2, ns)
+        out = host(out)
+        for h in range(Hq):
+            assert torch.equal(out[0, h], v[0, h // 2, 0])
+            assert torch.equal(out[1, h], v[1, h // 2, 299])
+
+
+def test_split_counts_agree(kvd):
+    B, Hq, Hkv, C, D = 2, 8, 2, 3000, 128
+    g = W.generator(10)
+    q = W.randn(g, (B, Hq, D))
+    k = W.randn(g, (B, Hkv, C, D))
+    v = W.randn(g, (B, Hkv, C, D))
+    mask = W.prefix_mask([3000, 1234], C)
+    ref, _ = oracle.attend_masked(q, k, v, mask, 0.1)
+    for ns in (1, 2, 5, 24):
+        out, _ = _run_masked(kvd, q, k, v, mask, 0.1, ns)
+        assert_attention_close(out, ref, torch.bfloat16, f"splits={ns}")
+
+
+def test_append_bit_exact_and_position_errors(kvd):
+    B, Hkv, C, D = 4, 8, 64, 128
+    g = W.generator(11)
+    k = W.randn(g, (B, Hkv, C, D))
+    v = W.randn(g, (B, Hkv, C, D))
+    kn = W.randn(g, (B, Hkv, D))
+    vn = W.randn(g, (B, Hkv, D))
+    mask = torch.zeros(B, C, dtype=torch.uint8)
+    pos = torch.tensor([0, 63, C, -1], dtype=torch.int32)
+    kd, vd, md = k.cuda(), v.cuda(), mask.cuda()
+    status = kvd.status_tensor()
+    kvd.append(kd, vd, kn.cuda(), vn.cuda(), pos.cuda(), md, status)
+    kh = k.view(torch.int16).numpy().copy()
+    vh = v.view(torch.int16).numpy().copy()
+    mh = mask.numpy().copy()
+    err = oracle.append(kh, vh, kn, vn, pos, mh)
+    torch.cuda.synchronize()
+    assert err == oracle.ERR_POS
+    assert int(status.item()) == kvd.DEV_POS_RANGE
+    assert np.array_equal(host(kd).view(torch.int16).numpy(), kh)
+    assert np.array_equal(host(vd).view(torch.int16).numpy(), vh)
+    assert np.array_equal(host(md).numpy(), mh)
+
+
+def test_combine_matches_oracle(kvd):
+    g = W.generator(12)
+    R, S, D = 37, 9, 128
+    po = W.randn(g, (R, S, D), torch.float32)
+    pl = W.randn(g, (R, S), torch.float32) * 3
+    pl[0, :] = float("-inf")
+    pl[1, 3:] = float("-inf")
+    po[1, 3:] = float("nan")  # empty ranges are not read
+    lse = torch.empty(R, device="cuda")
+    for odt in (torch.float32, torch.bfloat16):
+        out = kvd.combine(po.cuda(), pl.cuda(), lse=lse, out_dtype=odt)
+        ref, ref_lse = oracle.combine(po.double().numpy(), pl.double().numpy())
+        assert_attention_close(out, ref, odt, "combine")
+        assert_lse_close(lse, ref_lse)
+
+
+def test_host_side_errors(kvd):
+    q = torch.zeros(1, 4, 128, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 3, 64, 128, dtype=torch.bfloat16, device="cuda")
+    m = torch.ones(1, 64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvd.KvdError) as e:
+        kvd.attend_masked(q, k, k, m, 0.1)
+    assert e.value.status == "KVD_ERR_INVALID_ARG"
+    q2 = torch.zeros(1, 4, 96, dtype=torch.bfloat16, device="cuda")
+    k2 = torch.zeros(1, 4, 64, 96, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(kvd.KvdError) as e:
+        kvd.attend_masked(q2, k2, k2, m, 0.1)
+    assert e.value.status == "KVD_ERR_UNSUPPORTED"
