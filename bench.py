@@ -165,9 +165,12 @@ def bus_id_of(torch, dev):
 # ---------------------------------------------------------------- workloads
 
 class MaskedBench:
-    """Static-buffer workload: per layer append + masked attention."""
+    """Static-buffer workload: every layer appends the step's K/V row and runs
+    masked split-KV attention.  The 1152-slot buffer advances its append slot
+    each step (1024, 1025, ... 1151, then the response part is cleared and the
+    cycle restarts); the other workloads re-append at the last valid slot."""
 
-    def __init__(self, name, torch, kvd, dev, W):
+    def __init__(self, name, torch, kvd, dev):
         import workloads
         self.torch, self.kvd, self.dev, self.name = torch, kvd, dev, name
         if name == "npuw":
@@ -185,97 +188,129 @@ class MaskedBench:
         lay0 = w.layers[0]
         self.B, self.Hq, self.Hkv, self.C, self.D = w.B, w.Hq, w.Hkv, w.C, w.D
         self.elem = 2
+        self.layers = len(w.layers)
         base = lay0.pos.to(torch.int64)
-        # append position of step i: base + (i mod cycle)
+        # append slot of step j: base + (j mod cycle)
         self.pos_table = torch.stack([(base + i).to(torch.int32) for i in range(self.cycle)]).to(dev)
+        self.gpos = self.pos_table[0].clone()
         need = kvd.attend_masked_workspace_bytes(self.B, self.Hq, self.Hkv, self.C, self.D)
         self.ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
         self.splits = need > 0
         self.out = [torch.empty_like(l.q) for l in w.layers]
         self.status = kvd.status_tensor(dev)
         self.lengths0 = [int(x) for x in lay0.lengths]
+        self.graph = None
 
-    @property
-    def layers(self):
-        return len(self.w.layers)
-
-    def lengths_at(self, i):
-        return [L + (i % self.cycle) for L in self.lengths0]
-
-    def reset_if_wrapped(self, i):
-        if self.cycle > 1 and i % self.cycle == 0 and i > 0:
+    def reset_cycle(self):
+        if self.prompt is not None:
             for lay in self.w.layers:
                 lay.mask[:, self.prompt:] = 0
+        self.gpos.copy_(self.pos_table[0])
 
-    def step(self, i, events=None):
-        kvd = self.kvd
-        pos = self.pos_table[i % self.cycle]
+    def _wrap(self, j):
+        if self.cycle > 1 and j > 0 and j % self.cycle == 0:
+            self.reset_cycle()
+
+    def _layer(self, li, lay, pos):
+        self.kvd.append(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, pos, lay.mask, self.status)
+        self.kvd.attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale,
+                               out=self.out[li], workspace=self.ws, dev_status=self.status)
+
+    def eager_run(self, j, timing=False):
+        """One step, one binding call per kernel; with timing, CUDA events
+        around each call."""
+        torch, kvd = self.torch, self.kvd
+        self._wrap(j)
+        pos = self.pos_table[j % self.cycle]
+        evs = []
         for li, lay in enumerate(self.w.layers):
+            if timing:
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                e[0].record()
             kvd.append(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, pos, lay.mask, self.status)
-            if events is not None:
-                events[li][0].record()
+            if timing:
+                e[1].record()
             kvd.attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale,
                               out=self.out[li], workspace=self.ws, dev_status=self.status)
-            if events is not None:
-                events[li][1].record()
+            if timing:
+                e[2].record()
+                evs += [("append", e[0], e[1]), ("attend", e[1], e[2])]
+        return evs
+
+    def capture(self):
+        """The whole step as one CUDA graph; the append slot lives in a device
+        word that the graph itself advances."""
+        torch = self.torch
+        self.reset_cycle()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for li, lay in enumerate(self.w.layers):
+                self._layer(li, lay, self.gpos)
+            if self.cycle > 1:
+                self.gpos.add_(1)
+        self.graph = g
+        self.reset_cycle()
+
+    def graph_run(self, j):
+        self._wrap(j)
+        self.graph.replay()
 
     def launches_per_step(self):
         return self.layers * (2 + (1 if self.splits else 0))
 
-    def attend_bytes(self, i):
-        return masked_attend_bytes(self.lengths_at(i), self.Hq, self.Hkv, self.C, self.D, self.elem)
+    def lengths_at(self, j):
+        return [L + (j % self.cycle) for L in self.lengths0]
 
-    def step_bytes(self, i):
-        return self.layers * (self.attend_bytes(i) + append_bytes(self.B, self.Hkv, self.D, self.elem))
+    def attend_bytes(self, j):
+        return masked_attend_bytes(self.lengths_at(j), self.Hq, self.Hkv, self.C, self.D, self.elem)
+
+    def step_bytes(self, j):
+        return self.layers * (self.attend_bytes(j) + append_bytes(self.B, self.Hkv, self.D, self.elem))
 
     def tokens_per_step(self):
         return self.B
 
     def e2e_setup(self):
         torch = self.torch
-        self.h_q = [torch.empty(l.q.shape, dtype=l.q.dtype, pin_memory=True).copy_(l.q.cpu())
-                    for l in self.w.layers]
-        self.h_kn = [torch.empty(l.k_new.shape, dtype=l.k_new.dtype, pin_memory=True).copy_(l.k_new.cpu())
-                     for l in self.w.layers]
-        self.h_vn = [torch.empty(l.v_new.shape, dtype=l.v_new.dtype, pin_memory=True).copy_(l.v_new.cpu())
-                     for l in self.w.layers]
-        self.h_pos = torch.empty(self.pos_table.shape, dtype=torch.int32, pin_memory=True).copy_(
-            self.pos_table.cpu())
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())  # noqa
+        self.h_q = [pin(l.q) for l in self.w.layers]
+        self.h_kn = [pin(l.k_new) for l in self.w.layers]
+        self.h_vn = [pin(l.v_new) for l in self.w.layers]
+        self.h_pos = pin(self.pos_table)
         self.h_out = [torch.empty(l.q.shape, dtype=l.q.dtype, pin_memory=True) for l in self.w.layers]
         self.d_pos = torch.empty(self.B, dtype=torch.int32, device=self.dev)
         h2d = sum(t.numel() * t.element_size() for t in self.h_q + self.h_kn + self.h_vn) + self.B * 4
         d2h = sum(t.numel() * t.element_size() for t in self.h_out)
         return h2d, d2h
 
-    def e2e_step(self, i):
-        kvd = self.kvd
-        self.d_pos.copy_(self.h_pos[i % self.cycle], non_blocking=True)
+    def e2e_step(self, j):
+        """Host buffers in, host buffers out, through the binding."""
+        self._wrap(j)
+        self.d_pos.copy_(self.h_pos[j % self.cycle], non_blocking=True)
         for li, lay in enumerate(self.w.layers):
             lay.q.copy_(self.h_q[li], non_blocking=True)
             lay.k_new.copy_(self.h_kn[li], non_blocking=True)
             lay.v_new.copy_(self.h_vn[li], non_blocking=True)
-            kvd.append(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, self.d_pos, lay.mask,
-                       self.status)
-            kvd.attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale,
-                              out=self.out[li], workspace=self.ws, dev_status=self.status)
+            self._layer(li, lay, self.d_pos)
             self.h_out[li].copy_(self.out[li], non_blocking=True)
 
     def config(self):
-        e = self.elem
-        ws_bytes = self.layers * 2 * self.B * self.Hkv * self.C * self.D * e
+        cache = self.layers * 2 * self.B * self.Hkv * self.C * self.D * self.elem
+        L = self.lengths0
         return {"workload": self.name, "batch": self.B, "q_heads": self.Hq, "kv_heads": self.Hkv,
                 "head_dim": self.D, "capacity": self.C, "layers": self.layers,
-                "valid_len_step0": (self.lengths0 if len(self.lengths0) <= 4 else
-                                    {"min": min(self.lengths0), "max": max(self.lengths0),
-                                     "mean": sum(self.lengths0) / len(self.lengths0)}),
-                "l2": f"inputs larger than L2: {ws_bytes / 2**30:.2f} GiB of layer caches "
-                      f"rotated per step vs {L2_BYTES // 2**20} MiB L2"}
+                "valid_len_step0": (L if len(L) <= 4 else
+                                    {"min": min(L), "max": max(L), "mean": sum(L) / len(L)}),
+                "l2": f"inputs larger than L2: {cache / 2**30:.2f} GiB of layer caches rotated "
+                      f"per step vs {L2_BYTES // 2**20} MiB L2"}
 
 
 class PagedBench:
-    """Paged workload: gather_pa_kv_cache + paged attention over one cache."""
+    """Paged workload: gather_pa_kv_cache, then paged attention, over the
+    whole 8192-block cache."""
 
-    def __init__(self, torch, kvd, dev, W):
+    def __init__(self, torch, kvd, dev):
         import workloads
         self.torch, self.kvd, self.dev, self.name = torch, kvd, dev, "paged"
         pw = workloads.paged(device=dev)
@@ -283,6 +318,7 @@ class PagedBench:
         self.Q, self.Hq, self.D = pw.q.shape
         self.NB, self.BS, self.Hkv, _ = pw.key_cache.shape
         self.elem = 2
+        self.layers = 1
         self.lengths = [int(x) for x in pw.lengths]
         self.ko = torch.empty((pw.total_tokens, self.Hkv, self.D), dtype=torch.bfloat16, device=dev)
         self.vo = torch.empty_like(self.ko)
@@ -292,38 +328,60 @@ class PagedBench:
         self.ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
         self.splits = need > 0
         self.status = kvd.status_tensor(dev)
-        self.layers = 1
+        self.graph = None
 
-    def step(self, i, events=None, gather_events=None):
-        kvd, pw = self.kvd, self.pw
-        if gather_events is not None:
-            gather_events[0].record()
-        kvd.gather_paged(pw.key_cache, pw.value_cache, pw.block_tables, pw.seq_lens, pw.seq_offset,
-                         self.ko, self.vo, total_tokens=pw.total_tokens, dev_status=self.status)
-        if gather_events is not None:
-            gather_events[1].record()
-        if events is not None:
-            events[0][0].record()
-        kvd.attend_paged(pw.q, pw.key_cache, pw.value_cache, pw.block_tables, pw.seq_lens,
-                         pw.seq_offset, pw.scale, out=self.out, workspace=self.ws,
-                         dev_status=self.status)
-        if events is not None:
-            events[0][1].record()
-
-    def reset_if_wrapped(self, i):
+    def reset_cycle(self):
         pass
+
+    def _gather(self):
+        pw = self.pw
+        self.kvd.gather_paged(pw.key_cache, pw.value_cache, pw.block_tables, pw.seq_lens,
+                              pw.seq_offset, self.ko, self.vo, total_tokens=pw.total_tokens,
+                              dev_status=self.status)
+
+    def _attend(self):
+        pw = self.pw
+        self.kvd.attend_paged(pw.q, pw.key_cache, pw.value_cache, pw.block_tables, pw.seq_lens,
+                              pw.seq_offset, pw.scale, out=self.out, workspace=self.ws,
+                              dev_status=self.status)
+
+    def eager_run(self, j, timing=False):
+        torch = self.torch
+        if not timing:
+            self._gather()
+            self._attend()
+            return []
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        self._gather()
+        e[1].record()
+        self._attend()
+        e[2].record()
+        return [("gather", e[0], e[1]), ("attend", e[1], e[2])]
+
+    def capture(self):
+        torch = self.torch
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self._gather()
+            self._attend()
+        self.graph = g
+
+    def graph_run(self, j):
+        self.graph.replay()
 
     def launches_per_step(self):
         return 2 + (1 if self.splits else 0)
 
-    def attend_bytes(self, i):
+    def attend_bytes(self, j):
         return paged_attend_bytes(self.lengths, self.Hq, self.Hkv, self.D, self.elem, self.BS)
 
     def gather_bytes(self):
         return gather_bytes(self.lengths, self.Hkv, self.D, self.Hkv, self.D, self.elem, self.BS)
 
-    def step_bytes(self, i):
-        return self.attend_bytes(i) + self.gather_bytes()
+    def step_bytes(self, j):
+        return self.attend_bytes(j) + self.gather_bytes()
 
     def tokens_per_step(self):
         return self.Q
@@ -335,36 +393,46 @@ class PagedBench:
         self.h_out = torch.empty(self.pw.q.shape, dtype=self.pw.q.dtype, pin_memory=True)
         return self.h_q.numel() * 2, self.h_out.numel() * 2
 
-    def e2e_step(self, i):
+    def e2e_step(self, j):
         self.pw.q.copy_(self.h_q, non_blocking=True)
-        self.step(i)
+        self._gather()
+        self._attend()
         self.h_out.copy_(self.out, non_blocking=True)
 
     def config(self):
+        rows = 2 * sum(self.lengths) * self.Hkv * self.D * self.elem
         return {"workload": "paged", "num_blocks": self.NB, "block_size": self.BS,
                 "kv_heads": self.Hkv, "q_heads": self.Hq, "head_dim": self.D, "sequences": self.Q,
                 "total_tokens": self.pw.total_tokens,
-                "l2": f"inputs larger than L2: {2 * sum(self.lengths) * self.Hkv * self.D * 2 / 2**30:.2f}"
-                      f" GiB of valid K/V rows per step vs {L2_BYTES // 2**20} MiB L2"}
+                "l2": f"inputs larger than L2: {rows / 2**30:.2f} GiB of valid K/V rows per step "
+                      f"(of a {2 * self.pw.key_cache.numel() * 2 / 2**30:.0f} GiB cache) vs "
+                      f"{L2_BYTES // 2**20} MiB L2"}
 
 
 def make_bench(name, torch, kvd, dev):
     if name == "paged":
-        return PagedBench(torch, kvd, dev, None)
-    return MaskedBench(name, torch, kvd, dev, None)
+        return PagedBench(torch, kvd, dev)
+    return MaskedBench(name, torch, kvd, dev)
 
 
 # ------------------------------------------------------------------- timing
 
-def timed(torch, dist, fn, K, start=0):
+_T0 = time.time()
+
+
+def log(msg):
+    print(f"[bench {time.time() - _T0:7.1f}s] {msg}", file=sys.stderr, flush=True)
+
+
+def timed(torch, dist, fn, K):
     """Barrier + synchronize on both sides; CUDA events on the current stream."""
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for i in range(start, start + K):
-        fn(i)
+    for j in range(K):
+        fn(j)
     e1.record()
     torch.cuda.synchronize()
     if dist is not None:
@@ -388,125 +456,85 @@ def sum_over_ranks(torch, dist, x):
     return float(t.item())
 
 
-def measure_workload(b, torch, dist, K, W, peak, main=False, clocks=None):
-    """Warm-up, the timed K steps, a per-launch event pass for the attention
-    kernel, and (main only) the end-to-end pass and the graph pass."""
+def gate_stream(torch, ms=10):
+    """Hold the stream with a spinning kernel so that the launches queued
+    behind it run back to back, without host gaps between them."""
+    torch.cuda._sleep(int(ms * 1e-3 * 2.0e9))
+
+
+def measure_workload(b, torch, dist, K, W, peak, clocks=None):
+    """Warm-up; the timed K steps (the step captured once as a CUDA graph and
+    replayed K times); CUDA events around every kernel call of K more steps
+    queued behind a spinning kernel (per-launch durations); K eager steps
+    through the binding (host launch overhead included)."""
     res = {}
-    i = 0
-    for _ in range(W):
-        b.reset_if_wrapped(i)
-        b.step(i)
-        i += 1
+    b.reset_cycle()
+    for j in range(W):
+        b.eager_run(j)
     torch.cuda.synchronize()
-
-    def run(j):
-        b.reset_if_wrapped(j)
-        b.step(j)
-
+    log(f"  warm-up done (status {int(b.status.item())}); capturing the step")
+    b.capture()
+    for j in range(3):
+        b.graph_run(j)
+    torch.cuda.synchronize()
+    log(f"  graph replays done (status {int(b.status.item())})")
+    b.reset_cycle()
     if clocks is not None:
         clocks.start()
-        soak_end = time.time() + 0.6  # fill a few sampling intervals before the timed steps
+        soak_end, j = time.time() + 0.6, 0  # a few sampling intervals before the timed steps
         while time.time() < soak_end:
-            run(i)
-            i += 1
+            b.graph_run(j)
+            j += 1
             torch.cuda.synchronize()
-    start = i
-    ms = timed(torch, dist, run, K, start)
+        b.reset_cycle()
+    ms = timed(torch, dist, b.graph_run, K)
     if clocks is not None:
         res["clocks"] = clocks.stop()
-    i += K
-    step_bytes = sum(b.step_bytes(j) for j in range(start, start + K))
     ms = max_over_ranks(torch, dist, ms)
-    total_bytes = sum_over_ranks(torch, dist, step_bytes)
+    total = sum_over_ranks(torch, dist, sum(b.step_bytes(j) for j in range(K)))
     res["ms_per_step"] = ms / K
-    res["gbs"] = total_bytes / (ms / 1e3) / 1e9
+    res["gbs"] = total / (ms / 1e3) / 1e9
     res["tokens_per_s"] = sum_over_ranks(torch, dist, b.tokens_per_step() * K) / (ms / 1e3)
 
-    # per-launch attention durations (CUDA events around each attention call)
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(b.layers)] for _ in range(K)]
-    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)] if isinstance(b, PagedBench) else None
+    log(f"  timed steps done: {ms / K:.3f} ms/step; per-launch pass")
+    b.reset_cycle()
+    ev = []
+    for j in range(K):  # one step per gate: its launches fit in the launch queue
+        torch.cuda.synchronize()
+        gate_stream(torch)
+        ev.append(b.eager_run(j, timing=True))
     torch.cuda.synchronize()
-    for k in range(K):
-        b.reset_if_wrapped(i + k)
-        if gev is not None:
-            b.step(i + k, events=evs[k], gather_events=gev[k])
-        else:
-            b.step(i + k, events=evs[k])
-    torch.cuda.synchronize()
-    durs = [s.elapsed_time(e) for row in evs for (s, e) in row]
-    attend_bytes = sum(b.attend_bytes(i + k) for k in range(K)) / K
-    avg_ms = sum(durs) / len(durs)
-    achieved = attend_bytes / (avg_ms / 1e3) / 1e9
-    res["attend_ms_per_launch"] = avg_ms
-    res["attend_gbs"] = achieved
-    res["attend_frac"] = achieved / peak
-    if gev is not None:
-        gd = [s.elapsed_time(e) for (s, e) in gev]
-        g_ms = sum(gd) / len(gd)
-        res["gather_ms_per_launch"] = g_ms
-        res["gather_gbs"] = b.gather_bytes() / (g_ms / 1e3) / 1e9
+    for kind in ("attend", "append", "gather"):
+        d = [s.elapsed_time(e) for row in ev for (k2, s, e) in row if k2 == kind]
+        if d:
+            res[kind + "_ms_per_launch"] = sum(d) / len(d)
+    a_bytes = sum(b.attend_bytes(j) for j in range(K)) / K
+    res["attend_gbs"] = a_bytes / (res["attend_ms_per_launch"] / 1e3) / 1e9
+    res["attend_frac"] = res["attend_gbs"] / peak
+    if "gather_ms_per_launch" in res:
+        res["gather_gbs"] = b.gather_bytes() / (res["gather_ms_per_launch"] / 1e3) / 1e9
         res["gather_frac"] = res["gather_gbs"] / peak
-    i += K
-    res["_next_step"] = i
+
+    b.reset_cycle()
+    ms_e = max_over_ranks(torch, dist, timed(torch, dist, b.eager_run, K))
+    res["eager"] = {"gbs": sum_over_ranks(torch, dist, sum(b.step_bytes(j) for j in range(K)))
+                    / (ms_e / 1e3) / 1e9, "ms_per_step": ms_e / K}
+    b.reset_cycle()
     return res
 
 
-def measure_e2e(b, torch, dist, K, start):
+def measure_e2e(b, torch, dist, K):
     h2d, d2h = b.e2e_setup()
+    b.reset_cycle()
     for j in range(3):
-        b.reset_if_wrapped(start + j)
-        b.e2e_step(start + j)
-    torch.cuda.synchronize()
-    start += 3
-
-    def run(j):
-        b.reset_if_wrapped(j)
         b.e2e_step(j)
-
-    ms = timed(torch, dist, run, K, start)
-    ms = max_over_ranks(torch, dist, ms)
-    total = sum_over_ranks(torch, dist, sum(b.step_bytes(j) for j in range(start, start + K)))
+    torch.cuda.synchronize()
+    b.reset_cycle()
+    ms = max_over_ranks(torch, dist, timed(torch, dist, b.e2e_step, K))
+    total = sum_over_ranks(torch, dist, sum(b.step_bytes(j) for j in range(K)))
+    b.reset_cycle()
     return {"value": total / (ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms / K}, start + K
-
-
-def measure_graph(b, torch, K, start):
-    """The same steps captured once as a CUDA graph (launch overhead removed);
-    the append position advances inside the graph."""
-    if not isinstance(b, MaskedBench):
-        return None
-    pos = b.pos_table[0].clone()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for li, lay in enumerate(b.w.layers):
-            b.kvd.append(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, pos, lay.mask, b.status)
-            b.kvd.attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale,
-                                out=b.out[li], workspace=b.ws, dev_status=b.status)
-        if b.cycle > 1:
-            pos.add_(1)
-    # restart the position cycle
-    for lay in b.w.layers:
-        if b.prompt is not None:
-            lay.mask[:, b.prompt:] = 0
-    pos.copy_(b.pos_table[0])
-    n = min(K, b.cycle) if b.cycle > 1 else K
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(n):
-        g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    total = sum(b.step_bytes(j) for j in range(n))
-    for lay in b.w.layers:
-        if b.prompt is not None:
-            lay.mask[:, b.prompt:] = 0
-    return {"gbs": total / (ms / 1e3) / 1e9, "ms_per_step": ms / n,
-            "tokens_per_s": b.tokens_per_step() * n / (ms / 1e3), "steps": n}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / K}
 
 
 # -------------------------------------------------------------- CPU oracle
@@ -639,40 +667,46 @@ def main():
     kvd.load()
     peak, peak_src = measured_peak()
 
+    log(f"workload {args.workload}: building inputs")
     b = make_bench(args.workload, torch, kvd, dev)
     clocks = ClockSampler(bus_id_of(torch, dev))
-    res = measure_workload(b, torch, dist, args.steps, args.warmup, peak, main=True, clocks=clocks)
-    e2e, nxt = measure_e2e(b, torch, dist, args.steps, res["_next_step"])
-    graph = measure_graph(b, torch, args.steps, nxt) if world == 1 else None
+    log("timed steps")
+    res = measure_workload(b, torch, dist, args.steps, args.warmup, peak, clocks=clocks)
+    log(f"{args.workload}: {res['ms_per_step']:.3f} ms/step, {res['gbs']:.0f} GB/s; "
+        f"attention {res['attend_ms_per_launch'] * 1e3:.1f} us/launch; e2e pass")
+    e2e = measure_e2e(b, torch, dist, args.steps)
     st = int(b.status.item())
     if st != 0:
         raise RuntimeError(f"device status {st} during the benchmark")
 
-    traffic = None
-    key = (args.workload, kernel_source_hash())
-    if key in NCU_TRAFFIC:
-        traffic = NCU_TRAFFIC[key]
+    traffic = NCU_TRAFFIC.get((args.workload, kernel_source_hash()))
 
     others = {}
     if not args.no_others:
         for name in ("gqa", "long", "paged", "npuw"):
             if name == args.workload:
                 continue
+            log(f"workload {name}")
             ob = make_bench(name, torch, kvd, dev)
             r = measure_workload(ob, torch, dist, max(5, min(args.steps, 20)), 3, peak)
-            ent = {"gbs": r["gbs"], "frac_of_" + peak_src: r["gbs"] / peak,
-                   "ms_per_step": r["ms_per_step"], "tokens_per_s": r["tokens_per_s"],
-                   "attend_gbs": r["attend_gbs"], "attend_frac": r["attend_frac"],
-                   "attend_ms_per_launch": r["attend_ms_per_launch"], "config": ob.config()}
-            if "gather_gbs" in r:
-                ent.update(gather_gbs=r["gather_gbs"], gather_frac=r["gather_frac"],
-                           gather_ms_per_launch=r["gather_ms_per_launch"])
+            if int(ob.status.item()) != 0:
+                raise RuntimeError(f"device status {int(ob.status.item())} in workload {name}")
+            ent = {"gbs": r["gbs"], "frac": r["gbs"] / peak, "ms_per_step": r["ms_per_step"],
+                   "tokens_per_s": r["tokens_per_s"], "attend_gbs": r["attend_gbs"],
+                   "attend_frac": r["attend_frac"],
+                   "attend_ms_per_launch": r["attend_ms_per_launch"], "eager": r["eager"],
+                   "config": ob.config()}
+            for k in ("append_ms_per_launch", "gather_gbs", "gather_frac", "gather_ms_per_launch"):
+                if k in r:
+                    ent[k] = r[k]
+            log(f"{name}: {r['gbs']:.0f} GB/s, attention {r['attend_gbs']:.0f} GB/s")
             others[name] = ent
             del ob
             torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1:
+        log("cpu baseline (oracle)")
         try:
             v, cores, sample = oracle_rate(args.workload, args.cpu_seconds)
             cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
@@ -687,13 +721,16 @@ def main():
             "data": "synthetic", "config": b.config(),
             "frac_of_hbm_peak": res["gbs"] / peak, "peak_source": peak_src,
             "decode_tokens_per_s": res["tokens_per_s"],
+            "timing": "each timed step is one CUDA-graph replay of the decode step "
+                      "(all layers' kvd kernels); 'eager' = one binding call per kernel",
             "roofline": {"bound": "hbm", "achieved": res["attend_gbs"], "peak": peak, "unit": "GB/s",
                          "frac": res["attend_frac"], "traffic": traffic,
-                         "kernel": "attention (split-KV kernel + combine), per layer",
-                         "ms_per_launch": res["attend_ms_per_launch"],
-                         "peak_source": peak_src},
-            "e2e": e2e, "gpu_launches": b.launches_per_step() * args.steps,
-            "clocks": res.get("clocks"), "cuda_graph": graph, "cpu_baseline": cpu,
+                         "kernel": "attention per layer (split-KV kernel + combine)",
+                         "ms_per_launch": res["attend_ms_per_launch"], "peak_source": peak_src},
+            "append_ms_per_launch": res.get("append_ms_per_launch"),
+            "eager": res["eager"], "e2e": e2e,
+            "gpu_launches": b.launches_per_step() * args.steps,
+            "clocks": res.get("clocks"), "cpu_baseline": cpu,
             "workloads": others, "kernel_hash": kernel_source_hash(),
         }
         print(json.dumps(line), flush=True)

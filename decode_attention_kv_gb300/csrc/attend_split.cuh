@@ -296,13 +296,17 @@ attend_split_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
             if (failed) {
                 *abort_flag = 1;
                 report(p.dev_status, KVD_DEV_TIMEOUT);
+                // The consumers may leave early now: never let the CTA exit
+                // while a copy issued here may still be writing the ring.
+                // (On the normal path the consumers have waited for every
+                // issued tile before they see the end marker, and the end
+                // marker itself completes a phase, so no drain is needed.)
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_mask & (1u << s)) {
+                        const volatile int never = 0;
+                        mbar_wait(&full[s], (last_parity >> s) & 1u, &never);
+                    }
             }
-            // Never leave while a copy issued here may still be writing the ring.
-            for (int s = 0; s < STAGES; ++s)
-                if (issued_mask & (1u << s)) {
-                    const volatile int never = 0;
-                    mbar_wait(&full[s], (last_parity >> s) & 1u, &never);
-                }
         }
         return;
     }

@@ -129,3 +129,25 @@ def test_paged_full_size(kvd):
         s0 = int(sl[q])
         assert np.array_equal(_bits(ko[s0:s0 + n]), rk), f"gather seq {q}"
         assert np.array_equal(_bits(vo[s0:s0 + n]), rv), f"gather seq {q}"
+
+
+@pytest.mark.parametrize("name", ["gqa", "long"])
+def test_full_size_attention_finishes_far_below_the_wait_limit(kvd, name):
+    """A full-size launch takes well under a millisecond of HBM time; one that
+    takes anywhere near the kernels' one-second wait limit means some CTA sat
+    in a bounded wait (a pipeline bug even if the result is right)."""
+    import time
+    lay = getattr(W, name)(device="cuda", layers=1).layers[0]
+    status = kvd.status_tensor()
+    out = torch.empty_like(lay.q)
+    kvd.attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale, out=out,
+                      dev_status=status)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(3):
+        kvd.attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale, out=out,
+                          dev_status=status)
+    torch.cuda.synchronize()
+    per_call = (time.perf_counter() - t0) / 3
+    assert int(status.item()) == 0
+    assert per_call < 0.05, f"{name}: {per_call * 1e3:.1f} ms per attention call"
