@@ -1,0 +1,95 @@
+// attend_noalloc.cu -- kvd_attend_masked_noalloc: masked decode attention for
+// callers that cannot allocate device memory.
+//
+// kvd_attend_masked needs a caller workspace for its per-split partial rows
+// once the sequence axis is split across CTAs.  Some callers have no way to
+// provide one: a host runtime whose allocator already owns all device memory
+// and hands a plug-in only its inputs and outputs, an enqueue step that is
+// forbidden to allocate, or a latency-critical loop that cannot afford
+// cudaMalloc's implicit device synchronisation.  This entry point runs the
+// very same split kernel and combine kernel with a workspace that lives in a
+// fixed-size array compiled into the library (kNoAllocScratchBytes per
+// device, held by every GPU that loads the library until the process exits).
+//
+// The array is shared by every call on a device and keeps whatever the last
+// call left in it.  Nothing in it has to start at zero: each call writes the
+// log-sum-exp of every split it later reads and only reads the partial row of
+// a split whose log-sum-exp is finite, which that same call wrote.  Calls
+// that may run at the same time on the GPU (different streams, or different
+// host threads without ordering) race on the array and must be serialised by
+// the caller.
+#include <cstdio>
+#include <mutex>
+
+#include "kvd_device.cuh"
+#include "kvd_internal.h"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = KVD_NOALLOC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+// The workspace.  In host code this name is only a stand-in for the symbol,
+// never a device address: the address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char kvd_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current) and cached.
+cudaError_t scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, kvd_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvd_status kvd_attend_masked_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                     const uint8_t* mask, void* out, float* lse_out, int B,
+                                     int Hq, int Hkv, int C, int D, float scale, kvd_dtype dtype,
+                                     int num_splits, int32_t* dev_status, kvd_stream_t stream) {
+    if (B < 1 || C < 1) {
+        // Same argument rules as kvd_attend_masked (an empty batch is a no-op).
+        return kvd_attend_masked(q, k_cache, v_cache, mask, out, lse_out, B, Hq, Hkv, C, D, scale,
+                                 dtype, num_splits, nullptr, 0, dev_status, stream);
+    }
+    const size_t need =
+        kvd_attend_masked_workspace_bytes(B, Hq, Hkv, C, D, dtype, num_splits);
+    if (need > kNoAllocScratchBytes) {
+        char msg[256];
+        snprintf(msg, sizeof msg,
+                 "kvd_attend_masked_noalloc: these sizes need %zu bytes of split scratch, the "
+                 "built-in scratch holds %zu; use kvd_attend_masked with a workspace or fewer "
+                 "splits",
+                 need, kNoAllocScratchBytes);
+        kvd::set_last_error(msg);
+        return KVD_ERR_WORKSPACE;
+    }
+    void* scratch = nullptr;
+    const cudaError_t e = scratch_address(&scratch);
+    if (e != cudaSuccess) {
+        char msg[256];
+        snprintf(msg, sizeof msg, "kvd_attend_masked_noalloc: cudaGetSymbolAddress failed: %s",
+                 cudaGetErrorString(e));
+        kvd::set_last_error(msg);
+        return KVD_ERR_CUDA;
+    }
+    return kvd_attend_masked(q, k_cache, v_cache, mask, out, lse_out, B, Hq, Hkv, C, D, scale,
+                             dtype, num_splits, scratch, kNoAllocScratchBytes, dev_status, stream);
+}
+
+}  // extern "C"

@@ -188,6 +188,14 @@ kvd_status check_attention_shape(int Hq, int Hkv, int D, kvd_dtype dt) {
 
 }  // namespace
 
+namespace kvd {
+// Lets the other translation units of the library report a host-side error
+// through kvd_last_error().
+void set_last_error(const char* msg) {
+    snprintf(g_last_error, sizeof g_last_error, "%s", msg);
+}
+}  // namespace kvd
+
 // ===================================================================== C ABI
 extern "C" {
 

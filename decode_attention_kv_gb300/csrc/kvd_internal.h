@@ -29,6 +29,9 @@ cudaError_t launch_attend_split(kvd_dtype dt, int D, int G, bool paged, const At
                                 const CUtensorMap* kmap, const CUtensorMap* vmap, dim3 grid,
                                 cudaStream_t stream);
 
+// Sets the message kvd_last_error() returns on this thread.
+void set_last_error(const char* msg);
+
 cudaError_t launch_combine(const float* part_o, const float* part_lse, void* out,
                            float* lse_out, int R, int S, int D, kvd_dtype out_dt,
                            cudaStream_t stream);

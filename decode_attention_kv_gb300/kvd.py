@@ -34,6 +34,8 @@ SIGNATURES = {
     "kvd_attend_masked_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
     "kvd_attend_masked": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz,
                            _vp, _vp], _i),
+    "kvd_attend_masked_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i,
+                                   _vp, _vp], _i),
     "kvd_attend_paged_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i, _i], _sz),
     "kvd_attend_paged": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
                           _i, _i, _vp, _sz, _vp, _vp], _i),
@@ -176,6 +178,32 @@ def attend_masked(q, k_cache, v_cache, mask, scale=None, out=None, lse=None, num
                              _ptr(lse), B, Hq, Hkv, C, D, float(scale), dt, num_splits, _ptr(ws),
                              wsb, _ptr(dev_status), _stream(q.device))
     _check("kvd_attend_masked", st)
+    return out
+
+
+def attend_masked_noalloc(q, k_cache, v_cache, mask, scale=None, out=None, lse=None,
+                          num_splits=0, dev_status=None):
+    """kvd_attend_masked_noalloc: attend_masked for callers that cannot
+    allocate -- the split scratch is the library's built-in array (see
+    include/kvd.h for its size limit and sharing rules); ``out`` is the only
+    tensor this wrapper creates, and only when none is passed."""
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("mask", mask)):
+        _cuda_contig(n, t)
+    B, Hq, D = q.shape
+    Bk, Hkv, C, Dk = k_cache.shape
+    if Bk != B or Dk != D or v_cache.shape != k_cache.shape or mask.shape != (B, C):
+        raise ValueError("attend_masked_noalloc: shape mismatch")
+    if mask.dtype != torch.uint8 or not (q.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("attend_masked_noalloc: uint8 mask and one dtype for q and caches")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    st = load().kvd_attend_masked_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(mask),
+                                          _ptr(out), _ptr(lse), B, Hq, Hkv, C, D, float(scale),
+                                          _dtype_code(q), num_splits, _ptr(dev_status),
+                                          _stream(q.device))
+    _check("kvd_attend_masked_noalloc", st)
     return out
 
 

@@ -140,6 +140,37 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
  * Supported: D in {64, 128}; bf16 or f32; BS*Hkv*D*elem addressable by a
  * TMA tensor map (NB*BS < 2^31).
  */
+/*
+ * kvd_attend_masked_noalloc -- the pages have no counterpart to this call; it
+ * exists for callers that cannot allocate device memory.  Some host runtimes
+ * own all device memory through their own allocator and hand a kernel library
+ * only its input and output buffers; some enqueue paths may not allocate at
+ * all; some latency-critical loops cannot afford cudaMalloc's implicit device
+ * synchronisation.  Such callers cannot supply the workspace that
+ * kvd_attend_masked needs once it splits the sequence axis.
+ *
+ * Same arguments, same result and the same kernels as kvd_attend_masked,
+ * minus the workspace: the split scratch lives in an array of
+ * KVD_NOALLOC_SCRATCH_BYTES built into the library, which every GPU that
+ * loads the library holds until the process exits.  Nothing is allocated.
+ *  - Sizes whose split scratch (kvd_attend_masked_workspace_bytes with the
+ *    same arguments) exceeds KVD_NOALLOC_SCRATCH_BYTES are rejected with
+ *    KVD_ERR_WORKSPACE and a message in kvd_last_error(); pass fewer splits
+ *    (num_splits) or use kvd_attend_masked.
+ *  - The first call on a device looks up the array's device address on the
+ *    current device (cudaGetSymbolAddress) and caches it; make that first
+ *    call before any stream capture on that device.
+ *  - All calls on a device share the one array, which keeps the last call's
+ *    contents (nothing in it needs to start at zero).  Calls that may overlap
+ *    on the GPU (other streams, unordered host threads) race on it: the
+ *    caller must order them.
+ */
+#define KVD_NOALLOC_SCRATCH_BYTES (8u << 20)
+kvd_status kvd_attend_masked_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                     const uint8_t* mask, void* out, float* lse_out, int B,
+                                     int Hq, int Hkv, int C, int D, float scale, kvd_dtype dtype,
+                                     int num_splits, int32_t* dev_status, kvd_stream_t stream);
+
 size_t kvd_attend_paged_workspace_bytes(int Q, int Hq, int Hkv, int BS, int cols, int D,
                                         kvd_dtype dtype, int num_splits);
 kvd_status kvd_attend_paged(const void* q_in, const void* key_cache, const void* value_cache,
