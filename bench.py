@@ -170,17 +170,18 @@ class MaskedBench:
     each step (1024, 1025, ... 1151, then the response part is cleared and the
     cycle restarts); the other workloads re-append at the last valid slot."""
 
-    def __init__(self, name, torch, kvd, dev):
+    def __init__(self, name, torch, kvd, dev, layers=None):
         import workloads
         self.torch, self.kvd, self.dev, self.name = torch, kvd, dev, name
+        kw = {} if layers is None else {"layers": layers}
         if name == "npuw":
-            w = workloads.npuw(device=dev)
+            w = workloads.npuw(device=dev, **kw)
             self.cycle, self.prompt = 128, 1024
         elif name == "gqa":
-            w = workloads.gqa(device=dev)
+            w = workloads.gqa(device=dev, **kw)
             self.cycle, self.prompt = 1, None
         elif name == "long":
-            w = workloads.long(device=dev)
+            w = workloads.long(device=dev, **kw)
             self.cycle, self.prompt = 1, None
         else:
             raise ValueError(name)
@@ -409,10 +410,10 @@ class PagedBench:
                       f"{L2_BYTES // 2**20} MiB L2"}
 
 
-def make_bench(name, torch, kvd, dev):
+def make_bench(name, torch, kvd, dev, layers=None):
     if name == "paged":
         return PagedBench(torch, kvd, dev)
-    return MaskedBench(name, torch, kvd, dev)
+    return MaskedBench(name, torch, kvd, dev, layers)
 
 
 # ------------------------------------------------------------------- timing
@@ -639,6 +640,10 @@ def main():
     ap.add_argument("--workload", default="npuw", choices=["npuw", "gqa", "long", "paged"])
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile", action="store_true",
+                    help="no timing: run --warmup + --steps eager steps of --workload (for ncu)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layer caches of the static-buffer workloads (default: the workload's)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -667,8 +672,17 @@ def main():
     kvd.load()
     peak, peak_src = measured_peak()
 
+    if args.profile:
+        b = make_bench(args.workload, torch, kvd, dev, args.layers)
+        for j in range(args.warmup + args.steps):
+            b.eager_run(j)
+        torch.cuda.synchronize()
+        st = int(b.status.item())
+        log(f"profile run of {args.workload}: {args.warmup + args.steps} steps, status {st}")
+        return 0 if st == 0 else 1
+
     log(f"workload {args.workload}: building inputs")
-    b = make_bench(args.workload, torch, kvd, dev)
+    b = make_bench(args.workload, torch, kvd, dev, args.layers)
     clocks = ClockSampler(bus_id_of(torch, dev))
     log("timed steps")
     res = measure_workload(b, torch, dist, args.steps, args.warmup, peak, clocks=clocks)

@@ -9,7 +9,7 @@ cudaError_t launch_attend_f32(int D, int G, bool paged, const AttendParams& p,
     return launch_elem<float>(D, G, paged, p, kmap, vmap, grid, stream);
 }
 
-AttendGeom attend_geom_f32(int D) {
+AttendGeom attend_geom_f32(int D, int /*G*/) {
     return D == 64 ? geom_of<float, 64>() : geom_of<float, 128>();
 }
 

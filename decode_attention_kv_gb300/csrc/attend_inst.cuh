@@ -3,6 +3,7 @@
 // instantiations compile in parallel.
 #pragma once
 
+#include "attend_mma.cuh"
 #include "attend_split.cuh"
 #include "kvd_internal.h"
 
@@ -33,8 +34,8 @@ cudaError_t launch_one(const AttendParams& p, const CUtensorMap* kmap, const CUt
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    kern<<<grid, (Gm::NCW + 1) * 32, Sh::kSmemAlloc, stream>>>(p, *kmap, *vmap);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3((Gm::NCW + 1) * 32), Sh::kSmemAlloc, stream, p, *kmap,
+                      *vmap);
 }
 
 template <typename Elem, int D, bool PAGED>
@@ -65,7 +66,49 @@ template <typename Elem, int D>
 AttendGeom geom_of() {
     using Gm = Geom<Elem, D>;
     using Sh = AttendShape<Elem, D, 8, Gm::T, Gm::STAGES, Gm::NCW>;
-    return AttendGeom{Gm::T, Gm::STAGES, Gm::NCW, Sh::kSmemAlloc};
+    return AttendGeom{Gm::T, Gm::STAGES, Gm::NCW, Sh::kSmemAlloc, false};
+}
+
+// Tensor-core kernel geometry: 64-token stages (one 16-token slab per
+// consumer warp), three stages, two CTAs per SM.
+struct MmaGeom {
+    static constexpr int T = 64;
+    static constexpr int NCW = 4;
+    static constexpr int STAGES = 3;
+};
+
+template <int D, int G, bool PAGED>
+cudaError_t launch_mma_one(const AttendParams& p, const CUtensorMap* kmap,
+                           const CUtensorMap* vmap, dim3 grid, cudaStream_t stream) {
+    using Sh = MmaShape<D, G, MmaGeom::T, MmaGeom::STAGES, MmaGeom::NCW>;
+    auto kern = attend_mma_kernel<D, G, MmaGeom::T, MmaGeom::STAGES, MmaGeom::NCW, PAGED>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    return launch_pdl(kern, grid, dim3((MmaGeom::NCW + 1) * 32), Sh::kSmemAlloc, stream, p, *kmap,
+                      *vmap);
+}
+
+template <int D, bool PAGED>
+cudaError_t launch_mma_g(int G, const AttendParams& p, const CUtensorMap* kmap,
+                         const CUtensorMap* vmap, dim3 grid, cudaStream_t stream) {
+    switch (G) {
+        case 4: return launch_mma_one<D, 4, PAGED>(p, kmap, vmap, grid, stream);
+        case 8: return launch_mma_one<D, 8, PAGED>(p, kmap, vmap, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int D>
+AttendGeom mma_geom_of() {
+    using Sh = MmaShape<D, 8, MmaGeom::T, MmaGeom::STAGES, MmaGeom::NCW>;
+    return AttendGeom{MmaGeom::T, MmaGeom::STAGES, MmaGeom::NCW, Sh::kSmemAlloc, true};
 }
 
 }  // namespace kvd

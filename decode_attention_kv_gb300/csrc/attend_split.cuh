@@ -32,37 +32,9 @@
 // plus its log-sum-exp for the combine kernel.
 #pragma once
 
-#include "kvd_device.cuh"
+#include "attend_common.cuh"
 
 namespace kvd {
-
-constexpr int kMaxChunk = 4096;              // tokens per split, upper bound
-constexpr int kMaxWords = kMaxChunk / 32;    // validity words per split
-constexpr int kMaxBlocks = 128;              // block-table entries per split
-
-struct AttendParams {
-    const void* q;               // [rows, Hq, D]
-    const void* k;               // static buffer [B, Hkv, C, D]
-    const void* v;
-    const uint8_t* mask;         // static buffer [B, C]
-    const int32_t* block_tables; // paged [Q, cols]
-    const int32_t* seq_lens;     // paged [Q + 1]
-    const int32_t* seq_offset;   // paged [Q] or null
-    void* out;                   // [rows, Hq, D] (single split)
-    float* lse_out;              // [rows, Hq] or null (single split)
-    float* part_o;               // [rows * Hq, S, D]
-    float* part_lse;             // [rows * Hq, S]
-    int32_t* dev_status;
-    int Hq, Hkv, g, HG;          // g = Hq / Hkv, HG = head groups per kv head
-    int C;                       // static buffer capacity
-    int BS, cols, NB;            // paged geometry
-    int tile;                    // tokens per ring stage (paged: divides BS)
-    int chunk;                   // tokens per split (multiple of tile and of 32)
-    int S;                       // splits
-    int mask_vec;                // mask rows 16-byte aligned (C % 16 == 0)
-    float qscale;                // scale * log2(e)
-    int direct;                  // S == 1: write out / lse_out directly
-};
 
 template <typename Elem, int D, int G, int T, int STAGES, int NCW>
 struct AttendShape {
@@ -78,14 +50,7 @@ struct AttendShape {
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kRingBytes = STAGES * kStageBytes;
     static constexpr int kMergeBytes = NCW * G * (D + 2) * 4;
-    // ring | full[STAGES] | empty[STAGES] | meta[STAGES] | abort | words | blocks
-    static constexpr int kBarOff = kRingBytes;
-    static constexpr int kMetaOff = kBarOff + 2 * STAGES * 8;
-    static constexpr int kAbortOff = kMetaOff + STAGES * 4;
-    static constexpr int kWordsOff = (kAbortOff + 4 + 15) / 16 * 16;
-    static constexpr int kBlocksOff = kWordsOff + kMaxWords * 4;
-    static constexpr int kSmemBytes = kBlocksOff + kMaxBlocks * 4;
-    static constexpr int kSmemAlloc = kSmemBytes + 1024;  // base aligned up to 1 KiB
+    static constexpr int kSmemAlloc = kRingBytes + CtlLayout<STAGES>::kBytes + 1024;
 
     static_assert(D % kVec == 0 && kLPT <= 32 && 32 % kLPT == 0, "head_dim layout");
     static_assert(T % NCW == 0 && kTW % kTPW == 0, "tile layout");
@@ -93,28 +58,6 @@ struct AttendShape {
     static_assert(kMergeBytes <= kRingBytes, "merge area aliases the ring");
     static_assert(kTileBytes % 16 == 0, "bulk copies move 16-byte multiples");
 };
-
-// Any valid token among relative tokens [r0, r0 + n) of the split.
-__device__ __forceinline__ bool any_valid(const uint32_t* words, int r0, int n) {
-    int r = r0;
-    const int end = r0 + n;
-    while (r < end) {
-        const int w = r >> 5, b = r & 31;
-        const int take = min(32 - b, end - r);
-        const uint32_t m = (take == 32) ? 0xffffffffu : (((1u << take) - 1u) << b);
-        if (words[w] & m) return true;
-        r += take;
-    }
-    return false;
-}
-
-// Four bytes -> four bits (bit i set when byte i is nonzero).
-__device__ __forceinline__ uint32_t nonzero_bytes(uint32_t x) {
-    uint32_t t = x | (x >> 4);
-    t |= t >> 2;
-    t |= t >> 1;
-    return (t & 1u) | ((t >> 7) & 2u) | ((t >> 14) & 4u) | ((t >> 21) & 8u);
-}
 
 template <typename Elem, int D, int G, int T, int STAGES, int NCW, bool PAGED>
 __global__ void __launch_bounds__((NCW + 1) * 32)
@@ -125,188 +68,45 @@ attend_split_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sh::kBarOff);
-    uint64_t* empty = full + STAGES;
-    int* meta = reinterpret_cast<int*>(smem + Sh::kMetaOff);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Sh::kAbortOff);
-    uint32_t* words = reinterpret_cast<uint32_t*>(smem + Sh::kWordsOff);
-    int* blocks = reinterpret_cast<int*>(smem + Sh::kBlocksOff);
+    Ctl<STAGES> ctl(smem + Sh::kRingBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x;
     const int kvh = blockIdx.y / p.HG, hg = blockIdx.y % p.HG;
     const int bz = blockIdx.z;  // batch entry (static buffer) or sequence (paged)
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], NCW);
-        }
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
+    if (threadIdx.x == 0) ctl.init(NCW);
     if (PAGED && threadIdx.x == 32 * NCW) {
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
     }
-
-    // ---------------------------------------------------------- token range
-    // Both roles derive the split's token range [t_begin, t_end) themselves.
-    const int t_begin = split * p.chunk;
-    int t_end, first_col = 0;
-    if constexpr (PAGED) {
-        const int s0 = p.seq_lens[bz], s1 = p.seq_lens[bz + 1];
-        const int off = p.seq_offset ? p.seq_offset[bz] : 0;
-        int len = s1 - s0;
-        // A cumsum that does not start at 0 is reported; the differences are
-        // still well defined and used.  Other violations empty the sequence.
-        uint32_t bad = (bz == 0 && s0 != 0) ? KVD_DEV_SEQLENS : 0u;
-        if (len < 0) {
-            bad |= KVD_DEV_SEQLENS;
-            len = 0;
-        } else if (off < 0 || off % p.BS != 0) {
-            bad |= KVD_DEV_SEQ_OFFSET;
-            len = 0;
-        } else {
-            first_col = off / p.BS;
-            if (first_col + (len + p.BS - 1) / p.BS > p.cols) {
-                bad |= KVD_DEV_TABLE_COLS;
-                len = 0;
-            }
-        }
-        if (bad && threadIdx.x == 0 && split == 0 && blockIdx.y == 0) report(p.dev_status, bad);
-        t_end = min(len, t_begin + p.chunk);
-    } else {
-        t_end = min(p.C, t_begin + p.chunk);
-    }
-    const int ntok = max(0, t_end - t_begin);
-    const int ntiles = (ntok + p.tile - 1) / p.tile;
+    pdl_launch_dependents();
+    pdl_wait();
+    const SplitRange r = split_range<PAGED>(p, bz, split);
     __syncthreads();
 
     if (warp == NCW) {
         // ============================================================ producer
-        const int nwords = (ntiles * p.tile + 31) / 32;
-        int lb0 = 0;
-        if constexpr (PAGED) {
-            if (ntok > 0) {
-                lb0 = t_begin / p.BS;
-                const int nblk = (t_end - 1) / p.BS - lb0 + 1;
-                const int32_t* row = p.block_tables + (size_t)bz * p.cols + first_col + lb0;
-                for (int j = lane; j < nblk; j += 32) {
-                    int ph = row[j];
-                    if (ph < 0 || ph >= p.NB) {
-                        report(p.dev_status, KVD_DEV_BLOCK_RANGE);
-                        ph = -1;
-                    }
-                    blocks[j] = ph;
-                }
-                __syncwarp();
-            }
-            for (int j = 0; j < nwords; ++j) {
-                const int tok = t_begin + 32 * j + lane;
-                const bool ok = tok < t_end && blocks[tok / p.BS - lb0] >= 0;
-                const uint32_t w = __ballot_sync(0xffffffffu, ok);
-                if (lane == 0) words[j] = w;
-            }
-        } else {
-            const uint8_t* mrow = p.mask + (size_t)bz * p.C;
-            if (p.mask_vec) {
-                // 16 slots per lane per vector, 512 slots per warp round; the
-                // whole split's mask is requested before any bit is used.
-                constexpr int R = kMaxChunk / 512;
-                const int nvec = (ntok + 15) / 16;
-                const uint4* src = reinterpret_cast<const uint4*>(mrow + t_begin);
-                uint4 mv[R];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int vi = r * 32 + lane;
-                    mv[r] = vi < nvec ? __ldg(src + vi) : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int vi = r * 32 + lane;
-                    uint32_t bits = nonzero_bytes(mv[r].x) | (nonzero_bytes(mv[r].y) << 4) |
-                                    (nonzero_bytes(mv[r].z) << 8) | (nonzero_bytes(mv[r].w) << 12);
-                    const int nv = min(max(ntok - vi * 16, 0), 16);
-                    bits &= (nv >= 16) ? 0xffffu : ((1u << nv) - 1u);
-                    const uint32_t hi = __shfl_down_sync(0xffffffffu, bits, 1);
-                    const int j = vi >> 1;
-                    if ((lane & 1) == 0 && j < nwords) words[j] = bits | (hi << 16);
-                }
-            } else {
-                for (int j0 = 0; j0 < nwords; j0 += 8) {
-                    uint8_t mb[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int tok = t_begin + 32 * (j0 + u) + lane;
-                        mb[u] = (j0 + u < nwords && tok < t_end) ? __ldg(mrow + tok) : 0;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const uint32_t w = __ballot_sync(0xffffffffu, mb[u] != 0);
-                        if (lane == 0 && j0 + u < nwords) words[j0 + u] = w;
-                    }
-                }
-            }
-        }
-        __syncwarp();
+        const int lb0 = producer_scan<PAGED>(p, r, bz, lane, ctl.words, ctl.blocks);
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued_mask = 0, last_parity = 0;  // per stage: issued? parity of last issue
-            bool failed = false;
-            for (int i = 0; i < ntiles && !failed; ++i) {
-                const int r0 = i * p.tile;
-                const int n = min(p.tile, ntok - r0);
-                if (!any_valid(words, r0, n)) continue;  // all-zero tile: never read
-                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
-                    failed = true;
-                    break;
-                }
-                meta[stage] = i;
+            producer_issue<STAGES>(p, r, ctl, [&](int stage, int r0, int n, uint64_t* bar) {
                 unsigned char* sk = smem + stage * Sh::kStageBytes;
                 unsigned char* sv = sk + Sh::kTileBytes;
                 if constexpr (PAGED) {
-                    const int t0 = t_begin + r0;
-                    const int row = blocks[t0 / p.BS - lb0] * p.BS + t0 % p.BS;
-                    mbar_arrive_expect_tx(&full[stage], 2u * p.tile * D * sizeof(Elem));
-                    tma_g2s_3d(sk, &kmap, 0, kvh, row, &full[stage], pol);
-                    tma_g2s_3d(sv, &vmap, 0, kvh, row, &full[stage], pol);
+                    const int t0 = r.t_begin + r0;
+                    const int row = ctl.blocks[t0 / p.BS - lb0] * p.BS + t0 % p.BS;
+                    mbar_arrive_expect_tx(bar, 2u * p.tile * D * sizeof(Elem));
+                    tma_g2s_3d(sk, &kmap, 0, kvh, row, bar, pol);
+                    tma_g2s_3d(sv, &vmap, 0, kvh, row, bar, pol);
                 } else {
-                    const size_t base = (((size_t)bz * p.Hkv + kvh) * p.C + t_begin + r0) * D;
+                    const size_t base = (((size_t)bz * p.Hkv + kvh) * p.C + r.t_begin + r0) * D;
                     const uint32_t bytes = (uint32_t)n * D * sizeof(Elem);
-                    mbar_arrive_expect_tx(&full[stage], 2u * bytes);
-                    bulk_g2s(sk, static_cast<const Elem*>(p.k) + base, bytes, &full[stage], pol);
-                    bulk_g2s(sv, static_cast<const Elem*>(p.v) + base, bytes, &full[stage], pol);
+                    mbar_arrive_expect_tx(bar, 2u * bytes);
+                    bulk_g2s(sk, static_cast<const Elem*>(p.k) + base, bytes, bar, pol);
+                    bulk_g2s(sv, static_cast<const Elem*>(p.v) + base, bytes, bar, pol);
                 }
-                issued_mask |= 1u << stage;
-                last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-            if (!failed && mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
-                meta[stage] = -1;  // end of the split
-                mbar_arrive(&full[stage]);
-            } else {
-                failed = true;
-            }
-            if (failed) {
-                *abort_flag = 1;
-                report(p.dev_status, KVD_DEV_TIMEOUT);
-                // The consumers may leave early now: never let the CTA exit
-                // while a copy issued here may still be writing the ring.
-                // (On the normal path the consumers have waited for every
-                // issued tile before they see the end marker, and the end
-                // marker itself completes a phase, so no drain is needed.)
-                for (int s = 0; s < STAGES; ++s)
-                    if (issued_mask & (1u << s)) {
-                        const volatile int never = 0;
-                        mbar_wait(&full[s], (last_parity >> s) & 1u, &never);
-                    }
-            }
+            });
         }
         return;
     }
@@ -345,14 +145,7 @@ attend_split_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
     int stage = 0;
     uint32_t phase = 0;
     while (true) {
-        if (!mbar_wait(&full[stage], phase, abort_flag)) {
-            if (!*abort_flag) {
-                *abort_flag = 1;
-                report(p.dev_status, KVD_DEV_TIMEOUT);
-            }
-            break;
-        }
-        const int tile_i = meta[stage];
+        const int tile_i = consumer_next<STAGES>(ctl, stage, phase, p.dev_status);
         if (tile_i < 0) break;
         const Elem* Ks = reinterpret_cast<const Elem*>(smem + stage * Sh::kStageBytes);
         const Elem* Vs = Ks + T * D;
@@ -376,7 +169,7 @@ attend_split_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
                     s[i][hh] = a.x + a.y;
                 }
                 const int rel = r0 + tt;
-                val[i] = tt < p.tile && ((words[rel >> 5] >> (rel & 31)) & 1u);
+                val[i] = tt < p.tile && ((ctl.words[rel >> 5] >> (rel & 31)) & 1u);
             }
 #pragma unroll
             for (int off = Sh::kLPT / 2; off > 0; off >>= 1)
@@ -426,7 +219,7 @@ attend_split_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
+        if (lane == 0) mbar_arrive(&ctl.empty[stage]);
         if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -477,29 +270,7 @@ attend_split_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
     }
     asm volatile("bar.sync 1, %0;" ::"r"(NCW * 32) : "memory");
 
-    for (int idx = threadIdx.x; idx < g_here * D; idx += NCW * 32) {
-        const int hh = idx / D, d = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) M = fmaxf(M, ml_area[(w * G + hh) * 2]);
-        const float base = (M == -INFINITY) ? 0.f : M;
-        float L = 0.f, O = 0.f;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) {
-            const float sc = fast_exp2(ml_area[(w * G + hh) * 2] - base);
-            L = fmaf(ml_area[(w * G + hh) * 2 + 1], sc, L);
-            O = fmaf(mo_area[(w * G + hh) * D + d], sc, O);
-        }
-        const size_t row = qrow0 + hh;
-        const float lse = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-        if (p.direct) {
-            Tr::store(p.out, row * D + d, L > 0.f ? O / L : 0.f);
-            if (d == 0 && p.lse_out) p.lse_out[row] = lse;
-        } else {
-            if (L > 0.f) p.part_o[(row * p.S + split) * D + d] = O / L;
-            if (d == 0) p.part_lse[row * p.S + split] = lse;
-        }
-    }
+    write_rows<Elem, D, G, NCW>(p, mo_area, ml_area, qrow0, g_here, split);
 }
 
 }  // namespace kvd

@@ -6,79 +6,120 @@
 namespace kvd {
 
 // ------------------------------------------------------------------ combine
-// One warp per output row.  Merges S partial rows, each normalised over its
-// own key range, by their log-sum-exp ("Intel NPU running LLMs", Part 3,
-// Flash SDPA path: tiles merged exactly through running max and sum).
-constexpr int kCombineWarps = 4;
-constexpr int kCombineMaxVec = 8;  // float4 per lane: D <= 1024
+// One CTA per output row.  Merges S partial rows, each normalised over its own
+// key range, by their log-sum-exp ("Intel NPU running LLMs", Part 3, Flash
+// SDPA path: tiles merged exactly through running max and sum).  The row's
+// log-sum-exps are reduced first; then groups of threads split the S partial
+// rows between them (a thread owns one float4 of the row) so that the loads
+// of many partial rows are in flight at once; shared memory sums the groups.
+constexpr int kCombineThreads = 128;
+
+__device__ __forceinline__ float block_reduce(float x, bool is_max, float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, x, off);
+        x = is_max ? fmaxf(x, o) : x + o;
+    }
+    __syncthreads();  // red[] may still be read from a previous reduction
+    if (lane == 0) red[warp] = x;
+    __syncthreads();
+    x = red[0];
+#pragma unroll
+    for (int w = 1; w < kCombineThreads / 32; ++w) x = is_max ? fmaxf(x, red[w]) : x + red[w];
+    return x;
+}
 
 template <typename Out>
-__global__ void __launch_bounds__(kCombineWarps * 32)
+__global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                Out* __restrict__ out, float* __restrict__ lse_out, int R, int S, int D) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * kCombineWarps + warp;
-    if (row >= R) return;
+    __shared__ float red[kCombineThreads / 32];
+    __shared__ float4 acc_sm[kCombineThreads];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int row = blockIdx.x, tid = threadIdx.x;
     const float* ls = part_lse + (size_t)row * S;
     float M = -INFINITY;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, ls[s]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    const int nv = D / 4;
-    float4 acc[kCombineMaxVec];
-#pragma unroll
-    for (int k = 0; k < kCombineMaxVec; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float lse = -INFINITY;
-    if (M != -INFINITY) {
-        float sum = 0.f;
-        for (int s = lane; s < S; s += 32) sum += fast_exp2((ls[s] - M) * kLog2e);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    for (int s = tid; s < S; s += kCombineThreads) M = fmaxf(M, ls[s]);
+    M = block_reduce(M, true, red);
+    float sum = 0.f;
+    if (M != -INFINITY)
+        for (int s = tid; s < S; s += kCombineThreads) sum += fast_exp2((ls[s] - M) * kLog2e);
+    sum = block_reduce(sum, false, red);
+
+    const int nv = D / 4;                                    // float4 per row
+    const int groups = nv >= kCombineThreads ? 1 : kCombineThreads / nv;
+    const int g = tid / nv, v = tid % nv;                    // (g only meaningful if groups > 1)
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;    // D <= 1024: two float4 at most
+    const bool active = groups > 1 ? g < groups : true;
+    const int gg = groups > 1 ? g : 0;
+    const int v0 = groups > 1 ? v : tid;
+    if (M != -INFINITY && active) {
         const float inv = 1.f / sum;
-        lse = M + logf(sum);
-        const float4* po = reinterpret_cast<const float4*>(part_o + (size_t)row * S * D);
-        for (int s = 0; s < S; ++s) {
+        const float4* po = reinterpret_cast<const float4*>(part_o) + (size_t)row * S * nv;
+#pragma unroll 8
+        for (int s = gg; s < S; s += groups) {
             const float lsv = ls[s];
             if (lsv == -INFINITY) continue;  // empty range: its row is not read
             const float w = fast_exp2((lsv - M) * kLog2e) * inv;
-#pragma unroll
-            for (int k = 0; k < kCombineMaxVec; ++k) {
-                const int vi = lane + 32 * k;
-                if (vi < nv) {
-                    const float4 x = po[(size_t)s * nv + vi];
-                    acc[k].x = fmaf(w, x.x, acc[k].x);
-                    acc[k].y = fmaf(w, x.y, acc[k].y);
-                    acc[k].z = fmaf(w, x.z, acc[k].z);
-                    acc[k].w = fmaf(w, x.w, acc[k].w);
-                }
+            const float4* src = po + (size_t)s * nv;
+            if (v0 < nv) {
+                const float4 x = src[v0];
+                a0.x = fmaf(w, x.x, a0.x);
+                a0.y = fmaf(w, x.y, a0.y);
+                a0.z = fmaf(w, x.z, a0.z);
+                a0.w = fmaf(w, x.w, a0.w);
+            }
+            if (v0 + kCombineThreads < nv) {
+                const float4 x = src[v0 + kCombineThreads];
+                a1.x = fmaf(w, x.x, a1.x);
+                a1.y = fmaf(w, x.y, a1.y);
+                a1.z = fmaf(w, x.z, a1.z);
+                a1.w = fmaf(w, x.w, a1.w);
             }
         }
     }
-#pragma unroll
-    for (int k = 0; k < kCombineMaxVec; ++k) {
-        const int vi = lane + 32 * k;
-        if (vi < nv) {
-            const size_t o = (size_t)row * D + 4 * vi;
-            ElemTraits<Out>::store(out, o, acc[k].x);
-            ElemTraits<Out>::store(out, o + 1, acc[k].y);
-            ElemTraits<Out>::store(out, o + 2, acc[k].z);
-            ElemTraits<Out>::store(out, o + 3, acc[k].w);
+    if (groups > 1) {
+        acc_sm[tid] = a0;
+        __syncthreads();
+        if (g == 0) {
+            for (int k = 1; k < groups; ++k) {
+                const float4 x = acc_sm[k * nv + v];
+                a0.x += x.x;
+                a0.y += x.y;
+                a0.z += x.z;
+                a0.w += x.w;
+            }
         }
     }
-    if (lane == 0 && lse_out) lse_out[row] = lse;
+    if (groups == 1 || g == 0) {
+        const size_t o = (size_t)row * D;
+        if (v0 < nv) {
+            ElemTraits<Out>::store(out, o + 4 * v0, a0.x);
+            ElemTraits<Out>::store(out, o + 4 * v0 + 1, a0.y);
+            ElemTraits<Out>::store(out, o + 4 * v0 + 2, a0.z);
+            ElemTraits<Out>::store(out, o + 4 * v0 + 3, a0.w);
+        }
+        if (v0 + kCombineThreads < nv) {
+            const size_t o1 = o + 4 * (v0 + kCombineThreads);
+            ElemTraits<Out>::store(out, o1, a1.x);
+            ElemTraits<Out>::store(out, o1 + 1, a1.y);
+            ElemTraits<Out>::store(out, o1 + 2, a1.z);
+            ElemTraits<Out>::store(out, o1 + 3, a1.w);
+        }
+    }
+    if (tid == 0 && lse_out) lse_out[row] = M != -INFINITY ? M + logf(sum) : -INFINITY;
 }
 
 cudaError_t launch_combine(const float* part_o, const float* part_lse, void* out,
                            float* lse_out, int R, int S, int D, kvd_dtype out_dt,
                            cudaStream_t stream) {
-    const dim3 grid((R + kCombineWarps - 1) / kCombineWarps);
     if (out_dt == KVD_BF16)
-        combine_kernel<__nv_bfloat16><<<grid, kCombineWarps * 32, 0, stream>>>(
-            part_o, part_lse, static_cast<__nv_bfloat16*>(out), lse_out, R, S, D);
-    else
-        combine_kernel<float><<<grid, kCombineWarps * 32, 0, stream>>>(
-            part_o, part_lse, static_cast<float*>(out), lse_out, R, S, D);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(R), dim3(kCombineThreads), 0, stream,
+                          part_o, part_lse, static_cast<__nv_bfloat16*>(out), lse_out, R, S, D);
+    return launch_pdl(combine_kernel<float>, dim3(R), dim3(kCombineThreads), 0, stream, part_o,
+                      part_lse, static_cast<float*>(out), lse_out, R, S, D);
 }
 
 // ------------------------------------------------------------------- append
@@ -90,6 +131,8 @@ append_kernel(unsigned char* __restrict__ kc, unsigned char* __restrict__ vc,
               const unsigned char* __restrict__ kn, const unsigned char* __restrict__ vn,
               const int32_t* __restrict__ pos, uint8_t* __restrict__ mask, int Hkv, int C,
               int row_bytes, int32_t* dev_status) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int b = blockIdx.y;
     const int p = pos[b];
     if (p < 0 || p >= C) {
@@ -115,11 +158,11 @@ cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const
                           int row_bytes, int32_t* dev_status, cudaStream_t stream) {
     const int nvec = Hkv * (row_bytes / 16);
     const dim3 grid((nvec + 255) / 256, B);
-    append_kernel<<<grid, 256, 0, stream>>>(
-        static_cast<unsigned char*>(k_cache), static_cast<unsigned char*>(v_cache),
-        static_cast<const unsigned char*>(k_new), static_cast<const unsigned char*>(v_new), pos,
-        mask, Hkv, C, row_bytes, dev_status);
-    return cudaGetLastError();
+    return launch_pdl(append_kernel, grid, dim3(256), 0, stream, static_cast<unsigned char*>(k_cache),
+                      static_cast<unsigned char*>(v_cache),
+                      static_cast<const unsigned char*>(k_new),
+                      static_cast<const unsigned char*>(v_new), pos, mask, Hkv, C, row_bytes,
+                      dev_status);
 }
 
 // ------------------------------------------------------------------- gather
@@ -164,6 +207,8 @@ gather_kernel(const unsigned char* __restrict__ kc, const unsigned char* __restr
               const int32_t* __restrict__ seq_offset, unsigned char* __restrict__ ko,
               unsigned char* __restrict__ vo, int NB, int BS, int cols, long long krow,
               long long vrow, int total_tokens, int32_t* dev_status) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int q = blockIdx.x / cols, j = blockIdx.x % cols;
     const int s0 = seq_lens[q], s1 = seq_lens[q + 1];
     const int off = seq_offset ? seq_offset[q] : 0;
@@ -214,19 +259,16 @@ cudaError_t launch_gather(const void* key_cache, const void* value_cache,
     auto ko = static_cast<unsigned char*>(key_out);
     auto vo = static_cast<unsigned char*>(value_out);
     if (krow % 16 == 0 && vrow % 16 == 0)
-        gather_kernel<uint4><<<grid, 256, 0, stream>>>(kc, vc, block_tables, seq_lens, seq_offset,
-                                                       ko, vo, NB, BS, cols, krow, vrow,
-                                                       total_tokens, dev_status);
-    else if (krow % 4 == 0 && vrow % 4 == 0)
-        gather_kernel<unsigned int><<<grid, 256, 0, stream>>>(kc, vc, block_tables, seq_lens,
-                                                              seq_offset, ko, vo, NB, BS, cols,
-                                                              krow, vrow, total_tokens, dev_status);
-    else
-        gather_kernel<unsigned short><<<grid, 256, 0, stream>>>(kc, vc, block_tables, seq_lens,
-                                                                seq_offset, ko, vo, NB, BS, cols,
-                                                                krow, vrow, total_tokens,
-                                                                dev_status);
-    return cudaGetLastError();
+        return launch_pdl(gather_kernel<uint4>, grid, dim3(256), 0, stream, kc, vc, block_tables,
+                          seq_lens, seq_offset, ko, vo, NB, BS, cols, krow, vrow, total_tokens,
+                          dev_status);
+    if (krow % 4 == 0 && vrow % 4 == 0)
+        return launch_pdl(gather_kernel<unsigned int>, grid, dim3(256), 0, stream, kc, vc,
+                          block_tables, seq_lens, seq_offset, ko, vo, NB, BS, cols, krow, vrow,
+                          total_tokens, dev_status);
+    return launch_pdl(gather_kernel<unsigned short>, grid, dim3(256), 0, stream, kc, vc,
+                      block_tables, seq_lens, seq_offset, ko, vo, NB, BS, cols, krow, vrow,
+                      total_tokens, dev_status);
 }
 
 }  // namespace kvd

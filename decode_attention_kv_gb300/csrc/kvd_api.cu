@@ -18,8 +18,8 @@ cudaError_t launch_attend_bf16(int D, int G, bool paged, const AttendParams& p,
 cudaError_t launch_attend_f32(int D, int G, bool paged, const AttendParams& p,
                               const CUtensorMap* kmap, const CUtensorMap* vmap, dim3 grid,
                               cudaStream_t stream);
-AttendGeom attend_geom_bf16(int D);
-AttendGeom attend_geom_f32(int D);
+AttendGeom attend_geom_bf16(int D, int G);
+AttendGeom attend_geom_f32(int D, int G);
 }  // namespace kvd
 
 using namespace kvd;
@@ -83,7 +83,9 @@ long long gcd_ll(long long a, long long b) {
     return a;
 }
 
-AttendGeom geom(kvd_dtype dt, int D) { return dt == KVD_BF16 ? attend_geom_bf16(D) : attend_geom_f32(D); }
+AttendGeom geom(kvd_dtype dt, int D, int G) {
+    return dt == KVD_BF16 ? attend_geom_bf16(D, G) : attend_geom_f32(D, G);
+}
 
 // rows: batch entries (or sequences); cap: most tokens a row can hold;
 // BS > 0 for the paged layout.
@@ -93,7 +95,7 @@ Plan plan_attention(int rows, int Hq, int Hkv, int cap, int D, kvd_dtype dt, int
     const int g = Hq / Hkv;
     pl.G = group_width(g);
     pl.HG = (g + pl.G - 1) / pl.G;
-    const int T = geom(dt, D).tile_max;
+    const int T = geom(dt, D, pl.G).tile_max;
     if (BS > 0) {
         int t = T < BS ? T : BS;
         while (BS % t) --t;  // largest divisor of BS not above T
@@ -149,24 +151,40 @@ cudaError_t get_encoder() {
     return g_encode_err;
 }
 
-// Paged cache [NB, BS, Hkv, D] seen as a 3-D tensor (D, Hkv, NB*BS); one box
-// is one kv head of `tile` consecutive slots.
-kvd_status make_cache_map(CUtensorMap* map, const void* cache, kvd_dtype dt, int NB, int BS,
-                          int Hkv, int D, int tile) {
+// Tensor map over a K or V cache.
+//  paged [NB, BS, Hkv, D] -> 3-D (D, Hkv, NB*BS): a box is one kv head of
+//    `tile` consecutive slots;
+//  static buffer [B, Hkv, C, D] -> 2-D (D, B*Hkv*C): a box is `tile`
+//    consecutive rows of one (b, kv head).
+// With `swizzle` the box is 64 elements wide (128 bytes, the 128-byte swizzle
+// the tensor-core kernel reads with ldmatrix), else the whole head_dim.
+kvd_status make_cache_map(CUtensorMap* map, const void* cache, kvd_dtype dt, bool paged,
+                          long long rows, int Hkv, int D, int tile, bool swizzle) {
     const cudaError_t e = get_encoder();
     if (e != cudaSuccess || !g_encode) return cuda_fail(e, "cuTensorMapEncodeTiled lookup");
     const int es = elem_size(dt);
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)NB * BS};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)Hkv * D * es};
-    const cuuint32_t box[3] = {(cuuint32_t)D, 1u, (cuuint32_t)tile};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    const CUresult r = g_encode(map,
-                                dt == KVD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                                3, const_cast<void*>(cache), dims, strides, box, estr,
-                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const cuuint32_t inner = swizzle ? 64u : (cuuint32_t)D;
+    CUresult r;
+    const CUtensorMapDataType type =
+        dt == KVD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const CUtensorMapSwizzle sw = swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (paged) {
+        const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)rows};
+        const cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)Hkv * D * es};
+        const cuuint32_t box[3] = {inner, 1u, (cuuint32_t)tile};
+        const cuuint32_t estr[3] = {1u, 1u, 1u};
+        r = g_encode(map, type, 3, const_cast<void*>(cache), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)D * es};
+        const cuuint32_t box[2] = {inner, (cuuint32_t)tile};
+        const cuuint32_t estr[2] = {1u, 1u};
+        r = g_encode(map, type, 2, const_cast<void*>(cache), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS) return fail(KVD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return KVD_OK;
 }
@@ -288,10 +306,20 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
     p.mask_vec = (C % 16 == 0) && aligned(mask, 16);
     p.qscale = scale * kLog2e;
     p.direct = pl.S == 1;
-    CUtensorMap dummy;
-    std::memset(&dummy, 0, sizeof dummy);
+    CUtensorMap kmap, vmap;
+    std::memset(&kmap, 0, sizeof kmap);
+    std::memset(&vmap, 0, sizeof vmap);
+    if (attend_uses_mma(dtype, pl.G)) {
+        const long long rows = (long long)B * Hkv * C;
+        if (rows >= (1ll << 31))
+            return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_masked: B*Hkv*C >= 2^31 rows");
+        st = make_cache_map(&kmap, k_cache, dtype, false, rows, Hkv, D, pl.tile, true);
+        if (st != KVD_OK) return st;
+        st = make_cache_map(&vmap, v_cache, dtype, false, rows, Hkv, D, pl.tile, true);
+        if (st != KVD_OK) return st;
+    }
     const dim3 grid(pl.S, Hkv * pl.HG, B);
-    cudaError_t e = launch_attend(dtype, D, pl.G, false, p, &dummy, &dummy, grid, (cudaStream_t)stream);
+    cudaError_t e = launch_attend(dtype, D, pl.G, false, p, &kmap, &vmap, grid, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked split launch");
     if (pl.S > 1) {
         e = launch_combine(p.part_o, p.part_lse, out, lse_out, (int)R, pl.S, D, dtype, (cudaStream_t)stream);
@@ -336,9 +364,10 @@ kvd_status kvd_attend_paged(const void* q_in, const void* key_cache, const void*
         if (!aligned(workspace, 256)) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_paged: workspace not 256-byte aligned");
     }
     CUtensorMap kmap, vmap;
-    st = make_cache_map(&kmap, key_cache, dtype, NB, BS, Hkv, D, pl.tile);
+    const bool mma = attend_uses_mma(dtype, pl.G);
+    st = make_cache_map(&kmap, key_cache, dtype, true, (long long)NB * BS, Hkv, D, pl.tile, mma);
     if (st != KVD_OK) return st;
-    st = make_cache_map(&vmap, value_cache, dtype, NB, BS, Hkv, D, pl.tile);
+    st = make_cache_map(&vmap, value_cache, dtype, true, (long long)NB * BS, Hkv, D, pl.tile, mma);
     if (st != KVD_OK) return st;
     AttendParams p{};
     p.q = q_in;

@@ -29,6 +29,18 @@ __device__ __forceinline__ void report(int32_t* dev_status, uint32_t bits) {
     if (dev_status) atomicOr(reinterpret_cast<unsigned int*>(dev_status), bits);
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// Kernels of this library are launched with programmatic stream serialisation:
+// the next kernel on the stream may start its prologue while this one drains.
+// Every kernel therefore calls pdl_wait() before its first global memory
+// access (read or write), which returns once the previous kernel on the
+// stream has completed and its writes are visible; pdl_launch_dependents()
+// lets the next kernel be scheduled as soon as every CTA of this one runs.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -101,6 +113,16 @@ __device__ __forceinline__ void tma_g2s_3d(void* dst, const CUtensorMap* map, in
         ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
         "l"(policy)
+        : "memory");
+}
+
+// 2-D tiled tensor copy global -> shared through a tensor map.
+__device__ __forceinline__ void tma_g2s_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                           uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 

@@ -12,22 +12,37 @@ namespace kvd {
 
 struct AttendParams;
 
-// Tile geometry of the attention kernel for one element type / head_dim.
+// Launch with programmatic stream serialisation (the kernel may start while
+// the previous kernel on the stream drains; see pdl_wait in kvd_device.cuh).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// Tile geometry of the attention kernel for one element type / head_dim /
+// group width.
 struct AttendGeom {
     int tile_max;     // T: tokens per ring stage (static buffer tile)
     int stages;
     int consumer_warps;
     int smem_bytes;   // dynamic shared memory per CTA
+    bool mma;         // tensor-core consumers; K/V through 128-byte-swizzled TMA boxes
 };
 
-// Geometry of the instantiation the launchers use (G does not change it).
-AttendGeom attend_geom(kvd_dtype dt, int D);
-
-// Launch the split kernel: grid (S, Hkv * HG, rows).  `G` is the compile-time
-// group width (1, 2, 4 or 8).  Returns the launch error.
-cudaError_t launch_attend_split(kvd_dtype dt, int D, int G, bool paged, const AttendParams& p,
-                                const CUtensorMap* kmap, const CUtensorMap* vmap, dim3 grid,
-                                cudaStream_t stream);
+// Which kernel serves a group width: bf16 groups of 4 or 8 query heads per kv
+// head use the tensor-core consumers, everything else the CUDA-core ones.
+inline bool attend_uses_mma(kvd_dtype dt, int G) { return dt == KVD_BF16 && G >= 4; }
 
 // Sets the message kvd_last_error() returns on this thread.
 void set_last_error(const char* msg);

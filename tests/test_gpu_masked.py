@@ -107,10 +107,11 @@ def test_non_prefix_masks_and_skipped_tiles(kvd):
 
 
 @pytest.mark.parametrize("fill", [float("inf"), float("nan"), 1e3])
-def test_garbage_padding_is_ignored(kvd, fill):
+@pytest.mark.parametrize("Hq,Hkv", [(8, 4), (16, 2)])  # CUDA-core and tensor-core consumers
+def test_garbage_padding_is_ignored(kvd, fill, Hq, Hkv):
     """inf / NaN / large values in mask = 0 slots leave the GPU result
     bit-identical to zero padding, and equal to the oracle within tolerance."""
-    B, Hq, Hkv, C, D = 2, 8, 4, 700, 128
+    B, C, D = 2, 700, 128
     g = W.generator(8)
     q = W.randn(g, (B, Hq, D))
     k = W.randn(g, (B, Hkv, C, D))
@@ -125,8 +126,10 @@ def test_garbage_padding_is_ignored(kvd, fill):
     assert_attention_close(out1, ref, torch.bfloat16, "garbage")
 
 
-def test_single_valid_position_is_exact(kvd):
-    B, Hq, Hkv, C, D = 2, 4, 2, 300, 128
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (16, 4), (8, 1)])
+def test_single_valid_position_is_exact(kvd, Hq, Hkv):
+    B, C, D = 2, 300, 128
+    gs = Hq // Hkv
     g = W.generator(9)
     q = W.randn(g, (B, Hq, D))
     k = W.randn(g, (B, Hkv, C, D))
@@ -138,8 +141,8 @@ def test_single_valid_position_is_exact(kvd):
         out, _ = _run_masked(kvd, q, k, v, mask, 0.2, ns)
         out = host(out)
         for h in range(Hq):
-            assert torch.equal(out[0, h], v[0, h // 2, 0])
-            assert torch.equal(out[1, h], v[1, h // 2, 299])
+            assert torch.equal(out[0, h], v[0, h // gs, 0])
+            assert torch.equal(out[1, h], v[1, h // gs, 299])
 
 
 def test_split_counts_agree(kvd):
