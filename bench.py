@@ -195,7 +195,7 @@ class MaskedBench:
         self.pos_table = torch.stack([(base + i).to(torch.int32) for i in range(self.cycle)]).to(dev)
         self.gpos = self.pos_table[0].clone()
         need = kvd.attend_masked_workspace_bytes(self.B, self.Hq, self.Hkv, self.C, self.D)
-        self.ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        self.ws = kvd.workspace(need, dev)
         self.splits = need > 0
         self.out = [torch.empty_like(l.q) for l in w.layers]
         self.status = kvd.status_tensor(dev)
@@ -326,7 +326,7 @@ class PagedBench:
         self.out = torch.empty_like(pw.q)
         cols = pw.block_tables.shape[1]
         need = kvd.attend_paged_workspace_bytes(self.Q, self.Hq, self.Hkv, self.BS, cols, self.D)
-        self.ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        self.ws = kvd.workspace(need, dev)
         self.splits = need > 0
         self.status = kvd.status_tensor(dev)
         self.graph = None

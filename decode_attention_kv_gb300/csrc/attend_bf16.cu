@@ -1,26 +1,34 @@
-// attend_bf16.cu -- bf16 instantiations of the split-KV attention kernel.
+// attend_bf16.cu -- bf16 instantiations of the attention kernel: tensor-core
+// consumers for 4 or 8 query heads per kv head, CUDA-core consumers for 1-2.
 #include "attend_inst.cuh"
 
 namespace kvd {
 
 cudaError_t launch_attend_bf16(int D, int G, bool paged, const AttendParams& p,
-                               const CUtensorMap* kmap, const CUtensorMap* vmap, dim3 grid,
+                               const CUtensorMap* kmap, const CUtensorMap* vmap,
                                cudaStream_t stream) {
-    if (attend_uses_mma(KVD_BF16, G)) {
-        if (D == 64)
-            return paged ? launch_mma_g<64, true>(G, p, kmap, vmap, grid, stream)
-                         : launch_mma_g<64, false>(G, p, kmap, vmap, grid, stream);
-        if (D == 128)
-            return paged ? launch_mma_g<128, true>(G, p, kmap, vmap, grid, stream)
-                         : launch_mma_g<128, false>(G, p, kmap, vmap, grid, stream);
-        return cudaErrorInvalidValue;
+    if (D == 128) {
+        switch (G) {
+            case 1: return launch_simt<__nv_bfloat16, 128, 1>(paged, p, kmap, vmap, stream);
+            case 2: return launch_simt<__nv_bfloat16, 128, 2>(paged, p, kmap, vmap, stream);
+            case 4: return launch_mma<128, 4>(paged, p, kmap, vmap, stream);
+            case 8: return launch_mma<128, 8>(paged, p, kmap, vmap, stream);
+        }
+    } else if (D == 64) {
+        switch (G) {
+            case 1: return launch_simt<__nv_bfloat16, 64, 1>(paged, p, kmap, vmap, stream);
+            case 2: return launch_simt<__nv_bfloat16, 64, 2>(paged, p, kmap, vmap, stream);
+            case 4: return launch_mma<64, 4>(paged, p, kmap, vmap, stream);
+            case 8: return launch_mma<64, 8>(paged, p, kmap, vmap, stream);
+        }
     }
-    return launch_elem<__nv_bfloat16>(D, G, paged, p, kmap, vmap, grid, stream);
+    return cudaErrorInvalidValue;
 }
 
 AttendGeom attend_geom_bf16(int D, int G) {
-    if (attend_uses_mma(KVD_BF16, G)) return D == 64 ? mma_geom_of<64>() : mma_geom_of<128>();
-    return D == 64 ? geom_of<__nv_bfloat16, 64>() : geom_of<__nv_bfloat16, 128>();
+    if (attend_uses_mma(KVD_BF16, G)) return AttendGeom{64, 0, 4, 0, true};
+    (void)D;
+    return AttendGeom{32, 0, 4, 0, false};
 }
 
 }  // namespace kvd

@@ -1,0 +1,343 @@
+// attend_consumers.cuh -- the consumer warps of the split-KV decode attention
+// kernel: what they do with one ring tile of K/V rows.
+//
+// Both policies keep, per query head, the fp32 running max m (log2 units),
+// running sum l and unnormalised output acc over the tokens they have seen,
+// and update them per block of tokens with the correction exp(m_old - m_new)
+// ("Intel NPU running LLMs", Part 3 "Flash SDPA 路径" and Part 6 "ONNX 表达不了
+// tiling 策略"; "FlashMLA на Huawei Ascend", "Ход вычислений").  Slots whose
+// validity bit is 0 (mask = 0, past the sequence, dropped block) take no part
+// (Part 1 "解决方案：预分配 + Attention Mask").
+//
+//  SimtConsumer: CUDA cores.  D/VEC lanes hold one token's row as 16-byte
+//    vectors; q.k with packed fp32x2 FMAs and a shuffle reduction over the
+//    token's lanes; the running state is updated once per sub-chunk of tokens;
+//    p.V with packed FMAs.  Used for fp32 and for 1-2 query heads per kv head.
+//  MmaConsumer: tensor cores for bf16 groups of 4-8 query heads per kv head.
+//    q.K^T of a 16-token slab is mma.m16n8k16 with tokens on M and the packed
+//    heads on N; p.V is V^T p^T with p split into bf16 hi + lo parts (16
+//    significant bits, so the result matches the CUDA-core path to fp32
+//    rounding); K/V tiles arrive in the 128-byte swizzle so that ldmatrix is
+//    conflict-free; V rows of invalid tokens are zeroed first so that inf/NaN
+//    padding cannot reach the accumulator through 0 x inf.
+//
+// finish() leaves each warp's state in shared memory as mo[w][h][d]
+// (unnormalised output) and ml[w][h] = (m, l) for the CTA-wide merge.
+#pragma once
+
+#include "kvd_device.cuh"
+#include "mma_ptx.cuh"
+
+namespace kvd {
+
+template <typename Elem, int D, int G, int T, int NCW>
+struct SimtConsumer {
+    using Tr = ElemTraits<Elem>;
+    using ElemT = Elem;
+    static constexpr bool kSwizzled = false;
+    static constexpr int kD = D, kG = G, kT = T, kNCW = NCW;
+    static constexpr int kVec = Tr::kPerVec;   // elements per 16-byte lane vector
+    static constexpr int kPairs = kVec / 2;
+    static constexpr int kLPT = D / kVec;      // lanes per token
+    static constexpr int kTPW = 32 / kLPT;     // tokens per warp step
+    static constexpr int kTW = T / NCW;        // tokens per warp per tile
+    static constexpr int kSteps = kTW / kTPW;  // warp steps per tile
+    static constexpr int kSubWant = (32 / G) < 1 ? 1 : (32 / G);
+    static constexpr int kSub = kSteps < kSubWant ? kSteps : kSubWant;
+    static constexpr int kTileBytes = T * D * (int)sizeof(Elem);  // K (or V) of one tile
+    static_assert(D % kVec == 0 && kLPT <= 32 && 32 % kLPT == 0, "head_dim layout");
+    static_assert(T % NCW == 0 && kTW % kTPW == 0 && kSteps % kSub == 0, "tile layout");
+    static_assert(T <= 64, "validity bits of a tile fit 64 bits");
+
+    float2 q2[G][kPairs];
+    float m[G], l[G];
+    float2 acc[G][kPairs];
+
+    // q rows of the unit (staged in shared memory), scaled by scale*log2(e).
+    __device__ __forceinline__ void begin(const Elem* qs, int g_here, float qscale, int lane) {
+        const int sub = lane % kLPT;
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            if (hh < g_here) {
+                const uint4 raw = *reinterpret_cast<const uint4*>(qs + hh * D + sub * kVec);
+                Tr::unpack(raw, q2[hh]);
+#pragma unroll
+                for (int j = 0; j < kPairs; ++j) q2[hh][j] = fmul2(q2[hh][j], make_float2(qscale, qscale));
+            } else {
+#pragma unroll
+                for (int j = 0; j < kPairs; ++j) q2[hh][j] = make_float2(0.f, 0.f);
+            }
+            m[hh] = -INFINITY;
+            l[hh] = 0.f;
+#pragma unroll
+            for (int j = 0; j < kPairs; ++j) acc[hh][j] = make_float2(0.f, 0.f);
+        }
+    }
+
+    // One tile; returns whether it wrote to the ring (never, here).
+    __device__ __forceinline__ bool tile(unsigned char* kbuf, unsigned char* vbuf, uint64_t bits,
+                                         int warp, int lane, float /*qscale: folded into q*/) {
+        const Elem* Ks = reinterpret_cast<const Elem*>(kbuf);
+        const Elem* Vs = reinterpret_cast<const Elem*>(vbuf);
+        const int grp = lane / kLPT, sub = lane % kLPT;
+#pragma unroll
+        for (int c = 0; c < kSteps; c += kSub) {
+            float s[kSub][G];
+            bool val[kSub];
+#pragma unroll
+            for (int i = 0; i < kSub; ++i) {
+                const int tt = warp * kTW + (c + i) * kTPW + grp;
+                const uint4 kr = *reinterpret_cast<const uint4*>(Ks + tt * D + sub * kVec);
+                float2 kf[kPairs];
+                Tr::unpack(kr, kf);
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    float2 a = fmul2(q2[hh][0], kf[0]);
+#pragma unroll
+                    for (int j = 1; j < kPairs; ++j) a = ffma2(q2[hh][j], kf[j], a);
+                    s[i][hh] = a.x + a.y;
+                }
+                val[i] = (bits >> tt) & 1ull;
+            }
+#pragma unroll
+            for (int off = kLPT / 2; off > 0; off >>= 1)
+#pragma unroll
+                for (int i = 0; i < kSub; ++i)
+#pragma unroll
+                    for (int hh = 0; hh < G; ++hh)
+                        s[i][hh] += __shfl_xor_sync(0xffffffffu, s[i][hh], off);
+
+            float pr[kSub][G];
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < kSub; ++i) {
+                    s[i][hh] = val[i] ? s[i][hh] : -INFINITY;
+                    mx = fmaxf(mx, s[i][hh]);
+                }
+                const float mn = fmaxf(m[hh], mx);
+                const float base = (mn == -INFINITY) ? 0.f : mn;
+                const float corr = fast_exp2(m[hh] - base);
+                m[hh] = mn;
+                float ls = 0.f;
+#pragma unroll
+                for (int i = 0; i < kSub; ++i) {
+                    pr[i][hh] = fast_exp2(s[i][hh] - base);
+                    ls += pr[i][hh];
+                }
+                l[hh] = fmaf(l[hh], corr, ls);
+                const float2 c2 = make_float2(corr, corr);
+#pragma unroll
+                for (int j = 0; j < kPairs; ++j) acc[hh][j] = fmul2(acc[hh][j], c2);
+            }
+#pragma unroll
+            for (int i = 0; i < kSub; ++i) {
+                const int tt = warp * kTW + (c + i) * kTPW + grp;
+                uint4 vr = *reinterpret_cast<const uint4*>(Vs + tt * D + sub * kVec);
+                if (!val[i]) vr = make_uint4(0, 0, 0, 0);  // padding may hold inf/NaN
+                float2 vf[kPairs];
+                Tr::unpack(vr, vf);
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    const float2 pp = make_float2(pr[i][hh], pr[i][hh]);
+#pragma unroll
+                    for (int j = 0; j < kPairs; ++j) acc[hh][j] = ffma2(pp, vf[j], acc[hh][j]);
+                }
+            }
+        }
+        return false;
+    }
+
+    // Merge the lane groups (different tokens) of the warp; leave the warp's
+    // state in mo / ml.
+    __device__ __forceinline__ void finish(float* mo, float* ml, int warp, int lane) {
+#pragma unroll
+        for (int off = kLPT; off < 32; off <<= 1) {
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                const float mo_ = __shfl_xor_sync(0xffffffffu, m[hh], off);
+                const float lo = __shfl_xor_sync(0xffffffffu, l[hh], off);
+                const float mn = fmaxf(m[hh], mo_);
+                const float base = (mn == -INFINITY) ? 0.f : mn;
+                const float a = fast_exp2(m[hh] - base), b = fast_exp2(mo_ - base);
+                l[hh] = l[hh] * a + lo * b;
+                m[hh] = mn;
+#pragma unroll
+                for (int j = 0; j < kPairs; ++j) {
+                    float2 other;
+                    other.x = __shfl_xor_sync(0xffffffffu, acc[hh][j].x, off);
+                    other.y = __shfl_xor_sync(0xffffffffu, acc[hh][j].y, off);
+                    acc[hh][j] = ffma2(acc[hh][j], make_float2(a, a), fmul2(other, make_float2(b, b)));
+                }
+            }
+        }
+        const int grp = lane / kLPT, sub = lane % kLPT;
+        if (grp == 0) {
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+#pragma unroll
+                for (int j = 0; j < kPairs; ++j) {
+                    const int d = sub * kVec + 2 * j;
+                    mo[(warp * G + hh) * D + d] = acc[hh][j].x;
+                    mo[(warp * G + hh) * D + d + 1] = acc[hh][j].y;
+                }
+                if (sub == 0) {
+                    ml[(warp * G + hh) * 2] = m[hh];
+                    ml[(warp * G + hh) * 2 + 1] = l[hh];
+                }
+            }
+        }
+    }
+};
+
+template <int D, int G, int T, int NCW>
+struct MmaConsumer {
+    using ElemT = __nv_bfloat16;
+    static constexpr bool kSwizzled = true;
+    static constexpr int kD = D, kG = G, kT = T, kNCW = NCW;
+    static constexpr int kHalves = D / 64;      // 128-byte column halves per row
+    static constexpr int kHalfBytes = T * 128;
+    static constexpr int kTileBytes = kHalves * kHalfBytes;
+    static constexpr int kSlabsPerWarp = T / 16 / NCW;
+    static constexpr int kKSteps = D / 16;      // q.K^T: 16 dims per mma
+    static constexpr int kDBlocks = D / 16;     // p.V: 16 output dims per mma
+    static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
+    static_assert(G >= 1 && G <= 8, "at most 8 query heads per mma column block");
+    static_assert(T % (16 * NCW) == 0 && kSlabsPerWarp >= 1, "16-token slabs per warp");
+    static_assert(kHalfBytes % 1024 == 0, "swizzled halves stay 1024-byte aligned");
+    static_assert(T <= 64, "validity bits of a tile fit 64 bits");
+
+    uint32_t qb[kKSteps][2];  // q^T as the B operand: column gid = query head
+    float m[2], l[2];         // columns (heads) 2*tig, 2*tig + 1; l: this thread's rows
+    float acc[kDBlocks][4];   // V^T p^T: rows d*16 + gid (+8), columns 2*tig (+1)
+
+    __device__ __forceinline__ void begin(const __nv_bfloat16* qs, int g_here, float /*qscale*/,
+                                          int lane) {
+        const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int ks = 0; ks < kKSteps; ++ks) {
+            if (gid < g_here) {
+                const __nv_bfloat16* qp = qs + gid * D + ks * 16 + 2 * tig;
+                qb[ks][0] = *reinterpret_cast<const uint32_t*>(qp);
+                qb[ks][1] = *reinterpret_cast<const uint32_t*>(qp + 8);
+            } else {
+                qb[ks][0] = qb[ks][1] = 0u;
+            }
+        }
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
+#pragma unroll
+        for (int d = 0; d < kDBlocks; ++d) acc[d][0] = acc[d][1] = acc[d][2] = acc[d][3] = 0.f;
+    }
+
+    __device__ __forceinline__ bool tile(unsigned char* kbuf, unsigned char* vbuf, uint64_t bits,
+                                         int warp, int lane, float qscale) {
+        const int gid = lane >> 2, tig = lane & 3;
+        const uint32_t kbase = smem_u32(kbuf), vbase = smem_u32(vbuf);
+        bool wrote = false;
+#pragma unroll
+        for (int sl = 0; sl < kSlabsPerWarp; ++sl) {
+            const int slab0 = (warp * kSlabsPerWarp + sl) * 16;
+            const uint32_t vmask = (uint32_t)(bits >> slab0) & 0xffffu;
+            if (vmask == 0u) continue;
+            if (vmask != 0xffffu) {
+                for (int i = lane; i < 16 * kHalves * 8; i += 32) {
+                    const int row = i / (kHalves * 8);
+                    const int rest = i % (kHalves * 8);
+                    if (!((vmask >> row) & 1u)) {
+                        const int h = rest >> 3, ch = rest & 7;
+                        *reinterpret_cast<uint4*>(vbuf + h * kHalfBytes + (slab0 + row) * 128 +
+                                                  ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                wrote = true;
+                __syncwarp();
+            }
+            const bool v_lo = (vmask >> gid) & 1u, v_hi = (vmask >> (gid + 8)) & 1u;
+
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < kKSteps; ++ks) {
+                uint32_t a[4];
+                const int row = slab0 + (lane & 15);
+                const int ch = (ks & 3) * 2 + (lane >> 4);
+                ldsm_x4(kbase + (ks >> 2) * kHalfBytes + swz128(row, ch), a);
+                mma_bf16(s, a, qb[ks][0], qb[ks][1]);
+            }
+            s[0] = v_lo ? s[0] * qscale : -INFINITY;
+            s[1] = v_lo ? s[1] * qscale : -INFINITY;
+            s[2] = v_hi ? s[2] * qscale : -INFINITY;
+            s[3] = v_hi ? s[3] * qscale : -INFINITY;
+
+            float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+            const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float c0 = fast_exp2(m[0] - b0), c1 = fast_exp2(m[1] - b1);
+            m[0] = mn0;
+            m[1] = mn1;
+            const float p0 = fast_exp2(s[0] - b0), p1 = fast_exp2(s[1] - b1);
+            const float p2 = fast_exp2(s[2] - b0), p3 = fast_exp2(s[3] - b1);
+            l[0] = fmaf(l[0], c0, p0 + p2);
+            l[1] = fmaf(l[1], c1, p1 + p3);
+            const float2 cc = make_float2(c0, c1);
+#pragma unroll
+            for (int d = 0; d < kDBlocks; ++d) {
+                const float2 x = fmul2(make_float2(acc[d][0], acc[d][1]), cc);
+                const float2 y = fmul2(make_float2(acc[d][2], acc[d][3]), cc);
+                acc[d][0] = x.x;
+                acc[d][1] = x.y;
+                acc[d][2] = y.x;
+                acc[d][3] = y.y;
+            }
+
+            const uint32_t hi_lo = pack_bf16x2(p0, p1), hi_hi = pack_bf16x2(p2, p3);
+            const float2 h0 = bf16x2_to_float2(hi_lo), h1 = bf16x2_to_float2(hi_hi);
+            const uint32_t lo_lo = pack_bf16x2(p0 - h0.x, p1 - h0.y);
+            const uint32_t lo_hi = pack_bf16x2(p2 - h1.x, p3 - h1.y);
+            const uint32_t bh0 = movmatrix_trans(hi_lo), bh1 = movmatrix_trans(hi_hi);
+            const uint32_t bl0 = movmatrix_trans(lo_lo), bl1 = movmatrix_trans(lo_hi);
+#pragma unroll
+            for (int d = 0; d < kDBlocks; ++d) {
+                uint32_t a[4];
+                const int row = slab0 + (lane & 7) + ((lane >> 4) << 3);
+                const int ch = (d & 3) * 2 + ((lane >> 3) & 1);
+                ldsm_x4_trans(vbase + (d >> 2) * kHalfBytes + swz128(row, ch), a);
+                mma_bf16(acc[d], a, bh0, bh1);
+                mma_bf16(acc[d], a, bl0, bl1);
+            }
+        }
+        return wrote;
+    }
+
+    __device__ __forceinline__ void finish(float* mo, float* ml, int warp, int lane) {
+        const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+            l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int hh = 2 * tig + c;
+            if (hh < G) {
+#pragma unroll
+                for (int d = 0; d < kDBlocks; ++d) {
+                    mo[(warp * G + hh) * D + d * 16 + gid] = acc[d][c];
+                    mo[(warp * G + hh) * D + d * 16 + gid + 8] = acc[d][2 + c];
+                }
+                if (gid == 0) {
+                    ml[(warp * G + hh) * 2] = m[c];
+                    ml[(warp * G + hh) * 2 + 1] = l[c];
+                }
+            }
+        }
+    }
+};
+
+}  // namespace kvd

@@ -1,114 +1,89 @@
-// attend_inst.cuh -- instantiation and launch of the split kernel for one
-// element type.  Included by exactly one .cu per element type so that the
-// instantiations compile in parallel.
+// attend_inst.cuh -- instantiation and launch of the persistent attention
+// kernel for one element type.  Included by exactly one .cu per element type
+// so that the instantiations compile in parallel.
 #pragma once
 
-#include "attend_mma.cuh"
-#include "attend_split.cuh"
+#include <mutex>
+
+#include "attend_kernel.cuh"
 #include "kvd_internal.h"
 
 namespace kvd {
 
-// Tile / ring / warp geometry per element type and head_dim.  A ring stage
-// holds K and V of T tokens; two CTAs fit on one SM.
-template <typename Elem, int D>
-struct Geom {
-    static constexpr int T = 32;
-    static constexpr int NCW = 4;
-    static constexpr int kStage = 2 * T * D * (int)sizeof(Elem);
-    static constexpr int STAGES = (96 * 1024 / kStage) > 8 ? 8 : (96 * 1024 / kStage);
+// Ring depth that keeps a CTA near `budget` bytes of stages (2..8 stages).
+constexpr int stages_for(int stage_bytes, int budget) {
+    return budget / stage_bytes < 2 ? 2 : (budget / stage_bytes > 8 ? 8 : budget / stage_bytes);
+}
+
+// CUDA-core consumers: 32-token tiles, four consumer warps, about 100 KB of
+// ring so that two CTAs share an SM.
+template <typename Elem, int D, int G>
+struct SimtCfg {
+    using Cons = SimtConsumer<Elem, D, G, 32, 4>;
+    static constexpr int STAGES = stages_for(KernelShape<Cons, 2>::kStageBytes, 100 * 1024);
 };
 
-template <typename Elem, int D, int G, bool PAGED>
-cudaError_t launch_one(const AttendParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
-                       dim3 grid, cudaStream_t stream) {
-    using Gm = Geom<Elem, D>;
-    using Sh = AttendShape<Elem, D, G, Gm::T, Gm::STAGES, Gm::NCW>;
-    auto kern = attend_split_kernel<Elem, D, G, Gm::T, Gm::STAGES, Gm::NCW, PAGED>;
-    static int configured_device = -1;  // attribute set once per device
+// Tensor-core consumers: 64-token tiles (one 16-token slab per consumer
+// warp), a ring of about 170 KB, one CTA per SM.
+template <int D, int G>
+struct MmaCfg {
+    using Cons = MmaConsumer<D, G, 64, 4>;
+    static constexpr int STAGES = stages_for(KernelShape<Cons, 2>::kStageBytes, 160 * 1024);
+};
+
+// Per-device launch facts of one kernel instantiation: the shared-memory
+// attribute is set and the persistent grid sized once per device.
+struct DeviceFacts {
+    std::mutex mu;
+    int ctas[64] = {};  // persistent CTAs per device (0 = not set up yet)
+};
+
+template <class Cons, int STAGES, bool PAGED>
+cudaError_t launch_kernel(const AttendParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
+                          cudaStream_t stream) {
+    using Sh = KernelShape<Cons, STAGES>;
+    auto kern = attend_kernel<Cons, STAGES, PAGED>;
+    constexpr int kThreads = Sh::kThreads;
+    static DeviceFacts facts;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (configured_device != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmemAlloc);
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int ctas;
+    {
+        std::lock_guard<std::mutex> lock(facts.mu);
+        if (!facts.ctas[dev]) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Sh::kSmemAlloc);
+            if (e != cudaSuccess) return e;
+            int per_sm = 0, nsm = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads,
+                                                              Sh::kSmemAlloc);
+            if (e != cudaSuccess) return e;
+            e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess) return e;
+            facts.ctas[dev] = (per_sm < 1 ? 1 : per_sm) * (nsm < 1 ? 1 : nsm);
+        }
+        ctas = facts.ctas[dev];
     }
-    return launch_pdl(kern, grid, dim3((Gm::NCW + 1) * 32), Sh::kSmemAlloc, stream, p, *kmap,
-                      *vmap);
+    const int grid = p.units < ctas ? p.units : ctas;
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), Sh::kSmemAlloc, stream, p, *kmap, *vmap);
 }
 
-template <typename Elem, int D, bool PAGED>
-cudaError_t launch_g(int G, const AttendParams& p, const CUtensorMap* kmap,
-                     const CUtensorMap* vmap, dim3 grid, cudaStream_t stream) {
-    switch (G) {
-        case 1: return launch_one<Elem, D, 1, PAGED>(p, kmap, vmap, grid, stream);
-        case 2: return launch_one<Elem, D, 2, PAGED>(p, kmap, vmap, grid, stream);
-        case 4: return launch_one<Elem, D, 4, PAGED>(p, kmap, vmap, grid, stream);
-        case 8: return launch_one<Elem, D, 8, PAGED>(p, kmap, vmap, grid, stream);
-        default: return cudaErrorInvalidValue;
-    }
+template <typename Elem, int D, int G>
+cudaError_t launch_simt(bool paged, const AttendParams& p, const CUtensorMap* kmap,
+                        const CUtensorMap* vmap, cudaStream_t stream) {
+    using C = SimtCfg<Elem, D, G>;
+    return paged ? launch_kernel<typename C::Cons, C::STAGES, true>(p, kmap, vmap, stream)
+                 : launch_kernel<typename C::Cons, C::STAGES, false>(p, kmap, vmap, stream);
 }
 
-template <typename Elem>
-cudaError_t launch_elem(int D, int G, bool paged, const AttendParams& p, const CUtensorMap* kmap,
-                        const CUtensorMap* vmap, dim3 grid, cudaStream_t stream) {
-    if (D == 64)
-        return paged ? launch_g<Elem, 64, true>(G, p, kmap, vmap, grid, stream)
-                     : launch_g<Elem, 64, false>(G, p, kmap, vmap, grid, stream);
-    if (D == 128)
-        return paged ? launch_g<Elem, 128, true>(G, p, kmap, vmap, grid, stream)
-                     : launch_g<Elem, 128, false>(G, p, kmap, vmap, grid, stream);
-    return cudaErrorInvalidValue;
-}
-
-template <typename Elem, int D>
-AttendGeom geom_of() {
-    using Gm = Geom<Elem, D>;
-    using Sh = AttendShape<Elem, D, 8, Gm::T, Gm::STAGES, Gm::NCW>;
-    return AttendGeom{Gm::T, Gm::STAGES, Gm::NCW, Sh::kSmemAlloc, false};
-}
-
-// Tensor-core kernel geometry: 64-token stages (one 16-token slab per
-// consumer warp), three stages, two CTAs per SM.
-struct MmaGeom {
-    static constexpr int T = 64;
-    static constexpr int NCW = 4;
-    static constexpr int STAGES = 3;
-};
-
-template <int D, int G, bool PAGED>
-cudaError_t launch_mma_one(const AttendParams& p, const CUtensorMap* kmap,
-                           const CUtensorMap* vmap, dim3 grid, cudaStream_t stream) {
-    using Sh = MmaShape<D, G, MmaGeom::T, MmaGeom::STAGES, MmaGeom::NCW>;
-    auto kern = attend_mma_kernel<D, G, MmaGeom::T, MmaGeom::STAGES, MmaGeom::NCW, PAGED>;
-    static int configured_device = -1;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (configured_device != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmemAlloc);
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
-    return launch_pdl(kern, grid, dim3((MmaGeom::NCW + 1) * 32), Sh::kSmemAlloc, stream, p, *kmap,
-                      *vmap);
-}
-
-template <int D, bool PAGED>
-cudaError_t launch_mma_g(int G, const AttendParams& p, const CUtensorMap* kmap,
-                         const CUtensorMap* vmap, dim3 grid, cudaStream_t stream) {
-    switch (G) {
-        case 4: return launch_mma_one<D, 4, PAGED>(p, kmap, vmap, grid, stream);
-        case 8: return launch_mma_one<D, 8, PAGED>(p, kmap, vmap, grid, stream);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-template <int D>
-AttendGeom mma_geom_of() {
-    using Sh = MmaShape<D, 8, MmaGeom::T, MmaGeom::STAGES, MmaGeom::NCW>;
-    return AttendGeom{MmaGeom::T, MmaGeom::STAGES, MmaGeom::NCW, Sh::kSmemAlloc, true};
+template <int D, int G>
+cudaError_t launch_mma(bool paged, const AttendParams& p, const CUtensorMap* kmap,
+                       const CUtensorMap* vmap, cudaStream_t stream) {
+    using C = MmaCfg<D, G>;
+    return paged ? launch_kernel<typename C::Cons, C::STAGES, true>(p, kmap, vmap, stream)
+                 : launch_kernel<typename C::Cons, C::STAGES, false>(p, kmap, vmap, stream);
 }
 
 }  // namespace kvd

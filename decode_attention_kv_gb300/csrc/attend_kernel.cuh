@@ -1,0 +1,702 @@
+// attend_kernel.cuh -- persistent split-KV decode attention kernel (static
+// buffer + 0/1 mask, or paged cache through block tables).
+//
+// What it computes (page title, section):
+//  * "Intel NPU running LLMs" (OpenVINO community article 882): Part 1
+//    "解决方案：预分配 + Attention Mask" -- slots with mask = 0 take no part in
+//    the softmax; Part 3 "Attention 在 NPU 上的完整实现" -- decode is one query
+//    against all cached keys, and the Flash SDPA path tiles the sequence axis
+//    and merges the tiles exactly through a running output, max and sum.
+//  * "FlashMLA на Huawei Ascend", "Математическая постановка" / "Ход
+//    вычислений" -- out = softmax(q K^T * scale) V with fp32 running state and
+//    one log-sum-exp per row.
+//  * "PyPTO 实现 AscendC GatherPaKvCache（Norm/ND 分支）" 3.2-3.3 -- token t of
+//    sequence q is slot t % BS of block block_tables[q, seq_offset[q]/BS +
+//    t/BS]; cumsum seq_lens; the constraints on seq_offset and the table.
+//
+// Work.  A unit is one (row, split): row = (batch entry or sequence, kv head,
+// group of <= G query heads sharing it), split = a chunk of `chunk` token
+// slots of that row.  Units are numbered row-major (splits of one row are
+// consecutive) and handed out by a global counter, so the grid is persistent
+// (about one or two CTAs per SM) and load-balances rows of any length.
+//
+// CTA.  Four roles in warps:
+//  * scheduler (warp NCW+1): takes units from the work counter, reads their
+//    metadata (sequence length and block-table entries, or the split's mask)
+//    into 32-token validity words, and queues them for the loader up to four
+//    units ahead; a split without a valid token never reaches the loader --
+//    its log-sum-exps are set to -inf (or, single split, its rows to zero).
+//  * loader (warp NCW): skips tiles with no valid token and streams the others
+//    into a STAGES-deep ring with 1-D bulk copies (static buffer, CUDA-core
+//    consumers) or 2-D/3-D TMA tensor copies (paged, or 128-byte-swizzled
+//    boxes for the tensor-core consumers); a unit's q rows ride along with its
+//    first tile.  Each stage carries metadata: unit, tile, the tile's 64
+//    validity bits, first/last-tile flags.  It runs ahead across unit
+//    boundaries, so the ring does not drain between units.
+//  * consumers (warps 0..NCW-1, attend_consumers.cuh): the online softmax over
+//    the tiles; at a unit's last tile they drop their states into one of two
+//    merge buffers and go on with the next unit.
+//  * epilogue (warp NCW+2): merges the consumer warps' states of a unit and
+//    writes either the final rows (single split) or a normalised partial row
+//    and its log-sum-exp.
+// With more than one split the host launches the log-sum-exp combine kernel
+// right behind this one (programmatic dependent launch): it runs once the
+// partial rows are complete, without atomics or fences here.
+//
+// Counters (unit counter, CTAs-done counter) live in the caller's workspace:
+// zero before the first call; the last CTA to finish taking units resets them.
+// All waits are bounded; a wait that runs out sets KVD_DEV_TIMEOUT, after
+// which the counters must be zeroed again.
+#pragma once
+
+#include "attend_consumers.cuh"
+
+namespace kvd {
+
+constexpr int kMaxChunk = 4096;              // tokens per split, upper bound
+constexpr int kMaxWords = kMaxChunk / 32;    // validity words per split
+constexpr int kMaxBlocks = 128;              // block-table entries per split
+
+struct AttendParams {
+    const void* q;               // [rows, Hq, D]
+    const void* k;               // static buffer [B, Hkv, C, D]
+    const void* v;
+    const uint8_t* mask;         // static buffer [B, C]
+    const int32_t* block_tables; // paged [Q, cols]
+    const int32_t* seq_lens;     // paged [Q + 1]
+    const int32_t* seq_offset;   // paged [Q] or null
+    void* out;                   // [rows, Hq, D]
+    float* lse_out;              // [rows, Hq] or null
+    float* part_o;               // [rows * Hq, S, D]       (S > 1)
+    float* part_lse;             // [rows * Hq, S]          (S > 1)
+    uint32_t* sched;             // [0] next unit, [1] CTAs done
+    int32_t* dev_status;
+    int Hq, Hkv, g, HG;          // g = Hq / Hkv, HG = head groups per kv head
+    int C;                       // static buffer capacity
+    int BS, cols, NB;            // paged geometry
+    int tile;                    // tokens per ring stage (paged: divides BS)
+    int chunk;                   // tokens per split (multiple of tile and of 32)
+    int S;                       // splits per row
+    int units;                   // rows * Hkv * HG * S
+    int mask_vec;                // mask rows 16-byte aligned (C % 16 == 0)
+    float qscale;                // scale * log2(e)
+    int direct;                  // S == 1: units write the output rows directly
+};
+
+enum : uint32_t { kFirst = 1u, kLast = 2u, kCombine = 4u, kEnd = 8u };
+
+struct StageMeta {
+    int unit;
+    int tile;
+    uint32_t flags;
+    uint32_t pad;
+    unsigned long long bits;  // validity of the tile's tokens
+};
+
+// One unit: its split, its row (counter index) and the query rows it serves.
+struct Unit {
+    int split, ru, bz, kvh, hg, g_here;
+    size_t qrow0;
+};
+
+__device__ __forceinline__ Unit decode_unit(const AttendParams& p, int G, int u) {
+    Unit un;
+    un.split = u % p.S;
+    un.ru = u / p.S;
+    const int per_bz = p.Hkv * p.HG;
+    un.bz = un.ru / per_bz;
+    const int rem = un.ru % per_bz;
+    un.kvh = rem / p.HG;
+    un.hg = rem % p.HG;
+    un.g_here = min(G, p.g - un.hg * G);
+    un.qrow0 = (size_t)un.bz * p.Hq + (size_t)un.kvh * p.g + (size_t)un.hg * G;
+    return un;
+}
+
+// A unit prepared by the scheduler warp for the loader warp.
+enum : int { kSlotTiles = 0, kSlotCombine = 1, kSlotEnd = 2 };
+constexpr int kQueueSlots = 4;
+
+struct UnitSlot {
+    int kind;    // kSlotTiles: stream the unit's tiles; kSlotCombine: only merge its row
+    int unit;
+    int t_begin, ntok;
+    int last;    // last tile that holds a valid token
+    int lb0;     // first logical block of the split (paged)
+    int pad[2];
+    uint32_t words[kMaxWords];  // validity of the split's tokens
+    int blocks[kMaxBlocks];     // physical block of each logical block (paged; -1 = dropped)
+};
+
+constexpr int kMergeBufs = 2;
+
+// Shared-memory control block:
+// full[STAGES] | empty[STAGES] | qfull[Q] | qempty[Q] | mfull[M] | mempty[M] | meta[STAGES] |
+// abort | mhdr[M] | slots[Q]
+template <int STAGES, int G>
+struct CtlLayout {
+    static constexpr int kBar = 0;
+    static constexpr int kQBar = kBar + 2 * STAGES * 8;
+    static constexpr int kMBar = kQBar + 2 * kQueueSlots * 8;
+    static constexpr int kMeta = kMBar + 2 * kMergeBufs * 8;
+    static constexpr int kAbort = kMeta + STAGES * (int)sizeof(StageMeta);
+    static constexpr int kMhdr = kAbort + 4;
+    static constexpr int kSlots = (kMhdr + 4 * kMergeBufs + 15) / 16 * 16;
+    static constexpr int kBytes = kSlots + kQueueSlots * (int)sizeof(UnitSlot);
+};
+
+template <int STAGES, int G>
+struct Ctl {
+    uint64_t* full;     // ring stage landed (loader -> consumers)
+    uint64_t* empty;    // ring stage consumed (consumers -> loader)
+    uint64_t* qfull;    // unit slot filled (scheduler -> loader)
+    uint64_t* qempty;   // unit slot read (loader -> scheduler)
+    uint64_t* mfull;    // merge buffer filled (consumers -> epilogue)
+    uint64_t* mempty;   // merge buffer read (epilogue -> consumers)
+    StageMeta* meta;
+    volatile int* abort_flag;
+    int* mhdr;          // unit of each merge buffer (-1: end of work)
+    UnitSlot* slots;
+    __device__ explicit Ctl(unsigned char* base) {
+        using L = CtlLayout<STAGES, G>;
+        full = reinterpret_cast<uint64_t*>(base + L::kBar);
+        empty = full + STAGES;
+        qfull = reinterpret_cast<uint64_t*>(base + L::kQBar);
+        qempty = qfull + kQueueSlots;
+        mfull = reinterpret_cast<uint64_t*>(base + L::kMBar);
+        mempty = mfull + kMergeBufs;
+        meta = reinterpret_cast<StageMeta*>(base + L::kMeta);
+        abort_flag = reinterpret_cast<volatile int*>(base + L::kAbort);
+        mhdr = reinterpret_cast<int*>(base + L::kMhdr);
+        slots = reinterpret_cast<UnitSlot*>(base + L::kSlots);
+    }
+};
+
+template <class Cons, int STAGES>
+struct KernelShape {
+    using Elem = typename Cons::ElemT;
+    static constexpr int kQBytes = Cons::kG * Cons::kD * (int)sizeof(Elem);
+    static constexpr int kStageBytes = (2 * Cons::kTileBytes + kQBytes + 1023) / 1024 * 1024;
+    static constexpr int kRingBytes = STAGES * kStageBytes;
+    // one merge buffer: mo [NCW][G][D] then ml [NCW][G][2]
+    static constexpr int kMergeBuf = (Cons::kNCW * Cons::kG * (Cons::kD + 2) * 4 + 127) / 128 * 128;
+    static constexpr int kCtlOff = kRingBytes + kMergeBufs * kMergeBuf;
+    static constexpr int kSmemAlloc = kCtlOff + CtlLayout<STAGES, Cons::kG>::kBytes + 1024;
+    static constexpr int kThreads = (Cons::kNCW + 3) * 32;  // consumers, loader, scheduler, epilogue
+    static_assert(Cons::kTileBytes % 1024 == 0, "tiles keep stage parts 1024-byte aligned");
+};
+
+// The split's token range [t_begin, t_end) of its sequence, the ring tiles it
+// spans and (paged) the first block-table column.  Paged sequences that break
+// a constraint of the gather page become empty; `reporter` reports it.
+struct SplitRange {
+    int t_begin, t_end, ntok, ntiles, first_col;
+};
+
+template <bool PAGED>
+__device__ __forceinline__ SplitRange split_range(const AttendParams& p, int bz, int split,
+                                                  bool reporter) {
+    SplitRange r;
+    r.t_begin = split * p.chunk;
+    r.first_col = 0;
+    if constexpr (PAGED) {
+        const int s0 = p.seq_lens[bz], s1 = p.seq_lens[bz + 1];
+        const int off = p.seq_offset ? p.seq_offset[bz] : 0;
+        int len = s1 - s0;
+        // A cumsum that does not start at 0 is reported; the differences are
+        // still well defined and used.  Other violations empty the sequence.
+        uint32_t bad = (bz == 0 && s0 != 0) ? KVD_DEV_SEQLENS : 0u;
+        if (len < 0) {
+            bad |= KVD_DEV_SEQLENS;
+            len = 0;
+        } else if (off < 0 || off % p.BS != 0) {
+            bad |= KVD_DEV_SEQ_OFFSET;
+            len = 0;
+        } else {
+            r.first_col = off / p.BS;
+            if (r.first_col + (len + p.BS - 1) / p.BS > p.cols) {
+                bad |= KVD_DEV_TABLE_COLS;
+                len = 0;
+            }
+        }
+        if (bad && reporter) report(p.dev_status, bad);
+        r.t_end = min(len, r.t_begin + p.chunk);
+    } else {
+        r.t_end = min(p.C, r.t_begin + p.chunk);
+    }
+    r.ntok = max(0, r.t_end - r.t_begin);
+    r.ntiles = (r.ntok + p.tile - 1) / p.tile;
+    return r;
+}
+
+// Validity bits of relative tokens [r0, r0 + n) of the split (n <= 64).
+__device__ __forceinline__ uint64_t tile_bits(const uint32_t* words, int r0, int n) {
+    uint64_t bits = 0;
+    int k = 0;
+    while (k < n) {
+        const int w = (r0 + k) >> 5, b = (r0 + k) & 31;
+        const int take = min(32 - b, n - k);
+        const uint32_t m = (take == 32) ? 0xffffffffu : ((1u << take) - 1u);
+        bits |= (uint64_t)((words[w] >> b) & m) << k;
+        k += take;
+    }
+    return bits;
+}
+
+// Four bytes -> four bits (bit i set when byte i is nonzero).
+__device__ __forceinline__ uint32_t nonzero_bytes(uint32_t x) {
+    uint32_t t = x | (x >> 4);
+    t |= t >> 2;
+    t |= t >> 1;
+    return (t & 1u) | ((t >> 7) & 2u) | ((t >> 14) & 4u) | ((t >> 21) & 8u);
+}
+
+// Producer warp, all lanes: the split's validity words (bit = token valid:
+// mask != 0, or below the sequence length with its block id in range) and,
+// paged, the physical block of each logical block the split touches.  Writes
+// the words of every tile of the split (bits past the range are 0).  Returns
+// the split's first logical block (paged).
+template <bool PAGED>
+__device__ __forceinline__ int producer_scan(const AttendParams& p, const SplitRange& r, int bz,
+                                             int lane, uint32_t* words, int* blocks) {
+    const int nwords = (r.ntiles * p.tile + 31) / 32;
+    int lb0 = 0;
+    if constexpr (PAGED) {
+        if (r.ntok > 0) {
+            lb0 = r.t_begin / p.BS;
+            const int nblk = (r.t_end - 1) / p.BS - lb0 + 1;
+            const int32_t* row = p.block_tables + (size_t)bz * p.cols + r.first_col + lb0;
+            for (int j = lane; j < nblk; j += 32) {
+                int ph = row[j];
+                if (ph < 0 || ph >= p.NB) {
+                    report(p.dev_status, KVD_DEV_BLOCK_RANGE);
+                    ph = -1;
+                }
+                blocks[j] = ph;
+            }
+            __syncwarp();
+        }
+        for (int j = 0; j < nwords; ++j) {
+            const int tok = r.t_begin + 32 * j + lane;
+            const bool ok = tok < r.t_end && blocks[tok / p.BS - lb0] >= 0;
+            const uint32_t w = __ballot_sync(0xffffffffu, ok);
+            if (lane == 0) words[j] = w;
+        }
+    } else {
+        const uint8_t* mrow = p.mask + (size_t)bz * p.C;
+        if (p.mask_vec) {
+            // 16 slots per lane per vector, 512 slots per warp round; the whole
+            // split's mask is requested before any bit is used.
+            constexpr int R = kMaxChunk / 512;
+            const int nvec = (r.ntok + 15) / 16;
+            const uint4* src = reinterpret_cast<const uint4*>(mrow + r.t_begin);
+            uint4 mv[R];
+#pragma unroll
+            for (int k = 0; k < R; ++k) {
+                const int vi = k * 32 + lane;
+                mv[k] = vi < nvec ? __ldg(src + vi) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int k = 0; k < R; ++k) {
+                const int vi = k * 32 + lane;
+                uint32_t bits = nonzero_bytes(mv[k].x) | (nonzero_bytes(mv[k].y) << 4) |
+                                (nonzero_bytes(mv[k].z) << 8) | (nonzero_bytes(mv[k].w) << 12);
+                const int nv = min(max(r.ntok - vi * 16, 0), 16);
+                bits &= (nv >= 16) ? 0xffffu : ((1u << nv) - 1u);
+                const uint32_t hi = __shfl_down_sync(0xffffffffu, bits, 1);
+                const int j = vi >> 1;
+                if ((lane & 1) == 0 && j < nwords) words[j] = bits | (hi << 16);
+            }
+        } else {
+            for (int j0 = 0; j0 < nwords; j0 += 8) {
+                uint8_t mb[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int tok = r.t_begin + 32 * (j0 + u) + lane;
+                    mb[u] = (j0 + u < nwords && tok < r.t_end) ? __ldg(mrow + tok) : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint32_t w = __ballot_sync(0xffffffffu, mb[u] != 0);
+                    if (lane == 0 && j0 + u < nwords) words[j0 + u] = w;
+                }
+            }
+        }
+    }
+    __syncwarp();
+    return lb0;
+}
+
+// One warp turns the consumer warps' states of a unit (mo[w][h][d] and
+// ml[w][h] = (m, l) in a merge buffer) into the unit's rows: the final output
+// (single split) or a normalised partial row and its natural-log log-sum-exp.
+template <typename Elem, int D, int G, int NCW>
+__device__ __forceinline__ void write_rows(const AttendParams& p, const float* mo,
+                                           const float* ml, const Unit& un, int lane) {
+    for (int idx = lane; idx < un.g_here * D; idx += 32) {
+        const int hh = idx / D, d = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, ml[(w * G + hh) * 2]);
+        const float base = (M == -INFINITY) ? 0.f : M;
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+            const float sc = fast_exp2(ml[(w * G + hh) * 2] - base);
+            L = fmaf(ml[(w * G + hh) * 2 + 1], sc, L);
+            O = fmaf(mo[(w * G + hh) * D + d], sc, O);
+        }
+        const size_t row = un.qrow0 + hh;
+        const float lse = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+        if (p.direct) {
+            ElemTraits<Elem>::store(p.out, row * D + d, L > 0.f ? O / L : 0.f);
+            if (d == 0 && p.lse_out) p.lse_out[row] = lse;
+        } else {
+            if (L > 0.f) p.part_o[(row * p.S + un.split) * D + d] = O / L;
+            if (d == 0) p.part_lse[row * p.S + un.split] = lse;
+        }
+    }
+}
+
+// Bounded mbarrier wait whose outcome is the same for every lane of the warp
+// (every lane waits, for its own acquire; a timeout in any lane counts for all).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
+                                          const volatile int* abort_flag) {
+    const bool ok = mbar_wait(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, ok);
+}
+
+
+template <class Cons, int STAGES, bool PAGED>
+__global__ void __launch_bounds__(KernelShape<Cons, STAGES>::kThreads)
+attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
+              const __grid_constant__ CUtensorMap vmap) {
+    using Sh = KernelShape<Cons, STAGES>;
+    using Elem = typename Cons::ElemT;
+    constexpr int D = Cons::kD, G = Cons::kG, NCW = Cons::kNCW;
+    constexpr int kHalves = D / 64;
+    constexpr int kLoader = NCW, kScheduler = NCW + 1, kEpilogue = NCW + 2;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ctl<STAGES, G> ctl(smem + Sh::kCtlOff);
+    auto merge_mo = [&](int b) { return reinterpret_cast<float*>(smem + Sh::kRingBytes + b * Sh::kMergeBuf); };
+    auto merge_ml = [&](int b) { return merge_mo(b) + NCW * G * D; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&ctl.full[s], 1);
+            mbar_init(&ctl.empty[s], NCW);
+        }
+        for (int s = 0; s < kQueueSlots; ++s) {
+            mbar_init(&ctl.qfull[s], 32);   // every scheduler lane publishes its writes
+            mbar_init(&ctl.qempty[s], 32);  // every loader lane is done reading
+        }
+        for (int s = 0; s < kMergeBufs; ++s) {
+            mbar_init(&ctl.mfull[s], NCW * 32);  // every consumer thread publishes its state
+            mbar_init(&ctl.mempty[s], 32);       // every epilogue lane is done reading
+        }
+        *ctl.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (threadIdx.x == 32 * kLoader && (PAGED || Cons::kSwizzled)) {
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+    pdl_launch_dependents();
+    pdl_wait();
+    __syncthreads();
+
+    if (warp == kScheduler) {
+        // ========================================================== scheduler
+        // Takes units from the work counter, reads their metadata (sequence
+        // length, mask or block table) and queues them for the loader up to
+        // kQueueSlots ahead.  Empty splits never reach the loader: their
+        // -inf log-sum-exps are written here.
+        int slot = 0;
+        uint32_t sphase = 0;
+        bool failed = false;
+        // Work counter: lane 0 issues the atomic; the result is read (and
+        // waited for) only when the next unit is needed.
+        auto grab_issue = [&]() -> int { return lane == 0 ? (int)atomicAdd(&p.sched[0], 1u) : 0; };
+        auto grab_take = [&](int v) -> int { return __shfl_sync(0xffffffffu, v, 0); };
+        auto publish = [&]() {
+            mbar_arrive(&ctl.qfull[slot]);
+            if (++slot == kQueueSlots) {
+                slot = 0;
+                sphase ^= 1u;
+            }
+        };
+        int u = grab_take(grab_issue());
+        while (true) {
+            if (!warp_wait(&ctl.qempty[slot], sphase ^ 1u, ctl.abort_flag)) {
+                failed = true;
+                break;
+            }
+            UnitSlot& sl = ctl.slots[slot];
+            if (u >= p.units) {
+                if (lane == 0) sl.kind = kSlotEnd;
+                __syncwarp();
+                publish();
+                break;
+            }
+            const int next_ticket = grab_issue();  // in flight during this unit's scan
+            const Unit un = decode_unit(p, G, u);
+            const SplitRange r = split_range<PAGED>(
+                p, un.bz, un.split, lane == 0 && un.split == 0 && un.kvh == 0 && un.hg == 0);
+            const int lb0 = producer_scan<PAGED>(p, r, un.bz, lane, sl.words, sl.blocks);
+            int last = -1;
+            for (int i = r.ntiles - 1; i >= 0; --i)
+                if (tile_bits(sl.words, i * p.tile, min(p.tile, r.ntok - i * p.tile))) {
+                    last = i;
+                    break;
+                }
+            if (last >= 0) {
+                if (lane == 0) {
+                    sl.kind = kSlotTiles;
+                    sl.unit = u;
+                    sl.t_begin = r.t_begin;
+                    sl.ntok = r.ntok;
+                    sl.last = last;
+                    sl.lb0 = lb0;
+                }
+                __syncwarp();
+                publish();
+            } else if (p.direct) {
+                // the whole row is empty: zeros and lse = -inf
+                for (int idx = lane; idx < un.g_here * D; idx += 32)
+                    ElemTraits<Elem>::store(p.out, (un.qrow0 + idx / D) * D + idx % D, 0.f);
+                if (lane < un.g_here && p.lse_out) p.lse_out[un.qrow0 + lane] = -INFINITY;
+            } else if (lane < un.g_here) {
+                p.part_lse[(un.qrow0 + lane) * p.S + un.split] = -INFINITY;  // no partial row
+            }
+            u = grab_take(next_ticket);
+        }
+        if (failed && lane == 0 && !*ctl.abort_flag) {
+            *ctl.abort_flag = 1;
+            report(p.dev_status, KVD_DEV_TIMEOUT);
+        }
+        if (lane == 0) {
+            // The CTA that finishes taking units last leaves the scheduling
+            // counters at zero for the next call.
+            __threadfence();
+            if (atomicAdd(&p.sched[1], 1u) == gridDim.x - 1) {
+                atomicExch(&p.sched[0], 0u);
+                atomicExch(&p.sched[1], 0u);
+            }
+        }
+        return;
+    }
+
+    if (warp == kEpilogue) {
+        // =========================================================== epilogue
+        // Turns each finished unit's merge buffer into output or partial rows,
+        // off the consumers' path.
+        int mb = 0;
+        uint32_t eph = 0;
+        while (true) {
+            if (!warp_wait(&ctl.mfull[mb], eph, ctl.abort_flag)) {
+                if (lane == 0 && !*ctl.abort_flag) {
+                    *ctl.abort_flag = 1;
+                    report(p.dev_status, KVD_DEV_TIMEOUT);
+                }
+                break;
+            }
+            const int unit = ctl.mhdr[mb];
+            if (unit < 0) break;
+            const Unit un = decode_unit(p, G, unit);
+            write_rows<Elem, D, G, NCW>(p, merge_mo(mb), merge_ml(mb), un, lane);
+            __syncwarp();
+            mbar_arrive(&ctl.mempty[mb]);  // every lane: done reading the buffer
+            if (++mb == kMergeBufs) {
+                mb = 0;
+                eph ^= 1u;
+            }
+        }
+        return;
+    }
+
+    if (warp == kLoader) {
+        // ============================================================= loader
+        const uint64_t pol = policy_evict_first();
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0, last_parity = 0;  // per stage: issued? parity of the last issue
+        bool failed = false;
+        auto acquire = [&]() -> bool {
+            if (!warp_wait(&ctl.empty[stage], phase ^ 1u, ctl.abort_flag)) failed = true;
+            return !failed;
+        };
+        auto advance = [&]() {
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        };
+        int slot = 0;
+        uint32_t lphase = 0;
+        while (!failed) {
+            if (!warp_wait(&ctl.qfull[slot], lphase, ctl.abort_flag)) {
+                failed = true;
+                break;
+            }
+            const UnitSlot& sl = ctl.slots[slot];
+            if (sl.kind == kSlotEnd) break;
+            const Unit un = decode_unit(p, G, sl.unit);
+            const int t_begin = sl.t_begin, ntok = sl.ntok, last = sl.last, lb0 = sl.lb0;
+            bool first = true;
+            for (int i = 0; i <= last; ++i) {
+                const int r0 = i * p.tile;
+                const int n = min(p.tile, ntok - r0);
+                const uint64_t bits = tile_bits(sl.words, r0, n);
+                if (!bits) continue;  // all-zero tile: never read
+                if (!acquire()) break;
+                if (lane == 0) {
+                    StageMeta& mt = ctl.meta[stage];
+                    mt.unit = sl.unit;
+                    mt.tile = i;
+                    mt.flags = (first ? kFirst : 0u) | (i == last ? kLast : 0u);
+                    mt.bits = bits;
+                    unsigned char* sk = smem + stage * Sh::kStageBytes;
+                    unsigned char* sv = sk + Cons::kTileBytes;
+                    unsigned char* sq = sv + Cons::kTileBytes;
+                    const int t0 = t_begin + r0;
+                    const uint32_t qbytes = first ? (uint32_t)(un.g_here * D * sizeof(Elem)) : 0u;
+                    uint32_t kvbytes;
+                    if constexpr (Cons::kSwizzled) {
+                        kvbytes = 2u * kHalves * p.tile * 128u;  // whole boxes
+                    } else if constexpr (PAGED) {
+                        kvbytes = 2u * p.tile * D * sizeof(Elem);
+                    } else {
+                        kvbytes = 2u * n * D * sizeof(Elem);
+                    }
+                    mbar_arrive_expect_tx(&ctl.full[stage], kvbytes + qbytes);
+                    if constexpr (PAGED) {
+                        const int row = sl.blocks[t0 / p.BS - lb0] * p.BS + t0 % p.BS;
+                        if constexpr (Cons::kSwizzled) {
+#pragma unroll
+                            for (int h = 0; h < kHalves; ++h) {
+                                tma_g2s_3d(sk + h * Cons::kTileBytes / kHalves, &kmap, 64 * h,
+                                           un.kvh, row, &ctl.full[stage], pol);
+                                tma_g2s_3d(sv + h * Cons::kTileBytes / kHalves, &vmap, 64 * h,
+                                           un.kvh, row, &ctl.full[stage], pol);
+                            }
+                        } else {
+                            tma_g2s_3d(sk, &kmap, 0, un.kvh, row, &ctl.full[stage], pol);
+                            tma_g2s_3d(sv, &vmap, 0, un.kvh, row, &ctl.full[stage], pol);
+                        }
+                    } else {
+                        const size_t rowidx = ((size_t)un.bz * p.Hkv + un.kvh) * p.C + t0;
+                        if constexpr (Cons::kSwizzled) {
+#pragma unroll
+                            for (int h = 0; h < kHalves; ++h) {
+                                tma_g2s_2d(sk + h * Cons::kTileBytes / kHalves, &kmap, 64 * h,
+                                           (int)rowidx, &ctl.full[stage], pol);
+                                tma_g2s_2d(sv + h * Cons::kTileBytes / kHalves, &vmap, 64 * h,
+                                           (int)rowidx, &ctl.full[stage], pol);
+                            }
+                        } else {
+                            const uint32_t bytes = (uint32_t)n * D * sizeof(Elem);
+                            bulk_g2s(sk, static_cast<const Elem*>(p.k) + rowidx * D, bytes,
+                                     &ctl.full[stage], pol);
+                            bulk_g2s(sv, static_cast<const Elem*>(p.v) + rowidx * D, bytes,
+                                     &ctl.full[stage], pol);
+                        }
+                    }
+                    if (first)
+                        bulk_g2s(sq, static_cast<const Elem*>(p.q) + un.qrow0 * D, qbytes,
+                                 &ctl.full[stage], pol);
+                    issued_mask |= 1u << stage;
+                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                }
+                __syncwarp();
+                first = false;
+                advance();
+            }
+            if (failed) break;
+            __syncwarp();
+            mbar_arrive(&ctl.qempty[slot]);  // every lane: done with the slot
+            if (++slot == kQueueSlots) {
+                slot = 0;
+                lphase ^= 1u;
+            }
+        }
+        if (!failed && acquire()) {
+            if (lane == 0) {
+                ctl.meta[stage].flags = kEnd;
+                mbar_arrive(&ctl.full[stage]);
+            }
+            __syncwarp();
+        } else {
+            failed = true;
+        }
+        if (failed && lane == 0) {
+            *ctl.abort_flag = 1;
+            report(p.dev_status, KVD_DEV_TIMEOUT);
+            // The consumers may leave early now: never let the CTA exit while a
+            // copy issued here may still be writing the ring.  (On the normal
+            // path the consumers have waited for every issued tile before they
+            // see the end marker.)
+            for (int s = 0; s < STAGES; ++s)
+                if (issued_mask & (1u << s)) {
+                    const volatile int never = 0;
+                    mbar_wait(&ctl.full[s], (last_parity >> s) & 1u, &never);
+                }
+        }
+        return;
+    }
+
+    // ================================================================ consumers
+    Cons cons;
+    int stage = 0;
+    uint32_t phase = 0;
+    int mb = 0;
+    uint32_t mph = 0;
+    // Hand the warp's state of a finished unit (or the end of work, -1) to the
+    // epilogue warp through a merge buffer.
+    auto handoff = [&](int unit) -> bool {
+        if (!warp_wait(&ctl.mempty[mb], mph ^ 1u, ctl.abort_flag)) return false;
+        if (unit >= 0) cons.finish(merge_mo(mb), merge_ml(mb), warp, lane);
+        if (warp == 0 && lane == 0) ctl.mhdr[mb] = unit;
+        mbar_arrive(&ctl.mfull[mb]);  // every consumer thread
+        if (++mb == kMergeBufs) {
+            mb = 0;
+            mph ^= 1u;
+        }
+        return true;
+    };
+    while (true) {
+        if (!warp_wait(&ctl.full[stage], phase, ctl.abort_flag)) {
+            if (lane == 0 && !*ctl.abort_flag) {
+                *ctl.abort_flag = 1;
+                report(p.dev_status, KVD_DEV_TIMEOUT);
+            }
+            break;
+        }
+        const StageMeta mt = ctl.meta[stage];
+        if (mt.flags & kEnd) {
+            handoff(-1);
+            break;
+        }
+        unsigned char* sb = smem + stage * Sh::kStageBytes;
+        if (mt.flags & kFirst) {
+            const Unit un = decode_unit(p, G, mt.unit);
+            cons.begin(reinterpret_cast<const Elem*>(sb + 2 * Cons::kTileBytes), un.g_here,
+                       p.qscale, lane);
+        }
+        const bool wrote = cons.tile(sb, sb + Cons::kTileBytes, mt.bits, warp, lane, p.qscale);
+        // generic-proxy writes to the ring must be ordered before the next TMA
+        // write into this stage
+        if (wrote) fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.empty[stage]);
+        if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+        }
+        if ((mt.flags & kLast) && !handoff(mt.unit)) break;
+    }
+}
+
+}  // namespace kvd

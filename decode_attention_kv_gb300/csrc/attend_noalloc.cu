@@ -12,12 +12,13 @@
 // device, held by every GPU that loads the library until the process exits).
 //
 // The array is shared by every call on a device and keeps whatever the last
-// call left in it.  Nothing in it has to start at zero: each call writes the
-// log-sum-exp of every split it later reads and only reads the partial row of
-// a split whose log-sum-exp is finite, which that same call wrote.  Calls
-// that may run at the same time on the GPU (different streams, or different
-// host threads without ordering) race on the array and must be serialised by
-// the caller.
+// call left in it.  The attention kernel keeps its work counters there; they
+// must be zero when a call starts: the array is zero-initialised when the
+// library is loaded and every call leaves its counters at zero again (the
+// partial rows need no clearing: each call writes the log-sum-exp of every
+// split it reads and reads only partial rows it wrote).  Calls that may run
+// at the same time on the GPU (different streams, or different host threads
+// without ordering) race on the array and must be serialised by the caller.
 #include <cstdio>
 #include <mutex>
 

@@ -8,15 +8,15 @@
 #include <cstring>
 #include <mutex>
 
-#include "attend_split.cuh"
+#include "attend_kernel.cuh"
 #include "kvd_internal.h"
 
 namespace kvd {
 cudaError_t launch_attend_bf16(int D, int G, bool paged, const AttendParams& p,
-                               const CUtensorMap* kmap, const CUtensorMap* vmap, dim3 grid,
+                               const CUtensorMap* kmap, const CUtensorMap* vmap,
                                cudaStream_t stream);
 cudaError_t launch_attend_f32(int D, int G, bool paged, const AttendParams& p,
-                              const CUtensorMap* kmap, const CUtensorMap* vmap, dim3 grid,
+                              const CUtensorMap* kmap, const CUtensorMap* vmap,
                               cudaStream_t stream);
 AttendGeom attend_geom_bf16(int D, int G);
 AttendGeom attend_geom_f32(int D, int G);
@@ -53,19 +53,22 @@ bool dtype_ok(kvd_dtype dt) { return dt == KVD_BF16 || dt == KVD_F32; }
 // ----------------------------------------------------------------- planning
 // Splits of the sequence axis.  The planner is a function of the sizes only
 // (not of the device), so that the workspace size queried ahead of a call
-// equals what the call needs.  It aims at about kTargetCtas CTAs per launch
-// (several waves on 152 SMs at two CTAs per SM), with splits of at least
-// kMinChunk slots so that the partial rows stay a small fraction of the
-// KV traffic.
-constexpr long long kTargetCtas = 2048;
+// equals what the call needs.  It aims at about kTargetUnits (row, split)
+// units per launch -- several per CTA of the persistent grid, so that the
+// unit counter balances rows of different lengths -- with splits of at least
+// kMinChunk slots, so that the partial rows stay a small fraction of the KV
+// traffic.
+constexpr long long kTargetUnits = 2048;
 constexpr int kMinChunk = 128;
 
 struct Plan {
     int G, HG;      // compile-time group width, head groups per kv head
     int tile;       // tokens per ring stage
     int chunk;      // tokens per split
-    int S;          // splits
-    size_t ws;      // workspace bytes (0 when S == 1)
+    int S;          // splits per row
+    long long units;
+    // workspace: scheduling counters (256 bytes) | partial lse | partial rows
+    size_t off_lse, off_po, ws;
 };
 
 int group_width(int g) {
@@ -82,6 +85,8 @@ long long gcd_ll(long long a, long long b) {
     }
     return a;
 }
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 AttendGeom geom(kvd_dtype dt, int D, int G) {
     return dt == KVD_BF16 ? attend_geom_bf16(D, G) : attend_geom_f32(D, G);
@@ -110,12 +115,12 @@ Plan plan_attention(int rows, int Hq, int Hkv, int cap, int D, kvd_dtype dt, int
         if (by_blocks < max_chunk) max_chunk = by_blocks;
     }
     if (max_chunk < unit) max_chunk = unit;
+    const long long row_units = (long long)rows * Hkv * pl.HG;
     long long chunk;
     if (num_splits > 0) {
         chunk = ((long long)cap + num_splits - 1) / num_splits;
     } else {
-        const long long ctas_per_split = (long long)rows * Hkv * pl.HG;
-        chunk = ((long long)cap * ctas_per_split + kTargetCtas - 1) / kTargetCtas;
+        chunk = ((long long)cap * row_units + kTargetUnits - 1) / kTargetUnits;
         if (chunk < kMinChunk) chunk = kMinChunk;
     }
     chunk = (chunk + unit - 1) / unit * unit;
@@ -124,13 +129,38 @@ Plan plan_attention(int rows, int Hq, int Hkv, int cap, int D, kvd_dtype dt, int
     pl.chunk = (int)chunk;
     pl.S = (int)(((long long)cap + chunk - 1) / chunk);
     if (pl.S < 1) pl.S = 1;
+    pl.units = row_units * pl.S;
+    pl.off_lse = 256;
     if (pl.S > 1) {
         const size_t R = (size_t)rows * Hq;
-        const size_t po = R * pl.S * D * sizeof(float);
-        const size_t pls = R * pl.S * sizeof(float);
-        pl.ws = (po + 255) / 256 * 256 + pls;
+        pl.off_po = pl.off_lse + round256(R * pl.S * sizeof(float));
+        pl.ws = pl.off_po + R * pl.S * D * sizeof(float);
+    } else {
+        pl.off_po = pl.ws = pl.off_lse;
     }
     return pl;
+}
+
+// Attaches the workspace regions of a plan to the kernel parameters.
+void attach_workspace(AttendParams& p, const Plan& pl, void* ws) {
+    char* base = static_cast<char*>(ws);
+    p.sched = reinterpret_cast<uint32_t*>(base);
+    p.part_lse = pl.S > 1 ? reinterpret_cast<float*>(base + pl.off_lse) : nullptr;
+    p.part_o = pl.S > 1 ? reinterpret_cast<float*>(base + pl.off_po) : nullptr;
+    p.units = (int)pl.units;
+    p.HG = pl.HG;
+    p.tile = pl.tile;
+    p.chunk = pl.chunk;
+    p.S = pl.S;
+    p.direct = pl.S == 1;
+}
+
+kvd_status check_workspace(const char* fn, const Plan& pl, void* ws, size_t bytes) {
+    if (pl.units >= (1ll << 31)) return fail(KVD_ERR_UNSUPPORTED, "%s: too many (row, split) units", fn);
+    if (!ws) return fail(KVD_ERR_WORKSPACE, "%s: workspace required (%zu bytes)", fn, pl.ws);
+    if (bytes < pl.ws) return fail(KVD_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", fn, bytes, pl.ws);
+    if (!aligned(ws, 256)) return fail(KVD_ERR_INVALID_ARG, "%s: workspace not 256-byte aligned", fn);
+    return KVD_OK;
 }
 
 // ---------------------------------------------------------- tensor maps
@@ -190,10 +220,9 @@ kvd_status make_cache_map(CUtensorMap* map, const void* cache, kvd_dtype dt, boo
 }
 
 cudaError_t launch_attend(kvd_dtype dt, int D, int G, bool paged, const AttendParams& p,
-                          const CUtensorMap* kmap, const CUtensorMap* vmap, dim3 grid,
-                          cudaStream_t s) {
-    return dt == KVD_BF16 ? launch_attend_bf16(D, G, paged, p, kmap, vmap, grid, s)
-                          : launch_attend_f32(D, G, paged, p, kmap, vmap, grid, s);
+                          const CUtensorMap* kmap, const CUtensorMap* vmap, cudaStream_t s) {
+    return dt == KVD_BF16 ? launch_attend_bf16(D, G, paged, p, kmap, vmap, s)
+                          : launch_attend_f32(D, G, paged, p, kmap, vmap, s);
 }
 
 kvd_status check_attention_shape(int Hq, int Hkv, int D, kvd_dtype dt) {
@@ -272,16 +301,10 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         !aligned(lse_out, 4) || !aligned(dev_status, 4))
         return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked: misaligned pointer");
-    if (B > 65535) return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_masked: B > 65535");
     if (num_splits < 0) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked: num_splits < 0");
     const Plan pl = plan_attention(B, Hq, Hkv, C, D, dtype, 0, num_splits);
-    if ((long long)Hkv * pl.HG > 65535) return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_masked: too many heads");
-    if (pl.S > 1) {
-        if (!workspace) return fail(KVD_ERR_WORKSPACE, "kvd_attend_masked: workspace required (%zu bytes)", pl.ws);
-        if (workspace_bytes < pl.ws)
-            return fail(KVD_ERR_WORKSPACE, "kvd_attend_masked: workspace %zu < %zu bytes", workspace_bytes, pl.ws);
-        if (!aligned(workspace, 256)) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked: workspace not 256-byte aligned");
-    }
+    st = check_workspace("kvd_attend_masked", pl, workspace, workspace_bytes);
+    if (st != KVD_OK) return st;
     AttendParams p{};
     p.q = q;
     p.k = k_cache;
@@ -289,23 +312,14 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
     p.mask = mask;
     p.out = out;
     p.lse_out = lse_out;
-    const size_t R = (size_t)B * Hq;
-    p.part_o = static_cast<float*>(workspace);
-    p.part_lse = pl.S > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                                     (R * pl.S * D * sizeof(float) + 255) / 256 * 256)
-                          : nullptr;
     p.dev_status = dev_status;
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.g = Hq / Hkv;
-    p.HG = pl.HG;
     p.C = C;
-    p.tile = pl.tile;
-    p.chunk = pl.chunk;
-    p.S = pl.S;
     p.mask_vec = (C % 16 == 0) && aligned(mask, 16);
     p.qscale = scale * kLog2e;
-    p.direct = pl.S == 1;
+    attach_workspace(p, pl, workspace);
     CUtensorMap kmap, vmap;
     std::memset(&kmap, 0, sizeof kmap);
     std::memset(&vmap, 0, sizeof vmap);
@@ -318,11 +332,11 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
         st = make_cache_map(&vmap, v_cache, dtype, false, rows, Hkv, D, pl.tile, true);
         if (st != KVD_OK) return st;
     }
-    const dim3 grid(pl.S, Hkv * pl.HG, B);
-    cudaError_t e = launch_attend(dtype, D, pl.G, false, p, &kmap, &vmap, grid, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked split launch");
+    cudaError_t e = launch_attend(dtype, D, pl.G, false, p, &kmap, &vmap, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked launch");
     if (pl.S > 1) {
-        e = launch_combine(p.part_o, p.part_lse, out, lse_out, (int)R, pl.S, D, dtype, (cudaStream_t)stream);
+        e = launch_combine(p.part_o, p.part_lse, out, lse_out, B * Hq, pl.S, D, dtype,
+                           (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked combine launch");
     }
     return ok();
@@ -353,16 +367,10 @@ kvd_status kvd_attend_paged(const void* q_in, const void* key_cache, const void*
         return fail(KVD_ERR_INVALID_ARG, "kvd_attend_paged: misaligned pointer");
     if ((long long)NB * BS >= (1ll << 31)) return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_paged: NB*BS >= 2^31");
     if ((long long)cols * BS >= (1ll << 31)) return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_paged: cols*BS >= 2^31");
-    if (Q > 65535) return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_paged: Q > 65535");
     if (num_splits < 0) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_paged: num_splits < 0");
     const Plan pl = plan_attention(Q, Hq, Hkv, cols * BS, D, dtype, BS, num_splits);
-    if ((long long)Hkv * pl.HG > 65535) return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_paged: too many heads");
-    if (pl.S > 1) {
-        if (!workspace) return fail(KVD_ERR_WORKSPACE, "kvd_attend_paged: workspace required (%zu bytes)", pl.ws);
-        if (workspace_bytes < pl.ws)
-            return fail(KVD_ERR_WORKSPACE, "kvd_attend_paged: workspace %zu < %zu bytes", workspace_bytes, pl.ws);
-        if (!aligned(workspace, 256)) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_paged: workspace not 256-byte aligned");
-    }
+    st = check_workspace("kvd_attend_paged", pl, workspace, workspace_bytes);
+    if (st != KVD_OK) return st;
     CUtensorMap kmap, vmap;
     const bool mma = attend_uses_mma(dtype, pl.G);
     st = make_cache_map(&kmap, key_cache, dtype, true, (long long)NB * BS, Hkv, D, pl.tile, mma);
@@ -376,29 +384,20 @@ kvd_status kvd_attend_paged(const void* q_in, const void* key_cache, const void*
     p.seq_offset = seq_offset;
     p.out = out;
     p.lse_out = lse_out;
-    const size_t R = (size_t)Q * Hq;
-    p.part_o = static_cast<float*>(workspace);
-    p.part_lse = pl.S > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                                     (R * pl.S * D * sizeof(float) + 255) / 256 * 256)
-                          : nullptr;
     p.dev_status = dev_status;
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.g = Hq / Hkv;
-    p.HG = pl.HG;
     p.BS = BS;
     p.cols = cols;
     p.NB = NB;
-    p.tile = pl.tile;
-    p.chunk = pl.chunk;
-    p.S = pl.S;
     p.qscale = scale * kLog2e;
-    p.direct = pl.S == 1;
-    const dim3 grid(pl.S, Hkv * pl.HG, Q);
-    cudaError_t e = launch_attend(dtype, D, pl.G, true, p, &kmap, &vmap, grid, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_paged split launch");
+    attach_workspace(p, pl, workspace);
+    cudaError_t e = launch_attend(dtype, D, pl.G, true, p, &kmap, &vmap, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_paged launch");
     if (pl.S > 1) {
-        e = launch_combine(p.part_o, p.part_lse, out, lse_out, (int)R, pl.S, D, dtype, (cudaStream_t)stream);
+        e = launch_combine(p.part_o, p.part_lse, out, lse_out, Q * Hq, pl.S, D, dtype,
+                           (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_paged combine launch");
     }
     return ok();

@@ -137,14 +137,21 @@ def attend_masked_workspace_bytes(B, Hq, Hkv, C, D, dtype=torch.bfloat16, num_sp
                                                     num_splits)
 
 
-def _workspace(nbytes, device, workspace):
+def workspace(nbytes, device=None):
+    """A workspace for the attention calls: zero-filled, as the kernels
+    require before first use (each call leaves it zeroed again)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def _workspace(nbytes, device, ws):
     if nbytes == 0:
         return None, 0
-    if workspace is None:
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
-    if workspace.numel() * workspace.element_size() < nbytes:
+    if ws is None:
+        ws = workspace(nbytes, device)
+    have = ws.numel() * ws.element_size()
+    if have < nbytes:
         raise ValueError(f"workspace smaller than {nbytes} bytes")
-    return workspace, workspace.numel() * workspace.element_size()
+    return ws, have
 
 
 def attend_masked(q, k_cache, v_cache, mask, scale=None, out=None, lse=None, num_splits=0,

@@ -106,12 +106,17 @@ kvd_status kvd_append(void* k_cache, void* v_cache, const void* k_new, const voi
  *   out       [B, Hq, D] of `dtype` (fp32 result rounded to nearest even)
  *   lse_out   [B, Hq] float or NULL
  * A row with no valid slot gives out = 0 and lse = -inf.
- * The sequence axis is split across CTAs (num_splits; 0 = planned by the
- * library from the sizes); each split keeps an fp32 running max / sum /
- * output, and splits are merged by log-sum-exp (kvd_combine).  When more
- * than one split is used the call needs `workspace` of at least
- * kvd_attend_masked_workspace_bytes(...) bytes (any contents, 256-byte
- * aligned); with one split it may be NULL.
+ * The sequence axis of every (batch entry, kv head) row is cut into splits
+ * (num_splits; 0 = planned by the library from the sizes) that a persistent
+ * grid takes from a work counter; each split keeps an fp32 running max / sum
+ * / output.  With more than one split a second kernel merges the splits by
+ * log-sum-exp (the kvd_combine formula).
+ * Workspace: at least kvd_attend_masked_workspace_bytes(...) bytes (never
+ * less than 256), 256-byte aligned, holding the work counters and the
+ * partial rows.  Zero-fill it once before its first use; every call leaves
+ * its counters at zero again, so calls ordered on one stream can reuse it
+ * (calls that may overlap on the GPU must not share one).  After a call that
+ * reported KVD_DEV_TIMEOUT, zero it again.
  * Supported: D in {64, 128}; dtype bf16 or f32; any Hq multiple of Hkv.
  */
 size_t kvd_attend_masked_workspace_bytes(int B, int Hq, int Hkv, int C, int D, kvd_dtype dtype,
@@ -136,7 +141,8 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
  * Device-detected errors (KVD_DEV_SEQLENS, SEQ_OFFSET, TABLE_COLS) make the
  * sequence empty (out = 0, lse = -inf); an out-of-range block id
  * (KVD_DEV_BLOCK_RANGE) drops that block's tokens.  A sequence of length 0
- * gives out = 0, lse = -inf.  Workspace as for kvd_attend_masked.
+ * gives out = 0, lse = -inf.  One launch and a workspace as for
+ * kvd_attend_masked (zero-filled before first use, left zeroed by each call).
  * Supported: D in {64, 128}; bf16 or f32; BS*Hkv*D*elem addressable by a
  * TMA tensor map (NB*BS < 2^31).
  */
@@ -161,9 +167,10 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
  *    current device (cudaGetSymbolAddress) and caches it; make that first
  *    call before any stream capture on that device.
  *  - All calls on a device share the one array, which keeps the last call's
- *    contents (nothing in it needs to start at zero).  Calls that may overlap
- *    on the GPU (other streams, unordered host threads) race on it: the
- *    caller must order them.
+ *    contents.  Its work counters start at zero (the array is zero when the
+ *    library is loaded) and every call leaves them at zero again.  Calls that
+ *    may overlap on the GPU (other streams, unordered host threads) race on
+ *    it: the caller must order them.
  */
 #define KVD_NOALLOC_SCRATCH_BYTES (8u << 20)
 kvd_status kvd_attend_masked_noalloc(const void* q, const void* k_cache, const void* v_cache,

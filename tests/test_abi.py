@@ -52,7 +52,8 @@ def test_masked_host_validation(lib):
     assert _masked(lib, q=None) == 1                 # null pointer
     assert _masked(lib, B=0, q=None) == 0            # empty batch: nothing to do
     assert _masked(lib, C=0) == 1
-    assert _masked(lib, C=4096, ns=4) == 3           # splits need a workspace
+    assert _masked(lib, C=4096, ns=4) == 3           # the call needs a workspace
+    assert _masked(lib, C=64, ns=1) == 3             # even with one split (work counters)
     need = lib.kvd_attend_masked_workspace_bytes(2, 8, 2, 4096, 128, 0, 4)
     assert need > 0
     assert _masked(lib, C=4096, ns=4, ws=1, wsb=need - 1) == 3
@@ -73,13 +74,15 @@ def test_workspace_sizes_follow_the_plan(lib):
     R = 16 * 32
     S = None
     for s in range(1, 65):
-        po = (R * s * 128 * 4 + 255) // 256 * 256
-        if po + R * s * 4 == ws:
+        lse = (R * s * 4 + 255) // 256 * 256
+        if 256 + lse + R * s * 128 * 4 == ws:
             S = s
     assert S is not None and S > 1
-    assert lib.kvd_attend_masked_workspace_bytes(1, 4, 4, 32, 64, 1, 0) == 0  # tiny: one split
+    # one split: only the 256-byte block of scheduling counters
+    assert lib.kvd_attend_masked_workspace_bytes(1, 4, 4, 32, 64, 1, 0) == 256
+    # counters | 32 x 16 partial lse | 32 x 16 x 128 partial rows
     assert lib.kvd_attend_masked_workspace_bytes(1, 32, 32, 32768, 128, 0, 16) == \
-        (32 * 16 * 128 * 4 + 255) // 256 * 256 + 32 * 16 * 4
+        256 + 32 * 16 * 4 + 32 * 16 * 128 * 4
     assert lib.kvd_attend_paged_workspace_bytes(64, 32, 8, 128, 32, 128, 0, 0) > 0
     assert lib.kvd_attend_masked_workspace_bytes(1, 4, 3, 32, 64, 0, 0) == 0  # invalid -> 0
 
