@@ -10,80 +10,106 @@
 
 namespace kvd {
 
-// Ring depth that keeps a CTA near `budget` bytes of stages (2..8 stages).
-constexpr int stages_for(int stage_bytes, int budget) {
-    return budget / stage_bytes < 2 ? 2 : (budget / stage_bytes > 8 ? 8 : budget / stage_bytes);
+// Both configurations aim at two CTAs per SM (the SM's 228 KB shared memory,
+// less 1 KB reserved per CTA): the other CTA's consumer warps issue while one
+// CTA's warps wait on their own mma, shuffle or load latencies.  The ring
+// takes what the merge buffers and the control block leave of that share
+// (2..8 stages): the bytes in flight per SM are what hides HBM latency.
+constexpr int kCtaSmemTarget = 113 * 1024;
+
+template <class Cons, int MB>
+constexpr int ring_stages() {
+    using Sh = KernelShape<Cons, 2, MB>;
+    // the control block grows by about 40 bytes per stage: budget 8 stages
+    constexpr int fixed = Sh::kSmemAlloc - Sh::kRingBytes + 6 * 40;
+    constexpr int n = (kCtaSmemTarget - fixed) / Sh::kStageBytes;
+    return n < 2 ? 2 : (n > 8 ? 8 : n);
 }
 
-// CUDA-core consumers: 32-token tiles, four consumer warps, about 100 KB of
-// ring so that two CTAs share an SM.
+// CUDA-core consumers: 32-token tiles, four consumer warps, two merge buffers.
 template <typename Elem, int D, int G>
 struct SimtCfg {
     using Cons = SimtConsumer<Elem, D, G, 32, 4>;
-    static constexpr int STAGES = stages_for(KernelShape<Cons, 2>::kStageBytes, 100 * 1024);
+    static constexpr int MB = 2;
+    static constexpr int STAGES = ring_stages<Cons, MB>();
 };
 
 // Tensor-core consumers: 64-token tiles (one 16-token slab per consumer
-// warp), a ring of about 170 KB, one CTA per SM.
+// warp); one merge buffer (a unit spans several tiles, the epilogue empties
+// the buffer well within one), so that a third stage fits.
 template <int D, int G>
 struct MmaCfg {
     using Cons = MmaConsumer<D, G, 64, 4>;
-    static constexpr int STAGES = stages_for(KernelShape<Cons, 2>::kStageBytes, 160 * 1024);
+    static constexpr int MB = 1;
+    static constexpr int STAGES = ring_stages<Cons, MB>();
 };
+
+// Lookahead of the schedulers, per SM: about 5 us of one SM's share of HBM
+// bandwidth (~45 KB per us).
+constexpr int kLookBytesPerSm = 224 * 1024;
 
 // Per-device launch facts of one kernel instantiation: the shared-memory
 // attribute is set and the persistent grid sized once per device.
 struct DeviceFacts {
     std::mutex mu;
-    int ctas[64] = {};  // persistent CTAs per device (0 = not set up yet)
+    int ctas[64] = {};    // persistent CTAs per device (0 = not set up yet)
+    int per_sm[64] = {};  // of them resident on one SM
 };
 
-template <class Cons, int STAGES, bool PAGED>
+template <class Cons, int STAGES, int MB, bool PAGED>
 cudaError_t launch_kernel(const AttendParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
                           cudaStream_t stream) {
-    using Sh = KernelShape<Cons, STAGES>;
-    auto kern = attend_kernel<Cons, STAGES, PAGED>;
+    using Sh = KernelShape<Cons, STAGES, MB>;
+    static_assert(Sh::kSmemAlloc <= 227 * 1024, "shared memory of one CTA");
+    auto kern = attend_kernel<Cons, STAGES, MB, PAGED>;
     constexpr int kThreads = Sh::kThreads;
     static DeviceFacts facts;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    int ctas;
+    int ctas, per_sm;
     {
         std::lock_guard<std::mutex> lock(facts.mu);
         if (!facts.ctas[dev]) {
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      Sh::kSmemAlloc);
             if (e != cudaSuccess) return e;
-            int per_sm = 0, nsm = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads,
+            int resident = 0, nsm = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kern, kThreads,
                                                               Sh::kSmemAlloc);
             if (e != cudaSuccess) return e;
             e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return e;
-            facts.ctas[dev] = (per_sm < 1 ? 1 : per_sm) * (nsm < 1 ? 1 : nsm);
+            facts.per_sm[dev] = resident < 1 ? 1 : resident;
+            facts.ctas[dev] = facts.per_sm[dev] * (nsm < 1 ? 1 : nsm);
         }
         ctas = facts.ctas[dev];
+        per_sm = facts.per_sm[dev];
     }
+    // The SM's lookahead split between the CTAs that share it, at least two tiles.
+    AttendParams q = p;
+    const int bytes_per_token = 2 * Cons::kD * (int)sizeof(typename Cons::ElemT);
+    q.look = (kLookBytesPerSm / per_sm) / bytes_per_token;
+    if (q.look < 2 * p.tile) q.look = 2 * p.tile;
     const int grid = p.units < ctas ? p.units : ctas;
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), Sh::kSmemAlloc, stream, p, *kmap, *vmap);
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), Sh::kSmemAlloc, stream, q, *kmap, *vmap);
 }
 
 template <typename Elem, int D, int G>
 cudaError_t launch_simt(bool paged, const AttendParams& p, const CUtensorMap* kmap,
                         const CUtensorMap* vmap, cudaStream_t stream) {
     using C = SimtCfg<Elem, D, G>;
-    return paged ? launch_kernel<typename C::Cons, C::STAGES, true>(p, kmap, vmap, stream)
-                 : launch_kernel<typename C::Cons, C::STAGES, false>(p, kmap, vmap, stream);
+    return paged ? launch_kernel<typename C::Cons, C::STAGES, C::MB, true>(p, kmap, vmap, stream)
+                 : launch_kernel<typename C::Cons, C::STAGES, C::MB, false>(p, kmap, vmap, stream);
 }
 
 template <int D, int G>
 cudaError_t launch_mma(bool paged, const AttendParams& p, const CUtensorMap* kmap,
                        const CUtensorMap* vmap, cudaStream_t stream) {
     using C = MmaCfg<D, G>;
-    return paged ? launch_kernel<typename C::Cons, C::STAGES, true>(p, kmap, vmap, stream)
-                 : launch_kernel<typename C::Cons, C::STAGES, false>(p, kmap, vmap, stream);
+    return paged ? launch_kernel<typename C::Cons, C::STAGES, C::MB, true>(p, kmap, vmap, stream)
+                 : launch_kernel<typename C::Cons, C::STAGES, C::MB, false>(p, kmap, vmap, stream);
 }
 
 }  // namespace kvd

@@ -16,16 +16,20 @@
 //
 // Work.  A unit is one (row, split): row = (batch entry or sequence, kv head,
 // group of <= G query heads sharing it), split = a chunk of `chunk` token
-// slots of that row.  Units are numbered row-major (splits of one row are
-// consecutive) and handed out by a global counter, so the grid is persistent
-// (about one or two CTAs per SM) and load-balances rows of any length.
+// slots of that row.  Units are numbered split-major and handed out by a
+// global counter, so the grid is persistent (about one or two CTAs per SM)
+// and load-balances rows of any length.
 //
 // CTA.  Four roles in warps:
-//  * scheduler (warp NCW+1): takes units from the work counter, reads their
-//    metadata (sequence length and block-table entries, or the split's mask)
-//    into 32-token validity words, and queues them for the loader up to four
-//    units ahead; a split without a valid token never reaches the loader --
-//    its log-sum-exps are set to -inf (or, single split, its rows to zero).
+//  * schedulers (warps NCW+1, NCW+2): each takes units from the work counter,
+//    reads their metadata (sequence length and block-table entries, or the
+//    split's mask) into 32-token validity words and queues them for the
+//    loader in a ring of its own.  A scheduler takes a unit only while the
+//    CTA has fewer than `look` tokens of queued, not yet requested tiles
+//    (about 5 us of work), so that units stay with the counter until some
+//    CTA is ready for them.  A
+//    split without a valid token never reaches the loader: its log-sum-exps
+//    are set to -inf (or, single split, its rows to zero).
 //  * loader (warp NCW): skips tiles with no valid token and streams the others
 //    into a STAGES-deep ring with 1-D bulk copies (static buffer, CUDA-core
 //    consumers) or 2-D/3-D TMA tensor copies (paged, or 128-byte-swizzled
@@ -36,15 +40,17 @@
 //  * consumers (warps 0..NCW-1, attend_consumers.cuh): the online softmax over
 //    the tiles; at a unit's last tile they drop their states into one of two
 //    merge buffers and go on with the next unit.
-//  * epilogue (warp NCW+2): merges the consumer warps' states of a unit and
+//  * epilogue (warp NCW+3): merges the consumer warps' states of a unit and
 //    writes either the final rows (single split) or a normalised partial row
 //    and its log-sum-exp.
 // With more than one split the host launches the log-sum-exp combine kernel
 // right behind this one (programmatic dependent launch): it runs once the
 // partial rows are complete, without atomics or fences here.
 //
-// Counters (unit counter, CTAs-done counter) live in the caller's workspace:
-// zero before the first call; the last CTA to finish taking units resets them.
+// Counters (unit counter, schedulers-done counter) live in the caller's
+// workspace: zero before the first call; the last scheduler warp to finish
+// taking units resets them.  The first unit of each scheduler warp is
+// blockIdx.x * 2 + warp (no atomic); the counter hands out the rest.
 // All waits are bounded; a wait that runs out sets KVD_DEV_TIMEOUT, after
 // which the counters must be zeroed again.
 #pragma once
@@ -69,18 +75,21 @@ struct AttendParams {
     float* lse_out;              // [rows, Hq] or null
     float* part_o;               // [rows * Hq, S, D]       (S > 1)
     float* part_lse;             // [rows * Hq, S]          (S > 1)
-    uint32_t* sched;             // [0] next unit, [1] CTAs done
+    uint32_t* sched;             // [0] units taken beyond the first ones, [1] schedulers done
     int32_t* dev_status;
     int Hq, Hkv, g, HG;          // g = Hq / Hkv, HG = head groups per kv head
     int C;                       // static buffer capacity
     int BS, cols, NB;            // paged geometry
     int tile;                    // tokens per ring stage (paged: divides BS)
-    int chunk;                   // tokens per split (multiple of tile and of 32)
+    int chunk;                   // tokens per split [0, Sb) (multiple of tile and of 32)
+    int chunk2;                  // tokens per split [Sb, S) (multiple of tile and of 32)
+    int Sb;
     int S;                       // splits per row
     int units;                   // rows * Hkv * HG * S
     int mask_vec;                // mask rows 16-byte aligned (C % 16 == 0)
     float qscale;                // scale * log2(e)
     int direct;                  // S == 1: units write the output rows directly
+    int look;                    // a scheduler takes a unit only below this many queued tokens
 };
 
 enum : uint32_t { kFirst = 1u, kLast = 2u, kCombine = 4u, kEnd = 8u };
@@ -94,6 +103,9 @@ struct StageMeta {
 };
 
 // One unit: its split, its row (counter index) and the query rows it serves.
+// Units are numbered split-major (all rows' split 0, then split 1, ...): the
+// last units handed out are the late splits, which are short or empty when
+// lengths vary, so the CTAs finish close together.
 struct Unit {
     int split, ru, bz, kvh, hg, g_here;
     size_t qrow0;
@@ -101,8 +113,9 @@ struct Unit {
 
 __device__ __forceinline__ Unit decode_unit(const AttendParams& p, int G, int u) {
     Unit un;
-    un.split = u % p.S;
-    un.ru = u / p.S;
+    const int rows = p.units / p.S;
+    un.split = u / rows;
+    un.ru = u % rows;
     const int per_bz = p.Hkv * p.HG;
     un.bz = un.ru / per_bz;
     const int rem = un.ru % per_bz;
@@ -115,7 +128,9 @@ __device__ __forceinline__ Unit decode_unit(const AttendParams& p, int G, int u)
 
 // A unit prepared by the scheduler warp for the loader warp.
 enum : int { kSlotTiles = 0, kSlotCombine = 1, kSlotEnd = 2 };
-constexpr int kQueueSlots = 4;
+constexpr int kSchedWarps = 2;                         // scheduler warps per CTA
+constexpr int kRingSlots = 2;                          // queued units per scheduler
+constexpr int kQueueSlots = kSchedWarps * kRingSlots;  // scheduler s owns slots [2s, 2s + 2)
 
 struct UnitSlot {
     int kind;    // kSlotTiles: stream the unit's tiles; kSlotCombine: only merge its row
@@ -128,24 +143,23 @@ struct UnitSlot {
     int blocks[kMaxBlocks];     // physical block of each logical block (paged; -1 = dropped)
 };
 
-constexpr int kMergeBufs = 2;
-
 // Shared-memory control block:
 // full[STAGES] | empty[STAGES] | qfull[Q] | qempty[Q] | mfull[M] | mempty[M] | meta[STAGES] |
-// abort | mhdr[M] | slots[Q]
-template <int STAGES, int G>
+// abort | pending | mhdr[M] | slots[Q]
+template <int STAGES, int MB>
 struct CtlLayout {
     static constexpr int kBar = 0;
     static constexpr int kQBar = kBar + 2 * STAGES * 8;
     static constexpr int kMBar = kQBar + 2 * kQueueSlots * 8;
-    static constexpr int kMeta = kMBar + 2 * kMergeBufs * 8;
+    static constexpr int kMeta = kMBar + 2 * MB * 8;
     static constexpr int kAbort = kMeta + STAGES * (int)sizeof(StageMeta);
-    static constexpr int kMhdr = kAbort + 4;
-    static constexpr int kSlots = (kMhdr + 4 * kMergeBufs + 15) / 16 * 16;
+    static constexpr int kPending = kAbort + 4;
+    static constexpr int kMhdr = kPending + 4;
+    static constexpr int kSlots = (kMhdr + 4 * MB + 15) / 16 * 16;
     static constexpr int kBytes = kSlots + kQueueSlots * (int)sizeof(UnitSlot);
 };
 
-template <int STAGES, int G>
+template <int STAGES, int MB>
 struct Ctl {
     uint64_t* full;     // ring stage landed (loader -> consumers)
     uint64_t* empty;    // ring stage consumed (consumers -> loader)
@@ -155,24 +169,27 @@ struct Ctl {
     uint64_t* mempty;   // merge buffer read (epilogue -> consumers)
     StageMeta* meta;
     volatile int* abort_flag;
+    int* pending;       // tokens of queued tiles the loader has not requested yet
     int* mhdr;          // unit of each merge buffer (-1: end of work)
     UnitSlot* slots;
     __device__ explicit Ctl(unsigned char* base) {
-        using L = CtlLayout<STAGES, G>;
+        using L = CtlLayout<STAGES, MB>;
         full = reinterpret_cast<uint64_t*>(base + L::kBar);
         empty = full + STAGES;
         qfull = reinterpret_cast<uint64_t*>(base + L::kQBar);
         qempty = qfull + kQueueSlots;
         mfull = reinterpret_cast<uint64_t*>(base + L::kMBar);
-        mempty = mfull + kMergeBufs;
+        mempty = mfull + MB;
         meta = reinterpret_cast<StageMeta*>(base + L::kMeta);
         abort_flag = reinterpret_cast<volatile int*>(base + L::kAbort);
+        pending = reinterpret_cast<int*>(base + L::kPending);
         mhdr = reinterpret_cast<int*>(base + L::kMhdr);
         slots = reinterpret_cast<UnitSlot*>(base + L::kSlots);
     }
 };
 
-template <class Cons, int STAGES>
+// STAGES ring stages, MB merge buffers (consumers -> epilogue).
+template <class Cons, int STAGES, int MB>
 struct KernelShape {
     using Elem = typename Cons::ElemT;
     static constexpr int kQBytes = Cons::kG * Cons::kD * (int)sizeof(Elem);
@@ -180,9 +197,10 @@ struct KernelShape {
     static constexpr int kRingBytes = STAGES * kStageBytes;
     // one merge buffer: mo [NCW][G][D] then ml [NCW][G][2]
     static constexpr int kMergeBuf = (Cons::kNCW * Cons::kG * (Cons::kD + 2) * 4 + 127) / 128 * 128;
-    static constexpr int kCtlOff = kRingBytes + kMergeBufs * kMergeBuf;
-    static constexpr int kSmemAlloc = kCtlOff + CtlLayout<STAGES, Cons::kG>::kBytes + 1024;
-    static constexpr int kThreads = (Cons::kNCW + 3) * 32;  // consumers, loader, scheduler, epilogue
+    static constexpr int kCtlOff = kRingBytes + MB * kMergeBuf;
+    static constexpr int kSmemAlloc = kCtlOff + CtlLayout<STAGES, MB>::kBytes + 1024;
+    // consumers, loader, schedulers, epilogue
+    static constexpr int kThreads = (Cons::kNCW + 2 + kSchedWarps) * 32;
     static_assert(Cons::kTileBytes % 1024 == 0, "tiles keep stage parts 1024-byte aligned");
 };
 
@@ -197,7 +215,9 @@ template <bool PAGED>
 __device__ __forceinline__ SplitRange split_range(const AttendParams& p, int bz, int split,
                                                   bool reporter) {
     SplitRange r;
-    r.t_begin = split * p.chunk;
+    const bool big = split < p.Sb;
+    r.t_begin = big ? split * p.chunk : p.Sb * p.chunk + (split - p.Sb) * p.chunk2;
+    const int span = big ? p.chunk : p.chunk2;
     r.first_col = 0;
     if constexpr (PAGED) {
         const int s0 = p.seq_lens[bz], s1 = p.seq_lens[bz + 1];
@@ -220,9 +240,9 @@ __device__ __forceinline__ SplitRange split_range(const AttendParams& p, int bz,
             }
         }
         if (bad && reporter) report(p.dev_status, bad);
-        r.t_end = min(len, r.t_begin + p.chunk);
+        r.t_end = min(len, r.t_begin + span);
     } else {
-        r.t_end = min(p.C, r.t_begin + p.chunk);
+        r.t_end = min(p.C, r.t_begin + span);
     }
     r.ntok = max(0, r.t_end - r.t_begin);
     r.ntiles = (r.ntok + p.tile - 1) / p.tile;
@@ -276,11 +296,22 @@ __device__ __forceinline__ int producer_scan(const AttendParams& p, const SplitR
             }
             __syncwarp();
         }
-        for (int j = 0; j < nwords; ++j) {
-            const int tok = r.t_begin + 32 * j + lane;
-            const bool ok = tok < r.t_end && blocks[tok / p.BS - lb0] >= 0;
-            const uint32_t w = __ballot_sync(0xffffffffu, ok);
-            if (lane == 0) words[j] = w;
+        if (p.BS % 32 == 0) {
+            // t_begin is a multiple of 32, so each word lies in one block: a
+            // lane builds a whole word.
+            for (int j = lane; j < nwords; j += 32) {
+                const int tok0 = r.t_begin + 32 * j;
+                const int n = min(max(r.t_end - tok0, 0), 32);
+                const bool ok = n > 0 && blocks[tok0 / p.BS - lb0] >= 0;
+                words[j] = !ok ? 0u : (n == 32 ? 0xffffffffu : ((1u << n) - 1u));
+            }
+        } else {
+            for (int j = 0; j < nwords; ++j) {
+                const int tok = r.t_begin + 32 * j + lane;
+                const bool ok = tok < r.t_end && blocks[tok / p.BS - lb0] >= 0;
+                const uint32_t w = __ballot_sync(0xffffffffu, ok);
+                if (lane == 0) words[j] = w;
+            }
         }
     } else {
         const uint8_t* mrow = p.mask + (size_t)bz * p.C;
@@ -330,30 +361,45 @@ __device__ __forceinline__ int producer_scan(const AttendParams& p, const SplitR
 // One warp turns the consumer warps' states of a unit (mo[w][h][d] and
 // ml[w][h] = (m, l) in a merge buffer) into the unit's rows: the final output
 // (single split) or a normalised partial row and its natural-log log-sum-exp.
+// A lane handles four consecutive dims of one head (D % 4 == 0; rows of out
+// and part_o are 16-byte aligned).
 template <typename Elem, int D, int G, int NCW>
 __device__ __forceinline__ void write_rows(const AttendParams& p, const float* mo,
                                            const float* ml, const Unit& un, int lane) {
-    for (int idx = lane; idx < un.g_here * D; idx += 32) {
-        const int hh = idx / D, d = idx % D;
+    constexpr int V = D / 4;
+    static_assert(D % 4 == 0, "head_dim must be a multiple of 4");
+    for (int idx = lane; idx < un.g_here * V; idx += 32) {
+        const int hh = idx / V, d4 = idx % V;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < NCW; ++w) M = fmaxf(M, ml[(w * G + hh) * 2]);
         const float base = (M == -INFINITY) ? 0.f : M;
-        float L = 0.f, O = 0.f;
+        float L = 0.f;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < NCW; ++w) {
             const float sc = fast_exp2(ml[(w * G + hh) * 2] - base);
             L = fmaf(ml[(w * G + hh) * 2 + 1], sc, L);
-            O = fmaf(mo[(w * G + hh) * D + d], sc, O);
+            const float4 x = reinterpret_cast<const float4*>(mo + (w * G + hh) * D)[d4];
+            O.x = fmaf(x.x, sc, O.x);
+            O.y = fmaf(x.y, sc, O.y);
+            O.z = fmaf(x.z, sc, O.z);
+            O.w = fmaf(x.w, sc, O.w);
         }
         const size_t row = un.qrow0 + hh;
         const float lse = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        O.x *= inv;
+        O.y *= inv;
+        O.z *= inv;
+        O.w *= inv;
         if (p.direct) {
-            ElemTraits<Elem>::store(p.out, row * D + d, L > 0.f ? O / L : 0.f);
-            if (d == 0 && p.lse_out) p.lse_out[row] = lse;
+            ElemTraits<Elem>::store4(p.out, row * D + 4 * d4, O);
+            if (d4 == 0 && p.lse_out) p.lse_out[row] = lse;
         } else {
-            if (L > 0.f) p.part_o[(row * p.S + un.split) * D + d] = O / L;
-            if (d == 0) p.part_lse[row * p.S + un.split] = lse;
+            if (L > 0.f)
+                *reinterpret_cast<float4*>(p.part_o + (row * p.S + un.split) * D + 4 * d4) = O;
+            if (d4 == 0) p.part_lse[row * p.S + un.split] = lse;
         }
     }
 }
@@ -367,19 +413,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
 }
 
 
-template <class Cons, int STAGES, bool PAGED>
-__global__ void __launch_bounds__(KernelShape<Cons, STAGES>::kThreads)
+template <class Cons, int STAGES, int MB, bool PAGED>
+__global__ void __launch_bounds__(KernelShape<Cons, STAGES, MB>::kThreads)
 attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
               const __grid_constant__ CUtensorMap vmap) {
-    using Sh = KernelShape<Cons, STAGES>;
+    using Sh = KernelShape<Cons, STAGES, MB>;
     using Elem = typename Cons::ElemT;
     constexpr int D = Cons::kD, G = Cons::kG, NCW = Cons::kNCW;
     constexpr int kHalves = D / 64;
-    constexpr int kLoader = NCW, kScheduler = NCW + 1, kEpilogue = NCW + 2;
+    constexpr int kLoader = NCW, kSched0 = NCW + 1, kEpilogue = NCW + 1 + kSchedWarps;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Ctl<STAGES, G> ctl(smem + Sh::kCtlOff);
+    Ctl<STAGES, MB> ctl(smem + Sh::kCtlOff);
     auto merge_mo = [&](int b) { return reinterpret_cast<float*>(smem + Sh::kRingBytes + b * Sh::kMergeBuf); };
     auto merge_ml = [&](int b) { return merge_mo(b) + NCW * G * D; };
 
@@ -393,11 +439,12 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
             mbar_init(&ctl.qfull[s], 32);   // every scheduler lane publishes its writes
             mbar_init(&ctl.qempty[s], 32);  // every loader lane is done reading
         }
-        for (int s = 0; s < kMergeBufs; ++s) {
+        for (int s = 0; s < MB; ++s) {
             mbar_init(&ctl.mfull[s], NCW * 32);  // every consumer thread publishes its state
             mbar_init(&ctl.mempty[s], 32);       // every epilogue lane is done reading
         }
         *ctl.abort_flag = 0;
+        *ctl.pending = 0;
         fence_barrier_init();
     }
     if (threadIdx.x == 32 * kLoader && (PAGED || Cons::kSwizzled)) {
@@ -408,40 +455,68 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
     pdl_wait();
     __syncthreads();
 
-    if (warp == kScheduler) {
-        // ========================================================== scheduler
-        // Takes units from the work counter, reads their metadata (sequence
-        // length, mask or block table) and queues them for the loader up to
-        // kQueueSlots ahead.  Empty splits never reach the loader: their
-        // -inf log-sum-exps are written here.
-        int slot = 0;
+    if (warp >= kSched0 && warp < kSched0 + kSchedWarps) {
+        // ========================================================= schedulers
+        // Each takes units, reads their metadata (sequence length, mask or
+        // block table) and queues them for the loader in its own ring of
+        // kRingSlots.  Empty splits never reach the loader: their -inf
+        // log-sum-exps are written here.
+        const int sw = warp - kSched0;
+        int pos = 0;
         uint32_t sphase = 0;
         bool failed = false;
-        // Work counter: lane 0 issues the atomic; the result is read (and
-        // waited for) only when the next unit is needed.
-        auto grab_issue = [&]() -> int { return lane == 0 ? (int)atomicAdd(&p.sched[0], 1u) : 0; };
-        auto grab_take = [&](int v) -> int { return __shfl_sync(0xffffffffu, v, 0); };
-        auto publish = [&]() {
+        // Work counter: the first unit is fixed, the counter hands out the
+        // others in order after all first units.
+        const int first_units = kSchedWarps * (int)gridDim.x;
+        int u = (int)blockIdx.x * kSchedWarps + sw;
+        auto publish = [&](int slot) {
             mbar_arrive(&ctl.qfull[slot]);
-            if (++slot == kQueueSlots) {
-                slot = 0;
+            if (++pos == kRingSlots) {
+                pos = 0;
                 sphase ^= 1u;
             }
         };
-        int u = grab_take(grab_issue());
+        // Below the lookahead?  Lane 0 polls; every lane gets the outcome.
+        auto below_lookahead = [&]() -> bool {
+            int ok = 1;
+            if (lane == 0) {
+                const volatile int* pend = ctl.pending;
+                if (*pend >= p.look) {
+                    const unsigned long long t0 = global_timer_ns();
+                    while (*pend >= p.look) {
+                        if (*ctl.abort_flag || global_timer_ns() - t0 > kWaitLimitNs) {
+                            ok = 0;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                }
+            }
+            return __shfl_sync(0xffffffffu, ok, 0) != 0;
+        };
+        bool first = true;
         while (true) {
+            const int slot = sw * kRingSlots + pos;
             if (!warp_wait(&ctl.qempty[slot], sphase ^ 1u, ctl.abort_flag)) {
                 failed = true;
                 break;
             }
+            if (!first) {
+                if (!below_lookahead()) {
+                    failed = true;
+                    break;
+                }
+                const int t = lane == 0 ? (int)atomicAdd(&p.sched[0], 1u) : 0;
+                u = first_units + __shfl_sync(0xffffffffu, t, 0);
+            }
+            first = false;
             UnitSlot& sl = ctl.slots[slot];
             if (u >= p.units) {
                 if (lane == 0) sl.kind = kSlotEnd;
                 __syncwarp();
-                publish();
+                publish(slot);
                 break;
             }
-            const int next_ticket = grab_issue();  // in flight during this unit's scan
             const Unit un = decode_unit(p, G, u);
             const SplitRange r = split_range<PAGED>(
                 p, un.bz, un.split, lane == 0 && un.split == 0 && un.kvh == 0 && un.hg == 0);
@@ -460,9 +535,10 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                     sl.ntok = r.ntok;
                     sl.last = last;
                     sl.lb0 = lb0;
+                    atomicAdd(ctl.pending, (last + 1) * p.tile);
                 }
                 __syncwarp();
-                publish();
+                publish(slot);
             } else if (p.direct) {
                 // the whole row is empty: zeros and lse = -inf
                 for (int idx = lane; idx < un.g_here * D; idx += 32)
@@ -471,17 +547,16 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
             } else if (lane < un.g_here) {
                 p.part_lse[(un.qrow0 + lane) * p.S + un.split] = -INFINITY;  // no partial row
             }
-            u = grab_take(next_ticket);
         }
         if (failed && lane == 0 && !*ctl.abort_flag) {
             *ctl.abort_flag = 1;
             report(p.dev_status, KVD_DEV_TIMEOUT);
         }
         if (lane == 0) {
-            // The CTA that finishes taking units last leaves the scheduling
-            // counters at zero for the next call.
+            // The scheduler warp that finishes taking units last leaves the
+            // scheduling counters at zero for the next call.
             __threadfence();
-            if (atomicAdd(&p.sched[1], 1u) == gridDim.x - 1) {
+            if (atomicAdd(&p.sched[1], 1u) == (uint32_t)first_units - 1u) {
                 atomicExch(&p.sched[0], 0u);
                 atomicExch(&p.sched[1], 0u);
             }
@@ -509,7 +584,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
             write_rows<Elem, D, G, NCW>(p, merge_mo(mb), merge_ml(mb), un, lane);
             __syncwarp();
             mbar_arrive(&ctl.mempty[mb]);  // every lane: done reading the buffer
-            if (++mb == kMergeBufs) {
+            if (++mb == MB) {
                 mb = 0;
                 eph ^= 1u;
             }
@@ -534,18 +609,63 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                 phase ^= 1u;
             }
         };
-        int slot = 0;
-        uint32_t lphase = 0;
-        while (!failed) {
-            if (!warp_wait(&ctl.qfull[slot], lphase, ctl.abort_flag)) {
+        // Scheduler rings: position and parity of each ring's head, which
+        // rings have not ended yet; the loader takes whichever head is ready,
+        // starting with the ring it did not take last.
+        int rpos[kSchedWarps] = {};
+        uint32_t rphase = 0, live = (1u << kSchedWarps) - 1u;
+        int pref = 0;
+        while (!failed && live) {
+            int pick = -1;
+            if (lane == 0) {
+                const unsigned long long t0 = global_timer_ns();
+                for (uint32_t it = 0;; ++it) {
+#pragma unroll
+                    for (int k = 0; k < kSchedWarps; ++k) {
+                        const int rr = (pref + k) % kSchedWarps;
+                        int hp = 0;
+#pragma unroll
+                        for (int q = 0; q < kSchedWarps; ++q) hp = q == rr ? rpos[q] : hp;
+                        if (((live >> rr) & 1u) &&
+                            mbar_test(&ctl.qfull[rr * kRingSlots + hp], (rphase >> rr) & 1u)) {
+                            pick = rr;
+                            break;
+                        }
+                    }
+                    if (pick >= 0 || *ctl.abort_flag) break;
+                    if ((it & 15u) == 15u && global_timer_ns() - t0 > kWaitLimitNs) break;
+                }
+            }
+            pick = __shfl_sync(0xffffffffu, pick, 0);
+            if (pick < 0) {
                 failed = true;
                 break;
             }
+            int hp = 0;
+#pragma unroll
+            for (int q = 0; q < kSchedWarps; ++q) hp = q == pick ? rpos[q] : hp;
+            const int slot = pick * kRingSlots + hp;
+            // completed already: every lane acquires the scheduler's writes
+            if (!warp_wait(&ctl.qfull[slot], (rphase >> pick) & 1u, ctl.abort_flag)) {
+                failed = true;
+                break;
+            }
+#pragma unroll
+            for (int q = 0; q < kSchedWarps; ++q)
+                if (q == pick && ++rpos[q] == kRingSlots) {
+                    rpos[q] = 0;
+                    rphase ^= 1u << q;
+                }
+            pref = (pick + 1) % kSchedWarps;
             const UnitSlot& sl = ctl.slots[slot];
-            if (sl.kind == kSlotEnd) break;
+            if (sl.kind == kSlotEnd) {
+                live &= ~(1u << pick);
+                continue;
+            }
             const Unit un = decode_unit(p, G, sl.unit);
             const int t_begin = sl.t_begin, ntok = sl.ntok, last = sl.last, lb0 = sl.lb0;
             bool first = true;
+            int counted = 0;  // tiles already taken off ctl.pending
             for (int i = 0; i <= last; ++i) {
                 const int r0 = i * p.tile;
                 const int n = min(p.tile, ntok - r0);
@@ -553,6 +673,8 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                 if (!bits) continue;  // all-zero tile: never read
                 if (!acquire()) break;
                 if (lane == 0) {
+                    atomicAdd(ctl.pending, -(i + 1 - counted) * p.tile);
+                    counted = i + 1;
                     StageMeta& mt = ctl.meta[stage];
                     mt.unit = sl.unit;
                     mt.tile = i;
@@ -617,10 +739,6 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
             if (failed) break;
             __syncwarp();
             mbar_arrive(&ctl.qempty[slot]);  // every lane: done with the slot
-            if (++slot == kQueueSlots) {
-                slot = 0;
-                lphase ^= 1u;
-            }
         }
         if (!failed && acquire()) {
             if (lane == 0) {
@@ -660,7 +778,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
         if (unit >= 0) cons.finish(merge_mo(mb), merge_ml(mb), warp, lane);
         if (warp == 0 && lane == 0) ctl.mhdr[mb] = unit;
         mbar_arrive(&ctl.mfull[mb]);  // every consumer thread
-        if (++mb == kMergeBufs) {
+        if (++mb == MB) {
             mb = 0;
             mph ^= 1u;
         }

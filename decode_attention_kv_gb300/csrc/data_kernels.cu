@@ -6,120 +6,91 @@
 namespace kvd {
 
 // ------------------------------------------------------------------ combine
-// One CTA per output row.  Merges S partial rows, each normalised over its own
-// key range, by their log-sum-exp ("Intel NPU running LLMs", Part 3, Flash
-// SDPA path: tiles merged exactly through running max and sum).  The row's
-// log-sum-exps are reduced first; then groups of threads split the S partial
-// rows between them (a thread owns one float4 of the row) so that the loads
-// of many partial rows are in flight at once; shared memory sums the groups.
-constexpr int kCombineThreads = 128;
-
-__device__ __forceinline__ float block_reduce(float x, bool is_max, float* red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float o = __shfl_xor_sync(0xffffffffu, x, off);
-        x = is_max ? fmaxf(x, o) : x + o;
-    }
-    __syncthreads();  // red[] may still be read from a previous reduction
-    if (lane == 0) red[warp] = x;
-    __syncthreads();
-    x = red[0];
-#pragma unroll
-    for (int w = 1; w < kCombineThreads / 32; ++w) x = is_max ? fmaxf(x, red[w]) : x + red[w];
-    return x;
-}
+// Merges S partial rows, each normalised over its own key range, by their
+// log-sum-exp ("Intel NPU running LLMs", Part 3, Flash SDPA path: tiles merged
+// exactly through running max and sum).  An item is (row, 32-dim slice); a
+// lane owns one dim.  `wpi` warps share an item (more when S is large), each
+// taking every wpi-th split with a running max / sum / output and a batch of
+// splits' loads in flight (a split with lse = -inf has no partial row: its
+// values are loaded and discarded); the item's first warp merges the states.
+constexpr int kCombineWarps = 8;
+constexpr int kCombineBatch = 8;  // splits per warp with loads in flight
 
 template <typename Out>
-__global__ void __launch_bounds__(kCombineThreads)
+__global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
-               Out* __restrict__ out, float* __restrict__ lse_out, int R, int S, int D) {
-    __shared__ float red[kCombineThreads / 32];
-    __shared__ float4 acc_sm[kCombineThreads];
+               Out* __restrict__ out, float* __restrict__ lse_out, int R, int S, int D, int wpi) {
+    __shared__ float sm_m[kCombineWarps], sm_l[kCombineWarps];
+    __shared__ float sm_acc[kCombineWarps][32];
     pdl_launch_dependents();
     pdl_wait();
-    const int row = blockIdx.x, tid = threadIdx.x;
-    const float* ls = part_lse + (size_t)row * S;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int nslices = (D + 31) / 32;
+    const long long item = (long long)blockIdx.x * (kCombineWarps / wpi) + w / wpi;
+    const int sub = w % wpi;
+    const bool live = item < (long long)R * nslices;
+    const long long row = live ? item / nslices : 0;
+    const int d = (int)(item % nslices) * 32 + lane;
+    const bool has_d = live && d < D;
+    float m = -INFINITY, l = 0.f, acc = 0.f;  // m in log2 units
+    if (live) {
+        const float* ls = part_lse + row * S;
+        const float* po = part_o + row * S * D;
+        for (int s0 = sub; s0 < S; s0 += wpi * kCombineBatch) {
+            float lv[kCombineBatch], xv[kCombineBatch];
+#pragma unroll
+            for (int u = 0; u < kCombineBatch; ++u) {
+                const int s = s0 + u * wpi;
+                lv[u] = s < S ? ls[s] : -INFINITY;
+                xv[u] = (s < S && has_d) ? po[(size_t)s * D + d] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < kCombineBatch; ++u) {
+                if (lv[u] == -INFINITY) continue;
+                const float x2 = lv[u] * kLog2e;
+                const float mn = fmaxf(m, x2);
+                const float c = fast_exp2(m - mn), e = fast_exp2(x2 - mn);
+                l = fmaf(l, c, e);
+                acc = fmaf(acc, c, e * xv[u]);
+                m = mn;
+            }
+        }
+    }
+    if (lane == 0) {
+        sm_m[w] = m;
+        sm_l[w] = l;
+    }
+    sm_acc[w][lane] = acc;
+    __syncthreads();
+    if (!live || sub != 0) return;
     float M = -INFINITY;
-    for (int s = tid; s < S; s += kCombineThreads) M = fmaxf(M, ls[s]);
-    M = block_reduce(M, true, red);
-    float sum = 0.f;
-    if (M != -INFINITY)
-        for (int s = tid; s < S; s += kCombineThreads) sum += fast_exp2((ls[s] - M) * kLog2e);
-    sum = block_reduce(sum, false, red);
-
-    const int nv = D / 4;                                    // float4 per row
-    const int groups = nv >= kCombineThreads ? 1 : kCombineThreads / nv;
-    const int g = tid / nv, v = tid % nv;                    // (g only meaningful if groups > 1)
-    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;    // D <= 1024: two float4 at most
-    const bool active = groups > 1 ? g < groups : true;
-    const int gg = groups > 1 ? g : 0;
-    const int v0 = groups > 1 ? v : tid;
-    if (M != -INFINITY && active) {
-        const float inv = 1.f / sum;
-        const float4* po = reinterpret_cast<const float4*>(part_o) + (size_t)row * S * nv;
-#pragma unroll 8
-        for (int s = gg; s < S; s += groups) {
-            const float lsv = ls[s];
-            if (lsv == -INFINITY) continue;  // empty range: its row is not read
-            const float w = fast_exp2((lsv - M) * kLog2e) * inv;
-            const float4* src = po + (size_t)s * nv;
-            if (v0 < nv) {
-                const float4 x = src[v0];
-                a0.x = fmaf(w, x.x, a0.x);
-                a0.y = fmaf(w, x.y, a0.y);
-                a0.z = fmaf(w, x.z, a0.z);
-                a0.w = fmaf(w, x.w, a0.w);
-            }
-            if (v0 + kCombineThreads < nv) {
-                const float4 x = src[v0 + kCombineThreads];
-                a1.x = fmaf(w, x.x, a1.x);
-                a1.y = fmaf(w, x.y, a1.y);
-                a1.z = fmaf(w, x.z, a1.z);
-                a1.w = fmaf(w, x.w, a1.w);
-            }
+    for (int k = 0; k < wpi; ++k) M = fmaxf(M, sm_m[w + k]);
+    float L = 0.f, A = 0.f;
+    if (M != -INFINITY) {
+        for (int k = 0; k < wpi; ++k) {
+            const float c = fast_exp2(sm_m[w + k] - M);  // 0 for a warp without a split
+            L = fmaf(sm_l[w + k], c, L);
+            A = fmaf(sm_acc[w + k][lane], c, A);
         }
     }
-    if (groups > 1) {
-        acc_sm[tid] = a0;
-        __syncthreads();
-        if (g == 0) {
-            for (int k = 1; k < groups; ++k) {
-                const float4 x = acc_sm[k * nv + v];
-                a0.x += x.x;
-                a0.y += x.y;
-                a0.z += x.z;
-                a0.w += x.w;
-            }
-        }
-    }
-    if (groups == 1 || g == 0) {
-        const size_t o = (size_t)row * D;
-        if (v0 < nv) {
-            ElemTraits<Out>::store(out, o + 4 * v0, a0.x);
-            ElemTraits<Out>::store(out, o + 4 * v0 + 1, a0.y);
-            ElemTraits<Out>::store(out, o + 4 * v0 + 2, a0.z);
-            ElemTraits<Out>::store(out, o + 4 * v0 + 3, a0.w);
-        }
-        if (v0 + kCombineThreads < nv) {
-            const size_t o1 = o + 4 * (v0 + kCombineThreads);
-            ElemTraits<Out>::store(out, o1, a1.x);
-            ElemTraits<Out>::store(out, o1 + 1, a1.y);
-            ElemTraits<Out>::store(out, o1 + 2, a1.z);
-            ElemTraits<Out>::store(out, o1 + 3, a1.w);
-        }
-    }
-    if (tid == 0 && lse_out) lse_out[row] = M != -INFINITY ? M + logf(sum) : -INFINITY;
+    if (has_d) ElemTraits<Out>::store(out, (size_t)row * D + d, L > 0.f ? A / L : 0.f);
+    if (d == 0 && lse_out) lse_out[row] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
 }
 
 cudaError_t launch_combine(const float* part_o, const float* part_lse, void* out,
                            float* lse_out, int R, int S, int D, kvd_dtype out_dt,
                            cudaStream_t stream) {
+    // warps per item: about S / 8 (a power of two, 1..8)
+    int wpi = 1;
+    while (wpi < kCombineWarps && wpi * 2 * kCombineBatch <= S) wpi *= 2;
+    const long long items = (long long)R * ((D + 31) / 32);
+    const long long per_cta = kCombineWarps / wpi;
+    const dim3 grid((unsigned)((items + per_cta - 1) / per_cta));
     if (out_dt == KVD_BF16)
-        return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(R), dim3(kCombineThreads), 0, stream,
-                          part_o, part_lse, static_cast<__nv_bfloat16*>(out), lse_out, R, S, D);
-    return launch_pdl(combine_kernel<float>, dim3(R), dim3(kCombineThreads), 0, stream, part_o,
-                      part_lse, static_cast<float*>(out), lse_out, R, S, D);
+        return launch_pdl(combine_kernel<__nv_bfloat16>, grid, dim3(kCombineWarps * 32), 0, stream,
+                          part_o, part_lse, static_cast<__nv_bfloat16*>(out), lse_out, R, S, D, wpi);
+    return launch_pdl(combine_kernel<float>, grid, dim3(kCombineWarps * 32), 0, stream, part_o,
+                      part_lse, static_cast<float*>(out), lse_out, R, S, D, wpi);
 }
 
 // ------------------------------------------------------------------- append

@@ -57,14 +57,19 @@ bool dtype_ok(kvd_dtype dt) { return dt == KVD_BF16 || dt == KVD_F32; }
 // units per launch -- several per CTA of the persistent grid, so that the
 // unit counter balances rows of different lengths -- with splits of at least
 // kMinChunk slots, so that the partial rows stay a small fraction of the KV
-// traffic.
+// traffic.  Unless the caller fixes the number of splits, the last quarter or
+// so of the capacity is cut into splits of a quarter of the size: units are
+// handed out split-major, so these small units are the last ones taken and
+// the CTAs finish within a small unit of each other.
 constexpr long long kTargetUnits = 2048;
 constexpr int kMinChunk = 128;
 
 struct Plan {
     int G, HG;      // compile-time group width, head groups per kv head
     int tile;       // tokens per ring stage
-    int chunk;      // tokens per split
+    int chunk;      // tokens per split for splits [0, Sb)
+    int chunk2;     // tokens per split for splits [Sb, S)
+    int Sb;
     int S;          // splits per row
     long long units;
     // workspace: scheduling counters (256 bytes) | partial lse | partial rows
@@ -126,9 +131,17 @@ Plan plan_attention(int rows, int Hq, int Hkv, int cap, int D, kvd_dtype dt, int
     chunk = (chunk + unit - 1) / unit * unit;
     if (chunk > max_chunk) chunk = max_chunk;
     if (chunk < unit) chunk = unit;
-    pl.chunk = (int)chunk;
-    pl.S = (int)(((long long)cap + chunk - 1) / chunk);
-    if (pl.S < 1) pl.S = 1;
+    pl.chunk = pl.chunk2 = (int)chunk;
+    pl.S = pl.Sb = (int)(((long long)cap + chunk - 1) / chunk);
+    if (pl.S < 1) pl.S = pl.Sb = 1;
+    const long long small = ((chunk / 4) + unit - 1) / unit * unit;
+    if (num_splits <= 0 && pl.S > 1 && small < chunk) {
+        const int tail = pl.S / 4 > 1 ? pl.S / 4 : 1;  // big splits turned into small ones
+        pl.Sb = pl.S - tail;
+        pl.chunk2 = (int)small;
+        const long long rest = (long long)cap - (long long)pl.Sb * chunk;
+        pl.S = pl.Sb + (int)((rest + small - 1) / small);
+    }
     pl.units = row_units * pl.S;
     pl.off_lse = 256;
     if (pl.S > 1) {
@@ -151,6 +164,8 @@ void attach_workspace(AttendParams& p, const Plan& pl, void* ws) {
     p.HG = pl.HG;
     p.tile = pl.tile;
     p.chunk = pl.chunk;
+    p.chunk2 = pl.chunk2;
+    p.Sb = pl.Sb;
     p.S = pl.S;
     p.direct = pl.S == 1;
 }

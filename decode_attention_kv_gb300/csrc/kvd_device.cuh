@@ -79,6 +79,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false when
 // the wait limit runs out or another thread of the CTA raised `abort_flag`.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
@@ -188,6 +201,15 @@ struct ElemTraits<__nv_bfloat16> {
     __device__ __forceinline__ static void store(void* base, size_t i, float x) {
         reinterpret_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(x);
     }
+    // elements i..i+3, i a multiple of 4 (8-byte store)
+    __device__ __forceinline__ static void store4(void* base, size_t i, float4 x) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(x.z, x.w);
+        uint2 w;
+        w.x = *reinterpret_cast<const uint32_t*>(&a);
+        w.y = *reinterpret_cast<const uint32_t*>(&b);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(base) + i) = w;
+    }
 };
 
 template <>
@@ -199,6 +221,10 @@ struct ElemTraits<float> {
     }
     __device__ __forceinline__ static void store(void* base, size_t i, float x) {
         reinterpret_cast<float*>(base)[i] = x;
+    }
+    // elements i..i+3, i a multiple of 4 (16-byte store)
+    __device__ __forceinline__ static void store4(void* base, size_t i, float4 x) {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + i) = x;
     }
 };
 

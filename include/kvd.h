@@ -107,9 +107,11 @@ kvd_status kvd_append(void* k_cache, void* v_cache, const void* k_new, const voi
  *   lse_out   [B, Hq] float or NULL
  * A row with no valid slot gives out = 0 and lse = -inf.
  * The sequence axis of every (batch entry, kv head) row is cut into splits
- * (num_splits; 0 = planned by the library from the sizes) that a persistent
- * grid takes from a work counter; each split keeps an fp32 running max / sum
- * / output.  With more than one split a second kernel merges the splits by
+ * that a persistent grid takes from a work counter; each split keeps an fp32
+ * running max / sum / output.  num_splits > 0 asks for about that many equal
+ * splits (lengths rounded up to the kernel's tile, at most 4096 slots); 0
+ * lets the library plan from the sizes, with smaller splits over the end of
+ * the capacity.  With more than one split a second kernel merges the splits by
  * log-sum-exp (the kvd_combine formula).
  * Workspace: at least kvd_attend_masked_workspace_bytes(...) bytes (never
  * less than 256), 256-byte aligned, holding the work counters and the
