@@ -21,7 +21,7 @@
 // and load-balances rows of any length.
 //
 // CTA.  Four roles in warps:
-//  * schedulers (warps NCW+1, NCW+2): each takes units from the work counter,
+//  * schedulers (warps NCW+1 .. NCW+4): each takes units from the work counter,
 //    reads their metadata (sequence length and block-table entries, or the
 //    split's mask) into 32-token validity words and queues them for the
 //    loader in a ring of its own.  A scheduler takes a unit only while the
@@ -40,7 +40,7 @@
 //  * consumers (warps 0..NCW-1, attend_consumers.cuh): the online softmax over
 //    the tiles; at a unit's last tile they drop their states into one of two
 //    merge buffers and go on with the next unit.
-//  * epilogue (warp NCW+3): merges the consumer warps' states of a unit and
+//  * epilogue (warp NCW+5): merges the consumer warps' states of a unit and
 //    writes either the final rows (single split) or a normalised partial row
 //    and its log-sum-exp.
 // With more than one split the host launches the log-sum-exp combine kernel
@@ -49,8 +49,8 @@
 //
 // Counters (unit counter, schedulers-done counter) live in the caller's
 // workspace: zero before the first call; the last scheduler warp to finish
-// taking units resets them.  The first unit of each scheduler warp is
-// blockIdx.x * 2 + warp (no atomic); the counter hands out the rest.
+// taking units resets them.  The first unit of scheduler warp s is
+// s * gridDim.x + blockIdx.x (no atomic); the counter hands out the rest.
 // All waits are bounded; a wait that runs out sets KVD_DEV_TIMEOUT, after
 // which the counters must be zeroed again.
 #pragma once
@@ -128,9 +128,9 @@ __device__ __forceinline__ Unit decode_unit(const AttendParams& p, int G, int u)
 
 // A unit prepared by the scheduler warp for the loader warp.
 enum : int { kSlotTiles = 0, kSlotCombine = 1, kSlotEnd = 2 };
-constexpr int kSchedWarps = 2;                         // scheduler warps per CTA
-constexpr int kRingSlots = 2;                          // queued units per scheduler
-constexpr int kQueueSlots = kSchedWarps * kRingSlots;  // scheduler s owns slots [2s, 2s + 2)
+constexpr int kSchedWarps = 4;                         // scheduler warps per CTA
+constexpr int kRingSlots = 1;                          // queued units per scheduler
+constexpr int kQueueSlots = kSchedWarps * kRingSlots;  // scheduler s owns slot s
 
 struct UnitSlot {
     int kind;    // kSlotTiles: stream the unit's tiles; kSlotCombine: only merge its row
@@ -465,10 +465,15 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
         int pos = 0;
         uint32_t sphase = 0;
         bool failed = false;
-        // Work counter: the first unit is fixed, the counter hands out the
-        // others in order after all first units.
-        const int first_units = kSchedWarps * (int)gridDim.x;
-        int u = (int)blockIdx.x * kSchedWarps + sw;
+        // Work counter: the first unit of each scheduler is fixed, the counter
+        // hands out the others in order after them.  With enough units a CTA
+        // starts with kSchedWarps consecutive units -- one split of rows that
+        // share their mask row or sequence, so that the metadata reads after
+        // the first hit L1 -- else the first units are spread over all CTAs.
+        const int n_sched = kSchedWarps * (int)gridDim.x;
+        const int first_units = n_sched;
+        int u = p.units >= n_sched ? (int)blockIdx.x * kSchedWarps + sw
+                                   : sw * (int)gridDim.x + (int)blockIdx.x;
         auto publish = [&](int slot) {
             mbar_arrive(&ctl.qfull[slot]);
             if (++pos == kRingSlots) {
@@ -556,7 +561,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
             // The scheduler warp that finishes taking units last leaves the
             // scheduling counters at zero for the next call.
             __threadfence();
-            if (atomicAdd(&p.sched[1], 1u) == (uint32_t)first_units - 1u) {
+            if (atomicAdd(&p.sched[1], 1u) == (uint32_t)n_sched - 1u) {
                 atomicExch(&p.sched[0], 0u);
                 atomicExch(&p.sched[1], 0u);
             }
