@@ -80,9 +80,10 @@ combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_
 cudaError_t launch_combine(const float* part_o, const float* part_lse, void* out,
                            float* lse_out, int R, int S, int D, kvd_dtype out_dt,
                            cudaStream_t stream) {
-    // warps per item: about S / 8 (a power of two, 1..8)
+    // warps per item: enough that each warp's splits fit one batch of loads
+    // (a power of two, 1..8)
     int wpi = 1;
-    while (wpi < kCombineWarps && wpi * 2 * kCombineBatch <= S) wpi *= 2;
+    while (wpi < kCombineWarps && wpi * kCombineBatch < S) wpi *= 2;
     const long long items = (long long)R * ((D + 31) / 32);
     const long long per_cta = kCombineWarps / wpi;
     const dim3 grid((unsigned)((items + per_cta - 1) / per_cta));
