@@ -441,20 +441,29 @@ def timed(torch, dist, fn, K):
     return e0.elapsed_time(e1)
 
 
-def max_over_ranks(torch, dist, x):
+def _reduce(torch, dist, x, op):
     if dist is None:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=op)
     return float(t.item())
+
+
+def max_over_ranks(torch, dist, x):
+    return _reduce(torch, dist, x, None if dist is None else dist.ReduceOp.MAX)
 
 
 def sum_over_ranks(torch, dist, x):
-    if dist is None:
-        return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _reduce(torch, dist, x, None if dist is None else dist.ReduceOp.SUM)
+
+
+def whole_job_rate(torch, dist, ms, nbytes):
+    """Weak scaling: every rank processes its own workload; the job's rate is
+    the bytes all ranks moved over the slowest rank's time (GB/s, ms)."""
+    ms_max = max_over_ranks(torch, dist, ms)
+    total = sum_over_ranks(torch, dist, nbytes)
+    return total / (ms_max / 1e3) / 1e9, ms_max
 
 
 def gate_stream(torch, ms=10):
@@ -491,10 +500,8 @@ def measure_workload(b, torch, dist, K, W, peak, clocks=None):
     ms = timed(torch, dist, b.graph_run, K)
     if clocks is not None:
         res["clocks"] = clocks.stop()
-    ms = max_over_ranks(torch, dist, ms)
-    total = sum_over_ranks(torch, dist, sum(b.step_bytes(j) for j in range(K)))
+    res["gbs"], ms = whole_job_rate(torch, dist, ms, sum(b.step_bytes(j) for j in range(K)))
     res["ms_per_step"] = ms / K
-    res["gbs"] = total / (ms / 1e3) / 1e9
     res["tokens_per_s"] = sum_over_ranks(torch, dist, b.tokens_per_step() * K) / (ms / 1e3)
 
     log(f"  timed steps done: {ms / K:.3f} ms/step; per-launch pass")
@@ -517,9 +524,9 @@ def measure_workload(b, torch, dist, K, W, peak, clocks=None):
         res["gather_frac"] = res["gather_gbs"] / peak
 
     b.reset_cycle()
-    ms_e = max_over_ranks(torch, dist, timed(torch, dist, b.eager_run, K))
-    res["eager"] = {"gbs": sum_over_ranks(torch, dist, sum(b.step_bytes(j) for j in range(K)))
-                    / (ms_e / 1e3) / 1e9, "ms_per_step": ms_e / K}
+    gbs_e, ms_e = whole_job_rate(torch, dist, timed(torch, dist, b.eager_run, K),
+                                 sum(b.step_bytes(j) for j in range(K)))
+    res["eager"] = {"gbs": gbs_e, "ms_per_step": ms_e / K}
     b.reset_cycle()
     return res
 
@@ -531,10 +538,10 @@ def measure_e2e(b, torch, dist, K):
         b.e2e_step(j)
     torch.cuda.synchronize()
     b.reset_cycle()
-    ms = max_over_ranks(torch, dist, timed(torch, dist, b.e2e_step, K))
-    total = sum_over_ranks(torch, dist, sum(b.step_bytes(j) for j in range(K)))
+    gbs, ms = whole_job_rate(torch, dist, timed(torch, dist, b.e2e_step, K),
+                             sum(b.step_bytes(j) for j in range(K)))
     b.reset_cycle()
-    return {"value": total / (ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+    return {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms / K}
 
 
