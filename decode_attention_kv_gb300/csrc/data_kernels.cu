@@ -8,41 +8,66 @@ namespace kvd {
 // ------------------------------------------------------------------ combine
 // Merges S partial rows, each normalised over its own key range, by their
 // log-sum-exp ("Intel NPU running LLMs", Part 3, Flash SDPA path: tiles merged
-// exactly through running max and sum).  An item is (row, 32-dim slice); a
-// lane owns one dim.  `wpi` warps share an item (more when S is large), each
-// taking every wpi-th split with a running max / sum / output and a batch of
-// splits' loads in flight (a split with lse = -inf has no partial row: its
-// values are loaded and discarded); the item's first warp merges the states.
+// exactly through running max and sum).  An item is (row, slice of 32 * VPL
+// dims); a lane owns VPL consecutive dims.  `wpi` warps share an item (more
+// when S is large), each taking every wpi-th split with a running max / sum /
+// output and a batch of splits' loads in flight (a split with lse = -inf has
+// no partial row: its values are loaded and discarded); the item's first
+// warp merges the states.  VPL = 2 halves the CTAs when there are many rows.
 constexpr int kCombineWarps = 8;
 constexpr int kCombineBatch = 8;  // splits per warp with loads in flight
 
-template <typename Out>
+template <int VPL>
+struct CombineVec;
+template <>
+struct CombineVec<1> {
+    using T = float;
+    __device__ static float zero() { return 0.f; }
+    __device__ static void fma(float& a, float c, float e, float x) { a = fmaf(a, c, e * x); }
+};
+template <>
+struct CombineVec<2> {
+    using T = float2;
+    __device__ static float2 zero() { return make_float2(0.f, 0.f); }
+    __device__ static void fma(float2& a, float c, float e, float2 x) {
+        a.x = fmaf(a.x, c, e * x.x);
+        a.y = fmaf(a.y, c, e * x.y);
+    }
+};
+
+template <typename Out, int VPL>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
                Out* __restrict__ out, float* __restrict__ lse_out, int R, int S, int D, int wpi) {
+    using Vec = CombineVec<VPL>;
+    using T = typename Vec::T;
     __shared__ float sm_m[kCombineWarps], sm_l[kCombineWarps];
-    __shared__ float sm_acc[kCombineWarps][32];
+    __shared__ T sm_acc[kCombineWarps][32];
     pdl_launch_dependents();
     pdl_wait();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int nslices = (D + 31) / 32;
+    constexpr int kSlice = 32 * VPL;
+    const int nslices = (D + kSlice - 1) / kSlice;
     const long long item = (long long)blockIdx.x * (kCombineWarps / wpi) + w / wpi;
     const int sub = w % wpi;
     const bool live = item < (long long)R * nslices;
     const long long row = live ? item / nslices : 0;
-    const int d = (int)(item % nslices) * 32 + lane;
-    const bool has_d = live && d < D;
-    float m = -INFINITY, l = 0.f, acc = 0.f;  // m in log2 units
+    const int d = (int)(item % nslices) * kSlice + VPL * lane;
+    const bool has_d = live && d < D;  // D % 4 == 0: a lane's dims are all in or all out
+    float m = -INFINITY, l = 0.f;  // m in log2 units
+    T acc = Vec::zero();
     if (live) {
         const float* ls = part_lse + row * S;
         const float* po = part_o + row * S * D;
         for (int s0 = sub; s0 < S; s0 += wpi * kCombineBatch) {
-            float lv[kCombineBatch], xv[kCombineBatch];
+            float lv[kCombineBatch];
+            T xv[kCombineBatch];
 #pragma unroll
             for (int u = 0; u < kCombineBatch; ++u) {
                 const int s = s0 + u * wpi;
                 lv[u] = s < S ? ls[s] : -INFINITY;
-                xv[u] = (s < S && has_d) ? po[(size_t)s * D + d] : 0.f;
+                xv[u] = (s < S && has_d) ? *reinterpret_cast<const T*>(po + (size_t)s * D + d)
+                                         : Vec::zero();
             }
 #pragma unroll
             for (int u = 0; u < kCombineBatch; ++u) {
@@ -51,7 +76,7 @@ combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_
                 const float mn = fmaxf(m, x2);
                 const float c = fast_exp2(m - mn), e = fast_exp2(x2 - mn);
                 l = fmaf(l, c, e);
-                acc = fmaf(acc, c, e * xv[u]);
+                Vec::fma(acc, c, e, xv[u]);
                 m = mn;
             }
         }
@@ -65,16 +90,37 @@ combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_
     if (!live || sub != 0) return;
     float M = -INFINITY;
     for (int k = 0; k < wpi; ++k) M = fmaxf(M, sm_m[w + k]);
-    float L = 0.f, A = 0.f;
+    float L = 0.f;
+    T A = Vec::zero();
     if (M != -INFINITY) {
         for (int k = 0; k < wpi; ++k) {
             const float c = fast_exp2(sm_m[w + k] - M);  // 0 for a warp without a split
             L = fmaf(sm_l[w + k], c, L);
-            A = fmaf(sm_acc[w + k][lane], c, A);
+            Vec::fma(A, 1.f, c, sm_acc[w + k][lane]);
         }
     }
-    if (has_d) ElemTraits<Out>::store(out, (size_t)row * D + d, L > 0.f ? A / L : 0.f);
+    if (has_d) {
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const float* a = reinterpret_cast<const float*>(&A);
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) ElemTraits<Out>::store(out, (size_t)row * D + d + v, a[v] * inv);
+    }
     if (d == 0 && lse_out) lse_out[row] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+}
+
+template <int VPL>
+cudaError_t launch_combine_vpl(const float* part_o, const float* part_lse, void* out,
+                               float* lse_out, int R, int S, int D, kvd_dtype out_dt, int wpi,
+                               cudaStream_t stream) {
+    const long long items = (long long)R * ((D + 32 * VPL - 1) / (32 * VPL));
+    const long long per_cta = kCombineWarps / wpi;
+    const dim3 grid((unsigned)((items + per_cta - 1) / per_cta));
+    if (out_dt == KVD_BF16)
+        return launch_pdl(combine_kernel<__nv_bfloat16, VPL>, grid, dim3(kCombineWarps * 32), 0,
+                          stream, part_o, part_lse, static_cast<__nv_bfloat16*>(out), lse_out, R,
+                          S, D, wpi);
+    return launch_pdl(combine_kernel<float, VPL>, grid, dim3(kCombineWarps * 32), 0, stream, part_o,
+                      part_lse, static_cast<float*>(out), lse_out, R, S, D, wpi);
 }
 
 cudaError_t launch_combine(const float* part_o, const float* part_lse, void* out,
@@ -84,14 +130,10 @@ cudaError_t launch_combine(const float* part_o, const float* part_lse, void* out
     // (a power of two, 1..8)
     int wpi = 1;
     while (wpi < kCombineWarps && wpi * kCombineBatch < S) wpi *= 2;
-    const long long items = (long long)R * ((D + 31) / 32);
-    const long long per_cta = kCombineWarps / wpi;
-    const dim3 grid((unsigned)((items + per_cta - 1) / per_cta));
-    if (out_dt == KVD_BF16)
-        return launch_pdl(combine_kernel<__nv_bfloat16>, grid, dim3(kCombineWarps * 32), 0, stream,
-                          part_o, part_lse, static_cast<__nv_bfloat16*>(out), lse_out, R, S, D, wpi);
-    return launch_pdl(combine_kernel<float>, grid, dim3(kCombineWarps * 32), 0, stream, part_o,
-                      part_lse, static_cast<float*>(out), lse_out, R, S, D, wpi);
+    // two dims per lane once one dim per lane would need more than ~1024 items
+    if ((long long)R * ((D + 31) / 32) >= 1024 && D % 2 == 0)
+        return launch_combine_vpl<2>(part_o, part_lse, out, lse_out, R, S, D, out_dt, wpi, stream);
+    return launch_combine_vpl<1>(part_o, part_lse, out, lse_out, R, S, D, out_dt, wpi, stream);
 }
 
 // ------------------------------------------------------------------- append
