@@ -15,11 +15,19 @@
 //    p.V with packed FMAs.  Used for fp32 and for 1-2 query heads per kv head.
 //  MmaConsumer: tensor cores for bf16 groups of 4-8 query heads per kv head.
 //    q.K^T of a 16-token slab is mma.m16n8k16 with tokens on M and the packed
-//    heads on N; p.V is V^T p^T with p split into bf16 hi + lo parts (16
-//    significant bits, so the result matches the CUDA-core path to fp32
-//    rounding); K/V tiles arrive in the 128-byte swizzle so that ldmatrix is
+//    heads on N; p.V is V^T p^T with p rounded to bf16 first ("FlashMLA на
+//    Huawei Ascend": S is cast to bf16 before S.V) while the running sum l
+//    keeps the fp32 p, so that the log-sum-exp stays exact to fp32 rounding;
+//    K/V tiles arrive in the 128-byte swizzle so that ldmatrix is
 //    conflict-free; V rows of invalid tokens are zeroed first so that inf/NaN
 //    padding cannot reach the accumulator through 0 x inf.
+//
+// Both skip the rescale of the running output when a block's maximum is at
+// most kSkipScale above the running max ("FlashMLA на Huawei Ascend", the
+// online-softmax section: skip-scale with threshold 6): the stale max stays
+// the exponent base, so the block's weights reach at most e^6 (~400), well
+// inside fp32, and the result is the same up to rounding.  A warp rescales
+// only when one of its lanes needs it.
 //
 // finish() leaves each warp's state in shared memory as mo[w][h][d]
 // (unnormalised output) and ml[w][h] = (m, l) for the CTA-wide merge.
@@ -29,6 +37,8 @@
 #include "mma_ptx.cuh"
 
 namespace kvd {
+
+constexpr float kSkipScale = 6.f * kLog2e;  // threshold 6 (natural log) in log2 units
 
 template <typename Elem, int D, int G, int T, int NCW>
 struct SimtConsumer {
@@ -116,9 +126,10 @@ struct SimtConsumer {
                     s[i][hh] = val[i] ? s[i][hh] : -INFINITY;
                     mx = fmaxf(mx, s[i][hh]);
                 }
-                const float mn = fmaxf(m[hh], mx);
+                const bool up = mx > m[hh] + kSkipScale;  // m = -inf: any finite mx
+                const float mn = up ? mx : m[hh];
                 const float base = (mn == -INFINITY) ? 0.f : mn;
-                const float corr = fast_exp2(m[hh] - base);
+                const float corr = up ? fast_exp2(m[hh] - base) : 1.f;
                 m[hh] = mn;
                 float ls = 0.f;
 #pragma unroll
@@ -127,9 +138,11 @@ struct SimtConsumer {
                     ls += pr[i][hh];
                 }
                 l[hh] = fmaf(l[hh], corr, ls);
-                const float2 c2 = make_float2(corr, corr);
+                if (__any_sync(0xffffffffu, up)) {
+                    const float2 c2 = make_float2(corr, corr);
 #pragma unroll
-                for (int j = 0; j < kPairs; ++j) acc[hh][j] = fmul2(acc[hh][j], c2);
+                    for (int j = 0; j < kPairs; ++j) acc[hh][j] = fmul2(acc[hh][j], c2);
+                }
             }
 #pragma unroll
             for (int i = 0; i < kSub; ++i) {
@@ -276,32 +289,33 @@ struct MmaConsumer {
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
             }
-            const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+            const bool up0 = mx0 > m[0] + kSkipScale, up1 = mx1 > m[1] + kSkipScale;
+            const float mn0 = up0 ? mx0 : m[0], mn1 = up1 ? mx1 : m[1];
             const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float c0 = fast_exp2(m[0] - b0), c1 = fast_exp2(m[1] - b1);
+            const float c0 = up0 ? fast_exp2(m[0] - b0) : 1.f, c1 = up1 ? fast_exp2(m[1] - b1) : 1.f;
             m[0] = mn0;
             m[1] = mn1;
             const float p0 = fast_exp2(s[0] - b0), p1 = fast_exp2(s[1] - b1);
             const float p2 = fast_exp2(s[2] - b0), p3 = fast_exp2(s[3] - b1);
+            // l from the fp32 p (the log-sum-exp stays exact to fp32 rounding);
+            // p.V from p rounded to bf16 (a relative error of at most 2^-9 per weight)
             l[0] = fmaf(l[0], c0, p0 + p2);
             l[1] = fmaf(l[1], c1, p1 + p3);
-            const float2 cc = make_float2(c0, c1);
+            const uint32_t pk_lo = pack_bf16x2(p0, p1), pk_hi = pack_bf16x2(p2, p3);
+            if (__any_sync(0xffffffffu, up0 || up1)) {
+                const float2 cc = make_float2(c0, c1);
 #pragma unroll
-            for (int d = 0; d < kDBlocks; ++d) {
-                const float2 x = fmul2(make_float2(acc[d][0], acc[d][1]), cc);
-                const float2 y = fmul2(make_float2(acc[d][2], acc[d][3]), cc);
-                acc[d][0] = x.x;
-                acc[d][1] = x.y;
-                acc[d][2] = y.x;
-                acc[d][3] = y.y;
+                for (int d = 0; d < kDBlocks; ++d) {
+                    const float2 x = fmul2(make_float2(acc[d][0], acc[d][1]), cc);
+                    const float2 y = fmul2(make_float2(acc[d][2], acc[d][3]), cc);
+                    acc[d][0] = x.x;
+                    acc[d][1] = x.y;
+                    acc[d][2] = y.x;
+                    acc[d][3] = y.y;
+                }
             }
 
-            const uint32_t hi_lo = pack_bf16x2(p0, p1), hi_hi = pack_bf16x2(p2, p3);
-            const float2 h0 = bf16x2_to_float2(hi_lo), h1 = bf16x2_to_float2(hi_hi);
-            const uint32_t lo_lo = pack_bf16x2(p0 - h0.x, p1 - h0.y);
-            const uint32_t lo_hi = pack_bf16x2(p2 - h1.x, p3 - h1.y);
-            const uint32_t bh0 = movmatrix_trans(hi_lo), bh1 = movmatrix_trans(hi_hi);
-            const uint32_t bl0 = movmatrix_trans(lo_lo), bl1 = movmatrix_trans(lo_hi);
+            const uint32_t bh0 = movmatrix_trans(pk_lo), bh1 = movmatrix_trans(pk_hi);
 #pragma unroll
             for (int d = 0; d < kDBlocks; ++d) {
                 uint32_t a[4];
@@ -309,7 +323,6 @@ struct MmaConsumer {
                 const int ch = (d & 3) * 2 + ((lane >> 3) & 1);
                 ldsm_x4_trans(vbase + (d >> 2) * kHalfBytes + swz128(row, ch), a);
                 mma_bf16(acc[d], a, bh0, bh1);
-                mma_bf16(acc[d], a, bl0, bl1);
             }
         }
         return wrote;

@@ -210,3 +210,33 @@ def test_host_side_errors(kvd):
     with pytest.raises(kvd.KvdError) as e:
         kvd.attend_masked(q2, k2, k2, m, 0.1)
     assert e.value.status == "KVD_ERR_UNSUPPORTED"
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv", [(torch.bfloat16, 8, 8), (torch.bfloat16, 8, 2),
+                                          (torch.float32, 4, 4)])
+def test_skip_scale_paths(kvd, dtype, Hq, Hkv):
+    """Scores that climb slowly (the running max rises by less than the
+    skip-scale threshold from tile to tile, so the stale max is kept over
+    several tiles) and scores that jump (rescale taken), against the oracle.
+    The scores are steered through dim 0 of q and k."""
+    B, C, D = 3, 1536, 128
+    g = W.generator(77, "cpu")
+    q = W.randn(g, (B, Hq, D), dtype, scale=0.05)
+    k = W.randn(g, (B, Hkv, C, D), dtype, scale=0.05)
+    v = W.randn(g, (B, Hkv, C, D), dtype)
+    q[:, :, 0] = 4.0
+    t = torch.arange(C, dtype=torch.float32)
+    # row 0: slow climb of ~0.4 natural-log units per 64 slots (the stale
+    # max is kept for about fifteen tiles, then rescaled); row 1: a jump of ~8
+    # at slot 1000 (rescaled at once); row 2: a descent (the first tile holds
+    # the max).  Scores stay below ~10 so that the fp32 rounding of the scores
+    # themselves stays inside the fp32 bar.
+    k[0, :, :, 0] = (t * (0.4 / 64.0) * math.sqrt(D) / 4.0).to(dtype)
+    k[1, :, :, 0] = torch.where(t >= 1000, 8.0 * math.sqrt(D) / 4.0, 0.0).to(dtype)
+    k[2, :, :, 0] = ((C - t) * (0.25 / 64.0) * math.sqrt(D) / 4.0).to(dtype)
+    mask = W.prefix_mask([C, 1300, 900], C)
+    scale = 1.0 / math.sqrt(D)
+    out, lse = _run_masked(kvd, q, k, v, mask, scale)
+    ref, ref_lse = oracle.attend_masked(q, k, v, mask, scale)
+    assert_attention_close(out, ref, dtype, "skip-scale")
+    assert_lse_close(lse, ref_lse, "skip-scale")
