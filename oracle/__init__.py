@@ -75,12 +75,13 @@ def lib() -> ctypes.CDLL:
             L.kvd_oracle_attend_masked.argtypes = [vp, vp, vp, u8p, ci, ci, ci, ci, ci, ci,
                                                    cd, dp, dp, ci]
             L.kvd_oracle_append.argtypes = [vp, vp, vp, vp, i32p, u8p, ci, ci, ci, ci, ci]
+            L.kvd_oracle_copy_prefix.argtypes = [vp, vp, vp, vp, u8p, i32p, ci, ci, ci, ci, ci, ci]
             L.kvd_oracle_gather_paged.argtypes = [vp, vp, i32p, i32p, i32p, vp, vp] + [ci] * 10
             L.kvd_oracle_attend_paged.argtypes = [vp, vp, vp, i32p, i32p, i32p] + [ci] * 8 + [
                 cd, dp, dp, ci]
             L.kvd_oracle_combine.argtypes = [dp, dp, ci, ci, ci, dp, dp]
             L.kvd_oracle_threads.argtypes = []
-            for f in (L.kvd_oracle_attend_masked, L.kvd_oracle_append,
+            for f in (L.kvd_oracle_attend_masked, L.kvd_oracle_append, L.kvd_oracle_copy_prefix,
                       L.kvd_oracle_gather_paged, L.kvd_oracle_attend_paged,
                       L.kvd_oracle_combine, L.kvd_oracle_threads):
                 f.restype = ctypes.c_int
@@ -209,6 +210,31 @@ def append(k_cache, v_cache, k_new, v_new, pos, mask=None) -> int:
         mp = _p(mask, ctypes.c_uint8)
     return lib().kvd_oracle_append(_p(k_cache), _p(v_cache), _p(kn), _p(vn),
                                    _p(p, ctypes.c_int32), mp, B, Hkv, C, D, eb)
+
+
+def copy_prefix(k_src, v_src, k_dst, v_dst, n, mask=None) -> int:
+    """copy_kvcache for one layer, in place on numpy arrays (byte copy):
+    rows [0, n[b]) of k_src/v_src [B, Hkv, C_src, D] go to the same rows of
+    k_dst/v_dst [B, Hkv, C_dst, D]; mask [B, C_dst] uint8 (or None) becomes
+    the prefix mask of n[b].  Returns error bits (ERR_POS for an n[b] outside
+    [0, min(C_src, C_dst)])."""
+    for name, a in (("k_dst", k_dst), ("v_dst", v_dst)):
+        if not (isinstance(a, np.ndarray) and a.flags.c_contiguous):
+            raise TypeError(f"oracle.copy_prefix: {name} must be a contiguous numpy array")
+    B, Hkv, C_dst, D = k_dst.shape
+    ks = np.ascontiguousarray(_bytes_view(k_src))
+    vs = np.ascontiguousarray(_bytes_view(v_src))
+    eb = k_dst.dtype.itemsize
+    C_src = ks.size // (B * Hkv * D * eb)
+    if ks.size != B * Hkv * C_src * D * eb or vs.size != ks.size or v_dst.shape != k_dst.shape:
+        raise ValueError("oracle.copy_prefix: shape mismatch")
+    mp = None
+    if mask is not None:
+        if not (isinstance(mask, np.ndarray) and mask.dtype == np.uint8 and mask.flags.c_contiguous):
+            raise TypeError("oracle.copy_prefix: mask must be a contiguous uint8 numpy array")
+        mp = _p(mask, ctypes.c_uint8)
+    return lib().kvd_oracle_copy_prefix(_p(ks), _p(vs), _p(k_dst), _p(v_dst), mp,
+                                        _p(_i32(n), ctypes.c_int32), B, Hkv, C_src, C_dst, D, eb)
 
 
 def gather_paged(key_cache, value_cache, block_tables, seq_lens, seq_offset=None,

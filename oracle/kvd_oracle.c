@@ -180,6 +180,42 @@ int kvd_oracle_append(void* k_cache, void* v_cache, const void* k_new,
 }
 
 /*
+ * Prefill -> generate hand-over (copy_kvcache) for one layer
+ * ([NPU-KV] Part 2 "NPUW 的核心设计", step 3: the prefill model's present
+ * K/V, capacity 1024, are copied as the slice [0:N] into the generate
+ * model's past K/V, capacity 1152; 32 layers x K and V):
+ *   k_src, v_src [B, Hkv, C_src, D];  k_dst, v_dst [B, Hkv, C_dst, D]
+ *   n [B]: rows to copy for batch entry b (the prompt length)
+ *   mask [B, C_dst] uint8 or NULL: becomes 1 on [0, n[b]) and 0 after.
+ * n[b] outside [0, min(C_src, C_dst)] copies nothing for b, leaves its mask
+ * alone and sets ORC_ERR_POS.  Pure byte copy.
+ */
+int kvd_oracle_copy_prefix(const void* k_src, const void* v_src, void* k_dst, void* v_dst,
+                           uint8_t* mask, const int32_t* n, int B, int Hkv, int C_src,
+                           int C_dst, int D, int elem_bytes) {
+    int err = 0;
+    const size_t row = (size_t)D * elem_bytes;
+    const int cmax = C_src < C_dst ? C_src : C_dst;
+    for (int b = 0; b < B; ++b) {
+        const int nb = n[b];
+        if (nb < 0 || nb > cmax) {
+            err |= ORC_ERR_POS;
+            continue;
+        }
+        for (int h = 0; h < Hkv; ++h)
+            for (int t = 0; t < nb; ++t) {
+                const size_t src = (((size_t)b * Hkv + h) * C_src + t) * row;
+                const size_t dst = (((size_t)b * Hkv + h) * C_dst + t) * row;
+                memcpy((char*)k_dst + dst, (const char*)k_src + src, row);
+                memcpy((char*)v_dst + dst, (const char*)v_src + src, row);
+            }
+        if (mask)
+            for (int t = 0; t < C_dst; ++t) mask[(size_t)b * C_dst + t] = t < nb ? 1 : 0;
+    }
+    return err;
+}
+
+/*
  * Paged gather (gather_pa_kv_cache, Norm/ND branch):
  *   key_cache [NB, BS, Hk, Dk], value_cache [NB, BS, Hv, Dv]
  *   block_tables [Q, cols], seq_lens [Q + 1] cumsum with seq_lens[0] = 0,

@@ -308,3 +308,39 @@ def test_paged_attention_matches_torch_sdpa(oracle):
         ref = torch.nn.functional.scaled_dot_product_attention(
             q[i].double().unsqueeze(1), kk, vv, scale=0.11).squeeze(1)
         np.testing.assert_allclose(out[i], ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_copy_prefix_is_the_slice_assignment(oracle):
+    """copy_kvcache (NPU article, Part 2 'NPUW 的核心设计', step 3): the
+    prefill present[0:N] becomes the generate past[0:N]; checked against
+    numpy slice assignment on the raw 16-bit patterns, plus the prefix mask."""
+    g = W.generator(21)
+    B, H, Cs, Cd, D = 3, 2, 7, 9, 4
+    ks = W.randn(g, (B, H, Cs, D), torch.bfloat16).view(torch.int16).numpy()
+    vs = W.randn(g, (B, H, Cs, D), torch.bfloat16).view(torch.int16).numpy()
+    kd = W.randn(g, (B, H, Cd, D), torch.bfloat16).view(torch.int16).numpy().copy()
+    vd = W.randn(g, (B, H, Cd, D), torch.bfloat16).view(torch.int16).numpy().copy()
+    n = np.array([0, 7, 3], np.int32)
+    mask = np.full((B, Cd), 7, np.uint8)
+    ek, ev = kd.copy(), vd.copy()
+    for b in range(B):
+        ek[b, :, :n[b]] = ks[b, :, :n[b]]
+        ev[b, :, :n[b]] = vs[b, :, :n[b]]
+    assert oracle.copy_prefix(ks, vs, kd, vd, n, mask) == 0
+    assert np.array_equal(kd, ek) and np.array_equal(vd, ev)
+    assert np.array_equal(mask, (np.arange(Cd)[None, :] < n[:, None]).astype(np.uint8))
+
+
+def test_copy_prefix_longer_than_either_buffer_is_an_error(oracle):
+    """A prompt longer than the smaller capacity copies nothing for that
+    entry (over capacity is an error, NPU article, Part 5 '当前限制')."""
+    B, H, Cs, Cd, D = 2, 1, 6, 4, 2
+    ks = np.ones((B, H, Cs, D), np.float32)
+    kd = np.zeros((B, H, Cd, D), np.float32)
+    vd = np.zeros((B, H, Cd, D), np.float32)
+    mask = np.zeros((B, Cd), np.uint8)
+    assert oracle.copy_prefix(ks, ks, kd, vd, np.array([5, 2], np.int32), mask) == oracle.ERR_POS
+    assert np.all(kd[0] == 0) and np.all(mask[0] == 0)
+    assert np.all(kd[1, :, :2] == 1) and np.all(kd[1, :, 2:] == 0)
+    assert list(mask[1]) == [1, 1, 0, 0]
+    assert oracle.copy_prefix(ks, ks, kd, vd, np.array([-1, 0], np.int32), None) == oracle.ERR_POS
