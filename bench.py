@@ -257,6 +257,29 @@ class MaskedBench:
         self._wrap(j)
         self.graph.replay()
 
+    def copy_setup(self):
+        """copy_kvcache inputs for the static-buffer workload with a prompt:
+        prefill caches of capacity `prompt` holding the decode caches' prompt
+        rows, so that the hand-over rewrites identical rows and the prefix
+        mask of the prompt (the state reset_cycle leaves)."""
+        if self.prompt is None:
+            return False
+        torch = self.torch
+        self.pk = [l.k_cache[:, :, :self.prompt].contiguous() for l in self.w.layers]
+        self.pv = [l.v_cache[:, :, :self.prompt].contiguous() for l in self.w.layers]
+        self.cn = torch.full((self.B,), self.prompt, dtype=torch.int32, device=self.dev)
+        ws = self.w.layers
+        self.pcopy = self.kvd.PrefixCopy(self.pk, self.pv, [l.k_cache for l in ws],
+                                         [l.v_cache for l in ws], [l.mask for l in ws])
+        return True
+
+    def copy_run(self):
+        self.pcopy.run(self.cn, self.status)
+
+    def copy_bytes(self):
+        """Read + write of every copied K and V row of every layer."""
+        return 4 * self.layers * self.B * self.Hkv * self.prompt * self.D * self.elem
+
     def launches_per_step(self):
         return self.layers * (2 + (1 if self.splits else 0))
 
@@ -531,6 +554,29 @@ def measure_workload(b, torch, dist, K, W, peak, clocks=None):
     return res
 
 
+def measure_copy(b, torch, K):
+    """kvd_copy_prefix over all layers (one launch), CUDA events around each
+    launch queued behind a spinning kernel."""
+    if not (hasattr(b, "copy_setup") and b.copy_setup()):
+        return None
+    for _ in range(3):
+        b.copy_run()
+    torch.cuda.synchronize()
+    d = []
+    for _ in range(K):
+        gate_stream(torch)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        b.copy_run()
+        e1.record()
+        torch.cuda.synchronize()
+        d.append(e0.elapsed_time(e1))
+    b.reset_cycle()
+    ms = sum(d) / len(d)
+    return {"gbs": b.copy_bytes() / (ms / 1e3) / 1e9, "ms_per_launch": ms,
+            "bytes": b.copy_bytes(), "layers": b.layers}
+
+
 def measure_e2e(b, torch, dist, K):
     h2d, d2h = b.e2e_setup()
     b.reset_cycle()
@@ -696,6 +742,9 @@ def main():
     log(f"{args.workload}: {res['ms_per_step']:.3f} ms/step, {res['gbs']:.0f} GB/s; "
         f"attention {res['attend_ms_per_launch'] * 1e3:.1f} us/launch; e2e pass")
     e2e = measure_e2e(b, torch, dist, args.steps)
+    copy = measure_copy(b, torch, min(args.steps, 10))
+    if copy is not None:
+        log(f"{args.workload}: copy_kvcache of {copy['layers']} layers {copy['gbs']:.0f} GB/s")
     st = int(b.status.item())
     if st != 0:
         raise RuntimeError(f"device status {st} during the benchmark")
@@ -720,6 +769,9 @@ def main():
             for k in ("append_ms_per_launch", "gather_gbs", "gather_frac", "gather_ms_per_launch"):
                 if k in r:
                     ent[k] = r[k]
+            oc = measure_copy(ob, torch, 5)
+            if oc is not None:
+                ent["copy_prefix"] = oc
             log(f"{name}: {r['gbs']:.0f} GB/s, attention {r['attend_gbs']:.0f} GB/s")
             others[name] = ent
             del ob
@@ -749,6 +801,7 @@ def main():
                          "kernel": "attention per layer (split-KV kernel + combine)",
                          "ms_per_launch": res["attend_ms_per_launch"], "peak_source": peak_src},
             "append_ms_per_launch": res.get("append_ms_per_launch"),
+            "copy_prefix": copy,
             "eager": res["eager"], "e2e": e2e,
             "gpu_launches": b.launches_per_step() * args.steps,
             "clocks": res.get("clocks"), "cpu_baseline": cpu,

@@ -136,6 +136,80 @@ cudaError_t launch_combine(const float* part_o, const float* part_lse, void* out
     return launch_combine_vpl<1>(part_o, part_lse, out, lse_out, R, S, D, out_dt, wpi, stream);
 }
 
+// ---------------------------------------------------------- copy_kvcache
+// copy_kvcache ("Intel NPU running LLMs", Part 2 "NPUW 的核心设计", step 3):
+// rows [0, n[b]) of every layer's K and V go from the prefill caches to the
+// generate caches, all layers in one launch.  Grid (16-byte vectors of the
+// copied rows / (256 * kCopyVecs), B * Hkv, layers * 2): z = 2 * layer +
+// (0: K, 1: V); a thread moves kCopyVecs vectors, all loads before the
+// stores.  The K planes of kv head 0 also write the layer's mask row of b.
+constexpr int kCopyVecs = 8;
+__global__ void __launch_bounds__(256)
+copy_prefix_kernel(const unsigned char* const* __restrict__ k_src,
+                   const unsigned char* const* __restrict__ v_src,
+                   unsigned char* const* __restrict__ k_dst, unsigned char* const* __restrict__ v_dst,
+                   uint8_t* const* __restrict__ masks, const int32_t* __restrict__ n, int Hkv,
+                   int C_src, int C_dst, int row_bytes, int32_t* dev_status) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int layer = blockIdx.z >> 1, kv = blockIdx.z & 1;
+    const int b = blockIdx.y / Hkv, h = blockIdx.y % Hkv;
+    const bool lead = blockIdx.x == 0 && threadIdx.x == 0;
+    const int nb = n[b];
+    if (nb < 0 || nb > min(C_src, C_dst)) {
+        if (lead && h == 0 && blockIdx.z == 0) report(dev_status, KVD_DEV_POS_RANGE);
+        return;
+    }
+    const unsigned char* src = kv ? v_src[layer] : k_src[layer];
+    unsigned char* dst = kv ? v_dst[layer] : k_dst[layer];
+    if (!src || !dst || ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u)) {
+        if (lead) report(dev_status, KVD_DEV_POINTER);
+        return;
+    }
+    const int vpr = row_bytes / 16;
+    const long long nvec = (long long)nb * vpr;  // this plane's vectors: contiguous in src and dst rows
+    const size_t plane = (size_t)b * Hkv + h;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + plane * C_src * row_bytes);
+    uint4* d4 = reinterpret_cast<uint4*>(dst + plane * C_dst * row_bytes);
+    const long long v0 = (long long)blockIdx.x * blockDim.x * kCopyVecs + threadIdx.x;
+    uint4 x[kCopyVecs];
+#pragma unroll
+    for (int k = 0; k < kCopyVecs; ++k) {
+        const long long v = v0 + (long long)k * blockDim.x;
+        if (v < nvec) x[k] = s4[v];
+    }
+#pragma unroll
+    for (int k = 0; k < kCopyVecs; ++k) {
+        const long long v = v0 + (long long)k * blockDim.x;
+        if (v < nvec) d4[v] = x[k];
+    }
+    if (masks && kv == 0 && h == 0) {
+        uint8_t* m = masks[layer];
+        if (!m) {
+            if (lead) report(dev_status, KVD_DEV_POINTER);
+            return;
+        }
+        const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+        for (long long t = tid; t < C_dst; t += (long long)gridDim.x * blockDim.x)
+            m[(size_t)b * C_dst + t] = t < nb ? 1 : 0;
+    }
+}
+
+cudaError_t launch_copy_prefix(const void* const* k_src, const void* const* v_src,
+                               void* const* k_dst, void* const* v_dst, uint8_t* const* masks,
+                               const int32_t* n, int L, int B, int Hkv, int C_src, int C_dst,
+                               int row_bytes, int32_t* dev_status, cudaStream_t stream) {
+    const long long vecs = (long long)(C_src < C_dst ? C_src : C_dst) * (row_bytes / 16);
+    const long long bx = (vecs + 256 * kCopyVecs - 1) / (256 * kCopyVecs);
+    const dim3 grid((unsigned)(bx < 1 ? 1 : bx), (unsigned)(B * Hkv), (unsigned)(2 * L));
+    return launch_pdl(copy_prefix_kernel, grid, dim3(256), 0, stream,
+                      reinterpret_cast<const unsigned char* const*>(k_src),
+                      reinterpret_cast<const unsigned char* const*>(v_src),
+                      reinterpret_cast<unsigned char* const*>(k_dst),
+                      reinterpret_cast<unsigned char* const*>(v_dst), masks, n, Hkv, C_src, C_dst,
+                      row_bytes, dev_status);
+}
+
 // ------------------------------------------------------------------- append
 // update_kvcache_for ("Intel NPU running LLMs", Part 2): the new token's K and
 // V rows go to slot pos[b] of every kv head; the mask slot is set.  One

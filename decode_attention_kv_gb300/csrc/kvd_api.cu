@@ -296,6 +296,28 @@ kvd_status kvd_append(void* k_cache, void* v_cache, const void* k_new, const voi
     return ok();
 }
 
+kvd_status kvd_copy_prefix(const void* const* k_src, const void* const* v_src, void* const* k_dst,
+                           void* const* v_dst, uint8_t* const* masks, const int32_t* n, int L,
+                           int B, int Hkv, int C_src, int C_dst, int D, kvd_dtype dtype,
+                           int32_t* dev_status, kvd_stream_t stream) {
+    if (!k_src || !v_src || !k_dst || !v_dst || !n)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_copy_prefix: null pointer");
+    if (L < 1 || B < 1 || Hkv < 1 || C_src < 1 || C_dst < 1 || D < 1)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_copy_prefix: sizes must be >= 1");
+    if (!dtype_ok(dtype)) return fail(KVD_ERR_INVALID_ARG, "kvd_copy_prefix: unknown dtype");
+    const long long row = (long long)D * elem_size(dtype);
+    if (row % 16) return fail(KVD_ERR_INVALID_ARG, "kvd_copy_prefix: D*elem must be a multiple of 16 bytes");
+    if (!aligned(k_src, 8) || !aligned(v_src, 8) || !aligned(k_dst, 8) || !aligned(v_dst, 8) ||
+        !aligned(masks, 8) || !aligned(n, 4) || !aligned(dev_status, 4))
+        return fail(KVD_ERR_INVALID_ARG, "kvd_copy_prefix: misaligned pointer");
+    if ((long long)B * Hkv > 65535 || L > 32767)
+        return fail(KVD_ERR_UNSUPPORTED, "kvd_copy_prefix: B*Hkv > 65535 or L > 32767");
+    const cudaError_t e = launch_copy_prefix(k_src, v_src, k_dst, v_dst, masks, n, L, B, Hkv, C_src,
+                                             C_dst, (int)row, dev_status, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvd_copy_prefix launch");
+    return ok();
+}
+
 size_t kvd_attend_masked_workspace_bytes(int B, int Hq, int Hkv, int C, int D, kvd_dtype dtype,
                                          int num_splits) {
     if (B < 1 || C < 1 || check_attention_shape(Hq, Hkv, D, dtype) != KVD_OK) return 0;

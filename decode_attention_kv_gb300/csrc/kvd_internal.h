@@ -51,6 +51,11 @@ cudaError_t launch_combine(const float* part_o, const float* part_lse, void* out
                            float* lse_out, int R, int S, int D, kvd_dtype out_dt,
                            cudaStream_t stream);
 
+cudaError_t launch_copy_prefix(const void* const* k_src, const void* const* v_src,
+                               void* const* k_dst, void* const* v_dst, uint8_t* const* masks,
+                               const int32_t* n, int L, int B, int Hkv, int C_src, int C_dst,
+                               int row_bytes, int32_t* dev_status, cudaStream_t stream);
+
 cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                           const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int row_bytes,
                           int32_t* dev_status, cudaStream_t stream);

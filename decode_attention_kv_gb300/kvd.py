@@ -31,6 +31,7 @@ DEV_TIMEOUT = 32
 _vp, _sz, _i, _f = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
 SIGNATURES = {
     "kvd_append": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp], _i),
+    "kvd_copy_prefix": ([_vp, _vp, _vp, _vp, _vp, _vp] + [_i] * 7 + [_vp, _vp], _i),
     "kvd_attend_masked_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
     "kvd_attend_masked": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz,
                            _vp, _vp], _i),
@@ -127,6 +128,65 @@ def append(k_cache, v_cache, k_new, v_new, pos, mask=None, dev_status=None):
     st = load().kvd_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(pos),
                            _ptr(mask), B, Hkv, C, D, dt, _ptr(dev_status), _stream(k_cache.device))
     _check("kvd_append", st)
+
+
+def pointer_array(tensors, device):
+    """A device int64 tensor holding the data pointers of `tensors` (the
+    pointer arrays of kvd_copy_prefix).  Keep it alive until the call has run."""
+    return torch.tensor([t.data_ptr() for t in tensors], dtype=torch.int64, device=device)
+
+
+class PrefixCopy:
+    """kvd_copy_prefix with its device pointer arrays built once: for every
+    layer l, rows [0, n[b]) of k_src[l] / v_src[l] [B, Hkv, C_src, D] go to
+    k_dst[l] / v_dst[l] [B, Hkv, C_dst, D], and masks[l] [B, C_dst]
+    (optional) become the prefix masks; one launch per run()."""
+
+    def __init__(self, k_src, v_src, k_dst, v_dst, masks=None):
+        L = len(k_src)
+        if not (L == len(v_src) == len(k_dst) == len(v_dst)) or L < 1:
+            raise ValueError("copy_prefix: four lists of the same length >= 1")
+        B, Hkv, C_src, D = k_src[0].shape
+        C_dst = k_dst[0].shape[2]
+        for t in list(k_src) + list(v_src):
+            _cuda_contig("source cache", t)
+            if t.shape != (B, Hkv, C_src, D) or t.dtype != k_src[0].dtype:
+                raise ValueError("copy_prefix: source caches differ in shape or dtype")
+        for t in list(k_dst) + list(v_dst):
+            _cuda_contig("destination cache", t)
+            if t.shape != (B, Hkv, C_dst, D) or t.dtype != k_src[0].dtype:
+                raise ValueError("copy_prefix: destination caches differ in shape or dtype")
+        if masks is not None:
+            if len(masks) != L:
+                raise ValueError("copy_prefix: one mask per layer")
+            for m in masks:
+                _cuda_contig("mask", m)
+                if m.dtype != torch.uint8 or m.shape != (B, C_dst):
+                    raise ValueError("copy_prefix: masks must be uint8 [B, C_dst]")
+        self.dev = k_src[0].device
+        # the tensors stay referenced here, so their memory outlives the pointers
+        self.tensors = (list(k_src), list(v_src), list(k_dst), list(v_dst), masks)
+        self.arrays = [pointer_array(x, self.dev) for x in (k_src, v_src, k_dst, v_dst)]
+        self.marr = pointer_array(masks, self.dev) if masks is not None else None
+        self.sizes = (L, B, Hkv, C_src, C_dst, D)
+        self.dt = _dtype_code(k_src[0])
+
+    def run(self, n, dev_status=None):
+        L, B = self.sizes[0], self.sizes[1]
+        _cuda_contig("n", n)
+        if n.dtype != torch.int32 or n.numel() != B:
+            raise ValueError("copy_prefix: n must be int32 [B]")
+        st = load().kvd_copy_prefix(*(_ptr(a) for a in self.arrays), _ptr(self.marr), _ptr(n),
+                                    *self.sizes, self.dt, _ptr(dev_status), _stream(self.dev))
+        _check("kvd_copy_prefix", st)
+
+
+def copy_prefix(k_src, v_src, k_dst, v_dst, n, masks=None, dev_status=None):
+    """One kvd_copy_prefix call (see PrefixCopy); returns the PrefixCopy,
+    whose pointer arrays must live until the launch has run."""
+    pc = PrefixCopy(k_src, v_src, k_dst, v_dst, masks)
+    pc.run(n, dev_status)
+    return pc
 
 
 # ------------------------------------------------------------------ attention

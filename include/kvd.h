@@ -74,6 +74,7 @@ typedef enum { KVD_BF16 = 0, KVD_F32 = 1 } kvd_dtype;
 #define KVD_DEV_SEQLENS 8u       /* seq_lens not starting at 0, decreasing, or past total */
 #define KVD_DEV_SEQ_OFFSET 16u   /* seq_offset negative or not a multiple of block_size */
 #define KVD_DEV_TIMEOUT 32u      /* a bounded in-kernel wait ran out */
+#define KVD_DEV_POINTER 64u      /* a pointer read from a device pointer array is null or misaligned */
 
 /*
  * kvd_append -- [NPU] Part 2, update_kvcache_for: for every batch entry b
@@ -91,6 +92,31 @@ typedef enum { KVD_BF16 = 0, KVD_F32 = 1 } kvd_dtype;
 kvd_status kvd_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                       const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
                       kvd_dtype dtype, int32_t* dev_status, kvd_stream_t stream);
+
+/*
+ * kvd_copy_prefix -- copy_kvcache, the prefill -> generate hand-over ([NPU]
+ * Part 2 "NPUW 的核心设计", step 3: the prefill model's present K/V are copied
+ * as the slice [0:N] into the generate model's past K/V, capacities 1024 and
+ * 1152, all 32 layers x K and V at once).  For every layer l, batch entry b
+ * and kv head h, rows [0, n[b]) of k_src[l][b, h] and v_src[l][b, h] become
+ * the same rows of k_dst[l][b, h] and v_dst[l][b, h]; rows >= n[b] of the
+ * destination are left alone.  If `masks` is given, masks[l][b, t] becomes
+ * (t < n[b]) for every t < C_dst.
+ *   k_src, v_src  device arrays of L pointers to [B, Hkv, C_src, D] of `dtype`
+ *   k_dst, v_dst  device arrays of L pointers to [B, Hkv, C_dst, D]
+ *   masks         device array of L pointers to [B, C_dst] uint8, or NULL
+ *   n             [B] int32, device
+ * One launch for all layers; a byte copy.  n[b] outside [0, min(C_src,
+ * C_dst)] copies nothing for b (and leaves its masks) and sets
+ * KVD_DEV_POS_RANGE; a null or non-16-byte-aligned pointer in an array skips
+ * that layer and sets KVD_DEV_POINTER.
+ * Errors: INVALID_ARG for null arrays, sizes < 1, D*elem not a multiple of 16
+ * bytes, misaligned arrays; UNSUPPORTED for B*Hkv or L above 65535 / 32767.
+ */
+kvd_status kvd_copy_prefix(const void* const* k_src, const void* const* v_src, void* const* k_dst,
+                           void* const* v_dst, uint8_t* const* masks, const int32_t* n, int L,
+                           int B, int Hkv, int C_src, int C_dst, int D, kvd_dtype dtype,
+                           int32_t* dev_status, kvd_stream_t stream);
 
 /*
  * kvd_attend_masked -- decode attention over the static buffer ([NPU] Part 1
