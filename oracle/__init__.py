@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
             L.kvd_oracle_attend_masked.argtypes = [vp, vp, vp, u8p, ci, ci, ci, ci, ci, ci,
                                                    cd, dp, dp, ci]
             L.kvd_oracle_append.argtypes = [vp, vp, vp, vp, i32p, u8p, ci, ci, ci, ci, ci]
+            L.kvd_oracle_attend_indexed.argtypes = [vp, vp, vp, i32p, ci, ci, ci, ci, ci, ci, ci,
+                                                    cd, dp, dp, ci]
             L.kvd_oracle_copy_prefix.argtypes = [vp, vp, vp, vp, u8p, i32p, ci, ci, ci, ci, ci, ci]
             L.kvd_oracle_gather_paged.argtypes = [vp, vp, i32p, i32p, i32p, vp, vp] + [ci] * 10
             L.kvd_oracle_attend_paged.argtypes = [vp, vp, vp, i32p, i32p, i32p] + [ci] * 8 + [
@@ -82,6 +84,7 @@ def lib() -> ctypes.CDLL:
             L.kvd_oracle_combine.argtypes = [dp, dp, ci, ci, ci, dp, dp]
             L.kvd_oracle_threads.argtypes = []
             for f in (L.kvd_oracle_attend_masked, L.kvd_oracle_append, L.kvd_oracle_copy_prefix,
+                      L.kvd_oracle_attend_indexed,
                       L.kvd_oracle_gather_paged, L.kvd_oracle_attend_paged,
                       L.kvd_oracle_combine, L.kvd_oracle_threads):
                 f.restype = ctypes.c_int
@@ -186,6 +189,32 @@ def attend_masked(q, k, v, mask, scale: float, nthreads: int = 0):
     if rc != 0:
         raise RuntimeError(f"oracle attend_masked failed ({rc})")
     return out, lse
+
+
+def attend_indexed(q, k, v, indices, scale: float, nthreads: int = 0):
+    """Index-list decode attention, fp64: every entry j with 0 <= idx[b, j] <
+    C of indices [B, topk] is one softmax term over k, v [B, Hkv, C, D].
+    Returns (out [B, Hq, D] float64, lse [B, Hq] float64, error bits)."""
+    qa, dt = _storage(q)
+    ka, dk = _storage(k)
+    va, dv = _storage(v)
+    if not (dt == dk == dv):
+        raise TypeError("oracle: q, k, v must share one element type")
+    B, Hq, D = qa.shape
+    _, Hkv, C, Dk = ka.shape
+    if Dk != D or va.shape != ka.shape:
+        raise ValueError("oracle: shape mismatch")
+    idx = _i32(indices).reshape(B, -1)
+    topk = idx.shape[1]
+    out = np.zeros((B, Hq, D), np.float64)
+    lse = np.zeros((B, Hq), np.float64)
+    rc = lib().kvd_oracle_attend_indexed(_p(qa), _p(ka), _p(va), _p(idx, ctypes.c_int32), dt, B,
+                                         Hq, Hkv, C, topk, D, float(scale),
+                                         _p(out, ctypes.c_double), _p(lse, ctypes.c_double),
+                                         int(nthreads))
+    if rc < 0:
+        raise RuntimeError(f"oracle attend_indexed failed ({rc})")
+    return out, lse, rc
 
 
 def append(k_cache, v_cache, k_new, v_new, pos, mask=None) -> int:

@@ -152,6 +152,87 @@ int kvd_oracle_attend_masked(const void* q, const void* k, const void* v,
 }
 
 /*
+ * Index-list decode attention ([FlashMLA] "Математическая постановка": the
+ * indexer's top-k indices pick the KV rows; P = Q . gathered^T,
+ * S = softmax(P * sm_scale), out = S . gathered).
+ *   q [B, Hq, D]; k, v [B, Hkv, C, D]; indices [B, topk] (int32)
+ *   out [B, Hq, D] double; lse [B, Hq] double or NULL
+ * Every list entry j with 0 <= indices[b, j] < C is one term of the softmax
+ * (a repeated index counts once per entry); -1 marks an unused entry; any
+ * other value is skipped and sets ORC_ERR_POS.  No valid entry: out = 0,
+ * lse = -inf.  Returns the error bits (or < 0 on bad sizes / no memory).
+ */
+int kvd_oracle_attend_indexed(const void* q, const void* k, const void* v,
+                              const int32_t* indices, int dtype, int B, int Hq, int Hkv,
+                              int C, int topk, int D, double scale, double* out, double* lse,
+                              int nthreads) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || C < 0 || topk < 0 || D <= 0 || Hq % Hkv) return -1;
+    const int g = Hq / Hkv;
+    const long units = (long)B * Hq;
+    int err = 0;
+    for (long i = 0; i < (long)B * topk; ++i)
+        if (indices[i] < -1 || indices[i] >= C) err |= ORC_ERR_POS;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long u = 0; u < units; ++u) {
+        const int b = (int)(u / Hq), h = (int)(u % Hq), kvh = h / g;
+        double* s = (double*)malloc(sizeof(double) * (topk > 0 ? topk : 1));
+        double* num = (double*)malloc(sizeof(double) * D);
+        if (!s || !num) {
+            free(s);
+            free(num);
+#pragma omp atomic write
+            failed = 1;
+            continue;
+        }
+        const size_t qbase = ((size_t)b * Hq + h) * D;
+        const size_t kvbase = ((size_t)b * Hkv + kvh) * (size_t)C * D;
+        const int32_t* idx = indices + (size_t)b * topk;
+        /* pass 1: scores of the listed rows and their maximum */
+        double m = -INFINITY;
+        long nvalid = 0;
+        for (int j = 0; j < topk; ++j) {
+            const int t = idx[j];
+            if (t < 0 || t >= C) continue;
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += orc_elem(q, qbase + d, dtype) * orc_elem(k, kvbase + (size_t)t * D + d, dtype);
+            s[j] = scale * dot;
+            if (s[j] > m) m = s[j];
+            ++nvalid;
+        }
+        double* o = out + qbase;
+        if (nvalid == 0) {
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            if (lse) lse[(size_t)b * Hq + h] = -INFINITY;
+            free(s);
+            free(num);
+            continue;
+        }
+        /* pass 2: softmax weights and the weighted sum of the listed V rows */
+        double den = 0.0;
+        for (int d = 0; d < D; ++d) num[d] = 0.0;
+        for (int j = 0; j < topk; ++j) {
+            const int t = idx[j];
+            if (t < 0 || t >= C) continue;
+            const double w = exp(s[j] - m);
+            den += w;
+            for (int d = 0; d < D; ++d) num[d] += w * orc_elem(v, kvbase + (size_t)t * D + d, dtype);
+        }
+        for (int d = 0; d < D; ++d) o[d] = num[d] / den;
+        if (lse) lse[(size_t)b * Hq + h] = m + log(den);
+        free(s);
+        free(num);
+    }
+    return failed ? -2 : err;
+}
+
+/*
  * KV append: row pos[b] of every kv head of k_cache / v_cache [B, Hkv, C, D]
  * becomes k_new / v_new [B, Hkv, D]; if mask [B, C] is given its slot
  * pos[b] becomes 1.  A position outside [0, C) writes nothing for that batch

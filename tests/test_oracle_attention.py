@@ -212,3 +212,50 @@ def test_tiny_workload_flow(oracle):
                                                                   dtype=torch.uint8), scale)
         assert np.array_equal(out, ref)
         assert np.abs(out).max() < 10.0
+
+
+# ------------------------------------------------------------ index lists
+
+def test_indexed_with_unique_indices_is_masked_attention(oracle):
+    """FlashMLA on Ascend, 'Математическая постановка': attention over the
+    gathered top-k rows.  With unique indices this is masked attention with
+    the mask that marks exactly those slots (the masked oracle is pinned on
+    its own)."""
+    g = W.generator(41)
+    B, Hq, Hkv, C, D = 2, 4, 2, 50, 8
+    q = W.randn(g, (B, Hq, D), torch.float32)
+    k = W.randn(g, (B, Hkv, C, D), torch.float32)
+    v = W.randn(g, (B, Hkv, C, D), torch.float32)
+    idx = torch.stack([torch.randperm(C, generator=g)[:12] for _ in range(B)]).to(torch.int32)
+    mask = torch.zeros(B, C, dtype=torch.uint8)
+    for b in range(B):
+        mask[b, idx[b].long()] = 1
+    out, lse, err = oracle.attend_indexed(q, k, v, idx, 0.3)
+    ref, ref_lse = oracle.attend_masked(q, k, v, mask, 0.3)
+    assert err == 0
+    assert np.allclose(out, ref, rtol=0, atol=1e-13) and np.allclose(lse, ref_lse, rtol=0, atol=1e-13)
+
+
+def test_indexed_repeats_unused_entries_and_order(oracle):
+    """A repeated entry is one more term (the same as a duplicated K/V row in
+    the gathered matrix), -1 entries are ignored, and the order of the list
+    does not matter; an out-of-range entry is an error and is skipped."""
+    g = W.generator(42)
+    B, Hq, Hkv, C, D = 1, 2, 1, 10, 4
+    q = W.randn(g, (B, Hq, D), torch.float32)
+    k = W.randn(g, (B, Hkv, C, D), torch.float32)
+    v = W.randn(g, (B, Hkv, C, D), torch.float32)
+    idx = torch.tensor([[3, 7, 3, -1]], dtype=torch.int32)
+    out, _, err = oracle.attend_indexed(q, k, v, idx, 0.5)
+    assert err == 0
+    # the gathered matrix written out: rows 3, 7, 3 of the cache at slots 0, 1, 2
+    kg = k[:, :, [3, 7, 3]].contiguous()
+    vg = v[:, :, [3, 7, 3]].contiguous()
+    ref, _ = oracle.attend_masked(q, kg, vg, torch.ones(B, 3, dtype=torch.uint8), 0.5)
+    assert np.allclose(out, ref, rtol=0, atol=1e-13)
+    perm, _, _ = oracle.attend_indexed(q, k, v, torch.tensor([[-1, 3, 3, 7]], dtype=torch.int32), 0.5)
+    assert np.allclose(perm, out, rtol=0, atol=1e-13)
+    bad, _, err = oracle.attend_indexed(q, k, v, torch.tensor([[3, 7, 3, 10]], dtype=torch.int32), 0.5)
+    assert err == oracle.ERR_POS and np.allclose(bad, out, rtol=0, atol=1e-13)
+    empty, lse, _ = oracle.attend_indexed(q, k, v, torch.full((1, 4), -1, dtype=torch.int32), 0.5)
+    assert np.all(empty == 0) and np.all(np.isneginf(lse))
