@@ -4,22 +4,22 @@
 
 namespace kvd {
 
-cudaError_t launch_attend_f32(int D, int G, bool paged, const AttendParams& p,
+cudaError_t launch_attend_f32(int D, int G, int mode, const AttendParams& p,
                               const CUtensorMap* kmap, const CUtensorMap* vmap,
                               cudaStream_t stream) {
     if (D == 128) {
         switch (G) {
-            case 1: return launch_simt<float, 128, 1>(paged, p, kmap, vmap, stream);
-            case 2: return launch_simt<float, 128, 2>(paged, p, kmap, vmap, stream);
-            case 4: return launch_simt<float, 128, 4>(paged, p, kmap, vmap, stream);
-            case 8: return launch_simt<float, 128, 8>(paged, p, kmap, vmap, stream);
+            case 1: return launch_simt<float, 128, 1>(mode, p, kmap, vmap, stream);
+            case 2: return launch_simt<float, 128, 2>(mode, p, kmap, vmap, stream);
+            case 4: return launch_simt<float, 128, 4>(mode, p, kmap, vmap, stream);
+            case 8: return launch_simt<float, 128, 8>(mode, p, kmap, vmap, stream);
         }
     } else if (D == 64) {
         switch (G) {
-            case 1: return launch_simt<float, 64, 1>(paged, p, kmap, vmap, stream);
-            case 2: return launch_simt<float, 64, 2>(paged, p, kmap, vmap, stream);
-            case 4: return launch_simt<float, 64, 4>(paged, p, kmap, vmap, stream);
-            case 8: return launch_simt<float, 64, 8>(paged, p, kmap, vmap, stream);
+            case 1: return launch_simt<float, 64, 1>(mode, p, kmap, vmap, stream);
+            case 2: return launch_simt<float, 64, 2>(mode, p, kmap, vmap, stream);
+            case 4: return launch_simt<float, 64, 4>(mode, p, kmap, vmap, stream);
+            case 8: return launch_simt<float, 64, 8>(mode, p, kmap, vmap, stream);
         }
     }
     return cudaErrorInvalidValue;

@@ -56,12 +56,12 @@ struct DeviceFacts {
     int per_sm[64] = {};  // of them resident on one SM
 };
 
-template <class Cons, int STAGES, int MB, bool PAGED>
+template <class Cons, int STAGES, int MB, int MODE>
 cudaError_t launch_kernel(const AttendParams& p, const CUtensorMap* kmap, const CUtensorMap* vmap,
                           cudaStream_t stream) {
     using Sh = KernelShape<Cons, STAGES, MB>;
     static_assert(Sh::kSmemAlloc <= 227 * 1024, "shared memory of one CTA");
-    auto kern = attend_kernel<Cons, STAGES, MB, PAGED>;
+    auto kern = attend_kernel<Cons, STAGES, MB, MODE>;
     constexpr int kThreads = Sh::kThreads;
     static DeviceFacts facts;
     int dev = 0;
@@ -96,20 +96,31 @@ cudaError_t launch_kernel(const AttendParams& p, const CUtensorMap* kmap, const 
     return launch_pdl(kern, dim3(grid), dim3(kThreads), Sh::kSmemAlloc, stream, q, *kmap, *vmap);
 }
 
+template <class C>
+cudaError_t launch_cfg(int mode, const AttendParams& p, const CUtensorMap* kmap,
+                       const CUtensorMap* vmap, cudaStream_t stream) {
+    using Cons = typename C::Cons;
+    switch (mode) {
+        case kModeMasked:
+            return launch_kernel<Cons, C::STAGES, C::MB, kModeMasked>(p, kmap, vmap, stream);
+        case kModePaged:
+            return launch_kernel<Cons, C::STAGES, C::MB, kModePaged>(p, kmap, vmap, stream);
+        case kModeIndexed:
+            return launch_kernel<Cons, C::STAGES, C::MB, kModeIndexed>(p, kmap, vmap, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
 template <typename Elem, int D, int G>
-cudaError_t launch_simt(bool paged, const AttendParams& p, const CUtensorMap* kmap,
+cudaError_t launch_simt(int mode, const AttendParams& p, const CUtensorMap* kmap,
                         const CUtensorMap* vmap, cudaStream_t stream) {
-    using C = SimtCfg<Elem, D, G>;
-    return paged ? launch_kernel<typename C::Cons, C::STAGES, C::MB, true>(p, kmap, vmap, stream)
-                 : launch_kernel<typename C::Cons, C::STAGES, C::MB, false>(p, kmap, vmap, stream);
+    return launch_cfg<SimtCfg<Elem, D, G>>(mode, p, kmap, vmap, stream);
 }
 
 template <int D, int G>
-cudaError_t launch_mma(bool paged, const AttendParams& p, const CUtensorMap* kmap,
+cudaError_t launch_mma(int mode, const AttendParams& p, const CUtensorMap* kmap,
                        const CUtensorMap* vmap, cudaStream_t stream) {
-    using C = MmaCfg<D, G>;
-    return paged ? launch_kernel<typename C::Cons, C::STAGES, C::MB, true>(p, kmap, vmap, stream)
-                 : launch_kernel<typename C::Cons, C::STAGES, C::MB, false>(p, kmap, vmap, stream);
+    return launch_cfg<MmaCfg<D, G>>(mode, p, kmap, vmap, stream);
 }
 
 }  // namespace kvd

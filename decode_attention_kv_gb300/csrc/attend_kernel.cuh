@@ -59,6 +59,10 @@
 
 namespace kvd {
 
+// Where a row's tokens come from: a static buffer with a 0/1 mask, a paged
+// cache through block tables, or a list of cache slots (top-k indices).
+enum : int { kModeMasked = 0, kModePaged = 1, kModeIndexed = 2 };
+
 constexpr int kMaxChunk = 4096;              // tokens per split, upper bound
 constexpr int kMaxWords = kMaxChunk / 32;    // validity words per split
 constexpr int kMaxBlocks = 128;              // block-table entries per split
@@ -71,6 +75,7 @@ struct AttendParams {
     const int32_t* block_tables; // paged [Q, cols]
     const int32_t* seq_lens;     // paged [Q + 1]
     const int32_t* seq_offset;   // paged [Q] or null
+    const int32_t* indices;      // indexed [B, topk]: cache slots, -1 = unused entry
     void* out;                   // [rows, Hq, D]
     float* lse_out;              // [rows, Hq] or null
     float* part_o;               // [rows * Hq, S, D]       (S > 1)
@@ -79,6 +84,7 @@ struct AttendParams {
     int32_t* dev_status;
     int Hq, Hkv, g, HG;          // g = Hq / Hkv, HG = head groups per kv head
     int C;                       // static buffer capacity
+    int topk;                    // indexed: list entries per batch entry
     int BS, cols, NB;            // paged geometry
     int tile;                    // tokens per ring stage (paged: divides BS)
     int chunk;                   // tokens per split [0, Sb) (multiple of tile and of 32)
@@ -211,7 +217,7 @@ struct SplitRange {
     int t_begin, t_end, ntok, ntiles, first_col;
 };
 
-template <bool PAGED>
+template <int MODE>
 __device__ __forceinline__ SplitRange split_range(const AttendParams& p, int bz, int split,
                                                   bool reporter) {
     SplitRange r;
@@ -219,7 +225,7 @@ __device__ __forceinline__ SplitRange split_range(const AttendParams& p, int bz,
     r.t_begin = big ? split * p.chunk : p.Sb * p.chunk + (split - p.Sb) * p.chunk2;
     const int span = big ? p.chunk : p.chunk2;
     r.first_col = 0;
-    if constexpr (PAGED) {
+    if constexpr (MODE == kModePaged) {
         const int s0 = p.seq_lens[bz], s1 = p.seq_lens[bz + 1];
         const int off = p.seq_offset ? p.seq_offset[bz] : 0;
         int len = s1 - s0;
@@ -241,6 +247,8 @@ __device__ __forceinline__ SplitRange split_range(const AttendParams& p, int bz,
         }
         if (bad && reporter) report(p.dev_status, bad);
         r.t_end = min(len, r.t_begin + span);
+    } else if constexpr (MODE == kModeIndexed) {
+        r.t_end = min(p.topk, r.t_begin + span);  // positions in the index list
     } else {
         r.t_end = min(p.C, r.t_begin + span);
     }
@@ -276,12 +284,30 @@ __device__ __forceinline__ uint32_t nonzero_bytes(uint32_t x) {
 // paged, the physical block of each logical block the split touches.  Writes
 // the words of every tile of the split (bits past the range are 0).  Returns
 // the split's first logical block (paged).
-template <bool PAGED>
+template <int MODE>
 __device__ __forceinline__ int producer_scan(const AttendParams& p, const SplitRange& r, int bz,
                                              int lane, uint32_t* words, int* blocks) {
     const int nwords = (r.ntiles * p.tile + 31) / 32;
     int lb0 = 0;
-    if constexpr (PAGED) {
+    if constexpr (MODE == kModeIndexed) {
+        // blocks[j]: the cache slot of list entry t_begin + j (-1: none); an
+        // entry outside [-1, C) is reported and dropped
+        const int32_t* idx = p.indices + (size_t)bz * p.topk + r.t_begin;
+        for (int j = lane; j < r.ntok; j += 32) {
+            int t = idx[j];
+            if (t < -1 || t >= p.C) {
+                report(p.dev_status, KVD_DEV_POS_RANGE);
+                t = -1;
+            }
+            blocks[j] = t;
+        }
+        __syncwarp();
+        for (int j = 0; j < nwords; ++j) {
+            const int e = 32 * j + lane;
+            const uint32_t w = __ballot_sync(0xffffffffu, e < r.ntok && blocks[e] >= 0);
+            if (lane == 0) words[j] = w;
+        }
+    } else if constexpr (MODE == kModePaged) {
         if (r.ntok > 0) {
             lb0 = r.t_begin / p.BS;
             const int nblk = (r.t_end - 1) / p.BS - lb0 + 1;
@@ -413,7 +439,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
 }
 
 
-template <class Cons, int STAGES, int MB, bool PAGED>
+template <class Cons, int STAGES, int MB, int MODE>
 __global__ void __launch_bounds__(KernelShape<Cons, STAGES, MB>::kThreads)
 attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
               const __grid_constant__ CUtensorMap vmap) {
@@ -447,6 +473,8 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
         *ctl.pending = 0;
         fence_barrier_init();
     }
+    constexpr bool PAGED = MODE == kModePaged;
+    constexpr bool INDEXED = MODE == kModeIndexed;
     if (threadIdx.x == 32 * kLoader && (PAGED || Cons::kSwizzled)) {
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
@@ -523,9 +551,9 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                 break;
             }
             const Unit un = decode_unit(p, G, u);
-            const SplitRange r = split_range<PAGED>(
+            const SplitRange r = split_range<MODE>(
                 p, un.bz, un.split, lane == 0 && un.split == 0 && un.kvh == 0 && un.hg == 0);
-            const int lb0 = producer_scan<PAGED>(p, r, un.bz, lane, sl.words, sl.blocks);
+            const int lb0 = producer_scan<MODE>(p, r, un.bz, lane, sl.words, sl.blocks);
             int last = -1;
             for (int i = r.ntiles - 1; i >= 0; --i)
                 if (tile_bits(sl.words, i * p.tile, min(p.tile, r.ntok - i * p.tile))) {
@@ -691,7 +719,9 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                     const int t0 = t_begin + r0;
                     const uint32_t qbytes = first ? (uint32_t)(un.g_here * D * sizeof(Elem)) : 0u;
                     uint32_t kvbytes;
-                    if constexpr (Cons::kSwizzled) {
+                    if constexpr (INDEXED) {
+                        kvbytes = 2u * (uint32_t)__popcll(bits) * D * sizeof(Elem);  // listed rows
+                    } else if constexpr (Cons::kSwizzled) {
                         kvbytes = 2u * kHalves * p.tile * 128u;  // whole boxes
                     } else if constexpr (PAGED) {
                         kvbytes = 2u * p.tile * D * sizeof(Elem);
@@ -699,7 +729,9 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                         kvbytes = 2u * n * D * sizeof(Elem);
                     }
                     mbar_arrive_expect_tx(&ctl.full[stage], kvbytes + qbytes);
-                    if constexpr (PAGED) {
+                    if constexpr (INDEXED) {
+                        // the rows are copied by all lanes below
+                    } else if constexpr (PAGED) {
                         const int row = sl.blocks[t0 / p.BS - lb0] * p.BS + t0 % p.BS;
                         if constexpr (Cons::kSwizzled) {
 #pragma unroll
@@ -738,6 +770,34 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                 }
                 __syncwarp();
+                if constexpr (INDEXED) {
+                    // Gather: lane j copies the listed rows j, j + 32, ... of the
+                    // tile (one row per copy; tensor-core layout: one 64-column
+                    // box of one row per half, landing in its swizzled place)
+                    unsigned char* sk = smem + stage * Sh::kStageBytes;
+                    unsigned char* sv = sk + Cons::kTileBytes;
+                    const size_t plane = ((size_t)un.bz * p.Hkv + un.kvh) * p.C;
+                    for (int rr = lane; rr < n; rr += 32) {
+                        if (!((bits >> rr) & 1ull)) continue;
+                        const size_t rowidx = plane + (size_t)sl.blocks[r0 + rr];
+                        if constexpr (Cons::kSwizzled) {
+#pragma unroll
+                            for (int h = 0; h < kHalves; ++h) {
+                                tma_g2s_2d(sk + h * Cons::kTileBytes / kHalves + rr * 128, &kmap,
+                                           64 * h, (int)rowidx, &ctl.full[stage], pol);
+                                tma_g2s_2d(sv + h * Cons::kTileBytes / kHalves + rr * 128, &vmap,
+                                           64 * h, (int)rowidx, &ctl.full[stage], pol);
+                            }
+                        } else {
+                            const uint32_t bytes = (uint32_t)D * sizeof(Elem);
+                            bulk_g2s(sk + rr * bytes, static_cast<const Elem*>(p.k) + rowidx * D,
+                                     bytes, &ctl.full[stage], pol);
+                            bulk_g2s(sv + rr * bytes, static_cast<const Elem*>(p.v) + rowidx * D,
+                                     bytes, &ctl.full[stage], pol);
+                        }
+                    }
+                    __syncwarp();
+                }
                 first = false;
                 advance();
             }

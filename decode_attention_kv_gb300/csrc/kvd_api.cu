@@ -12,10 +12,10 @@
 #include "kvd_internal.h"
 
 namespace kvd {
-cudaError_t launch_attend_bf16(int D, int G, bool paged, const AttendParams& p,
+cudaError_t launch_attend_bf16(int D, int G, int mode, const AttendParams& p,
                                const CUtensorMap* kmap, const CUtensorMap* vmap,
                                cudaStream_t stream);
-cudaError_t launch_attend_f32(int D, int G, bool paged, const AttendParams& p,
+cudaError_t launch_attend_f32(int D, int G, int mode, const AttendParams& p,
                               const CUtensorMap* kmap, const CUtensorMap* vmap,
                               cudaStream_t stream);
 AttendGeom attend_geom_bf16(int D, int G);
@@ -97,10 +97,11 @@ AttendGeom geom(kvd_dtype dt, int D, int G) {
     return dt == KVD_BF16 ? attend_geom_bf16(D, G) : attend_geom_f32(D, G);
 }
 
-// rows: batch entries (or sequences); cap: most tokens a row can hold;
-// BS > 0 for the paged layout.
+// rows: batch entries (or sequences); cap: most tokens a row can hold (the
+// list length for index lists); BS > 0 for the paged layout; `indexed`: a
+// split holds at most kMaxBlocks list entries (their slots travel with it).
 Plan plan_attention(int rows, int Hq, int Hkv, int cap, int D, kvd_dtype dt, int BS,
-                    int num_splits) {
+                    int num_splits, bool indexed = false) {
     Plan pl{};
     const int g = Hq / Hkv;
     pl.G = group_width(g);
@@ -118,6 +119,10 @@ Plan plan_attention(int rows, int Hq, int Hkv, int cap, int D, kvd_dtype dt, int
     if (BS > 0) {
         const long long by_blocks = (long long)(kMaxBlocks - 2) * BS / unit * unit;
         if (by_blocks < max_chunk) max_chunk = by_blocks;
+    }
+    if (indexed) {
+        const long long by_list = (long long)kMaxBlocks / unit * unit;
+        if (by_list < max_chunk) max_chunk = by_list;
     }
     if (max_chunk < unit) max_chunk = unit;
     const long long row_units = (long long)rows * Hkv * pl.HG;
@@ -234,10 +239,10 @@ kvd_status make_cache_map(CUtensorMap* map, const void* cache, kvd_dtype dt, boo
     return KVD_OK;
 }
 
-cudaError_t launch_attend(kvd_dtype dt, int D, int G, bool paged, const AttendParams& p,
+cudaError_t launch_attend(kvd_dtype dt, int D, int G, int mode, const AttendParams& p,
                           const CUtensorMap* kmap, const CUtensorMap* vmap, cudaStream_t s) {
-    return dt == KVD_BF16 ? launch_attend_bf16(D, G, paged, p, kmap, vmap, s)
-                          : launch_attend_f32(D, G, paged, p, kmap, vmap, s);
+    return dt == KVD_BF16 ? launch_attend_bf16(D, G, mode, p, kmap, vmap, s)
+                          : launch_attend_f32(D, G, mode, p, kmap, vmap, s);
 }
 
 kvd_status check_attention_shape(int Hq, int Hkv, int D, kvd_dtype dt) {
@@ -369,12 +374,74 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
         st = make_cache_map(&vmap, v_cache, dtype, false, rows, Hkv, D, pl.tile, true);
         if (st != KVD_OK) return st;
     }
-    cudaError_t e = launch_attend(dtype, D, pl.G, false, p, &kmap, &vmap, (cudaStream_t)stream);
+    cudaError_t e = launch_attend(dtype, D, pl.G, kModeMasked, p, &kmap, &vmap, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked launch");
     if (pl.S > 1) {
         e = launch_combine(p.part_o, p.part_lse, out, lse_out, B * Hq, pl.S, D, dtype,
                            (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked combine launch");
+    }
+    return ok();
+}
+
+size_t kvd_attend_indexed_workspace_bytes(int B, int Hq, int Hkv, int topk, int D,
+                                          kvd_dtype dtype, int num_splits) {
+    if (B < 1 || topk < 1 || check_attention_shape(Hq, Hkv, D, dtype) != KVD_OK) return 0;
+    return plan_attention(B, Hq, Hkv, topk, D, dtype, 0, num_splits, true).ws;
+}
+
+kvd_status kvd_attend_indexed(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* indices, void* out, float* lse_out, int B, int Hq,
+                              int Hkv, int C, int topk, int D, float scale, kvd_dtype dtype,
+                              int num_splits, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_status, kvd_stream_t stream) {
+    kvd_status st = check_attention_shape(Hq, Hkv, D, dtype);
+    if (st != KVD_OK) return st;
+    if (B < 0 || C < 1 || topk < 1)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_indexed: B >= 0, C >= 1 and topk >= 1 required");
+    if (B == 0) return ok();
+    if (!q || !k_cache || !v_cache || !indices || !out)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_indexed: null pointer");
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(indices, 4) || !aligned(lse_out, 4) || !aligned(dev_status, 4))
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_indexed: misaligned pointer");
+    if (num_splits < 0) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_indexed: num_splits < 0");
+    const long long rows = (long long)B * Hkv * C;
+    if (rows >= (1ll << 31)) return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_indexed: B*Hkv*C >= 2^31 rows");
+    const Plan pl = plan_attention(B, Hq, Hkv, topk, D, dtype, 0, num_splits, true);
+    st = check_workspace("kvd_attend_indexed", pl, workspace, workspace_bytes);
+    if (st != KVD_OK) return st;
+    AttendParams p{};
+    p.q = q;
+    p.k = k_cache;
+    p.v = v_cache;
+    p.indices = indices;
+    p.out = out;
+    p.lse_out = lse_out;
+    p.dev_status = dev_status;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.g = Hq / Hkv;
+    p.C = C;
+    p.topk = topk;
+    p.qscale = scale * kLog2e;
+    attach_workspace(p, pl, workspace);
+    CUtensorMap kmap, vmap;
+    std::memset(&kmap, 0, sizeof kmap);
+    std::memset(&vmap, 0, sizeof vmap);
+    if (attend_uses_mma(dtype, pl.G)) {
+        // one row per box: the listed rows are gathered one by one
+        st = make_cache_map(&kmap, k_cache, dtype, false, rows, Hkv, D, 1, true);
+        if (st != KVD_OK) return st;
+        st = make_cache_map(&vmap, v_cache, dtype, false, rows, Hkv, D, 1, true);
+        if (st != KVD_OK) return st;
+    }
+    cudaError_t e = launch_attend(dtype, D, pl.G, kModeIndexed, p, &kmap, &vmap, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_indexed launch");
+    if (pl.S > 1) {
+        e = launch_combine(p.part_o, p.part_lse, out, lse_out, B * Hq, pl.S, D, dtype,
+                           (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_indexed combine launch");
     }
     return ok();
 }
@@ -430,7 +497,7 @@ kvd_status kvd_attend_paged(const void* q_in, const void* key_cache, const void*
     p.NB = NB;
     p.qscale = scale * kLog2e;
     attach_workspace(p, pl, workspace);
-    cudaError_t e = launch_attend(dtype, D, pl.G, true, p, &kmap, &vmap, (cudaStream_t)stream);
+    cudaError_t e = launch_attend(dtype, D, pl.G, kModePaged, p, &kmap, &vmap, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_paged launch");
     if (pl.S > 1) {
         e = launch_combine(p.part_o, p.part_lse, out, lse_out, Q * Hq, pl.S, D, dtype,

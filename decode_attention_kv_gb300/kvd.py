@@ -37,6 +37,9 @@ SIGNATURES = {
                            _vp, _vp], _i),
     "kvd_attend_masked_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i,
                                    _vp, _vp], _i),
+    "kvd_attend_indexed_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
+    "kvd_attend_indexed": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp,
+                            _sz, _vp, _vp], _i),
     "kvd_attend_paged_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i, _i], _sz),
     "kvd_attend_paged": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
                           _i, _i, _vp, _sz, _vp, _vp], _i),
@@ -245,6 +248,49 @@ def attend_masked(q, k_cache, v_cache, mask, scale=None, out=None, lse=None, num
                              _ptr(lse), B, Hq, Hkv, C, D, float(scale), dt, num_splits, _ptr(ws),
                              wsb, _ptr(dev_status), _stream(q.device))
     _check("kvd_attend_masked", st)
+    return out
+
+
+def attend_indexed_workspace_bytes(B, Hq, Hkv, topk, D, dtype=torch.bfloat16, num_splits=0):
+    return load().kvd_attend_indexed_workspace_bytes(B, Hq, Hkv, topk, D,
+                                                     BF16 if dtype == torch.bfloat16 else F32,
+                                                     num_splits)
+
+
+def attend_indexed(q, k_cache, v_cache, indices, scale=None, out=None, lse=None, num_splits=0,
+                   workspace=None, dev_status=None):
+    """kvd_attend_indexed: decode attention over the cache slots listed in
+    indices [B, topk] int32 (-1 = unused entry).
+
+    q [B, Hq, D]; k_cache, v_cache [B, Hkv, C, D].  Returns out [B, Hq, D];
+    fills ``lse`` [B, Hq] fp32 if given.
+    """
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("indices", indices)):
+        _cuda_contig(n, t)
+    B, Hq, D = q.shape
+    Bk, Hkv, C, Dk = k_cache.shape
+    if Bk != B or Dk != D or v_cache.shape != k_cache.shape or indices.dim() != 2 or \
+            indices.shape[0] != B:
+        raise ValueError("attend_indexed: shape mismatch")
+    if indices.dtype != torch.int32:
+        raise ValueError("attend_indexed: indices must be int32")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("attend_indexed: q and caches must share a dtype")
+    topk = indices.shape[1]
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is not None:
+        _cuda_contig("lse", lse)
+    L = load()
+    need = L.kvd_attend_indexed_workspace_bytes(B, Hq, Hkv, topk, D, dt, num_splits)
+    ws, wsb = _workspace(need, q.device, workspace)
+    st = L.kvd_attend_indexed(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(indices), _ptr(out),
+                              _ptr(lse), B, Hq, Hkv, C, topk, D, float(scale), dt, num_splits,
+                              _ptr(ws), wsb, _ptr(dev_status), _stream(q.device))
+    _check("kvd_attend_indexed", st)
     return out
 
 

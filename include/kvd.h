@@ -175,6 +175,32 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
  * TMA tensor map (NB*BS < 2^31).
  */
 /*
+ * kvd_attend_indexed -- decode attention over a list of cache slots per batch
+ * entry ([FlashMLA] "Математическая постановка": the indexer's top-k indices
+ * pick the KV rows, P = Q . gathered^T, S = softmax(P * sm_scale),
+ * out = S . gathered):
+ *   out[b, h, :] = sum_j w_j v[b, h/g, indices[b, j], :] / sum_j w_j,
+ *   w_j = exp(scale * q[b, h, :] . k[b, h/g, indices[b, j], :] - max), over
+ *   the entries j with 0 <= indices[b, j] < C.
+ *   q [B, Hq, D]; k_cache, v_cache [B, Hkv, C, D]; indices [B, topk] int32,
+ *   device (-1 = unused entry); out [B, Hq, D]; lse_out [B, Hq] float or NULL
+ * Every entry is one term of the softmax (a repeated slot counts once per
+ * entry; the list order does not matter).  An entry outside [-1, C) is
+ * skipped and sets KVD_DEV_POS_RANGE.  No valid entry: out = 0, lse = -inf.
+ * The list is cut into splits of at most 128 entries that the persistent grid
+ * takes from its work counter; the listed rows are gathered row by row.
+ * Workspace, num_splits and dtypes as for kvd_attend_masked (the list length
+ * topk takes the place of the capacity).
+ */
+size_t kvd_attend_indexed_workspace_bytes(int B, int Hq, int Hkv, int topk, int D,
+                                          kvd_dtype dtype, int num_splits);
+kvd_status kvd_attend_indexed(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* indices, void* out, float* lse_out, int B, int Hq,
+                              int Hkv, int C, int topk, int D, float scale, kvd_dtype dtype,
+                              int num_splits, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_status, kvd_stream_t stream);
+
+/*
  * kvd_attend_masked_noalloc -- the pages have no counterpart to this call; it
  * exists for callers that cannot allocate device memory.  Some host runtimes
  * own all device memory through their own allocator and hand a kernel library
