@@ -433,9 +433,79 @@ class PagedBench:
                       f"{L2_BYTES // 2**20} MiB L2"}
 
 
+def index_lists(torch, lengths, topk, seed=7):
+    """[B, topk] int32: per entry, min(topk, L) unique slots drawn from its
+    valid prefix [0, L) (seeded), -1 after them."""
+    import workloads
+    g = workloads.generator(seed, "cpu")
+    rows = []
+    for L in lengths:
+        n = min(topk, L)
+        r = torch.full((topk,), -1, dtype=torch.int32)
+        r[:n] = torch.randperm(L, generator=g)[:n].to(torch.int32)
+        rows.append(r)
+    return torch.stack(rows)
+
+
+class IndexedBench(MaskedBench):
+    """Top-k sparse decode on the batched-GQA caches: every layer appends the
+    step's K/V row, then attends over 2048 slots per batch entry drawn once
+    (seeded, unique, from the entry's valid prefix; -1 pads a shorter
+    prefix) -- the index-list attention of sparse (top-k) attention."""
+
+    TOPK = 2048
+
+    def __init__(self, torch, kvd, dev, layers=None):
+        super().__init__("gqa", torch, kvd, dev, layers)
+        self.name = "indexed"
+        self.indices = index_lists(torch, self.lengths0, self.TOPK).to(dev)
+        self.listed = [min(self.TOPK, L) for L in self.lengths0]
+        need = kvd.attend_indexed_workspace_bytes(self.B, self.Hq, self.Hkv, self.TOPK, self.D)
+        self.ws = kvd.workspace(need, dev)
+
+    def _layer(self, li, lay, pos):
+        self.kvd.append(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, pos, None, self.status)
+        self.kvd.attend_indexed(lay.q, lay.k_cache, lay.v_cache, self.indices, lay.scale,
+                                out=self.out[li], workspace=self.ws, dev_status=self.status)
+
+    def eager_run(self, j, timing=False):
+        torch, kvd = self.torch, self.kvd
+        pos = self.pos_table[j % self.cycle]
+        evs = []
+        for li, lay in enumerate(self.w.layers):
+            if timing:
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                e[0].record()
+            kvd.append(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, pos, None, self.status)
+            if timing:
+                e[1].record()
+            kvd.attend_indexed(lay.q, lay.k_cache, lay.v_cache, self.indices, lay.scale,
+                               out=self.out[li], workspace=self.ws, dev_status=self.status)
+            if timing:
+                e[2].record()
+                evs += [("append", e[0], e[1]), ("attend", e[1], e[2])]
+        return evs
+
+    def attend_bytes(self, j):
+        """Listed K and V rows of every kv head, the index lists, q and out."""
+        return (sum(self.listed) * self.Hkv * self.D * 2 * self.elem + self.B * self.TOPK * 4
+                + 2 * self.B * self.Hq * self.D * self.elem)
+
+    def copy_setup(self):
+        return False
+
+    def config(self):
+        c = super().config()
+        c.update({"workload": "indexed", "topk": self.TOPK,
+                  "listed_per_entry": {"min": min(self.listed), "max": max(self.listed)}})
+        return c
+
+
 def make_bench(name, torch, kvd, dev, layers=None):
     if name == "paged":
         return PagedBench(torch, kvd, dev)
+    if name == "indexed":
+        return IndexedBench(torch, kvd, dev, layers)
     return MaskedBench(name, torch, kvd, dev, layers)
 
 
@@ -624,6 +694,24 @@ def oracle_rate(name, seconds, W_mod=None):
                 break
         return done_bytes / el / 1e9, oracle.threads(), f"{n} sequences of the paged workload " \
             f"(gather + paged attention), {el:.1f} s"
+    if name == "indexed":
+        w = workloads.gqa(device="cpu", layers=1)
+        lay = w.layers[0]
+        topk = IndexedBench.TOPK
+        L = [int(x) for x in lay.lengths]
+        idx = index_lists(torch, L, topk)
+        per = (sum(min(topk, x) for x in L) * w.Hkv * w.D * 2 * 2 + w.B * topk * 4
+               + 2 * w.B * w.Hq * w.D * 2)
+        done_bytes, t0, n = 0, time.perf_counter(), 0
+        while True:
+            oracle.attend_indexed(lay.q, lay.k_cache, lay.v_cache, idx, lay.scale)
+            done_bytes += per
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+        return done_bytes / el / 1e9, oracle.threads(), \
+            f"{n} layers of index-list attention (gqa caches, top-{topk}), {el:.1f} s"
     if name == "npuw":
         w = workloads.npuw(device="cpu", layers=4)
     elif name == "gqa":
@@ -690,7 +778,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvd", choices=["kvd", "reference"])
-    ap.add_argument("--workload", default="npuw", choices=["npuw", "gqa", "long", "paged"])
+    ap.add_argument("--workload", default="npuw",
+                    choices=["npuw", "gqa", "long", "paged", "indexed"])
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true",
@@ -753,7 +842,7 @@ def main():
 
     others = {}
     if not args.no_others:
-        for name in ("gqa", "long", "paged", "npuw"):
+        for name in ("gqa", "long", "paged", "indexed", "npuw"):
             if name == args.workload:
                 continue
             log(f"workload {name}")
