@@ -475,7 +475,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
     }
     constexpr bool PAGED = MODE == kModePaged;
     constexpr bool INDEXED = MODE == kModeIndexed;
-    if (threadIdx.x == 32 * kLoader && (PAGED || Cons::kSwizzled)) {
+    if (threadIdx.x == 32 * kLoader && (PAGED || Cons::kSwizzled) && !INDEXED) {
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
     }
@@ -705,6 +705,45 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                 const uint64_t bits = tile_bits(sl.words, r0, n);
                 if (!bits) continue;  // all-zero tile: never read
                 if (!acquire()) break;
+                if constexpr (INDEXED) {
+                    // Gather the tile's listed rows: 16-byte cp.async copies, a
+                    // warp pass covering 32 / cpr whole rows (K and V), each chunk
+                    // landing where the consumer's layout puts it.  The stage's
+                    // full barrier waits for them through the cp.async arrival,
+                    // made before lane 0's own arrival below.  (Per-row TMA
+                    // boxes, four rows per box at best, issue too slowly here:
+                    // the tensor engine's per-copy cost bounds a 512-byte box.)
+                    unsigned char* gk = smem + stage * Sh::kStageBytes;
+                    unsigned char* gv = gk + Cons::kTileBytes;
+                    constexpr int cpr = D * (int)sizeof(Elem) / 16, rpi = 32 / cpr;
+                    constexpr int epc = 16 / (int)sizeof(Elem);  // elements per chunk
+                    const int c = lane % cpr;
+                    const size_t plane = ((size_t)un.bz * p.Hkv + un.kvh) * p.C;
+                    const Elem* kb = static_cast<const Elem*>(p.k) + plane * D + c * epc;
+                    const Elem* vb = static_cast<const Elem*>(p.v) + plane * D + c * epc;
+                    // slots of tile rows lane and lane + 32 (-1: unlisted or past the tile)
+                    const int s_lo = lane < n && ((bits >> lane) & 1ull) ? sl.blocks[r0 + lane] : -1;
+                    const int s_hi = lane + 32 < n && ((bits >> (lane + 32)) & 1ull)
+                                         ? sl.blocks[r0 + lane + 32] : -1;
+#pragma unroll 4
+                    for (int rb = 0; rb < n; rb += rpi) {
+                        const int row = rb + lane / cpr;
+                        const int a = __shfl_sync(0xffffffffu, s_lo, row & 31);
+                        const int b = __shfl_sync(0xffffffffu, s_hi, row & 31);
+                        const int slot_row = row < 32 ? a : b;
+                        if (row < n && slot_row >= 0) {
+                            uint32_t off;
+                            if constexpr (Cons::kSwizzled)
+                                off = (c >> 3) * (Cons::kTileBytes / kHalves) + swz128(row, c & 7);
+                            else
+                                off = row * D * (int)sizeof(Elem) + c * 16;
+                            cp_async16(gk + off, kb + (size_t)slot_row * D, pol);
+                            cp_async16(gv + off, vb + (size_t)slot_row * D, pol);
+                        }
+                    }
+                    cp_async_mbar_arrive(&ctl.full[stage]);
+                    __syncwarp();
+                }
                 if (lane == 0) {
                     atomicAdd(ctl.pending, -(i + 1 - counted) * p.tile);
                     counted = i + 1;
@@ -720,7 +759,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                     const uint32_t qbytes = first ? (uint32_t)(un.g_here * D * sizeof(Elem)) : 0u;
                     uint32_t kvbytes;
                     if constexpr (INDEXED) {
-                        kvbytes = 2u * (uint32_t)__popcll(bits) * D * sizeof(Elem);  // listed rows
+                        kvbytes = 0u;  // the listed rows were gathered above (cp.async)
                     } else if constexpr (Cons::kSwizzled) {
                         kvbytes = 2u * kHalves * p.tile * 128u;  // whole boxes
                     } else if constexpr (PAGED) {
@@ -730,7 +769,6 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                     }
                     mbar_arrive_expect_tx(&ctl.full[stage], kvbytes + qbytes);
                     if constexpr (INDEXED) {
-                        // the rows are copied by all lanes below
                     } else if constexpr (PAGED) {
                         const int row = sl.blocks[t0 / p.BS - lb0] * p.BS + t0 % p.BS;
                         if constexpr (Cons::kSwizzled) {
@@ -770,34 +808,6 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                     last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                 }
                 __syncwarp();
-                if constexpr (INDEXED) {
-                    // Gather: lane j copies the listed rows j, j + 32, ... of the
-                    // tile (one row per copy; tensor-core layout: one 64-column
-                    // box of one row per half, landing in its swizzled place)
-                    unsigned char* sk = smem + stage * Sh::kStageBytes;
-                    unsigned char* sv = sk + Cons::kTileBytes;
-                    const size_t plane = ((size_t)un.bz * p.Hkv + un.kvh) * p.C;
-                    for (int rr = lane; rr < n; rr += 32) {
-                        if (!((bits >> rr) & 1ull)) continue;
-                        const size_t rowidx = plane + (size_t)sl.blocks[r0 + rr];
-                        if constexpr (Cons::kSwizzled) {
-#pragma unroll
-                            for (int h = 0; h < kHalves; ++h) {
-                                tma_g2s_2d(sk + h * Cons::kTileBytes / kHalves + rr * 128, &kmap,
-                                           64 * h, (int)rowidx, &ctl.full[stage], pol);
-                                tma_g2s_2d(sv + h * Cons::kTileBytes / kHalves + rr * 128, &vmap,
-                                           64 * h, (int)rowidx, &ctl.full[stage], pol);
-                            }
-                        } else {
-                            const uint32_t bytes = (uint32_t)D * sizeof(Elem);
-                            bulk_g2s(sk + rr * bytes, static_cast<const Elem*>(p.k) + rowidx * D,
-                                     bytes, &ctl.full[stage], pol);
-                            bulk_g2s(sv + rr * bytes, static_cast<const Elem*>(p.v) + rowidx * D,
-                                     bytes, &ctl.full[stage], pol);
-                        }
-                    }
-                    __syncwarp();
-                }
                 first = false;
                 advance();
             }

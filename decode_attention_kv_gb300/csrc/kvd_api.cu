@@ -406,8 +406,6 @@ kvd_status kvd_attend_indexed(const void* q, const void* k_cache, const void* v_
         !aligned(indices, 4) || !aligned(lse_out, 4) || !aligned(dev_status, 4))
         return fail(KVD_ERR_INVALID_ARG, "kvd_attend_indexed: misaligned pointer");
     if (num_splits < 0) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_indexed: num_splits < 0");
-    const long long rows = (long long)B * Hkv * C;
-    if (rows >= (1ll << 31)) return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_indexed: B*Hkv*C >= 2^31 rows");
     const Plan pl = plan_attention(B, Hq, Hkv, topk, D, dtype, 0, num_splits, true);
     st = check_workspace("kvd_attend_indexed", pl, workspace, workspace_bytes);
     if (st != KVD_OK) return st;
@@ -426,16 +424,9 @@ kvd_status kvd_attend_indexed(const void* q, const void* k_cache, const void* v_
     p.topk = topk;
     p.qscale = scale * kLog2e;
     attach_workspace(p, pl, workspace);
-    CUtensorMap kmap, vmap;
+    CUtensorMap kmap, vmap;  // unused: the kernel gathers the listed rows with cp.async
     std::memset(&kmap, 0, sizeof kmap);
     std::memset(&vmap, 0, sizeof vmap);
-    if (attend_uses_mma(dtype, pl.G)) {
-        // one row per box: the listed rows are gathered one by one
-        st = make_cache_map(&kmap, k_cache, dtype, false, rows, Hkv, D, 1, true);
-        if (st != KVD_OK) return st;
-        st = make_cache_map(&vmap, v_cache, dtype, false, rows, Hkv, D, 1, true);
-        if (st != KVD_OK) return st;
-    }
     cudaError_t e = launch_attend(dtype, D, pl.G, kModeIndexed, p, &kmap, &vmap, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_indexed launch");
     if (pl.S > 1) {

@@ -139,6 +139,20 @@ __device__ __forceinline__ void tma_g2s_2d(void* dst, const CUtensorMap* map, in
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L1 (cp.async, cached in
+// L2 only) under an L2 policy.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)),
+                 "l"(src), "l"(policy)
+                 : "memory");
+}
+
+// The mbarrier's current phase also waits for this thread's cp.async copies
+// issued so far (the arrival count is raised now and lowered when they land).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -188,7 +188,8 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
  * entry; the list order does not matter).  An entry outside [-1, C) is
  * skipped and sets KVD_DEV_POS_RANGE.  No valid entry: out = 0, lse = -inf.
  * The list is cut into splits of at most 128 entries that the persistent grid
- * takes from its work counter; the listed rows are gathered row by row.
+ * takes from its work counter; the listed rows are gathered into shared
+ * memory with 16-byte cp.async copies.
  * Workspace, num_splits and dtypes as for kvd_attend_masked (the list length
  * topk takes the place of the capacity).
  */
