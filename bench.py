@@ -2,7 +2,8 @@
 """Decode-attention benchmark: KV GB/s, fraction of the HBM roofline, and
 decode tokens/s on GB300, through libkvd's C ABI.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload npuw|gqa|long|paged]
+    python bench.py [--gpus N] [--steps K] [--warmup W]
+                    [--workload npuw|gqa|long|paged|indexed|window]
     python bench.py --impl reference ...     # the fp64 CPU oracle as the reference arm
 
 A step is one decode step of the workload: for the static-buffer workloads,
@@ -14,9 +15,10 @@ split scratch), whole job over all ranks.  Multi-GPU runs are independent
 replicas (weak scaling, no data-path collective).
 
 Besides the main line (the 1152-slot NPUW-default buffer by default), the
-JSON carries the same measurement for the other workloads under "workloads"
-(batched GQA, paged, long context), which are the ones the 75 % HBM gate is
-stated on.
+JSON carries the same measurement for the other workloads under "workloads":
+batched GQA, paged and long context (the ones the 75 % HBM gate is stated
+on), top-k index lists over the GQA caches and a 4096-slot sliding window over
+the long-context caches.
 """
 from __future__ import annotations
 
@@ -183,6 +185,9 @@ class MaskedBench:
         elif name == "long":
             w = workloads.long(device=dev, **kw)
             self.cycle, self.prompt = 1, None
+        elif name == "window":
+            w = workloads.window(device=dev, **kw)
+            self.cycle, self.prompt = 1, None
         else:
             raise ValueError(name)
         self.w = w
@@ -286,8 +291,13 @@ class MaskedBench:
     def lengths_at(self, j):
         return [L + (j % self.cycle) for L in self.lengths0]
 
+    def rows_at(self, j):
+        """Rows each batch entry attends to (the window's, if it has one)."""
+        L = self.lengths_at(j)
+        return [min(x, self.w.window) for x in L] if self.w.window else L
+
     def attend_bytes(self, j):
-        return masked_attend_bytes(self.lengths_at(j), self.Hq, self.Hkv, self.C, self.D, self.elem)
+        return masked_attend_bytes(self.rows_at(j), self.Hq, self.Hkv, self.C, self.D, self.elem)
 
     def step_bytes(self, j):
         return self.layers * (self.attend_bytes(j) + append_bytes(self.B, self.Hkv, self.D, self.elem))
@@ -327,7 +337,15 @@ class MaskedBench:
                 "valid_len_step0": (L if len(L) <= 4 else
                                     {"min": min(L), "max": max(L), "mean": sum(L) / len(L)}),
                 "l2": f"inputs larger than L2: {cache / 2**30:.2f} GiB of layer caches rotated "
-                      f"per step vs {L2_BYTES // 2**20} MiB L2"}
+                      f"per step vs {L2_BYTES // 2**20} MiB L2"} | self._window_config()
+
+    def _window_config(self):
+        if not self.w.window:
+            return {}
+        rows = self.layers * 2 * self.Hkv * sum(self.rows_at(0)) * self.D * self.elem
+        return {"window": self.w.window,
+                "l2": f"inputs larger than L2: the windows' K/V rows of the {self.layers} layers "
+                      f"read per step are {rows / 2**20:.0f} MiB vs {L2_BYTES // 2**20} MiB L2"}
 
 
 class PagedBench:
@@ -433,20 +451,6 @@ class PagedBench:
                       f"{L2_BYTES // 2**20} MiB L2"}
 
 
-def index_lists(torch, lengths, topk, seed=7):
-    """[B, topk] int32: per entry, min(topk, L) unique slots drawn from its
-    valid prefix [0, L) (seeded), -1 after them."""
-    import workloads
-    g = workloads.generator(seed, "cpu")
-    rows = []
-    for L in lengths:
-        n = min(topk, L)
-        r = torch.full((topk,), -1, dtype=torch.int32)
-        r[:n] = torch.randperm(L, generator=g)[:n].to(torch.int32)
-        rows.append(r)
-    return torch.stack(rows)
-
-
 class IndexedBench(MaskedBench):
     """Top-k sparse decode on the batched-GQA caches: every layer appends the
     step's K/V row, then attends over 2048 slots per batch entry drawn once
@@ -456,9 +460,10 @@ class IndexedBench(MaskedBench):
     TOPK = 2048
 
     def __init__(self, torch, kvd, dev, layers=None):
+        import workloads
         super().__init__("gqa", torch, kvd, dev, layers)
         self.name = "indexed"
-        self.indices = index_lists(torch, self.lengths0, self.TOPK).to(dev)
+        self.indices = workloads.index_lists(self.lengths0, self.TOPK).to(dev)
         self.listed = [min(self.TOPK, L) for L in self.lengths0]
         need = kvd.attend_indexed_workspace_bytes(self.B, self.Hq, self.Hkv, self.TOPK, self.D)
         self.ws = kvd.workspace(need, dev)
@@ -699,7 +704,7 @@ def oracle_rate(name, seconds, W_mod=None):
         lay = w.layers[0]
         topk = IndexedBench.TOPK
         L = [int(x) for x in lay.lengths]
-        idx = index_lists(torch, L, topk)
+        idx = workloads.index_lists(L, topk)
         per = (sum(min(topk, x) for x in L) * w.Hkv * w.D * 2 * 2 + w.B * topk * 4
                + 2 * w.B * w.Hq * w.D * 2)
         done_bytes, t0, n = 0, time.perf_counter(), 0
@@ -716,6 +721,8 @@ def oracle_rate(name, seconds, W_mod=None):
         w = workloads.npuw(device="cpu", layers=4)
     elif name == "gqa":
         w = workloads.gqa(device="cpu", layers=1)
+    elif name == "window":
+        w = workloads.window(device="cpu", layers=1)
     else:
         w = workloads.long(device="cpu", layers=1)
     done_bytes, t0, n = 0, time.perf_counter(), 0
@@ -729,7 +736,7 @@ def oracle_rate(name, seconds, W_mod=None):
         oracle.attend_masked(lay.q, torch.from_numpy(kh).view(torch.bfloat16),
                              torch.from_numpy(vh).view(torch.bfloat16), torch.from_numpy(mh),
                              lay.scale)
-        L = [int(x) for x in lay.lengths]
+        L = [min(int(x), w.window) if w.window else int(x) for x in lay.lengths]
         done_bytes += masked_attend_bytes(L, w.Hq, w.Hkv, w.C, w.D, 2) + append_bytes(w.B, w.Hkv, w.D, 2)
         n += 1
         el = time.perf_counter() - t0
@@ -779,7 +786,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvd", choices=["kvd", "reference"])
     ap.add_argument("--workload", default="npuw",
-                    choices=["npuw", "gqa", "long", "paged", "indexed"])
+                    choices=["npuw", "gqa", "long", "paged", "indexed", "window"])
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true",
@@ -842,7 +849,7 @@ def main():
 
     others = {}
     if not args.no_others:
-        for name in ("gqa", "long", "paged", "indexed", "npuw"):
+        for name in ("gqa", "long", "paged", "indexed", "window", "npuw"):
             if name == args.workload:
                 continue
             log(f"workload {name}")

@@ -259,3 +259,34 @@ def test_indexed_repeats_unused_entries_and_order(oracle):
     assert err == oracle.ERR_POS and np.allclose(bad, out, rtol=0, atol=1e-13)
     empty, lse, _ = oracle.attend_indexed(q, k, v, torch.full((1, 4), -1, dtype=torch.int32), 0.5)
     assert np.all(empty == 0) and np.all(np.isneginf(lse))
+
+
+# ------------------------------------------------------------ sliding window
+
+@pytest.mark.parametrize("L,Wn", [(40, 1), (40, 7), (40, 40), (40, 64), (23, 16), (1, 5)])
+def test_sliding_window_is_attention_over_the_last_rows(oracle, L, Wn):
+    """Sliding-window decode (cuTile on NPU, Part 1, the tile-level variants):
+    the step attends to the newest Wn rows only.  The window mask through the
+    masked oracle equals float64 softmax attention written out over the slice
+    k[L - Wn : L] (torch), and is bit-identical to the masked oracle on that
+    slice alone; a window at least as long as the sequence is the prefix."""
+    g = W.generator(60 + L + Wn)
+    B, Hq, Hkv, C, D = 1, 4, 2, 64, 16
+    q = W.randn(g, (B, Hq, D), torch.bfloat16)
+    k = W.randn(g, (B, Hkv, C, D), torch.bfloat16)
+    v = W.randn(g, (B, Hkv, C, D), torch.bfloat16)
+    mask = W.window_mask([L], C, Wn)
+    lo = max(0, L - Wn)
+    assert int(mask.sum()) == L - lo and int(mask[0, lo]) == 1 and int(mask[0, L - 1]) == 1
+    out, lse = oracle.attend_masked(q, k, v, mask, 0.2)
+    ks = k[:, :, lo:L].double().repeat_interleave(Hq // Hkv, 1)
+    vs = v[:, :, lo:L].double().repeat_interleave(Hq // Hkv, 1)
+    s = torch.einsum("bhd,bhtd->bht", q.double(), ks) * 0.2
+    ref = torch.einsum("bht,bhtd->bhd", torch.softmax(s, -1), vs)
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, torch.logsumexp(s, -1).numpy(), rtol=1e-12, atol=1e-12)
+    o2, l2 = oracle.attend_masked(q, k[:, :, lo:L].contiguous(), v[:, :, lo:L].contiguous(),
+                                  torch.ones(1, L - lo, dtype=torch.uint8), 0.2)
+    assert np.array_equal(out, o2) and np.array_equal(lse, l2)
+    if Wn >= L:
+        assert np.array_equal(mask, W.prefix_mask([L], C))

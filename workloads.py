@@ -41,7 +41,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-SEEDS = {"tiny": 1, "npuw": 2, "gqa": 3, "paged": 4, "long": 5}
+SEEDS = {"tiny": 1, "npuw": 2, "gqa": 3, "paged": 4, "long": 5, "window": 6}
 
 
 def generator(seed: int, device="cpu") -> torch.Generator:
@@ -73,6 +73,29 @@ def prefix_mask(lengths, capacity: int, device="cpu"):
     lengths = torch.as_tensor(lengths, dtype=torch.int64, device=device)
     ar = torch.arange(capacity, device=device).unsqueeze(0)
     return (ar < lengths.unsqueeze(1)).to(torch.uint8)
+
+
+def window_mask(lengths, capacity: int, window: int, device="cpu"):
+    """uint8 [B, capacity]: 1 on the last ``window`` slots of each valid
+    prefix, [max(0, lengths[b] - window), lengths[b])."""
+    lengths = torch.as_tensor(lengths, dtype=torch.int64, device=device)
+    ar = torch.arange(capacity, device=device).unsqueeze(0)
+    end = lengths.unsqueeze(1)
+    return ((ar < end) & (ar >= end - window)).to(torch.uint8)
+
+
+def index_lists(lengths, topk: int, seed: int = 7):
+    """int32 [B, topk]: per entry, min(topk, L) unique slots drawn from its
+    valid prefix [0, L) in random order (seeded), -1 after them."""
+    g = generator(seed, "cpu")
+    rows = []
+    for L in lengths:
+        L = int(L)
+        n = min(topk, L)
+        r = torch.full((topk,), -1, dtype=torch.int32)
+        r[:n] = torch.randperm(L, generator=g)[:n].to(torch.int32)
+        rows.append(r)
+    return torch.stack(rows)
 
 
 def cumsum_lengths(lengths):
@@ -115,6 +138,7 @@ class MaskedWorkload:
     D: int
     dtype: torch.dtype
     layers: list = field(default_factory=list)
+    window: int = 0  # > 0: each row attends to its last `window` slots only
 
 
 def masked_layer(g, B, Hq, Hkv, C, D, lengths, dtype=torch.bfloat16, device="cpu",
@@ -202,6 +226,21 @@ def gqa(device="cpu", layers: int = 32, seed: int | None = None, B: int = 16,
     for _ in range(layers):
         w.layers.append(masked_layer(g, B, Hq, Hkv, C, D, lengths, torch.bfloat16, device,
                                      k_scale=0.5))
+    return w
+
+
+def window(device="cpu", layers: int = 8, seed: int | None = None, C: int = 32768,
+           H: int = 32, D: int = 128, W: int = 4096) -> MaskedWorkload:
+    """Sliding-window decode over the long caches: one sequence filling its
+    capacity, attending to its last W slots (the W - 1 newest rows before the
+    step plus the row the step appends at C - 1)."""
+    g = generator(SEEDS["window"] if seed is None else seed, device)
+    w = MaskedWorkload("window", 1, H, H, C, D, torch.bfloat16, window=W)
+    lengths = torch.full((1,), C, dtype=torch.int64)
+    for _ in range(layers):
+        lay = masked_layer(g, 1, H, H, C, D, lengths, torch.bfloat16, device)
+        lay.mask = window_mask(lengths - 1, C, W - 1, device)
+        w.layers.append(lay)
     return w
 
 
