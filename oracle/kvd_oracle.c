@@ -25,6 +25,13 @@
  *  [FlashMLA] "FlashMLA на Huawei Ascend: ядро разреженного внимания
  *             изнутри", section "Математическая постановка" (P = Q K^T,
  *             S = softmax(P * sm_scale), out = S V; lse per row).
+ *  [FlashMLA-KV] same page, "Ограничение по деквантованию" (decoding reads
+ *             the KV cache in FP8, dequantises it to bf16 and feeds the
+ *             matrix unit) and "Оптимизация раскладки KV-кэша при decoding"
+ *             (each token's quantised values and its scale are stored side
+ *             by side).  The scale granularity and encoding are not given;
+ *             the reading taken here is one fp32 scale per token row of a kv
+ *             head (absmax / 448), stored right after the row's E4M3 codes.
  *  [PyPTO]    "PyPTO 实现 AscendC GatherPaKvCache（Norm/ND 分支）", sections
  *             3.1 (tensor contract), 3.2 (gather semantics: logical_block =
  *             t // block_size, slot = t % block_size, physical_block =
@@ -46,6 +53,7 @@
 /* element types of the storage */
 #define ORC_BF16 0
 #define ORC_F32 1
+#define ORC_FP8ROW 2 /* K/V only: rows of D E4M3 codes + fp32 scale + 12 zero bytes */
 
 /* error bits reported by the data-movement oracles (own numbering) */
 #define ORC_ERR_POS 1        /* append position outside [0, capacity) */
@@ -67,6 +75,105 @@ static double orc_elem(const void* base, size_t i, int dtype) {
     return (double)((const float*)base)[i];
 }
 
+/* ------------------------------------------------------------ E4M3 codes
+ * OCP 8-bit floating point, E4M3 variant: 1 sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits; exponent field 0 holds the subnormals f * 2^-9;
+ * no infinities; S.1111.111 is NaN, so the largest finite value is
+ * 1.75 * 2^8 = 448. */
+static double orc_e4m3_value(uint8_t c) {
+    const int e = (c >> 3) & 15, f = c & 7;
+    double x;
+    if (e == 15 && f == 7)
+        x = NAN;
+    else if (e == 0)
+        x = ldexp((double)f, -9);
+    else
+        x = ldexp((double)(8 + f), e - 10); /* (1 + f/8) * 2^(e-7) */
+    return (c & 0x80) ? -x : x;
+}
+
+/* Nearest E4M3 value of x, ties to the even code, magnitudes from 448 up
+ * (and infinities) saturated to 448; NaN stays NaN. */
+static uint8_t orc_e4m3_code(float x) {
+    const uint8_t sign = signbit(x) ? 0x80 : 0;
+    if (isnan(x)) return sign | 0x7F;
+    const double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a == 0.0) return sign;
+    int ex;
+    frexp(a, &ex); /* a in [2^(ex-1), 2^ex) */
+    int e = ex - 1;
+    if (e < -6) e = -6; /* below 2^-6 the spacing stays that of the subnormals */
+    const double step = ldexp(1.0, e - 3);
+    const double val = nearbyint(a / step) * step; /* exact quotient; ties to even */
+    if (val == 0.0) return sign;
+    int ev;
+    frexp(val, &ev);
+    const int E = ev - 1 + 7;
+    if (E <= 0) return sign | (uint8_t)(val * 512.0); /* f * 2^-9 */
+    const int f = (int)(val / ldexp(1.0, ev - 1) * 8.0) - 8;
+    return sign | (uint8_t)(E << 3) | (uint8_t)f;
+}
+
+/* fp32 scale of a quantised row (bytes D..D+3, little-endian). */
+static float orc_row_scale(const uint8_t* row, int D) {
+    const uint32_t u = (uint32_t)row[D] | ((uint32_t)row[D + 1] << 8) |
+                       ((uint32_t)row[D + 2] << 16) | ((uint32_t)row[D + 3] << 24);
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Element d of K/V row `row` (rows of D elements, or quantised rows). */
+static double orc_kv(const void* base, size_t row, int d, int kvtype, int D) {
+    if (kvtype == ORC_FP8ROW) {
+        const uint8_t* r = (const uint8_t*)base + row * (size_t)(D + 16);
+        return (double)orc_row_scale(r, D) * orc_e4m3_value(r[d]);
+    }
+    return orc_elem(base, row * (size_t)D + d, kvtype);
+}
+
+/*
+ * Row quantisation ([FlashMLA-KV], reading above): for each row of D values,
+ * amax = max |v_d|, scale = amax / 448 and code_d = E4M3(v_d / scale), both
+ * divisions in fp32 with round-to-nearest; a row of zeros gets scale 0 and
+ * zero codes.  dst rows: codes, the scale's 4 bytes (little-endian), 12 zero
+ * bytes.  Inputs are finite.
+ */
+static void orc_quantize_row(const void* src, size_t row, int dtype, int D, uint8_t* dst) {
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        const float a = fabsf((float)orc_elem(src, row * (size_t)D + d, dtype));
+        if (a > amax) amax = a;
+    }
+    const float scale = amax / 448.0f;
+    for (int d = 0; d < D; ++d) {
+        const float v = (float)orc_elem(src, row * (size_t)D + d, dtype);
+        dst[d] = scale > 0.0f ? orc_e4m3_code(v / scale) : 0;
+    }
+    uint32_t u;
+    memcpy(&u, &scale, sizeof u);
+    for (int i = 0; i < 4; ++i) dst[D + i] = (uint8_t)(u >> (8 * i));
+    memset(dst + D + 4, 0, 12);
+}
+
+int kvd_oracle_quantize_rows(const void* src, int dtype, long rows, int D, uint8_t* dst) {
+    if (rows < 0 || D <= 0) return -1;
+    for (long r = 0; r < rows; ++r)
+        orc_quantize_row(src, (size_t)r, dtype, D, dst + (size_t)r * (D + 16));
+    return 0;
+}
+
+int kvd_oracle_e4m3_codes(const float* x, long n, uint8_t* out) {
+    for (long i = 0; i < n; ++i) out[i] = orc_e4m3_code(x[i]);
+    return 0;
+}
+
+int kvd_oracle_e4m3_values(const uint8_t* c, long n, double* out) {
+    for (long i = 0; i < n; ++i) out[i] = orc_e4m3_value(c[i]);
+    return 0;
+}
+
 int kvd_oracle_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
@@ -85,10 +192,10 @@ int kvd_oracle_threads(void) {
  * when the padding holds inf or NaN.  A row with no valid slot gives out = 0
  * and lse = -inf.
  */
-int kvd_oracle_attend_masked(const void* q, const void* k, const void* v,
-                             const uint8_t* mask, int dtype, int B, int Hq,
-                             int Hkv, int C, int D, double scale, double* out,
-                             double* lse, int nthreads) {
+static int orc_attend_masked(const void* q, int dtype, const void* k, const void* v,
+                             int kvtype, const uint8_t* mask, int B, int Hq, int Hkv,
+                             int C, int D, double scale, double* out, double* lse,
+                             int nthreads) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || C < 0 || D <= 0 || Hq % Hkv) return -1;
     const int g = Hq / Hkv;
     const long units = (long)B * Hq;
@@ -111,7 +218,7 @@ int kvd_oracle_attend_masked(const void* q, const void* k, const void* v,
             continue;
         }
         const size_t qbase = ((size_t)b * Hq + h) * D;
-        const size_t kvbase = ((size_t)b * Hkv + kvh) * (size_t)C * D;
+        const size_t kvrow = ((size_t)b * Hkv + kvh) * (size_t)C;
         /* pass 1: scores of the valid slots and their maximum */
         double m = -INFINITY;
         long nvalid = 0;
@@ -119,8 +226,7 @@ int kvd_oracle_attend_masked(const void* q, const void* k, const void* v,
             if (!mask[(size_t)b * C + t]) continue;
             double dot = 0.0;
             for (int d = 0; d < D; ++d)
-                dot += orc_elem(q, qbase + d, dtype) *
-                       orc_elem(k, kvbase + (size_t)t * D + d, dtype);
+                dot += orc_elem(q, qbase + d, dtype) * orc_kv(k, kvrow + t, d, kvtype, D);
             s[t] = scale * dot;
             if (s[t] > m) m = s[t];
             ++nvalid;
@@ -140,8 +246,7 @@ int kvd_oracle_attend_masked(const void* q, const void* k, const void* v,
             if (!mask[(size_t)b * C + t]) continue;
             const double w = exp(s[t] - m);
             den += w;
-            for (int d = 0; d < D; ++d)
-                num[d] += w * orc_elem(v, kvbase + (size_t)t * D + d, dtype);
+            for (int d = 0; d < D; ++d) num[d] += w * orc_kv(v, kvrow + t, d, kvtype, D);
         }
         for (int d = 0; d < D; ++d) o[d] = num[d] / den;
         if (lse) lse[(size_t)b * Hq + h] = m + log(den);
@@ -149,6 +254,27 @@ int kvd_oracle_attend_masked(const void* q, const void* k, const void* v,
         free(num);
     }
     return failed ? -2 : 0;
+}
+
+int kvd_oracle_attend_masked(const void* q, const void* k, const void* v,
+                             const uint8_t* mask, int dtype, int B, int Hq,
+                             int Hkv, int C, int D, double scale, double* out,
+                             double* lse, int nthreads) {
+    return orc_attend_masked(q, dtype, k, v, dtype, mask, B, Hq, Hkv, C, D, scale, out, lse,
+                             nthreads);
+}
+
+/*
+ * Masked decode attention over quantised K/V rows ([FlashMLA-KV]): the same
+ * definition as kvd_oracle_attend_masked with every K and V element taken as
+ * scale_row * E4M3(code), exactly, in double.
+ *   q [B, Hq, D] (qtype); k, v [B, Hkv, C, D + 16] bytes.
+ */
+int kvd_oracle_attend_masked_fp8(const void* q, int qtype, const uint8_t* k, const uint8_t* v,
+                                 const uint8_t* mask, int B, int Hq, int Hkv, int C, int D,
+                                 double scale, double* out, double* lse, int nthreads) {
+    return orc_attend_masked(q, qtype, k, v, ORC_FP8ROW, mask, B, Hq, Hkv, C, D, scale, out, lse,
+                             nthreads);
 }
 
 /*
@@ -254,6 +380,34 @@ int kvd_oracle_append(void* k_cache, void* v_cache, const void* k_new,
             const size_t src = ((size_t)b * Hkv + h) * row;
             memcpy((char*)k_cache + dst, (const char*)k_new + src, row);
             memcpy((char*)v_cache + dst, (const char*)v_new + src, row);
+        }
+        if (mask) mask[(size_t)b * C + p] = 1;
+    }
+    return err;
+}
+
+/*
+ * KV append into quantised caches ([NPU-KV] Part 2, update_kvcache_for, with
+ * the row format of [FlashMLA-KV]): row pos[b] of every kv head of k_cache /
+ * v_cache [B, Hkv, C, D + 16] bytes becomes the quantised k_new / v_new
+ * [B, Hkv, D] (dtype); mask slot pos[b] becomes 1.  A position outside
+ * [0, C) writes nothing for that entry and sets ORC_ERR_POS.
+ */
+int kvd_oracle_append_fp8(uint8_t* k_cache, uint8_t* v_cache, const void* k_new,
+                          const void* v_new, int dtype, const int32_t* pos, uint8_t* mask,
+                          int B, int Hkv, int C, int D) {
+    int err = 0;
+    const size_t rb = (size_t)D + 16;
+    for (int b = 0; b < B; ++b) {
+        const int p = pos[b];
+        if (p < 0 || p >= C) {
+            err |= ORC_ERR_POS;
+            continue;
+        }
+        for (int h = 0; h < Hkv; ++h) {
+            const size_t dst = (((size_t)b * Hkv + h) * C + p) * rb;
+            orc_quantize_row(k_new, (size_t)b * Hkv + h, dtype, D, k_cache + dst);
+            orc_quantize_row(v_new, (size_t)b * Hkv + h, dtype, D, v_cache + dst);
         }
         if (mask) mask[(size_t)b * C + p] = 1;
     }
