@@ -29,6 +29,15 @@
 // inside fp32, and the result is the same up to rounding.  A warp rescales
 // only when one of its lanes needs it.
 //
+//  Fp8MmaConsumer: tensor cores over quantised K/V rows (E4M3 codes, the
+//    row's fp32 scale beside them; "FlashMLA на Huawei Ascend", "Ограничение
+//    по деквантованию" and "Оптимизация раскладки KV-кэша при decoding").
+//    The codes become f16 in registers (exactly), read with plain 16-byte
+//    shared loads in a dims-to-lanes order that both mma operands share;
+//    each row's scale multiplies its score (K) or its weight p (V), so no
+//    element is ever multiplied by its scale.  Any query head count up to 8
+//    per kv head.
+//
 // finish() leaves each warp's state in shared memory as mo[w][h][d]
 // (unnormalised output) and ml[w][h] = (m, l) for the CTA-wide merge.
 #pragma once
@@ -55,6 +64,7 @@ struct SimtConsumer {
     static constexpr int kSubWant = (32 / G) < 1 ? 1 : (32 / G);
     static constexpr int kSub = kSteps < kSubWant ? kSteps : kSubWant;
     static constexpr int kTileBytes = T * D * (int)sizeof(Elem);  // K (or V) of one tile
+    static constexpr int kRowBytes = D * (int)sizeof(Elem);
     static_assert(D % kVec == 0 && kLPT <= 32 && 32 % kLPT == 0, "head_dim layout");
     static_assert(T % NCW == 0 && kTW % kTPW == 0 && kSteps % kSub == 0, "tile layout");
     static_assert(T <= 64, "validity bits of a tile fit 64 bits");
@@ -212,6 +222,7 @@ struct MmaConsumer {
     static constexpr int kHalves = D / 64;      // 128-byte column halves per row
     static constexpr int kHalfBytes = T * 128;
     static constexpr int kTileBytes = kHalves * kHalfBytes;
+    static constexpr int kRowBytes = D * 2;
     static constexpr int kSlabsPerWarp = T / 16 / NCW;
     static constexpr int kKSteps = D / 16;      // q.K^T: 16 dims per mma
     static constexpr int kDBlocks = D / 16;     // p.V: 16 output dims per mma
@@ -343,6 +354,229 @@ struct MmaConsumer {
                 for (int d = 0; d < kDBlocks; ++d) {
                     mo[(warp * G + hh) * D + d * 16 + gid] = acc[d][c];
                     mo[(warp * G + hh) * D + d * 16 + gid + 8] = acc[d][2 + c];
+                }
+                if (gid == 0) {
+                    ml[(warp * G + hh) * 2] = m[c];
+                    ml[(warp * G + hh) * 2 + 1] = l[c];
+                }
+            }
+        }
+    }
+};
+
+// Quantised rows: kRowBytes = D codes + fp32 scale + 12 zero bytes.
+//  q.K^T, per k-step ks of 16 dims: lane (gid, tig) holds k-indices 2tig,
+//    2tig+1, 2tig+8, 2tig+9, mapped to dims (D/4)tig + 4ks + 0..3, so that
+//    its K codes for all k-steps are D/4 consecutive bytes of a row (one or
+//    two 16-byte loads per token, conflict-free for the 16 * (D + 16)-byte
+//    stride) and q takes the same order.  K codes -> f16 exactly; q -> f16
+//    (exact for |q| in the f16 normal range); the score is then scaled by the
+//    row's K scale.
+//  p.V as V^T p^T, per 16-dim block j: m-row r < 8 is dim (D/8)r + 2j, row
+//    r + 8 is dim (D/8)r + 2j + 1, so that lane gid's V codes of all blocks
+//    are D/8 consecutive bytes of a row.  V codes -> f16 exactly; each
+//    token's weight p carries its V scale divided by 2^ve, where 2^ve is the
+//    power of two of the largest V scale seen so far (a running maximum like
+//    the softmax's: when it grows, the output is rescaled by an exact power
+//    of two), so the f16 weights stay within 2 * e^6 and keep 11 bits; the
+//    output is multiplied by 2^ve at the end.
+template <int D, int G, int T, int NCW>
+struct Fp8MmaConsumer {
+    using ElemT = __nv_bfloat16;  // q and out
+    static constexpr bool kSwizzled = false;
+    static constexpr int kD = D, kG = G, kT = T, kNCW = NCW;
+    static constexpr int kRowBytes = D + 16;
+    static constexpr int kTileBytes = T * kRowBytes;
+    static constexpr int kSlabsPerWarp = T / 16 / NCW;
+    static constexpr int kKSteps = D / 16;
+    static constexpr int kDBlocks = D / 16;
+    static constexpr int kKWords = D / 16;  // words of a lane's K bytes (D/4 bytes)
+    static constexpr int kVWords = D / 32;  // words of a lane's V bytes (D/8 bytes)
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    static_assert(G >= 1 && G <= 8, "at most 8 query heads per mma column block");
+    static_assert(T % (16 * NCW) == 0 && kSlabsPerWarp >= 1, "16-token slabs per warp");
+    static_assert(T <= 64, "validity bits of a tile fit 64 bits");
+
+    uint32_t qb[kKSteps][2];  // q^T as the f16 B operand, dims in the order above
+    float m[2], l[2];         // heads 2*tig, 2*tig + 1
+    float acc[kDBlocks][4];   // out^T / 2^(ve-127): dims (D/8)gid + 2j (+1 for 2, 3), heads 2tig (+1)
+    int ve;                   // biased exponent of the largest V scale so far (0: none yet)
+    float vinv;               // 2^(127 - ve)
+
+    // 2^k for -126 <= k <= 127 (0 below)
+    __device__ __forceinline__ static float pow2i(int k) {
+        return __int_as_float(k < -126 ? 0 : (k + 127) << 23);
+    }
+
+    __device__ __forceinline__ void begin(const __nv_bfloat16* qs, int g_here, float /*qscale*/,
+                                          int lane) {
+        const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int ks = 0; ks < kKSteps; ++ks) {
+            if (gid < g_here) {
+                const __nv_bfloat16* qp = qs + gid * D + (D / 4) * tig + 4 * ks;
+                qb[ks][0] = pack_f16x2(__bfloat162float(qp[0]), __bfloat162float(qp[1]));
+                qb[ks][1] = pack_f16x2(__bfloat162float(qp[2]), __bfloat162float(qp[3]));
+            } else {
+                qb[ks][0] = qb[ks][1] = 0u;
+            }
+        }
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
+        ve = 0;
+        vinv = 0.f;
+#pragma unroll
+        for (int d = 0; d < kDBlocks; ++d) acc[d][0] = acc[d][1] = acc[d][2] = acc[d][3] = 0.f;
+    }
+
+    __device__ __forceinline__ bool tile(unsigned char* kbuf, unsigned char* vbuf, uint64_t bits,
+                                         int warp, int lane, float qscale) {
+        const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int sl = 0; sl < kSlabsPerWarp; ++sl) {
+            const int slab0 = (warp * kSlabsPerWarp + sl) * 16;
+            const uint32_t vmask = (uint32_t)(bits >> slab0) & 0xffffu;
+            if (vmask == 0u) continue;
+            const bool v_lo = (vmask >> gid) & 1u, v_hi = (vmask >> (gid + 8)) & 1u;
+            // V scales of tokens gid, gid + 8 (0 for invalid rows) and the
+            // running power of two of the largest one
+            const unsigned char* vs = vbuf + (slab0 + gid) * kRowBytes + D;
+            const float sv0 = v_lo ? *reinterpret_cast<const float*>(vs) : 0.f;
+            const float sv1 = v_hi ? *reinterpret_cast<const float*>(vs + 8 * kRowBytes) : 0.f;
+            float smax = fmaxf(sv0, sv1);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1)
+                smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, off));
+            const int es = (__float_as_int(smax) >> 23) & 0xff;  // warp-uniform
+            if (es > ve) {
+                const float r = pow2i(ve - es);
+#pragma unroll
+                for (int d = 0; d < kDBlocks; ++d) {
+                    acc[d][0] *= r;
+                    acc[d][1] *= r;
+                    acc[d][2] *= r;
+                    acc[d][3] *= r;
+                }
+                ve = es;
+                vinv = pow2i(127 - es);
+            }
+
+            // ---- q.K^T: tokens gid, gid + 8 of the slab
+            const unsigned char* k0 = kbuf + (slab0 + gid) * kRowBytes;
+            const unsigned char* k1 = k0 + 8 * kRowBytes;
+            uint32_t kw0[kKWords], kw1[kKWords];
+#pragma unroll
+            for (int i = 0; i < kKWords / 4; ++i) {
+                const uint4 x = *reinterpret_cast<const uint4*>(k0 + (D / 4) * tig + 16 * i);
+                const uint4 y = *reinterpret_cast<const uint4*>(k1 + (D / 4) * tig + 16 * i);
+                kw0[4 * i] = x.x; kw0[4 * i + 1] = x.y; kw0[4 * i + 2] = x.z; kw0[4 * i + 3] = x.w;
+                kw1[4 * i] = y.x; kw1[4 * i + 1] = y.y; kw1[4 * i + 2] = y.z; kw1[4 * i + 3] = y.w;
+            }
+            const float sk0 = *reinterpret_cast<const float*>(k0 + D) * qscale;
+            const float sk1 = *reinterpret_cast<const float*>(k1 + D) * qscale;
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < kKSteps; ++ks) {
+                uint32_t a[4];
+                a[0] = e4m3x2_to_f16x2(kw0[ks]);
+                a[1] = e4m3x2_to_f16x2(kw1[ks]);
+                a[2] = e4m3x2_to_f16x2(kw0[ks] >> 16);
+                a[3] = e4m3x2_to_f16x2(kw1[ks] >> 16);
+                mma_f16(s, a, qb[ks][0], qb[ks][1]);
+            }
+            s[0] = v_lo ? s[0] * sk0 : -INFINITY;
+            s[1] = v_lo ? s[1] * sk0 : -INFINITY;
+            s[2] = v_hi ? s[2] * sk1 : -INFINITY;
+            s[3] = v_hi ? s[3] * sk1 : -INFINITY;
+
+            float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const bool up0 = mx0 > m[0] + kSkipScale, up1 = mx1 > m[1] + kSkipScale;
+            const float mn0 = up0 ? mx0 : m[0], mn1 = up1 ? mx1 : m[1];
+            const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float c0 = up0 ? fast_exp2(m[0] - b0) : 1.f, c1 = up1 ? fast_exp2(m[1] - b1) : 1.f;
+            m[0] = mn0;
+            m[1] = mn1;
+            const float p0 = fast_exp2(s[0] - b0), p1 = fast_exp2(s[1] - b1);
+            const float p2 = fast_exp2(s[2] - b0), p3 = fast_exp2(s[3] - b1);
+            l[0] = fmaf(l[0], c0, p0 + p2);
+            l[1] = fmaf(l[1], c1, p1 + p3);
+            if (__any_sync(0xffffffffu, up0 || up1)) {
+                const float2 cc = make_float2(c0, c1);
+#pragma unroll
+                for (int d = 0; d < kDBlocks; ++d) {
+                    const float2 x = fmul2(make_float2(acc[d][0], acc[d][1]), cc);
+                    const float2 y = fmul2(make_float2(acc[d][2], acc[d][3]), cc);
+                    acc[d][0] = x.x;
+                    acc[d][1] = x.y;
+                    acc[d][2] = y.x;
+                    acc[d][3] = y.y;
+                }
+            }
+
+            // ---- p.V: weights times V scale / 2^ve in f16, zero for invalid rows
+            const float w0 = sv0 * vinv, w1 = sv1 * vinv;
+            const uint32_t pk_lo = pack_f16x2(p0 * w0, p1 * w0);
+            const uint32_t pk_hi = pack_f16x2(p2 * w1, p3 * w1);
+            const uint32_t bh0 = movmatrix_trans(pk_lo), bh1 = movmatrix_trans(pk_hi);
+
+            // V codes of tokens 2tig, 2tig+1, 2tig+8, 2tig+9 at bytes (D/8)gid..;
+            // codes of invalid rows become 0 (NaN codes must not meet a 0 weight)
+            uint32_t vw[4][kVWords];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int t = 2 * tig + (u & 1) + (u >> 1) * 8;
+                const unsigned char* vr = vbuf + (slab0 + t) * kRowBytes + (D / 8) * gid;
+                const bool ok = (vmask >> t) & 1u;
+                if constexpr (kVWords == 4) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(vr);
+                    vw[u][0] = ok ? x.x : 0u;
+                    vw[u][1] = ok ? x.y : 0u;
+                    vw[u][2] = ok ? x.z : 0u;
+                    vw[u][3] = ok ? x.w : 0u;
+                } else {
+                    const uint2 x = *reinterpret_cast<const uint2*>(vr);
+                    vw[u][0] = ok ? x.x : 0u;
+                    vw[u][1] = ok ? x.y : 0u;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kDBlocks; ++j) {
+                const uint32_t sel = (j & 1) ? 0x7362u : 0x5140u;  // bytes 2j%4, 2j%4+1 of two rows
+                const uint32_t lo = byte_perm(vw[0][j >> 1], vw[1][j >> 1], sel);
+                const uint32_t hi = byte_perm(vw[2][j >> 1], vw[3][j >> 1], sel);
+                uint32_t a[4];
+                a[0] = e4m3x2_to_f16x2(lo);
+                a[1] = e4m3x2_to_f16x2(lo >> 16);
+                a[2] = e4m3x2_to_f16x2(hi);
+                a[3] = e4m3x2_to_f16x2(hi >> 16);
+                mma_f16(acc[j], a, bh0, bh1);
+            }
+        }
+        return false;  // the ring is only read
+    }
+
+    __device__ __forceinline__ void finish(float* mo, float* ml, int warp, int lane) {
+        const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+            l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
+        }
+        const float vs = pow2i(ve - 127);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int hh = 2 * tig + c;
+            if (hh < G) {
+#pragma unroll
+                for (int j = 0; j < kDBlocks; ++j) {
+                    const int d = (D / 8) * gid + 2 * j;
+                    mo[(warp * G + hh) * D + d] = acc[j][c] * vs;
+                    mo[(warp * G + hh) * D + d + 1] = acc[j][2 + c] * vs;
                 }
                 if (gid == 0) {
                     ml[(warp * G + hh) * 2] = m[c];

@@ -3,6 +3,7 @@
 // so that the instantiations compile in parallel.
 #pragma once
 
+#include <cstring>
 #include <mutex>
 
 #include "attend_kernel.cuh"
@@ -40,6 +41,15 @@ struct SimtCfg {
 template <int D, int G>
 struct MmaCfg {
     using Cons = MmaConsumer<D, G, 64, 4>;
+    static constexpr int MB = 1;
+    static constexpr int STAGES = ring_stages<Cons, MB>();
+};
+
+// Tensor-core consumers over quantised rows (E4M3 codes + scale): 64-token
+// tiles of D + 16-byte rows, one merge buffer.
+template <int D, int G>
+struct Fp8Cfg {
+    using Cons = Fp8MmaConsumer<D, G, 64, 4>;
     static constexpr int MB = 1;
     static constexpr int STAGES = ring_stages<Cons, MB>();
 };
@@ -89,7 +99,7 @@ cudaError_t launch_kernel(const AttendParams& p, const CUtensorMap* kmap, const 
     }
     // The SM's lookahead split between the CTAs that share it, at least two tiles.
     AttendParams q = p;
-    const int bytes_per_token = 2 * Cons::kD * (int)sizeof(typename Cons::ElemT);
+    const int bytes_per_token = 2 * Cons::kRowBytes;
     q.look = (kLookBytesPerSm / per_sm) / bytes_per_token;
     if (q.look < 2 * p.tile) q.look = 2 * p.tile;
     const int grid = p.units < ctas ? p.units : ctas;
@@ -121,6 +131,16 @@ template <int D, int G>
 cudaError_t launch_mma(int mode, const AttendParams& p, const CUtensorMap* kmap,
                        const CUtensorMap* vmap, cudaStream_t stream) {
     return launch_cfg<MmaCfg<D, G>>(mode, p, kmap, vmap, stream);
+}
+
+// Quantised rows: static-buffer mode only (no tensor maps: rows arrive by
+// bulk copies of whole tiles).
+template <int D, int G>
+cudaError_t launch_fp8(const AttendParams& p, cudaStream_t stream) {
+    using C = Fp8Cfg<D, G>;
+    CUtensorMap none;
+    std::memset(&none, 0, sizeof none);
+    return launch_kernel<typename C::Cons, C::STAGES, C::MB, kModeMasked>(p, &none, &none, stream);
 }
 
 }  // namespace kvd

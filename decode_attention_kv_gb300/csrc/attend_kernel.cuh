@@ -475,6 +475,8 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
     }
     constexpr bool PAGED = MODE == kModePaged;
     constexpr bool INDEXED = MODE == kModeIndexed;
+    static_assert(MODE == kModeMasked || Cons::kRowBytes == D * (int)sizeof(Elem),
+                  "quantised rows: static-buffer mode only");
     if (threadIdx.x == 32 * kLoader && (PAGED || Cons::kSwizzled) && !INDEXED) {
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
@@ -765,7 +767,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                     } else if constexpr (PAGED) {
                         kvbytes = 2u * p.tile * D * sizeof(Elem);
                     } else {
-                        kvbytes = 2u * n * D * sizeof(Elem);
+                        kvbytes = 2u * n * Cons::kRowBytes;
                     }
                     mbar_arrive_expect_tx(&ctl.full[stage], kvbytes + qbytes);
                     if constexpr (INDEXED) {
@@ -794,11 +796,11 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                                            (int)rowidx, &ctl.full[stage], pol);
                             }
                         } else {
-                            const uint32_t bytes = (uint32_t)n * D * sizeof(Elem);
-                            bulk_g2s(sk, static_cast<const Elem*>(p.k) + rowidx * D, bytes,
-                                     &ctl.full[stage], pol);
-                            bulk_g2s(sv, static_cast<const Elem*>(p.v) + rowidx * D, bytes,
-                                     &ctl.full[stage], pol);
+                            const uint32_t bytes = (uint32_t)n * Cons::kRowBytes;
+                            bulk_g2s(sk, static_cast<const unsigned char*>(p.k) + rowidx * Cons::kRowBytes,
+                                     bytes, &ctl.full[stage], pol);
+                            bulk_g2s(sv, static_cast<const unsigned char*>(p.v) + rowidx * Cons::kRowBytes,
+                                     bytes, &ctl.full[stage], pol);
                         }
                     }
                     if (first)

@@ -1,5 +1,7 @@
 // data_kernels.cu -- the log-sum-exp combine, the KV append and the paged
 // gather kernels, with their launchers.
+#include <cuda_fp8.h>
+
 #include "kvd_device.cuh"
 #include "kvd_internal.h"
 
@@ -251,6 +253,90 @@ cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const
                       static_cast<const unsigned char*>(k_new),
                       static_cast<const unsigned char*>(v_new), pos, mask, Hkv, C, row_bytes,
                       dev_status);
+}
+
+// ------------------------------------------------------------- append_fp8
+// KV append into quantised caches: the step's K/V rows of every kv head are
+// quantised (amax = max |v|, scale = amax / 448, code = E4M3(v / scale), both
+// divisions fp32 round-to-nearest, codes rounded to nearest even and
+// saturated at 448; an all-zero row gets scale 0 and zero codes) and written
+// as D codes, the scale and 12 zero bytes at slot pos[b].  One warp per row
+// (K or V of one (b, kv head)); D / 32 values per lane.
+__device__ __forceinline__ float as_float(float x) { return x; }
+__device__ __forceinline__ float as_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename In, int D>
+__global__ void __launch_bounds__(128)
+append_fp8_kernel(unsigned char* __restrict__ kc, unsigned char* __restrict__ vc,
+                  const In* __restrict__ kn, const In* __restrict__ vn,
+                  const int32_t* __restrict__ pos, uint8_t* __restrict__ mask, int B, int Hkv,
+                  int C, int32_t* dev_status) {
+    pdl_launch_dependents();
+    pdl_wait();
+    constexpr int VPL = D / 32;
+    constexpr int RB = D + 16;
+    const int lane = threadIdx.x & 31;
+    const long long job = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (job >= 2ll * B * Hkv) return;
+    const int kv = (int)(job & 1);
+    const long long bh = job >> 1;
+    const int b = (int)(bh / Hkv);
+    const int p = pos[b];
+    if (p < 0 || p >= C) {
+        if (lane == 0 && kv == 0 && bh % Hkv == 0) report(dev_status, KVD_DEV_POS_RANGE);
+        return;
+    }
+    const In* src = (kv ? vn : kn) + bh * D + VPL * lane;
+    float x[VPL];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        x[i] = as_float(src[i]);
+        amax = fmaxf(amax, fabsf(x[i]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float scale = __fdiv_rn(amax, 448.f);
+    uint32_t codes = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const uint32_t c = scale > 0.f ? (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(x[i], scale),
+                                                                          __NV_SATFINITE, __NV_E4M3)
+                                       : 0u;
+        codes |= c << (8 * i);
+    }
+    unsigned char* row = (kv ? vc : kc) + ((size_t)bh * C + p) * RB;
+    if constexpr (VPL == 4)
+        *reinterpret_cast<uint32_t*>(row + 4 * lane) = codes;
+    else
+        *reinterpret_cast<uint16_t*>(row + 2 * lane) = (uint16_t)codes;
+    if (lane == 0) {
+        *reinterpret_cast<uint4*>(row + D) = make_uint4(__float_as_uint(scale), 0u, 0u, 0u);
+        if (mask && kv == 0 && bh % Hkv == 0) mask[(size_t)b * C + p] = 1;
+    }
+}
+
+cudaError_t launch_append_fp8(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                              const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
+                              kvd_dtype in_dt, int32_t* dev_status, cudaStream_t stream) {
+    const long long jobs = 2ll * B * Hkv;
+    const dim3 grid((unsigned)((jobs + 3) / 4));
+    unsigned char* kc = static_cast<unsigned char*>(k_cache);
+    unsigned char* vc = static_cast<unsigned char*>(v_cache);
+    if (in_dt == KVD_BF16) {
+        const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(k_new);
+        const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(v_new);
+        return D == 128 ? launch_pdl(append_fp8_kernel<__nv_bfloat16, 128>, grid, dim3(128), 0, stream,
+                                     kc, vc, kn, vn, pos, mask, B, Hkv, C, dev_status)
+                        : launch_pdl(append_fp8_kernel<__nv_bfloat16, 64>, grid, dim3(128), 0, stream,
+                                     kc, vc, kn, vn, pos, mask, B, Hkv, C, dev_status);
+    }
+    const float* kn = static_cast<const float*>(k_new);
+    const float* vn = static_cast<const float*>(v_new);
+    return D == 128 ? launch_pdl(append_fp8_kernel<float, 128>, grid, dim3(128), 0, stream, kc, vc,
+                                 kn, vn, pos, mask, B, Hkv, C, dev_status)
+                    : launch_pdl(append_fp8_kernel<float, 64>, grid, dim3(128), 0, stream, kc, vc,
+                                 kn, vn, pos, mask, B, Hkv, C, dev_status);
 }
 
 // ------------------------------------------------------------------- gather

@@ -20,6 +20,7 @@ cudaError_t launch_attend_f32(int D, int G, int mode, const AttendParams& p,
                               cudaStream_t stream);
 AttendGeom attend_geom_bf16(int D, int G);
 AttendGeom attend_geom_f32(int D, int G);
+cudaError_t launch_attend_fp8(int D, int G, const AttendParams& p, cudaStream_t stream);
 }  // namespace kvd
 
 using namespace kvd;
@@ -100,13 +101,14 @@ AttendGeom geom(kvd_dtype dt, int D, int G) {
 // rows: batch entries (or sequences); cap: most tokens a row can hold (the
 // list length for index lists); BS > 0 for the paged layout; `indexed`: a
 // split holds at most kMaxBlocks list entries (their slots travel with it).
+// tile_max > 0 overrides the element type's tile (quantised rows: 64).
 Plan plan_attention(int rows, int Hq, int Hkv, int cap, int D, kvd_dtype dt, int BS,
-                    int num_splits, bool indexed = false) {
+                    int num_splits, bool indexed = false, int tile_max = 0) {
     Plan pl{};
     const int g = Hq / Hkv;
     pl.G = group_width(g);
     pl.HG = (g + pl.G - 1) / pl.G;
-    const int T = geom(dt, D, pl.G).tile_max;
+    const int T = tile_max > 0 ? tile_max : geom(dt, D, pl.G).tile_max;
     if (BS > 0) {
         int t = T < BS ? T : BS;
         while (BS % t) --t;  // largest divisor of BS not above T
@@ -380,6 +382,74 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
         e = launch_combine(p.part_o, p.part_lse, out, lse_out, B * Hq, pl.S, D, dtype,
                            (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked combine launch");
+    }
+    return ok();
+}
+
+kvd_status kvd_append_fp8(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                          const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
+                          kvd_dtype new_dtype, int32_t* dev_status, kvd_stream_t stream) {
+    if (!k_cache || !v_cache || !k_new || !v_new || !pos)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_append_fp8: null pointer");
+    if (B < 1 || Hkv < 1 || C < 1) return fail(KVD_ERR_INVALID_ARG, "kvd_append_fp8: sizes must be >= 1");
+    if (!dtype_ok(new_dtype)) return fail(KVD_ERR_INVALID_ARG, "kvd_append_fp8: unknown dtype");
+    if (D != 64 && D != 128) return fail(KVD_ERR_UNSUPPORTED, "kvd_append_fp8: head_dim %d (supported: 64, 128)", D);
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) ||
+        !aligned(pos, 4) || !aligned(dev_status, 4))
+        return fail(KVD_ERR_INVALID_ARG, "kvd_append_fp8: misaligned pointer");
+    if (2ll * B * Hkv > (1ll << 33)) return fail(KVD_ERR_UNSUPPORTED, "kvd_append_fp8: B*Hkv too large");
+    const cudaError_t e = launch_append_fp8(k_cache, v_cache, k_new, v_new, pos, mask, B, Hkv, C, D,
+                                            new_dtype, dev_status, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvd_append_fp8 launch");
+    return ok();
+}
+
+constexpr int kFp8Tile = 64;  // tokens per ring stage over quantised rows
+
+size_t kvd_attend_masked_fp8_workspace_bytes(int B, int Hq, int Hkv, int C, int D, int num_splits) {
+    if (B < 1 || C < 1 || check_attention_shape(Hq, Hkv, D, KVD_BF16) != KVD_OK) return 0;
+    return plan_attention(B, Hq, Hkv, C, D, KVD_BF16, 0, num_splits, false, kFp8Tile).ws;
+}
+
+kvd_status kvd_attend_masked_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                 const uint8_t* mask, void* out, float* lse_out, int B, int Hq,
+                                 int Hkv, int C, int D, float scale, int num_splits,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                 kvd_stream_t stream) {
+    kvd_status st = check_attention_shape(Hq, Hkv, D, KVD_BF16);
+    if (st != KVD_OK) return st;
+    if (B < 0 || C < 1) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_fp8: B >= 0 and C >= 1 required");
+    if (B == 0) return ok();
+    if (!q || !k_cache || !v_cache || !mask || !out)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_fp8: null pointer");
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(lse_out, 4) || !aligned(dev_status, 4))
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_fp8: misaligned pointer");
+    if (num_splits < 0) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_fp8: num_splits < 0");
+    const Plan pl = plan_attention(B, Hq, Hkv, C, D, KVD_BF16, 0, num_splits, false, kFp8Tile);
+    st = check_workspace("kvd_attend_masked_fp8", pl, workspace, workspace_bytes);
+    if (st != KVD_OK) return st;
+    AttendParams p{};
+    p.q = q;
+    p.k = k_cache;
+    p.v = v_cache;
+    p.mask = mask;
+    p.out = out;
+    p.lse_out = lse_out;
+    p.dev_status = dev_status;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.g = Hq / Hkv;
+    p.C = C;
+    p.mask_vec = (C % 16 == 0) && aligned(mask, 16);
+    p.qscale = scale * kLog2e;
+    attach_workspace(p, pl, workspace);
+    cudaError_t e = launch_attend_fp8(D, pl.G, p, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked_fp8 launch");
+    if (pl.S > 1) {
+        e = launch_combine(p.part_o, p.part_lse, out, lse_out, B * Hq, pl.S, D, KVD_BF16,
+                           (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked_fp8 combine launch");
     }
     return ok();
 }

@@ -20,6 +20,10 @@
  *           изнутри", "Математическая постановка" -- out = softmax(Q K^T *
  *           sm_scale) V per query token; "Ход вычислений" -- fp32 running
  *           max / sum / output and a log-sum-exp per row.
+ *  [FlashMLA-KV] the same page, "Ограничение по деквантованию" -- decoding
+ *           reads the KV cache in FP8, dequantises it to bf16 and feeds the
+ *           matrix unit; "Оптимизация раскладки KV-кэша при decoding" -- a
+ *           token's quantised values and its scale are stored side by side.
  *  [PyPTO]  "PyPTO 实现 AscendC GatherPaKvCache（Norm/ND 分支）" sections
  *           3.1-3.3 -- key_cache [num_blocks, block_size, heads, dim],
  *           int32 block_tables [Q, cols], cumsum seq_lens [Q+1] starting at
@@ -202,6 +206,53 @@ kvd_status kvd_attend_indexed(const void* q, const void* k_cache, const void* v_
                               int32_t* dev_status, kvd_stream_t stream);
 
 /*
+ * Quantised KV rows ([FlashMLA-KV]; the scale granularity and encoding are
+ * this library's reading, the page gives neither): one row of a kv head is
+ *   bytes [0, D)        OCP FP8 E4M3 codes (bias 7, max 448, no infinities)
+ *   bytes [D, D + 4)    the row's scale, fp32 little-endian
+ *   bytes [D + 4, D+16) zero
+ * so a cache is uint8 [B, Hkv, C, D + KVD_FP8_ROW_PAD] and element d of a row
+ * is scale * E4M3(code[d]).  kvd_append_fp8 writes such rows; the attention
+ * reads them directly (no bf16 copy of the cache exists).
+ */
+#define KVD_FP8_ROW_PAD 16
+
+/*
+ * kvd_append_fp8 -- kvd_append ([NPU] Part 2, update_kvcache_for) into
+ * quantised caches: for every kv head h the new rows k_new[b, h, :],
+ * v_new[b, h, :] ([B, Hkv, D], new_dtype bf16 or fp32, finite) are quantised
+ *   amax = max_d |x_d|, scale = amax / 448, code_d = E4M3(x_d / scale)
+ * (both divisions fp32 round-to-nearest; codes rounded to nearest even and
+ * saturated at 448; amax = 0 gives scale 0 and zero codes) and written as
+ * row pos[b] of k_cache / v_cache [B, Hkv, C, D + 16] (uint8); mask[b, pos[b]]
+ * becomes 1 if mask is not NULL.  D is 64 or 128.  pos[b] outside [0, C)
+ * writes nothing for b and sets KVD_DEV_POS_RANGE.
+ */
+kvd_status kvd_append_fp8(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                          const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
+                          kvd_dtype new_dtype, int32_t* dev_status, kvd_stream_t stream);
+
+/*
+ * kvd_attend_masked_fp8 -- kvd_attend_masked over quantised caches: the same
+ * definition with every K/V element dequantised (scale * E4M3(code)).
+ *   q [B, Hq, D] bf16; k_cache, v_cache uint8 [B, Hkv, C, D + 16] (rows as
+ *   above); mask [B, C]; out [B, Hq, D] bf16; lse_out [B, Hq] float or NULL.
+ * The tensor-core kernel never builds a dequantised copy: K codes meet q in
+ * fp16 (q is converted to fp16, so |q| must stay below 65504) and each row's
+ * scale multiplies its score; V codes meet the softmax weights in fp16, each
+ * weight carrying its row's scale relative to a running power of two (row
+ * scales must be finite and below 2^126).  D is 64 or 128; any Hq / Hkv (up
+ * to 8 query heads per kv head in one group, larger groups are split).
+ * Workspace and num_splits as for kvd_attend_masked (64-token tiles).
+ */
+size_t kvd_attend_masked_fp8_workspace_bytes(int B, int Hq, int Hkv, int C, int D, int num_splits);
+kvd_status kvd_attend_masked_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                 const uint8_t* mask, void* out, float* lse_out, int B, int Hq,
+                                 int Hkv, int C, int D, float scale, int num_splits,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                 kvd_stream_t stream);
+
+/*
  * kvd_attend_masked_noalloc -- the pages have no counterpart to this call; it
  * exists for callers that cannot allocate device memory.  Some host runtimes
  * own all device memory through their own allocator and hand a kernel library
@@ -268,7 +319,7 @@ kvd_status kvd_gather_paged(const void* key_cache, const void* value_cache,
  *   LSE[r] = log sum_s exp(part_lse[r, s]),
  *   out[r, :] = sum_s exp(part_lse[r, s] - LSE[r]) * part_o[r, s, :]
  *   part_o [R, S, D] float (each normalised over its range), part_lse [R, S]
- *   float (natural log, -inf = empty range whose part_o is not read)
+ *   float (natural log, -inf = empty range whose part_o is ignored)
  *   out [R, D] of out_dtype;  lse_out [R] float or NULL
  * All ranges empty: out = 0, LSE = -inf.  D a multiple of 4, at most 1024.
  */

@@ -102,3 +102,16 @@ def test_other_entry_points_validate(lib):
     # paged: NB*BS beyond the tensor-map range
     assert lib.kvd_attend_paged(P(1), P(1), P(1), P(1), P(1), None, P(1), None, 1, 4, 4,
                                 1 << 24, 256, 4, 128, 0.1, 0, 0, None, 0, None, None) == 2
+
+
+def test_fp8_entry_points_validate(lib):
+    P = lambda x: ctypes.c_void_p(x * 4096)  # noqa: E731
+    # head_dim 96 is not supported by the quantiser
+    assert lib.kvd_append_fp8(P(1), P(1), P(1), P(1), P(1), None, 1, 1, 8, 96, 0, None, None) == 2
+    assert lib.kvd_append_fp8(P(1), P(1), P(1), P(1), None, None, 1, 1, 8, 128, 0, None, None) == 1
+    # workspace: one split needs the counters only; many splits need partials
+    assert lib.kvd_attend_masked_fp8_workspace_bytes(1, 4, 4, 32, 128, 1) == 256
+    assert lib.kvd_attend_masked_fp8_workspace_bytes(16, 32, 8, 8192, 128, 0) > 256
+    assert lib.kvd_attend_masked_fp8_workspace_bytes(1, 4, 3, 32, 128, 0) == 0
+    assert lib.kvd_attend_masked_fp8(P(1), P(1), P(1), P(1), P(1), None, 2, 8, 2, 4096, 128, 0.1, 4,
+                                     None, 0, None, None) == 3

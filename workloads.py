@@ -41,7 +41,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-SEEDS = {"tiny": 1, "npuw": 2, "gqa": 3, "paged": 4, "long": 5, "window": 6}
+SEEDS = {"tiny": 1, "npuw": 2, "gqa": 3, "paged": 4, "long": 5, "window": 6, "gqa_fp8": 7}
 
 
 def generator(seed: int, device="cpu") -> torch.Generator:
@@ -66,6 +66,24 @@ def uniform(g, shape, lo: float, hi: float, dtype=torch.float32, device="cpu"):
 def randint(g, n: int, lo: int, hi: int, device="cpu"):
     """n integers uniform in [lo, hi] (both ends included), int64."""
     return torch.randint(lo, hi + 1, (n,), generator=g, device=device, dtype=torch.int64)
+
+
+FP8_ROW_PAD = 16  # quantised rows: D E4M3 codes, fp32 scale, 12 zero bytes
+
+
+def fp8_rows(g, shape, D: int, scale_lo: float = 2e-3, scale_hi: float = 2e-2, device="cpu"):
+    """uint8 [*shape, D + 16]: quantised K/V rows with random content -- codes
+    uniform over the 254 finite E4M3 codes (0x7F and 0xFF are NaN), a scale
+    uniform in [scale_lo, scale_hi] as fp32 little-endian bytes, 12 zero
+    bytes.  Random bytes, not the result of quantising anything."""
+    shape = tuple(shape)
+    r = torch.randint(0, 254, shape + (D,), generator=g, device=device, dtype=torch.int32)
+    codes = (r + (r >= 0x7F).to(torch.int32)).to(torch.uint8)
+    scale = uniform(g, shape + (1,), scale_lo, scale_hi, torch.float32, device)
+    out = torch.zeros(shape + (D + FP8_ROW_PAD,), dtype=torch.uint8, device=device)
+    out[..., :D] = codes
+    out[..., D:D + 4] = scale.contiguous().view(torch.uint8)
+    return out
 
 
 def prefix_mask(lengths, capacity: int, device="cpu"):
@@ -226,6 +244,36 @@ def gqa(device="cpu", layers: int = 32, seed: int | None = None, B: int = 16,
     for _ in range(layers):
         w.layers.append(masked_layer(g, B, Hq, Hkv, C, D, lengths, torch.bfloat16, device,
                                      k_scale=0.5))
+    return w
+
+
+def fp8_layer(g, B, Hq, Hkv, C, D, lengths, device="cpu") -> MaskedLayer:
+    """A static-buffer layer with quantised K/V caches (random rows, see
+    fp8_rows) holding lengths[b] - 1 rows before the step; q and the step's
+    new rows in bf16."""
+    lengths = torch.as_tensor(lengths, dtype=torch.int64)
+    k = fp8_rows(g, (B, Hkv, C), D, device=device)
+    v = fp8_rows(g, (B, Hkv, C), D, device=device)
+    q = randn(g, (B, Hq, D), torch.bfloat16, device)
+    k_new = randn(g, (B, Hkv, D), torch.bfloat16, device, 0.5)
+    v_new = randn(g, (B, Hkv, D), torch.bfloat16, device)
+    return MaskedLayer(q=q, k_cache=k, v_cache=v,
+                       mask=prefix_mask((lengths - 1).clamp(min=0), C, device), k_new=k_new,
+                       v_new=v_new, pos=(lengths - 1).to(torch.int32).to(device), lengths=lengths,
+                       scale=1.0 / math.sqrt(D))
+
+
+def gqa_fp8(device="cpu", layers: int = 32, seed: int | None = None, B: int = 16,
+            Hq: int = 32, Hkv: int = 8, C: int = 8192, D: int = 128, lo: int = 512,
+            hi: int = 8192) -> MaskedWorkload:
+    """Batched GQA decode (the gqa shapes and length mix, drawn the same way)
+    over quantised caches: rows of D E4M3 codes + fp32 scale + 12 zero bytes."""
+    gl = generator(SEEDS["gqa"] if seed is None else seed, "cpu")
+    lengths = randint(gl, B, lo, hi)
+    g = generator((SEEDS["gqa_fp8"] if seed is None else seed) + 1000, device)
+    w = MaskedWorkload("gqa_fp8", B, Hq, Hkv, C, D, torch.uint8)
+    for _ in range(layers):
+        w.layers.append(fp8_layer(g, B, Hq, Hkv, C, D, lengths, device))
     return w
 
 
