@@ -188,6 +188,9 @@ class MaskedBench:
         elif name == "window":
             w = workloads.window(device=dev, **kw)
             self.cycle, self.prompt = 1, None
+        elif name == "gqa_fp8":
+            w = workloads.gqa_fp8(device=dev, **kw)
+            self.cycle, self.prompt = 1, None
         else:
             raise ValueError(name)
         self.w = w
@@ -201,7 +204,7 @@ class MaskedBench:
         self.gpos = self.pos_table[0].clone()
         need = kvd.attend_masked_workspace_bytes(self.B, self.Hq, self.Hkv, self.C, self.D)
         self.ws = kvd.workspace(need, dev)
-        self.splits = need > 0
+        self.splits = need > 256  # more than the scheduling counters: the combine runs
         self.out = [torch.empty_like(l.q) for l in w.layers]
         self.status = kvd.status_tensor(dev)
         self.lengths0 = [int(x) for x in lay0.lengths]
@@ -368,7 +371,7 @@ class PagedBench:
         cols = pw.block_tables.shape[1]
         need = kvd.attend_paged_workspace_bytes(self.Q, self.Hq, self.Hkv, self.BS, cols, self.D)
         self.ws = kvd.workspace(need, dev)
-        self.splits = need > 0
+        self.splits = need > 256  # more than the scheduling counters: the combine runs
         self.status = kvd.status_tensor(dev)
         self.graph = None
 
@@ -506,9 +509,71 @@ class IndexedBench(MaskedBench):
         return c
 
 
+class Fp8Bench(MaskedBench):
+    """The batched-GQA step over quantised caches (rows of 128 E4M3 codes +
+    fp32 scale + 12 zero bytes): every layer quantises and appends the step's
+    bf16 K/V rows, then attends over the quantised rows."""
+
+    def __init__(self, torch, kvd, dev, layers=None):
+        super().__init__("gqa_fp8", torch, kvd, dev, layers)
+        self.row = self.D + kvd.FP8_ROW_PAD
+        need = kvd.attend_masked_fp8_workspace_bytes(self.B, self.Hq, self.Hkv, self.C, self.D)
+        self.ws = kvd.workspace(need, dev)
+        self.splits = need > 256
+
+    def _layer(self, li, lay, pos):
+        self.kvd.append_fp8(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, pos, lay.mask,
+                            self.status)
+        self.kvd.attend_masked_fp8(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale,
+                                   out=self.out[li], workspace=self.ws, dev_status=self.status)
+
+    def eager_run(self, j, timing=False):
+        torch, kvd = self.torch, self.kvd
+        pos = self.pos_table[j % self.cycle]
+        evs = []
+        for li, lay in enumerate(self.w.layers):
+            if timing:
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                e[0].record()
+            kvd.append_fp8(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, pos, lay.mask,
+                           self.status)
+            if timing:
+                e[1].record()
+            kvd.attend_masked_fp8(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale,
+                                  out=self.out[li], workspace=self.ws, dev_status=self.status)
+            if timing:
+                e[2].record()
+                evs += [("append", e[0], e[1]), ("attend", e[1], e[2])]
+        return evs
+
+    def attend_bytes(self, j):
+        """Valid quantised K and V rows (codes + scale + pad), the mask row, q and out."""
+        L = self.lengths_at(j)
+        return (sum(L) * self.Hkv * self.row * 2 + self.B * self.C
+                + 2 * self.B * self.Hq * self.D * 2)
+
+    def step_bytes(self, j):
+        """Attention plus the append: bf16 new rows read, quantised rows written."""
+        app = 2 * self.B * self.Hkv * (self.D * 2 + self.row)
+        return self.layers * (self.attend_bytes(j) + app)
+
+    def copy_setup(self):
+        return False
+
+    def config(self):
+        c = super().config()
+        cache = self.layers * 2 * self.B * self.Hkv * self.C * self.row
+        c.update({"workload": "gqa_fp8", "kv_format": f"E4M3 codes + fp32 row scale, "
+                  f"{self.row}-byte rows", "l2": f"inputs larger than L2: {cache / 2**30:.2f} GiB "
+                  f"of layer caches rotated per step vs {L2_BYTES // 2**20} MiB L2"})
+        return c
+
+
 def make_bench(name, torch, kvd, dev, layers=None):
     if name == "paged":
         return PagedBench(torch, kvd, dev)
+    if name == "gqa_fp8":
+        return Fp8Bench(torch, kvd, dev, layers)
     if name == "indexed":
         return IndexedBench(torch, kvd, dev, layers)
     return MaskedBench(name, torch, kvd, dev, layers)
@@ -717,6 +782,25 @@ def oracle_rate(name, seconds, W_mod=None):
                 break
         return done_bytes / el / 1e9, oracle.threads(), \
             f"{n} layers of index-list attention (gqa caches, top-{topk}), {el:.1f} s"
+    if name == "gqa_fp8":
+        w = workloads.gqa_fp8(device="cpu", layers=1)
+        lay = w.layers[0]
+        kh, vh, mh = lay.k_cache.numpy().copy(), lay.v_cache.numpy().copy(), lay.mask.numpy().copy()
+        L = [int(x) for x in lay.lengths]
+        row = w.D + oracle.FP8_ROW_PAD
+        per = (sum(L) * w.Hkv * row * 2 + w.B * w.C + 2 * w.B * w.Hq * w.D * 2
+               + 2 * w.B * w.Hkv * (w.D * 2 + row))
+        done_bytes, t0, n = 0, time.perf_counter(), 0
+        while True:
+            oracle.append_fp8(kh, vh, lay.k_new, lay.v_new, lay.pos, mh)
+            oracle.attend_masked_fp8(lay.q, kh, vh, mh, lay.scale)
+            done_bytes += per
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+        return done_bytes / el / 1e9, oracle.threads(), \
+            f"{n} layer-steps (quantising append + attention) of the gqa_fp8 workload, {el:.1f} s"
     if name == "npuw":
         w = workloads.npuw(device="cpu", layers=4)
     elif name == "gqa":
@@ -786,7 +870,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvd", choices=["kvd", "reference"])
     ap.add_argument("--workload", default="npuw",
-                    choices=["npuw", "gqa", "long", "paged", "indexed", "window"])
+                    choices=["npuw", "gqa", "long", "paged", "indexed", "window", "gqa_fp8"])
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true",
@@ -849,7 +933,7 @@ def main():
 
     others = {}
     if not args.no_others:
-        for name in ("gqa", "long", "paged", "indexed", "window", "npuw"):
+        for name in ("gqa", "long", "paged", "indexed", "window", "gqa_fp8", "npuw"):
             if name == args.workload:
                 continue
             log(f"workload {name}")
