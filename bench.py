@@ -43,7 +43,15 @@ L2_BYTES = 129 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the attention
 # split kernel, from the ncu capture summarised in profiles/, keyed by the
 # hash of the kernel sources it was taken on (reported only while they match).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    ("npuw", "948a63acfb2a92b6"): 17376768,     # profiles/attend_kernel_npuw.md
+    ("gqa", "948a63acfb2a92b6"): 212795904,     # profiles/attend_kernel_gqa.md
+    ("long", "948a63acfb2a92b6"): 540449024,    # profiles/attend_kernel_long.md
+    ("paged", "948a63acfb2a92b6"): 521775104,   # profiles/attend_kernel_paged.md
+    ("indexed", "948a63acfb2a92b6"): 122708224,  # profiles/attend_kernel_indexed.md
+    ("window", "948a63acfb2a92b6"): 68007424,   # profiles/attend_kernel_window.md
+    ("gqa_fp8", "948a63acfb2a92b6"): 120497920,  # profiles/attend_kernel_gqa_fp8.md
+}
 
 
 # ------------------------------------------------------------ byte accounting
@@ -945,6 +953,7 @@ def main():
                    "tokens_per_s": r["tokens_per_s"], "attend_gbs": r["attend_gbs"],
                    "attend_frac": r["attend_frac"],
                    "attend_ms_per_launch": r["attend_ms_per_launch"], "eager": r["eager"],
+                   "attend_traffic": NCU_TRAFFIC.get((name, kernel_source_hash())),
                    "config": ob.config()}
             for k in ("append_ms_per_launch", "gather_gbs", "gather_frac", "gather_ms_per_launch"):
                 if k in r:
