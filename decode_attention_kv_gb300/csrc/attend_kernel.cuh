@@ -530,6 +530,11 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
             return __shfl_sync(0xffffffffu, ok, 0) != 0;
         };
         bool first = true;
+        // Scheduler 0 of the static buffer publishes its first slot without
+        // the lookahead gate: the loader waits for that slot first (its
+        // unit's first tiles were loaded speculatively) and takes no other
+        // ring's units off the lookahead count until then.
+        bool gated = !(MODE == kModeMasked && sw == 0 && p.units < n_sched);
         while (true) {
             const int slot = sw * kRingSlots + pos;
             if (!warp_wait(&ctl.qempty[slot], sphase ^ 1u, ctl.abort_flag)) {
@@ -537,7 +542,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                 break;
             }
             if (!first) {
-                if (!below_lookahead()) {
+                if (gated && !below_lookahead()) {
                     failed = true;
                     break;
                 }
@@ -574,6 +579,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                 }
                 __syncwarp();
                 publish(slot);
+                gated = true;
             } else if (p.direct) {
                 // the whole row is empty: zeros and lse = -inf
                 for (int idx = lane; idx < un.g_here * D; idx += 32)
@@ -644,9 +650,66 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                 phase ^= 1u;
             }
         };
+        // Static buffer with fewer units than scheduler warps (a launch
+        // bounded by latency, every CTA starting on a leading split): the
+        // first tiles of scheduler 0's first unit are loaded before its mask
+        // is read (their addresses need no metadata) and delivered when that
+        // unit's slot arrives -- as its tiles if the slot holds that unit,
+        // else (the unit was empty) as empty tiles the consumers only
+        // release.  Each carries q, so any of them can open the unit.
+        int spec_n = 0, spec_unit = -1;
+        uint32_t spec_mask = 0;  // stages issued but not yet delivered
+        if constexpr (MODE == kModeMasked) {
+            const int n_sched = kSchedWarps * (int)gridDim.x;
+            const int u0 = (int)blockIdx.x;  // scheduler 0's first unit when units < n_sched
+            if (p.units < n_sched && u0 < p.units) {
+                const Unit un0 = decode_unit(p, G, u0);
+                const SplitRange r = split_range<MODE>(p, un0.bz, un0.split, false);
+                spec_unit = u0;
+                spec_n = min(STAGES, r.ntiles);
+                const uint32_t qbytes = (uint32_t)(un0.g_here * D * sizeof(Elem));
+                for (int i = 0; i < spec_n; ++i) {
+                    if (!acquire()) break;  // the ring is empty: returns at once
+                    if (lane == 0) {
+                        const int n = min(p.tile, r.ntok - i * p.tile);
+                        unsigned char* sk = smem + stage * Sh::kStageBytes;
+                        unsigned char* sv = sk + Cons::kTileBytes;
+                        unsigned char* sq = sv + Cons::kTileBytes;
+                        const size_t rowidx =
+                            ((size_t)un0.bz * p.Hkv + un0.kvh) * p.C + r.t_begin + i * p.tile;
+                        if constexpr (Cons::kSwizzled) {
+                            mbar_expect_tx(&ctl.full[stage], 2u * kHalves * p.tile * 128u + qbytes);
+#pragma unroll
+                            for (int h = 0; h < kHalves; ++h) {
+                                tma_g2s_2d(sk + h * Cons::kTileBytes / kHalves, &kmap, 64 * h,
+                                           (int)rowidx, &ctl.full[stage], pol);
+                                tma_g2s_2d(sv + h * Cons::kTileBytes / kHalves, &vmap, 64 * h,
+                                           (int)rowidx, &ctl.full[stage], pol);
+                            }
+                        } else {
+                            const uint32_t bytes = (uint32_t)n * Cons::kRowBytes;
+                            mbar_expect_tx(&ctl.full[stage], 2u * bytes + qbytes);
+                            bulk_g2s(sk, static_cast<const unsigned char*>(p.k) + rowidx * Cons::kRowBytes,
+                                     bytes, &ctl.full[stage], pol);
+                            bulk_g2s(sv, static_cast<const unsigned char*>(p.v) + rowidx * Cons::kRowBytes,
+                                     bytes, &ctl.full[stage], pol);
+                        }
+                        bulk_g2s(sq, static_cast<const Elem*>(p.q) + un0.qrow0 * D, qbytes,
+                                 &ctl.full[stage], pol);
+                        issued_mask |= 1u << stage;
+                        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                    }
+                    spec_mask |= 1u << stage;
+                    __syncwarp();
+                    advance();
+                }
+                if (failed) spec_n = 0;
+            }
+        }
         // Scheduler rings: position and parity of each ring's head, which
         // rings have not ended yet; the loader takes whichever head is ready,
-        // starting with the ring it did not take last.
+        // starting with the ring it did not take last (scheduler 0's ring
+        // first while speculated tiles wait for it).
         int rpos[kSchedWarps] = {};
         uint32_t rphase = 0, live = (1u << kSchedWarps) - 1u;
         int pref = 0;
@@ -658,6 +721,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
                     for (int k = 0; k < kSchedWarps; ++k) {
                         const int rr = (pref + k) % kSchedWarps;
+                        if (spec_n > 0 && rr != 0) continue;
                         int hp = 0;
 #pragma unroll
                         for (int q = 0; q < kSchedWarps; ++q) hp = q == rr ? rpos[q] : hp;
@@ -693,15 +757,43 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                 }
             pref = (pick + 1) % kSchedWarps;
             const UnitSlot& sl = ctl.slots[slot];
+            bool first = true;
+            int counted = 0;  // tiles already taken off ctl.pending
+            int i_start = 0;
+            if (spec_n > 0) {
+                // deliver the speculated stages (the oldest ones, in ring order)
+                const bool same = sl.kind != kSlotEnd && sl.unit == spec_unit;
+                int sstage = 0;  // speculation started at stage 0, phase 0
+                for (int i = 0; i < spec_n; ++i, ++sstage) {
+                    uint64_t bits = 0;
+                    if (same && i <= sl.last)
+                        bits = tile_bits(sl.words, i * p.tile, min(p.tile, sl.ntok - i * p.tile));
+                    if (lane == 0) {
+                        StageMeta& mt = ctl.meta[sstage];
+                        mt.unit = same ? sl.unit : 0;
+                        mt.tile = i;
+                        mt.flags = bits ? ((first ? kFirst : 0u) | (i == sl.last ? kLast : 0u)) : 0u;
+                        mt.bits = bits;
+                        if (same && i <= sl.last) {
+                            atomicAdd(ctl.pending, -(i + 1 - counted) * p.tile);
+                            counted = i + 1;
+                        }
+                        mbar_arrive(&ctl.full[sstage]);
+                    }
+                    if (bits) first = false;
+                }
+                __syncwarp();
+                spec_mask = 0;
+                i_start = same ? spec_n : 0;
+                spec_n = 0;
+            }
             if (sl.kind == kSlotEnd) {
                 live &= ~(1u << pick);
                 continue;
             }
             const Unit un = decode_unit(p, G, sl.unit);
             const int t_begin = sl.t_begin, ntok = sl.ntok, last = sl.last, lb0 = sl.lb0;
-            bool first = true;
-            int counted = 0;  // tiles already taken off ctl.pending
-            for (int i = 0; i <= last; ++i) {
+            for (int i = i_start; i <= last; ++i) {
                 const int r0 = i * p.tile;
                 const int n = min(p.tile, ntok - r0);
                 const uint64_t bits = tile_bits(sl.words, r0, n);
@@ -829,6 +921,8 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
         if (failed && lane == 0) {
             *ctl.abort_flag = 1;
             report(p.dev_status, KVD_DEV_TIMEOUT);
+            for (int s = 0; s < STAGES; ++s)  // speculated stages never delivered
+                if (spec_mask & (1u << s)) mbar_arrive(&ctl.full[s]);
             // The consumers may leave early now: never let the CTA exit while a
             // copy issued here may still be writing the ring.  (On the normal
             // path the consumers have waited for every issued tile before they
@@ -880,7 +974,9 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
             cons.begin(reinterpret_cast<const Elem*>(sb + 2 * Cons::kTileBytes), un.g_here,
                        p.qscale, lane);
         }
-        const bool wrote = cons.tile(sb, sb + Cons::kTileBytes, mt.bits, warp, lane, p.qscale);
+        // an empty tile (a speculated tile of a unit that turned out empty) is only released
+        const bool wrote =
+            mt.bits ? cons.tile(sb, sb + Cons::kTileBytes, mt.bits, warp, lane, p.qscale) : false;
         // generic-proxy writes to the ring must be ordered before the next TMA
         // write into this stage
         if (wrote) fence_proxy_async_smem();

@@ -240,3 +240,24 @@ def test_skip_scale_paths(kvd, dtype, Hq, Hkv):
     ref, ref_lse = oracle.attend_masked(q, k, v, mask, scale)
     assert_attention_close(out, ref, dtype, "skip-scale")
     assert_lse_close(lse, ref_lse, "skip-scale")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(32, 32), (32, 8), (16, 2)])
+@pytest.mark.parametrize("start", [0, 40, 200, 1000])
+def test_leading_tiles_empty_or_valid(kvd, Hq, Hkv, start):
+    """Small launches (fewer units than scheduler warps) load the first tiles
+    of a CTA's first unit before its mask is read: masks whose valid slots
+    start inside or after that unit's tiles ([start, start + 150)), and one
+    batch entry whose row is empty, give the oracle's result."""
+    B, C, D = 2, 1152, 128
+    g = W.generator(900 + start + Hq)
+    q = W.randn(g, (B, Hq, D))
+    k = W.randn(g, (B, Hkv, C, D))
+    v = W.randn(g, (B, Hkv, C, D))
+    mask = torch.zeros(B, C, dtype=torch.uint8)
+    mask[0, start:start + 150] = 1
+    out, lse = _run_masked(kvd, q, k, v, mask, 0.1)
+    ref, ref_lse = oracle.attend_masked(q, k, v, mask, 0.1)
+    assert_attention_close(out, ref, torch.bfloat16, f"leading tiles from {start}")
+    assert_lse_close(lse, ref_lse)
+    assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
