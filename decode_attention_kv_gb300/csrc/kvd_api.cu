@@ -63,6 +63,7 @@ bool dtype_ok(kvd_dtype dt) { return dt == KVD_BF16 || dt == KVD_F32; }
 // handed out split-major, so these small units are the last ones taken and
 // the CTAs finish within a small unit of each other.
 constexpr long long kTargetUnits = 2048;
+constexpr long long kGridUnitsHint = 304;  // persistent CTAs on GB300: 2 per SM x 152 SMs
 constexpr int kMinChunk = 128;
 
 struct Plan {
@@ -142,7 +143,11 @@ Plan plan_attention(int rows, int Hq, int Hkv, int cap, int D, kvd_dtype dt, int
     pl.S = pl.Sb = (int)(((long long)cap + chunk - 1) / chunk);
     if (pl.S < 1) pl.S = pl.Sb = 1;
     const long long small = ((chunk / 4) + unit - 1) / unit * unit;
-    if (num_splits <= 0 && pl.S > 1 && small < chunk) {
+    // A launch whose units all fit the persistent grid at once (one unit per
+    // CTA) keeps equal splits: small tail splits would only give some CTAs a
+    // second unit.
+    const bool fits_grid = row_units * pl.S <= kGridUnitsHint;
+    if (num_splits <= 0 && pl.S > 1 && small < chunk && !fits_grid) {
         const int tail = pl.S / 4 > 1 ? pl.S / 4 : 1;  // big splits turned into small ones
         pl.Sb = pl.S - tail;
         pl.chunk2 = (int)small;
