@@ -229,29 +229,27 @@ class MaskedBench:
             self.reset_cycle()
 
     def _layer(self, li, lay, pos):
-        self.kvd.append(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, pos, lay.mask, self.status)
-        self.kvd.attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale,
-                               out=self.out[li], workspace=self.ws, dev_status=self.status)
+        """The layer's decode step: append + attention in one call (one
+        launch and the combine)."""
+        self.kvd.append_attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.k_new,
+                                      lay.v_new, pos, lay.scale, out=self.out[li],
+                                      workspace=self.ws, dev_status=self.status)
 
     def eager_run(self, j, timing=False):
-        """One step, one binding call per kernel; with timing, CUDA events
+        """One step, one binding call per layer; with timing, CUDA events
         around each call."""
-        torch, kvd = self.torch, self.kvd
+        torch = self.torch
         self._wrap(j)
         pos = self.pos_table[j % self.cycle]
         evs = []
         for li, lay in enumerate(self.w.layers):
             if timing:
-                e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
                 e[0].record()
-            kvd.append(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, pos, lay.mask, self.status)
+            self._layer(li, lay, pos)
             if timing:
                 e[1].record()
-            kvd.attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale,
-                              out=self.out[li], workspace=self.ws, dev_status=self.status)
-            if timing:
-                e[2].record()
-                evs += [("append", e[0], e[1]), ("attend", e[1], e[2])]
+                evs.append(("attend", e[0], e[1]))
         return evs
 
     def capture(self):
@@ -297,7 +295,7 @@ class MaskedBench:
         return 4 * self.layers * self.B * self.Hkv * self.prompt * self.D * self.elem
 
     def launches_per_step(self):
-        return self.layers * (2 + (1 if self.splits else 0))
+        return self.layers * (1 + (1 if self.splits else 0))
 
     def lengths_at(self, j):
         return [L + (j % self.cycle) for L in self.lengths0]
@@ -502,6 +500,9 @@ class IndexedBench(MaskedBench):
                 evs += [("append", e[0], e[1]), ("attend", e[1], e[2])]
         return evs
 
+    def launches_per_step(self):
+        return self.layers * (2 + (1 if self.splits else 0))  # append, attention, combine
+
     def attend_bytes(self, j):
         """Listed K and V rows of every kv head, the index lists, q and out."""
         return (sum(self.listed) * self.Hkv * self.D * 2 * self.elem + self.B * self.TOPK * 4
@@ -553,6 +554,9 @@ class Fp8Bench(MaskedBench):
                 e[2].record()
                 evs += [("append", e[0], e[1]), ("attend", e[1], e[2])]
         return evs
+
+    def launches_per_step(self):
+        return self.layers * (2 + (1 if self.splits else 0))  # append_fp8, attention, combine
 
     def attend_bytes(self, j):
         """Valid quantised K and V rows (codes + scale + pad), the mask row, q and out."""

@@ -96,6 +96,12 @@ struct AttendParams {
     float qscale;                // scale * log2(e)
     int direct;                  // S == 1: units write the output rows directly
     int look;                    // a scheduler takes a unit only below this many queued tokens
+    // fused append (static buffer, one head group per kv head): the step's rows
+    // k_new/v_new [rows, Hkv, D] go to slot pos[b] of the caches and the mask
+    const void* k_new;           // null: no append
+    const void* v_new;
+    const int32_t* pos;          // [rows]
+    uint8_t* mask_w;             // the mask, written at pos
 };
 
 enum : uint32_t { kFirst = 1u, kLast = 2u, kCombine = 4u, kEnd = 8u };
@@ -384,6 +390,43 @@ __device__ __forceinline__ int producer_scan(const AttendParams& p, const SplitR
     return lb0;
 }
 
+// Fused append ("Intel NPU running LLMs", Part 2, update_kvcache_for): the
+// unit whose token range holds pos[b] writes the step's K/V rows of its kv
+// head into the cache at pos[b] (kv head 0 also sets the mask slot) before it
+// is published, and counts pos[b] as valid; the loader's copies of the unit,
+// issued after the slot is published, read the new rows (the proxy fence
+// orders the plain stores before them).  Every (row, kv head) has exactly one
+// such unit (one head group per kv head).  A pos outside [0, C) writes
+// nothing and is reported once per batch entry.
+template <typename Elem, int D>
+__device__ __forceinline__ void fused_append(const AttendParams& p, const Unit& un,
+                                             const SplitRange& r, int lane, uint32_t* words) {
+    const int pb = __ldg(p.pos + un.bz);
+    if (pb < 0 || pb >= p.C) {
+        if (lane == 0 && un.kvh == 0 && un.hg == 0 && un.split == 0)
+            report(p.dev_status, KVD_DEV_POS_RANGE);
+        return;
+    }
+    if (pb < r.t_begin || pb >= r.t_end) return;
+    constexpr int kWords = D * (int)sizeof(Elem) / 4;  // 32-bit words of a row
+    const size_t src = ((size_t)un.bz * p.Hkv + un.kvh) * D;
+    const size_t dst = (((size_t)un.bz * p.Hkv + un.kvh) * p.C + pb) * D;
+    const uint32_t* ks = reinterpret_cast<const uint32_t*>(static_cast<const Elem*>(p.k_new) + src);
+    const uint32_t* vs = reinterpret_cast<const uint32_t*>(static_cast<const Elem*>(p.v_new) + src);
+    uint32_t* kd = reinterpret_cast<uint32_t*>(const_cast<Elem*>(static_cast<const Elem*>(p.k) + dst));
+    uint32_t* vd = reinterpret_cast<uint32_t*>(const_cast<Elem*>(static_cast<const Elem*>(p.v) + dst));
+#pragma unroll
+    for (int i = lane; i < kWords; i += 32) {
+        kd[i] = __ldg(ks + i);
+        vd[i] = __ldg(vs + i);
+    }
+    if (lane == 0 && un.kvh == 0 && p.mask_w) p.mask_w[(size_t)un.bz * p.C + pb] = 1;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) words[(pb - r.t_begin) >> 5] |= 1u << ((pb - r.t_begin) & 31);
+    __syncwarp();
+}
+
 // One warp turns the consumer warps' states of a unit (mo[w][h][d] and
 // ml[w][h] = (m, l) in a merge buffer) into the unit's rows: the final output
 // (single split) or a normalised partial row and its natural-log log-sum-exp.
@@ -561,6 +604,9 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
             const SplitRange r = split_range<MODE>(
                 p, un.bz, un.split, lane == 0 && un.split == 0 && un.kvh == 0 && un.hg == 0);
             const int lb0 = producer_scan<MODE>(p, r, un.bz, lane, sl.words, sl.blocks);
+            if constexpr (MODE == kModeMasked) {
+                if (p.pos) fused_append<Elem, D>(p, un, r, lane, sl.words);
+            }
             int last = -1;
             for (int i = r.ntiles - 1; i >= 0; --i)
                 if (tile_bits(sl.words, i * p.tile, min(p.tile, r.ntok - i * p.tile))) {
@@ -667,6 +713,10 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                 const SplitRange r = split_range<MODE>(p, un0.bz, un0.split, false);
                 spec_unit = u0;
                 spec_n = min(STAGES, r.ntiles);
+                if (p.pos) {  // never before the tile the fused append writes into
+                    const int pb = __ldg(p.pos + un0.bz);
+                    if (pb >= r.t_begin && pb < r.t_end) spec_n = min(spec_n, (pb - r.t_begin) / p.tile);
+                }
                 const uint32_t qbytes = (uint32_t)(un0.g_here * D * sizeof(Elem));
                 for (int i = 0; i < spec_n; ++i) {
                     if (!acquire()) break;  // the ring is empty: returns at once

@@ -336,23 +336,29 @@ size_t kvd_attend_masked_workspace_bytes(int B, int Hq, int Hkv, int C, int D, k
     return plan_attention(B, Hq, Hkv, C, D, dtype, 0, num_splits).ws;
 }
 
-kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_cache,
-                             const uint8_t* mask, void* out, float* lse_out, int B, int Hq,
-                             int Hkv, int C, int D, float scale, kvd_dtype dtype, int num_splits,
-                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                             kvd_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// kvd_attend_masked, with the step's append fused into the launch when k_new
+// is given (the caller has checked that a kv head has one head group).
+kvd_status attend_masked_impl(const char* fn, const void* q, const void* k_cache,
+                              const void* v_cache, const uint8_t* mask, void* out,
+                              float* lse_out, int B, int Hq, int Hkv, int C, int D, float scale,
+                              kvd_dtype dtype, int num_splits, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_status, kvd_stream_t stream,
+                              const void* k_new, const void* v_new, const int32_t* pos) {
     kvd_status st = check_attention_shape(Hq, Hkv, D, dtype);
     if (st != KVD_OK) return st;
-    if (B < 0 || C < 1) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked: B >= 0 and C >= 1 required");
+    if (B < 0 || C < 1) return fail(KVD_ERR_INVALID_ARG, "%s: B >= 0 and C >= 1 required", fn);
     if (B == 0) return ok();
     if (!q || !k_cache || !v_cache || !mask || !out)
-        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked: null pointer");
+        return fail(KVD_ERR_INVALID_ARG, "%s: null pointer", fn);
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         !aligned(lse_out, 4) || !aligned(dev_status, 4))
-        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked: misaligned pointer");
-    if (num_splits < 0) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked: num_splits < 0");
+        return fail(KVD_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+    if (num_splits < 0) return fail(KVD_ERR_INVALID_ARG, "%s: num_splits < 0", fn);
     const Plan pl = plan_attention(B, Hq, Hkv, C, D, dtype, 0, num_splits);
-    st = check_workspace("kvd_attend_masked", pl, workspace, workspace_bytes);
+    st = check_workspace(fn, pl, workspace, workspace_bytes);
     if (st != KVD_OK) return st;
     AttendParams p{};
     p.q = q;
@@ -368,6 +374,10 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
     p.C = C;
     p.mask_vec = (C % 16 == 0) && aligned(mask, 16);
     p.qscale = scale * kLog2e;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.pos = k_new ? pos : nullptr;
+    p.mask_w = const_cast<uint8_t*>(mask);
     attach_workspace(p, pl, workspace);
     CUtensorMap kmap, vmap;
     std::memset(&kmap, 0, sizeof kmap);
@@ -375,20 +385,61 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
     if (attend_uses_mma(dtype, pl.G)) {
         const long long rows = (long long)B * Hkv * C;
         if (rows >= (1ll << 31))
-            return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_masked: B*Hkv*C >= 2^31 rows");
+            return fail(KVD_ERR_UNSUPPORTED, "%s: B*Hkv*C >= 2^31 rows", fn);
         st = make_cache_map(&kmap, k_cache, dtype, false, rows, Hkv, D, pl.tile, true);
         if (st != KVD_OK) return st;
         st = make_cache_map(&vmap, v_cache, dtype, false, rows, Hkv, D, pl.tile, true);
         if (st != KVD_OK) return st;
     }
     cudaError_t e = launch_attend(dtype, D, pl.G, kModeMasked, p, &kmap, &vmap, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked launch");
+    if (e != cudaSuccess) return cuda_fail(e, fn);
     if (pl.S > 1) {
         e = launch_combine(p.part_o, p.part_lse, out, lse_out, B * Hq, pl.S, D, dtype,
                            (cudaStream_t)stream);
-        if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked combine launch");
+        if (e != cudaSuccess) return cuda_fail(e, fn);
     }
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_cache,
+                             const uint8_t* mask, void* out, float* lse_out, int B, int Hq,
+                             int Hkv, int C, int D, float scale, kvd_dtype dtype, int num_splits,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             kvd_stream_t stream) {
+    return attend_masked_impl("kvd_attend_masked", q, k_cache, v_cache, mask, out, lse_out, B, Hq,
+                              Hkv, C, D, scale, dtype, num_splits, workspace, workspace_bytes,
+                              dev_status, stream, nullptr, nullptr, nullptr);
+}
+
+kvd_status kvd_append_attend_masked(const void* q, void* k_cache, void* v_cache, uint8_t* mask,
+                                    const void* k_new, const void* v_new, const int32_t* pos,
+                                    void* out, float* lse_out, int B, int Hq, int Hkv, int C,
+                                    int D, float scale, kvd_dtype dtype, int num_splits,
+                                    void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                    kvd_stream_t stream) {
+    const char* fn = "kvd_append_attend_masked";
+    if (B == 0) return ok();
+    if (!k_new || !v_new || !pos) return fail(KVD_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(pos, 4))
+        return fail(KVD_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+    const kvd_status st = check_attention_shape(Hq, Hkv, D, dtype);
+    if (st != KVD_OK) return st;
+    if (group_width(Hq / Hkv) < Hq / Hkv) {
+        // several head groups per kv head: the append first, then the attention
+        const kvd_status sa = kvd_append(k_cache, v_cache, k_new, v_new, pos, mask, B, Hkv, C, D,
+                                         dtype, dev_status, stream);
+        if (sa != KVD_OK) return sa;
+        return attend_masked_impl(fn, q, k_cache, v_cache, mask, out, lse_out, B, Hq, Hkv, C, D,
+                                  scale, dtype, num_splits, workspace, workspace_bytes, dev_status,
+                                  stream, nullptr, nullptr, nullptr);
+    }
+    return attend_masked_impl(fn, q, k_cache, v_cache, mask, out, lse_out, B, Hq, Hkv, C, D, scale,
+                              dtype, num_splits, workspace, workspace_bytes, dev_status, stream,
+                              k_new, v_new, pos);
 }
 
 kvd_status kvd_append_fp8(void* k_cache, void* v_cache, const void* k_new, const void* v_new,

@@ -37,6 +37,8 @@ SIGNATURES = {
                            _vp, _vp], _i),
     "kvd_attend_masked_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i,
                                    _vp, _vp], _i),
+    "kvd_append_attend_masked": ([_vp] * 7 + [_vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz,
+                                  _vp, _vp], _i),
     "kvd_append_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp], _i),
     "kvd_attend_masked_fp8_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
     "kvd_attend_masked_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz,
@@ -317,6 +319,40 @@ def attend_masked(q, k_cache, v_cache, mask, scale=None, out=None, lse=None, num
                              _ptr(lse), B, Hq, Hkv, C, D, float(scale), dt, num_splits, _ptr(ws),
                              wsb, _ptr(dev_status), _stream(q.device))
     _check("kvd_attend_masked", st)
+    return out
+
+
+def append_attend_masked(q, k_cache, v_cache, mask, k_new, v_new, pos, scale=None, out=None,
+                         lse=None, num_splits=0, workspace=None, dev_status=None):
+    """kvd_append_attend_masked: kvd_append then kvd_attend_masked in one call
+    (one launch when Hq / Hkv <= 8).  Returns out [B, Hq, D]."""
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("mask", mask),
+                 ("k_new", k_new), ("v_new", v_new), ("pos", pos)):
+        _cuda_contig(n, t)
+    B, Hq, D = q.shape
+    Bk, Hkv, C, Dk = k_cache.shape
+    if Bk != B or Dk != D or v_cache.shape != k_cache.shape or mask.shape != (B, C) or \
+            k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D):
+        raise ValueError("append_attend_masked: shape mismatch")
+    if mask.dtype != torch.uint8 or pos.dtype != torch.int32 or pos.numel() != B:
+        raise ValueError("append_attend_masked: mask uint8 [B, C], pos int32 [B]")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype == k_new.dtype == v_new.dtype):
+        raise TypeError("append_attend_masked: q, caches and new rows must share a dtype")
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is not None:
+        _cuda_contig("lse", lse)
+    L = load()
+    need = L.kvd_attend_masked_workspace_bytes(B, Hq, Hkv, C, D, dt, num_splits)
+    ws, wsb = _workspace(need, q.device, workspace)
+    st = L.kvd_append_attend_masked(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(mask), _ptr(k_new),
+                                    _ptr(v_new), _ptr(pos), _ptr(out), _ptr(lse), B, Hq, Hkv, C,
+                                    D, float(scale), dt, num_splits, _ptr(ws), wsb,
+                                    _ptr(dev_status), _stream(q.device))
+    _check("kvd_append_attend_masked", st)
     return out
 
 

@@ -179,6 +179,28 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
  * TMA tensor map (NB*BS < 2^31).
  */
 /*
+ * kvd_append_attend_masked -- one decode step over the static buffer: the
+ * result of kvd_append(k_cache, v_cache, k_new, v_new, pos, mask) followed by
+ * kvd_attend_masked(q, k_cache, v_cache, mask, ...) ([NPU] Part 2,
+ * update_kvcache_for, then Part 3), with the append done inside the
+ * attention launch when every kv head has a single group of query heads
+ * (Hq / Hkv <= 8): the split holding pos[b] writes the new rows of its kv
+ * head and kv head 0's split sets mask[b, pos[b]], before that split's tiles
+ * are read.  Larger groups run the append kernel first.  Arguments as for
+ * the two calls (k_new, v_new [B, Hkv, D] of `dtype`, pos [B] int32, mask
+ * written); the caches, the mask and the output end exactly as after the two
+ * calls.  pos[b] outside [0, C) writes nothing for b and sets
+ * KVD_DEV_POS_RANGE; the attention then runs over the mask as it is.
+ * Workspace: kvd_attend_masked_workspace_bytes.
+ */
+kvd_status kvd_append_attend_masked(const void* q, void* k_cache, void* v_cache, uint8_t* mask,
+                                    const void* k_new, const void* v_new, const int32_t* pos,
+                                    void* out, float* lse_out, int B, int Hq, int Hkv, int C,
+                                    int D, float scale, kvd_dtype dtype, int num_splits,
+                                    void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                    kvd_stream_t stream);
+
+/*
  * kvd_attend_indexed -- decode attention over a list of cache slots per batch
  * entry ([FlashMLA] "Математическая постановка": the indexer's top-k indices
  * pick the KV rows, P = Q . gathered^T, S = softmax(P * sm_scale),
