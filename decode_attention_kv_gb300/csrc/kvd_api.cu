@@ -21,6 +21,10 @@ cudaError_t launch_attend_f32(int D, int G, int mode, const AttendParams& p,
 AttendGeom attend_geom_bf16(int D, int G);
 AttendGeom attend_geom_f32(int D, int G);
 cudaError_t launch_attend_fp8(int D, int G, const AttendParams& p, cudaStream_t stream);
+cudaError_t launch_attend_small(kvd_dtype dt, int D, int G, const AttendParams& p, int S, int rows,
+                                const CUtensorMap* kmap, const CUtensorMap* vmap,
+                                cudaStream_t stream);
+int small_shared_bytes(kvd_dtype dt, int D, int G, int chunk);
 }  // namespace kvd
 
 using namespace kvd;
@@ -64,6 +68,10 @@ bool dtype_ok(kvd_dtype dt) { return dt == KVD_BF16 || dt == KVD_F32; }
 // the CTAs finish within a small unit of each other.
 constexpr long long kTargetUnits = 2048;
 constexpr long long kGridUnitsHint = 304;  // persistent CTAs on GB300: 2 per SM x 152 SMs
+// Small static-buffer launches (one CTA per (row, split), a cluster per row)
+constexpr int kSmallSplits = 8;            // splits per row: the portable cluster size
+constexpr int kSmallTokens = 384;          // tokens per split, all resident
+constexpr int kSmallShared = 113 * 1024;   // shared memory per CTA: two CTAs per SM
 constexpr int kMinChunk = 128;
 
 struct Plan {
@@ -390,6 +398,24 @@ kvd_status attend_masked_impl(const char* fn, const void* q, const void* k_cache
         if (st != KVD_OK) return st;
         st = make_cache_map(&vmap, v_cache, dtype, false, rows, Hkv, D, pl.tile, true);
         if (st != KVD_OK) return st;
+    }
+    if (num_splits == 0) {
+        // Small launch: every split of every row resident at once in a
+        // cluster of at most 8 CTAs that merges the row itself
+        const int T = pl.tile;
+        const long long rows = (long long)B * Hkv * pl.HG;
+        const int chunk = (int)(((C + kSmallSplits - 1) / kSmallSplits + T - 1) / T * T);
+        const int S = (C + chunk - 1) / chunk;
+        if (chunk <= kSmallTokens && rows * S <= kGridUnitsHint && rows <= 65535 &&
+            small_shared_bytes(dtype, D, pl.G, chunk) <= kSmallShared) {
+            AttendParams ps = p;
+            ps.chunk = chunk;
+            ps.S = S;
+            const cudaError_t e = launch_attend_small(dtype, D, pl.G, ps, S, (int)rows, &kmap,
+                                                      &vmap, (cudaStream_t)stream);
+            if (e != cudaSuccess) return cuda_fail(e, fn);
+            return ok();
+        }
     }
     cudaError_t e = launch_attend(dtype, D, pl.G, kModeMasked, p, &kmap, &vmap, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, fn);
