@@ -115,16 +115,7 @@ attend_small_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
     pdl_wait();
     __syncthreads();
 
-    int pb = -1;  // fused append: this CTA's slot of the new row, or -1
-    if (p.pos) {
-        const int x = __ldg(p.pos + bz);
-        if (x < 0 || x >= p.C) {
-            if (threadIdx.x == 0 && split == 0 && kvh == 0 && hg == 0)
-                report(p.dev_status, KVD_DEV_POS_RANGE);
-        } else if (x >= t_begin && x < t_end) {
-            pb = x;
-        }
-    }
+    int pb = -1;  // fused append (warp NCW): this CTA's slot of the new row, or -1
     if (warp == NCW) {
         const uint64_t pol = policy_evict_first();
         if (lane == 0) {
@@ -154,16 +145,47 @@ attend_small_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
             }
             bulk_g2s(smem + L.q_off, static_cast<const Elem*>(p.q) + qrow0 * D, qbytes, bar, pol);
         }
-        // validity words of the split (read while the copies fly)
+        // the new row's slot and the split's validity words, read while the
+        // copies fly (all loads issued before any is used)
+        const int x = p.pos ? __ldg(p.pos + bz) : -1;
         const uint8_t* mrow = p.mask + (size_t)bz * p.C;
         const int nwords = (ntiles * T + 31) / 32;
-        for (int j = 0; j < nwords; ++j) {
-            const int tok = t_begin + 32 * j + lane;
-            const bool v = tok < t_end && mrow[tok] != 0;
-            const uint32_t w = __ballot_sync(0xffffffffu, v);
-            if (lane == 0) words[j] = w;
+        if (p.mask_vec) {
+            // 16 slots per lane (t_begin is a multiple of 32, the rows 16-byte aligned)
+            const int nvec = (ntok + 15) / 16;
+            uint32_t bits = 0;
+            if (lane < nvec) {
+                const uint4 mv = __ldg(reinterpret_cast<const uint4*>(mrow + t_begin) + lane);
+                bits = nonzero_bytes(mv.x) | (nonzero_bytes(mv.y) << 4) |
+                       (nonzero_bytes(mv.z) << 8) | (nonzero_bytes(mv.w) << 12);
+                const int nv = min(ntok - lane * 16, 16);
+                bits &= nv >= 16 ? 0xffffu : ((1u << nv) - 1u);
+            }
+            const uint32_t hi = __shfl_down_sync(0xffffffffu, bits, 1);
+            if ((lane & 1) == 0 && (lane >> 1) < nwords) words[lane >> 1] = bits | (hi << 16);
+        } else {
+            constexpr int kW = kSmallMaxTokens / 32;
+            uint8_t mb[kW];
+#pragma unroll
+            for (int j = 0; j < kW; ++j) {
+                const int tok = t_begin + 32 * j + lane;
+                mb[j] = (j < nwords && tok < t_end) ? __ldg(mrow + tok) : 0;
+            }
+#pragma unroll
+            for (int j = 0; j < kW; ++j) {
+                const uint32_t w = __ballot_sync(0xffffffffu, mb[j] != 0);
+                if (lane == 0 && j < nwords) words[j] = w;
+            }
         }
         __syncwarp();
+        if (p.pos) {
+            if (x < 0 || x >= p.C) {
+                if (lane == 0 && split == 0 && kvh == 0 && hg == 0)
+                    report(p.dev_status, KVD_DEV_POS_RANGE);
+            } else if (x >= t_begin && x < t_end) {
+                pb = x;
+            }
+        }
         if (pb >= 0) {
             // fused append: the cache row (head group 0 writes it), the mask
             // slot (kv head 0) and the validity bit
