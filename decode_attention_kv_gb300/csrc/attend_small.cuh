@@ -151,7 +151,7 @@ attend_small_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
         const uint8_t* mrow = p.mask + (size_t)bz * p.C;
         const int nwords = (ntiles * T + 31) / 32;
         if (p.mask_vec) {
-            // 16 slots per lane (t_begin is a multiple of 32, the rows 16-byte aligned)
+            // 16 slots per lane (t_begin is a multiple of 16, the rows 16-byte aligned)
             const int nvec = (ntok + 15) / 16;
             uint32_t bits = 0;
             if (lane < nvec) {

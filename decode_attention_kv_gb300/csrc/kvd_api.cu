@@ -402,9 +402,12 @@ kvd_status attend_masked_impl(const char* fn, const void* q, const void* k_cache
     if (num_splits == 0) {
         // Small launch: every split of every row resident at once in a
         // cluster of at most 8 CTAs that merges the row itself
+        // splits as equal as the copies allow: whole 64-row boxes for the
+        // tensor-core layout, any 16 rows for row copies (16-byte mask vectors)
         const int T = pl.tile;
+        const int q = attend_uses_mma(dtype, pl.G) ? T : 16;
         const long long rows = (long long)B * Hkv * pl.HG;
-        const int chunk = (int)(((C + kSmallSplits - 1) / kSmallSplits + T - 1) / T * T);
+        const int chunk = (int)(((C + kSmallSplits - 1) / kSmallSplits + q - 1) / q * q);
         const int S = (C + chunk - 1) / chunk;
         if (chunk <= kSmallTokens && rows * S <= kGridUnitsHint && rows <= 65535 &&
             small_shared_bytes(dtype, D, pl.G, chunk) <= kSmallShared) {
