@@ -295,7 +295,10 @@ class MaskedBench:
         return 4 * self.layers * self.B * self.Hkv * self.prompt * self.D * self.elem
 
     def launches_per_step(self):
-        return self.layers * (1 + (1 if self.splits else 0))
+        """One fused append + attention call per layer: one launch (the
+        small-launch kernel) or two (the split kernel and the combine)."""
+        return self.layers * self.kvd.attend_masked_launches(self.B, self.Hq, self.Hkv, self.C,
+                                                             self.D)
 
     def lengths_at(self, j):
         return [L + (j % self.cycle) for L in self.lengths0]
@@ -1008,7 +1011,7 @@ def main():
                       "(all layers' kvd kernels); 'eager' = one binding call per kernel",
             "roofline": {"bound": "hbm", "achieved": res["attend_gbs"], "peak": peak, "unit": "GB/s",
                          "frac": res["attend_frac"], "traffic": traffic,
-                         "kernel": "attention per layer (split-KV kernel + combine)",
+                         "kernel": "attention per layer (the fused step's kernels)",
                          "ms_per_launch": res["attend_ms_per_launch"], "peak_source": peak_src},
             "append_ms_per_launch": res.get("append_ms_per_launch"),
             "copy_prefix": copy,

@@ -174,6 +174,31 @@ Plan plan_attention(int rows, int Hq, int Hkv, int cap, int D, kvd_dtype dt, int
     return pl;
 }
 
+// Small static-buffer launch (no caller split count; every split of every row
+// resident at once, a cluster of at most 8 CTAs per row that merges the row
+// itself).  Splits as equal as the copies allow: whole 64-row boxes for the
+// tensor-core layout, any 16 rows for row copies (16-byte mask vectors).
+struct SmallPlan {
+    bool use;
+    int chunk, S, rows;
+};
+
+SmallPlan plan_small(int B, int Hkv, int C, int D, kvd_dtype dt, const Plan& pl, int num_splits) {
+    SmallPlan sp{};
+    if (num_splits != 0) return sp;
+    const int T = pl.tile;
+    const int q = attend_uses_mma(dt, pl.G) ? T : 16;
+    const long long rows = (long long)B * Hkv * pl.HG;
+    const long long chunk = ((C + kSmallSplits - 1) / kSmallSplits + q - 1) / q * q;
+    const long long S = (C + chunk - 1) / chunk;
+    sp.use = chunk <= kSmallTokens && rows * S <= kGridUnitsHint && rows <= 65535 &&
+             small_shared_bytes(dt, D, pl.G, (int)chunk) <= kSmallShared;
+    sp.chunk = (int)chunk;
+    sp.S = (int)S;
+    sp.rows = (int)rows;
+    return sp;
+}
+
 // Attaches the workspace regions of a plan to the kernel parameters.
 void attach_workspace(AttendParams& p, const Plan& pl, void* ws) {
     char* base = static_cast<char*>(ws);
@@ -338,6 +363,15 @@ kvd_status kvd_copy_prefix(const void* const* k_src, const void* const* v_src, v
     return ok();
 }
 
+int kvd_attend_masked_launches(int B, int Hq, int Hkv, int C, int D, kvd_dtype dtype,
+                               int num_splits) {
+    if (B < 1 || C < 1 || num_splits < 0 || check_attention_shape(Hq, Hkv, D, dtype) != KVD_OK)
+        return 0;
+    const Plan pl = plan_attention(B, Hq, Hkv, C, D, dtype, 0, num_splits);
+    if (plan_small(B, Hkv, C, D, dtype, pl, num_splits).use) return 1;
+    return pl.S > 1 ? 2 : 1;
+}
+
 size_t kvd_attend_masked_workspace_bytes(int B, int Hq, int Hkv, int C, int D, kvd_dtype dtype,
                                          int num_splits) {
     if (B < 1 || C < 1 || check_attention_shape(Hq, Hkv, D, dtype) != KVD_OK) return 0;
@@ -399,26 +433,15 @@ kvd_status attend_masked_impl(const char* fn, const void* q, const void* k_cache
         st = make_cache_map(&vmap, v_cache, dtype, false, rows, Hkv, D, pl.tile, true);
         if (st != KVD_OK) return st;
     }
-    if (num_splits == 0) {
-        // Small launch: every split of every row resident at once in a
-        // cluster of at most 8 CTAs that merges the row itself
-        // splits as equal as the copies allow: whole 64-row boxes for the
-        // tensor-core layout, any 16 rows for row copies (16-byte mask vectors)
-        const int T = pl.tile;
-        const int q = attend_uses_mma(dtype, pl.G) ? T : 16;
-        const long long rows = (long long)B * Hkv * pl.HG;
-        const int chunk = (int)(((C + kSmallSplits - 1) / kSmallSplits + q - 1) / q * q);
-        const int S = (C + chunk - 1) / chunk;
-        if (chunk <= kSmallTokens && rows * S <= kGridUnitsHint && rows <= 65535 &&
-            small_shared_bytes(dtype, D, pl.G, chunk) <= kSmallShared) {
-            AttendParams ps = p;
-            ps.chunk = chunk;
-            ps.S = S;
-            const cudaError_t e = launch_attend_small(dtype, D, pl.G, ps, S, (int)rows, &kmap,
-                                                      &vmap, (cudaStream_t)stream);
-            if (e != cudaSuccess) return cuda_fail(e, fn);
-            return ok();
-        }
+    const SmallPlan sp = plan_small(B, Hkv, C, D, dtype, pl, num_splits);
+    if (sp.use) {
+        AttendParams ps = p;
+        ps.chunk = sp.chunk;
+        ps.S = sp.S;
+        const cudaError_t e = launch_attend_small(dtype, D, pl.G, ps, sp.S, sp.rows, &kmap, &vmap,
+                                                  (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+        return ok();
     }
     cudaError_t e = launch_attend(dtype, D, pl.G, kModeMasked, p, &kmap, &vmap, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, fn);

@@ -33,6 +33,7 @@ SIGNATURES = {
     "kvd_append": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp], _i),
     "kvd_copy_prefix": ([_vp, _vp, _vp, _vp, _vp, _vp] + [_i] * 7 + [_vp, _vp], _i),
     "kvd_attend_masked_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
+    "kvd_attend_masked_launches": ([_i, _i, _i, _i, _i, _i, _i], _i),
     "kvd_attend_masked": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz,
                            _vp, _vp], _i),
     "kvd_attend_masked_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i,
@@ -286,6 +287,12 @@ def _workspace(nbytes, device, ws):
     if have < nbytes:
         raise ValueError(f"workspace smaller than {nbytes} bytes")
     return ws, have
+
+
+def attend_masked_launches(B, Hq, Hkv, C, D, dtype=torch.bfloat16, num_splits=0):
+    """Kernel launches of one kvd_attend_masked call for these sizes (1 or 2)."""
+    return load().kvd_attend_masked_launches(B, Hq, Hkv, C, D,
+                                             BF16 if dtype == torch.bfloat16 else F32, num_splits)
 
 
 def attend_masked(q, k_cache, v_cache, mask, scale=None, out=None, lse=None, num_splits=0,

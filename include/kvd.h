@@ -153,6 +153,10 @@ kvd_status kvd_copy_prefix(const void* const* k_src, const void* const* v_src, v
  */
 size_t kvd_attend_masked_workspace_bytes(int B, int Hq, int Hkv, int C, int D, kvd_dtype dtype,
                                          int num_splits);
+/* Kernel launches one kvd_attend_masked (or kvd_append_attend_masked with
+ * Hq / Hkv <= 8) call makes for these sizes: 1 or 2; 0 for invalid sizes. */
+int kvd_attend_masked_launches(int B, int Hq, int Hkv, int C, int D, kvd_dtype dtype,
+                               int num_splits);
 kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_cache,
                              const uint8_t* mask, void* out, float* lse_out, int B, int Hq,
                              int Hkv, int C, int D, float scale, kvd_dtype dtype, int num_splits,

@@ -115,3 +115,13 @@ def test_fp8_entry_points_validate(lib):
     assert lib.kvd_attend_masked_fp8_workspace_bytes(1, 4, 3, 32, 128, 0) == 0
     assert lib.kvd_attend_masked_fp8(P(1), P(1), P(1), P(1), P(1), None, 2, 8, 2, 4096, 128, 0.1, 4,
                                      None, 0, None, None) == 3
+
+
+def test_launch_counts(lib):
+    """The small static-buffer launch (one cluster kernel) for short buffers,
+    the split kernel plus the combine for long ones, none for bad sizes."""
+    assert lib.kvd_attend_masked_launches(1, 32, 32, 1152, 128, 0, 0) == 1
+    assert lib.kvd_attend_masked_launches(16, 32, 8, 8192, 128, 0, 0) == 2
+    assert lib.kvd_attend_masked_launches(1, 32, 32, 1152, 128, 0, 3) == 2  # explicit splits
+    assert lib.kvd_attend_masked_launches(1, 4, 4, 32, 64, 0, 0) == 1
+    assert lib.kvd_attend_masked_launches(1, 4, 3, 32, 64, 0, 0) == 0
