@@ -44,13 +44,13 @@ L2_BYTES = 129 * 1024 * 1024
 # split kernel, from the ncu capture summarised in profiles/, keyed by the
 # hash of the kernel sources it was taken on (reported only while they match).
 NCU_TRAFFIC = {
-    ("npuw", "5357c55c3d9a464b"): 17379840,  # profiles/attend_kernel_npuw.md
-    ("gqa", "5357c55c3d9a464b"): 212605184,  # profiles/attend_kernel_gqa.md
-    ("long", "5357c55c3d9a464b"): 540686336,  # profiles/attend_kernel_long.md
-    ("paged", "5357c55c3d9a464b"): 521680128,  # profiles/attend_kernel_paged.md
-    ("indexed", "5357c55c3d9a464b"): 122679040,  # profiles/attend_kernel_indexed.md
-    ("window", "5357c55c3d9a464b"): 68204288,  # profiles/attend_kernel_window.md
-    ("gqa_fp8", "5357c55c3d9a464b"): 120423424,  # profiles/attend_kernel_gqa_fp8.md
+    ("npuw", "6dfa2864b2d54c58"): 18933760,  # profiles/attend_small_kernel_npuw.md
+    ("gqa", "6dfa2864b2d54c58"): 212684544,  # profiles/attend_kernel_gqa.md
+    ("long", "6dfa2864b2d54c58"): 540365312,  # profiles/attend_kernel_long.md
+    ("paged", "6dfa2864b2d54c58"): 521772544,  # profiles/attend_kernel_paged.md
+    ("indexed", "6dfa2864b2d54c58"): 122704896,  # profiles/attend_kernel_indexed.md
+    ("window", "6dfa2864b2d54c58"): 68165888,  # profiles/attend_kernel_window.md
+    ("gqa_fp8", "6dfa2864b2d54c58"): 120636672,  # profiles/attend_kernel_gqa_fp8.md
 }
 
 
