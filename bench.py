@@ -44,13 +44,13 @@ L2_BYTES = 129 * 1024 * 1024
 # split kernel, from the ncu capture summarised in profiles/, keyed by the
 # hash of the kernel sources it was taken on (reported only while they match).
 NCU_TRAFFIC = {
-    ("npuw", "6dfa2864b2d54c58"): 18933760,  # profiles/attend_small_kernel_npuw.md
-    ("gqa", "6dfa2864b2d54c58"): 212684544,  # profiles/attend_kernel_gqa.md
-    ("long", "6dfa2864b2d54c58"): 540365312,  # profiles/attend_kernel_long.md
-    ("paged", "6dfa2864b2d54c58"): 521772544,  # profiles/attend_kernel_paged.md
-    ("indexed", "6dfa2864b2d54c58"): 122704896,  # profiles/attend_kernel_indexed.md
-    ("window", "6dfa2864b2d54c58"): 68165888,  # profiles/attend_kernel_window.md
-    ("gqa_fp8", "6dfa2864b2d54c58"): 120636672,  # profiles/attend_kernel_gqa_fp8.md
+    ("npuw", "9672dd47ba34f1d1"): 18933760,  # profiles/attend_small_kernel_npuw.md
+    ("gqa", "9672dd47ba34f1d1"): 212684544,  # profiles/attend_kernel_gqa.md
+    ("long", "9672dd47ba34f1d1"): 540365312,  # profiles/attend_kernel_long.md
+    ("paged", "9672dd47ba34f1d1"): 521772544,  # profiles/attend_kernel_paged.md
+    ("indexed", "9672dd47ba34f1d1"): 122704896,  # profiles/attend_kernel_indexed.md
+    ("window", "9672dd47ba34f1d1"): 68165888,  # profiles/attend_kernel_window.md
+    ("gqa_fp8", "9672dd47ba34f1d1"): 120636672,  # profiles/attend_kernel_gqa_fp8.md
 }
 
 
@@ -89,12 +89,19 @@ def attention_flops(lengths, Hq, D):
 
 
 def kernel_source_hash():
+    """Hash of the CUDA sources' code (comments and blank space left out, so
+    that documentation edits keep a profile's counters attached)."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_attention_kv_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+            with open(os.path.join(csrc, name)) as f:
+                code = f.read()
+            code = re.sub(r"/\*.*?\*/", "", code, flags=re.S)
+            code = re.sub(r"//[^\n]*", "", code)
+            code = re.sub(r"\s+", " ", code)
+            h.update(name.encode() + code.encode())
     return h.hexdigest()[:16]
 
 

@@ -49,8 +49,10 @@
 //
 // Counters (unit counter, schedulers-done counter) live in the caller's
 // workspace: zero before the first call; the last scheduler warp to finish
-// taking units resets them.  The first unit of scheduler warp s is
-// s * gridDim.x + blockIdx.x (no atomic); the counter hands out the rest.
+// taking units resets them.  The first unit of scheduler warp s (no atomic)
+// is blockIdx.x * 4 + s -- four consecutive rows of one split, which share a
+// mask row or a sequence -- or, with fewer units than scheduler warps,
+// s * gridDim.x + blockIdx.x; the counter hands out the rest.
 // All waits are bounded; a wait that runs out sets KVD_DEV_TIMEOUT, after
 // which the counters must be zeroed again.
 #pragma once
