@@ -261,3 +261,25 @@ def test_leading_tiles_empty_or_valid(kvd, Hq, Hkv, start):
     assert_attention_close(out, ref, torch.bfloat16, f"leading tiles from {start}")
     assert_lse_close(lse, ref_lse)
     assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,D", [
+    (torch.float32, 16, 4, 128), (torch.float32, 16, 2, 64), (torch.bfloat16, 8, 4, 64),
+    (torch.bfloat16, 4, 4, 64), (torch.bfloat16, 32, 4, 64), (torch.bfloat16, 24, 1, 128)])
+def test_small_launch_matches_split_kernel(kvd, dtype, Hq, Hkv, D):
+    """Short buffers take the small-launch kernel (one cluster per row, no
+    combine); an explicit split count takes the split kernel.  Both equal the
+    oracle, for every group width and head_dim."""
+    B, C = 2, 700
+    g = W.generator(950 + Hq + D)
+    q = W.randn(g, (B, Hq, D), dtype)
+    k = W.randn(g, (B, Hkv, C, D), dtype)
+    v = W.randn(g, (B, Hkv, C, D), dtype)
+    mask = W.prefix_mask([700, 413], C)
+    mask[0, 300:360] = 0
+    assert kvd.attend_masked_launches(B, Hq, Hkv, C, D, dtype) == 1
+    ref, ref_lse = oracle.attend_masked(q, k, v, mask, 0.11)
+    for ns in (0, 3):
+        out, lse = _run_masked(kvd, q, k, v, mask, 0.11, ns)
+        assert_attention_close(out, ref, dtype, f"num_splits {ns}")
+        assert_lse_close(lse, ref_lse)
