@@ -106,7 +106,7 @@ struct AttendParams {
     uint8_t* mask_w;             // the mask, written at pos
 };
 
-enum : uint32_t { kFirst = 1u, kLast = 2u, kCombine = 4u, kEnd = 8u };
+enum : uint32_t { kFirst = 1u, kLast = 2u, kEnd = 8u };
 
 struct StageMeta {
     int unit;
@@ -141,13 +141,13 @@ __device__ __forceinline__ Unit decode_unit(const AttendParams& p, int G, int u)
 }
 
 // A unit prepared by the scheduler warp for the loader warp.
-enum : int { kSlotTiles = 0, kSlotCombine = 1, kSlotEnd = 2 };
+enum : int { kSlotTiles = 0, kSlotEnd = 2 };
 constexpr int kSchedWarps = 4;                         // scheduler warps per CTA
 constexpr int kRingSlots = 1;                          // queued units per scheduler
 constexpr int kQueueSlots = kSchedWarps * kRingSlots;  // scheduler s owns slot s
 
 struct UnitSlot {
-    int kind;    // kSlotTiles: stream the unit's tiles; kSlotCombine: only merge its row
+    int kind;    // kSlotTiles: stream the unit's tiles; kSlotEnd: the scheduler is done
     int unit;
     int t_begin, ntok;
     int last;    // last tile that holds a valid token

@@ -142,7 +142,11 @@ kvd_status kvd_copy_prefix(const void* const* k_src, const void* const* v_src, v
  * splits (lengths rounded up to the kernel's tile, at most 4096 slots); 0
  * lets the library plan from the sizes, with smaller splits over the end of
  * the capacity.  With more than one split a second kernel merges the splits by
- * log-sum-exp (the kvd_combine formula).
+ * log-sum-exp (the kvd_combine formula).  Short buffers with num_splits = 0
+ * (at most 8 splits of at most 384 slots per row, every split of every row
+ * resident at once on the GPU) take one launch instead: a thread-block
+ * cluster per row whose CTAs hold one split each and merge the row through
+ * distributed shared memory (kvd_attend_masked_launches tells which).
  * Workspace: at least kvd_attend_masked_workspace_bytes(...) bytes (never
  * less than 256), 256-byte aligned, holding the work counters and the
  * partial rows.  Zero-fill it once before its first use; every call leaves
