@@ -44,13 +44,13 @@ L2_BYTES = 129 * 1024 * 1024
 # split kernel, from the ncu capture summarised in profiles/, keyed by the
 # hash of the kernel sources it was taken on (reported only while they match).
 NCU_TRAFFIC = {
-    ("npuw", "9672dd47ba34f1d1"): 18933760,  # profiles/attend_small_kernel_npuw.md
-    ("gqa", "9672dd47ba34f1d1"): 212684544,  # profiles/attend_kernel_gqa.md
-    ("long", "9672dd47ba34f1d1"): 540365312,  # profiles/attend_kernel_long.md
-    ("paged", "9672dd47ba34f1d1"): 521772544,  # profiles/attend_kernel_paged.md
-    ("indexed", "9672dd47ba34f1d1"): 122704896,  # profiles/attend_kernel_indexed.md
-    ("window", "9672dd47ba34f1d1"): 68165888,  # profiles/attend_kernel_window.md
-    ("gqa_fp8", "9672dd47ba34f1d1"): 120636672,  # profiles/attend_kernel_gqa_fp8.md
+    ("npuw", "e52ec2adbae6cdd8"): 18934016,  # profiles/attend_small_kernel_npuw.md
+    ("gqa", "e52ec2adbae6cdd8"): 212675328,  # profiles/attend_kernel_gqa.md
+    ("long", "e52ec2adbae6cdd8"): 540688384,  # profiles/attend_kernel_long.md
+    ("paged", "e52ec2adbae6cdd8"): 521886976,  # profiles/attend_kernel_paged.md
+    ("indexed", "e52ec2adbae6cdd8"): 122669568,  # profiles/attend_kernel_indexed.md
+    ("window", "e52ec2adbae6cdd8"): 67984384,  # profiles/attend_kernel_window.md
+    ("gqa_fp8", "e52ec2adbae6cdd8"): 120647936,  # profiles/attend_kernel_gqa_fp8.md
 }
 
 
