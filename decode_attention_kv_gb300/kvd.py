@@ -118,6 +118,27 @@ def status_tensor(device=None):
     return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
 
 
+# the KVD_DEV_* bits of kvd.h
+DEV_BITS = {1: "KVD_DEV_POS_RANGE", 2: "KVD_DEV_BLOCK_RANGE", 4: "KVD_DEV_TABLE_COLS",
+            8: "KVD_DEV_SEQLENS", 16: "KVD_DEV_SEQ_OFFSET", 32: "KVD_DEV_TIMEOUT",
+            64: "KVD_DEV_POINTER"}
+
+
+class KvdDeviceError(RuntimeError):
+    def __init__(self, bits):
+        self.bits = bits
+        self.names = [n for b, n in DEV_BITS.items() if bits & b]
+        super().__init__(f"device status {bits}: {', '.join(self.names) or 'unknown bits'}")
+
+
+def check(dev_status):
+    """Wait for the work queued so far (reading the word synchronises) and
+    raise KvdDeviceError naming the bits the kernels set in ``dev_status``."""
+    bits = int(dev_status.item())
+    if bits:
+        raise KvdDeviceError(bits)
+
+
 # ------------------------------------------------------------------ append
 
 def append(k_cache, v_cache, k_new, v_new, pos, mask=None, dev_status=None):

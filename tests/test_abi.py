@@ -125,3 +125,17 @@ def test_launch_counts(lib):
     assert lib.kvd_attend_masked_launches(1, 32, 32, 1152, 128, 0, 3) == 2  # explicit splits
     assert lib.kvd_attend_masked_launches(1, 4, 4, 32, 64, 0, 0) == 1
     assert lib.kvd_attend_masked_launches(1, 4, 3, 32, 64, 0, 0) == 0
+
+
+def test_device_status_check():
+    """kvd.check names the KVD_DEV_* bits (the same values as kvd.h) and
+    passes a clean status word."""
+    import torch
+    from decode_attention_kv_gb300 import kvd
+    text = open(os.path.join(ROOT, "include", "kvd.h")).read()
+    defs = {n: int(v) for n, v in re.findall(r"#define (KVD_DEV_\w+) (\d+)u", text)}
+    assert {b: n for n, b in defs.items()} == kvd.DEV_BITS
+    kvd.check(torch.zeros(1, dtype=torch.int32))
+    with pytest.raises(kvd.KvdDeviceError) as e:
+        kvd.check(torch.tensor([1 | 32], dtype=torch.int32))
+    assert e.value.names == ["KVD_DEV_POS_RANGE", "KVD_DEV_TIMEOUT"]
