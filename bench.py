@@ -27,6 +27,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -324,6 +325,11 @@ class MaskedBench:
     def tokens_per_step(self):
         return self.B
 
+    def flops_per_step(self):
+        """Attention FLOPs of one step (reported, not bounding): 4 per query
+        head, attended slot and dim."""
+        return self.layers * attention_flops(self.rows_at(0), self.Hq, self.D)
+
     def e2e_setup(self):
         """End to end as a caller runs the step: every layer's q and new K/V
         rows live in one device staging buffer filled by one host-to-device
@@ -464,6 +470,9 @@ class PagedBench:
     def tokens_per_step(self):
         return self.Q
 
+    def flops_per_step(self):
+        return attention_flops(self.lengths, self.Hq, self.D)
+
     def e2e_setup(self):
         torch = self.torch
         self.h_q = torch.empty(self.pw.q.shape, dtype=self.pw.q.dtype, pin_memory=True).copy_(
@@ -529,6 +538,9 @@ class IndexedBench(MaskedBench):
 
     def launches_per_step(self):
         return self.layers * (2 + (1 if self.splits else 0))  # append, attention, combine
+
+    def flops_per_step(self):
+        return self.layers * attention_flops(self.listed, self.Hq, self.D)
 
     def attend_bytes(self, j):
         """Listed K and V rows of every kv head, the index lists, q and out."""
@@ -643,6 +655,43 @@ def timed(torch, dist, fn, K):
     return e0.elapsed_time(e1)
 
 
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it (model name, else the Arm
+    implementer / part codes), with the machine type."""
+    import platform
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        info = ""
+    m = re.search(r"^model name\s*:\s*(.+)$", info, re.M)
+    if m:
+        return m.group(1).strip()
+    imp = re.search(r"^CPU implementer\s*:\s*(\S+)", info, re.M)
+    part = re.search(r"^CPU part\s*:\s*(\S+)", info, re.M)
+    if imp and part:
+        return f"{platform.machine()} implementer {imp.group(1)} part {part.group(1)}"
+    return platform.machine()
+
+
+def step_quantiles(torch, b, K, flush):
+    """p10 / p50 / p90 of K single graph replays, each between its own CUDA
+    events; with ``flush``, a buffer of twice the L2 is written (untimed)
+    before each step."""
+    evs = []
+    for j in range(K):
+        if flush is not None:
+            flush.fill_(float(j))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        b.graph_run(j)
+        e1.record()
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    d = sorted(a.elapsed_time(c) for a, c in evs)
+    q = lambda f: d[min(len(d) - 1, int(f * (len(d) - 1) + 0.5))]  # noqa: E731
+    return {"p10": q(0.1), "p50": q(0.5), "p90": q(0.9), "n": len(d)}
+
+
 def _reduce(torch, dist, x, op):
     if dist is None:
         return x
@@ -705,6 +754,14 @@ def measure_workload(b, torch, dist, K, W, peak, clocks=None):
     res["gbs"], ms = whole_job_rate(torch, dist, ms, sum(b.step_bytes(j) for j in range(K)))
     res["ms_per_step"] = ms / K
     res["tokens_per_s"] = sum_over_ranks(torch, dist, b.tokens_per_step() * K) / (ms / 1e3)
+    res["attention_tflops"] = b.flops_per_step() / (ms / K / 1e3) / 1e12
+    # the distribution of single steps, and the same with L2 flushed before each
+    b.reset_cycle()
+    res["step_ms"] = step_quantiles(torch, b, K, None)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=b.dev)
+    b.reset_cycle()
+    res["step_ms_l2_flushed"] = step_quantiles(torch, b, K, flush)
+    del flush
 
     log(f"  timed steps done: {ms / K:.3f} ms/step; per-launch pass")
     b.reset_cycle()
@@ -1002,7 +1059,8 @@ def main():
         log("cpu baseline (oracle)")
         try:
             v, cores, sample = oracle_rate(args.workload, args.cpu_seconds)
-            cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+            cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+                   "cpu_model": cpu_model()}
         except Exception as e:  # the oracle needs gcc on the host
             cpu = {"unavailable": f"{type(e).__name__}: {e}"}
 
@@ -1014,6 +1072,9 @@ def main():
             "data": "synthetic", "config": b.config(),
             "frac_of_hbm_peak": res["gbs"] / peak, "peak_source": peak_src,
             "decode_tokens_per_s": res["tokens_per_s"],
+            "decode_tokens_per_s_eager": b.tokens_per_step() / (res["eager"]["ms_per_step"] / 1e3),
+            "attention_tflops": res["attention_tflops"],
+            "step_ms": res["step_ms"], "step_ms_l2_flushed": res["step_ms_l2_flushed"],
             "timing": "each timed step is one CUDA-graph replay of the decode step "
                       "(all layers' kvd kernels); 'eager' = one binding call per kernel",
             "roofline": {"bound": "hbm", "achieved": res["attend_gbs"], "peak": peak, "unit": "GB/s",
