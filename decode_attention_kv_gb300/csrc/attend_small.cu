@@ -1,5 +1,6 @@
 // attend_small.cu -- instantiations and launch of the small-launch attention
 // kernel (one CTA per (row, split), the row's splits in one cluster).
+#include <cstring>
 #include <mutex>
 
 #include "attend_small.cuh"
@@ -67,6 +68,34 @@ cudaError_t launch_small_d(int G, bool mma, const AttendParams& p, int S, int ro
 }
 
 }  // namespace
+
+int small_shared_bytes_fp8(int D, int G, int chunk) {
+    const int T = 64;
+    const SmallLayout L = SmallLayout::make((chunk + T - 1) / T, T * (D + 16), T, D, G, 4, 2);
+    return L.bytes + 1024;
+}
+
+cudaError_t launch_attend_small_fp8(int D, int G, const AttendParams& p, int S, int rows,
+                                    cudaStream_t stream) {
+    CUtensorMap none;
+    std::memset(&none, 0, sizeof none);
+    if (D == 128) {
+        switch (G) {
+            case 1: return launch_small_cfg<Fp8MmaConsumer<128, 1, 64, 4>>(p, S, rows, &none, &none, stream);
+            case 2: return launch_small_cfg<Fp8MmaConsumer<128, 2, 64, 4>>(p, S, rows, &none, &none, stream);
+            case 4: return launch_small_cfg<Fp8MmaConsumer<128, 4, 64, 4>>(p, S, rows, &none, &none, stream);
+            case 8: return launch_small_cfg<Fp8MmaConsumer<128, 8, 64, 4>>(p, S, rows, &none, &none, stream);
+        }
+    } else if (D == 64) {
+        switch (G) {
+            case 1: return launch_small_cfg<Fp8MmaConsumer<64, 1, 64, 4>>(p, S, rows, &none, &none, stream);
+            case 2: return launch_small_cfg<Fp8MmaConsumer<64, 2, 64, 4>>(p, S, rows, &none, &none, stream);
+            case 4: return launch_small_cfg<Fp8MmaConsumer<64, 4, 64, 4>>(p, S, rows, &none, &none, stream);
+            case 8: return launch_small_cfg<Fp8MmaConsumer<64, 8, 64, 4>>(p, S, rows, &none, &none, stream);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
 
 int small_shared_bytes(kvd_dtype dt, int D, int G, int chunk) {
     const bool mma = attend_uses_mma(dt, G);

@@ -147,7 +147,9 @@ attend_small_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
         }
         // the new row's slot and the split's validity words, read while the
         // copies fly (all loads issued before any is used)
-        const int x = p.pos ? __ldg(p.pos + bz) : -1;
+        // the fused append (rows of Elem; never with quantised rows)
+        constexpr bool kAppend = Cons::kRowBytes == D * (int)sizeof(Elem);
+        const int x = (kAppend && p.pos) ? __ldg(p.pos + bz) : -1;
         const uint8_t* mrow = p.mask + (size_t)bz * p.C;
         const int nwords = (ntiles * T + 31) / 32;
         if (p.mask_vec) {
@@ -178,7 +180,7 @@ attend_small_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
             }
         }
         __syncwarp();
-        if (p.pos) {
+        if (kAppend && p.pos) {
             if (x < 0 || x >= p.C) {
                 if (lane == 0 && split == 0 && kvh == 0 && hg == 0)
                     report(p.dev_status, KVD_DEV_POS_RANGE);
@@ -186,7 +188,7 @@ attend_small_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
                 pb = x;
             }
         }
-        if (pb >= 0) {
+        if (kAppend && pb >= 0) {
             // fused append: the cache row (head group 0 writes it), the mask
             // slot (kv head 0) and the validity bit
             if (hg == 0) {
@@ -211,7 +213,7 @@ attend_small_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
     const volatile int never = 0;
     const bool landed = mbar_wait(bar, 0, &never);
     if (!landed && threadIdx.x == 0) report(p.dev_status, KVD_DEV_TIMEOUT);
-    if (landed && pb >= 0 && warp == NCW) {
+    if (Cons::kRowBytes == D * (int)sizeof(Elem) && landed && pb >= 0 && warp == NCW) {
         // the copied tile holds the old row at pb: put the new one in its place
         const int r = pb - t_begin, i = r / T, rr = r % T;
         constexpr int kChunks = D * (int)sizeof(Elem) / 16;

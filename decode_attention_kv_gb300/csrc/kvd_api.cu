@@ -25,6 +25,9 @@ cudaError_t launch_attend_small(kvd_dtype dt, int D, int G, const AttendParams& 
                                 const CUtensorMap* kmap, const CUtensorMap* vmap,
                                 cudaStream_t stream);
 int small_shared_bytes(kvd_dtype dt, int D, int G, int chunk);
+int small_shared_bytes_fp8(int D, int G, int chunk);
+cudaError_t launch_attend_small_fp8(int D, int G, const AttendParams& p, int S, int rows,
+                                    cudaStream_t stream);
 }  // namespace kvd
 
 using namespace kvd;
@@ -183,16 +186,20 @@ struct SmallPlan {
     int chunk, S, rows;
 };
 
-SmallPlan plan_small(int B, int Hkv, int C, int D, kvd_dtype dt, const Plan& pl, int num_splits) {
+// fp8: quantised rows (row copies of D + 16 bytes, 64-row tiles).
+SmallPlan plan_small(int B, int Hkv, int C, int D, kvd_dtype dt, const Plan& pl, int num_splits,
+                     bool fp8 = false) {
     SmallPlan sp{};
     if (num_splits != 0) return sp;
     const int T = pl.tile;
-    const int q = attend_uses_mma(dt, pl.G) ? T : 16;
+    const int q = (!fp8 && attend_uses_mma(dt, pl.G)) ? T : 16;
     const long long rows = (long long)B * Hkv * pl.HG;
     const long long chunk = ((C + kSmallSplits - 1) / kSmallSplits + q - 1) / q * q;
     const long long S = (C + chunk - 1) / chunk;
+    const int smem = fp8 ? small_shared_bytes_fp8(D, pl.G, (int)chunk)
+                         : small_shared_bytes(dt, D, pl.G, (int)chunk);
     sp.use = chunk <= kSmallTokens && rows * S <= kGridUnitsHint && rows <= 65535 &&
-             small_shared_bytes(dt, D, pl.G, (int)chunk) <= kSmallShared;
+             smem <= kSmallShared;
     sp.chunk = (int)chunk;
     sp.S = (int)S;
     sp.rows = (int)rows;
@@ -552,6 +559,15 @@ kvd_status kvd_attend_masked_fp8(const void* q, const void* k_cache, const void*
     p.mask_vec = (C % 16 == 0) && aligned(mask, 16);
     p.qscale = scale * kLog2e;
     attach_workspace(p, pl, workspace);
+    const SmallPlan sp = plan_small(B, Hkv, C, D, KVD_BF16, pl, num_splits, true);
+    if (sp.use) {
+        AttendParams ps = p;
+        ps.chunk = sp.chunk;
+        ps.S = sp.S;
+        const cudaError_t es = launch_attend_small_fp8(D, pl.G, ps, sp.S, sp.rows, (cudaStream_t)stream);
+        if (es != cudaSuccess) return cuda_fail(es, "kvd_attend_masked_fp8 launch");
+        return ok();
+    }
     cudaError_t e = launch_attend_fp8(D, pl.G, p, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked_fp8 launch");
     if (pl.S > 1) {

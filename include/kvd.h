@@ -273,7 +273,9 @@ kvd_status kvd_append_fp8(void* k_cache, void* v_cache, const void* k_new, const
  * weight carrying its row's scale relative to a running power of two (row
  * scales must be finite and below 2^126).  D is 64 or 128; any Hq / Hkv (up
  * to 8 query heads per kv head in one group, larger groups are split).
- * Workspace and num_splits as for kvd_attend_masked (64-token tiles).
+ * Workspace and num_splits as for kvd_attend_masked (64-token tiles), short
+ * buffers included: with num_splits = 0 they take the one-launch cluster
+ * path.
  */
 size_t kvd_attend_masked_fp8_workspace_bytes(int B, int Hq, int Hkv, int C, int D, int num_splits);
 kvd_status kvd_attend_masked_fp8(const void* q, const void* k_cache, const void* v_cache,
