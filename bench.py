@@ -45,13 +45,13 @@ L2_BYTES = 129 * 1024 * 1024
 # split kernel, from the ncu capture summarised in profiles/, keyed by the
 # hash of the kernel sources it was taken on (reported only while they match).
 NCU_TRAFFIC = {
-    ("npuw", "e52ec2adbae6cdd8"): 18934016,  # profiles/attend_small_kernel_npuw.md
-    ("gqa", "e52ec2adbae6cdd8"): 212675328,  # profiles/attend_kernel_gqa.md
-    ("long", "e52ec2adbae6cdd8"): 540688384,  # profiles/attend_kernel_long.md
-    ("paged", "e52ec2adbae6cdd8"): 521886976,  # profiles/attend_kernel_paged.md
-    ("indexed", "e52ec2adbae6cdd8"): 122669568,  # profiles/attend_kernel_indexed.md
-    ("window", "e52ec2adbae6cdd8"): 67984384,  # profiles/attend_kernel_window.md
-    ("gqa_fp8", "e52ec2adbae6cdd8"): 120647936,  # profiles/attend_kernel_gqa_fp8.md
+    ("npuw", "867e092d422aa277"): 18934016,  # profiles/attend_small_kernel_npuw.md
+    ("gqa", "867e092d422aa277"): 212566528,  # profiles/attend_kernel_gqa.md
+    ("long", "867e092d422aa277"): 540652288,  # profiles/attend_kernel_long.md
+    ("paged", "867e092d422aa277"): 521710848,  # profiles/attend_kernel_paged.md
+    ("indexed", "867e092d422aa277"): 122729216,  # profiles/attend_kernel_indexed.md
+    ("window", "867e092d422aa277"): 68096768,  # profiles/attend_kernel_window.md
+    ("gqa_fp8", "867e092d422aa277"): 120336896,  # profiles/attend_kernel_gqa_fp8.md
 }
 
 
