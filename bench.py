@@ -84,6 +84,26 @@ def gather_bytes(lengths, Hk, Dk, Hv, Dv, elem, BS):
     return 2 * T * (Hk * Dk + Hv * Dv) * elem + entries * 4 + (Q + 1) * 4
 
 
+def fp8_attend_bytes(lengths, Hq, Hkv, C, D, pad):
+    """Valid quantised K and V rows (D codes + fp32 scale + zero pad, D + pad
+    bytes each), the mask row, bf16 q and out."""
+    B = len(lengths)
+    return (sum(int(L) for L in lengths) * Hkv * (D + pad) * 2 + B * C + 2 * B * Hq * D * 2)
+
+
+def fp8_append_bytes(B, Hkv, D, pad):
+    """bf16 new K and V rows read, their quantised rows written."""
+    return 2 * B * Hkv * (D * 2 + D + pad)
+
+
+def indexed_attend_bytes(listed, topk, Hq, Hkv, D, elem):
+    """The listed K and V rows of every kv head, the index lists (topk int32
+    entries per query, padding included), q and out."""
+    B = len(listed)
+    return (sum(int(n) for n in listed) * Hkv * D * 2 * elem + B * topk * 4
+            + 2 * B * Hq * D * elem)
+
+
 def attention_flops(lengths, Hq, D):
     return 4 * sum(int(L) for L in lengths) * Hq * D
 
@@ -542,9 +562,7 @@ class IndexedBench(MaskedBench):
         return self.layers * attention_flops(self.listed, self.Hq, self.D)
 
     def attend_bytes(self, j):
-        """Listed K and V rows of every kv head, the index lists, q and out."""
-        return (sum(self.listed) * self.Hkv * self.D * 2 * self.elem + self.B * self.TOPK * 4
-                + 2 * self.B * self.Hq * self.D * self.elem)
+        return indexed_attend_bytes(self.listed, self.TOPK, self.Hq, self.Hkv, self.D, self.elem)
 
     def copy_setup(self):
         return False
@@ -597,14 +615,12 @@ class Fp8Bench(MaskedBench):
         return self.layers * (2 + (1 if self.splits else 0))  # append_fp8, attention, combine
 
     def attend_bytes(self, j):
-        """Valid quantised K and V rows (codes + scale + pad), the mask row, q and out."""
-        L = self.lengths_at(j)
-        return (sum(L) * self.Hkv * self.row * 2 + self.B * self.C
-                + 2 * self.B * self.Hq * self.D * 2)
+        return fp8_attend_bytes(self.lengths_at(j), self.Hq, self.Hkv, self.C, self.D,
+                                self.kvd.FP8_ROW_PAD)
 
     def step_bytes(self, j):
-        """Attention plus the append: bf16 new rows read, quantised rows written."""
-        app = 2 * self.B * self.Hkv * (self.D * 2 + self.row)
+        """Attention plus the append of the step's rows."""
+        app = fp8_append_bytes(self.B, self.Hkv, self.D, self.kvd.FP8_ROW_PAD)
         return self.layers * (self.attend_bytes(j) + app)
 
     def copy_setup(self):

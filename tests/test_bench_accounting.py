@@ -28,3 +28,29 @@ def test_paged_and_gather_accounting():
     assert a == rows * 8 * 128 * 2 * 2 + (1 + 1 + 2) * 4 + 4 * 4 + 2 * 3 * 32 * 128 * 2
     g = bench.gather_bytes(lengths, 8, 128, 1, 64, 2, 128)
     assert g == 2 * rows * (8 * 128 + 64) * 2 + 4 * 4 + 4 * 4
+
+
+def test_fp8_accounting_row_format():
+    """A quantised row is D E4M3 codes (one byte each) + one fp32 scale + 12
+    zero bytes: 144 bytes for D = 128, against 256 for a bf16 row, so the
+    cache part of the attention bytes shrinks to 144/256 of the bf16 figure
+    while the mask, q and out (bf16) stay."""
+    lengths, Hq, Hkv, C, D = [1, 64, 700], 32, 8, 1024, 128
+    rows = sum(lengths)
+    f = bench.fp8_attend_bytes(lengths, Hq, Hkv, C, D, 16)
+    b = bench.masked_attend_bytes(lengths, Hq, Hkv, C, D, 2)
+    side = len(lengths) * C + 2 * len(lengths) * Hq * D * 2
+    assert f - side == rows * Hkv * 2 * 144
+    assert (f - side) * 256 == (b - side) * 144
+    # the append reads the bf16 row and writes the quantised one, K and V
+    assert bench.fp8_append_bytes(4, Hkv, D, 16) == 4 * Hkv * 2 * (256 + 144)
+
+
+def test_indexed_accounting_counts_listed_rows_and_whole_lists():
+    """Only the listed rows are read; every query's list is read whole
+    (topk int32 entries, padding included)."""
+    listed, topk, Hq, Hkv, D = [3, 2048, 0], 2048, 16, 1, 512
+    a = bench.indexed_attend_bytes(listed, topk, Hq, Hkv, D, 2)
+    assert a == (2051 * 1 * 512 * 2 * 2) + 3 * 2048 * 4 + 2 * 3 * 16 * 512 * 2
+    # an empty list still reads its list, q and writes out
+    assert bench.indexed_attend_bytes([0], topk, Hq, Hkv, D, 2) == 2048 * 4 + 2 * 16 * 512 * 2
