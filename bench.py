@@ -3,7 +3,7 @@
 decode tokens/s on GB300, through libkvd's C ABI.
 
     python bench.py [--gpus N] [--steps K] [--warmup W]
-                    [--workload npuw|gqa|long|paged|indexed|window]
+                    [--workload gqa|long|paged|npuw|indexed|window|gqa_fp8]
     python bench.py --impl reference ...     # the fp64 CPU oracle as the reference arm
 
 A step is one decode step of the workload: for the static-buffer workloads,
@@ -14,11 +14,13 @@ second (valid K/V rows, mask, q and out, appended rows; no padding and no
 split scratch), whole job over all ranks.  Multi-GPU runs are independent
 replicas (weak scaling, no data-path collective).
 
-Besides the main line (the 1152-slot NPUW-default buffer by default), the
-JSON carries the same measurement for the other workloads under "workloads":
-batched GQA, paged and long context (the ones the 75 % HBM gate is stated
-on), top-k index lists over the GQA caches and a 4096-slot sliding window over
-the long-context caches.
+The main line is the batched-GQA workload (16 sequences, 32/8 heads,
+capacity 8192, 32 layers: the largest single-GPU configuration, one of the
+two the 75 % HBM target is stated on).  The same measurement of every other
+workload -- long context (the other target), the paged cache, the
+1152-slot static buffer, top-k index lists, a sliding window and quantised
+caches -- goes under "workloads", each with its own roofline, CPU baseline
+and end-to-end figure.
 """
 from __future__ import annotations
 
@@ -40,19 +42,19 @@ if ROOT not in sys.path:
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the attention
-# split kernel, from the ncu capture summarised in profiles/, keyed by the
-# hash of the kernel sources it was taken on (reported only while they match).
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of each
+# workload's attention kernel from an ncu capture, keyed by the hash of the
+# kernel sources it was taken on: reported only while the sources still hash
+# to that revision, else null.
 NCU_TRAFFIC = {
-    ("npuw", "867e092d422aa277"): 18934016,  # profiles/attend_small_kernel_npuw.md
-    ("gqa", "867e092d422aa277"): 212566528,  # profiles/attend_kernel_gqa.md
-    ("long", "867e092d422aa277"): 540652288,  # profiles/attend_kernel_long.md
-    ("paged", "867e092d422aa277"): 521710848,  # profiles/attend_kernel_paged.md
-    ("indexed", "867e092d422aa277"): 122729216,  # profiles/attend_kernel_indexed.md
-    ("window", "867e092d422aa277"): 68096768,  # profiles/attend_kernel_window.md
-    ("gqa_fp8", "867e092d422aa277"): 120336896,  # profiles/attend_kernel_gqa_fp8.md
+    ("npuw", "867e092d422aa277"): 18934016,  # attend_small_kernel, 1152-slot buffer
+    ("gqa", "867e092d422aa277"): 212566528,  # attend_kernel, tensor-core consumers, batched GQA
+    ("long", "867e092d422aa277"): 540652288,  # attend_kernel, CUDA-core consumers, 32768 slots
+    ("paged", "867e092d422aa277"): 521710848,  # attend_kernel, paged mode
+    ("indexed", "867e092d422aa277"): 122729216,  # attend_kernel, index-list mode
+    ("window", "867e092d422aa277"): 68096768,  # attend_kernel, 4096-slot window
+    ("gqa_fp8", "867e092d422aa277"): 120336896,  # attend_kernel, E4M3 consumers
 }
-
 
 # ------------------------------------------------------------ byte accounting
 
@@ -200,6 +202,76 @@ def bus_id_of(torch, dev):
 
 
 # ---------------------------------------------------------------- workloads
+
+# Layer caches of each static-buffer workload (the workload generators' defaults).
+LAYERS = {"npuw": 32, "gqa": 32, "long": 8, "window": 8, "gqa_fp8": 32, "indexed": 32}
+
+
+def masked_config(name, w, layers, lengths0):
+    """The config block of a static-buffer workload (both arms print it)."""
+    elem = 2
+    cache = layers * 2 * w.B * w.Hkv * w.C * w.D * elem
+    L = lengths0
+    c = {"workload": name, "batch": w.B, "q_heads": w.Hq, "kv_heads": w.Hkv,
+         "head_dim": w.D, "capacity": w.C, "layers": layers, "dtype": "bf16",
+         "valid_len_step0": (L if len(L) <= 4 else
+                             {"min": min(L), "max": max(L), "mean": sum(L) / len(L)}),
+         "l2": f"inputs larger than L2: {cache / 2**30:.2f} GiB of layer caches rotated "
+               f"per step vs {L2_BYTES // 2**20} MiB L2"}
+    if w.window:
+        rows = layers * 2 * w.Hkv * sum(min(x, w.window) for x in L) * w.D * elem
+        c.update({"window": w.window,
+                  "l2": f"inputs larger than L2: the windows' K/V rows of the {layers} layers "
+                        f"read per step are {rows / 2**20:.0f} MiB vs {L2_BYTES // 2**20} MiB L2"})
+    if name == "indexed":
+        listed = [min(IndexedBench.TOPK, x) for x in L]
+        c.update({"topk": IndexedBench.TOPK,
+                  "listed_per_entry": {"min": min(listed), "max": max(listed)}})
+    if name == "gqa_fp8":
+        row = w.D + FP8_ROW_PAD
+        cache = layers * 2 * w.B * w.Hkv * w.C * row
+        c.update({"dtype": "e4m3 K/V, bf16 q/out",
+                  "kv_format": f"E4M3 codes + fp32 row scale, {row}-byte rows",
+                  "l2": f"inputs larger than L2: {cache / 2**30:.2f} GiB of layer caches "
+                        f"rotated per step vs {L2_BYTES // 2**20} MiB L2"})
+    return c
+
+
+def paged_config(pw):
+    NB, BS, Hkv, D = pw.key_cache.shape
+    Q, Hq, _ = pw.q.shape
+    lengths = [int(x) for x in pw.lengths]
+    rows = 2 * sum(lengths) * Hkv * D * 2
+    return {"workload": "paged", "num_blocks": NB, "block_size": BS, "kv_heads": Hkv,
+            "q_heads": Hq, "head_dim": D, "sequences": Q, "dtype": "bf16",
+            "total_tokens": pw.total_tokens,
+            "l2": f"inputs larger than L2: {rows / 2**30:.2f} GiB of valid K/V rows per step "
+                  f"(of a {2 * pw.key_cache.numel() * 2 / 2**30:.0f} GiB cache) vs "
+                  f"{L2_BYTES // 2**20} MiB L2"}
+
+
+def workload_config(name):
+    """The config block of a workload, built from host copies of its inputs
+    (the reference arm prints the same block as the GPU arm)."""
+    import workloads
+    if name == "paged":
+        return paged_config(workloads.paged(device="cpu"))
+    gen = {"indexed": "gqa"}.get(name, name)
+    w = getattr(workloads, gen)(device="cpu", layers=1)
+    return masked_config(name, w, LAYERS[name], [int(x) for x in w.layers[0].lengths])
+
+
+FP8_ROW_PAD = 16  # quantised rows: D codes, fp32 scale, 12 zero bytes
+
+
+def attention_kernel_name(kind, plan_splits, g, dtype="bf16", mode="masked", fused=False):
+    """The kernel that runs a workload's attention, as the launch list names it."""
+    if plan_splits == 0:
+        return f"attend_small_kernel ({kind} consumers; one CTA per split, cluster merge)"
+    tail = ", fused append" if fused else ""
+    comb = ", then combine_kernel" if plan_splits > 1 else ", rows written directly"
+    return f"attend_kernel ({kind} consumers, {mode} mode, g={g}{tail}){comb}"
+
 
 class MaskedBench:
     """Static-buffer workload: every layer appends the step's K/V row and runs
@@ -390,23 +462,27 @@ class MaskedBench:
         self.graph.replay()
         self.h_out.copy_(self.d_out, non_blocking=True)
 
-    def config(self):
-        cache = self.layers * 2 * self.B * self.Hkv * self.C * self.D * self.elem
-        L = self.lengths0
-        return {"workload": self.name, "batch": self.B, "q_heads": self.Hq, "kv_heads": self.Hkv,
-                "head_dim": self.D, "capacity": self.C, "layers": self.layers,
-                "valid_len_step0": (L if len(L) <= 4 else
-                                    {"min": min(L), "max": max(L), "mean": sum(L) / len(L)}),
-                "l2": f"inputs larger than L2: {cache / 2**30:.2f} GiB of layer caches rotated "
-                      f"per step vs {L2_BYTES // 2**20} MiB L2"} | self._window_config()
+    def attention_plan(self):
+        return self.kvd.attend_masked_plan(self.B, self.Hq, self.Hkv, self.C, self.D)
 
-    def _window_config(self):
-        if not self.w.window:
+    def kernel_name(self):
+        g = self.Hq // self.Hkv
+        kind = "tensor-core" if g >= 4 else "CUDA-core"
+        return attention_kernel_name(kind, self.attention_plan()[0], g, fused=True)
+
+    def aux_ops(self):
+        """The step's launches other than the attention kernel, per layer:
+        the combine, when the plan splits rows (the append runs inside the
+        attention launch)."""
+        part = self.kvd.workspace_partials(self.ws, self.attention_plan(), self.B * self.Hq,
+                                           self.D)
+        if part is None:
             return {}
-        rows = self.layers * 2 * self.Hkv * sum(self.rows_at(0)) * self.D * self.elem
-        return {"window": self.w.window,
-                "l2": f"inputs larger than L2: the windows' K/V rows of the {self.layers} layers "
-                      f"read per step are {rows / 2**20:.0f} MiB vs {L2_BYTES // 2**20} MiB L2"}
+        po, pl = part
+        return {"combine": lambda li: self.kvd.combine(po, pl, out=self.out[li].view(-1, self.D))}
+
+    def config(self):
+        return masked_config(self.name, self.w, self.layers, self.lengths0)
 
 
 class PagedBench:
@@ -505,14 +581,26 @@ class PagedBench:
         self._attend()
         self.h_out.copy_(self.out, non_blocking=True)
 
+    def attention_plan(self):
+        cols = self.pw.block_tables.shape[1]
+        return self.kvd.attend_paged_plan(self.Q, self.Hq, self.Hkv, self.BS, cols, self.D)
+
+    def kernel_name(self):
+        return attention_kernel_name("tensor-core", self.attention_plan()[0], self.Hq // self.Hkv,
+                                     mode="paged")
+
+    def aux_ops(self):
+        """The gather, and the combine behind the paged attention."""
+        ops = {"gather": lambda li: self._gather()}
+        part = self.kvd.workspace_partials(self.ws, self.attention_plan(), self.Q * self.Hq,
+                                           self.D)
+        if part is not None:
+            po, pl = part
+            ops["combine"] = lambda li: self.kvd.combine(po, pl, out=self.out.view(-1, self.D))
+        return ops
+
     def config(self):
-        rows = 2 * sum(self.lengths) * self.Hkv * self.D * self.elem
-        return {"workload": "paged", "num_blocks": self.NB, "block_size": self.BS,
-                "kv_heads": self.Hkv, "q_heads": self.Hq, "head_dim": self.D, "sequences": self.Q,
-                "total_tokens": self.pw.total_tokens,
-                "l2": f"inputs larger than L2: {rows / 2**30:.2f} GiB of valid K/V rows per step "
-                      f"(of a {2 * self.pw.key_cache.numel() * 2 / 2**30:.0f} GiB cache) vs "
-                      f"{L2_BYTES // 2**20} MiB L2"}
+        return paged_config(self.pw)
 
 
 class IndexedBench(MaskedBench):
@@ -567,11 +655,28 @@ class IndexedBench(MaskedBench):
     def copy_setup(self):
         return False
 
+    def attention_plan(self):
+        return self.kvd.attend_indexed_plan(self.B, self.Hq, self.Hkv, self.TOPK, self.D)
+
+    def kernel_name(self):
+        return attention_kernel_name("tensor-core", self.attention_plan()[0], self.Hq // self.Hkv,
+                                     mode="index-list")
+
+    def aux_ops(self):
+        """The append kernel and the combine."""
+        lays = self.w.layers
+        ops = {"append": lambda li: self.kvd.append(lays[li].k_cache, lays[li].v_cache,
+                                                    lays[li].k_new, lays[li].v_new, self.gpos,
+                                                    None, self.status)}
+        part = self.kvd.workspace_partials(self.ws, self.attention_plan(), self.B * self.Hq,
+                                           self.D)
+        if part is not None:
+            po, pl = part
+            ops["combine"] = lambda li: self.kvd.combine(po, pl, out=self.out[li].view(-1, self.D))
+        return ops
+
     def config(self):
-        c = super().config()
-        c.update({"workload": "indexed", "topk": self.TOPK,
-                  "listed_per_entry": {"min": min(self.listed), "max": max(self.listed)}})
-        return c
+        return masked_config("indexed", self.w, self.layers, self.lengths0)
 
 
 class Fp8Bench(MaskedBench):
@@ -626,13 +731,28 @@ class Fp8Bench(MaskedBench):
     def copy_setup(self):
         return False
 
+    def attention_plan(self):
+        return self.kvd.attend_masked_fp8_plan(self.B, self.Hq, self.Hkv, self.C, self.D)
+
+    def kernel_name(self):
+        return attention_kernel_name("E4M3 tensor-core", self.attention_plan()[0],
+                                     self.Hq // self.Hkv)
+
+    def aux_ops(self):
+        """The quantising append kernel and the combine."""
+        lays = self.w.layers
+        ops = {"append": lambda li: self.kvd.append_fp8(lays[li].k_cache, lays[li].v_cache,
+                                                        lays[li].k_new, lays[li].v_new,
+                                                        self.gpos, lays[li].mask, self.status)}
+        part = self.kvd.workspace_partials(self.ws, self.attention_plan(), self.B * self.Hq,
+                                           self.D)
+        if part is not None:
+            po, pl = part
+            ops["combine"] = lambda li: self.kvd.combine(po, pl, out=self.out[li].view(-1, self.D))
+        return ops
+
     def config(self):
-        c = super().config()
-        cache = self.layers * 2 * self.B * self.Hkv * self.C * self.row
-        c.update({"workload": "gqa_fp8", "kv_format": f"E4M3 codes + fp32 row scale, "
-                  f"{self.row}-byte rows", "l2": f"inputs larger than L2: {cache / 2**30:.2f} GiB "
-                  f"of layer caches rotated per step vs {L2_BYTES // 2**20} MiB L2"})
-        return c
+        return masked_config("gqa_fp8", self.w, self.layers, self.lengths0)
 
 
 def make_bench(name, torch, kvd, dev, layers=None):
@@ -688,19 +808,24 @@ def cpu_model():
     return platform.machine()
 
 
-def roofline_entry(res, peak, peak_src, traffic):
-    """The dominant kernel against the HBM roofline.  When the step is one
-    attention launch per layer, its average duration comes from the timed
-    steps themselves (launches back to back, as a caller runs them); else from
-    the per-launch pass (each call between CUDA events, which also keeps
-    consecutive kernels from overlapping)."""
-    in_step = "attend_gbs_in_step" in res
-    ach = res["attend_gbs_in_step"] if in_step else res["attend_gbs"]
+def roofline_entry(b, res, peak, peak_src, traffic):
+    """The attention kernel against the HBM roofline.  Its duration comes from
+    the timed steps: the step time minus the step's other launches (the
+    combine, a separate append, the gather), each kind timed on its own as a
+    CUDA graph of its launches for every layer of the step, per layer."""
+    ach = res["attend_gbs_in_step"]
     return {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-            "traffic": traffic, "kernel": "attention per layer (the fused step's kernels)",
-            "ms_per_launch": res["attend_ms_in_step"] if in_step else res["attend_ms_per_launch"],
-            "duration_from": "timed steps / launches" if in_step else "per-launch CUDA events",
-            "per_launch_pass": {"achieved": res["attend_gbs"], "frac": res["attend_frac"],
+            "traffic": traffic, "bytes_per_launch": res["attend_bytes"],
+            "kernel": b.kernel_name(), "ms_per_launch": res["attend_ms_in_step"],
+            "duration_from": "timed steps minus the graph-timed other launches of the step",
+            "other_launches_ms_per_step": res["aux_ms_per_step"],
+            "attention_op": {"what": "attention + combine per layer inside the timed steps",
+                             "ms_per_layer": res["op_ms_in_step"],
+                             "achieved": res["op_gbs_in_step"],
+                             "frac": res["op_gbs_in_step"] / peak},
+            "per_launch_pass": {"what": "each attention call (attention + combine) between CUDA "
+                                        "events, launches queued behind a spinning kernel",
+                                "achieved": res["attend_gbs"], "frac": res["attend_frac"],
                                 "ms_per_launch": res["attend_ms_per_launch"]},
             "peak_source": peak_src}
 
@@ -753,6 +878,31 @@ def gate_stream(torch, ms=10):
     """Hold the stream with a spinning kernel so that the launches queued
     behind it run back to back, without host gaps between them."""
     torch.cuda._sleep(int(ms * 1e-3 * 2.0e9))
+
+
+def measure_aux(b, torch, K):
+    """Each kind of the step's non-attention launches timed on its own: a CUDA
+    graph of that kind's launch for every layer, replayed K times between CUDA
+    events.  Returns ms per step by kind."""
+    out = {}
+    for kind, op in b.aux_ops().items():
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for li in range(b.layers):
+                op(li)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        out[kind] = e0.elapsed_time(e1) / K
+        del g
+    return out
 
 
 def measure_workload(b, torch, dist, K, W, peak, clocks=None):
@@ -808,17 +958,27 @@ def measure_workload(b, torch, dist, K, W, peak, clocks=None):
         if d:
             res[kind + "_ms_per_launch"] = sum(d) / len(d)
     a_bytes = sum(b.attend_bytes(j) for j in range(K)) / K
-    res["attend_gbs"] = a_bytes / (res["attend_ms_per_launch"] / 1e3) / 1e9
+    res["attend_bytes"] = a_bytes
+    res["attend_gbs_per_launch"] = a_bytes / (res["attend_ms_per_launch"] / 1e3) / 1e9
+    res["attend_gbs"] = res["attend_gbs_per_launch"]
     res["attend_frac"] = res["attend_gbs"] / peak
-    # a step made of one attention launch per layer and nothing else: the
-    # launch's average duration inside the timed (captured) steps
+    # the attention kernel's duration inside the timed steps: the step time
+    # minus the step's other launches, each kind timed alone as a graph
     layers = getattr(b, "layers", 1)
-    if b.launches_per_step() == layers:
-        res["attend_ms_in_step"] = res["ms_per_step"] / layers
-        res["attend_gbs_in_step"] = a_bytes / (res["attend_ms_in_step"] / 1e3) / 1e9
+    aux = measure_aux(b, torch, K)
+    res["aux_ms_per_step"] = aux
+    attn_step = max(res["ms_per_step"] - sum(aux.values()), 1e-6)
+    res["attend_ms_in_step"] = attn_step / layers
+    res["attend_gbs_in_step"] = a_bytes / (res["attend_ms_in_step"] / 1e3) / 1e9
+    # the attention operation (kernel + combine) per layer inside the steps
+    op_step = max(res["ms_per_step"] - sum(v for k, v in aux.items() if k != "combine"), 1e-6)
+    res["op_ms_in_step"] = op_step / layers
+    res["op_gbs_in_step"] = a_bytes / (res["op_ms_in_step"] / 1e3) / 1e9
     if "gather_ms_per_launch" in res:
         res["gather_gbs"] = b.gather_bytes() / (res["gather_ms_per_launch"] / 1e3) / 1e9
         res["gather_frac"] = res["gather_gbs"] / peak
+    if "gather" in aux:
+        res["gather_gbs_graph"] = b.gather_bytes() / (aux["gather"] / 1e3) / 1e9
 
     b.reset_cycle()
     gbs_e, ms_e = whole_job_rate(torch, dist, timed(torch, dist, b.eager_run, K),
@@ -867,86 +1027,80 @@ def measure_e2e(b, torch, dist, K):
 
 # -------------------------------------------------------------- CPU oracle
 
-def oracle_rate(name, seconds, W_mod=None):
-    """Time the fp64 oracle (append + attention, or gather + paged attention)
-    on host copies of the workload, for about `seconds` of CPU work.
-    Returns (GB/s of algorithmic bytes, cores, description of the sample)."""
+def oracle_rate(name, seconds):
+    """Time the fp64 oracle on host copies of the workload: whole layers
+    (append + attention; for the paged workload gather + paged attention over
+    all sequences), repeated for about ``seconds`` of CPU work and at least
+    one layer.  Returns the cpu_baseline dict: GB/s of the same algorithmic
+    bytes as the GPU line, per-layer milliseconds, cores, sample."""
     import torch
 
     import oracle
     import workloads
     oracle.build()
+
+    def run(step, per_layer_bytes, what):
+        done, t0, n = 0, time.perf_counter(), 0
+        while True:
+            step(n)
+            done += per_layer_bytes
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+        return {"value": done / el / 1e9, "unit": "GB/s", "cores": oracle.threads(),
+                "kind": "oracle", "per_layer_ms": el / n * 1e3, "layers_timed": n,
+                "sample": f"{n} whole layers of the {name} workload ({what}), {el:.1f} s",
+                "cpu_model": cpu_model()}
+
     if name == "paged":
         pw = workloads.paged(device="cpu")
         lengths = [int(x) for x in pw.lengths]
         kb = pw.key_cache.view(torch.int16).numpy()
         vb = pw.value_cache.view(torch.int16).numpy()
-        done_bytes, t0, n = 0, time.perf_counter(), 0
-        Q = len(lengths)
-        while True:
-            q = n % Q
-            sl_q = torch.tensor([0, lengths[q]], dtype=torch.int32)
-            bt_q = pw.block_tables[q:q + 1]
-            oracle.gather_paged(kb, vb, bt_q, sl_q)
-            oracle.attend_paged(pw.q[q:q + 1], pw.key_cache, pw.value_cache, bt_q, sl_q, None,
-                                pw.scale)
-            done_bytes += paged_attend_bytes([lengths[q]], 32, 8, 128, 2, 128) + \
-                gather_bytes([lengths[q]], 8, 128, 8, 128, 2, 128)
-            n += 1
-            el = time.perf_counter() - t0
-            if el >= seconds or n >= 4 * Q:
-                break
-        return done_bytes / el / 1e9, oracle.threads(), f"{n} sequences of the paged workload " \
-            f"(gather + paged attention), {el:.1f} s"
+        per = (paged_attend_bytes(lengths, 32, 8, 128, 2, 128)
+               + gather_bytes(lengths, 8, 128, 8, 128, 2, 128))
+
+        def step(n):
+            oracle.gather_paged(kb, vb, pw.block_tables, pw.seq_lens, pw.seq_offset)
+            oracle.attend_paged(pw.q, pw.key_cache, pw.value_cache, pw.block_tables, pw.seq_lens,
+                                pw.seq_offset, pw.scale)
+        return run(step, per, "gather + paged attention of all 64 sequences")
     if name == "indexed":
         w = workloads.gqa(device="cpu", layers=1)
         lay = w.layers[0]
         topk = IndexedBench.TOPK
         L = [int(x) for x in lay.lengths]
         idx = workloads.index_lists(L, topk)
-        per = (sum(min(topk, x) for x in L) * w.Hkv * w.D * 2 * 2 + w.B * topk * 4
-               + 2 * w.B * w.Hq * w.D * 2)
-        done_bytes, t0, n = 0, time.perf_counter(), 0
-        while True:
-            oracle.attend_indexed(lay.q, lay.k_cache, lay.v_cache, idx, lay.scale)
-            done_bytes += per
-            n += 1
-            el = time.perf_counter() - t0
-            if el >= seconds:
-                break
-        return done_bytes / el / 1e9, oracle.threads(), \
-            f"{n} layers of index-list attention (gqa caches, top-{topk}), {el:.1f} s"
+        per = (indexed_attend_bytes([min(topk, x) for x in L], topk, w.Hq, w.Hkv, w.D, 2)
+               + append_bytes(w.B, w.Hkv, w.D, 2))
+        kh, vh = lay.k_cache.view(torch.int16).numpy().copy(), lay.v_cache.view(torch.int16).numpy().copy()
+
+        def step(n):
+            oracle.append(kh, vh, lay.k_new, lay.v_new, lay.pos, None)
+            oracle.attend_indexed(lay.q, torch.from_numpy(kh).view(torch.bfloat16),
+                                  torch.from_numpy(vh).view(torch.bfloat16), idx, lay.scale)
+        return run(step, per, f"append + index-list attention, top-{topk}")
     if name == "gqa_fp8":
         w = workloads.gqa_fp8(device="cpu", layers=1)
         lay = w.layers[0]
         kh, vh, mh = lay.k_cache.numpy().copy(), lay.v_cache.numpy().copy(), lay.mask.numpy().copy()
         L = [int(x) for x in lay.lengths]
-        row = w.D + oracle.FP8_ROW_PAD
-        per = (sum(L) * w.Hkv * row * 2 + w.B * w.C + 2 * w.B * w.Hq * w.D * 2
-               + 2 * w.B * w.Hkv * (w.D * 2 + row))
-        done_bytes, t0, n = 0, time.perf_counter(), 0
-        while True:
+        per = (fp8_attend_bytes(L, w.Hq, w.Hkv, w.C, w.D, oracle.FP8_ROW_PAD)
+               + fp8_append_bytes(w.B, w.Hkv, w.D, oracle.FP8_ROW_PAD))
+
+        def step(n):
             oracle.append_fp8(kh, vh, lay.k_new, lay.v_new, lay.pos, mh)
             oracle.attend_masked_fp8(lay.q, kh, vh, mh, lay.scale)
-            done_bytes += per
-            n += 1
-            el = time.perf_counter() - t0
-            if el >= seconds:
-                break
-        return done_bytes / el / 1e9, oracle.threads(), \
-            f"{n} layer-steps (quantising append + attention) of the gqa_fp8 workload, {el:.1f} s"
-    if name == "npuw":
-        w = workloads.npuw(device="cpu", layers=4)
-    elif name == "gqa":
-        w = workloads.gqa(device="cpu", layers=1)
-    elif name == "window":
-        w = workloads.window(device="cpu", layers=1)
-    else:
-        w = workloads.long(device="cpu", layers=1)
-    done_bytes, t0, n = 0, time.perf_counter(), 0
+        return run(step, per, "quantising append + attention")
+    w = getattr(workloads, name)(device="cpu", layers=4 if name == "npuw" else 1)
     caches = [(l.k_cache.view(torch.int16).numpy().copy(), l.v_cache.view(torch.int16).numpy().copy(),
                l.mask.numpy().copy()) for l in w.layers]
-    while True:
+    lay0 = w.layers[0]
+    L = [min(int(x), w.window) if w.window else int(x) for x in lay0.lengths]
+    per = masked_attend_bytes(L, w.Hq, w.Hkv, w.C, w.D, 2) + append_bytes(w.B, w.Hkv, w.D, 2)
+
+    def step(n):
         li = n % len(w.layers)
         lay = w.layers[li]
         kh, vh, mh = caches[li]
@@ -954,14 +1108,7 @@ def oracle_rate(name, seconds, W_mod=None):
         oracle.attend_masked(lay.q, torch.from_numpy(kh).view(torch.bfloat16),
                              torch.from_numpy(vh).view(torch.bfloat16), torch.from_numpy(mh),
                              lay.scale)
-        L = [min(int(x), w.window) if w.window else int(x) for x in lay.lengths]
-        done_bytes += masked_attend_bytes(L, w.Hq, w.Hkv, w.C, w.D, 2) + append_bytes(w.B, w.Hkv, w.D, 2)
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return done_bytes / el / 1e9, oracle.threads(), \
-        f"{n} layer-steps (append + attention) of the {name} workload, {el:.1f} s"
+    return run(step, per, "append + attention")
 
 
 # -------------------------------------------------------------------- main
@@ -971,26 +1118,26 @@ METRIC = "decode-attention KV GB/s and % of GB300 HBM peak; decode tokens/sec at
 
 def reference_arm(args, rank, world):
     """The reference arm: the fp64 CPU oracle as it stands, on the host cores,
-    each step a bounded sample of the workload."""
+    each step a bounded sample of whole layers of the workload."""
     if rank != 0:
         return 0
     per_step = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         oracle_rate(args.workload, per_step * 0.2)
-    rates = []
+    rates, cb = [], None
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        r, cores, sample = oracle_rate(args.workload, per_step)
-        rates.append(r)
+        cb = oracle_rate(args.workload, per_step)
+        rates.append(cb["value"])
     el = time.perf_counter() - t0
     value = statistics.mean(rates)
+    cb = dict(cb, value=value, sample=f"per step: {cb['sample']}")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                             "sample": f"per step: {sample}"},
+            "config": workload_config(args.workload),
+            "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -1003,10 +1150,13 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvd", choices=["kvd", "reference"])
-    ap.add_argument("--workload", default="npuw",
-                    choices=["npuw", "gqa", "long", "paged", "indexed", "window", "gqa_fp8"])
+    ap.add_argument("--workload", default="gqa",
+                    choices=["gqa", "long", "paged", "npuw", "indexed", "window", "gqa_fp8"])
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="oracle seconds for the main workload's CPU baseline")
+    ap.add_argument("--cpu-seconds-others", type=float, default=4.0,
+                    help="oracle seconds for each other workload's CPU baseline")
     ap.add_argument("--profile", action="store_true",
                     help="no timing: run --warmup + --steps eager steps of --workload (for ncu)")
     ap.add_argument("--layers", type=int, default=None,
@@ -1048,13 +1198,47 @@ def main():
         log(f"profile run of {args.workload}: {args.warmup + args.steps} steps, status {st}")
         return 0 if st == 0 else 1
 
+    khash = kernel_source_hash()
+    want_cpu = rank == 0 and world == 1
+
+    def cpu_leg(name, seconds):
+        if not want_cpu:
+            return None
+        log(f"{name}: cpu baseline (oracle)")
+        try:
+            return oracle_rate(name, seconds)
+        except Exception as e:  # the oracle needs gcc on the host
+            return {"unavailable": f"{type(e).__name__}: {e}"}
+
+    def entry(name, b, res, e2e, cpu, copy):
+        """One workload's figures: the step rate, the attention kernel's
+        roofline, the end-to-end rate, the oracle beside it."""
+        ent = {"value": res["gbs"], "unit": "GB/s", "frac_of_hbm_peak": res["gbs"] / peak,
+               "ms_per_step": res["ms_per_step"], "decode_tokens_per_s": res["tokens_per_s"],
+               "decode_tokens_per_s_eager":
+                   b.tokens_per_step() / (res["eager"]["ms_per_step"] / 1e3),
+               "attend_frac": res["op_gbs_in_step"] / peak,
+               "attend_frac_per_launch_pass": res["attend_frac"],
+               "roofline": roofline_entry(b, res, peak, peak_src, NCU_TRAFFIC.get((name, khash))),
+               "e2e": e2e, "cpu_baseline": cpu, "eager": res["eager"],
+               "attention_tflops": res["attention_tflops"],
+               "step_ms": res["step_ms"], "step_ms_l2_flushed": res["step_ms_l2_flushed"],
+               "gpu_launches_per_step": b.launches_per_step(), "config": b.config()}
+        for k in ("append_ms_per_launch", "gather_gbs", "gather_frac", "gather_ms_per_launch",
+                  "gather_gbs_graph"):
+            if k in res:
+                ent[k] = res[k]
+        if copy is not None:
+            ent["copy_prefix"] = copy
+        return ent
+
     log(f"workload {args.workload}: building inputs")
     b = make_bench(args.workload, torch, kvd, dev, args.layers)
     clocks = ClockSampler(bus_id_of(torch, dev))
     log("timed steps")
     res = measure_workload(b, torch, dist, args.steps, args.warmup, peak, clocks=clocks)
     log(f"{args.workload}: {res['ms_per_step']:.3f} ms/step, {res['gbs']:.0f} GB/s; "
-        f"attention {res['attend_ms_per_launch'] * 1e3:.1f} us/launch; e2e pass")
+        f"attention kernel {res['attend_ms_in_step'] * 1e3:.1f} us/layer in the step; e2e pass")
     e2e = measure_e2e(b, torch, dist, args.steps)
     copy = measure_copy(b, torch, min(args.steps, 10))
     if copy is not None:
@@ -1062,68 +1246,51 @@ def main():
     st = int(b.status.item())
     if st != 0:
         raise RuntimeError(f"device status {st} during the benchmark")
-
-    traffic = NCU_TRAFFIC.get((args.workload, kernel_source_hash()))
+    main_launches = b.launches_per_step()
 
     others = {}
     if not args.no_others:
-        for name in ("gqa", "long", "paged", "indexed", "window", "gqa_fp8", "npuw"):
+        for name in ("long", "paged", "npuw", "gqa", "indexed", "window", "gqa_fp8"):
             if name == args.workload:
                 continue
             log(f"workload {name}")
             ob = make_bench(name, torch, kvd, dev)
             r = measure_workload(ob, torch, dist, max(5, min(args.steps, 20)), 3, peak)
+            oe = measure_e2e(ob, torch, dist, max(5, min(args.steps, 20)))
+            oc = measure_copy(ob, torch, 5)
             if int(ob.status.item()) != 0:
                 raise RuntimeError(f"device status {int(ob.status.item())} in workload {name}")
-            ent = {"gbs": r["gbs"], "frac": r["gbs"] / peak, "ms_per_step": r["ms_per_step"],
-                   "tokens_per_s": r["tokens_per_s"], "attend_gbs": r["attend_gbs"],
-                   "attend_frac": r["attend_frac"],
-                   "attend_ms_per_launch": r["attend_ms_per_launch"], "eager": r["eager"],
-                   "attend_traffic": NCU_TRAFFIC.get((name, kernel_source_hash())),
-                   "config": ob.config()}
-            for k in ("append_ms_per_launch", "gather_gbs", "gather_frac", "gather_ms_per_launch",
-                      "attend_gbs_in_step", "attend_ms_in_step"):
-                if k in r:
-                    ent[k] = r[k]
-            oc = measure_copy(ob, torch, 5)
-            if oc is not None:
-                ent["copy_prefix"] = oc
-            log(f"{name}: {r['gbs']:.0f} GB/s, attention {r['attend_gbs']:.0f} GB/s")
-            others[name] = ent
+            log(f"{name}: {r['gbs']:.0f} GB/s; attention kernel {r['attend_gbs_in_step']:.0f} GB/s "
+                f"in the step, attention + combine {r['op_gbs_in_step']:.0f} GB/s")
+            others[name] = entry(name, ob, r, oe, None, oc)
             del ob
             torch.cuda.empty_cache()
 
-    cpu = None
-    if rank == 0 and world == 1:
-        log("cpu baseline (oracle)")
-        try:
-            v, cores, sample = oracle_rate(args.workload, args.cpu_seconds)
-            cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
-                   "cpu_model": cpu_model()}
-        except Exception as e:  # the oracle needs gcc on the host
-            cpu = {"unavailable": f"{type(e).__name__}: {e}"}
+    cpu = cpu_leg(args.workload, args.cpu_seconds)
+    for name, ent in others.items():
+        ent["cpu_baseline"] = cpu_leg(name, args.cpu_seconds_others)
 
     if rank == 0:
+        ent = entry(args.workload, b, res, e2e, cpu, copy)
         line = {
             "metric": METRIC, "value": res["gbs"], "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if args.workload != "gqa_fp8" else "e4m3 kv / bf16",
             "data": "synthetic", "config": b.config(),
-            "frac_of_hbm_peak": res["gbs"] / peak, "peak_source": peak_src,
-            "decode_tokens_per_s": res["tokens_per_s"],
-            "decode_tokens_per_s_eager": b.tokens_per_step() / (res["eager"]["ms_per_step"] / 1e3),
-            "attention_tflops": res["attention_tflops"],
-            "step_ms": res["step_ms"], "step_ms_l2_flushed": res["step_ms_l2_flushed"],
+            "peak_source": peak_src,
             "timing": "each timed step is one CUDA-graph replay of the decode step "
                       "(all layers' kvd kernels); 'eager' = one binding call per kernel",
-            "roofline": roofline_entry(res, peak, peak_src, traffic),
-            "append_ms_per_launch": res.get("append_ms_per_launch"),
-            "copy_prefix": copy,
-            "eager": res["eager"], "e2e": e2e,
-            "gpu_launches": b.launches_per_step() * args.steps,
-            "clocks": res.get("clocks"), "cpu_baseline": cpu,
-            "workloads": others, "kernel_hash": kernel_source_hash(),
+            "roofline": ent.pop("roofline"), "e2e": ent.pop("e2e"),
+            "cpu_baseline": ent.pop("cpu_baseline"),
+            "gpu_launches": main_launches * args.steps,
+            "clocks": res.get("clocks"), "kernel_hash": khash,
         }
+        ent.pop("config")
+        for k, v in ent.items():
+            if k not in line and k != "value":
+                line[k] = v
+        line["workloads"] = others
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()

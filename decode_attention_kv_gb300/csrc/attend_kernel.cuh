@@ -104,7 +104,26 @@ struct AttendParams {
     const void* v_new;
     const int32_t* pos;          // [rows]
     uint8_t* mask_w;             // the mask, written at pos
+    int out_f32;                 // out is fp32 whatever the element type (a range's partial)
 };
+
+// Output rows: the element type of q, or fp32 for a token range's partial
+// (out_f32), which another step merges by log-sum-exp.
+template <typename Elem>
+__device__ __forceinline__ void store_out4(const AttendParams& p, size_t i, float4 x) {
+    if (p.out_f32)
+        ElemTraits<float>::store4(p.out, i, x);
+    else
+        ElemTraits<Elem>::store4(p.out, i, x);
+}
+
+template <typename Elem>
+__device__ __forceinline__ void store_out1(const AttendParams& p, size_t i, float x) {
+    if (p.out_f32)
+        ElemTraits<float>::store(p.out, i, x);
+    else
+        ElemTraits<Elem>::store(p.out, i, x);
+}
 
 enum : uint32_t { kFirst = 1u, kLast = 2u, kEnd = 8u };
 
@@ -287,6 +306,29 @@ __device__ __forceinline__ uint32_t nonzero_bytes(uint32_t x) {
     return (t & 1u) | ((t >> 7) & 2u) | ((t >> 14) & 4u) | ((t >> 21) & 8u);
 }
 
+// Mask loads.  Without the fused append the mask is read-only for the whole
+// launch: non-coherent cached loads.  With it, the unit of kv head 0 whose
+// range holds pos[b] stores the mask slot during the launch while other units
+// read the same row, so the loads go to L2 (ld.global.cg), never to a stale
+// L1 line.  A read that comes before that store sees 0 at pos[b]; that is
+// harmless, because every unit whose range holds pos[b] ORs the bit into its
+// own validity words itself (fused_append).
+__device__ __forceinline__ uint4 ld_mask16(const uint4* ptr, bool written) {
+    if (!written) return __ldg(ptr);
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr));
+    return v;
+}
+
+__device__ __forceinline__ uint8_t ld_mask1(const uint8_t* ptr, bool written) {
+    if (!written) return __ldg(ptr);
+    unsigned short v;
+    asm volatile("ld.global.cg.u8 %0, [%1];" : "=h"(v) : "l"(ptr));
+    return (uint8_t)v;
+}
+
 // Producer warp, all lanes: the split's validity words (bit = token valid:
 // mask != 0, or below the sequence length with its block id in range) and,
 // paged, the physical block of each logical block the split touches.  Writes
@@ -349,6 +391,7 @@ __device__ __forceinline__ int producer_scan(const AttendParams& p, const SplitR
         }
     } else {
         const uint8_t* mrow = p.mask + (size_t)bz * p.C;
+        const bool written = p.pos != nullptr && p.mask_w != nullptr;  // fused append
         if (p.mask_vec) {
             // 16 slots per lane per vector, 512 slots per warp round; the whole
             // split's mask is requested before any bit is used.
@@ -359,7 +402,7 @@ __device__ __forceinline__ int producer_scan(const AttendParams& p, const SplitR
 #pragma unroll
             for (int k = 0; k < R; ++k) {
                 const int vi = k * 32 + lane;
-                mv[k] = vi < nvec ? __ldg(src + vi) : make_uint4(0, 0, 0, 0);
+                mv[k] = vi < nvec ? ld_mask16(src + vi, written) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int k = 0; k < R; ++k) {
@@ -378,7 +421,7 @@ __device__ __forceinline__ int producer_scan(const AttendParams& p, const SplitR
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int tok = r.t_begin + 32 * (j0 + u) + lane;
-                    mb[u] = (j0 + u < nwords && tok < r.t_end) ? __ldg(mrow + tok) : 0;
+                    mb[u] = (j0 + u < nwords && tok < r.t_end) ? ld_mask1(mrow + tok, written) : 0;
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -465,7 +508,7 @@ __device__ __forceinline__ void write_rows(const AttendParams& p, const float* m
         O.z *= inv;
         O.w *= inv;
         if (p.direct) {
-            ElemTraits<Elem>::store4(p.out, row * D + 4 * d4, O);
+            store_out4<Elem>(p, row * D + 4 * d4, O);
             if (d4 == 0 && p.lse_out) p.lse_out[row] = lse;
         } else {
             if (L > 0.f)
@@ -631,7 +674,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
             } else if (p.direct) {
                 // the whole row is empty: zeros and lse = -inf
                 for (int idx = lane; idx < un.g_here * D; idx += 32)
-                    ElemTraits<Elem>::store(p.out, (un.qrow0 + idx / D) * D + idx % D, 0.f);
+                    store_out1<Elem>(p, (un.qrow0 + idx / D) * D + idx % D, 0.f);
                 if (lane < un.g_here && p.lse_out) p.lse_out[un.qrow0 + lane] = -INFINITY;
             } else if (lane < un.g_here) {
                 p.part_lse[(un.qrow0 + lane) * p.S + un.split] = -INFINITY;  // no partial row

@@ -12,13 +12,16 @@
 // device, held by every GPU that loads the library until the process exits).
 //
 // The array is shared by every call on a device and keeps whatever the last
-// call left in it.  The attention kernel keeps its work counters there; they
-// must be zero when a call starts: the array is zero-initialised when the
-// library is loaded and every call leaves its counters at zero again (the
-// partial rows need no clearing: each call writes the log-sum-exp of every
-// split it reads and reads only partial rows it wrote).  Calls that may run
-// at the same time on the GPU (different streams, or different host threads
-// without ordering) race on the array and must be serialised by the caller.
+// call left in it.  The attention kernel keeps its work counters in the first
+// 256 bytes; they must be zero when a launch starts.  A completed launch
+// leaves them at zero, but one whose bounded waits ran out (KVD_DEV_TIMEOUT)
+// may not, so every call clears that block on the caller's stream
+// (cudaMemsetAsync: stream-ordered, allocates nothing) before its launch.
+// The partial rows need no clearing: each call writes the log-sum-exp of
+// every split it reads and reads only partial rows it wrote.  Calls that may
+// run at the same time on the GPU (different streams, or different host
+// threads without ordering) race on the array and must be serialised by the
+// caller.
 #include <cstdio>
 #include <mutex>
 
@@ -34,24 +37,52 @@ constexpr int kMaxDevices = 64;
 // never a device address: the address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char kvd_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+// Driver entry point used to tell one context of a device from the next
+// (after cudaDeviceReset the library's module is loaded again, possibly at
+// another address).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+std::once_flag g_ctx_once;
 
-// Device address of the scratch array on the current device, looked up once
-// per device (with that device current) and cached.
+std::mutex g_scratch_mutex;
+struct ScratchEntry {
+    CUcontext ctx;
+    void* ptr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
+
+// Device address of the scratch array in the current device's current
+// context, looked up with that device current the first time a context is
+// seen, then cached.
 cudaError_t scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(g_ctx_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    });
+    // No context may be current yet on this thread (cudaGetDevice creates
+    // none); the symbol lookup makes the primary context current, so the
+    // context is asked for again after it.
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current) g_ctx_get_current(&ctx);
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
+    ScratchEntry& ent = g_scratch[dev];
+    if (!ent.ptr || !ctx || ent.ctx != ctx) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, kvd_noalloc_scratch);
         if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
+        if (g_ctx_get_current) g_ctx_get_current(&ctx);
+        ent.ctx = ctx;
+        ent.ptr = p;
     }
-    *out = g_scratch_ptr[dev];
+    *out = ent.ptr;
     return cudaSuccess;
 }
 
@@ -86,6 +117,16 @@ kvd_status kvd_attend_masked_noalloc(const void* q, const void* k_cache, const v
         char msg[256];
         snprintf(msg, sizeof msg, "kvd_attend_masked_noalloc: cudaGetSymbolAddress failed: %s",
                  cudaGetErrorString(e));
+        kvd::set_last_error(msg);
+        return KVD_ERR_CUDA;
+    }
+    // Work counters to zero first (a previous call's timed-out launch may have
+    // left them set); stream-ordered before the launch.
+    const cudaError_t ez = cudaMemsetAsync(scratch, 0, 256, (cudaStream_t)stream);
+    if (ez != cudaSuccess) {
+        char msg[256];
+        snprintf(msg, sizeof msg, "kvd_attend_masked_noalloc: clearing the counters failed: %s",
+                 cudaGetErrorString(ez));
         kvd::set_last_error(msg);
         return KVD_ERR_CUDA;
     }

@@ -151,13 +151,14 @@ attend_small_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
         constexpr bool kAppend = Cons::kRowBytes == D * (int)sizeof(Elem);
         const int x = (kAppend && p.pos) ? __ldg(p.pos + bz) : -1;
         const uint8_t* mrow = p.mask + (size_t)bz * p.C;
+        const bool written = kAppend && p.pos != nullptr && p.mask_w != nullptr;
         const int nwords = (ntiles * T + 31) / 32;
         if (p.mask_vec) {
             // 16 slots per lane (t_begin is a multiple of 16, the rows 16-byte aligned)
             const int nvec = (ntok + 15) / 16;
             uint32_t bits = 0;
             if (lane < nvec) {
-                const uint4 mv = __ldg(reinterpret_cast<const uint4*>(mrow + t_begin) + lane);
+                const uint4 mv = ld_mask16(reinterpret_cast<const uint4*>(mrow + t_begin) + lane, written);
                 bits = nonzero_bytes(mv.x) | (nonzero_bytes(mv.y) << 4) |
                        (nonzero_bytes(mv.z) << 8) | (nonzero_bytes(mv.w) << 12);
                 const int nv = min(ntok - lane * 16, 16);
@@ -171,7 +172,7 @@ attend_small_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
 #pragma unroll
             for (int j = 0; j < kW; ++j) {
                 const int tok = t_begin + 32 * j + lane;
-                mb[j] = (j < nwords && tok < t_end) ? __ldg(mrow + tok) : 0;
+                mb[j] = (j < nwords && tok < t_end) ? ld_mask1(mrow + tok, written) : 0;
             }
 #pragma unroll
             for (int j = 0; j < kW; ++j) {
@@ -308,7 +309,7 @@ attend_small_kernel(const AttendParams p, const __grid_constant__ CUtensorMap km
             O.z *= inv;
             O.w *= inv;
             const size_t row = qrow0 + hh;
-            ElemTraits<Elem>::store4(p.out, row * D + 4 * d4, O);
+            store_out4<Elem>(p, row * D + 4 * d4, O);
             if (d4 == 0 && p.lse_out)
                 p.lse_out[row] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
         }

@@ -16,7 +16,16 @@ namespace kvd {
 // output and a batch of splits' loads in flight (a split with lse = -inf has
 // no partial row: its values are loaded and discarded); the item's first
 // warp merges the states.  VPL = 2 halves the CTAs when there are many rows.
+// Strides (in elements) place the partials: row-major [R, S, D] / [R, S]
+// (what the split attention writes), or one block per split of R rows of D
+// then the R log-sum-exps (what gathering every range's packed partial one
+// after the other gives).
 constexpr int kCombineWarps = 8;
+
+struct CombineStrides {
+    long long o_row, o_split;      // part_o
+    long long lse_row, lse_split;  // part_lse
+};
 constexpr int kCombineBatch = 8;  // splits per warp with loads in flight
 
 template <int VPL>
@@ -40,7 +49,8 @@ struct CombineVec<2> {
 template <typename Out, int VPL>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
-               Out* __restrict__ out, float* __restrict__ lse_out, int R, int S, int D, int wpi) {
+               Out* __restrict__ out, float* __restrict__ lse_out, int R, int S, int D, int wpi,
+               CombineStrides st) {
     using Vec = CombineVec<VPL>;
     using T = typename Vec::T;
     __shared__ float sm_m[kCombineWarps], sm_l[kCombineWarps];
@@ -59,17 +69,18 @@ combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_
     float m = -INFINITY, l = 0.f;  // m in log2 units
     T acc = Vec::zero();
     if (live) {
-        const float* ls = part_lse + row * S;
-        const float* po = part_o + row * S * D;
+        const float* ls = part_lse + row * st.lse_row;
+        const float* po = part_o + row * st.o_row;
         for (int s0 = sub; s0 < S; s0 += wpi * kCombineBatch) {
             float lv[kCombineBatch];
             T xv[kCombineBatch];
 #pragma unroll
             for (int u = 0; u < kCombineBatch; ++u) {
                 const int s = s0 + u * wpi;
-                lv[u] = s < S ? ls[s] : -INFINITY;
-                xv[u] = (s < S && has_d) ? *reinterpret_cast<const T*>(po + (size_t)s * D + d)
-                                         : Vec::zero();
+                lv[u] = s < S ? ls[(long long)s * st.lse_split] : -INFINITY;
+                xv[u] = (s < S && has_d)
+                            ? *reinterpret_cast<const T*>(po + (long long)s * st.o_split + d)
+                            : Vec::zero();
             }
 #pragma unroll
             for (int u = 0; u < kCombineBatch; ++u) {
@@ -113,29 +124,36 @@ combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_
 template <int VPL>
 cudaError_t launch_combine_vpl(const float* part_o, const float* part_lse, void* out,
                                float* lse_out, int R, int S, int D, kvd_dtype out_dt, int wpi,
-                               cudaStream_t stream) {
+                               const CombineStrides& st, cudaStream_t stream) {
     const long long items = (long long)R * ((D + 32 * VPL - 1) / (32 * VPL));
     const long long per_cta = kCombineWarps / wpi;
     const dim3 grid((unsigned)((items + per_cta - 1) / per_cta));
     if (out_dt == KVD_BF16)
         return launch_pdl(combine_kernel<__nv_bfloat16, VPL>, grid, dim3(kCombineWarps * 32), 0,
                           stream, part_o, part_lse, static_cast<__nv_bfloat16*>(out), lse_out, R,
-                          S, D, wpi);
+                          S, D, wpi, st);
     return launch_pdl(combine_kernel<float, VPL>, grid, dim3(kCombineWarps * 32), 0, stream, part_o,
-                      part_lse, static_cast<float*>(out), lse_out, R, S, D, wpi);
+                      part_lse, static_cast<float*>(out), lse_out, R, S, D, wpi, st);
 }
 
 cudaError_t launch_combine(const float* part_o, const float* part_lse, void* out,
                            float* lse_out, int R, int S, int D, kvd_dtype out_dt,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, long long gathered_stride) {
+    // row-major [R, S, D] / [R, S], or blocks of gathered_stride floats per split
+    const CombineStrides st = gathered_stride > 0
+                                  ? CombineStrides{D, gathered_stride, 1, gathered_stride}
+                                  : CombineStrides{(long long)S * D, D, S, 1};
     // warps per item: enough that each warp's splits fit one batch of loads
     // (a power of two, 1..8)
     int wpi = 1;
     while (wpi < kCombineWarps && wpi * kCombineBatch < S) wpi *= 2;
     // two dims per lane once one dim per lane would need more than ~1024 items
-    if ((long long)R * ((D + 31) / 32) >= 1024 && D % 2 == 0)
-        return launch_combine_vpl<2>(part_o, part_lse, out, lse_out, R, S, D, out_dt, wpi, stream);
-    return launch_combine_vpl<1>(part_o, part_lse, out, lse_out, R, S, D, out_dt, wpi, stream);
+    // (8-byte loads: every row of every split must start 8-byte aligned)
+    const bool even = D % 2 == 0 && st.o_split % 2 == 0;
+    if ((long long)R * ((D + 31) / 32) >= 1024 && even)
+        return launch_combine_vpl<2>(part_o, part_lse, out, lse_out, R, S, D, out_dt, wpi, st,
+                                     stream);
+    return launch_combine_vpl<1>(part_o, part_lse, out, lse_out, R, S, D, out_dt, wpi, st, stream);
 }
 
 // ---------------------------------------------------------- copy_kvcache

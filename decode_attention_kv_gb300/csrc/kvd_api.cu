@@ -300,6 +300,19 @@ kvd_status check_attention_shape(int Hq, int Hkv, int D, kvd_dtype dt) {
     return KVD_OK;
 }
 
+// What the *_plan queries report: S of the split kernel (0 for the
+// one-launch cluster kernel) and where its partial rows sit in the workspace.
+void put_plan(const Plan& pl, bool small, int32_t* splits, size_t* lse_offset, size_t* o_offset) {
+    if (small) {
+        *splits = 0;  // one launch, merged inside thread-block clusters: no partial rows
+        *lse_offset = *o_offset = 0;
+    } else {
+        *splits = pl.S;
+        *lse_offset = pl.S > 1 ? pl.off_lse : 0;
+        *o_offset = pl.S > 1 ? pl.off_po : 0;
+    }
+}
+
 }  // namespace
 
 namespace kvd {
@@ -385,6 +398,21 @@ size_t kvd_attend_masked_workspace_bytes(int B, int Hq, int Hkv, int C, int D, k
     return plan_attention(B, Hq, Hkv, C, D, dtype, 0, num_splits).ws;
 }
 
+kvd_status kvd_attend_masked_plan(int B, int Hq, int Hkv, int C, int D, kvd_dtype dtype,
+                                  int num_splits, int32_t* splits, size_t* lse_offset,
+                                  size_t* o_offset) {
+    if (!splits || !lse_offset || !o_offset)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_plan: null pointer");
+    if (B < 1 || C < 1 || num_splits < 0)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_plan: B, C >= 1 and num_splits >= 0 required");
+    const kvd_status st = check_attention_shape(Hq, Hkv, D, dtype);
+    if (st != KVD_OK) return st;
+    const Plan pl = plan_attention(B, Hq, Hkv, C, D, dtype, 0, num_splits);
+    put_plan(pl, plan_small(B, Hkv, C, D, dtype, pl, num_splits).use, splits, lse_offset,
+             o_offset);
+    return ok();
+}
+
 }  // extern "C"
 
 namespace {
@@ -395,7 +423,8 @@ kvd_status attend_masked_impl(const char* fn, const void* q, const void* k_cache
                               float* lse_out, int B, int Hq, int Hkv, int C, int D, float scale,
                               kvd_dtype dtype, int num_splits, void* workspace,
                               size_t workspace_bytes, int32_t* dev_status, kvd_stream_t stream,
-                              const void* k_new, const void* v_new, const int32_t* pos) {
+                              const void* k_new, const void* v_new, const int32_t* pos,
+                              bool out_f32 = false) {
     kvd_status st = check_attention_shape(Hq, Hkv, D, dtype);
     if (st != KVD_OK) return st;
     if (B < 0 || C < 1) return fail(KVD_ERR_INVALID_ARG, "%s: B >= 0 and C >= 1 required", fn);
@@ -427,6 +456,7 @@ kvd_status attend_masked_impl(const char* fn, const void* q, const void* k_cache
     p.v_new = v_new;
     p.pos = k_new ? pos : nullptr;
     p.mask_w = const_cast<uint8_t*>(mask);
+    p.out_f32 = out_f32 ? 1 : 0;
     attach_workspace(p, pl, workspace);
     CUtensorMap kmap, vmap;
     std::memset(&kmap, 0, sizeof kmap);
@@ -453,8 +483,8 @@ kvd_status attend_masked_impl(const char* fn, const void* q, const void* k_cache
     cudaError_t e = launch_attend(dtype, D, pl.G, kModeMasked, p, &kmap, &vmap, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, fn);
     if (pl.S > 1) {
-        e = launch_combine(p.part_o, p.part_lse, out, lse_out, B * Hq, pl.S, D, dtype,
-                           (cudaStream_t)stream);
+        e = launch_combine(p.part_o, p.part_lse, out, lse_out, B * Hq, pl.S, D,
+                           out_f32 ? KVD_F32 : dtype, (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, fn);
     }
     return ok();
@@ -472,6 +502,19 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
     return attend_masked_impl("kvd_attend_masked", q, k_cache, v_cache, mask, out, lse_out, B, Hq,
                               Hkv, C, D, scale, dtype, num_splits, workspace, workspace_bytes,
                               dev_status, stream, nullptr, nullptr, nullptr);
+}
+
+kvd_status kvd_attend_masked_partial(const void* q, const void* k_cache, const void* v_cache,
+                                     const uint8_t* mask, float* out, float* lse_out, int B,
+                                     int Hq, int Hkv, int C, int D, float scale, kvd_dtype dtype,
+                                     int num_splits, void* workspace, size_t workspace_bytes,
+                                     int32_t* dev_status, kvd_stream_t stream) {
+    if (B > 0 && !lse_out)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_partial: lse_out required");
+    return attend_masked_impl("kvd_attend_masked_partial", q, k_cache, v_cache, mask, out, lse_out,
+                              B, Hq, Hkv, C, D, scale, dtype, num_splits, workspace,
+                              workspace_bytes, dev_status, stream, nullptr, nullptr, nullptr,
+                              true);
 }
 
 kvd_status kvd_append_attend_masked(const void* q, void* k_cache, void* v_cache, uint8_t* mask,
@@ -524,6 +567,20 @@ constexpr int kFp8Tile = 64;  // tokens per ring stage over quantised rows
 size_t kvd_attend_masked_fp8_workspace_bytes(int B, int Hq, int Hkv, int C, int D, int num_splits) {
     if (B < 1 || C < 1 || check_attention_shape(Hq, Hkv, D, KVD_BF16) != KVD_OK) return 0;
     return plan_attention(B, Hq, Hkv, C, D, KVD_BF16, 0, num_splits, false, kFp8Tile).ws;
+}
+
+kvd_status kvd_attend_masked_fp8_plan(int B, int Hq, int Hkv, int C, int D, int num_splits,
+                                      int32_t* splits, size_t* lse_offset, size_t* o_offset) {
+    if (!splits || !lse_offset || !o_offset)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_fp8_plan: null pointer");
+    if (B < 1 || C < 1 || num_splits < 0)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_fp8_plan: B, C >= 1 and num_splits >= 0 required");
+    const kvd_status st = check_attention_shape(Hq, Hkv, D, KVD_BF16);
+    if (st != KVD_OK) return st;
+    const Plan pl = plan_attention(B, Hq, Hkv, C, D, KVD_BF16, 0, num_splits, false, kFp8Tile);
+    put_plan(pl, plan_small(B, Hkv, C, D, KVD_BF16, pl, num_splits, true).use, splits, lse_offset,
+             o_offset);
+    return ok();
 }
 
 kvd_status kvd_attend_masked_fp8(const void* q, const void* k_cache, const void* v_cache,
@@ -584,6 +641,20 @@ size_t kvd_attend_indexed_workspace_bytes(int B, int Hq, int Hkv, int topk, int 
     return plan_attention(B, Hq, Hkv, topk, D, dtype, 0, num_splits, true).ws;
 }
 
+kvd_status kvd_attend_indexed_plan(int B, int Hq, int Hkv, int topk, int D, kvd_dtype dtype,
+                                   int num_splits, int32_t* splits, size_t* lse_offset,
+                                   size_t* o_offset) {
+    if (!splits || !lse_offset || !o_offset)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_indexed_plan: null pointer");
+    if (B < 1 || topk < 1 || num_splits < 0)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_indexed_plan: B, topk >= 1 and num_splits >= 0 required");
+    const kvd_status st = check_attention_shape(Hq, Hkv, D, dtype);
+    if (st != KVD_OK) return st;
+    put_plan(plan_attention(B, Hq, Hkv, topk, D, dtype, 0, num_splits, true), false, splits,
+             lse_offset, o_offset);
+    return ok();
+}
+
 kvd_status kvd_attend_indexed(const void* q, const void* k_cache, const void* v_cache,
                               const int32_t* indices, void* out, float* lse_out, int B, int Hq,
                               int Hkv, int C, int topk, int D, float scale, kvd_dtype dtype,
@@ -635,6 +706,22 @@ size_t kvd_attend_paged_workspace_bytes(int Q, int Hq, int Hkv, int BS, int cols
                                         kvd_dtype dtype, int num_splits) {
     if (Q < 1 || BS < 1 || cols < 1 || check_attention_shape(Hq, Hkv, D, dtype) != KVD_OK) return 0;
     return plan_attention(Q, Hq, Hkv, (int)((long long)cols * BS), D, dtype, BS, num_splits).ws;
+}
+
+kvd_status kvd_attend_paged_plan(int Q, int Hq, int Hkv, int BS, int cols, int D, kvd_dtype dtype,
+                                 int num_splits, int32_t* splits, size_t* lse_offset,
+                                 size_t* o_offset) {
+    if (!splits || !lse_offset || !o_offset)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_paged_plan: null pointer");
+    if (Q < 1 || BS < 1 || cols < 1 || num_splits < 0)
+        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_paged_plan: Q, BS, cols >= 1 and num_splits >= 0 required");
+    if ((long long)cols * BS >= (1ll << 31))
+        return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_paged_plan: cols*BS >= 2^31");
+    const kvd_status st = check_attention_shape(Hq, Hkv, D, dtype);
+    if (st != KVD_OK) return st;
+    put_plan(plan_attention(Q, Hq, Hkv, cols * BS, D, dtype, BS, num_splits), false, splits,
+             lse_offset, o_offset);
+    return ok();
 }
 
 kvd_status kvd_attend_paged(const void* q_in, const void* key_cache, const void* value_cache,
@@ -730,6 +817,23 @@ kvd_status kvd_combine(const float* part_o, const float* part_lse, void* out, fl
         return fail(KVD_ERR_INVALID_ARG, "kvd_combine: misaligned pointer");
     const cudaError_t e = launch_combine(part_o, part_lse, out, lse_out, R, S, D, out_dtype, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "kvd_combine launch");
+    return ok();
+}
+
+kvd_status kvd_combine_gathered(const float* parts, void* out, float* lse_out, int R, int S,
+                                int D, kvd_dtype out_dtype, kvd_stream_t stream) {
+    const char* fn = "kvd_combine_gathered";
+    if (R < 0 || S < 1 || D < 4 || D % 4 || D > 1024)
+        return fail(KVD_ERR_INVALID_ARG, "%s: R >= 0, S >= 1, D %% 4 == 0 and 4 <= D <= 1024 required", fn);
+    if (!dtype_ok(out_dtype)) return fail(KVD_ERR_INVALID_ARG, "%s: unknown dtype", fn);
+    if (R == 0) return ok();
+    if (!parts || !out) return fail(KVD_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned(parts, 16) || !aligned(out, 16) || !aligned(lse_out, 4))
+        return fail(KVD_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+    const long long block = (long long)R * (D + 1);  // floats per split: R rows of D, R lse
+    const cudaError_t e = launch_combine(parts, parts + (long long)R * D, out, lse_out, R, S, D,
+                                         out_dtype, (cudaStream_t)stream, block);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
     return ok();
 }
 

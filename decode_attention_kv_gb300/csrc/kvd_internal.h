@@ -47,9 +47,12 @@ inline bool attend_uses_mma(kvd_dtype dt, int G) { return dt == KVD_BF16 && G >=
 // Sets the message kvd_last_error() returns on this thread.
 void set_last_error(const char* msg);
 
+// part_o [R, S, D] / part_lse [R, S]; or, with gathered_stride > 0, split s's
+// rows at part_o + s * gathered_stride ([R, D]) and its log-sum-exps at
+// part_lse + s * gathered_stride ([R]).
 cudaError_t launch_combine(const float* part_o, const float* part_lse, void* out,
                            float* lse_out, int R, int S, int D, kvd_dtype out_dt,
-                           cudaStream_t stream);
+                           cudaStream_t stream, long long gathered_stride = 0);
 
 cudaError_t launch_copy_prefix(const void* const* k_src, const void* const* v_src,
                                void* const* k_dst, void* const* v_dst, uint8_t* const* masks,

@@ -36,6 +36,12 @@ SIGNATURES = {
     "kvd_attend_masked_launches": ([_i, _i, _i, _i, _i, _i, _i], _i),
     "kvd_attend_masked": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz,
                            _vp, _vp], _i),
+    "kvd_attend_masked_plan": ([_i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp], _i),
+    "kvd_attend_masked_fp8_plan": ([_i, _i, _i, _i, _i, _i, _vp, _vp, _vp], _i),
+    "kvd_attend_indexed_plan": ([_i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp], _i),
+    "kvd_attend_paged_plan": ([_i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp], _i),
+    "kvd_attend_masked_partial": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i,
+                                   _vp, _sz, _vp, _vp], _i),
     "kvd_attend_masked_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i,
                                    _vp, _vp], _i),
     "kvd_append_attend_masked": ([_vp] * 7 + [_vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz,
@@ -52,6 +58,7 @@ SIGNATURES = {
                           _i, _i, _vp, _sz, _vp, _vp], _i),
     "kvd_gather_paged": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp] + [_i] * 10 + [_vp, _vp], _i),
     "kvd_combine": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
+    "kvd_combine_gathered": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
     "kvd_status_string": ([_i], ctypes.c_char_p),
     "kvd_last_error": ([], ctypes.c_char_p),
     "kvd_version": ([], _i),
@@ -350,6 +357,84 @@ def attend_masked(q, k_cache, v_cache, mask, scale=None, out=None, lse=None, num
     return out
 
 
+def _plan(name, *args):
+    S = ctypes.c_int32()
+    lo, oo = ctypes.c_size_t(), ctypes.c_size_t()
+    st = getattr(load(), name)(*args, ctypes.byref(S), ctypes.byref(lo), ctypes.byref(oo))
+    _check(name, st)
+    return S.value, lo.value, oo.value
+
+
+def attend_masked_plan(B, Hq, Hkv, C, D, dtype=torch.bfloat16, num_splits=0):
+    """kvd_attend_masked_plan: (splits, part_lse byte offset, part_o byte
+    offset) of kvd_attend_masked's workspace for these sizes; splits 0 = the
+    one-launch cluster kernel, 1 = no combine."""
+    return _plan("kvd_attend_masked_plan", B, Hq, Hkv, C, D,
+                 BF16 if dtype == torch.bfloat16 else F32, num_splits)
+
+
+def attend_masked_fp8_plan(B, Hq, Hkv, C, D, num_splits=0):
+    return _plan("kvd_attend_masked_fp8_plan", B, Hq, Hkv, C, D, num_splits)
+
+
+def attend_indexed_plan(B, Hq, Hkv, topk, D, dtype=torch.bfloat16, num_splits=0):
+    return _plan("kvd_attend_indexed_plan", B, Hq, Hkv, topk, D,
+                 BF16 if dtype == torch.bfloat16 else F32, num_splits)
+
+
+def attend_paged_plan(Q, Hq, Hkv, BS, cols, D, dtype=torch.bfloat16, num_splits=0):
+    return _plan("kvd_attend_paged_plan", Q, Hq, Hkv, BS, cols, D,
+                 BF16 if dtype == torch.bfloat16 else F32, num_splits)
+
+
+def workspace_partials(ws, plan, R, D):
+    """Views of a workspace's partial rows for a plan from one of the *_plan
+    queries: (part_o [R, S, D], part_lse [R, S]) fp32, or None without
+    partial rows (splits <= 1)."""
+    S, lo, oo = plan
+    if S <= 1:
+        return None
+    flat = ws.view(torch.uint8)
+    part_lse = flat[lo:lo + R * S * 4].view(torch.float32).view(R, S)
+    part_o = flat[oo:oo + R * S * D * 4].view(torch.float32).view(R, S, D)
+    return part_o, part_lse
+
+
+def attend_masked_partial(q, k_cache, v_cache, mask, scale=None, out=None, lse=None, num_splits=0,
+                          workspace=None, dev_status=None):
+    """kvd_attend_masked_partial: attend_masked with fp32 output rows and
+    their log-sum-exp -- the partial of one token range, merged with the
+    other ranges' by combine / combine_gathered.  Returns (out [B, Hq, D]
+    fp32, lse [B, Hq] fp32)."""
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("mask", mask)):
+        _cuda_contig(n, t)
+    B, Hq, D = q.shape
+    Bk, Hkv, C, Dk = k_cache.shape
+    if Bk != B or Dk != D or v_cache.shape != k_cache.shape or mask.shape != (B, C):
+        raise ValueError("attend_masked_partial: shape mismatch")
+    if mask.dtype != torch.uint8 or not (q.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("attend_masked_partial: uint8 mask and one dtype for q and caches")
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    for n, t in (("out", out), ("lse", lse)):
+        _cuda_contig(n, t)
+        if t.dtype != torch.float32:
+            raise TypeError(f"attend_masked_partial: {n} must be fp32")
+    L = load()
+    need = L.kvd_attend_masked_workspace_bytes(B, Hq, Hkv, C, D, dt, num_splits)
+    ws, wsb = _workspace(need, q.device, workspace)
+    st = L.kvd_attend_masked_partial(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(mask), _ptr(out),
+                                     _ptr(lse), B, Hq, Hkv, C, D, float(scale), dt, num_splits,
+                                     _ptr(ws), wsb, _ptr(dev_status), _stream(q.device))
+    _check("kvd_attend_masked_partial", st)
+    return out, lse
+
+
 def append_attend_masked(q, k_cache, v_cache, mask, k_new, v_new, pos, scale=None, out=None,
                          lse=None, num_splits=0, workspace=None, dev_status=None):
     """kvd_append_attend_masked: kvd_append then kvd_attend_masked in one call
@@ -552,4 +637,19 @@ def combine(part_o, part_lse, out=None, lse=None, out_dtype=torch.float32):
     st = load().kvd_combine(_ptr(part_o), _ptr(part_lse), _ptr(out), _ptr(lse), R, S, D,
                             _dtype_code(out), _stream(part_o.device))
     _check("kvd_combine", st)
+    return out
+
+
+def combine_gathered(parts, R, D, out=None, lse=None, out_dtype=torch.float32):
+    """kvd_combine_gathered: log-sum-exp merge of S ranges' packed partials,
+    parts fp32 [S, R * (D + 1)] (per range: R rows of D, then R lse)."""
+    _cuda_contig("parts", parts)
+    if parts.dtype != torch.float32 or parts.dim() != 2 or parts.shape[1] != R * (D + 1):
+        raise ValueError("combine_gathered: parts fp32 [S, R * (D + 1)] required")
+    S = parts.shape[0]
+    if out is None:
+        out = torch.empty((R, D), dtype=out_dtype, device=parts.device)
+    st = load().kvd_combine_gathered(_ptr(parts), _ptr(out), _ptr(lse), R, S, D, _dtype_code(out),
+                                     _stream(parts.device))
+    _check("kvd_combine_gathered", st)
     return out

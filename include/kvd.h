@@ -168,6 +168,39 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
                              kvd_stream_t stream);
 
 /*
+ * kvd_attend_masked_plan -- how kvd_attend_masked splits these sizes, for a
+ * caller that reads the workspace's partial rows or times the two launches
+ * apart.  *splits = S of the split kernel: 1 when its units write the output
+ * rows directly (one launch), > 1 when a combine launch follows (the partial
+ * rows are then in the workspace: part_lse float [B*Hq, S] at *lse_offset
+ * bytes and part_o float [B*Hq, S, D] at *o_offset, the kvd_combine
+ * layout), 0 when the one-launch cluster kernel runs (no partial rows; the
+ * offsets are then 0).  Arguments as for kvd_attend_masked; errors as for it.
+ */
+kvd_status kvd_attend_masked_plan(int B, int Hq, int Hkv, int C, int D, kvd_dtype dtype,
+                                  int num_splits, int32_t* splits, size_t* lse_offset,
+                                  size_t* o_offset);
+
+/*
+ * kvd_attend_masked_partial -- the same attention as kvd_attend_masked, but
+ * the output rows stay in fp32 whatever `dtype` is: out [B, Hq, D] float,
+ * lse_out [B, Hq] float (required).  This is the partial result of one range
+ * of a sequence's tokens ([NPU] Part 3, Flash SDPA path: each tile's output
+ * is normalised over its own keys and carried with its max and sum), which
+ * kvd_combine or kvd_combine_gathered merges exactly with the other
+ * ranges' partials -- e.g. when the sequence axis of one long sequence is
+ * spread over several GPUs, each holding a slice [B, Hkv, C_r, D] of the
+ * cache and the matching slice [B, C_r] of the mask.  A range with no valid
+ * slot gives out = 0 and lse = -inf (weight 0 in the merge).  Workspace,
+ * splits and errors as for kvd_attend_masked.
+ */
+kvd_status kvd_attend_masked_partial(const void* q, const void* k_cache, const void* v_cache,
+                                     const uint8_t* mask, float* out, float* lse_out, int B,
+                                     int Hq, int Hkv, int C, int D, float scale, kvd_dtype dtype,
+                                     int num_splits, void* workspace, size_t workspace_bytes,
+                                     int32_t* dev_status, kvd_stream_t stream);
+
+/*
  * kvd_attend_paged -- decode attention over the paged cache: for sequence q
  * the keys/values are the rows kvd_gather_paged would produce for q
  * ([PyPTO] 3.2), all valid, and q_in[q, h] attends over them with kv head
@@ -229,6 +262,11 @@ kvd_status kvd_append_attend_masked(const void* q, void* k_cache, void* v_cache,
  */
 size_t kvd_attend_indexed_workspace_bytes(int B, int Hq, int Hkv, int topk, int D,
                                           kvd_dtype dtype, int num_splits);
+/* As kvd_attend_masked_plan, for kvd_attend_indexed (the one-launch cluster
+ * kernel is never used: *splits >= 1). */
+kvd_status kvd_attend_indexed_plan(int B, int Hq, int Hkv, int topk, int D, kvd_dtype dtype,
+                                   int num_splits, int32_t* splits, size_t* lse_offset,
+                                   size_t* o_offset);
 kvd_status kvd_attend_indexed(const void* q, const void* k_cache, const void* v_cache,
                               const int32_t* indices, void* out, float* lse_out, int B, int Hq,
                               int Hkv, int C, int topk, int D, float scale, kvd_dtype dtype,
@@ -278,6 +316,9 @@ kvd_status kvd_append_fp8(void* k_cache, void* v_cache, const void* k_new, const
  * path.
  */
 size_t kvd_attend_masked_fp8_workspace_bytes(int B, int Hq, int Hkv, int C, int D, int num_splits);
+/* As kvd_attend_masked_plan, for kvd_attend_masked_fp8. */
+kvd_status kvd_attend_masked_fp8_plan(int B, int Hq, int Hkv, int C, int D, int num_splits,
+                                      int32_t* splits, size_t* lse_offset, size_t* o_offset);
 kvd_status kvd_attend_masked_fp8(const void* q, const void* k_cache, const void* v_cache,
                                  const uint8_t* mask, void* out, float* lse_out, int B, int Hq,
                                  int Hkv, int C, int D, float scale, int num_splits,
@@ -301,14 +342,16 @@ kvd_status kvd_attend_masked_fp8(const void* q, const void* k_cache, const void*
  *    same arguments) exceeds KVD_NOALLOC_SCRATCH_BYTES are rejected with
  *    KVD_ERR_WORKSPACE and a message in kvd_last_error(); pass fewer splits
  *    (num_splits) or use kvd_attend_masked.
- *  - The first call on a device looks up the array's device address on the
- *    current device (cudaGetSymbolAddress) and caches it; make that first
- *    call before any stream capture on that device.
+ *  - The first call in a device's context looks up the array's device
+ *    address there (cudaGetSymbolAddress) and caches it per context; make
+ *    that first call before any stream capture on that device (and again
+ *    after a cudaDeviceReset, which loads the library's module anew).
  *  - All calls on a device share the one array, which keeps the last call's
- *    contents.  Its work counters start at zero (the array is zero when the
- *    library is loaded) and every call leaves them at zero again.  Calls that
- *    may overlap on the GPU (other streams, unordered host threads) race on
- *    it: the caller must order them.
+ *    contents.  Each call first clears the array's 256 bytes of work counters
+ *    with cudaMemsetAsync on `stream` (stream-ordered; no allocation), so a
+ *    call whose launch gave up on a bounded wait (KVD_DEV_TIMEOUT) does not
+ *    poison the next one.  Calls that may overlap on the GPU (other streams,
+ *    unordered host threads) race on the array: the caller must order them.
  */
 #define KVD_NOALLOC_SCRATCH_BYTES (8u << 20)
 kvd_status kvd_attend_masked_noalloc(const void* q, const void* k_cache, const void* v_cache,
@@ -318,6 +361,11 @@ kvd_status kvd_attend_masked_noalloc(const void* q, const void* k_cache, const v
 
 size_t kvd_attend_paged_workspace_bytes(int Q, int Hq, int Hkv, int BS, int cols, int D,
                                         kvd_dtype dtype, int num_splits);
+/* As kvd_attend_masked_plan, for kvd_attend_paged (rows = sequences; the
+ * one-launch cluster kernel is never used: *splits >= 1). */
+kvd_status kvd_attend_paged_plan(int Q, int Hq, int Hkv, int BS, int cols, int D, kvd_dtype dtype,
+                                 int num_splits, int32_t* splits, size_t* lse_offset,
+                                 size_t* o_offset);
 kvd_status kvd_attend_paged(const void* q_in, const void* key_cache, const void* value_cache,
                             const int32_t* block_tables, const int32_t* seq_lens,
                             const int32_t* seq_offset, void* out, float* lse_out, int Q, int Hq,
@@ -357,6 +405,19 @@ kvd_status kvd_gather_paged(const void* key_cache, const void* value_cache,
  */
 kvd_status kvd_combine(const float* part_o, const float* part_lse, void* out, float* lse_out,
                        int R, int S, int D, kvd_dtype out_dtype, kvd_stream_t stream);
+
+/*
+ * kvd_combine_gathered -- kvd_combine over the exchange layout of a
+ * sequence split across S ranks: `parts` float [S, R * (D + 1)] holds, for
+ * range s, its R partial rows [R, D] followed by their R log-sum-exps
+ * (kvd_attend_masked_partial writing out and lse_out into the two parts of
+ * one rank's block), the blocks one after the other as an all-gather of the
+ * blocks along the first axis leaves them.  Same formula, outputs and rules
+ * as kvd_combine (range s of row r has part_o = parts[s, r*D : (r+1)*D] and
+ * part_lse = parts[s, R*D + r]).
+ */
+kvd_status kvd_combine_gathered(const float* parts, void* out, float* lse_out, int R, int S,
+                                int D, kvd_dtype out_dtype, kvd_stream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char* kvd_status_string(kvd_status status);

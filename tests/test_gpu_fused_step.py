@@ -27,18 +27,29 @@ def _bits(t):
 
 
 CASES = [
-    # dtype, B, Hq, Hkv, C, D, first positions
-    (torch.bfloat16, 1, 32, 32, 1152, 128, [1024]),        # the static-buffer default, one CTA per unit
-    (torch.bfloat16, 2, 32, 8, 1152, 128, [5, 640]),       # tensor-core consumers, small launch
-    (torch.bfloat16, 3, 32, 8, 8192, 128, [8191, 4096, 63]),  # many units per CTA
-    (torch.bfloat16, 2, 8, 4, 700, 64, [0, 31]),           # two heads per kv head, first tiles
-    (torch.float32, 2, 4, 4, 300, 128, [64, 299]),
-    (torch.bfloat16, 2, 48, 3, 520, 64, [100, 519]),       # two head groups: append kernel first
+    # dtype, B, Hq, Hkv, C, D, first positions, num_splits
+    (torch.bfloat16, 1, 32, 32, 1152, 128, [1024], 0),        # the static-buffer default, one CTA per unit
+    (torch.bfloat16, 2, 32, 8, 1152, 128, [5, 640], 0),       # tensor-core consumers, small launch
+    (torch.bfloat16, 3, 32, 8, 8192, 128, [8191, 4096, 63], 0),  # many units per CTA
+    (torch.bfloat16, 2, 8, 4, 700, 64, [0, 31], 0),           # two heads per kv head, first tiles
+    (torch.float32, 2, 4, 4, 300, 128, [64, 299], 0),
+    (torch.bfloat16, 2, 48, 3, 520, 64, [100, 519], 0),       # two head groups: append kernel first
+    # The persistent split kernel with CUDA-core consumers and the append in
+    # its scheduler warps (launches too large for the one-CTA-per-split path):
+    # one query head per kv head, splits of 256 slots (a tail of 64-slot
+    # splits from 6144 on); positions cross a split edge (254 -> 256) and
+    # fill the last split (8189 -> 8191).
+    (torch.bfloat16, 2, 32, 32, 8192, 128, [254, 8189], 0),
+    (torch.bfloat16, 2, 16, 8, 4096, 128, [1023, 4093], 0),   # two query heads per kv head
+    (torch.float32, 2, 4, 4, 4096, 128, [511, 4094], 0),      # fp32 rows
+    (torch.bfloat16, 1, 8, 8, 2048, 64, [700], 5),            # an explicit split count, D 64
+    (torch.bfloat16, 2, 32, 8, 4096, 128, [2047, 3000], 7),   # explicit splits, tensor cores
+    (torch.float32, 1, 4, 2, 1000, 64, [333], 1),             # one split: rows written directly
 ]
 
 
-@pytest.mark.parametrize("dtype,B,Hq,Hkv,C,D,pos0", CASES)
-def test_fused_step_parity(kvd, dtype, B, Hq, Hkv, C, D, pos0):
+@pytest.mark.parametrize("dtype,B,Hq,Hkv,C,D,pos0,num_splits", CASES)
+def test_fused_step_parity(kvd, dtype, B, Hq, Hkv, C, D, pos0, num_splits):
     g = W.generator(1100 + C + Hq)
     k = W.randn(g, (B, Hkv, C, D), dtype)
     v = W.randn(g, (B, Hkv, C, D), dtype)
@@ -54,7 +65,8 @@ def test_fused_step_parity(kvd, dtype, B, Hq, Hkv, C, D, pos0):
         pos = torch.tensor([min(p + step, C - 1) for p in pos0], dtype=torch.int32)
         lse = torch.empty(B, Hq, device="cuda")
         out = kvd.append_attend_masked(q.cuda(), kd, vd, md, kn.cuda(), vn.cuda(), pos.cuda(),
-                                       scale, lse=lse, dev_status=status)
+                                       scale, lse=lse, num_splits=num_splits,
+                                       dev_status=status)
         assert oracle.append(kh, vh, kn, vn, pos, mh) == 0
         torch.cuda.synchronize()
         assert int(status.item()) == 0

@@ -96,8 +96,7 @@ def test_indexed_bad_entries_and_empty_lists(kvd):
 def test_indexed_full_size(kvd):
     """The benchmark's configuration: the batched-GQA caches (16 x 32/8 heads,
     capacity 8192, lengths 512..8192) with 2048 listed slots per entry (fewer
-    for a shorter prefix, -1 after them); entries sampled across the length
-    range, all their heads compared."""
+    for a shorter prefix, -1 after them); every entry and head compared."""
     lay = W.gqa(device="cuda", layers=1).layers[0]
     L = [int(x) for x in lay.lengths]
     idx = W.index_lists(L, 2048)
@@ -107,11 +106,8 @@ def test_indexed_full_size(kvd):
                              dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    order = sorted(range(16), key=lambda b: L[b])
-    for b in (order[0], order[7], order[-1]):
-        ref, ref_lse, err = oracle.attend_indexed(lay.q[b:b + 1].cpu(), lay.k_cache[b:b + 1].cpu(),
-                                                  lay.v_cache[b:b + 1].cpu(), idx[b:b + 1],
-                                                  lay.scale)
-        assert err == 0
-        assert_attention_close(out[b:b + 1], ref, torch.bfloat16, f"indexed entry {b} (L={L[b]})")
-        assert_lse_close(lse[b:b + 1], ref_lse)
+    ref, ref_lse, err = oracle.attend_indexed(lay.q.cpu(), lay.k_cache.cpu(), lay.v_cache.cpu(),
+                                              idx, lay.scale)
+    assert err == 0
+    assert_attention_close(out, ref, torch.bfloat16, "indexed, all entries")
+    assert_lse_close(lse, ref_lse, "indexed lse")

@@ -49,22 +49,3 @@ def test_window_parity(kvd, dtype, B, Hq, Hkv, C, D, lengths, window, num_splits
     ref, ref_lse = oracle.attend_masked(q, k, v, mask, scale)
     assert_attention_close(out, ref, dtype, f"window {window}")
     assert_lse_close(lse, ref_lse, f"window {window} lse")
-
-
-def test_window_full_size(kvd):
-    """The 32768-slot sequence with its 4096-slot window, as the benchmark
-    runs it (append at C - 1, library-planned splits): all 32 heads."""
-    lay = W.window(device="cuda", layers=1).layers[0]
-    status = kvd.status_tensor("cuda")
-    kvd.append(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, lay.pos, lay.mask, status)
-    lse = torch.empty(1, 32, device="cuda")
-    out = kvd.attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale, lse=lse,
-                            dev_status=status)
-    torch.cuda.synchronize()
-    assert int(status.item()) == 0
-    mask = lay.mask.cpu()
-    assert int(mask.sum()) == 4096 and int(mask[0, -1]) == 1 and int(mask[0, -4096]) == 1
-    ref, ref_lse = oracle.attend_masked(lay.q.cpu(), lay.k_cache.cpu(), lay.v_cache.cpu(), mask,
-                                        lay.scale)
-    assert_attention_close(out, ref, torch.bfloat16, "window full size")
-    assert_lse_close(lse, ref_lse, "window full size lse")

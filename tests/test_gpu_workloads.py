@@ -1,11 +1,14 @@
-"""Parity at the workloads' full sizes, in the launch configuration the
-benchmark times (library-planned splits), on outputs sampled so that the
-fp64 oracle computes them one by one in seconds.
+"""Parity at the workloads' full sizes, in the launch configurations the
+benchmark times (library-planned splits), every output element compared.
 
 Workloads (see workloads.py): the 1152-slot static buffer (MHA 32 x 128,
 bf16), batched GQA (16 x 32/8 heads, capacity 8192, lengths 512..8192), the
 paged cache (8192 blocks of 128 slots x 8 heads x 128, 64 sequences of
-1..4096 tokens) and the 32768-token single sequence.
+1..4096 tokens), the 32768-token single sequence and its 4096-slot sliding
+window.  The static-buffer steps run both ways a caller can run them: the
+append and the attention as two calls, and the fused call the benchmark
+times (the append inside the attention launch).  The fp64 oracle computes
+the whole layer (every batch entry, every head) on the host cores.
 """
 import numpy as np
 import pytest
@@ -29,42 +32,39 @@ def _bits(t):
     return host(t).view(torch.int16).numpy()
 
 
-def _masked_step_and_check(kvd, lay, sample, what):
-    """Append + attend one layer on the GPU; check the append byte for byte
-    over the whole cache and the attention on the sampled (b, h) rows."""
+def _masked_step_and_check(kvd, lay, what, fused):
+    """Append + attend one layer on the GPU (two calls, or the fused call);
+    the append compared byte for byte over the whole cache and mask, the
+    attention over every (batch entry, head) against the oracle's append
+    followed by its attention."""
     dev = "cuda"
     B, Hkv, C, D = lay.k_cache.shape
     Hq = lay.q.shape[1]
-    g = Hq // Hkv
     kh, vh, mh = _bits(lay.k_cache).copy(), _bits(lay.v_cache).copy(), host(lay.mask).numpy().copy()
     status = kvd.status_tensor(dev)
-    kvd.append(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, lay.pos, lay.mask, status)
     lse = torch.empty(B, Hq, device=dev)
-    out = kvd.attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale, lse=lse,
-                            dev_status=status)
+    if fused:
+        out = kvd.append_attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.k_new,
+                                       lay.v_new, lay.pos, lay.scale, lse=lse, dev_status=status)
+    else:
+        kvd.append(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, lay.pos, lay.mask, status)
+        out = kvd.attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale, lse=lse,
+                                dev_status=status)
     assert oracle.append(kh, vh, host(lay.k_new), host(lay.v_new), host(lay.pos), mh) == 0
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert np.array_equal(_bits(lay.k_cache), kh), f"{what}: append (K) not bit-exact"
     assert np.array_equal(_bits(lay.v_cache), vh), f"{what}: append (V) not bit-exact"
-    assert np.array_equal(host(lay.mask).numpy(), mh)
-    qh = host(lay.q)
-    outs, refs, lses, rlses = [], [], [], []
-    for b, h in sample:
-        kvh = h // g
-        ref, rl = oracle.attend_masked(
-            qh[b:b + 1, h:h + 1], torch.from_numpy(kh[b:b + 1, kvh:kvh + 1]).view(torch.bfloat16),
-            torch.from_numpy(vh[b:b + 1, kvh:kvh + 1]).view(torch.bfloat16),
-            torch.from_numpy(mh[b:b + 1]), lay.scale, nthreads=0)
-        outs.append(out[b, h])
-        refs.append(ref[0, 0])
-        lses.append(lse[b, h])
-        rlses.append(rl[0, 0])
-    assert_attention_close(torch.stack(outs), np.stack(refs), torch.bfloat16, what)
-    assert_lse_close(torch.stack(lses), np.array(rlses), what)
+    assert np.array_equal(host(lay.mask).numpy(), mh), f"{what}: mask after the append"
+    ref, rl = oracle.attend_masked(host(lay.q), torch.from_numpy(kh).view(torch.bfloat16),
+                                   torch.from_numpy(vh).view(torch.bfloat16),
+                                   torch.from_numpy(mh), lay.scale)
+    assert_attention_close(out, ref, torch.bfloat16, what)
+    assert_lse_close(lse, rl, what)
 
 
-def test_npuw_default_buffer_steps(kvd):
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+def test_npuw_default_buffer_steps(kvd, fused):
     """1152-slot buffer: four decode steps (appends at 1024..1027), all 32
     heads compared after each."""
     w = W.npuw(device="cuda", layers=1)
@@ -76,27 +76,39 @@ def test_npuw_default_buffer_steps(kvd):
             lay.k_new = W.randn(g, lay.k_new.shape, torch.bfloat16, "cuda")
             lay.v_new = W.randn(g, lay.v_new.shape, torch.bfloat16, "cuda")
             lay.pos = lay.pos + 1
-        _masked_step_and_check(kvd, lay, [(0, h) for h in range(32)], f"npuw step {step}")
+        _masked_step_and_check(kvd, lay, f"npuw step {step}", fused)
         assert int(host(lay.mask).sum()) == 1025 + step
 
 
-def test_batched_gqa_full_size(kvd):
-    w = W.gqa(device="cuda", layers=1)
-    lay = w.layers[0]
-    L = lay.lengths
-    order = torch.argsort(L)
-    bs = [int(order[0]), int(order[1]), int(order[len(order) // 2]), int(order[-1])]
-    sample = [(b, h) for b in bs for h in (0, 3, 4, 17, 31)]
-    _masked_step_and_check(kvd, lay, sample, "gqa")
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+def test_batched_gqa_full_size(kvd, fused):
+    """All 16 batch entries x 32 query heads (512 rows)."""
+    lay = W.gqa(device="cuda", layers=1).layers[0]
+    _masked_step_and_check(kvd, lay, "gqa", fused)
 
 
-def test_long_context_full_size(kvd):
-    w = W.long(device="cuda", layers=1)
-    lay = w.layers[0]
-    _masked_step_and_check(kvd, lay, [(0, h) for h in (0, 5, 13, 31)], "long")
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+def test_long_context_full_size(kvd, fused):
+    """All 32 heads of the 32768-slot sequence.  The fused call runs the
+    append inside the persistent split kernel with CUDA-core consumers (one
+    query head per kv head), in the launch the benchmark times."""
+    lay = W.long(device="cuda", layers=1).layers[0]
+    _masked_step_and_check(kvd, lay, "long", fused)
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+def test_window_full_size(kvd, fused):
+    """The 32768-slot sequence with its 4096-slot window, appended at C - 1:
+    all 32 heads; the window is the mask after the append."""
+    lay = W.window(device="cuda", layers=1).layers[0]
+    _masked_step_and_check(kvd, lay, "window", fused)
+    mask = host(lay.mask)
+    assert int(mask.sum()) == 4096 and int(mask[0, -1]) == 1 and int(mask[0, -4096]) == 1
 
 
 def test_paged_full_size(kvd):
+    """All 64 sequences x 32 query heads of paged attention; the whole
+    gathered K and V buffers byte for byte."""
     pw = W.paged(device="cuda")
     status = kvd.status_tensor()
     lse = torch.empty(pw.q.shape[:2], device="cuda")
@@ -107,28 +119,16 @@ def test_paged_full_size(kvd):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert ko.shape == (pw.total_tokens, 8, 128)
-    L = pw.lengths
-    order = torch.argsort(L)
-    sample = [int(order[0]), int(order[1]), int(order[32]), int(order[-2]), int(order[-1])]
-    bt = host(pw.block_tables)
-    sl = host(pw.seq_lens)
-    for q in sample:
-        n = int(L[q])
-        nblk = (n + 127) // 128
-        idx = bt[q, :nblk].long()
-        kq = host(pw.key_cache.index_select(0, idx.cuda()))
-        vq = host(pw.value_cache.index_select(0, idx.cuda()))
-        bt_q = torch.arange(nblk, dtype=torch.int32)[None]
-        sl_q = torch.tensor([0, n], dtype=torch.int32)
-        ref, rl = oracle.attend_paged(host(pw.q[q:q + 1]), kq, vq, bt_q, sl_q, None, pw.scale)
-        assert_attention_close(out[q:q + 1], ref, torch.bfloat16, f"paged seq {q} (len {n})")
-        assert_lse_close(lse[q:q + 1], rl)
-        rk, rv, err = oracle.gather_paged(kq.view(torch.int16).numpy(), vq.view(torch.int16).numpy(),
-                                          bt_q, sl_q)
-        assert err == 0
-        s0 = int(sl[q])
-        assert np.array_equal(_bits(ko[s0:s0 + n]), rk), f"gather seq {q}"
-        assert np.array_equal(_bits(vo[s0:s0 + n]), rv), f"gather seq {q}"
+    kc, vc = host(pw.key_cache), host(pw.value_cache)
+    bt, sl, so = host(pw.block_tables), host(pw.seq_lens), host(pw.seq_offset)
+    ref, rl = oracle.attend_paged(host(pw.q), kc, vc, bt, sl, so, pw.scale)
+    assert_attention_close(out, ref, torch.bfloat16, "paged attention, all sequences")
+    assert_lse_close(lse, rl, "paged attention lse")
+    rk, rv, err = oracle.gather_paged(kc.view(torch.int16).numpy(), vc.view(torch.int16).numpy(),
+                                      bt, sl, so)
+    assert err == 0
+    assert np.array_equal(_bits(ko), rk), "gather: key buffer not bit-exact"
+    assert np.array_equal(_bits(vo), rv), "gather: value buffer not bit-exact"
 
 
 @pytest.mark.parametrize("name", ["gqa", "long"])

@@ -64,15 +64,34 @@ def test_reference_arm_prints_on_rank_zero_only(capsys, monkeypatch):
     import bench
 
     class Args:
-        steps, warmup, gpus, workload = 1, 0, 2, "tiny-not-used"
+        steps, warmup, gpus, workload = 1, 0, 2, "gqa"
 
     # rank 1 returns without work and prints nothing
     assert bench.reference_arm(Args(), 1, 2) == 0
     assert capsys.readouterr().out == ""
-    # rank 0 prints one JSON line (the oracle rate is stubbed: no timing here)
-    monkeypatch.setattr(bench, "oracle_rate", lambda name, seconds: (1.5, 4, "stub sample"))
+    # rank 0 prints one JSON line (the oracle rate and the config are stubbed:
+    # no timing here)
+    monkeypatch.setattr(bench, "oracle_rate", lambda name, seconds: {
+        "value": 1.5, "unit": "GB/s", "cores": 4, "kind": "oracle", "sample": "stub sample",
+        "per_layer_ms": 2.0})
+    monkeypatch.setattr(bench, "workload_config", lambda name: {"workload": name, "batch": 16})
     assert bench.reference_arm(Args(), 0, 2) == 0
     line = json.loads(capsys.readouterr().out.strip())
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] == 1.5
-    assert line["cpu_baseline"]["cores"] == 4
+    assert line["cpu_baseline"]["cores"] == 4 and line["cpu_baseline"]["per_layer_ms"] == 2.0
+    assert line["config"] == {"workload": "gqa", "batch": 16}
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_config_matches_the_gpu_arm_config():
+    """Both arms print the same config block for a workload (built from host
+    copies of the inputs here; from the device inputs in the GPU arm)."""
+    import bench
+    import workloads
+    c = bench.workload_config("npuw")
+    w = workloads.npuw(device="cpu", layers=1)
+    assert c == bench.masked_config("npuw", w, 32, [int(x) for x in w.layers[0].lengths])
+    assert c["layers"] == 32 and c["capacity"] == 1152 and c["q_heads"] == 32
+    g = bench.workload_config("gqa")
+    assert g["batch"] == 16 and g["kv_heads"] == 8 and g["layers"] == 32
+    assert g["valid_len_step0"]["min"] >= 512 and g["valid_len_step0"]["max"] <= 8192

@@ -7,8 +7,9 @@ It is called here through the C ABI and must give the same output as
 kvd_attend_masked with a caller workspace, within the bf16 attention
 tolerance (max |diff| <= 1e-2, relative L2 <= 5e-3), on two calls in a row
 whose shapes differ, so that whatever the first call left in the shared
-built-in scratch cannot leak into the second.  Sizes whose scratch exceeds the
-built-in array are refused.  This file is collected last on purpose.
+built-in scratch cannot leak into the second; the same calls are also held
+against the fp64 oracle.  Sizes whose scratch exceeds the built-in array are
+refused.  This file is collected last on purpose.
 """
 import ctypes
 import math
@@ -17,8 +18,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
-from parity_util import assert_attention_close
+from parity_util import assert_attention_close, assert_lse_close
 
 pytestmark = pytest.mark.gpu
 
@@ -71,6 +73,9 @@ def test_noalloc_matches_the_workspace_entry_point_twice(kvd):
         r, o = ref_lse.cpu().numpy(), lse.cpu().numpy()
         assert np.array_equal(np.isneginf(r), np.isneginf(o))
         assert np.allclose(o[np.isfinite(r)], r[np.isfinite(r)], rtol=0, atol=1e-4)
+        oref, olse = oracle.attend_masked(q.cpu(), k.cpu(), v.cpu(), mask.cpu(), 1.0 / math.sqrt(D))
+        assert_attention_close(out, oref, torch.bfloat16, f"call {n} against the oracle")
+        assert_lse_close(lse, olse, f"call {n} lse against the oracle")
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch(kvd):
