@@ -4,8 +4,12 @@ Tolerances (stated for decode attention outputs):
   bf16 inputs/outputs: max |gpu - oracle| <= 1e-2 and ||gpu - oracle|| / ||oracle|| <= 5e-3
   fp32 inputs/outputs: max |gpu - oracle| <= 1e-5 and relative L2 <= 1e-6
 The bf16 output grid is coarser than 1e-2 above |x| = 4 (half an ulp there
-is 2^-6), so for elements with |oracle| >= 4 the element bound is half a bf16
-ulp of the oracle value plus 1e-3; the relative-L2 bound is unchanged.
+is 2^-6), so there the element bar is faithful rounding: the output must be
+one of the two bf16 values adjacent to the exact result, |gpu - oracle| <
+ulp(oracle).  That is the accuracy the method's own arithmetic guarantees:
+the weights p are rounded to bf16 before P.V ("FlashMLA на Huawei Ascend",
+online softmax), up to 2^-9 relative, i.e. up to half an output ulp before
+the output's own rounding.  The relative-L2 bound is unchanged.
 Append and gather are byte copies and compare byte for byte.
 """
 import numpy as np
@@ -14,10 +18,29 @@ import torch
 TOL = {torch.bfloat16: (1e-2, 5e-3), torch.float32: (1e-5, 1e-6)}
 
 
-def bf16_half_ulp(x):
+def bf16_ulp(x):
+    """Spacing of the bf16 values around x (8 significant bits)."""
     a = np.maximum(np.abs(x), 2.0 ** -126)
     e = np.floor(np.log2(a))
-    return 2.0 ** (e - 8)
+    return 2.0 ** (e - 7)
+
+
+def element_bound(ref, dtype):
+    """Per-element bound on |gpu - oracle| (see the module docstring) and the
+    mask of elements whose bound is strict (faithful rounding: err < ulp)."""
+    max_abs, _ = TOL[dtype]
+    bound = np.full_like(ref, max_abs)
+    strict = np.zeros(ref.shape, bool)
+    if dtype == torch.bfloat16:
+        strict = np.abs(ref) >= 4.0
+        bound[strict] = bf16_ulp(ref[strict])
+    return bound, strict
+
+
+def violations(err, ref, dtype):
+    """Elements whose error breaks the element bound."""
+    bound, strict = element_bound(ref, dtype)
+    return (err > bound) | (strict & (err >= bound)), bound
 
 
 def assert_attention_close(gpu, ref, dtype, what=""):
@@ -26,15 +49,13 @@ def assert_attention_close(gpu, ref, dtype, what=""):
     ref = np.asarray(ref, dtype=np.float64)
     assert g.shape == ref.shape, (g.shape, ref.shape)
     assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
-    max_abs, rel_l2 = TOL[dtype]
+    _, rel_l2 = TOL[dtype]
     err = np.abs(g - ref)
-    bound = np.full_like(ref, max_abs)
-    if dtype == torch.bfloat16:
-        big = np.abs(ref) >= 4.0
-        bound[big] = bf16_half_ulp(ref[big]) + 1e-3
-    worst = np.max(err - bound) if err.size else -1
-    assert worst <= 0, (f"{what}: max abs err {err.max():.3e} exceeds the bound "
-                        f"(tol {max_abs}) at {np.unravel_index(np.argmax(err - bound), err.shape)}")
+    bad, bound = violations(err, ref, dtype)
+    if bad.any():
+        i = np.unravel_index(np.argmax(np.where(bad, err - bound, -np.inf)), err.shape)
+        raise AssertionError(f"{what}: error {err[i]:.3e} exceeds the bound {bound[i]:.3e} at {i} "
+                             f"(oracle {ref[i]:.6g}, gpu {g[i]:.6g}; max abs err {err.max():.3e})")
     nref = np.linalg.norm(ref)
     if nref > 0:
         rel = np.linalg.norm(g - ref) / nref

@@ -94,7 +94,7 @@ SPLIT_CASES = [
 
 @pytest.mark.parametrize("dtype,B,Hq,Hkv,C,D,lengths,ranks", SPLIT_CASES)
 def test_ranges_merged_equal_the_unsplit_attention(kvd, dtype, B, Hq, Hkv, C, D, lengths, ranks):
-    g = W.generator(5300 + C + ranks)
+    g = W.generator(5300 + C + ranks, "cuda")
     q = W.randn(g, (B, Hq, D), dtype, "cuda")
     k = W.randn(g, (B, Hkv, C, D), dtype, "cuda")
     v = W.randn(g, (B, Hkv, C, D), dtype, "cuda")
@@ -121,7 +121,7 @@ def test_one_rank_module_equals_the_plain_call(kvd):
     """SequenceSplitAttention without a process group (one rank) is the
     plain attention: the exchange hands back the rank's own block."""
     B, Hq, Hkv, C, D = 2, 16, 4, 2048, 128
-    g = W.generator(5400)
+    g = W.generator(5400, "cuda")
     q = W.randn(g, (B, Hq, D), torch.bfloat16, "cuda")
     k = W.randn(g, (B, Hkv, C, D), torch.bfloat16, "cuda")
     v = W.randn(g, (B, Hkv, C, D), torch.bfloat16, "cuda")
