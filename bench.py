@@ -264,13 +264,16 @@ def workload_config(name):
 FP8_ROW_PAD = 16  # quantised rows: D codes, fp32 scale, 12 zero bytes
 
 
-def attention_kernel_name(kind, plan_splits, g, dtype="bf16", mode="masked", fused=False):
+def attention_kernel_name(kind, plan, g, mode="masked", fused=False):
     """The kernel that runs a workload's attention, as the launch list names it."""
-    if plan_splits == 0:
+    if plan.splits == 0:
         return f"attend_small_kernel ({kind} consumers; one CTA per split, cluster merge)"
     tail = ", fused append" if fused else ""
-    comb = ", then combine_kernel" if plan_splits > 1 else ", rows written directly"
-    return f"attend_kernel ({kind} consumers, {mode} mode, g={g}{tail}){comb}"
+    if plan.splits == 1:
+        comb = ", rows written directly"
+    else:
+        comb = f", {plan.splits} splits, then combine_kernel"
+    return f"attend_kernel ({kind} consumers, {mode} mode, g={g}{tail}{comb})"
 
 
 class MaskedBench:
@@ -311,7 +314,6 @@ class MaskedBench:
         self.gpos = self.pos_table[0].clone()
         need = kvd.attend_masked_workspace_bytes(self.B, self.Hq, self.Hkv, self.C, self.D)
         self.ws = kvd.workspace(need, dev)
-        self.splits = need > 256  # more than the scheduling counters: the combine runs
         self.out = [torch.empty_like(l.q) for l in w.layers]
         self.status = kvd.status_tensor(dev)
         self.lengths0 = [int(x) for x in lay0.lengths]
@@ -468,15 +470,15 @@ class MaskedBench:
     def kernel_name(self):
         g = self.Hq // self.Hkv
         kind = "tensor-core" if g >= 4 else "CUDA-core"
-        return attention_kernel_name(kind, self.attention_plan()[0], g, fused=True)
+        return attention_kernel_name(kind, self.attention_plan(), g, fused=True)
 
     def aux_ops(self):
         """The step's launches other than the attention kernel, per layer:
         the combine, when the plan splits rows (the append runs inside the
         attention launch)."""
-        part = self.kvd.workspace_partials(self.ws, self.attention_plan(), self.B * self.Hq,
-                                           self.D)
-        if part is None:
+        plan = self.attention_plan()
+        part = self.kvd.workspace_partials(self.ws, plan, self.B * self.Hq, self.D)
+        if part is None or plan.launches < 2:
             return {}
         po, pl = part
         return {"combine": lambda li: self.kvd.combine(po, pl, out=self.out[li].view(-1, self.D))}
@@ -505,7 +507,6 @@ class PagedBench:
         cols = pw.block_tables.shape[1]
         need = kvd.attend_paged_workspace_bytes(self.Q, self.Hq, self.Hkv, self.BS, cols, self.D)
         self.ws = kvd.workspace(need, dev)
-        self.splits = need > 256  # more than the scheduling counters: the combine runs
         self.status = kvd.status_tensor(dev)
         self.graph = None
 
@@ -551,7 +552,7 @@ class PagedBench:
         self.graph.replay()
 
     def launches_per_step(self):
-        return 2 + (1 if self.splits else 0)
+        return 1 + self.attention_plan().launches  # gather, attention (+ combine)
 
     def attend_bytes(self, j):
         return paged_attend_bytes(self.lengths, self.Hq, self.Hkv, self.D, self.elem, self.BS)
@@ -586,15 +587,15 @@ class PagedBench:
         return self.kvd.attend_paged_plan(self.Q, self.Hq, self.Hkv, self.BS, cols, self.D)
 
     def kernel_name(self):
-        return attention_kernel_name("tensor-core", self.attention_plan()[0], self.Hq // self.Hkv,
+        return attention_kernel_name("tensor-core", self.attention_plan(), self.Hq // self.Hkv,
                                      mode="paged")
 
     def aux_ops(self):
         """The gather, and the combine behind the paged attention."""
         ops = {"gather": lambda li: self._gather()}
-        part = self.kvd.workspace_partials(self.ws, self.attention_plan(), self.Q * self.Hq,
-                                           self.D)
-        if part is not None:
+        plan = self.attention_plan()
+        part = self.kvd.workspace_partials(self.ws, plan, self.Q * self.Hq, self.D)
+        if part is not None and plan.launches > 1:
             po, pl = part
             ops["combine"] = lambda li: self.kvd.combine(po, pl, out=self.out.view(-1, self.D))
         return ops
@@ -644,7 +645,7 @@ class IndexedBench(MaskedBench):
         return evs
 
     def launches_per_step(self):
-        return self.layers * (2 + (1 if self.splits else 0))  # append, attention, combine
+        return self.layers * (1 + self.attention_plan().launches)  # append, attention (+ combine)
 
     def flops_per_step(self):
         return self.layers * attention_flops(self.listed, self.Hq, self.D)
@@ -659,7 +660,7 @@ class IndexedBench(MaskedBench):
         return self.kvd.attend_indexed_plan(self.B, self.Hq, self.Hkv, self.TOPK, self.D)
 
     def kernel_name(self):
-        return attention_kernel_name("tensor-core", self.attention_plan()[0], self.Hq // self.Hkv,
+        return attention_kernel_name("tensor-core", self.attention_plan(), self.Hq // self.Hkv,
                                      mode="index-list")
 
     def aux_ops(self):
@@ -668,9 +669,9 @@ class IndexedBench(MaskedBench):
         ops = {"append": lambda li: self.kvd.append(lays[li].k_cache, lays[li].v_cache,
                                                     lays[li].k_new, lays[li].v_new, self.gpos,
                                                     None, self.status)}
-        part = self.kvd.workspace_partials(self.ws, self.attention_plan(), self.B * self.Hq,
-                                           self.D)
-        if part is not None:
+        plan = self.attention_plan()
+        part = self.kvd.workspace_partials(self.ws, plan, self.B * self.Hq, self.D)
+        if part is not None and plan.launches > 1:
             po, pl = part
             ops["combine"] = lambda li: self.kvd.combine(po, pl, out=self.out[li].view(-1, self.D))
         return ops
@@ -689,7 +690,6 @@ class Fp8Bench(MaskedBench):
         self.row = self.D + kvd.FP8_ROW_PAD
         need = kvd.attend_masked_fp8_workspace_bytes(self.B, self.Hq, self.Hkv, self.C, self.D)
         self.ws = kvd.workspace(need, dev)
-        self.splits = need > 256
 
     def _layer(self, li, lay, pos):
         self.kvd.append_fp8(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, pos, lay.mask,
@@ -717,7 +717,7 @@ class Fp8Bench(MaskedBench):
         return evs
 
     def launches_per_step(self):
-        return self.layers * (2 + (1 if self.splits else 0))  # append_fp8, attention, combine
+        return self.layers * (1 + self.attention_plan().launches)  # append_fp8, attention (+ combine)
 
     def attend_bytes(self, j):
         return fp8_attend_bytes(self.lengths_at(j), self.Hq, self.Hkv, self.C, self.D,
@@ -735,7 +735,7 @@ class Fp8Bench(MaskedBench):
         return self.kvd.attend_masked_fp8_plan(self.B, self.Hq, self.Hkv, self.C, self.D)
 
     def kernel_name(self):
-        return attention_kernel_name("E4M3 tensor-core", self.attention_plan()[0],
+        return attention_kernel_name("E4M3 tensor-core", self.attention_plan(),
                                      self.Hq // self.Hkv)
 
     def aux_ops(self):
@@ -744,9 +744,9 @@ class Fp8Bench(MaskedBench):
         ops = {"append": lambda li: self.kvd.append_fp8(lays[li].k_cache, lays[li].v_cache,
                                                         lays[li].k_new, lays[li].v_new,
                                                         self.gpos, lays[li].mask, self.status)}
-        part = self.kvd.workspace_partials(self.ws, self.attention_plan(), self.B * self.Hq,
-                                           self.D)
-        if part is not None:
+        plan = self.attention_plan()
+        part = self.kvd.workspace_partials(self.ws, plan, self.B * self.Hq, self.D)
+        if part is not None and plan.launches > 1:
             po, pl = part
             ops["combine"] = lambda li: self.kvd.combine(po, pl, out=self.out[li].view(-1, self.D))
         return ops

@@ -12,8 +12,9 @@
 // device, held by every GPU that loads the library until the process exits).
 //
 // The array is shared by every call on a device and keeps whatever the last
-// call left in it.  The attention kernel keeps its work counters in the first
-// 256 bytes; they must be zero when a launch starts.  A completed launch
+// call left in it.  The attention kernel keeps its work counters in the
+// array's leading bytes (kvd_plan.counter_bytes); they must be zero when a
+// launch starts.  A completed launch
 // leaves them at zero, but one whose bounded waits ran out (KVD_DEV_TIMEOUT)
 // may not, so every call clears that block on the caller's stream
 // (cudaMemsetAsync: stream-ordered, allocates nothing) before its launch.
@@ -122,7 +123,11 @@ kvd_status kvd_attend_masked_noalloc(const void* q, const void* k_cache, const v
     }
     // Work counters to zero first (a previous call's timed-out launch may have
     // left them set); stream-ordered before the launch.
-    const cudaError_t ez = cudaMemsetAsync(scratch, 0, 256, (cudaStream_t)stream);
+    kvd_plan plan;
+    const kvd_status sp = kvd_attend_masked_plan(B, Hq, Hkv, C, D, dtype, num_splits, &plan);
+    if (sp != KVD_OK) return sp;
+    const size_t counters = plan.counter_bytes > 256 ? plan.counter_bytes : 256;
+    const cudaError_t ez = cudaMemsetAsync(scratch, 0, counters, (cudaStream_t)stream);
     if (ez != cudaSuccess) {
         char msg[256];
         snprintf(msg, sizeof msg, "kvd_attend_masked_noalloc: clearing the counters failed: %s",

@@ -300,17 +300,19 @@ kvd_status check_attention_shape(int Hq, int Hkv, int D, kvd_dtype dt) {
     return KVD_OK;
 }
 
-// What the *_plan queries report: S of the split kernel (0 for the
-// one-launch cluster kernel) and where its partial rows sit in the workspace.
-void put_plan(const Plan& pl, bool small, int32_t* splits, size_t* lse_offset, size_t* o_offset) {
+// What the *_plan queries report (kvd_plan in kvd.h).
+void put_plan(const Plan& pl, bool small, kvd_plan* out) {
+    std::memset(out, 0, sizeof *out);
     if (small) {
-        *splits = 0;  // one launch, merged inside thread-block clusters: no partial rows
-        *lse_offset = *o_offset = 0;
+        out->splits = 0;  // one launch, merged inside thread-block clusters: no partial rows
+        out->launches = 1;
     } else {
-        *splits = pl.S;
-        *lse_offset = pl.S > 1 ? pl.off_lse : 0;
-        *o_offset = pl.S > 1 ? pl.off_po : 0;
+        out->splits = pl.S;
+        out->launches = pl.S > 1 ? 2 : 1;
+        out->lse_offset = pl.S > 1 ? pl.off_lse : 0;
+        out->o_offset = pl.S > 1 ? pl.off_po : 0;
     }
+    out->counter_bytes = small ? 0 : pl.off_lse;
 }
 
 }  // namespace
@@ -399,17 +401,15 @@ size_t kvd_attend_masked_workspace_bytes(int B, int Hq, int Hkv, int C, int D, k
 }
 
 kvd_status kvd_attend_masked_plan(int B, int Hq, int Hkv, int C, int D, kvd_dtype dtype,
-                                  int num_splits, int32_t* splits, size_t* lse_offset,
-                                  size_t* o_offset) {
-    if (!splits || !lse_offset || !o_offset)
+                                  int num_splits, kvd_plan* plan) {
+    if (!plan)
         return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_plan: null pointer");
     if (B < 1 || C < 1 || num_splits < 0)
         return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_plan: B, C >= 1 and num_splits >= 0 required");
     const kvd_status st = check_attention_shape(Hq, Hkv, D, dtype);
     if (st != KVD_OK) return st;
     const Plan pl = plan_attention(B, Hq, Hkv, C, D, dtype, 0, num_splits);
-    put_plan(pl, plan_small(B, Hkv, C, D, dtype, pl, num_splits).use, splits, lse_offset,
-             o_offset);
+    put_plan(pl, plan_small(B, Hkv, C, D, dtype, pl, num_splits).use, plan);
     return ok();
 }
 
@@ -570,16 +570,15 @@ size_t kvd_attend_masked_fp8_workspace_bytes(int B, int Hq, int Hkv, int C, int 
 }
 
 kvd_status kvd_attend_masked_fp8_plan(int B, int Hq, int Hkv, int C, int D, int num_splits,
-                                      int32_t* splits, size_t* lse_offset, size_t* o_offset) {
-    if (!splits || !lse_offset || !o_offset)
+                                      kvd_plan* plan) {
+    if (!plan)
         return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_fp8_plan: null pointer");
     if (B < 1 || C < 1 || num_splits < 0)
         return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_fp8_plan: B, C >= 1 and num_splits >= 0 required");
     const kvd_status st = check_attention_shape(Hq, Hkv, D, KVD_BF16);
     if (st != KVD_OK) return st;
     const Plan pl = plan_attention(B, Hq, Hkv, C, D, KVD_BF16, 0, num_splits, false, kFp8Tile);
-    put_plan(pl, plan_small(B, Hkv, C, D, KVD_BF16, pl, num_splits, true).use, splits, lse_offset,
-             o_offset);
+    put_plan(pl, plan_small(B, Hkv, C, D, KVD_BF16, pl, num_splits, true).use, plan);
     return ok();
 }
 
@@ -642,16 +641,14 @@ size_t kvd_attend_indexed_workspace_bytes(int B, int Hq, int Hkv, int topk, int 
 }
 
 kvd_status kvd_attend_indexed_plan(int B, int Hq, int Hkv, int topk, int D, kvd_dtype dtype,
-                                   int num_splits, int32_t* splits, size_t* lse_offset,
-                                   size_t* o_offset) {
-    if (!splits || !lse_offset || !o_offset)
+                                   int num_splits, kvd_plan* plan) {
+    if (!plan)
         return fail(KVD_ERR_INVALID_ARG, "kvd_attend_indexed_plan: null pointer");
     if (B < 1 || topk < 1 || num_splits < 0)
         return fail(KVD_ERR_INVALID_ARG, "kvd_attend_indexed_plan: B, topk >= 1 and num_splits >= 0 required");
     const kvd_status st = check_attention_shape(Hq, Hkv, D, dtype);
     if (st != KVD_OK) return st;
-    put_plan(plan_attention(B, Hq, Hkv, topk, D, dtype, 0, num_splits, true), false, splits,
-             lse_offset, o_offset);
+    put_plan(plan_attention(B, Hq, Hkv, topk, D, dtype, 0, num_splits, true), false, plan);
     return ok();
 }
 
@@ -709,9 +706,8 @@ size_t kvd_attend_paged_workspace_bytes(int Q, int Hq, int Hkv, int BS, int cols
 }
 
 kvd_status kvd_attend_paged_plan(int Q, int Hq, int Hkv, int BS, int cols, int D, kvd_dtype dtype,
-                                 int num_splits, int32_t* splits, size_t* lse_offset,
-                                 size_t* o_offset) {
-    if (!splits || !lse_offset || !o_offset)
+                                 int num_splits, kvd_plan* plan) {
+    if (!plan)
         return fail(KVD_ERR_INVALID_ARG, "kvd_attend_paged_plan: null pointer");
     if (Q < 1 || BS < 1 || cols < 1 || num_splits < 0)
         return fail(KVD_ERR_INVALID_ARG, "kvd_attend_paged_plan: Q, BS, cols >= 1 and num_splits >= 0 required");
@@ -719,8 +715,7 @@ kvd_status kvd_attend_paged_plan(int Q, int Hq, int Hkv, int BS, int cols, int D
         return fail(KVD_ERR_UNSUPPORTED, "kvd_attend_paged_plan: cols*BS >= 2^31");
     const kvd_status st = check_attention_shape(Hq, Hkv, D, dtype);
     if (st != KVD_OK) return st;
-    put_plan(plan_attention(Q, Hq, Hkv, cols * BS, D, dtype, BS, num_splits), false, splits,
-             lse_offset, o_offset);
+    put_plan(plan_attention(Q, Hq, Hkv, cols * BS, D, dtype, BS, num_splits), false, plan);
     return ok();
 }
 

@@ -36,10 +36,10 @@ SIGNATURES = {
     "kvd_attend_masked_launches": ([_i, _i, _i, _i, _i, _i, _i], _i),
     "kvd_attend_masked": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz,
                            _vp, _vp], _i),
-    "kvd_attend_masked_plan": ([_i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp], _i),
-    "kvd_attend_masked_fp8_plan": ([_i, _i, _i, _i, _i, _i, _vp, _vp, _vp], _i),
-    "kvd_attend_indexed_plan": ([_i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp], _i),
-    "kvd_attend_paged_plan": ([_i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp], _i),
+    "kvd_attend_masked_plan": ([_i, _i, _i, _i, _i, _i, _i, _vp], _i),
+    "kvd_attend_masked_fp8_plan": ([_i, _i, _i, _i, _i, _i, _vp], _i),
+    "kvd_attend_indexed_plan": ([_i, _i, _i, _i, _i, _i, _i, _vp], _i),
+    "kvd_attend_paged_plan": ([_i, _i, _i, _i, _i, _i, _i, _i, _vp], _i),
     "kvd_attend_masked_partial": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i,
                                    _vp, _sz, _vp, _vp], _i),
     "kvd_attend_masked_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i,
@@ -357,18 +357,24 @@ def attend_masked(q, k_cache, v_cache, mask, scale=None, out=None, lse=None, num
     return out
 
 
+class Plan(ctypes.Structure):
+    """kvd_plan (include/kvd.h): how a split attention call runs."""
+    _fields_ = [("splits", ctypes.c_int32), ("launches", ctypes.c_int32),
+                ("lse_offset", ctypes.c_size_t), ("o_offset", ctypes.c_size_t),
+                ("counter_bytes", ctypes.c_size_t)]
+
+
 def _plan(name, *args):
-    S = ctypes.c_int32()
-    lo, oo = ctypes.c_size_t(), ctypes.c_size_t()
-    st = getattr(load(), name)(*args, ctypes.byref(S), ctypes.byref(lo), ctypes.byref(oo))
+    pl = Plan()
+    st = getattr(load(), name)(*args, ctypes.byref(pl))
     _check(name, st)
-    return S.value, lo.value, oo.value
+    return pl
 
 
 def attend_masked_plan(B, Hq, Hkv, C, D, dtype=torch.bfloat16, num_splits=0):
-    """kvd_attend_masked_plan: (splits, part_lse byte offset, part_o byte
-    offset) of kvd_attend_masked's workspace for these sizes; splits 0 = the
-    one-launch cluster kernel, 1 = no combine."""
+    """kvd_attend_masked_plan: the Plan of kvd_attend_masked for these sizes
+    (splits 0 = the one-launch cluster kernel, 1 = no merge; launches 1 or 2;
+    workspace offsets of the partial rows)."""
     return _plan("kvd_attend_masked_plan", B, Hq, Hkv, C, D,
                  BF16 if dtype == torch.bfloat16 else F32, num_splits)
 
@@ -388,10 +394,10 @@ def attend_paged_plan(Q, Hq, Hkv, BS, cols, D, dtype=torch.bfloat16, num_splits=
 
 
 def workspace_partials(ws, plan, R, D):
-    """Views of a workspace's partial rows for a plan from one of the *_plan
+    """Views of a workspace's partial rows for a Plan from one of the *_plan
     queries: (part_o [R, S, D], part_lse [R, S]) fp32, or None without
     partial rows (splits <= 1)."""
-    S, lo, oo = plan
+    S, lo, oo = plan.splits, plan.lse_offset, plan.o_offset
     if S <= 1:
         return None
     flat = ws.view(torch.uint8)

@@ -168,18 +168,32 @@ kvd_status kvd_attend_masked(const void* q, const void* k_cache, const void* v_c
                              kvd_stream_t stream);
 
 /*
- * kvd_attend_masked_plan -- how kvd_attend_masked splits these sizes, for a
- * caller that reads the workspace's partial rows or times the two launches
- * apart.  *splits = S of the split kernel: 1 when its units write the output
- * rows directly (one launch), > 1 when a combine launch follows (the partial
- * rows are then in the workspace: part_lse float [B*Hq, S] at *lse_offset
- * bytes and part_o float [B*Hq, S, D] at *o_offset, the kvd_combine
- * layout), 0 when the one-launch cluster kernel runs (no partial rows; the
- * offsets are then 0).  Arguments as for kvd_attend_masked; errors as for it.
+ * How a split attention call runs for given sizes (the *_plan queries), for a
+ * caller that reads the workspace's partial rows or times the launches apart:
+ *   splits            S of the split kernel: 1 = its units write the output
+ *                     rows directly; > 1 = partial rows merged by log-sum-exp;
+ *                     0 = the one-launch cluster kernel (no partial rows)
+ *   launches          kernel launches of one call (1, or 2 when the combine
+ *                     launch merges the splits)
+ *   lse_offset, o_offset  with S > 1, the workspace byte offsets of part_lse
+ *                     float [rows*Hq, S] and part_o float [rows*Hq, S, D] (the
+ *                     kvd_combine layout); 0 otherwise
+ *   counter_bytes     leading workspace bytes holding work counters (zero
+ *                     before a call; every completed call leaves them zero)
  */
+typedef struct {
+    int32_t splits;
+    int32_t launches;
+    size_t lse_offset;
+    size_t o_offset;
+    size_t counter_bytes;
+} kvd_plan;
+
+/* kvd_attend_masked_plan -- kvd_plan of kvd_attend_masked (and of
+ * kvd_append_attend_masked, kvd_attend_masked_partial) for these sizes.
+ * Arguments and errors as for kvd_attend_masked. */
 kvd_status kvd_attend_masked_plan(int B, int Hq, int Hkv, int C, int D, kvd_dtype dtype,
-                                  int num_splits, int32_t* splits, size_t* lse_offset,
-                                  size_t* o_offset);
+                                  int num_splits, kvd_plan* plan);
 
 /*
  * kvd_attend_masked_partial -- the same attention as kvd_attend_masked, but
@@ -263,10 +277,9 @@ kvd_status kvd_append_attend_masked(const void* q, void* k_cache, void* v_cache,
 size_t kvd_attend_indexed_workspace_bytes(int B, int Hq, int Hkv, int topk, int D,
                                           kvd_dtype dtype, int num_splits);
 /* As kvd_attend_masked_plan, for kvd_attend_indexed (the one-launch cluster
- * kernel is never used: *splits >= 1). */
+ * kernel is never used: splits >= 1). */
 kvd_status kvd_attend_indexed_plan(int B, int Hq, int Hkv, int topk, int D, kvd_dtype dtype,
-                                   int num_splits, int32_t* splits, size_t* lse_offset,
-                                   size_t* o_offset);
+                                   int num_splits, kvd_plan* plan);
 kvd_status kvd_attend_indexed(const void* q, const void* k_cache, const void* v_cache,
                               const int32_t* indices, void* out, float* lse_out, int B, int Hq,
                               int Hkv, int C, int topk, int D, float scale, kvd_dtype dtype,
@@ -318,7 +331,7 @@ kvd_status kvd_append_fp8(void* k_cache, void* v_cache, const void* k_new, const
 size_t kvd_attend_masked_fp8_workspace_bytes(int B, int Hq, int Hkv, int C, int D, int num_splits);
 /* As kvd_attend_masked_plan, for kvd_attend_masked_fp8. */
 kvd_status kvd_attend_masked_fp8_plan(int B, int Hq, int Hkv, int C, int D, int num_splits,
-                                      int32_t* splits, size_t* lse_offset, size_t* o_offset);
+                                      kvd_plan* plan);
 kvd_status kvd_attend_masked_fp8(const void* q, const void* k_cache, const void* v_cache,
                                  const uint8_t* mask, void* out, float* lse_out, int B, int Hq,
                                  int Hkv, int C, int D, float scale, int num_splits,
@@ -347,8 +360,9 @@ kvd_status kvd_attend_masked_fp8(const void* q, const void* k_cache, const void*
  *    that first call before any stream capture on that device (and again
  *    after a cudaDeviceReset, which loads the library's module anew).
  *  - All calls on a device share the one array, which keeps the last call's
- *    contents.  Each call first clears the array's 256 bytes of work counters
- *    with cudaMemsetAsync on `stream` (stream-ordered; no allocation), so a
+ *    contents.  Each call first clears the array's work counters
+ *    (kvd_plan.counter_bytes) with cudaMemsetAsync on `stream`
+ *    (stream-ordered; no allocation), so a
  *    call whose launch gave up on a bounded wait (KVD_DEV_TIMEOUT) does not
  *    poison the next one.  Calls that may overlap on the GPU (other streams,
  *    unordered host threads) race on the array: the caller must order them.
@@ -362,10 +376,9 @@ kvd_status kvd_attend_masked_noalloc(const void* q, const void* k_cache, const v
 size_t kvd_attend_paged_workspace_bytes(int Q, int Hq, int Hkv, int BS, int cols, int D,
                                         kvd_dtype dtype, int num_splits);
 /* As kvd_attend_masked_plan, for kvd_attend_paged (rows = sequences; the
- * one-launch cluster kernel is never used: *splits >= 1). */
+ * one-launch cluster kernel is never used: splits >= 1). */
 kvd_status kvd_attend_paged_plan(int Q, int Hq, int Hkv, int BS, int cols, int D, kvd_dtype dtype,
-                                 int num_splits, int32_t* splits, size_t* lse_offset,
-                                 size_t* o_offset);
+                                 int num_splits, kvd_plan* plan);
 kvd_status kvd_attend_paged(const void* q_in, const void* key_cache, const void* value_cache,
                             const int32_t* block_tables, const int32_t* seq_lens,
                             const int32_t* seq_offset, void* out, float* lse_out, int Q, int Hq,

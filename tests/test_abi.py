@@ -67,22 +67,26 @@ def test_masked_host_validation(lib):
 
 
 def test_workspace_sizes_follow_the_plan(lib):
-    """Workspace = partial rows + their log-sum-exps for S splits; one split
-    needs none.  The plan depends on the sizes only."""
-    # 16 x 32 heads over capacity 8192: 512 rows
+    """Workspace = counters | partial log-sum-exps | partial rows, for S
+    splits; one split needs only the counters.  The plan depends on the sizes
+    only."""
+    from decode_attention_kv_gb300 import kvd
+    # 16 x 32 heads over capacity 8192: 512 query rows
     ws = lib.kvd_attend_masked_workspace_bytes(16, 32, 8, 8192, 128, 0, 0)
-    R = 16 * 32
-    S = None
-    for s in range(1, 65):
-        lse = (R * s * 4 + 255) // 256 * 256
-        if 256 + lse + R * s * 128 * 4 == ws:
-            S = s
-    assert S is not None and S > 1
+    pl = kvd.attend_masked_plan(16, 32, 8, 8192, 128)
+    R, S = 16 * 32, pl.splits
+    assert S > 1 and pl.launches == 2
+    assert pl.counter_bytes == 256 == pl.lse_offset
+    assert pl.o_offset == pl.lse_offset + (R * S * 4 + 255) // 256 * 256
+    assert ws == pl.o_offset + R * S * 128 * 4
     # one split: only the 256-byte block of scheduling counters
     assert lib.kvd_attend_masked_workspace_bytes(1, 4, 4, 32, 64, 1, 0) == 256
     # counters | 32 x 16 partial lse | 32 x 16 x 128 partial rows
     assert lib.kvd_attend_masked_workspace_bytes(1, 32, 32, 32768, 128, 0, 16) == \
         256 + 32 * 16 * 4 + 32 * 16 * 128 * 4
+    # the short static buffer: the one-launch cluster kernel
+    pl = kvd.attend_masked_plan(1, 32, 32, 1152, 128)
+    assert pl.splits == 0 and pl.launches == 1
     assert lib.kvd_attend_paged_workspace_bytes(64, 32, 8, 128, 32, 128, 0, 0) > 0
     assert lib.kvd_attend_masked_workspace_bytes(1, 4, 3, 32, 64, 0, 0) == 0  # invalid -> 0
 

@@ -283,3 +283,43 @@ def test_small_launch_matches_split_kernel(kvd, dtype, Hq, Hkv, D):
         out, lse = _run_masked(kvd, q, k, v, mask, 0.11, ns)
         assert_attention_close(out, ref, dtype, f"num_splits {ns}")
         assert_lse_close(lse, ref_lse)
+
+
+MERGE_CASES = [
+    # dtype, B, Hq, Hkv, C, D, num_splits
+    (torch.bfloat16, 4, 32, 8, 4096, 128, 0),     # tensor-core consumers
+    (torch.bfloat16, 3, 16, 16, 6000, 64, 0),     # CUDA-core consumers, D 64
+    (torch.float32, 2, 8, 2, 3000, 128, 24),      # fp32, explicit splits
+    (torch.bfloat16, 1, 32, 32, 32768, 128, 0),   # 112 splits per row
+]
+
+
+@pytest.mark.parametrize("dtype,B,Hq,Hkv,C,D,ns", MERGE_CASES)
+def test_split_merge_reuses_its_workspace(kvd, dtype, B, Hq, Hkv, C, D, ns):
+    """Four calls on one workspace, lengths changing between them: every
+    output matches the oracle and every call leaves the workspace's work
+    counters at zero."""
+    import math
+    plan = kvd.attend_masked_plan(B, Hq, Hkv, C, D, dtype, ns)
+    assert plan.splits > 1
+    need = kvd.attend_masked_workspace_bytes(B, Hq, Hkv, C, D, dtype, ns)
+    ws = kvd.workspace(need, "cuda")
+    g = W.generator(7700 + C)
+    q = W.randn(g, (B, Hq, D), dtype)
+    k = W.randn(g, (B, Hkv, C, D), dtype)
+    v = W.randn(g, (B, Hkv, C, D), dtype)
+    kd, vd = k.cuda(), v.cuda()
+    status = kvd.status_tensor()
+    gl = W.generator(7800 + C)
+    for call in range(4):
+        lengths = [int(x) for x in W.randint(gl, B, 0 if call == 3 else 1, C)]
+        mask = W.prefix_mask(lengths, C)
+        lse = torch.empty(B, Hq, device="cuda")
+        out = kvd.attend_masked(q.cuda(), kd, vd, mask.cuda(), 1.0 / math.sqrt(D), lse=lse,
+                                num_splits=ns, workspace=ws, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert int(ws[:plan.counter_bytes].count_nonzero()) == 0, f"call {call}: counters left set"
+        ref, ref_lse = oracle.attend_masked(q, k, v, mask, 1.0 / math.sqrt(D))
+        assert_attention_close(out, ref, dtype, f"call {call}")
+        assert_lse_close(lse, ref_lse, f"call {call}")
