@@ -237,12 +237,12 @@ def masked_config(name, w, layers, lengths0):
     return c
 
 
-def paged_config(pw):
+def paged_config(pw, name="paged"):
     NB, BS, Hkv, D = pw.key_cache.shape
     Q, Hq, _ = pw.q.shape
     lengths = [int(x) for x in pw.lengths]
     rows = 2 * sum(lengths) * Hkv * D * 2
-    return {"workload": "paged", "num_blocks": NB, "block_size": BS, "kv_heads": Hkv,
+    return {"workload": name, "num_blocks": NB, "block_size": BS, "kv_heads": Hkv,
             "q_heads": Hq, "head_dim": D, "sequences": Q, "dtype": "bf16",
             "total_tokens": pw.total_tokens,
             "l2": f"inputs larger than L2: {rows / 2**30:.2f} GiB of valid K/V rows per step "
@@ -254,8 +254,8 @@ def workload_config(name):
     """The config block of a workload, built from host copies of its inputs
     (the reference arm prints the same block as the GPU arm)."""
     import workloads
-    if name == "paged":
-        return paged_config(workloads.paged(device="cpu"))
+    if name in ("paged", "paged_gather"):
+        return paged_config(workloads.paged(device="cpu"), name)
     gen = {"indexed": "gqa"}.get(name, name)
     w = getattr(workloads, gen)(device="cpu", layers=1)
     return masked_config(name, w, LAYERS[name], [int(x) for x in w.layers[0].lengths])
@@ -488,12 +488,18 @@ class MaskedBench:
 
 
 class PagedBench:
-    """Paged workload: gather_pa_kv_cache, then paged attention, over the
-    whole 8192-block cache."""
+    """Paged workload over the whole 8192-block cache, in one of two steps:
+    ``paged`` = paged decode attention (every sequence's query against its
+    blocks, through the block tables), ``paged_gather`` = gather_pa_kv_cache
+    into contiguous rows.  The two are separate steps: a decode step reads the
+    paged cache directly; the gather serves consumers of the contiguous layout
+    (and, run right before the attention, would leave it a cache full of the
+    gather's dirty lines to write back)."""
 
-    def __init__(self, torch, kvd, dev):
+    def __init__(self, torch, kvd, dev, mode="paged"):
         import workloads
-        self.torch, self.kvd, self.dev, self.name = torch, kvd, dev, "paged"
+        self.torch, self.kvd, self.dev, self.name = torch, kvd, dev, mode
+        self.gather_mode = mode == "paged_gather"
         pw = workloads.paged(device=dev)
         self.pw = pw
         self.Q, self.Hq, self.D = pw.q.shape
@@ -501,8 +507,10 @@ class PagedBench:
         self.elem = 2
         self.layers = 1
         self.lengths = [int(x) for x in pw.lengths]
-        self.ko = torch.empty((pw.total_tokens, self.Hkv, self.D), dtype=torch.bfloat16, device=dev)
-        self.vo = torch.empty_like(self.ko)
+        if self.gather_mode:
+            self.ko = torch.empty((pw.total_tokens, self.Hkv, self.D), dtype=torch.bfloat16,
+                                  device=dev)
+            self.vo = torch.empty_like(self.ko)
         self.out = torch.empty_like(pw.q)
         cols = pw.block_tables.shape[1]
         need = kvd.attend_paged_workspace_bytes(self.Q, self.Hq, self.Hkv, self.BS, cols, self.D)
@@ -525,60 +533,82 @@ class PagedBench:
                               pw.seq_offset, pw.scale, out=self.out, workspace=self.ws,
                               dev_status=self.status)
 
+    def _step(self):
+        if self.gather_mode:
+            self._gather()
+        else:
+            self._attend()
+
     def eager_run(self, j, timing=False):
+        """One step; with timing, CUDA events around the call (its main
+        kernel: the attention, or the gather)."""
         torch = self.torch
         if not timing:
-            self._gather()
-            self._attend()
+            self._step()
             return []
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         e[0].record()
-        self._gather()
+        self._step()
         e[1].record()
-        self._attend()
-        e[2].record()
-        return [("gather", e[0], e[1]), ("attend", e[1], e[2])]
+        return [("attend", e[0], e[1])]
 
     def capture(self):
         torch = self.torch
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self._gather()
-            self._attend()
+            self._step()
         self.graph = g
 
     def graph_run(self, j):
         self.graph.replay()
 
     def launches_per_step(self):
-        return 1 + self.attention_plan().launches  # gather, attention (+ combine)
+        return 1 if self.gather_mode else self.attention_plan().launches
 
     def attend_bytes(self, j):
+        """Algorithmic bytes of the step's main kernel."""
+        if self.gather_mode:
+            return self.gather_bytes()
         return paged_attend_bytes(self.lengths, self.Hq, self.Hkv, self.D, self.elem, self.BS)
 
     def gather_bytes(self):
         return gather_bytes(self.lengths, self.Hkv, self.D, self.Hkv, self.D, self.elem, self.BS)
 
     def step_bytes(self, j):
-        return self.attend_bytes(j) + self.gather_bytes()
+        return self.attend_bytes(j)
 
     def tokens_per_step(self):
-        return self.Q
+        return 0 if self.gather_mode else self.Q
 
     def flops_per_step(self):
-        return attention_flops(self.lengths, self.Hq, self.D)
+        return 0 if self.gather_mode else attention_flops(self.lengths, self.Hq, self.D)
 
     def e2e_setup(self):
+        """Attention: the step's queries in from pinned host memory, the
+        outputs back.  Gather: the step's block tables, cumsum lengths and
+        offsets in, the device status word back (the gathered rows stay on
+        the device for their consumer)."""
         torch = self.torch
-        self.h_q = torch.empty(self.pw.q.shape, dtype=self.pw.q.dtype, pin_memory=True).copy_(
-            self.pw.q.cpu())
-        self.h_out = torch.empty(self.pw.q.shape, dtype=self.pw.q.dtype, pin_memory=True)
+        pw = self.pw
+        if self.gather_mode:
+            self.h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
+                         for t in (pw.block_tables, pw.seq_lens, pw.seq_offset)]
+            self.h_st = torch.empty(1, dtype=torch.int32, pin_memory=True)
+            return sum(t.numel() * 4 for t in self.h_in), 4
+        self.h_q = torch.empty(pw.q.shape, dtype=pw.q.dtype, pin_memory=True).copy_(pw.q.cpu())
+        self.h_out = torch.empty(pw.q.shape, dtype=pw.q.dtype, pin_memory=True)
         return self.h_q.numel() * 2, self.h_out.numel() * 2
 
     def e2e_step(self, j):
-        self.pw.q.copy_(self.h_q, non_blocking=True)
-        self._gather()
+        pw = self.pw
+        if self.gather_mode:
+            for d, h in zip((pw.block_tables, pw.seq_lens, pw.seq_offset), self.h_in):
+                d.copy_(h, non_blocking=True)
+            self._gather()
+            self.h_st.copy_(self.status, non_blocking=True)
+            return
+        pw.q.copy_(self.h_q, non_blocking=True)
         self._attend()
         self.h_out.copy_(self.out, non_blocking=True)
 
@@ -587,21 +617,25 @@ class PagedBench:
         return self.kvd.attend_paged_plan(self.Q, self.Hq, self.Hkv, self.BS, cols, self.D)
 
     def kernel_name(self):
+        if self.gather_mode:
+            return "gather_kernel (16-byte vectors, block-table indirection)"
         return attention_kernel_name("tensor-core", self.attention_plan(), self.Hq // self.Hkv,
                                      mode="paged")
 
     def aux_ops(self):
-        """The gather, and the combine behind the paged attention."""
-        ops = {"gather": lambda li: self._gather()}
+        """The combine behind the paged attention (the gather step is one
+        launch)."""
+        if self.gather_mode:
+            return {}
         plan = self.attention_plan()
         part = self.kvd.workspace_partials(self.ws, plan, self.Q * self.Hq, self.D)
         if part is not None and plan.launches > 1:
             po, pl = part
-            ops["combine"] = lambda li: self.kvd.combine(po, pl, out=self.out.view(-1, self.D))
-        return ops
+            return {"combine": lambda li: self.kvd.combine(po, pl, out=self.out.view(-1, self.D))}
+        return {}
 
     def config(self):
-        return paged_config(self.pw)
+        return paged_config(self.pw, self.name)
 
 
 class IndexedBench(MaskedBench):
@@ -756,8 +790,8 @@ class Fp8Bench(MaskedBench):
 
 
 def make_bench(name, torch, kvd, dev, layers=None):
-    if name == "paged":
-        return PagedBench(torch, kvd, dev)
+    if name in ("paged", "paged_gather"):
+        return PagedBench(torch, kvd, dev, name)
     if name == "gqa_fp8":
         return Fp8Bench(torch, kvd, dev, layers)
     if name == "indexed":
@@ -1053,19 +1087,23 @@ def oracle_rate(name, seconds):
                 "sample": f"{n} whole layers of the {name} workload ({what}), {el:.1f} s",
                 "cpu_model": cpu_model()}
 
-    if name == "paged":
+    if name in ("paged", "paged_gather"):
         pw = workloads.paged(device="cpu")
         lengths = [int(x) for x in pw.lengths]
-        kb = pw.key_cache.view(torch.int16).numpy()
-        vb = pw.value_cache.view(torch.int16).numpy()
-        per = (paged_attend_bytes(lengths, 32, 8, 128, 2, 128)
-               + gather_bytes(lengths, 8, 128, 8, 128, 2, 128))
+        if name == "paged_gather":
+            kb = pw.key_cache.view(torch.int16).numpy()
+            vb = pw.value_cache.view(torch.int16).numpy()
+
+            def step(n):
+                oracle.gather_paged(kb, vb, pw.block_tables, pw.seq_lens, pw.seq_offset)
+            return run(step, gather_bytes(lengths, 8, 128, 8, 128, 2, 128),
+                       "gather of all 64 sequences")
 
         def step(n):
-            oracle.gather_paged(kb, vb, pw.block_tables, pw.seq_lens, pw.seq_offset)
             oracle.attend_paged(pw.q, pw.key_cache, pw.value_cache, pw.block_tables, pw.seq_lens,
                                 pw.seq_offset, pw.scale)
-        return run(step, per, "gather + paged attention of all 64 sequences")
+        return run(step, paged_attend_bytes(lengths, 32, 8, 128, 2, 128),
+                   "paged attention of all 64 sequences")
     if name == "indexed":
         w = workloads.gqa(device="cpu", layers=1)
         lay = w.layers[0]
@@ -1151,7 +1189,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvd", choices=["kvd", "reference"])
     ap.add_argument("--workload", default="gqa",
-                    choices=["gqa", "long", "paged", "npuw", "indexed", "window", "gqa_fp8"])
+                    choices=["gqa", "long", "paged", "paged_gather", "npuw", "indexed", "window",
+                             "gqa_fp8"])
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="oracle seconds for the main workload's CPU baseline")
@@ -1250,7 +1289,8 @@ def main():
 
     others = {}
     if not args.no_others:
-        for name in ("long", "paged", "npuw", "gqa", "indexed", "window", "gqa_fp8"):
+        for name in ("long", "paged", "paged_gather", "npuw", "gqa", "indexed", "window",
+                     "gqa_fp8"):
             if name == args.workload:
                 continue
             log(f"workload {name}")

@@ -105,6 +105,8 @@ struct AttendParams {
     const int32_t* pos;          // [rows]
     uint8_t* mask_w;             // the mask, written at pos
     int out_f32;                 // out is fp32 whatever the element type (a range's partial)
+    int small_push;              // one-launch kernel: the splits push partials into split 0
+    int small_nwg;               // one-launch kernel: consumer warp groups per CTA (1 or 2)
 };
 
 // Output rows: the element type of q, or fp32 for a token range's partial

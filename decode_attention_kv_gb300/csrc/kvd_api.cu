@@ -24,8 +24,8 @@ cudaError_t launch_attend_fp8(int D, int G, const AttendParams& p, cudaStream_t 
 cudaError_t launch_attend_small(kvd_dtype dt, int D, int G, const AttendParams& p, int S, int rows,
                                 const CUtensorMap* kmap, const CUtensorMap* vmap,
                                 cudaStream_t stream);
-int small_shared_bytes(kvd_dtype dt, int D, int G, int chunk);
-int small_shared_bytes_fp8(int D, int G, int chunk);
+int small_shared_bytes(kvd_dtype dt, int D, int G, int chunk, int slots, int nwg);
+int small_shared_bytes_fp8(int D, int G, int chunk, int slots, int nwg);
 cudaError_t launch_attend_small_fp8(int D, int G, const AttendParams& p, int S, int rows,
                                     cudaStream_t stream);
 }  // namespace kvd
@@ -183,6 +183,8 @@ Plan plan_attention(int rows, int Hq, int Hkv, int cap, int D, kvd_dtype dt, int
 // tensor-core layout, any 16 rows for row copies (16-byte mask vectors).
 struct SmallPlan {
     bool use;
+    bool push;  // every split's partial fits split 0's shared memory
+    int nwg;    // consumer warp groups per CTA
     int chunk, S, rows;
 };
 
@@ -191,15 +193,30 @@ SmallPlan plan_small(int B, int Hkv, int C, int D, kvd_dtype dt, const Plan& pl,
                      bool fp8 = false) {
     SmallPlan sp{};
     if (num_splits != 0) return sp;
-    const int T = pl.tile;
-    const int q = (!fp8 && attend_uses_mma(dt, pl.G)) ? T : 16;
+    const int q = (!fp8 && small_uses_mma(dt, pl.G)) ? 64 : 16;  // 64-row boxes or 16-row copies
     const long long rows = (long long)B * Hkv * pl.HG;
     const long long chunk = ((C + kSmallSplits - 1) / kSmallSplits + q - 1) / q * q;
     const long long S = (C + chunk - 1) / chunk;
-    const int smem = fp8 ? small_shared_bytes_fp8(D, pl.G, (int)chunk)
-                         : small_shared_bytes(dt, D, pl.G, (int)chunk);
-    sp.use = chunk <= kSmallTokens && rows * S <= kGridUnitsHint && rows <= 65535 &&
-             smem <= kSmallShared;
+    auto smem = [&](int slots, int nwg) {
+        return fp8 ? small_shared_bytes_fp8(D, pl.G, (int)chunk, slots, nwg)
+                   : small_shared_bytes(dt, D, pl.G, (int)chunk, slots, nwg);
+    };
+    // the first layout that fits two CTAs per SM: two consumer warp groups
+    // (tensor-core consumers over two or more tiles) before one; partials
+    // pushed into split 0 before pulled from the others
+    const int nt = (int)((chunk + q - 1) / q);
+    const bool two = !fp8 && small_uses_mma(dt, pl.G) && nt >= 2;
+    sp.use = false;
+    for (int nwg = two ? 2 : 1; nwg >= 1 && !sp.use; --nwg) {
+        for (int push = 1; push >= 0 && !sp.use; --push) {
+            if (smem(push ? (int)S : 1, nwg) <= kSmallShared) {
+                sp.use = true;
+                sp.push = push != 0;
+                sp.nwg = nwg;
+            }
+        }
+    }
+    sp.use = sp.use && chunk <= kSmallTokens && rows * S <= kGridUnitsHint && rows <= 65535;
     sp.chunk = (int)chunk;
     sp.S = (int)S;
     sp.rows = (int)rows;
@@ -461,20 +478,24 @@ kvd_status attend_masked_impl(const char* fn, const void* q, const void* k_cache
     CUtensorMap kmap, vmap;
     std::memset(&kmap, 0, sizeof kmap);
     std::memset(&vmap, 0, sizeof vmap);
-    if (attend_uses_mma(dtype, pl.G)) {
+    const SmallPlan sp = plan_small(B, Hkv, C, D, dtype, pl, num_splits);
+    if (sp.use ? small_uses_mma(dtype, pl.G) : attend_uses_mma(dtype, pl.G)) {
+        // 128-byte-swizzled boxes of 64 dims x (tile rows) for the tensor-core consumers
         const long long rows = (long long)B * Hkv * C;
         if (rows >= (1ll << 31))
             return fail(KVD_ERR_UNSUPPORTED, "%s: B*Hkv*C >= 2^31 rows", fn);
-        st = make_cache_map(&kmap, k_cache, dtype, false, rows, Hkv, D, pl.tile, true);
+        const int box_rows = sp.use ? 64 : pl.tile;
+        st = make_cache_map(&kmap, k_cache, dtype, false, rows, Hkv, D, box_rows, true);
         if (st != KVD_OK) return st;
-        st = make_cache_map(&vmap, v_cache, dtype, false, rows, Hkv, D, pl.tile, true);
+        st = make_cache_map(&vmap, v_cache, dtype, false, rows, Hkv, D, box_rows, true);
         if (st != KVD_OK) return st;
     }
-    const SmallPlan sp = plan_small(B, Hkv, C, D, dtype, pl, num_splits);
     if (sp.use) {
         AttendParams ps = p;
         ps.chunk = sp.chunk;
         ps.S = sp.S;
+        ps.small_push = sp.push ? 1 : 0;
+        ps.small_nwg = sp.nwg;
         const cudaError_t e = launch_attend_small(dtype, D, pl.G, ps, sp.S, sp.rows, &kmap, &vmap,
                                                   (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, fn);
@@ -620,6 +641,8 @@ kvd_status kvd_attend_masked_fp8(const void* q, const void* k_cache, const void*
         AttendParams ps = p;
         ps.chunk = sp.chunk;
         ps.S = sp.S;
+        ps.small_push = sp.push ? 1 : 0;
+        ps.small_nwg = sp.nwg;
         const cudaError_t es = launch_attend_small_fp8(D, pl.G, ps, sp.S, sp.rows, (cudaStream_t)stream);
         if (es != cudaSuccess) return cuda_fail(es, "kvd_attend_masked_fp8 launch");
         return ok();

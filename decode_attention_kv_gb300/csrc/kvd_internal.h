@@ -44,6 +44,12 @@ struct AttendGeom {
 // head use the tensor-core consumers, everything else the CUDA-core ones.
 inline bool attend_uses_mma(kvd_dtype dt, int G) { return dt == KVD_BF16 && G >= 4; }
 
+// The one-launch cluster kernel (short buffers) uses the tensor-core
+// consumers for every bf16 group width: there the consumers' latency, not
+// HBM, bounds the launch, and 16 mma per 16-token slab (unused head columns
+// included) finish a split far sooner than per-token shuffle reductions.
+inline bool small_uses_mma(kvd_dtype dt, int G) { (void)G; return dt == KVD_BF16; }
+
 // Sets the message kvd_last_error() returns on this thread.
 void set_last_error(const char* msg);
 
