@@ -14,6 +14,8 @@ Every function states what it computes and the page section it follows:
 * ``append`` -- same article, Part 2 "NPUW 的核心设计" (update_kvcache_for).
 * ``gather_paged`` -- "PyPTO 实现 AscendC GatherPaKvCache（Norm/ND 分支）",
   sections 3.1-3.3 and 7.
+* ``append_paged`` -- the append of Part 2 ("update_kvcache_for") into the
+  paged layout, through the gather's index mapping (section 3.2).
 * ``attend_paged`` -- gather (above) followed by ``attend_masked`` with an
   all-ones mask.
 * ``e4m3_codes``, ``e4m3_values``, ``quantize_rows``, ``append_fp8``,
@@ -87,6 +89,7 @@ def lib() -> ctypes.CDLL:
                                                     cd, dp, dp, ci]
             L.kvd_oracle_copy_prefix.argtypes = [vp, vp, vp, vp, u8p, i32p, ci, ci, ci, ci, ci, ci]
             L.kvd_oracle_gather_paged.argtypes = [vp, vp, i32p, i32p, i32p, vp, vp] + [ci] * 10
+            L.kvd_oracle_append_paged.argtypes = [vp, vp, i32p, i32p, vp, vp, i32p] + [ci] * 7
             L.kvd_oracle_attend_paged.argtypes = [vp, vp, vp, i32p, i32p, i32p] + [ci] * 8 + [
                 cd, dp, dp, ci]
             L.kvd_oracle_combine.argtypes = [dp, dp, ci, ci, ci, dp, dp]
@@ -101,6 +104,7 @@ def lib() -> ctypes.CDLL:
             for f in (L.kvd_oracle_attend_masked, L.kvd_oracle_append, L.kvd_oracle_copy_prefix,
                       L.kvd_oracle_attend_indexed,
                       L.kvd_oracle_gather_paged, L.kvd_oracle_attend_paged,
+                      L.kvd_oracle_append_paged,
                       L.kvd_oracle_combine, L.kvd_oracle_threads):
                 f.restype = ctypes.c_int
             _lib = L
@@ -313,6 +317,29 @@ def gather_paged(key_cache, value_cache, block_tables, seq_lens, seq_offset=None
                                         _p(ko), _p(vo), Q, NB, BS, cols, Hk, Dk, Hv, Dv, T,
                                         kc.dtype.itemsize)
     return ko, vo, err
+
+
+def append_paged(key_cache, value_cache, block_tables, seq_offset, k_new, v_new, pos) -> int:
+    """Paged KV append in place on numpy caches [NB, BS, Hkv, D] (any element
+    type, byte copy): token pos[q] of sequence q goes to the block and slot
+    the paged gather reads it from (same index mapping); k_new, v_new
+    [Q, Hkv, D]; seq_offset [Q] or None.  Returns error bits."""
+    if not (isinstance(key_cache, np.ndarray) and isinstance(value_cache, np.ndarray)):
+        raise TypeError("oracle.append_paged works in place on numpy arrays")
+    NB, BS, Hkv, D = key_cache.shape
+    eb = key_cache.dtype.itemsize
+    bt = _i32(block_tables)
+    Q, cols = bt.shape
+    kn = np.ascontiguousarray(_bytes_view(k_new))
+    vn = np.ascontiguousarray(_bytes_view(v_new))
+    if kn.size != Q * Hkv * D * eb or vn.size != kn.size:
+        raise ValueError("oracle.append_paged: new rows have the wrong size")
+    p = _i32(pos)
+    so = None if seq_offset is None else _i32(seq_offset)
+    return lib().kvd_oracle_append_paged(_p(key_cache), _p(value_cache), _p(bt, ctypes.c_int32),
+                                         None if so is None else _p(so, ctypes.c_int32),
+                                         _p(kn), _p(vn), _p(p, ctypes.c_int32), Q, NB, BS, cols,
+                                         Hkv, D, eb)
 
 
 def attend_paged(q, key_cache, value_cache, block_tables, seq_lens, seq_offset, scale: float,

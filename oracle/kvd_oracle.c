@@ -507,6 +507,53 @@ int kvd_oracle_gather_paged(const void* key_cache, const void* value_cache,
 }
 
 /*
+ * Paged KV append: the step's new token of sequence q goes where the paged
+ * gather (above) finds token pos[q] of q -- the same index mapping, written
+ * instead of read:
+ *   physical = block_tables[q, seq_offset[q] / BS + pos[q] / BS]
+ *   key_cache[physical, pos[q] % BS] = k_new[q]   (all Hkv x D; same for value)
+ *   key_cache, value_cache [NB, BS, Hkv, D]; k_new, v_new [Q, Hkv, D];
+ *   pos [Q]; seq_offset [Q] or NULL (zeros).
+ * A sequence whose pos is negative (ORC_ERR_POS), whose seq_offset is
+ * negative or not a multiple of BS (ORC_ERR_OFFSET), whose column is past the
+ * table (ORC_ERR_COLS) or whose block id is outside [0, NB) (ORC_ERR_BLOCK)
+ * writes nothing; the bits are returned.  Pure byte copy.
+ */
+int kvd_oracle_append_paged(void* key_cache, void* value_cache, const int32_t* block_tables,
+                            const int32_t* seq_offset, const void* k_new, const void* v_new,
+                            const int32_t* pos, int Q, int NB, int BS, int cols, int Hkv, int D,
+                            int elem_bytes) {
+    int err = 0;
+    const size_t row = (size_t)Hkv * D * elem_bytes;
+    for (int q = 0; q < Q; ++q) {
+        const long t = pos[q];
+        if (t < 0) {
+            err |= ORC_ERR_POS;
+            continue;
+        }
+        const long off = seq_offset ? seq_offset[q] : 0;
+        if (off < 0 || off % BS) {
+            err |= ORC_ERR_OFFSET;
+            continue;
+        }
+        const long col = off / BS + t / BS;
+        if (col >= cols) {
+            err |= ORC_ERR_COLS;
+            continue;
+        }
+        const long phys = block_tables[(size_t)q * cols + col];
+        if (phys < 0 || phys >= NB) {
+            err |= ORC_ERR_BLOCK;
+            continue;
+        }
+        const size_t dst = ((size_t)phys * BS + (size_t)(t % BS)) * row;
+        memcpy((char*)key_cache + dst, (const char*)k_new + (size_t)q * row, row);
+        memcpy((char*)value_cache + dst, (const char*)v_new + (size_t)q * row, row);
+    }
+    return err;
+}
+
+/*
  * Paged decode attention: for sequence q, the keys and values are the rows
  * the gather above produces for q (all of them valid), and the query
  * q_in[q, h, :] attends over them with kv head h / (Hq / Hkv).
