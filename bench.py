@@ -489,9 +489,9 @@ class MaskedBench:
 
 class PagedBench:
     """Paged workload over the whole 8192-block cache, in one of two steps:
-    ``paged`` = paged decode attention (every sequence's query against its
-    blocks, through the block tables), ``paged_gather`` = gather_pa_kv_cache
-    into contiguous rows.  The two are separate steps: a decode step reads the
+    ``paged`` = one paged decode step (every sequence appends its new token
+    into its block, then its query attends over its blocks through the block
+    tables), ``paged_gather`` = gather_pa_kv_cache into contiguous rows.  The two are separate steps: a decode step reads the
     paged cache directly; the gather serves consumers of the contiguous layout
     (and, run right before the attention, would leave it a cache full of the
     gather's dirty lines to write back)."""
@@ -533,10 +533,16 @@ class PagedBench:
                               pw.seq_offset, pw.scale, out=self.out, workspace=self.ws,
                               dev_status=self.status)
 
+    def _append(self):
+        pw = self.pw
+        self.kvd.append_paged(pw.key_cache, pw.value_cache, pw.block_tables, pw.seq_offset,
+                              pw.k_new, pw.v_new, pw.pos, dev_status=self.status)
+
     def _step(self):
         if self.gather_mode:
             self._gather()
         else:
+            self._append()
             self._attend()
 
     def eager_run(self, j, timing=False):
@@ -546,11 +552,19 @@ class PagedBench:
         if not timing:
             self._step()
             return []
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        if self.gather_mode:
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            e[0].record()
+            self._gather()
+            e[1].record()
+            return [("attend", e[0], e[1])]
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         e[0].record()
-        self._step()
+        self._append()
         e[1].record()
-        return [("attend", e[0], e[1])]
+        self._attend()
+        e[2].record()
+        return [("append", e[0], e[1]), ("attend", e[1], e[2])]
 
     def capture(self):
         torch = self.torch
@@ -564,7 +578,7 @@ class PagedBench:
         self.graph.replay()
 
     def launches_per_step(self):
-        return 1 if self.gather_mode else self.attention_plan().launches
+        return 1 if self.gather_mode else 1 + self.attention_plan().launches
 
     def attend_bytes(self, j):
         """Algorithmic bytes of the step's main kernel."""
@@ -576,7 +590,9 @@ class PagedBench:
         return gather_bytes(self.lengths, self.Hkv, self.D, self.Hkv, self.D, self.elem, self.BS)
 
     def step_bytes(self, j):
-        return self.attend_bytes(j)
+        if self.gather_mode:
+            return self.attend_bytes(j)
+        return self.attend_bytes(j) + append_bytes(self.Q, self.Hkv, self.D, self.elem)
 
     def tokens_per_step(self):
         return 0 if self.gather_mode else self.Q
@@ -596,9 +612,11 @@ class PagedBench:
                          for t in (pw.block_tables, pw.seq_lens, pw.seq_offset)]
             self.h_st = torch.empty(1, dtype=torch.int32, pin_memory=True)
             return sum(t.numel() * 4 for t in self.h_in), 4
-        self.h_q = torch.empty(pw.q.shape, dtype=pw.q.dtype, pin_memory=True).copy_(pw.q.cpu())
+        self.h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
+                     for t in (pw.q, pw.k_new, pw.v_new, pw.pos)]
         self.h_out = torch.empty(pw.q.shape, dtype=pw.q.dtype, pin_memory=True)
-        return self.h_q.numel() * 2, self.h_out.numel() * 2
+        return (sum(t.numel() * t.element_size() for t in self.h_in),
+                self.h_out.numel() * self.h_out.element_size())
 
     def e2e_step(self, j):
         pw = self.pw
@@ -608,7 +626,9 @@ class PagedBench:
             self._gather()
             self.h_st.copy_(self.status, non_blocking=True)
             return
-        pw.q.copy_(self.h_q, non_blocking=True)
+        for d, h in zip((pw.q, pw.k_new, pw.v_new, pw.pos), self.h_in):
+            d.copy_(h, non_blocking=True)
+        self._append()
         self._attend()
         self.h_out.copy_(self.out, non_blocking=True)
 
@@ -623,16 +643,17 @@ class PagedBench:
                                      mode="paged")
 
     def aux_ops(self):
-        """The combine behind the paged attention (the gather step is one
-        launch)."""
+        """The paged append and the combine around the paged attention (the
+        gather step is one launch)."""
         if self.gather_mode:
             return {}
+        ops = {"append": lambda li: self._append()}
         plan = self.attention_plan()
         part = self.kvd.workspace_partials(self.ws, plan, self.Q * self.Hq, self.D)
         if part is not None and plan.launches > 1:
             po, pl = part
-            return {"combine": lambda li: self.kvd.combine(po, pl, out=self.out.view(-1, self.D))}
-        return {}
+            ops["combine"] = lambda li: self.kvd.combine(po, pl, out=self.out.view(-1, self.D))
+        return ops
 
     def config(self):
         return paged_config(self.pw, self.name)
@@ -1099,11 +1120,15 @@ def oracle_rate(name, seconds):
             return run(step, gather_bytes(lengths, 8, 128, 8, 128, 2, 128),
                        "gather of all 64 sequences")
 
+        kb = pw.key_cache.view(torch.int16).numpy()
+        vb = pw.value_cache.view(torch.int16).numpy()
+
         def step(n):
+            oracle.append_paged(kb, vb, pw.block_tables, pw.seq_offset, pw.k_new, pw.v_new, pw.pos)
             oracle.attend_paged(pw.q, pw.key_cache, pw.value_cache, pw.block_tables, pw.seq_lens,
                                 pw.seq_offset, pw.scale)
-        return run(step, paged_attend_bytes(lengths, 32, 8, 128, 2, 128),
-                   "paged attention of all 64 sequences")
+        return run(step, paged_attend_bytes(lengths, 32, 8, 128, 2, 128) + append_bytes(64, 8, 128, 2),
+                   "paged append + attention of all 64 sequences")
     if name == "indexed":
         w = workloads.gqa(device="cpu", layers=1)
         lay = w.layers[0]

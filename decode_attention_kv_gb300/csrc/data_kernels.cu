@@ -273,6 +273,68 @@ cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const
                       dev_status);
 }
 
+// ----------------------------------------------------------- append_paged
+// Paged KV append ("Intel NPU running LLMs", Part 2, update_kvcache_for, in
+// the paged layout of "PyPTO 实现 AscendC GatherPaKvCache" 3.2): token pos[q]
+// of sequence q goes to block block_tables[q, seq_offset[q] / BS + pos[q] /
+// BS], slot pos[q] % BS -- all Hkv x D of it, one contiguous row of the
+// [NB, BS, Hkv, D] cache.  Grid (16-byte vectors of a row / 256, Q).  The
+// checks follow the gather's order; a failing sequence writes nothing.
+__global__ void __launch_bounds__(256)
+append_paged_kernel(unsigned char* __restrict__ kc, unsigned char* __restrict__ vc,
+                    const unsigned char* __restrict__ kn, const unsigned char* __restrict__ vn,
+                    const int32_t* __restrict__ block_tables, const int32_t* __restrict__ seq_offset,
+                    const int32_t* __restrict__ pos, int NB, int BS, int cols, int row_bytes,
+                    int32_t* dev_status) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int q = blockIdx.y;
+    const bool reporter = blockIdx.x == 0 && threadIdx.x == 0;
+    const long long t = pos[q];
+    if (t < 0) {
+        if (reporter) report(dev_status, KVD_DEV_POS_RANGE);
+        return;
+    }
+    const long long off = seq_offset ? seq_offset[q] : 0;
+    if (off < 0 || off % BS) {
+        if (reporter) report(dev_status, KVD_DEV_SEQ_OFFSET);
+        return;
+    }
+    const long long col = off / BS + t / BS;
+    if (col >= cols) {
+        if (reporter) report(dev_status, KVD_DEV_TABLE_COLS);
+        return;
+    }
+    const long long phys = block_tables[(size_t)q * cols + col];
+    if (phys < 0 || phys >= NB) {
+        if (reporter) report(dev_status, KVD_DEV_BLOCK_RANGE);
+        return;
+    }
+    const int v = blockIdx.x * blockDim.x + threadIdx.x;
+    if (v < row_bytes / 16) {
+        const size_t src = (size_t)q * row_bytes + (size_t)v * 16;
+        const size_t dst = ((size_t)phys * BS + (size_t)(t % BS)) * row_bytes + (size_t)v * 16;
+        const uint4 kx = *reinterpret_cast<const uint4*>(kn + src);
+        const uint4 vx = *reinterpret_cast<const uint4*>(vn + src);
+        *reinterpret_cast<uint4*>(kc + dst) = kx;
+        *reinterpret_cast<uint4*>(vc + dst) = vx;
+    }
+}
+
+cudaError_t launch_append_paged(void* key_cache, void* value_cache, const void* k_new,
+                                const void* v_new, const int32_t* block_tables,
+                                const int32_t* seq_offset, const int32_t* pos, int Q, int NB,
+                                int BS, int cols, int row_bytes, int32_t* dev_status,
+                                cudaStream_t stream) {
+    const int nvec = row_bytes / 16;
+    const dim3 grid((nvec + 255) / 256, Q);
+    return launch_pdl(append_paged_kernel, grid, dim3(256), 0, stream,
+                      static_cast<unsigned char*>(key_cache), static_cast<unsigned char*>(value_cache),
+                      static_cast<const unsigned char*>(k_new),
+                      static_cast<const unsigned char*>(v_new), block_tables, seq_offset, pos, NB,
+                      BS, cols, row_bytes, dev_status);
+}
+
 // ------------------------------------------------------------- append_fp8
 // KV append into quantised caches: the step's K/V rows of every kv head are
 // quantised (amax = max |v|, scale = amax / 448, code = E4M3(v / scale), both

@@ -380,6 +380,33 @@ kvd_status kvd_append(void* k_cache, void* v_cache, const void* k_new, const voi
     return ok();
 }
 
+kvd_status kvd_append_paged(void* key_cache, void* value_cache, const void* k_new,
+                            const void* v_new, const int32_t* block_tables,
+                            const int32_t* seq_offset, const int32_t* pos, int Q, int NB, int BS,
+                            int cols, int Hkv, int D, kvd_dtype dtype, int32_t* dev_status,
+                            kvd_stream_t stream) {
+    const char* fn = "kvd_append_paged";
+    if (Q < 0 || NB < 1 || BS < 1 || cols < 1 || Hkv < 1 || D < 1)
+        return fail(KVD_ERR_INVALID_ARG, "%s: Q >= 0 and NB, BS, cols, Hkv, D >= 1 required", fn);
+    if (!dtype_ok(dtype)) return fail(KVD_ERR_INVALID_ARG, "%s: unknown dtype", fn);
+    if (Q == 0) return ok();
+    if (!key_cache || !value_cache || !k_new || !v_new || !block_tables || !pos)
+        return fail(KVD_ERR_INVALID_ARG, "%s: null pointer", fn);
+    const long long row = (long long)Hkv * D * elem_size(dtype);
+    if (row % 16) return fail(KVD_ERR_INVALID_ARG, "%s: Hkv*D*elem must be a multiple of 16 bytes", fn);
+    if (row >= (1ll << 31)) return fail(KVD_ERR_UNSUPPORTED, "%s: row too large", fn);
+    if (!aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(k_new, 16) ||
+        !aligned(v_new, 16) || !aligned(block_tables, 4) || !aligned(seq_offset, 4) ||
+        !aligned(pos, 4) || !aligned(dev_status, 4))
+        return fail(KVD_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+    if (Q > 65535) return fail(KVD_ERR_UNSUPPORTED, "%s: Q > 65535", fn);
+    const cudaError_t e = launch_append_paged(key_cache, value_cache, k_new, v_new, block_tables,
+                                              seq_offset, pos, Q, NB, BS, cols, (int)row,
+                                              dev_status, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kvd_append_paged launch");
+    return ok();
+}
+
 kvd_status kvd_copy_prefix(const void* const* k_src, const void* const* v_src, void* const* k_dst,
                            void* const* v_dst, uint8_t* const* masks, const int32_t* n, int L,
                            int B, int Hkv, int C_src, int C_dst, int D, kvd_dtype dtype,

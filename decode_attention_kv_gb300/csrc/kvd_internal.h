@@ -69,6 +69,12 @@ cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const
                           const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int row_bytes,
                           int32_t* dev_status, cudaStream_t stream);
 
+cudaError_t launch_append_paged(void* key_cache, void* value_cache, const void* k_new,
+                                const void* v_new, const int32_t* block_tables,
+                                const int32_t* seq_offset, const int32_t* pos, int Q, int NB,
+                                int BS, int cols, int row_bytes, int32_t* dev_status,
+                                cudaStream_t stream);
+
 cudaError_t launch_append_fp8(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                               const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
                               kvd_dtype in_dt, int32_t* dev_status, cudaStream_t stream);

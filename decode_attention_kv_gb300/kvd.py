@@ -56,6 +56,7 @@ SIGNATURES = {
     "kvd_attend_paged_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i, _i], _sz),
     "kvd_attend_paged": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
                           _i, _i, _vp, _sz, _vp, _vp], _i),
+    "kvd_append_paged": ([_vp] * 7 + [_i] * 7 + [_vp, _vp], _i),
     "kvd_gather_paged": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp] + [_i] * 10 + [_vp, _vp], _i),
     "kvd_combine": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
     "kvd_combine_gathered": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
@@ -590,6 +591,30 @@ def attend_paged(q, key_cache, value_cache, block_tables, seq_lens, seq_offset=N
 
 
 # ------------------------------------------------------------------ gather
+
+def append_paged(key_cache, value_cache, block_tables, seq_offset, k_new, v_new, pos,
+                 dev_status=None):
+    """kvd_append_paged: token pos[q] of every sequence q into the paged
+    caches [NB, BS, Hkv, D] (k_new, v_new [Q, Hkv, D], pos [Q] int32)."""
+    for n, t in (("key_cache", key_cache), ("value_cache", value_cache), ("k_new", k_new),
+                 ("v_new", v_new), ("block_tables", block_tables), ("pos", pos)):
+        _cuda_contig(n, t)
+    NB, BS, Hkv, D = key_cache.shape
+    Q, cols = block_tables.shape
+    if value_cache.shape != key_cache.shape or k_new.shape != (Q, Hkv, D) or \
+            v_new.shape != (Q, Hkv, D) or pos.numel() != Q:
+        raise ValueError("append_paged: shape mismatch")
+    if block_tables.dtype != torch.int32 or pos.dtype != torch.int32 or \
+            (seq_offset is not None and seq_offset.dtype != torch.int32):
+        raise ValueError("append_paged: int32 tables, offsets and positions")
+    if not (key_cache.dtype == value_cache.dtype == k_new.dtype == v_new.dtype):
+        raise TypeError("append_paged: caches and new rows must share a dtype")
+    st = load().kvd_append_paged(_ptr(key_cache), _ptr(value_cache), _ptr(k_new), _ptr(v_new),
+                                 _ptr(block_tables), _ptr(seq_offset), _ptr(pos), Q, NB, BS, cols,
+                                 Hkv, D, _dtype_code(key_cache), _ptr(dev_status),
+                                 _stream(key_cache.device))
+    _check("kvd_append_paged", st)
+
 
 def gather_paged(key_cache, value_cache, block_tables, seq_lens, seq_offset=None,
                  key_out=None, value_out=None, total_tokens=None, dev_status=None):

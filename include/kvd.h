@@ -387,6 +387,27 @@ kvd_status kvd_attend_paged(const void* q_in, const void* key_cache, const void*
                             size_t workspace_bytes, int32_t* dev_status, kvd_stream_t stream);
 
 /*
+ * kvd_append_paged -- the step's KV append ([NPU] Part 2, update_kvcache_for)
+ * into the paged cache, through the gather's index mapping ([PyPTO] 3.2):
+ * token pos[q] of sequence q is written to
+ *   key_cache[block_tables[q, seq_offset[q] / BS + pos[q] / BS], pos[q] % BS]
+ * (all Hkv x D of it; value_cache likewise), i.e. where kvd_gather_paged and
+ * kvd_attend_paged read token pos[q] of q once seq_lens counts it.
+ *   key_cache, value_cache [NB, BS, Hkv, D] of `dtype`
+ *   k_new, v_new [Q, Hkv, D] of `dtype`;  pos [Q] int32 (device)
+ *   block_tables [Q, cols] int32;  seq_offset [Q] int32 or NULL (zeros)
+ * A byte copy.  Device-detected errors skip that sequence (nothing written):
+ * pos[q] < 0 (KVD_DEV_POS_RANGE), seq_offset negative or not a multiple of
+ * BS (KVD_DEV_SEQ_OFFSET), table column past cols (KVD_DEV_TABLE_COLS), block
+ * id outside [0, NB) (KVD_DEV_BLOCK_RANGE).  The caller keeps seq_lens.
+ */
+kvd_status kvd_append_paged(void* key_cache, void* value_cache, const void* k_new,
+                            const void* v_new, const int32_t* block_tables,
+                            const int32_t* seq_offset, const int32_t* pos, int Q, int NB, int BS,
+                            int cols, int Hkv, int D, kvd_dtype dtype, int32_t* dev_status,
+                            kvd_stream_t stream);
+
+/*
  * kvd_gather_paged -- gather_pa_kv_cache, Norm/ND branch ([PyPTO] 3.2):
  * for every sequence q and t < seq_lens[q+1] - seq_lens[q]:
  *   phys = block_tables[q, seq_offset[q] / BS + t / BS]

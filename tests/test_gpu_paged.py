@@ -214,3 +214,76 @@ def test_paged_device_errors(kvd):
 
     out, lse, st = run(bt, sl, torch.tensor([0, 0, 48], dtype=torch.int32))
     assert st == kvd.DEV_TABLE_COLS and torch.all(out[2] == 0)
+
+
+APPEND_CASES = [
+    # dtype, NB, BS, Hkv, D, lengths (tokens before the step), cols, offsets (blocks)
+    (torch.bfloat16, 160, 128, 8, 128, [0, 127, 128, 1000, 4095], 32, None),
+    (torch.bfloat16, 50, 16, 2, 64, [5, 16, 31, 0], 6, [0, 1, 2, 4]),
+    (torch.float32, 48, 1, 3, 64, [0, 7, 12], 15, [2, 0, 1]),
+]
+
+
+@pytest.mark.parametrize("dtype,NB,BS,Hkv,D,lengths,cols,offs", APPEND_CASES)
+def test_append_paged_then_attend(kvd, dtype, NB, BS, Hkv, D, lengths, cols, offs):
+    """One paged decode step: every sequence appends its new token at its
+    current length (byte-exact against the oracle's append over the whole
+    caches), then paged attention runs over the one-token-longer sequences
+    (against the oracle's attention)."""
+    g = W.generator(8800 + NB + BS)
+    kc = W.randn(g, (NB, BS, Hkv, D), dtype)
+    vc = W.randn(g, (NB, BS, Hkv, D), dtype)
+    Q, Hq = len(lengths), 4 * Hkv
+    kn = W.randn(g, (Q, Hkv, D), dtype)
+    vn = W.randn(g, (Q, Hkv, D), dtype)
+    q = W.randn(g, (Q, Hq, D), dtype)
+    bt, _, off = _layout(7, Q, BS, cols, NB, lengths, offs)
+    pos = torch.tensor(lengths, dtype=torch.int32)
+    kd, vd = kc.cuda(), vc.cuda()
+    status = kvd.status_tensor()
+    kvd.append_paged(kd, vd, bt.cuda(), off.cuda(), kn.cuda(), vn.cuda(), pos.cuda(), status)
+    kh = _bytes(kc).reshape(NB, BS, Hkv, -1).copy()
+    vh = _bytes(vc).reshape(NB, BS, Hkv, -1).copy()
+    assert oracle.append_paged(kh, vh, bt, off, _bytes(kn).reshape(Q, Hkv, -1),
+                               _bytes(vn).reshape(Q, Hkv, -1), pos) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(_bytes(kd).reshape(kh.shape), kh), "append (K) not bit-exact"
+    assert np.array_equal(_bytes(vd).reshape(vh.shape), vh), "append (V) not bit-exact"
+    sl = W.cumsum_lengths([L + 1 for L in lengths])
+    lse = torch.empty(Q, Hq, device="cuda")
+    out = kvd.attend_paged(q.cuda(), kd, vd, bt.cuda(), sl.cuda(), off.cuda(), 1.0 / math.sqrt(D),
+                           lse=lse, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref, ref_lse = oracle.attend_paged(q, host(kd), host(vd), bt, sl, off, 1.0 / math.sqrt(D))
+    assert_attention_close(out, ref, dtype, "append then attend")
+    assert_lse_close(lse, ref_lse, "append then attend lse")
+
+
+def test_append_paged_device_errors(kvd):
+    """Each failing sequence writes nothing and sets its bit; the others are
+    appended (byte-exact against the oracle)."""
+    NB, BS, Hkv, D, cols = 16, 4, 2, 64, 3
+    g = W.generator(8900)
+    kc = W.randn(g, (NB, BS, Hkv, D))
+    vc = W.randn(g, (NB, BS, Hkv, D))
+    kn = W.randn(g, (5, Hkv, D))
+    vn = W.randn(g, (5, Hkv, D))
+    bt = torch.arange(15, dtype=torch.int32).reshape(5, 3)
+    bt[3, 0] = 99  # a block id out of range
+    off = torch.tensor([0, 4, 3, 0, 0], dtype=torch.int32)  # q2: not a multiple of BS
+    pos = torch.tensor([-1, 0, 0, 2, 12], dtype=torch.int32)  # q0 negative, q4 past the table
+    kd, vd = kc.cuda(), vc.cuda()
+    status = kvd.status_tensor()
+    kvd.append_paged(kd, vd, bt.cuda(), off.cuda(), kn.cuda(), vn.cuda(), pos.cuda(), status)
+    torch.cuda.synchronize()
+    kh = _bytes(kc).reshape(NB, BS, Hkv, -1).copy()
+    vh = _bytes(vc).reshape(NB, BS, Hkv, -1).copy()
+    err = oracle.append_paged(kh, vh, bt, off, _bytes(kn).reshape(5, Hkv, -1),
+                              _bytes(vn).reshape(5, Hkv, -1), pos)
+    assert err == oracle.ERR_POS | oracle.ERR_OFFSET | oracle.ERR_BLOCK | oracle.ERR_COLS
+    assert int(status.item()) == (kvd.DEV_POS_RANGE | kvd.DEV_SEQ_OFFSET |
+                                  kvd.DEV_BLOCK_RANGE | kvd.DEV_TABLE_COLS)
+    assert np.array_equal(_bytes(kd).reshape(kh.shape), kh)
+    assert np.array_equal(_bytes(vd).reshape(vh.shape), vh)

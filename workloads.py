@@ -25,8 +25,10 @@ Workloads (shapes and value distributions follow the pages' own examples):
                    block_tables [64, 32] = the first 2048 entries of a random
                    permutation of the 8192 physical blocks, 64 lengths uniform
                    in [1, 4096], seq_lens = their cumsum with a leading 0,
-                   seq_offset zeros, 32 query heads.  (Tensor contract of
-                   "PyPTO 实现 AscendC GatherPaKvCache", section 3.1.)
+                   seq_offset zeros, 32 query heads; the decode step's new
+                   K/V rows N(0,1), appended at each sequence's last token.
+                   (Tensor contract of "PyPTO 实现 AscendC GatherPaKvCache",
+                   section 3.1.)
 * ``long``      -- batch 1, 32 heads (MHA), head_dim 128, bf16, capacity =
                    valid length = 32768, 8 layer caches, N(0,1); one step
                    appends at 32767 and attends over all slots.
@@ -314,6 +316,9 @@ class PagedWorkload:
     lengths: torch.Tensor       # [Q] int64
     total_tokens: int
     scale: float
+    k_new: torch.Tensor = None  # [Q, Hkv, D]: the step's new rows (appended at pos)
+    v_new: torch.Tensor = None
+    pos: torch.Tensor = None    # [Q] int32 = lengths - 1: the last token of each sequence
 
 
 def paged(device="cpu", seed: int | None = None, NB: int = 8192, BS: int = 128,
@@ -331,8 +336,11 @@ def paged(device="cpu", seed: int | None = None, NB: int = 8192, BS: int = 128,
     kc = randn(g, (NB, BS, Hkv, D), dtype, device)
     vc = randn(g, (NB, BS, Hkv, D), dtype, device)
     q = randn(g, (Q, Hq, D), dtype, device)
+    k_new = randn(g, (Q, Hkv, D), dtype, device)
+    v_new = randn(g, (Q, Hkv, D), dtype, device)
     return PagedWorkload(q=q, key_cache=kc, value_cache=vc, block_tables=bt.to(device),
                          seq_lens=sl.to(device),
                          seq_offset=torch.zeros(Q, dtype=torch.int32, device=device),
                          lengths=lengths, total_tokens=int(sl[-1]),
-                         scale=1.0 / math.sqrt(D))
+                         scale=1.0 / math.sqrt(D), k_new=k_new, v_new=v_new,
+                         pos=(lengths - 1).to(torch.int32).to(device))
