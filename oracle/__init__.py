@@ -25,6 +25,10 @@ Every function states what it computes and the page section it follows:
   token side by side); the scale encoding is this package's reading: one fp32
   absmax/448 scale per row, after the row's E4M3 codes, rows padded to D + 16
   bytes.
+* ``e2m1_codes``, ``e2m1_values``, ``quantize_rows_fp4``, ``append_fp4``,
+  ``attend_masked_fp4`` -- the FP4 rows the same section names beside FP8:
+  E2M1 codes two per byte (element 2j in the low nibble of byte j), one fp32
+  absmax/6 scale per row after them, rows padded to D/2 + 16 bytes.
 * ``combine`` -- the log-sum-exp merge of disjoint key ranges (Part 3, "Flash
   SDPA 路径": tiles merged exactly through running max and sum).
 """
@@ -100,6 +104,12 @@ def lib() -> ctypes.CDLL:
             L.kvd_oracle_quantize_rows.argtypes = [vp, ci, cl, ci, u8p]
             L.kvd_oracle_append_fp8.argtypes = [u8p, u8p, vp, vp, ci, i32p, u8p, ci, ci, ci, ci]
             L.kvd_oracle_attend_masked_fp8.argtypes = [vp, ci, u8p, u8p, u8p, ci, ci, ci, ci, ci,
+                                                       cd, dp, dp, ci]
+            L.kvd_oracle_e2m1_codes.argtypes = [ctypes.POINTER(ctypes.c_float), cl, u8p]
+            L.kvd_oracle_e2m1_values.argtypes = [u8p, cl, dp]
+            L.kvd_oracle_quantize_rows_fp4.argtypes = [vp, ci, cl, ci, u8p]
+            L.kvd_oracle_append_fp4.argtypes = [u8p, u8p, vp, vp, ci, i32p, u8p, ci, ci, ci, ci]
+            L.kvd_oracle_attend_masked_fp4.argtypes = [vp, ci, u8p, u8p, u8p, ci, ci, ci, ci, ci,
                                                        cd, dp, dp, ci]
             for f in (L.kvd_oracle_attend_masked, L.kvd_oracle_append, L.kvd_oracle_copy_prefix,
                       L.kvd_oracle_attend_indexed,
@@ -469,4 +479,91 @@ def attend_masked_fp8(q, k_rows, v_rows, mask, scale: float, nthreads: int = 0):
                                             _p(lse, ctypes.c_double), int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle attend_masked_fp8 failed ({rc})")
+    return out, lse
+
+
+# ------------------------------------------------------------ FP4 rows
+
+def e2m1_codes(x) -> np.ndarray:
+    """float32 values -> E2M1 codes 0..15 (nearest, ties to the even code,
+    saturating at 6; NaN -> +6)."""
+    xa = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.zeros(xa.shape, np.uint8)
+    lib().kvd_oracle_e2m1_codes(_p(xa, ctypes.c_float), xa.size, _p(out, ctypes.c_uint8))
+    return out
+
+
+def e2m1_values(codes) -> np.ndarray:
+    """E2M1 codes 0..15 -> their values (float64)."""
+    ca = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.zeros(ca.shape, np.float64)
+    lib().kvd_oracle_e2m1_values(_p(ca, ctypes.c_uint8), ca.size, _p(out, ctypes.c_double))
+    return out
+
+
+def quantize_rows_fp4(x) -> np.ndarray:
+    """Rows [..., D] (bf16 or fp32) -> FP4 rows uint8 [..., D/2 + 16]."""
+    xa, dt = _storage(x)
+    D = xa.shape[-1]
+    rows = xa.size // D
+    out = np.zeros(xa.shape[:-1] + (D // 2 + FP8_ROW_PAD,), np.uint8)
+    rc = lib().kvd_oracle_quantize_rows_fp4(_p(xa), dt, rows, D, _p(out, ctypes.c_uint8))
+    if rc != 0:
+        raise RuntimeError("oracle quantize_rows_fp4 failed")
+    return out
+
+
+def dequantize_rows_fp4(rows) -> np.ndarray:
+    """FP4 rows uint8 [..., D/2 + 16] -> float64 [..., D] (scale * value)."""
+    ra = np.ascontiguousarray(rows, dtype=np.uint8)
+    half = ra.shape[-1] - FP8_ROW_PAD
+    scale = ra[..., half:half + 4].copy().view("<f4")[..., 0].astype(np.float64)
+    codes = np.stack([ra[..., :half] & 0xF, ra[..., :half] >> 4], axis=-1).reshape(
+        ra.shape[:-1] + (2 * half,))
+    return e2m1_values(codes) * scale[..., None]
+
+
+def append_fp4(k_cache, v_cache, k_new, v_new, pos, mask=None) -> int:
+    """Append into FP4 caches in place: k_cache, v_cache uint8 numpy
+    [B, Hkv, C, D/2 + 16]; k_new, v_new [B, Hkv, D] (bf16 or fp32); pos [B];
+    mask [B, C] uint8 numpy or None.  Returns error bits."""
+    for a in (k_cache, v_cache):
+        if not (isinstance(a, np.ndarray) and a.dtype == np.uint8 and a.flags.c_contiguous):
+            raise TypeError("oracle.append_fp4 works in place on contiguous uint8 numpy arrays")
+    B, Hkv, C, RB = k_cache.shape
+    D = 2 * (RB - FP8_ROW_PAD)
+    kn, dk = _storage(k_new)
+    vn, dv = _storage(v_new)
+    if dk != dv or kn.size != B * Hkv * D or vn.size != kn.size:
+        raise ValueError("oracle.append_fp4: new rows have the wrong size or types")
+    p = _i32(pos)
+    mp = None
+    if mask is not None:
+        if not (isinstance(mask, np.ndarray) and mask.dtype == np.uint8 and mask.flags.c_contiguous):
+            raise TypeError("oracle.append_fp4: mask must be a contiguous uint8 numpy array")
+        mp = _p(mask, ctypes.c_uint8)
+    return lib().kvd_oracle_append_fp4(_p(k_cache, ctypes.c_uint8), _p(v_cache, ctypes.c_uint8),
+                                       _p(kn), _p(vn), dk, _p(p, ctypes.c_int32), mp, B, Hkv, C, D)
+
+
+def attend_masked_fp4(q, k_rows, v_rows, mask, scale: float, nthreads: int = 0):
+    """Masked decode attention over FP4 K/V rows, fp64: q [B, Hq, D] (bf16 or
+    fp32); k_rows, v_rows uint8 [B, Hkv, C, D/2 + 16]; mask [B, C].
+    Returns (out [B, Hq, D], lse [B, Hq])."""
+    qa, dt = _storage(q)
+    ka = np.ascontiguousarray(_u8(k_rows))
+    va = np.ascontiguousarray(_u8(v_rows))
+    B, Hq, D = qa.shape
+    _, Hkv, C, RB = ka.shape
+    if RB != D // 2 + FP8_ROW_PAD or va.shape != ka.shape:
+        raise ValueError("oracle: shape mismatch")
+    m = _u8(mask).reshape(B, C) if C > 0 else np.zeros((B, 1), np.uint8)
+    out = np.zeros((B, Hq, D), np.float64)
+    lse = np.zeros((B, Hq), np.float64)
+    rc = lib().kvd_oracle_attend_masked_fp4(_p(qa), dt, _p(ka, ctypes.c_uint8),
+                                            _p(va, ctypes.c_uint8), _p(m, ctypes.c_uint8), B, Hq,
+                                            Hkv, C, D, float(scale), _p(out, ctypes.c_double),
+                                            _p(lse, ctypes.c_double), int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle attend_masked_fp4 failed ({rc})")
     return out, lse

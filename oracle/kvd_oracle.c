@@ -32,6 +32,9 @@
  *             by side).  The scale granularity and encoding are not given;
  *             the reading taken here is one fp32 scale per token row of a kv
  *             head (absmax / 448), stored right after the row's E4M3 codes.
+ *             The same page names FP4 beside FP8: E2M1 codes (OCP 4-bit
+ *             floating point), two per byte (element 2j in the low nibble of
+ *             byte j), one fp32 scale per row (absmax / 6) after them.
  *  [PyPTO]    "PyPTO 实现 AscendC GatherPaKvCache（Norm/ND 分支）", sections
  *             3.1 (tensor contract), 3.2 (gather semantics: logical_block =
  *             t // block_size, slot = t % block_size, physical_block =
@@ -54,6 +57,7 @@
 #define ORC_BF16 0
 #define ORC_F32 1
 #define ORC_FP8ROW 2 /* K/V only: rows of D E4M3 codes + fp32 scale + 12 zero bytes */
+#define ORC_FP4ROW 3 /* K/V only: rows of D/2 bytes of E2M1 codes + fp32 scale + 12 zero bytes */
 
 /* error bits reported by the data-movement oracles (own numbering) */
 #define ORC_ERR_POS 1        /* append position outside [0, capacity) */
@@ -115,6 +119,40 @@ static uint8_t orc_e4m3_code(float x) {
     return sign | (uint8_t)(E << 3) | (uint8_t)f;
 }
 
+/* ------------------------------------------------------------ E2M1 codes
+ * OCP 4-bit floating point, E2M1: 1 sign bit, 2 exponent bits with bias 1,
+ * 1 mantissa bit; exponent 0 is subnormal (m * 0.5).  The magnitudes are 0,
+ * 0.5, 1, 1.5, 2, 3, 4, 6; there is no infinity or NaN. */
+static double orc_e2m1_value(uint8_t c) {
+    const double sign = (c & 0x8) ? -1.0 : 1.0;
+    const int e = (c >> 1) & 0x3, m = c & 0x1;
+    if (e == 0) return sign * 0.5 * m;
+    return sign * ldexp(1.0 + 0.5 * m, e - 1);
+}
+
+/* Nearest E2M1 value of x, ties to the even code (mantissa bit 0),
+ * magnitudes from 6 up saturating to 6; NaN gives +6 (this reading follows
+ * the saturating conversion's rule for NaN inputs). */
+static uint8_t orc_e2m1_code(float x) {
+    if (isnan(x)) return 0x7;
+    const uint8_t sign = signbit(x) ? 0x8 : 0;
+    const double a = fabs((double)x);
+    if (a >= 6.0) return sign | 0x7;
+    /* spacing: 0.5 below 2 (subnormals and [1, 2)), then 2^(e - 1) in [2^e, 2^(e+1)) */
+    double step = 0.5;
+    if (a >= 2.0) {
+        int ex;
+        frexp(a, &ex); /* a in [2^(ex-1), 2^ex) */
+        step = ldexp(1.0, ex - 2);
+    }
+    const double val = nearbyint(a / step) * step; /* exact quotient; ties to even */
+    /* the grid's magnitudes in code order */
+    static const double grid[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    for (int i = 0; i < 8; ++i)
+        if (val == grid[i]) return sign | (uint8_t)i;
+    return sign | 0x7; /* val == 6 after rounding up from (5, 6) */
+}
+
 /* fp32 scale of a quantised row (bytes D..D+3, little-endian). */
 static float orc_row_scale(const uint8_t* row, int D) {
     const uint32_t u = (uint32_t)row[D] | ((uint32_t)row[D + 1] << 8) |
@@ -129,6 +167,11 @@ static double orc_kv(const void* base, size_t row, int d, int kvtype, int D) {
     if (kvtype == ORC_FP8ROW) {
         const uint8_t* r = (const uint8_t*)base + row * (size_t)(D + 16);
         return (double)orc_row_scale(r, D) * orc_e4m3_value(r[d]);
+    }
+    if (kvtype == ORC_FP4ROW) {
+        const uint8_t* r = (const uint8_t*)base + row * (size_t)(D / 2 + 16);
+        const uint8_t code = (uint8_t)((r[d / 2] >> (4 * (d & 1))) & 0xF);
+        return (double)orc_row_scale(r, D / 2) * orc_e2m1_value(code);
     }
     return orc_elem(base, row * (size_t)D + d, kvtype);
 }
@@ -155,6 +198,49 @@ static void orc_quantize_row(const void* src, size_t row, int dtype, int D, uint
     memcpy(&u, &scale, sizeof u);
     for (int i = 0; i < 4; ++i) dst[D + i] = (uint8_t)(u >> (8 * i));
     memset(dst + D + 4, 0, 12);
+}
+
+/*
+ * FP4 row quantisation ([FlashMLA-KV], FP4 reading above): for each row of D
+ * values, amax = max |v_d|, scale = amax / 6 and code_d = E2M1(v_d / scale),
+ * both divisions in fp32 with round-to-nearest; a row of zeros gets scale 0
+ * and zero codes.  dst rows: D/2 bytes of codes (element 2j in the low
+ * nibble of byte j), the scale's 4 bytes (little-endian), 12 zero bytes.
+ */
+static void orc_quantize_row_fp4(const void* src, size_t row, int dtype, int D, uint8_t* dst) {
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        const float a = fabsf((float)orc_elem(src, row * (size_t)D + d, dtype));
+        if (a > amax) amax = a;
+    }
+    const float scale = amax / 6.0f;
+    memset(dst, 0, (size_t)D / 2);
+    for (int d = 0; d < D; ++d) {
+        const float v = (float)orc_elem(src, row * (size_t)D + d, dtype);
+        const uint8_t c = scale > 0.0f ? orc_e2m1_code(v / scale) : 0;
+        dst[d / 2] |= (uint8_t)(c << (4 * (d & 1)));
+    }
+    uint32_t u;
+    memcpy(&u, &scale, sizeof u);
+    for (int i = 0; i < 4; ++i) dst[D / 2 + i] = (uint8_t)(u >> (8 * i));
+    memset(dst + D / 2 + 4, 0, 12);
+}
+
+int kvd_oracle_quantize_rows_fp4(const void* src, int dtype, long rows, int D, uint8_t* dst) {
+    if (rows < 0 || D <= 0 || D % 2) return -1;
+    for (long r = 0; r < rows; ++r)
+        orc_quantize_row_fp4(src, (size_t)r, dtype, D, dst + (size_t)r * (D / 2 + 16));
+    return 0;
+}
+
+int kvd_oracle_e2m1_codes(const float* x, long n, uint8_t* out) {
+    for (long i = 0; i < n; ++i) out[i] = orc_e2m1_code(x[i]);
+    return 0;
+}
+
+int kvd_oracle_e2m1_values(const uint8_t* c, long n, double* out) {
+    for (long i = 0; i < n; ++i) out[i] = orc_e2m1_value(c[i]);
+    return 0;
 }
 
 int kvd_oracle_quantize_rows(const void* src, int dtype, long rows, int D, uint8_t* dst) {
@@ -274,6 +360,17 @@ int kvd_oracle_attend_masked_fp8(const void* q, int qtype, const uint8_t* k, con
                                  const uint8_t* mask, int B, int Hq, int Hkv, int C, int D,
                                  double scale, double* out, double* lse, int nthreads) {
     return orc_attend_masked(q, qtype, k, v, ORC_FP8ROW, mask, B, Hq, Hkv, C, D, scale, out, lse,
+                             nthreads);
+}
+
+/*
+ * The same masked attention over FP4 rows (E2M1 codes + fp32 row scale):
+ * every K/V element is scale_row * E2M1(code), exactly, in double.
+ */
+int kvd_oracle_attend_masked_fp4(const void* q, int qtype, const uint8_t* k, const uint8_t* v,
+                                 const uint8_t* mask, int B, int Hq, int Hkv, int C, int D,
+                                 double scale, double* out, double* lse, int nthreads) {
+    return orc_attend_masked(q, qtype, k, v, ORC_FP4ROW, mask, B, Hq, Hkv, C, D, scale, out, lse,
                              nthreads);
 }
 
@@ -408,6 +505,33 @@ int kvd_oracle_append_fp8(uint8_t* k_cache, uint8_t* v_cache, const void* k_new,
             const size_t dst = (((size_t)b * Hkv + h) * C + p) * rb;
             orc_quantize_row(k_new, (size_t)b * Hkv + h, dtype, D, k_cache + dst);
             orc_quantize_row(v_new, (size_t)b * Hkv + h, dtype, D, v_cache + dst);
+        }
+        if (mask) mask[(size_t)b * C + p] = 1;
+    }
+    return err;
+}
+
+/*
+ * KV append into FP4 caches: row pos[b] of every kv head of k_cache /
+ * v_cache [B, Hkv, C, D/2 + 16] bytes becomes the FP4-quantised k_new / v_new
+ * [B, Hkv, D] (dtype); mask slot pos[b] becomes 1.  A position outside
+ * [0, C) writes nothing for that entry and sets ORC_ERR_POS.
+ */
+int kvd_oracle_append_fp4(uint8_t* k_cache, uint8_t* v_cache, const void* k_new,
+                          const void* v_new, int dtype, const int32_t* pos, uint8_t* mask,
+                          int B, int Hkv, int C, int D) {
+    int err = 0;
+    const size_t rb = (size_t)D / 2 + 16;
+    for (int b = 0; b < B; ++b) {
+        const int p = pos[b];
+        if (p < 0 || p >= C) {
+            err |= ORC_ERR_POS;
+            continue;
+        }
+        for (int h = 0; h < Hkv; ++h) {
+            const size_t dst = (((size_t)b * Hkv + h) * C + p) * rb;
+            orc_quantize_row_fp4(k_new, (size_t)b * Hkv + h, dtype, D, k_cache + dst);
+            orc_quantize_row_fp4(v_new, (size_t)b * Hkv + h, dtype, D, v_cache + dst);
         }
         if (mask) mask[(size_t)b * C + p] = 1;
     }
