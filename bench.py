@@ -3,7 +3,7 @@
 decode tokens/s on GB300, through libkvd's C ABI.
 
     python bench.py [--gpus N] [--steps K] [--warmup W]
-                    [--workload gqa|long|paged|npuw|indexed|window|gqa_fp8]
+                    [--workload gqa|long|paged|paged_gather|npuw|indexed|window|gqa_fp8|gqa_fp4]
     python bench.py --impl reference ...     # the fp64 CPU oracle as the reference arm
 
 A step is one decode step of the workload: for the static-buffer workloads,
@@ -86,16 +86,17 @@ def gather_bytes(lengths, Hk, Dk, Hv, Dv, elem, BS):
     return 2 * T * (Hk * Dk + Hv * Dv) * elem + entries * 4 + (Q + 1) * 4
 
 
-def fp8_attend_bytes(lengths, Hq, Hkv, C, D, pad):
-    """Valid quantised K and V rows (D codes + fp32 scale + zero pad, D + pad
-    bytes each), the mask row, bf16 q and out."""
+def quant_attend_bytes(lengths, Hq, Hkv, C, D, row):
+    """Valid quantised K and V rows (codes + fp32 scale + zero pad, `row`
+    bytes each: D + 16 for E4M3, D/2 + 16 for E2M1), the mask row, bf16 q
+    and out."""
     B = len(lengths)
-    return (sum(int(L) for L in lengths) * Hkv * (D + pad) * 2 + B * C + 2 * B * Hq * D * 2)
+    return (sum(int(L) for L in lengths) * Hkv * row * 2 + B * C + 2 * B * Hq * D * 2)
 
 
-def fp8_append_bytes(B, Hkv, D, pad):
+def quant_append_bytes(B, Hkv, D, row):
     """bf16 new K and V rows read, their quantised rows written."""
-    return 2 * B * Hkv * (D * 2 + D + pad)
+    return 2 * B * Hkv * (D * 2 + row)
 
 
 def indexed_attend_bytes(listed, topk, Hq, Hkv, D, elem):
@@ -204,7 +205,8 @@ def bus_id_of(torch, dev):
 # ---------------------------------------------------------------- workloads
 
 # Layer caches of each static-buffer workload (the workload generators' defaults).
-LAYERS = {"npuw": 32, "gqa": 32, "long": 8, "window": 8, "gqa_fp8": 32, "indexed": 32}
+LAYERS = {"npuw": 32, "gqa": 32, "long": 8, "window": 8, "gqa_fp8": 32, "gqa_fp4": 32,
+          "indexed": 32}
 
 
 def masked_config(name, w, layers, lengths0):
@@ -227,11 +229,12 @@ def masked_config(name, w, layers, lengths0):
         listed = [min(IndexedBench.TOPK, x) for x in L]
         c.update({"topk": IndexedBench.TOPK,
                   "listed_per_entry": {"min": min(listed), "max": max(listed)}})
-    if name == "gqa_fp8":
-        row = w.D + FP8_ROW_PAD
+    if name in QUANT_FORMATS:
+        fmt = QUANT_FORMATS[name]
+        row = quant_row_bytes(name, w.D)
         cache = layers * 2 * w.B * w.Hkv * w.C * row
-        c.update({"dtype": "e4m3 K/V, bf16 q/out",
-                  "kv_format": f"E4M3 codes + fp32 row scale, {row}-byte rows",
+        c.update({"dtype": f"{fmt.lower()} K/V, bf16 q/out",
+                  "kv_format": f"{fmt} codes + fp32 row scale, {row}-byte rows",
                   "l2": f"inputs larger than L2: {cache / 2**30:.2f} GiB of layer caches "
                         f"rotated per step vs {L2_BYTES // 2**20} MiB L2"})
     return c
@@ -261,7 +264,14 @@ def workload_config(name):
     return masked_config(name, w, LAYERS[name], [int(x) for x in w.layers[0].lengths])
 
 
-FP8_ROW_PAD = 16  # quantised rows: D codes, fp32 scale, 12 zero bytes
+ROW_PAD = 16  # quantised rows: codes, fp32 scale, 12 zero bytes
+QUANT_FORMATS = {"gqa_fp8": "E4M3", "gqa_fp4": "E2M1"}
+
+
+def quant_row_bytes(name, D):
+    """Bytes of one quantised K/V row: D E4M3 codes or D/2 bytes of E2M1
+    code pairs, then the 16-byte scale field."""
+    return (D if name == "gqa_fp8" else D // 2) + ROW_PAD
 
 
 def attention_kernel_name(kind, plan, g, mode="masked", fused=False):
@@ -298,8 +308,8 @@ class MaskedBench:
         elif name == "window":
             w = workloads.window(device=dev, **kw)
             self.cycle, self.prompt = 1, None
-        elif name == "gqa_fp8":
-            w = workloads.gqa_fp8(device=dev, **kw)
+        elif name in ("gqa_fp8", "gqa_fp4"):
+            w = getattr(workloads, name)(device=dev, **kw)
             self.cycle, self.prompt = 1, None
         else:
             raise ValueError(name)
@@ -735,70 +745,74 @@ class IndexedBench(MaskedBench):
         return masked_config("indexed", self.w, self.layers, self.lengths0)
 
 
-class Fp8Bench(MaskedBench):
-    """The batched-GQA step over quantised caches (rows of 128 E4M3 codes +
-    fp32 scale + 12 zero bytes): every layer quantises and appends the step's
-    bf16 K/V rows, then attends over the quantised rows."""
+class QuantBench(MaskedBench):
+    """The batched-GQA step over quantised caches (rows of 128 E4M3 codes, or
+    64 bytes of E2M1 code pairs, + fp32 scale + 12 zero bytes): every layer
+    quantises and appends the step's bf16 K/V rows, then attends over the
+    quantised rows."""
 
-    def __init__(self, torch, kvd, dev, layers=None):
-        super().__init__("gqa_fp8", torch, kvd, dev, layers)
-        self.row = self.D + kvd.FP8_ROW_PAD
-        need = kvd.attend_masked_fp8_workspace_bytes(self.B, self.Hq, self.Hkv, self.C, self.D)
+    def __init__(self, name, torch, kvd, dev, layers=None):
+        super().__init__(name, torch, kvd, dev, layers)
+        self.fmt = "fp8" if name == "gqa_fp8" else "fp4"
+        self.row = quant_row_bytes(name, self.D)
+        self.append_fn = getattr(kvd, f"append_{self.fmt}")
+        self.attend_fn = getattr(kvd, f"attend_masked_{self.fmt}")
+        need = getattr(kvd, f"attend_masked_{self.fmt}_workspace_bytes")(
+            self.B, self.Hq, self.Hkv, self.C, self.D)
         self.ws = kvd.workspace(need, dev)
 
     def _layer(self, li, lay, pos):
-        self.kvd.append_fp8(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, pos, lay.mask,
-                            self.status)
-        self.kvd.attend_masked_fp8(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale,
-                                   out=self.out[li], workspace=self.ws, dev_status=self.status)
+        self.append_fn(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, pos, lay.mask, self.status)
+        self.attend_fn(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale, out=self.out[li],
+                       workspace=self.ws, dev_status=self.status)
 
     def eager_run(self, j, timing=False):
-        torch, kvd = self.torch, self.kvd
+        torch = self.torch
         pos = self.pos_table[j % self.cycle]
         evs = []
         for li, lay in enumerate(self.w.layers):
             if timing:
                 e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
                 e[0].record()
-            kvd.append_fp8(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, pos, lay.mask,
+            self.append_fn(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, pos, lay.mask,
                            self.status)
             if timing:
                 e[1].record()
-            kvd.attend_masked_fp8(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale,
-                                  out=self.out[li], workspace=self.ws, dev_status=self.status)
+            self.attend_fn(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale,
+                           out=self.out[li], workspace=self.ws, dev_status=self.status)
             if timing:
                 e[2].record()
                 evs += [("append", e[0], e[1]), ("attend", e[1], e[2])]
         return evs
 
     def launches_per_step(self):
-        return self.layers * (1 + self.attention_plan().launches)  # append_fp8, attention (+ combine)
+        return self.layers * (1 + self.attention_plan().launches)  # append, attention (+ combine)
 
     def attend_bytes(self, j):
-        return fp8_attend_bytes(self.lengths_at(j), self.Hq, self.Hkv, self.C, self.D,
-                                self.kvd.FP8_ROW_PAD)
+        return quant_attend_bytes(self.lengths_at(j), self.Hq, self.Hkv, self.C, self.D, self.row)
 
     def step_bytes(self, j):
         """Attention plus the append of the step's rows."""
-        app = fp8_append_bytes(self.B, self.Hkv, self.D, self.kvd.FP8_ROW_PAD)
+        app = quant_append_bytes(self.B, self.Hkv, self.D, self.row)
         return self.layers * (self.attend_bytes(j) + app)
 
     def copy_setup(self):
         return False
 
     def attention_plan(self):
-        return self.kvd.attend_masked_fp8_plan(self.B, self.Hq, self.Hkv, self.C, self.D)
+        return getattr(self.kvd, f"attend_masked_{self.fmt}_plan")(self.B, self.Hq, self.Hkv,
+                                                                   self.C, self.D)
 
     def kernel_name(self):
-        return attention_kernel_name("E4M3 tensor-core", self.attention_plan(),
-                                     self.Hq // self.Hkv)
+        return attention_kernel_name(f"{QUANT_FORMATS[self.name]} tensor-core",
+                                     self.attention_plan(), self.Hq // self.Hkv)
 
     def aux_ops(self):
         """The quantising append kernel and the combine."""
         lays = self.w.layers
-        ops = {"append": lambda li: self.kvd.append_fp8(lays[li].k_cache, lays[li].v_cache,
-                                                        lays[li].k_new, lays[li].v_new,
-                                                        self.gpos, lays[li].mask, self.status)}
+        ops = {"append": lambda li: self.append_fn(lays[li].k_cache, lays[li].v_cache,
+                                                   lays[li].k_new, lays[li].v_new, self.gpos,
+                                                   lays[li].mask, self.status)}
         plan = self.attention_plan()
         part = self.kvd.workspace_partials(self.ws, plan, self.B * self.Hq, self.D)
         if part is not None and plan.launches > 1:
@@ -807,14 +821,14 @@ class Fp8Bench(MaskedBench):
         return ops
 
     def config(self):
-        return masked_config("gqa_fp8", self.w, self.layers, self.lengths0)
+        return masked_config(self.name, self.w, self.layers, self.lengths0)
 
 
 def make_bench(name, torch, kvd, dev, layers=None):
     if name in ("paged", "paged_gather"):
         return PagedBench(torch, kvd, dev, name)
-    if name == "gqa_fp8":
-        return Fp8Bench(torch, kvd, dev, layers)
+    if name in QUANT_FORMATS:
+        return QuantBench(name, torch, kvd, dev, layers)
     if name == "indexed":
         return IndexedBench(torch, kvd, dev, layers)
     return MaskedBench(name, torch, kvd, dev, layers)
@@ -1144,18 +1158,21 @@ def oracle_rate(name, seconds):
             oracle.attend_indexed(lay.q, torch.from_numpy(kh).view(torch.bfloat16),
                                   torch.from_numpy(vh).view(torch.bfloat16), idx, lay.scale)
         return run(step, per, f"append + index-list attention, top-{topk}")
-    if name == "gqa_fp8":
-        w = workloads.gqa_fp8(device="cpu", layers=1)
+    if name in QUANT_FORMATS:
+        w = getattr(workloads, name)(device="cpu", layers=1)
         lay = w.layers[0]
         kh, vh, mh = lay.k_cache.numpy().copy(), lay.v_cache.numpy().copy(), lay.mask.numpy().copy()
         L = [int(x) for x in lay.lengths]
-        per = (fp8_attend_bytes(L, w.Hq, w.Hkv, w.C, w.D, oracle.FP8_ROW_PAD)
-               + fp8_append_bytes(w.B, w.Hkv, w.D, oracle.FP8_ROW_PAD))
+        row = quant_row_bytes(name, w.D)
+        per = (quant_attend_bytes(L, w.Hq, w.Hkv, w.C, w.D, row)
+               + quant_append_bytes(w.B, w.Hkv, w.D, row))
+        fmt = "fp8" if name == "gqa_fp8" else "fp4"
+        append, attend = getattr(oracle, f"append_{fmt}"), getattr(oracle, f"attend_masked_{fmt}")
 
         def step(n):
-            oracle.append_fp8(kh, vh, lay.k_new, lay.v_new, lay.pos, mh)
-            oracle.attend_masked_fp8(lay.q, kh, vh, mh, lay.scale)
-        return run(step, per, "quantising append + attention")
+            append(kh, vh, lay.k_new, lay.v_new, lay.pos, mh)
+            attend(lay.q, kh, vh, mh, lay.scale)
+        return run(step, per, f"{QUANT_FORMATS[name]} quantising append + attention")
     w = getattr(workloads, name)(device="cpu", layers=4 if name == "npuw" else 1)
     caches = [(l.k_cache.view(torch.int16).numpy().copy(), l.v_cache.view(torch.int16).numpy().copy(),
                l.mask.numpy().copy()) for l in w.layers]
@@ -1215,7 +1232,7 @@ def main():
     ap.add_argument("--impl", default="kvd", choices=["kvd", "reference"])
     ap.add_argument("--workload", default="gqa",
                     choices=["gqa", "long", "paged", "paged_gather", "npuw", "indexed", "window",
-                             "gqa_fp8"])
+                             "gqa_fp8", "gqa_fp4"])
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="oracle seconds for the main workload's CPU baseline")
@@ -1315,7 +1332,7 @@ def main():
     others = {}
     if not args.no_others:
         for name in ("long", "paged", "paged_gather", "npuw", "gqa", "indexed", "window",
-                     "gqa_fp8"):
+                     "gqa_fp8", "gqa_fp4"):
             if name == args.workload:
                 continue
             log(f"workload {name}")
@@ -1341,7 +1358,8 @@ def main():
             "metric": METRIC, "value": res["gbs"], "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if args.workload != "gqa_fp8" else "e4m3 kv / bf16",
+            "dtype": ("bf16" if args.workload not in QUANT_FORMATS
+                      else f"{QUANT_FORMATS[args.workload].lower()} kv / bf16"),
             "data": "synthetic", "config": b.config(),
             "peak_source": peak_src,
             "timing": "each timed step is one CUDA-graph replay of the decode step "

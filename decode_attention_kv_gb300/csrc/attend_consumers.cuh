@@ -380,18 +380,25 @@ struct MmaConsumer {
 //    the softmax's: when it grows, the output is rescaled by an exact power
 //    of two), so the f16 weights stay within 2 * e^6 and keep 11 bits; the
 //    output is multiplied by 2^ve at the end.
-template <int D, int G, int T, int NCW>
-struct Fp8MmaConsumer {
+// FP4 rows (kFp4): D/2 bytes of E2M1 codes (element 2j in the low nibble of
+// byte j) + fp32 scale + 12 zero bytes.  The same dims-to-lanes order: a
+// lane's K codes are D/8 consecutive bytes (two codes per byte, one byte per
+// two dims of a k-step), its V codes D/16 bytes; for V the codes of the two
+// tokens that share an f16x2 fragment register are interleaved nibble-wise
+// before the E2M1 -> f16 conversion (exact).
+template <int D, int G, int T, int NCW, bool kFp4>
+struct QuantMmaConsumer {
     using ElemT = __nv_bfloat16;  // q and out
     static constexpr bool kSwizzled = false;
     static constexpr int kD = D, kG = G, kT = T, kNCW = NCW;
-    static constexpr int kRowBytes = D + 16;
+    static constexpr int kCodeBytes = kFp4 ? D / 2 : D;  // codes of a row; the scale follows
+    static constexpr int kRowBytes = kCodeBytes + 16;
     static constexpr int kTileBytes = T * kRowBytes;
     static constexpr int kSlabsPerWarp = T / 16 / NCW;
     static constexpr int kKSteps = D / 16;
     static constexpr int kDBlocks = D / 16;
-    static constexpr int kKWords = D / 16;  // words of a lane's K bytes (D/4 bytes)
-    static constexpr int kVWords = D / 32;  // words of a lane's V bytes (D/8 bytes)
+    static constexpr int kKWords = kFp4 ? D / 32 : D / 16;  // words of a lane's K codes
+    static constexpr int kVWords = kFp4 ? D / 64 : D / 32;  // words of a lane's V codes
     static_assert(D == 64 || D == 128, "head_dim 64 or 128");
     static_assert(G >= 1 && G <= 8, "at most 8 query heads per mma column block");
     static_assert(T % (16 * NCW) == 0 && kSlabsPerWarp >= 1, "16-token slabs per warp");
@@ -440,7 +447,7 @@ struct Fp8MmaConsumer {
             const bool v_lo = (vmask >> gid) & 1u, v_hi = (vmask >> (gid + 8)) & 1u;
             // V scales of tokens gid, gid + 8 (0 for invalid rows) and the
             // running power of two of the largest one
-            const unsigned char* vs = vbuf + (slab0 + gid) * kRowBytes + D;
+            const unsigned char* vs = vbuf + (slab0 + gid) * kRowBytes + kCodeBytes;
             const float sv0 = v_lo ? *reinterpret_cast<const float*>(vs) : 0.f;
             const float sv1 = v_hi ? *reinterpret_cast<const float*>(vs + 8 * kRowBytes) : 0.f;
             float smax = fmaxf(sv0, sv1);
@@ -465,23 +472,41 @@ struct Fp8MmaConsumer {
             const unsigned char* k0 = kbuf + (slab0 + gid) * kRowBytes;
             const unsigned char* k1 = k0 + 8 * kRowBytes;
             uint32_t kw0[kKWords], kw1[kKWords];
+            constexpr int kLaneKBytes = 4 * kKWords;
+            if constexpr (kKWords >= 4) {
 #pragma unroll
-            for (int i = 0; i < kKWords / 4; ++i) {
-                const uint4 x = *reinterpret_cast<const uint4*>(k0 + (D / 4) * tig + 16 * i);
-                const uint4 y = *reinterpret_cast<const uint4*>(k1 + (D / 4) * tig + 16 * i);
-                kw0[4 * i] = x.x; kw0[4 * i + 1] = x.y; kw0[4 * i + 2] = x.z; kw0[4 * i + 3] = x.w;
-                kw1[4 * i] = y.x; kw1[4 * i + 1] = y.y; kw1[4 * i + 2] = y.z; kw1[4 * i + 3] = y.w;
+                for (int i = 0; i < kKWords / 4; ++i) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(k0 + kLaneKBytes * tig + 16 * i);
+                    const uint4 y = *reinterpret_cast<const uint4*>(k1 + kLaneKBytes * tig + 16 * i);
+                    kw0[4 * i] = x.x; kw0[4 * i + 1] = x.y; kw0[4 * i + 2] = x.z; kw0[4 * i + 3] = x.w;
+                    kw1[4 * i] = y.x; kw1[4 * i + 1] = y.y; kw1[4 * i + 2] = y.z; kw1[4 * i + 3] = y.w;
+                }
+            } else {
+                const uint2 x = *reinterpret_cast<const uint2*>(k0 + kLaneKBytes * tig);
+                const uint2 y = *reinterpret_cast<const uint2*>(k1 + kLaneKBytes * tig);
+                kw0[0] = x.x; kw0[1] = x.y;
+                kw1[0] = y.x; kw1[1] = y.y;
             }
-            const float sk0 = *reinterpret_cast<const float*>(k0 + D) * qscale;
-            const float sk1 = *reinterpret_cast<const float*>(k1 + D) * qscale;
+            const float sk0 = *reinterpret_cast<const float*>(k0 + kCodeBytes) * qscale;
+            const float sk1 = *reinterpret_cast<const float*>(k1 + kCodeBytes) * qscale;
             float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < kKSteps; ++ks) {
                 uint32_t a[4];
-                a[0] = e4m3x2_to_f16x2(kw0[ks]);
-                a[1] = e4m3x2_to_f16x2(kw1[ks]);
-                a[2] = e4m3x2_to_f16x2(kw0[ks] >> 16);
-                a[3] = e4m3x2_to_f16x2(kw1[ks] >> 16);
+                if constexpr (kFp4) {
+                    // two bytes per k-step: dims 4ks..4ks+1, 4ks+2..4ks+3 of the lane's range
+                    const uint32_t w0 = kw0[ks >> 1] >> (16 * (ks & 1));
+                    const uint32_t w1 = kw1[ks >> 1] >> (16 * (ks & 1));
+                    a[0] = e2m1x2_to_f16x2(w0);
+                    a[1] = e2m1x2_to_f16x2(w1);
+                    a[2] = e2m1x2_to_f16x2(w0 >> 8);
+                    a[3] = e2m1x2_to_f16x2(w1 >> 8);
+                } else {
+                    a[0] = e4m3x2_to_f16x2(kw0[ks]);
+                    a[1] = e4m3x2_to_f16x2(kw1[ks]);
+                    a[2] = e4m3x2_to_f16x2(kw0[ks] >> 16);
+                    a[3] = e4m3x2_to_f16x2(kw1[ks] >> 16);
+                }
                 mma_f16(s, a, qb[ks][0], qb[ks][1]);
             }
             s[0] = v_lo ? s[0] * sk0 : -INFINITY;
@@ -524,13 +549,14 @@ struct Fp8MmaConsumer {
             const uint32_t pk_hi = pack_f16x2(p2 * w1, p3 * w1);
             const uint32_t bh0 = movmatrix_trans(pk_lo), bh1 = movmatrix_trans(pk_hi);
 
-            // V codes of tokens 2tig, 2tig+1, 2tig+8, 2tig+9 at bytes (D/8)gid..;
-            // codes of invalid rows become 0 (NaN codes must not meet a 0 weight)
+            // V codes of tokens 2tig, 2tig+1, 2tig+8, 2tig+9: the lane's D/8
+            // dims from byte (D/8)gid (E4M3) or (D/16)gid (E2M1); codes of
+            // invalid rows become 0 (NaN codes must not meet a 0 weight)
             uint32_t vw[4][kVWords];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int t = 2 * tig + (u & 1) + (u >> 1) * 8;
-                const unsigned char* vr = vbuf + (slab0 + t) * kRowBytes + (D / 8) * gid;
+                const unsigned char* vr = vbuf + (slab0 + t) * kRowBytes + 4 * kVWords * gid;
                 const bool ok = (vmask >> t) & 1u;
                 if constexpr (kVWords == 4) {
                     const uint4 x = *reinterpret_cast<const uint4*>(vr);
@@ -538,22 +564,37 @@ struct Fp8MmaConsumer {
                     vw[u][1] = ok ? x.y : 0u;
                     vw[u][2] = ok ? x.z : 0u;
                     vw[u][3] = ok ? x.w : 0u;
-                } else {
+                } else if constexpr (kVWords == 2) {
                     const uint2 x = *reinterpret_cast<const uint2*>(vr);
                     vw[u][0] = ok ? x.x : 0u;
                     vw[u][1] = ok ? x.y : 0u;
+                } else {
+                    const uint32_t x = *reinterpret_cast<const uint32_t*>(vr);
+                    vw[u][0] = ok ? x : 0u;
                 }
             }
 #pragma unroll
             for (int j = 0; j < kDBlocks; ++j) {
-                const uint32_t sel = (j & 1) ? 0x7362u : 0x5140u;  // bytes 2j%4, 2j%4+1 of two rows
-                const uint32_t lo = byte_perm(vw[0][j >> 1], vw[1][j >> 1], sel);
-                const uint32_t hi = byte_perm(vw[2][j >> 1], vw[3][j >> 1], sel);
                 uint32_t a[4];
-                a[0] = e4m3x2_to_f16x2(lo);
-                a[1] = e4m3x2_to_f16x2(lo >> 16);
-                a[2] = e4m3x2_to_f16x2(hi);
-                a[3] = e4m3x2_to_f16x2(hi >> 16);
+                if constexpr (kFp4) {
+                    // byte j of the lane's range: dims 2j (low nibble), 2j + 1 (high);
+                    // pair the two tokens of a fragment register nibble-wise
+                    const int w = j >> 2, sh = 8 * (j & 3);
+                    const uint32_t x0 = vw[0][w] >> sh, x1 = vw[1][w] >> sh;
+                    const uint32_t x2 = vw[2][w] >> sh, x3 = vw[3][w] >> sh;
+                    a[0] = e2m1x2_to_f16x2((x0 & 0x0fu) | ((x1 & 0x0fu) << 4));
+                    a[1] = e2m1x2_to_f16x2(((x0 >> 4) & 0x0fu) | (x1 & 0xf0u));
+                    a[2] = e2m1x2_to_f16x2((x2 & 0x0fu) | ((x3 & 0x0fu) << 4));
+                    a[3] = e2m1x2_to_f16x2(((x2 >> 4) & 0x0fu) | (x3 & 0xf0u));
+                } else {
+                    const uint32_t sel = (j & 1) ? 0x7362u : 0x5140u;  // bytes 2j%4, 2j%4+1 of two rows
+                    const uint32_t lo = byte_perm(vw[0][j >> 1], vw[1][j >> 1], sel);
+                    const uint32_t hi = byte_perm(vw[2][j >> 1], vw[3][j >> 1], sel);
+                    a[0] = e4m3x2_to_f16x2(lo);
+                    a[1] = e4m3x2_to_f16x2(lo >> 16);
+                    a[2] = e4m3x2_to_f16x2(hi);
+                    a[3] = e4m3x2_to_f16x2(hi >> 16);
+                }
                 mma_f16(acc[j], a, bh0, bh1);
             }
         }
@@ -586,5 +627,10 @@ struct Fp8MmaConsumer {
         }
     }
 };
+
+template <int D, int G, int T, int NCW>
+using Fp8MmaConsumer = QuantMmaConsumer<D, G, T, NCW, false>;
+template <int D, int G, int T, int NCW>
+using Fp4MmaConsumer = QuantMmaConsumer<D, G, T, NCW, true>;
 
 }  // namespace kvd

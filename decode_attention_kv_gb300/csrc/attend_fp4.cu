@@ -1,0 +1,20 @@
+// attend_fp4.cu -- the attention kernels over E2M1 rows (D/2 code bytes, two
+// codes per byte, + a 16-byte field holding the row's fp32 scale).
+#include "attend_quant.cuh"
+
+namespace kvd {
+
+cudaError_t launch_attend_fp4(int D, int G, const AttendParams& p, cudaStream_t stream) {
+    return launch_attend_quant<true>(D, G, p, stream);
+}
+
+int small_shared_bytes_fp4(int D, int G, int chunk, int slots, int nwg) {
+    return small_shared_bytes_quant<true>(D, G, chunk, slots, nwg);
+}
+
+cudaError_t launch_attend_small_fp4(int D, int G, const AttendParams& p, int S, int rows,
+                                    cudaStream_t stream) {
+    return launch_attend_small_quant<true>(D, G, p, S, rows, stream);
+}
+
+}  // namespace kvd

@@ -1,27 +1,20 @@
-// attend_fp8.cu -- instantiations of the attention kernel over quantised K/V
-// rows (E4M3 codes with a per-row fp32 scale; q and out bf16): tensor-core
-// consumers for every group width up to 8 query heads per kv head.
-#include "attend_inst.cuh"
+// attend_fp8.cu -- the attention kernels over E4M3 rows (D code bytes + a
+// 16-byte field holding the row's fp32 scale).
+#include "attend_quant.cuh"
 
 namespace kvd {
 
 cudaError_t launch_attend_fp8(int D, int G, const AttendParams& p, cudaStream_t stream) {
-    if (D == 128) {
-        switch (G) {
-            case 1: return launch_fp8<128, 1>(p, stream);
-            case 2: return launch_fp8<128, 2>(p, stream);
-            case 4: return launch_fp8<128, 4>(p, stream);
-            case 8: return launch_fp8<128, 8>(p, stream);
-        }
-    } else if (D == 64) {
-        switch (G) {
-            case 1: return launch_fp8<64, 1>(p, stream);
-            case 2: return launch_fp8<64, 2>(p, stream);
-            case 4: return launch_fp8<64, 4>(p, stream);
-            case 8: return launch_fp8<64, 8>(p, stream);
-        }
-    }
-    return cudaErrorInvalidValue;
+    return launch_attend_quant<false>(D, G, p, stream);
+}
+
+int small_shared_bytes_fp8(int D, int G, int chunk, int slots, int nwg) {
+    return small_shared_bytes_quant<false>(D, G, chunk, slots, nwg);
+}
+
+cudaError_t launch_attend_small_fp8(int D, int G, const AttendParams& p, int S, int rows,
+                                    cudaStream_t stream) {
+    return launch_attend_small_quant<false>(D, G, p, S, rows, stream);
 }
 
 }  // namespace kvd

@@ -45,11 +45,12 @@ struct MmaCfg {
     static constexpr int STAGES = ring_stages<Cons, MB>();
 };
 
-// Tensor-core consumers over quantised rows (E4M3 codes + scale): 64-token
-// tiles of D + 16-byte rows, one merge buffer.
-template <int D, int G>
-struct Fp8Cfg {
-    using Cons = Fp8MmaConsumer<D, G, 64, 4>;
+// Tensor-core consumers over quantised rows (E4M3 codes, D + 16-byte rows,
+// or E2M1 codes, D/2 + 16-byte rows; each with its fp32 scale): 64-token
+// tiles, one merge buffer.
+template <int D, int G, bool kFp4>
+struct QuantCfg {
+    using Cons = QuantMmaConsumer<D, G, 64, 4, kFp4>;
     static constexpr int MB = 1;
     static constexpr int STAGES = ring_stages<Cons, MB>();
 };
@@ -135,9 +136,9 @@ cudaError_t launch_mma(int mode, const AttendParams& p, const CUtensorMap* kmap,
 
 // Quantised rows: static-buffer mode only (no tensor maps: rows arrive by
 // bulk copies of whole tiles).
-template <int D, int G>
-cudaError_t launch_fp8(const AttendParams& p, cudaStream_t stream) {
-    using C = Fp8Cfg<D, G>;
+template <int D, int G, bool kFp4>
+cudaError_t launch_quant(const AttendParams& p, cudaStream_t stream) {
+    using C = QuantCfg<D, G, kFp4>;
     CUtensorMap none;
     std::memset(&none, 0, sizeof none);
     return launch_kernel<typename C::Cons, C::STAGES, C::MB, kModeMasked>(p, &none, &none, stream);

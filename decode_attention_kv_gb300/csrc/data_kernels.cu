@@ -419,6 +419,96 @@ cudaError_t launch_append_fp8(void* k_cache, void* v_cache, const void* k_new, c
                                  kn, vn, pos, mask, B, Hkv, C, dev_status);
 }
 
+// ------------------------------------------------------------- append_fp4
+// The FP4 counterpart: scale = amax / 6, code = nearest E2M1 magnitude of
+// x / scale (ties to the even code, saturated at 6), two codes per byte with
+// element 2j in the low nibble.  One warp per (entry, kv head, K|V) row.
+
+// Nearest E2M1 code of x: the magnitude's code is the number of rounding
+// boundaries it passes (the midpoints of 0, 0.5, 1, 1.5, 2, 3, 4, 6; a value
+// on a midpoint goes to the neighbour with the even code, so the boundary
+// is passed with > or >= accordingly); NaN gives +6.
+__device__ __forceinline__ uint32_t e2m1_code(float x) {
+    if (x != x) return 0x7u;
+    const float a = fabsf(x);
+    const uint32_t c = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+                       (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
+                       (uint32_t)(a > 5.f);
+    return c | (signbit(x) ? 0x8u : 0u);
+}
+
+template <typename In, int D>
+__global__ void __launch_bounds__(128)
+append_fp4_kernel(unsigned char* __restrict__ kc, unsigned char* __restrict__ vc,
+                  const In* __restrict__ kn, const In* __restrict__ vn,
+                  const int32_t* __restrict__ pos, uint8_t* __restrict__ mask, int B, int Hkv,
+                  int C, int32_t* dev_status) {
+    pdl_launch_dependents();
+    pdl_wait();
+    constexpr int VPL = D / 32;  // elements per lane: 2 or 4, i.e. 1 or 2 code bytes
+    constexpr int RB = D / 2 + 16;
+    const int lane = threadIdx.x & 31;
+    const long long job = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (job >= 2ll * B * Hkv) return;
+    const int kv = (int)(job & 1);
+    const long long bh = job >> 1;
+    const int b = (int)(bh / Hkv);
+    const int p = pos[b];
+    if (p < 0 || p >= C) {
+        if (lane == 0 && kv == 0 && bh % Hkv == 0) report(dev_status, KVD_DEV_POS_RANGE);
+        return;
+    }
+    const In* src = (kv ? vn : kn) + bh * D + VPL * lane;
+    float x[VPL];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        x[i] = as_float(src[i]);
+        amax = fmaxf(amax, fabsf(x[i]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float scale = __fdiv_rn(amax, 6.f);
+    uint32_t codes = 0;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const uint32_t c = scale > 0.f ? e2m1_code(__fdiv_rn(x[i], scale)) : 0u;
+        codes |= c << (4 * i);
+    }
+    unsigned char* row = (kv ? vc : kc) + ((size_t)bh * C + p) * RB;
+    if constexpr (VPL == 4)
+        *reinterpret_cast<uint16_t*>(row + 2 * lane) = (uint16_t)codes;
+    else
+        row[lane] = (unsigned char)codes;
+    if (lane == 0) {
+        *reinterpret_cast<uint4*>(row + D / 2) = make_uint4(__float_as_uint(scale), 0u, 0u, 0u);
+        if (mask && kv == 0 && bh % Hkv == 0) mask[(size_t)b * C + p] = 1;
+    }
+}
+
+cudaError_t launch_append_fp4(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                              const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
+                              kvd_dtype in_dt, int32_t* dev_status, cudaStream_t stream) {
+    const long long jobs = 2ll * B * Hkv;
+    const dim3 grid((unsigned)((jobs + 3) / 4));
+    unsigned char* kc = static_cast<unsigned char*>(k_cache);
+    unsigned char* vc = static_cast<unsigned char*>(v_cache);
+    if (in_dt == KVD_BF16) {
+        const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(k_new);
+        const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(v_new);
+        return D == 128 ? launch_pdl(append_fp4_kernel<__nv_bfloat16, 128>, grid, dim3(128), 0, stream,
+                                     kc, vc, kn, vn, pos, mask, B, Hkv, C, dev_status)
+                        : launch_pdl(append_fp4_kernel<__nv_bfloat16, 64>, grid, dim3(128), 0, stream,
+                                     kc, vc, kn, vn, pos, mask, B, Hkv, C, dev_status);
+    }
+    const float* kn = static_cast<const float*>(k_new);
+    const float* vn = static_cast<const float*>(v_new);
+    return D == 128 ? launch_pdl(append_fp4_kernel<float, 128>, grid, dim3(128), 0, stream, kc, vc,
+                                 kn, vn, pos, mask, B, Hkv, C, dev_status)
+                    : launch_pdl(append_fp4_kernel<float, 64>, grid, dim3(128), 0, stream, kc, vc,
+                                 kn, vn, pos, mask, B, Hkv, C, dev_status);
+}
+
 // ------------------------------------------------------------------- gather
 // gather_pa_kv_cache, Norm/ND branch ("PyPTO 实现 AscendC GatherPaKvCache",
 // 3.2): CTA q * cols + j copies the valid rows of logical block j of

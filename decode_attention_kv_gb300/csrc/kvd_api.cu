@@ -26,6 +26,10 @@ cudaError_t launch_attend_small(kvd_dtype dt, int D, int G, const AttendParams& 
                                 cudaStream_t stream);
 int small_shared_bytes(kvd_dtype dt, int D, int G, int chunk, int slots, int nwg);
 int small_shared_bytes_fp8(int D, int G, int chunk, int slots, int nwg);
+int small_shared_bytes_fp4(int D, int G, int chunk, int slots, int nwg);
+cudaError_t launch_attend_fp4(int D, int G, const AttendParams& p, cudaStream_t stream);
+cudaError_t launch_attend_small_fp4(int D, int G, const AttendParams& p, int S, int rows,
+                                    cudaStream_t stream);
 cudaError_t launch_attend_small_fp8(int D, int G, const AttendParams& p, int S, int rows,
                                     cudaStream_t stream);
 }  // namespace kvd
@@ -188,18 +192,23 @@ struct SmallPlan {
     int chunk, S, rows;
 };
 
-// fp8: quantised rows (row copies of D + 16 bytes, 64-row tiles).
+// Rows of the cache: elements of dt, or quantised rows (row copies of
+// D + 16 or D/2 + 16 bytes, 64-row tiles).
+enum RowKind { kRowsPlain = 0, kRowsFp8 = 1, kRowsFp4 = 2 };
+
 SmallPlan plan_small(int B, int Hkv, int C, int D, kvd_dtype dt, const Plan& pl, int num_splits,
-                     bool fp8 = false) {
+                     RowKind rk = kRowsPlain) {
     SmallPlan sp{};
     if (num_splits != 0) return sp;
+    const bool fp8 = rk != kRowsPlain;
     const int q = (!fp8 && small_uses_mma(dt, pl.G)) ? 64 : 16;  // 64-row boxes or 16-row copies
     const long long rows = (long long)B * Hkv * pl.HG;
     const long long chunk = ((C + kSmallSplits - 1) / kSmallSplits + q - 1) / q * q;
     const long long S = (C + chunk - 1) / chunk;
     auto smem = [&](int slots, int nwg) {
-        return fp8 ? small_shared_bytes_fp8(D, pl.G, (int)chunk, slots, nwg)
-                   : small_shared_bytes(dt, D, pl.G, (int)chunk, slots, nwg);
+        if (rk == kRowsFp4) return small_shared_bytes_fp4(D, pl.G, (int)chunk, slots, nwg);
+        if (rk == kRowsFp8) return small_shared_bytes_fp8(D, pl.G, (int)chunk, slots, nwg);
+        return small_shared_bytes(dt, D, pl.G, (int)chunk, slots, nwg);
     };
     // the first layout that fits two CTAs per SM: two consumer warp groups
     // (tensor-core consumers over two or more tiles) before one; partials
@@ -592,61 +601,63 @@ kvd_status kvd_append_attend_masked(const void* q, void* k_cache, void* v_cache,
                               k_new, v_new, pos);
 }
 
-kvd_status kvd_append_fp8(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
-                          const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
-                          kvd_dtype new_dtype, int32_t* dev_status, kvd_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+kvd_status append_quant(const char* fn, bool fp4, void* k_cache, void* v_cache, const void* k_new,
+                        const void* v_new, const int32_t* pos, uint8_t* mask, int B, int Hkv,
+                        int C, int D, kvd_dtype new_dtype, int32_t* dev_status,
+                        kvd_stream_t stream) {
     if (!k_cache || !v_cache || !k_new || !v_new || !pos)
-        return fail(KVD_ERR_INVALID_ARG, "kvd_append_fp8: null pointer");
-    if (B < 1 || Hkv < 1 || C < 1) return fail(KVD_ERR_INVALID_ARG, "kvd_append_fp8: sizes must be >= 1");
-    if (!dtype_ok(new_dtype)) return fail(KVD_ERR_INVALID_ARG, "kvd_append_fp8: unknown dtype");
-    if (D != 64 && D != 128) return fail(KVD_ERR_UNSUPPORTED, "kvd_append_fp8: head_dim %d (supported: 64, 128)", D);
+        return fail(KVD_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (B < 1 || Hkv < 1 || C < 1) return fail(KVD_ERR_INVALID_ARG, "%s: sizes must be >= 1", fn);
+    if (!dtype_ok(new_dtype)) return fail(KVD_ERR_INVALID_ARG, "%s: unknown dtype", fn);
+    if (D != 64 && D != 128) return fail(KVD_ERR_UNSUPPORTED, "%s: head_dim %d (supported: 64, 128)", fn, D);
     if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) ||
         !aligned(pos, 4) || !aligned(dev_status, 4))
-        return fail(KVD_ERR_INVALID_ARG, "kvd_append_fp8: misaligned pointer");
-    if (2ll * B * Hkv > (1ll << 33)) return fail(KVD_ERR_UNSUPPORTED, "kvd_append_fp8: B*Hkv too large");
-    const cudaError_t e = launch_append_fp8(k_cache, v_cache, k_new, v_new, pos, mask, B, Hkv, C, D,
-                                            new_dtype, dev_status, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "kvd_append_fp8 launch");
+        return fail(KVD_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+    if (2ll * B * Hkv > (1ll << 33)) return fail(KVD_ERR_UNSUPPORTED, "%s: B*Hkv too large", fn);
+    const cudaError_t e =
+        fp4 ? launch_append_fp4(k_cache, v_cache, k_new, v_new, pos, mask, B, Hkv, C, D, new_dtype,
+                                dev_status, (cudaStream_t)stream)
+            : launch_append_fp8(k_cache, v_cache, k_new, v_new, pos, mask, B, Hkv, C, D, new_dtype,
+                                dev_status, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, fp4 ? "kvd_append_fp4 launch" : "kvd_append_fp8 launch");
     return ok();
 }
 
-constexpr int kFp8Tile = 64;  // tokens per ring stage over quantised rows
+constexpr int kQuantTile = 64;  // tokens per ring stage over quantised rows
 
-size_t kvd_attend_masked_fp8_workspace_bytes(int B, int Hq, int Hkv, int C, int D, int num_splits) {
-    if (B < 1 || C < 1 || check_attention_shape(Hq, Hkv, D, KVD_BF16) != KVD_OK) return 0;
-    return plan_attention(B, Hq, Hkv, C, D, KVD_BF16, 0, num_splits, false, kFp8Tile).ws;
-}
-
-kvd_status kvd_attend_masked_fp8_plan(int B, int Hq, int Hkv, int C, int D, int num_splits,
-                                      kvd_plan* plan) {
-    if (!plan)
-        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_fp8_plan: null pointer");
+kvd_status quant_plan(const char* fn, RowKind rk, int B, int Hq, int Hkv, int C, int D,
+                      int num_splits, kvd_plan* plan) {
+    if (!plan) return fail(KVD_ERR_INVALID_ARG, "%s: null pointer", fn);
     if (B < 1 || C < 1 || num_splits < 0)
-        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_fp8_plan: B, C >= 1 and num_splits >= 0 required");
+        return fail(KVD_ERR_INVALID_ARG, "%s: B, C >= 1 and num_splits >= 0 required", fn);
     const kvd_status st = check_attention_shape(Hq, Hkv, D, KVD_BF16);
     if (st != KVD_OK) return st;
-    const Plan pl = plan_attention(B, Hq, Hkv, C, D, KVD_BF16, 0, num_splits, false, kFp8Tile);
-    put_plan(pl, plan_small(B, Hkv, C, D, KVD_BF16, pl, num_splits, true).use, plan);
+    const Plan pl = plan_attention(B, Hq, Hkv, C, D, KVD_BF16, 0, num_splits, false, kQuantTile);
+    put_plan(pl, plan_small(B, Hkv, C, D, KVD_BF16, pl, num_splits, rk).use, plan);
     return ok();
 }
 
-kvd_status kvd_attend_masked_fp8(const void* q, const void* k_cache, const void* v_cache,
-                                 const uint8_t* mask, void* out, float* lse_out, int B, int Hq,
-                                 int Hkv, int C, int D, float scale, int num_splits,
-                                 void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                                 kvd_stream_t stream) {
+kvd_status attend_quant(const char* fn, RowKind rk, const void* q, const void* k_cache,
+                        const void* v_cache, const uint8_t* mask, void* out, float* lse_out, int B,
+                        int Hq, int Hkv, int C, int D, float scale, int num_splits,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        kvd_stream_t stream) {
     kvd_status st = check_attention_shape(Hq, Hkv, D, KVD_BF16);
     if (st != KVD_OK) return st;
-    if (B < 0 || C < 1) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_fp8: B >= 0 and C >= 1 required");
+    if (B < 0 || C < 1) return fail(KVD_ERR_INVALID_ARG, "%s: B >= 0 and C >= 1 required", fn);
     if (B == 0) return ok();
     if (!q || !k_cache || !v_cache || !mask || !out)
-        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_fp8: null pointer");
+        return fail(KVD_ERR_INVALID_ARG, "%s: null pointer", fn);
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         !aligned(lse_out, 4) || !aligned(dev_status, 4))
-        return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_fp8: misaligned pointer");
-    if (num_splits < 0) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_masked_fp8: num_splits < 0");
-    const Plan pl = plan_attention(B, Hq, Hkv, C, D, KVD_BF16, 0, num_splits, false, kFp8Tile);
-    st = check_workspace("kvd_attend_masked_fp8", pl, workspace, workspace_bytes);
+        return fail(KVD_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+    if (num_splits < 0) return fail(KVD_ERR_INVALID_ARG, "%s: num_splits < 0", fn);
+    const Plan pl = plan_attention(B, Hq, Hkv, C, D, KVD_BF16, 0, num_splits, false, kQuantTile);
+    st = check_workspace(fn, pl, workspace, workspace_bytes);
     if (st != KVD_OK) return st;
     AttendParams p{};
     p.q = q;
@@ -663,25 +674,90 @@ kvd_status kvd_attend_masked_fp8(const void* q, const void* k_cache, const void*
     p.mask_vec = (C % 16 == 0) && aligned(mask, 16);
     p.qscale = scale * kLog2e;
     attach_workspace(p, pl, workspace);
-    const SmallPlan sp = plan_small(B, Hkv, C, D, KVD_BF16, pl, num_splits, true);
+    const bool fp4 = rk == kRowsFp4;
+    const SmallPlan sp = plan_small(B, Hkv, C, D, KVD_BF16, pl, num_splits, rk);
     if (sp.use) {
         AttendParams ps = p;
         ps.chunk = sp.chunk;
         ps.S = sp.S;
         ps.small_push = sp.push ? 1 : 0;
         ps.small_nwg = sp.nwg;
-        const cudaError_t es = launch_attend_small_fp8(D, pl.G, ps, sp.S, sp.rows, (cudaStream_t)stream);
-        if (es != cudaSuccess) return cuda_fail(es, "kvd_attend_masked_fp8 launch");
+        const cudaError_t es =
+            fp4 ? launch_attend_small_fp4(D, pl.G, ps, sp.S, sp.rows, (cudaStream_t)stream)
+                : launch_attend_small_fp8(D, pl.G, ps, sp.S, sp.rows, (cudaStream_t)stream);
+        if (es != cudaSuccess) return cuda_fail(es, fn);
         return ok();
     }
-    cudaError_t e = launch_attend_fp8(D, pl.G, p, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked_fp8 launch");
+    cudaError_t e = fp4 ? launch_attend_fp4(D, pl.G, p, (cudaStream_t)stream)
+                        : launch_attend_fp8(D, pl.G, p, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
     if (pl.S > 1) {
         e = launch_combine(p.part_o, p.part_lse, out, lse_out, B * Hq, pl.S, D, KVD_BF16,
                            (cudaStream_t)stream);
-        if (e != cudaSuccess) return cuda_fail(e, "kvd_attend_masked_fp8 combine launch");
+        if (e != cudaSuccess) return cuda_fail(e, "combine launch");
     }
     return ok();
+}
+
+size_t quant_workspace_bytes(int B, int Hq, int Hkv, int C, int D, int num_splits) {
+    if (B < 1 || C < 1 || check_attention_shape(Hq, Hkv, D, KVD_BF16) != KVD_OK) return 0;
+    return plan_attention(B, Hq, Hkv, C, D, KVD_BF16, 0, num_splits, false, kQuantTile).ws;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvd_status kvd_append_fp8(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                          const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
+                          kvd_dtype new_dtype, int32_t* dev_status, kvd_stream_t stream) {
+    return append_quant("kvd_append_fp8", false, k_cache, v_cache, k_new, v_new, pos, mask, B,
+                        Hkv, C, D, new_dtype, dev_status, stream);
+}
+
+kvd_status kvd_append_fp4(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                          const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
+                          kvd_dtype new_dtype, int32_t* dev_status, kvd_stream_t stream) {
+    return append_quant("kvd_append_fp4", true, k_cache, v_cache, k_new, v_new, pos, mask, B,
+                        Hkv, C, D, new_dtype, dev_status, stream);
+}
+
+size_t kvd_attend_masked_fp8_workspace_bytes(int B, int Hq, int Hkv, int C, int D, int num_splits) {
+    return quant_workspace_bytes(B, Hq, Hkv, C, D, num_splits);
+}
+
+size_t kvd_attend_masked_fp4_workspace_bytes(int B, int Hq, int Hkv, int C, int D, int num_splits) {
+    return quant_workspace_bytes(B, Hq, Hkv, C, D, num_splits);
+}
+
+kvd_status kvd_attend_masked_fp8_plan(int B, int Hq, int Hkv, int C, int D, int num_splits,
+                                      kvd_plan* plan) {
+    return quant_plan("kvd_attend_masked_fp8_plan", kRowsFp8, B, Hq, Hkv, C, D, num_splits, plan);
+}
+
+kvd_status kvd_attend_masked_fp4_plan(int B, int Hq, int Hkv, int C, int D, int num_splits,
+                                      kvd_plan* plan) {
+    return quant_plan("kvd_attend_masked_fp4_plan", kRowsFp4, B, Hq, Hkv, C, D, num_splits, plan);
+}
+
+kvd_status kvd_attend_masked_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                 const uint8_t* mask, void* out, float* lse_out, int B, int Hq,
+                                 int Hkv, int C, int D, float scale, int num_splits,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                 kvd_stream_t stream) {
+    return attend_quant("kvd_attend_masked_fp8", kRowsFp8, q, k_cache, v_cache, mask, out, lse_out,
+                        B, Hq, Hkv, C, D, scale, num_splits, workspace, workspace_bytes,
+                        dev_status, stream);
+}
+
+kvd_status kvd_attend_masked_fp4(const void* q, const void* k_cache, const void* v_cache,
+                                 const uint8_t* mask, void* out, float* lse_out, int B, int Hq,
+                                 int Hkv, int C, int D, float scale, int num_splits,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                 kvd_stream_t stream) {
+    return attend_quant("kvd_attend_masked_fp4", kRowsFp4, q, k_cache, v_cache, mask, out, lse_out,
+                        B, Hq, Hkv, C, D, scale, num_splits, workspace, workspace_bytes,
+                        dev_status, stream);
 }
 
 size_t kvd_attend_indexed_workspace_bytes(int B, int Hq, int Hkv, int topk, int D,

@@ -79,6 +79,10 @@ cudaError_t launch_append_fp8(void* k_cache, void* v_cache, const void* k_new, c
                               const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
                               kvd_dtype in_dt, int32_t* dev_status, cudaStream_t stream);
 
+cudaError_t launch_append_fp4(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                              const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
+                              kvd_dtype in_dt, int32_t* dev_status, cudaStream_t stream);
+
 cudaError_t launch_gather(const void* key_cache, const void* value_cache,
                           const int32_t* block_tables, const int32_t* seq_lens,
                           const int32_t* seq_offset, void* key_out, void* value_out, int Q,

@@ -47,6 +47,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
     return r;
 }
 
+// Two E2M1 codes (the low byte of x: low nibble -> low half) -> f16x2, exactly.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t x) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 c;\n\tcvt.u8.u32 c, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, c;\n\t}"
+        : "=r"(r)
+        : "r"(x & 0xffu));
+    return r;
+}
+
 // Byte select of two words (prmt): result byte i = byte sel_i of {b:a}.
 __device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;

@@ -38,6 +38,7 @@ SIGNATURES = {
                            _vp, _vp], _i),
     "kvd_attend_masked_plan": ([_i, _i, _i, _i, _i, _i, _i, _vp], _i),
     "kvd_attend_masked_fp8_plan": ([_i, _i, _i, _i, _i, _i, _vp], _i),
+    "kvd_attend_masked_fp4_plan": ([_i, _i, _i, _i, _i, _i, _vp], _i),
     "kvd_attend_indexed_plan": ([_i, _i, _i, _i, _i, _i, _i, _vp], _i),
     "kvd_attend_paged_plan": ([_i, _i, _i, _i, _i, _i, _i, _i, _vp], _i),
     "kvd_attend_masked_partial": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i,
@@ -49,6 +50,10 @@ SIGNATURES = {
     "kvd_append_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp], _i),
     "kvd_attend_masked_fp8_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
     "kvd_attend_masked_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz,
+                               _vp, _vp], _i),
+    "kvd_append_fp4": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp], _i),
+    "kvd_attend_masked_fp4_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
+    "kvd_attend_masked_fp4": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz,
                                _vp, _vp], _i),
     "kvd_attend_indexed_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
     "kvd_attend_indexed": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp,
@@ -172,52 +177,73 @@ def append(k_cache, v_cache, k_new, v_new, pos, mask=None, dev_status=None):
 FP8_ROW_PAD = 16  # KVD_FP8_ROW_PAD: bytes after the D codes of a quantised row
 
 
-def append_fp8(k_cache, v_cache, k_new, v_new, pos, mask=None, dev_status=None):
-    """kvd_append_fp8: quantise the step's K/V rows (bf16 or fp32 [B, Hkv, D])
-    into row pos[b] of the quantised caches (uint8 [B, Hkv, C, D + 16]); set
-    mask[b, pos[b]]."""
+FP4_ROW_PAD = 16  # KVD_FP4_ROW_PAD: bytes after the D/2 code bytes of an FP4 row
+
+# code bytes of a row of D elements, per row format
+_CODE_BYTES = {"fp8": lambda D: D, "fp4": lambda D: D // 2}
+_ROW_D = {"fp8": lambda RB: RB - FP8_ROW_PAD, "fp4": lambda RB: 2 * (RB - FP4_ROW_PAD)}
+
+
+def _append_quant(fmt, k_cache, v_cache, k_new, v_new, pos, mask, dev_status):
+    name = f"append_{fmt}"
     for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_new", k_new), ("v_new", v_new),
                  ("pos", pos)):
         _cuda_contig(n, t)
     B, Hkv, C, RB = k_cache.shape
-    D = RB - FP8_ROW_PAD
+    D = _ROW_D[fmt](RB)
     if k_cache.dtype != torch.uint8 or v_cache.shape != k_cache.shape or \
             v_cache.dtype != torch.uint8:
-        raise ValueError("append_fp8: caches must be uint8 [B, Hkv, C, D + 16]")
+        raise ValueError(f"{name}: caches must be uint8 [B, Hkv, C, row bytes]")
     if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or k_new.dtype != v_new.dtype:
-        raise ValueError("append_fp8: shape mismatch")
+        raise ValueError(f"{name}: shape mismatch")
     if pos.dtype != torch.int32 or pos.numel() != B:
-        raise ValueError("append_fp8: pos must be int32 [B]")
+        raise ValueError(f"{name}: pos must be int32 [B]")
     if mask is not None:
         _cuda_contig("mask", mask)
         if mask.dtype != torch.uint8 or mask.shape != (B, C):
-            raise ValueError("append_fp8: mask must be uint8 [B, C]")
-    st = load().kvd_append_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(pos),
-                               _ptr(mask), B, Hkv, C, D, _dtype_code(k_new), _ptr(dev_status),
-                               _stream(k_cache.device))
-    _check("kvd_append_fp8", st)
+            raise ValueError(f"{name}: mask must be uint8 [B, C]")
+    fn = f"kvd_append_{fmt}"
+    st = getattr(load(), fn)(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(pos),
+                             _ptr(mask), B, Hkv, C, D, _dtype_code(k_new), _ptr(dev_status),
+                             _stream(k_cache.device))
+    _check(fn, st)
+
+
+def append_fp8(k_cache, v_cache, k_new, v_new, pos, mask=None, dev_status=None):
+    """kvd_append_fp8: quantise the step's K/V rows (bf16 or fp32 [B, Hkv, D])
+    into row pos[b] of the E4M3 caches (uint8 [B, Hkv, C, D + 16]); set
+    mask[b, pos[b]]."""
+    _append_quant("fp8", k_cache, v_cache, k_new, v_new, pos, mask, dev_status)
+
+
+def append_fp4(k_cache, v_cache, k_new, v_new, pos, mask=None, dev_status=None):
+    """kvd_append_fp4: as append_fp8 into E2M1 caches (uint8
+    [B, Hkv, C, D/2 + 16])."""
+    _append_quant("fp4", k_cache, v_cache, k_new, v_new, pos, mask, dev_status)
 
 
 def attend_masked_fp8_workspace_bytes(B, Hq, Hkv, C, D, num_splits=0):
     return load().kvd_attend_masked_fp8_workspace_bytes(B, Hq, Hkv, C, D, num_splits)
 
 
-def attend_masked_fp8(q, k_cache, v_cache, mask, scale=None, out=None, lse=None, num_splits=0,
-                      workspace=None, dev_status=None):
-    """kvd_attend_masked_fp8: decode attention over quantised caches.
+def attend_masked_fp4_workspace_bytes(B, Hq, Hkv, C, D, num_splits=0):
+    return load().kvd_attend_masked_fp4_workspace_bytes(B, Hq, Hkv, C, D, num_splits)
 
-    q [B, Hq, D] bf16; k_cache, v_cache uint8 [B, Hkv, C, D + 16]; mask [B, C]
-    uint8.  Returns out [B, Hq, D] bf16; fills ``lse`` [B, Hq] fp32 if given.
-    """
+
+def _attend_quant(fmt, q, k_cache, v_cache, mask, scale, out, lse, num_splits, workspace,
+                  dev_status):
+    name = f"attend_masked_{fmt}"
     for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("mask", mask)):
         _cuda_contig(n, t)
     B, Hq, D = q.shape
     Bk, Hkv, C, RB = k_cache.shape
-    if Bk != B or RB != D + FP8_ROW_PAD or v_cache.shape != k_cache.shape or mask.shape != (B, C):
-        raise ValueError("attend_masked_fp8: shape mismatch")
+    pad = FP8_ROW_PAD if fmt == "fp8" else FP4_ROW_PAD
+    if Bk != B or RB != _CODE_BYTES[fmt](D) + pad or v_cache.shape != k_cache.shape or \
+            mask.shape != (B, C):
+        raise ValueError(f"{name}: shape mismatch")
     if q.dtype != torch.bfloat16 or k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8 \
             or mask.dtype != torch.uint8:
-        raise TypeError("attend_masked_fp8: q bf16, caches and mask uint8")
+        raise TypeError(f"{name}: q bf16, caches and mask uint8")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
@@ -225,13 +251,33 @@ def attend_masked_fp8(q, k_cache, v_cache, mask, scale=None, out=None, lse=None,
     if lse is not None:
         _cuda_contig("lse", lse)
     L = load()
-    need = L.kvd_attend_masked_fp8_workspace_bytes(B, Hq, Hkv, C, D, num_splits)
+    fn = f"kvd_attend_masked_{fmt}"
+    need = getattr(L, fn + "_workspace_bytes")(B, Hq, Hkv, C, D, num_splits)
     ws, wsb = _workspace(need, q.device, workspace)
-    st = L.kvd_attend_masked_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(mask), _ptr(out),
-                                 _ptr(lse), B, Hq, Hkv, C, D, float(scale), num_splits, _ptr(ws),
-                                 wsb, _ptr(dev_status), _stream(q.device))
-    _check("kvd_attend_masked_fp8", st)
+    st = getattr(L, fn)(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(mask), _ptr(out), _ptr(lse),
+                        B, Hq, Hkv, C, D, float(scale), num_splits, _ptr(ws), wsb,
+                        _ptr(dev_status), _stream(q.device))
+    _check(fn, st)
     return out
+
+
+def attend_masked_fp8(q, k_cache, v_cache, mask, scale=None, out=None, lse=None, num_splits=0,
+                      workspace=None, dev_status=None):
+    """kvd_attend_masked_fp8: decode attention over E4M3 caches.
+
+    q [B, Hq, D] bf16; k_cache, v_cache uint8 [B, Hkv, C, D + 16]; mask [B, C]
+    uint8.  Returns out [B, Hq, D] bf16; fills ``lse`` [B, Hq] fp32 if given.
+    """
+    return _attend_quant("fp8", q, k_cache, v_cache, mask, scale, out, lse, num_splits,
+                         workspace, dev_status)
+
+
+def attend_masked_fp4(q, k_cache, v_cache, mask, scale=None, out=None, lse=None, num_splits=0,
+                      workspace=None, dev_status=None):
+    """kvd_attend_masked_fp4: decode attention over E2M1 caches (uint8
+    [B, Hkv, C, D/2 + 16]); otherwise as attend_masked_fp8."""
+    return _attend_quant("fp4", q, k_cache, v_cache, mask, scale, out, lse, num_splits,
+                         workspace, dev_status)
 
 
 def pointer_array(tensors, device):
@@ -382,6 +428,10 @@ def attend_masked_plan(B, Hq, Hkv, C, D, dtype=torch.bfloat16, num_splits=0):
 
 def attend_masked_fp8_plan(B, Hq, Hkv, C, D, num_splits=0):
     return _plan("kvd_attend_masked_fp8_plan", B, Hq, Hkv, C, D, num_splits)
+
+
+def attend_masked_fp4_plan(B, Hq, Hkv, C, D, num_splits=0):
+    return _plan("kvd_attend_masked_fp4_plan", B, Hq, Hkv, C, D, num_splits)
 
 
 def attend_indexed_plan(B, Hq, Hkv, topk, D, dtype=torch.bfloat16, num_splits=0):

@@ -339,6 +339,49 @@ kvd_status kvd_attend_masked_fp8(const void* q, const void* k_cache, const void*
                                  kvd_stream_t stream);
 
 /*
+ * FP4 KV rows ([FlashMLA-KV], which names FP4 beside FP8; the granularity and
+ * encoding are this library's reading, as for FP8): one row of a kv head is
+ *   bytes [0, D/2)          OCP FP4 E2M1 codes, two per byte: element 2j in
+ *                           the low nibble of byte j, 2j + 1 in the high one
+ *                           (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6)
+ *   bytes [D/2, D/2 + 4)    the row's scale, fp32 little-endian
+ *   bytes [D/2 + 4, D/2+16) zero
+ * so a cache is uint8 [B, Hkv, C, D/2 + KVD_FP4_ROW_PAD] and element d of a
+ * row is scale * E2M1(code[d]).
+ */
+#define KVD_FP4_ROW_PAD 16
+
+/*
+ * kvd_append_fp4 -- kvd_append_fp8 with FP4 rows: per new row
+ *   amax = max_d |x_d|, scale = amax / 6, code_d = E2M1(x_d / scale)
+ * (both divisions fp32 round-to-nearest; codes rounded to the nearest
+ * magnitude, ties to the even code, saturated at 6; amax = 0 gives scale 0
+ * and zero codes), written as row pos[b] of k_cache / v_cache
+ * [B, Hkv, C, D/2 + 16] (uint8).  Arguments, mask, D and errors as for
+ * kvd_append_fp8.
+ */
+kvd_status kvd_append_fp4(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                          const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
+                          kvd_dtype new_dtype, int32_t* dev_status, kvd_stream_t stream);
+
+/*
+ * kvd_attend_masked_fp4 -- kvd_attend_masked over FP4 caches: the same
+ * definition with every K/V element dequantised (scale * E2M1(code)).
+ *   k_cache, v_cache uint8 [B, Hkv, C, D/2 + 16]; every other argument, the
+ * precision rules (E2M1 codes are exact in fp16), workspace, plan and paths as
+ * for kvd_attend_masked_fp8.
+ */
+size_t kvd_attend_masked_fp4_workspace_bytes(int B, int Hq, int Hkv, int C, int D, int num_splits);
+/* As kvd_attend_masked_plan, for kvd_attend_masked_fp4. */
+kvd_status kvd_attend_masked_fp4_plan(int B, int Hq, int Hkv, int C, int D, int num_splits,
+                                      kvd_plan* plan);
+kvd_status kvd_attend_masked_fp4(const void* q, const void* k_cache, const void* v_cache,
+                                 const uint8_t* mask, void* out, float* lse_out, int B, int Hq,
+                                 int Hkv, int C, int D, float scale, int num_splits,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                 kvd_stream_t stream);
+
+/*
  * kvd_attend_masked_noalloc -- the pages have no counterpart to this call; it
  * exists for callers that cannot allocate device memory.  Some host runtimes
  * own all device memory through their own allocator and hand a kernel library

@@ -30,20 +30,24 @@ def test_paged_and_gather_accounting():
     assert g == 2 * rows * (8 * 128 + 64) * 2 + 4 * 4 + 4 * 4
 
 
-def test_fp8_accounting_row_format():
-    """A quantised row is D E4M3 codes (one byte each) + one fp32 scale + 12
-    zero bytes: 144 bytes for D = 128, against 256 for a bf16 row, so the
-    cache part of the attention bytes shrinks to 144/256 of the bf16 figure
-    while the mask, q and out (bf16) stay."""
+def test_quantised_accounting_row_formats():
+    """A quantised row is D E4M3 codes (one byte each), or D/2 bytes of E2M1
+    code pairs, + one fp32 scale + 12 zero bytes: 144 or 80 bytes for
+    D = 128, against 256 for a bf16 row, so the cache part of the attention
+    bytes shrinks to 144/256 or 80/256 of the bf16 figure while the mask, q
+    and out (bf16) stay."""
     lengths, Hq, Hkv, C, D = [1, 64, 700], 32, 8, 1024, 128
     rows = sum(lengths)
-    f = bench.fp8_attend_bytes(lengths, Hq, Hkv, C, D, 16)
+    assert bench.quant_row_bytes("gqa_fp8", D) == 144
+    assert bench.quant_row_bytes("gqa_fp4", D) == 80
     b = bench.masked_attend_bytes(lengths, Hq, Hkv, C, D, 2)
     side = len(lengths) * C + 2 * len(lengths) * Hq * D * 2
-    assert f - side == rows * Hkv * 2 * 144
-    assert (f - side) * 256 == (b - side) * 144
-    # the append reads the bf16 row and writes the quantised one, K and V
-    assert bench.fp8_append_bytes(4, Hkv, D, 16) == 4 * Hkv * 2 * (256 + 144)
+    for row in (144, 80):
+        f = bench.quant_attend_bytes(lengths, Hq, Hkv, C, D, row)
+        assert f - side == rows * Hkv * 2 * row
+        assert (f - side) * 256 == (b - side) * row
+        # the append reads the bf16 row and writes the quantised one, K and V
+        assert bench.quant_append_bytes(4, Hkv, D, row) == 4 * Hkv * 2 * (256 + row)
 
 
 def test_indexed_accounting_counts_listed_rows_and_whole_lists():

@@ -43,7 +43,8 @@ from dataclasses import dataclass, field
 
 import torch
 
-SEEDS = {"tiny": 1, "npuw": 2, "gqa": 3, "paged": 4, "long": 5, "window": 6, "gqa_fp8": 7}
+SEEDS = {"tiny": 1, "npuw": 2, "gqa": 3, "paged": 4, "long": 5, "window": 6, "gqa_fp8": 7,
+         "gqa_fp4": 8}
 
 
 def generator(seed: int, device="cpu") -> torch.Generator:
@@ -85,6 +86,24 @@ def fp8_rows(g, shape, D: int, scale_lo: float = 2e-3, scale_hi: float = 2e-2, d
     out = torch.zeros(shape + (D + FP8_ROW_PAD,), dtype=torch.uint8, device=device)
     out[..., :D] = codes
     out[..., D:D + 4] = scale.contiguous().view(torch.uint8)
+    return out
+
+
+FP4_ROW_PAD = 16  # FP4 rows: D/2 bytes of E2M1 codes, fp32 scale, 12 zero bytes
+
+
+def fp4_rows(g, shape, D: int, scale_lo: float = 0.1, scale_hi: float = 0.4, device="cpu"):
+    """uint8 [*shape, D/2 + 16]: FP4 K/V rows with random content -- code
+    bytes uniform over 0..255 (every nibble is a finite E2M1 code), a scale
+    uniform in [scale_lo, scale_hi] as fp32 little-endian bytes, 12 zero
+    bytes.  Random bytes, not the result of quantising anything."""
+    shape = tuple(shape)
+    codes = torch.randint(0, 256, shape + (D // 2,), generator=g, device=device,
+                          dtype=torch.int32).to(torch.uint8)
+    scale = uniform(g, shape + (1,), scale_lo, scale_hi, torch.float32, device)
+    out = torch.zeros(shape + (D // 2 + FP4_ROW_PAD,), dtype=torch.uint8, device=device)
+    out[..., :D // 2] = codes
+    out[..., D // 2:D // 2 + 4] = scale.contiguous().view(torch.uint8)
     return out
 
 
@@ -249,13 +268,14 @@ def gqa(device="cpu", layers: int = 32, seed: int | None = None, B: int = 16,
     return w
 
 
-def fp8_layer(g, B, Hq, Hkv, C, D, lengths, device="cpu") -> MaskedLayer:
+def fp8_layer(g, B, Hq, Hkv, C, D, lengths, device="cpu", rows=None) -> MaskedLayer:
     """A static-buffer layer with quantised K/V caches (random rows, see
-    fp8_rows) holding lengths[b] - 1 rows before the step; q and the step's
-    new rows in bf16."""
+    fp8_rows; fp4_rows with rows=fp4_rows) holding lengths[b] - 1 rows
+    before the step; q and the step's new rows in bf16."""
     lengths = torch.as_tensor(lengths, dtype=torch.int64)
-    k = fp8_rows(g, (B, Hkv, C), D, device=device)
-    v = fp8_rows(g, (B, Hkv, C), D, device=device)
+    rows = rows or fp8_rows
+    k = rows(g, (B, Hkv, C), D, device=device)
+    v = rows(g, (B, Hkv, C), D, device=device)
     q = randn(g, (B, Hq, D), torch.bfloat16, device)
     k_new = randn(g, (B, Hkv, D), torch.bfloat16, device, 0.5)
     v_new = randn(g, (B, Hkv, D), torch.bfloat16, device)
@@ -276,6 +296,21 @@ def gqa_fp8(device="cpu", layers: int = 32, seed: int | None = None, B: int = 16
     w = MaskedWorkload("gqa_fp8", B, Hq, Hkv, C, D, torch.uint8)
     for _ in range(layers):
         w.layers.append(fp8_layer(g, B, Hq, Hkv, C, D, lengths, device))
+    return w
+
+
+def gqa_fp4(device="cpu", layers: int = 32, seed: int | None = None, B: int = 16,
+            Hq: int = 32, Hkv: int = 8, C: int = 8192, D: int = 128, lo: int = 512,
+            hi: int = 8192) -> MaskedWorkload:
+    """Batched GQA decode (the gqa shapes and length mix, drawn the same way)
+    over FP4 caches: rows of D/2 bytes of E2M1 codes + fp32 scale + 12 zero
+    bytes."""
+    gl = generator(SEEDS["gqa"] if seed is None else seed, "cpu")
+    lengths = randint(gl, B, lo, hi)
+    g = generator((SEEDS["gqa_fp4"] if seed is None else seed) + 1000, device)
+    w = MaskedWorkload("gqa_fp4", B, Hq, Hkv, C, D, torch.uint8)
+    for _ in range(layers):
+        w.layers.append(fp8_layer(g, B, Hq, Hkv, C, D, lengths, device, rows=fp4_rows))
     return w
 
 
