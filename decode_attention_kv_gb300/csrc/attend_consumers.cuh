@@ -280,15 +280,18 @@ struct MmaConsumer {
             }
             const bool v_lo = (vmask >> gid) & 1u, v_hi = (vmask >> (gid + 8)) & 1u;
 
-            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            // two accumulators (even and odd k-steps) halve the mma chain
+            float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < kKSteps; ++ks) {
                 uint32_t a[4];
                 const int row = slab0 + (lane & 15);
                 const int ch = (ks & 3) * 2 + (lane >> 4);
                 ldsm_x4(kbase + (ks >> 2) * kHalfBytes + swz128(row, ch), a);
-                mma_bf16(s, a, qb[ks][0], qb[ks][1]);
+                mma_bf16((ks & 1) ? s2 : s, a, qb[ks][0], qb[ks][1]);
             }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s[i] += s2[i];
             s[0] = v_lo ? s[0] * qscale : -INFINITY;
             s[1] = v_lo ? s[1] * qscale : -INFINITY;
             s[2] = v_hi ? s[2] * qscale : -INFINITY;
@@ -436,40 +439,47 @@ struct QuantMmaConsumer {
         for (int d = 0; d < kDBlocks; ++d) acc[d][0] = acc[d][1] = acc[d][2] = acc[d][3] = 0.f;
     }
 
-    __device__ __forceinline__ bool tile(unsigned char* kbuf, unsigned char* vbuf, uint64_t bits,
-                                         int warp, int lane, float qscale) {
+    // N 16-token slabs (rows at kb[n], vb[n]; validity vmask[n], nonzero)
+    // under one softmax update (the tiles use N = 1).
+    template <int N>
+    __device__ __forceinline__ void slabs(const unsigned char* const* kb,
+                                          const unsigned char* const* vb, const uint32_t* vmask,
+                                          int lane, float qscale) {
         const int gid = lane >> 2, tig = lane & 3;
+        // V scales of tokens gid, gid + 8 of each slab (0 for invalid rows)
+        // and the running power of two of the largest one
+        float sv0[N], sv1[N];
+        float smax = 0.f;
 #pragma unroll
-        for (int sl = 0; sl < kSlabsPerWarp; ++sl) {
-            const int slab0 = (warp * kSlabsPerWarp + sl) * 16;
-            const uint32_t vmask = (uint32_t)(bits >> slab0) & 0xffffu;
-            if (vmask == 0u) continue;
-            const bool v_lo = (vmask >> gid) & 1u, v_hi = (vmask >> (gid + 8)) & 1u;
-            // V scales of tokens gid, gid + 8 (0 for invalid rows) and the
-            // running power of two of the largest one
-            const unsigned char* vs = vbuf + (slab0 + gid) * kRowBytes + kCodeBytes;
-            const float sv0 = v_lo ? *reinterpret_cast<const float*>(vs) : 0.f;
-            const float sv1 = v_hi ? *reinterpret_cast<const float*>(vs + 8 * kRowBytes) : 0.f;
-            float smax = fmaxf(sv0, sv1);
+        for (int n = 0; n < N; ++n) {
+            const unsigned char* vs = vb[n] + gid * kRowBytes + kCodeBytes;
+            sv0[n] = (vmask[n] >> gid) & 1u ? *reinterpret_cast<const float*>(vs) : 0.f;
+            sv1[n] = (vmask[n] >> (gid + 8)) & 1u ? *reinterpret_cast<const float*>(vs + 8 * kRowBytes)
+                                                  : 0.f;
+            smax = fmaxf(smax, fmaxf(sv0[n], sv1[n]));
+        }
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1)
-                smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, off));
-            const int es = (__float_as_int(smax) >> 23) & 0xff;  // warp-uniform
-            if (es > ve) {
-                const float r = pow2i(ve - es);
+        for (int off = 4; off < 32; off <<= 1)
+            smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, off));
+        const int es = (__float_as_int(smax) >> 23) & 0xff;  // warp-uniform
+        if (es > ve) {
+            const float r = pow2i(ve - es);
 #pragma unroll
-                for (int d = 0; d < kDBlocks; ++d) {
-                    acc[d][0] *= r;
-                    acc[d][1] *= r;
-                    acc[d][2] *= r;
-                    acc[d][3] *= r;
-                }
-                ve = es;
-                vinv = pow2i(127 - es);
+            for (int d = 0; d < kDBlocks; ++d) {
+                acc[d][0] *= r;
+                acc[d][1] *= r;
+                acc[d][2] *= r;
+                acc[d][3] *= r;
             }
+            ve = es;
+            vinv = pow2i(127 - es);
+        }
 
-            // ---- q.K^T: tokens gid, gid + 8 of the slab
-            const unsigned char* k0 = kbuf + (slab0 + gid) * kRowBytes;
+        // ---- q.K^T: tokens gid, gid + 8 of each slab
+        float s[N][4];
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+            const unsigned char* k0 = kb[n] + gid * kRowBytes;
             const unsigned char* k1 = k0 + 8 * kRowBytes;
             uint32_t kw0[kKWords], kw1[kKWords];
             constexpr int kLaneKBytes = 4 * kKWords;
@@ -489,7 +499,8 @@ struct QuantMmaConsumer {
             }
             const float sk0 = *reinterpret_cast<const float*>(k0 + kCodeBytes) * qscale;
             const float sk1 = *reinterpret_cast<const float*>(k1 + kCodeBytes) * qscale;
-            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            // one slab: two accumulators (even and odd k-steps) halve the mma chain
+            float t[4] = {0.f, 0.f, 0.f, 0.f}, t2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < kKSteps; ++ks) {
                 uint32_t a[4];
@@ -507,48 +518,68 @@ struct QuantMmaConsumer {
                     a[2] = e4m3x2_to_f16x2(kw0[ks] >> 16);
                     a[3] = e4m3x2_to_f16x2(kw1[ks] >> 16);
                 }
-                mma_f16(s, a, qb[ks][0], qb[ks][1]);
+                mma_f16((N == 1 && (ks & 1)) ? t2 : t, a, qb[ks][0], qb[ks][1]);
             }
-            s[0] = v_lo ? s[0] * sk0 : -INFINITY;
-            s[1] = v_lo ? s[1] * sk0 : -INFINITY;
-            s[2] = v_hi ? s[2] * sk1 : -INFINITY;
-            s[3] = v_hi ? s[3] * sk1 : -INFINITY;
+            const bool v_lo = (vmask[n] >> gid) & 1u, v_hi = (vmask[n] >> (gid + 8)) & 1u;
+            s[n][0] = v_lo ? (t[0] + t2[0]) * sk0 : -INFINITY;
+            s[n][1] = v_lo ? (t[1] + t2[1]) * sk0 : -INFINITY;
+            s[n][2] = v_hi ? (t[2] + t2[2]) * sk1 : -INFINITY;
+            s[n][3] = v_hi ? (t[3] + t2[3]) * sk1 : -INFINITY;
+        }
 
-            float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-            }
-            const bool up0 = mx0 > m[0] + kSkipScale, up1 = mx1 > m[1] + kSkipScale;
-            const float mn0 = up0 ? mx0 : m[0], mn1 = up1 ? mx1 : m[1];
-            const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float c0 = up0 ? fast_exp2(m[0] - b0) : 1.f, c1 = up1 ? fast_exp2(m[1] - b1) : 1.f;
-            m[0] = mn0;
-            m[1] = mn1;
-            const float p0 = fast_exp2(s[0] - b0), p1 = fast_exp2(s[1] - b1);
-            const float p2 = fast_exp2(s[2] - b0), p3 = fast_exp2(s[3] - b1);
-            l[0] = fmaf(l[0], c0, p0 + p2);
-            l[1] = fmaf(l[1], c1, p1 + p3);
-            if (__any_sync(0xffffffffu, up0 || up1)) {
-                const float2 cc = make_float2(c0, c1);
+        for (int n = 0; n < N; ++n) {
+            mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][2]));
+            mx1 = fmaxf(mx1, fmaxf(s[n][1], s[n][3]));
+        }
 #pragma unroll
-                for (int d = 0; d < kDBlocks; ++d) {
-                    const float2 x = fmul2(make_float2(acc[d][0], acc[d][1]), cc);
-                    const float2 y = fmul2(make_float2(acc[d][2], acc[d][3]), cc);
-                    acc[d][0] = x.x;
-                    acc[d][1] = x.y;
-                    acc[d][2] = y.x;
-                    acc[d][3] = y.y;
-                }
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const bool up0 = mx0 > m[0] + kSkipScale, up1 = mx1 > m[1] + kSkipScale;
+        const float mn0 = up0 ? mx0 : m[0], mn1 = up1 ? mx1 : m[1];
+        const float b0 = mn0 == -INFINITY ? 0.f : mn0, b1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float c0 = up0 ? fast_exp2(m[0] - b0) : 1.f, c1 = up1 ? fast_exp2(m[1] - b1) : 1.f;
+        m[0] = mn0;
+        m[1] = mn1;
+        float p[N][4];
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+            p[n][0] = fast_exp2(s[n][0] - b0);
+            p[n][1] = fast_exp2(s[n][1] - b1);
+            p[n][2] = fast_exp2(s[n][2] - b0);
+            p[n][3] = fast_exp2(s[n][3] - b1);
+            ps0 += p[n][0] + p[n][2];
+            ps1 += p[n][1] + p[n][3];
+        }
+        l[0] = fmaf(l[0], c0, ps0);
+        l[1] = fmaf(l[1], c1, ps1);
+        if (__any_sync(0xffffffffu, up0 || up1)) {
+            const float2 cc = make_float2(c0, c1);
+#pragma unroll
+            for (int d = 0; d < kDBlocks; ++d) {
+                const float2 x = fmul2(make_float2(acc[d][0], acc[d][1]), cc);
+                const float2 y = fmul2(make_float2(acc[d][2], acc[d][3]), cc);
+                acc[d][0] = x.x;
+                acc[d][1] = x.y;
+                acc[d][2] = y.x;
+                acc[d][3] = y.y;
             }
+        }
 
-            // ---- p.V: weights times V scale / 2^ve in f16, zero for invalid rows
-            const float w0 = sv0 * vinv, w1 = sv1 * vinv;
-            const uint32_t pk_lo = pack_f16x2(p0 * w0, p1 * w0);
-            const uint32_t pk_hi = pack_f16x2(p2 * w1, p3 * w1);
-            const uint32_t bh0 = movmatrix_trans(pk_lo), bh1 = movmatrix_trans(pk_hi);
-
+        // ---- p.V: weights times V scale / 2^ve in f16, zero for invalid rows
+        uint32_t bh0[N], bh1[N];
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+            const float w0 = sv0[n] * vinv, w1 = sv1[n] * vinv;
+            bh0[n] = movmatrix_trans(pack_f16x2(p[n][0] * w0, p[n][1] * w0));
+            bh1[n] = movmatrix_trans(pack_f16x2(p[n][2] * w1, p[n][3] * w1));
+        }
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
             // V codes of tokens 2tig, 2tig+1, 2tig+8, 2tig+9: the lane's D/8
             // dims from byte (D/8)gid (E4M3) or (D/16)gid (E2M1); codes of
             // invalid rows become 0 (NaN codes must not meet a 0 weight)
@@ -556,8 +587,8 @@ struct QuantMmaConsumer {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int t = 2 * tig + (u & 1) + (u >> 1) * 8;
-                const unsigned char* vr = vbuf + (slab0 + t) * kRowBytes + 4 * kVWords * gid;
-                const bool ok = (vmask >> t) & 1u;
+                const unsigned char* vr = vb[n] + t * kRowBytes + 4 * kVWords * gid;
+                const bool ok = (vmask[n] >> t) & 1u;
                 if constexpr (kVWords == 4) {
                     const uint4 x = *reinterpret_cast<const uint4*>(vr);
                     vw[u][0] = ok ? x.x : 0u;
@@ -573,19 +604,31 @@ struct QuantMmaConsumer {
                     vw[u][0] = ok ? x : 0u;
                 }
             }
+            // FP4: byte j of the lane's range holds dims 2j (low nibble) and
+            // 2j + 1 (high); pair the two tokens of a fragment register
+            // nibble-wise, four bytes (blocks) per word: byte j of vlo[.]
+            // holds (dim 2j of token 2tig | of token 2tig + 1), of vhi[.] dim
+            // 2j + 1
+            uint32_t vlo[2][kVWords], vhi[2][kVWords];
+            if constexpr (kFp4) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int w = 0; w < kVWords; ++w) {
+                        const uint32_t x0 = vw[2 * h][w], x1 = vw[2 * h + 1][w];
+                        vlo[h][w] = (x0 & 0x0f0f0f0fu) | ((x1 << 4) & 0xf0f0f0f0u);
+                        vhi[h][w] = ((x0 >> 4) & 0x0f0f0f0fu) | (x1 & 0xf0f0f0f0u);
+                    }
+            }
 #pragma unroll
             for (int j = 0; j < kDBlocks; ++j) {
                 uint32_t a[4];
                 if constexpr (kFp4) {
-                    // byte j of the lane's range: dims 2j (low nibble), 2j + 1 (high);
-                    // pair the two tokens of a fragment register nibble-wise
                     const int w = j >> 2, sh = 8 * (j & 3);
-                    const uint32_t x0 = vw[0][w] >> sh, x1 = vw[1][w] >> sh;
-                    const uint32_t x2 = vw[2][w] >> sh, x3 = vw[3][w] >> sh;
-                    a[0] = e2m1x2_to_f16x2((x0 & 0x0fu) | ((x1 & 0x0fu) << 4));
-                    a[1] = e2m1x2_to_f16x2(((x0 >> 4) & 0x0fu) | (x1 & 0xf0u));
-                    a[2] = e2m1x2_to_f16x2((x2 & 0x0fu) | ((x3 & 0x0fu) << 4));
-                    a[3] = e2m1x2_to_f16x2(((x2 >> 4) & 0x0fu) | (x3 & 0xf0u));
+                    a[0] = e2m1x2_to_f16x2(vlo[0][w] >> sh);
+                    a[1] = e2m1x2_to_f16x2(vhi[0][w] >> sh);
+                    a[2] = e2m1x2_to_f16x2(vlo[1][w] >> sh);
+                    a[3] = e2m1x2_to_f16x2(vhi[1][w] >> sh);
                 } else {
                     const uint32_t sel = (j & 1) ? 0x7362u : 0x5140u;  // bytes 2j%4, 2j%4+1 of two rows
                     const uint32_t lo = byte_perm(vw[0][j >> 1], vw[1][j >> 1], sel);
@@ -595,8 +638,21 @@ struct QuantMmaConsumer {
                     a[2] = e4m3x2_to_f16x2(hi);
                     a[3] = e4m3x2_to_f16x2(hi >> 16);
                 }
-                mma_f16(acc[j], a, bh0, bh1);
+                mma_f16(acc[j], a, bh0[n], bh1[n]);
             }
+        }
+    }
+
+    __device__ __forceinline__ bool tile(unsigned char* kbuf, unsigned char* vbuf, uint64_t bits,
+                                         int warp, int lane, float qscale) {
+#pragma unroll
+        for (int sl = 0; sl < kSlabsPerWarp; ++sl) {
+            const int slab0 = (warp * kSlabsPerWarp + sl) * 16;
+            const uint32_t vmask = (uint32_t)(bits >> slab0) & 0xffffu;
+            if (vmask == 0u) continue;
+            const unsigned char* kb = kbuf + slab0 * kRowBytes;
+            const unsigned char* vb = vbuf + slab0 * kRowBytes;
+            slabs<1>(&kb, &vb, &vmask, lane, qscale);
         }
         return false;  // the ring is only read
     }
