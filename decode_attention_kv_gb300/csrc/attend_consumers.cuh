@@ -257,7 +257,7 @@ struct MmaConsumer {
 
     __device__ __forceinline__ bool tile(unsigned char* kbuf, unsigned char* vbuf, uint64_t bits,
                                          int warp, int lane, float qscale) {
-        const int gid = lane >> 2, tig = lane & 3;
+        const int gid = lane >> 2;
         const uint32_t kbase = smem_u32(kbuf), vbase = smem_u32(vbuf);
         bool wrote = false;
 #pragma unroll

@@ -179,12 +179,12 @@ struct UnitSlot {
 };
 
 // Shared-memory control block:
-// full[STAGES] | empty[STAGES] | qfull[Q] | qempty[Q] | mfull[M] | mempty[M] | meta[STAGES] |
-// abort | pending | mhdr[M] | slots[Q]
+// full[STAGES] | empty[STAGES] | gjob[STAGES] | qfull[Q] | qempty[Q] | mfull[M] | mempty[M] |
+// meta[STAGES] | abort | pending | mhdr[M] | slots[Q]
 template <int STAGES, int MB>
 struct CtlLayout {
     static constexpr int kBar = 0;
-    static constexpr int kQBar = kBar + 2 * STAGES * 8;
+    static constexpr int kQBar = kBar + 3 * STAGES * 8;
     static constexpr int kMBar = kQBar + 2 * kQueueSlots * 8;
     static constexpr int kMeta = kMBar + 2 * MB * 8;
     static constexpr int kAbort = kMeta + STAGES * (int)sizeof(StageMeta);
@@ -198,6 +198,7 @@ template <int STAGES, int MB>
 struct Ctl {
     uint64_t* full;     // ring stage landed (loader -> consumers)
     uint64_t* empty;    // ring stage consumed (consumers -> loader)
+    uint64_t* gjob;     // index-list mode: stage's tile posted (loader -> gather warp)
     uint64_t* qfull;    // unit slot filled (scheduler -> loader)
     uint64_t* qempty;   // unit slot read (loader -> scheduler)
     uint64_t* mfull;    // merge buffer filled (consumers -> epilogue)
@@ -211,6 +212,7 @@ struct Ctl {
         using L = CtlLayout<STAGES, MB>;
         full = reinterpret_cast<uint64_t*>(base + L::kBar);
         empty = full + STAGES;
+        gjob = empty + STAGES;
         qfull = reinterpret_cast<uint64_t*>(base + L::kQBar);
         qempty = qfull + kQueueSlots;
         mfull = reinterpret_cast<uint64_t*>(base + L::kMBar);
@@ -284,6 +286,40 @@ __device__ __forceinline__ SplitRange split_range(const AttendParams& p, int bz,
     r.ntok = max(0, r.t_end - r.t_begin);
     r.ntiles = (r.ntok + p.tile - 1) / p.tile;
     return r;
+}
+
+// Index-list mode: one warp gathers tile rows [row0, min(n, row1)) of a kv
+// head's plane (row1 - row0 <= 32; row j's cache slot in lane j - row0's
+// `slot`, -1: not listed) into a stage with 16-byte cp.async copies, a warp pass covering
+// 32 / cpr whole rows (K and V), each chunk landing where the consumer's
+// layout puts it.  (Per-row TMA boxes, four rows per box at best, issue too
+// slowly here: the tensor engine's per-copy cost bounds a 512-byte box.)
+template <class Cons, typename Elem, int D>
+__device__ __forceinline__ void gather_rows(unsigned char* gk, unsigned char* gv, const Elem* k,
+                                            const Elem* v, size_t plane, int slot, int row0,
+                                            int row1, int n, int lane, uint64_t pol) {
+    constexpr int kHalves = D / 64;
+    constexpr int cpr = D * (int)sizeof(Elem) / 16, rpi = 32 / cpr;
+    constexpr int epc = 16 / (int)sizeof(Elem);  // elements per chunk
+    const int c = lane % cpr;
+    const Elem* kb = k + plane * D + c * epc;
+    const Elem* vb = v + plane * D + c * epc;
+    const int rows = min(n, row1) - row0;
+#pragma unroll 4
+    for (int rb = 0; rb < rows; rb += rpi) {
+        const int rr = rb + lane / cpr;
+        const int slot_row = __shfl_sync(0xffffffffu, slot, rr & 31);
+        if (rr < rows && slot_row >= 0) {
+            const int row = row0 + rr;
+            uint32_t off;
+            if constexpr (Cons::kSwizzled)
+                off = (c >> 3) * (Cons::kTileBytes / kHalves) + swz128(row, c & 7);
+            else
+                off = row * D * (int)sizeof(Elem) + c * 16;
+            cp_async16(gk + off, kb + (size_t)slot_row * D, pol);
+            cp_async16(gv + off, vb + (size_t)slot_row * D, pol);
+        }
+    }
 }
 
 // Validity bits of relative tokens [r0, r0 + n) of the split (n <= 64).
@@ -537,7 +573,17 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
     using Elem = typename Cons::ElemT;
     constexpr int D = Cons::kD, G = Cons::kG, NCW = Cons::kNCW;
     constexpr int kHalves = D / 64;
+    constexpr bool PAGED = MODE == kModePaged;
+    constexpr bool INDEXED = MODE == kModeIndexed;
+    // Index-list mode: the last kGatherN scheduler warps gather shares of
+    // each tile's rows beside the loader (its 16-byte copies, one per lane,
+    // are what bounds that mode); the others schedule.
+    constexpr int kGatherN = INDEXED ? 1 : 0;
+    constexpr int kSchedN = kSchedWarps - kGatherN;
     constexpr int kLoader = NCW, kSched0 = NCW + 1, kEpilogue = NCW + 1 + kSchedWarps;
+    constexpr int kGather = kSched0 + kSchedN;  // first gather warp (index-list mode)
+    // rows [gather_row(w), gather_row(w + 1)) of a tile: loader w = 0, gather warps 1..
+    auto gather_row = [&](int w) { return w * p.tile / (kGatherN + 1); };
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -548,12 +594,14 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&ctl.full[s], 1);
+            mbar_init(&ctl.full[s], 1 + kGatherN);  // the loader (and the gather warps)
             mbar_init(&ctl.empty[s], NCW);
+            mbar_init(&ctl.gjob[s], 1);
         }
         for (int s = 0; s < kQueueSlots; ++s) {
-            mbar_init(&ctl.qfull[s], 32);   // every scheduler lane publishes its writes
-            mbar_init(&ctl.qempty[s], 32);  // every loader lane is done reading
+            mbar_init(&ctl.qfull[s], 32);  // every scheduler lane publishes its writes
+            // every loader (and gather-warp) lane is done reading
+            mbar_init(&ctl.qempty[s], 32 * (1 + kGatherN));
         }
         for (int s = 0; s < MB; ++s) {
             mbar_init(&ctl.mfull[s], NCW * 32);  // every consumer thread publishes its state
@@ -563,8 +611,6 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
         *ctl.pending = 0;
         fence_barrier_init();
     }
-    constexpr bool PAGED = MODE == kModePaged;
-    constexpr bool INDEXED = MODE == kModeIndexed;
     static_assert(MODE == kModeMasked || Cons::kRowBytes == D * (int)sizeof(Elem),
                   "quantised rows: static-buffer mode only");
     if (threadIdx.x == 32 * kLoader && (PAGED || Cons::kSwizzled) && !INDEXED) {
@@ -575,7 +621,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
     pdl_wait();
     __syncthreads();
 
-    if (warp >= kSched0 && warp < kSched0 + kSchedWarps) {
+    if (warp >= kSched0 && warp < kSched0 + kSchedN) {
         // ========================================================= schedulers
         // Each takes units, reads their metadata (sequence length, mask or
         // block table) and queues them for the loader in its own ring of
@@ -587,12 +633,12 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
         bool failed = false;
         // Work counter: the first unit of each scheduler is fixed, the counter
         // hands out the others in order after them.  With enough units a CTA
-        // starts with kSchedWarps consecutive units -- one split of rows that
+        // starts with one unit per scheduler warp, consecutive -- one split of rows that
         // share their mask row or sequence, so that the metadata reads after
         // the first hit L1 -- else the first units are spread over all CTAs.
-        const int n_sched = kSchedWarps * (int)gridDim.x;
+        const int n_sched = kSchedN * (int)gridDim.x;
         const int first_units = n_sched;
-        int u = p.units >= n_sched ? (int)blockIdx.x * kSchedWarps + sw
+        int u = p.units >= n_sched ? (int)blockIdx.x * kSchedN + sw
                                    : sw * (int)gridDim.x + (int)blockIdx.x;
         auto publish = [&](int slot) {
             mbar_arrive(&ctl.qfull[slot]);
@@ -698,6 +744,50 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
         return;
     }
 
+    if constexpr (INDEXED) {
+        if (warp >= kGather && warp < kGather + kGatherN) {
+            // ==================================================== gather warps
+            // A share of the rows of every tile the loader posts, in ring
+            // order; the unit's slot is released (with the loader) after its
+            // last tile.
+            const int gw = warp - kGather + 1;
+            const int row0 = gather_row(gw), row1 = gather_row(gw + 1);
+            const uint64_t pol = policy_evict_first();
+            int stage = 0;
+            uint32_t phase = 0;
+            while (true) {
+                if (!warp_wait(&ctl.gjob[stage], phase, ctl.abort_flag)) break;
+                const StageMeta mt = ctl.meta[stage];
+                if (mt.flags & kEnd) break;
+                const int slot = (int)mt.pad;
+                const UnitSlot& sl = ctl.slots[slot];
+                const Unit un = decode_unit(p, G, mt.unit);
+                const int r0 = mt.tile * p.tile;
+                const int n = min(p.tile, sl.ntok - r0);
+                const int row = row0 + lane;
+                const int s_row = row < min(n, row1) && ((mt.bits >> row) & 1ull)
+                                      ? sl.blocks[r0 + row] : -1;
+                if (n > row0) {
+                    unsigned char* gk = smem + stage * Sh::kStageBytes;
+                    gather_rows<Cons, Elem, D>(gk, gk + Cons::kTileBytes,
+                                               static_cast<const Elem*>(p.k),
+                                               static_cast<const Elem*>(p.v),
+                                               ((size_t)un.bz * p.Hkv + un.kvh) * p.C, s_row,
+                                               row0, row1, n, lane, pol);
+                }
+                cp_async_mbar_arrive(&ctl.full[stage]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl.full[stage]);
+                if (mt.flags & kLast) mbar_arrive(&ctl.qempty[slot]);  // every lane
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            return;
+        }
+    }
+
     if (warp == kEpilogue) {
         // =========================================================== epilogue
         // Turns each finished unit's merge buffer into output or partial rows,
@@ -753,7 +843,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
         int spec_n = 0, spec_unit = -1;
         uint32_t spec_mask = 0;  // stages issued but not yet delivered
         if constexpr (MODE == kModeMasked) {
-            const int n_sched = kSchedWarps * (int)gridDim.x;
+            const int n_sched = kSchedN * (int)gridDim.x;
             const int u0 = (int)blockIdx.x;  // scheduler 0's first unit when units < n_sched
             if (p.units < n_sched && u0 < p.units) {
                 const Unit un0 = decode_unit(p, G, u0);
@@ -808,7 +898,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
         // starting with the ring it did not take last (scheduler 0's ring
         // first while speculated tiles wait for it).
         int rpos[kSchedWarps] = {};
-        uint32_t rphase = 0, live = (1u << kSchedWarps) - 1u;
+        uint32_t rphase = 0, live = (1u << kSchedN) - 1u;
         int pref = 0;
         while (!failed && live) {
             int pick = -1;
@@ -816,8 +906,8 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                 const unsigned long long t0 = global_timer_ns();
                 for (uint32_t it = 0;; ++it) {
 #pragma unroll
-                    for (int k = 0; k < kSchedWarps; ++k) {
-                        const int rr = (pref + k) % kSchedWarps;
+                    for (int k = 0; k < kSchedN; ++k) {
+                        const int rr = (pref + k) % kSchedN;
                         if (spec_n > 0 && rr != 0) continue;
                         int hp = 0;
 #pragma unroll
@@ -852,7 +942,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                     rpos[q] = 0;
                     rphase ^= 1u << q;
                 }
-            pref = (pick + 1) % kSchedWarps;
+            pref = (pick + 1) % kSchedN;
             const UnitSlot& sl = ctl.slots[slot];
             bool first = true;
             int counted = 0;  // tiles already taken off ctl.pending
@@ -897,52 +987,39 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                 if (!bits) continue;  // all-zero tile: never read
                 if (!acquire()) break;
                 if constexpr (INDEXED) {
-                    // Gather the tile's listed rows: 16-byte cp.async copies, a
-                    // warp pass covering 32 / cpr whole rows (K and V), each chunk
-                    // landing where the consumer's layout puts it.  The stage's
-                    // full barrier waits for them through the cp.async arrival,
-                    // made before lane 0's own arrival below.  (Per-row TMA
-                    // boxes, four rows per box at best, issue too slowly here:
-                    // the tensor engine's per-copy cost bounds a 512-byte box.)
-                    unsigned char* gk = smem + stage * Sh::kStageBytes;
-                    unsigned char* gv = gk + Cons::kTileBytes;
-                    constexpr int cpr = D * (int)sizeof(Elem) / 16, rpi = 32 / cpr;
-                    constexpr int epc = 16 / (int)sizeof(Elem);  // elements per chunk
-                    const int c = lane % cpr;
-                    const size_t plane = ((size_t)un.bz * p.Hkv + un.kvh) * p.C;
-                    const Elem* kb = static_cast<const Elem*>(p.k) + plane * D + c * epc;
-                    const Elem* vb = static_cast<const Elem*>(p.v) + plane * D + c * epc;
-                    // slots of tile rows lane and lane + 32 (-1: unlisted or past the tile)
-                    const int s_lo = lane < n && ((bits >> lane) & 1ull) ? sl.blocks[r0 + lane] : -1;
-                    const int s_hi = lane + 32 < n && ((bits >> (lane + 32)) & 1ull)
-                                         ? sl.blocks[r0 + lane + 32] : -1;
-#pragma unroll 4
-                    for (int rb = 0; rb < n; rb += rpi) {
-                        const int row = rb + lane / cpr;
-                        const int a = __shfl_sync(0xffffffffu, s_lo, row & 31);
-                        const int b = __shfl_sync(0xffffffffu, s_hi, row & 31);
-                        const int slot_row = row < 32 ? a : b;
-                        if (row < n && slot_row >= 0) {
-                            uint32_t off;
-                            if constexpr (Cons::kSwizzled)
-                                off = (c >> 3) * (Cons::kTileBytes / kHalves) + swz128(row, c & 7);
-                            else
-                                off = row * D * (int)sizeof(Elem) + c * 16;
-                            cp_async16(gk + off, kb + (size_t)slot_row * D, pol);
-                            cp_async16(gv + off, vb + (size_t)slot_row * D, pol);
-                        }
+                    // Post the tile to the gather warps, gather the first share
+                    // of its rows here.  The stage's full barrier waits for
+                    // every warp's copies through its cp.async arrivals, each
+                    // made before that warp's own arrival.
+                    if (lane == 0) {
+                        StageMeta& mt = ctl.meta[stage];
+                        mt.unit = sl.unit;
+                        mt.tile = i;
+                        mt.flags = (first ? kFirst : 0u) | (i == last ? kLast : 0u);
+                        mt.pad = (uint32_t)slot;
+                        mt.bits = bits;
+                        mbar_arrive(&ctl.gjob[stage]);
                     }
+                    unsigned char* gk = smem + stage * Sh::kStageBytes;
+                    const int g1 = gather_row(1);
+                    const int s_lo = lane < min(n, g1) && ((bits >> lane) & 1ull) ? sl.blocks[r0 + lane] : -1;
+                    gather_rows<Cons, Elem, D>(gk, gk + Cons::kTileBytes, static_cast<const Elem*>(p.k),
+                                               static_cast<const Elem*>(p.v),
+                                               ((size_t)un.bz * p.Hkv + un.kvh) * p.C, s_lo, 0, g1,
+                                               n, lane, pol);
                     cp_async_mbar_arrive(&ctl.full[stage]);
                     __syncwarp();
                 }
                 if (lane == 0) {
                     atomicAdd(ctl.pending, -(i + 1 - counted) * p.tile);
                     counted = i + 1;
-                    StageMeta& mt = ctl.meta[stage];
-                    mt.unit = sl.unit;
-                    mt.tile = i;
-                    mt.flags = (first ? kFirst : 0u) | (i == last ? kLast : 0u);
-                    mt.bits = bits;
+                    if constexpr (!INDEXED) {  // (posted above in index-list mode)
+                        StageMeta& mt = ctl.meta[stage];
+                        mt.unit = sl.unit;
+                        mt.tile = i;
+                        mt.flags = (first ? kFirst : 0u) | (i == last ? kLast : 0u);
+                        mt.bits = bits;
+                    }
                     unsigned char* sk = smem + stage * Sh::kStageBytes;
                     unsigned char* sv = sk + Cons::kTileBytes;
                     unsigned char* sq = sv + Cons::kTileBytes;
@@ -1010,6 +1087,11 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
             if (lane == 0) {
                 ctl.meta[stage].flags = kEnd;
                 mbar_arrive(&ctl.full[stage]);
+                if constexpr (INDEXED) {
+                    for (int w = 0; w < kGatherN; ++w)
+                        mbar_arrive(&ctl.full[stage]);  // in place of the gather warps' arrivals
+                    mbar_arrive(&ctl.gjob[stage]);
+                }
             }
             __syncwarp();
         } else {
