@@ -482,6 +482,7 @@ struct QuantMmaConsumer {
             const unsigned char* k0 = kb[n] + gid * kRowBytes;
             const unsigned char* k1 = k0 + 8 * kRowBytes;
             uint32_t kw0[kKWords], kw1[kKWords];
+            uint32_t kf0[4], kf1[4];  // FP4: one word's four converted pairs
             constexpr int kLaneKBytes = 4 * kKWords;
             if constexpr (kKWords >= 4) {
 #pragma unroll
@@ -505,18 +506,25 @@ struct QuantMmaConsumer {
             for (int ks = 0; ks < kKSteps; ++ks) {
                 uint32_t a[4];
                 if constexpr (kFp4) {
-                    // two bytes per k-step: dims 4ks..4ks+1, 4ks+2..4ks+3 of the lane's range
-                    const uint32_t w0 = kw0[ks >> 1] >> (16 * (ks & 1));
-                    const uint32_t w1 = kw1[ks >> 1] >> (16 * (ks & 1));
-                    a[0] = e2m1x2_to_f16x2(w0);
-                    a[1] = e2m1x2_to_f16x2(w1);
-                    a[2] = e2m1x2_to_f16x2(w0 >> 8);
-                    a[3] = e2m1x2_to_f16x2(w1 >> 8);
+                    // one word per two k-steps: bytes 2(ks%2), 2(ks%2)+1 hold dims
+                    // 4ks..4ks+1 and 4ks+2..4ks+3 of the lane's range
+                    if ((ks & 1) == 0) {
+                        e2m1x8_to_f16x2x4(kw0[ks >> 1], kf0);
+                        e2m1x8_to_f16x2x4(kw1[ks >> 1], kf1);
+                    }
+                    const int h = 2 * (ks & 1);
+                    a[0] = kf0[h];
+                    a[1] = kf1[h];
+                    a[2] = kf0[h + 1];
+                    a[3] = kf1[h + 1];
                 } else {
-                    a[0] = e4m3x2_to_f16x2(kw0[ks]);
-                    a[1] = e4m3x2_to_f16x2(kw1[ks]);
-                    a[2] = e4m3x2_to_f16x2(kw0[ks] >> 16);
-                    a[3] = e4m3x2_to_f16x2(kw1[ks] >> 16);
+                    uint32_t x[2], y[2];
+                    e4m3x4_to_f16x2x2(kw0[ks], x);
+                    e4m3x4_to_f16x2x2(kw1[ks], y);
+                    a[0] = x[0];
+                    a[1] = y[0];
+                    a[2] = x[1];
+                    a[3] = y[1];
                 }
                 mma_f16((N == 1 && (ks & 1)) ? t2 : t, a, qb[ks][0], qb[ks][1]);
             }
@@ -620,23 +628,31 @@ struct QuantMmaConsumer {
                         vhi[h][w] = ((x0 >> 4) & 0x0f0f0f0fu) | (x1 & 0xf0f0f0f0u);
                     }
             }
+            uint32_t f[4][4];  // FP4: the converted pairs of one word of vlo / vhi
 #pragma unroll
             for (int j = 0; j < kDBlocks; ++j) {
                 uint32_t a[4];
                 if constexpr (kFp4) {
-                    const int w = j >> 2, sh = 8 * (j & 3);
-                    a[0] = e2m1x2_to_f16x2(vlo[0][w] >> sh);
-                    a[1] = e2m1x2_to_f16x2(vhi[0][w] >> sh);
-                    a[2] = e2m1x2_to_f16x2(vlo[1][w] >> sh);
-                    a[3] = e2m1x2_to_f16x2(vhi[1][w] >> sh);
+                    const int w = j >> 2, b = j & 3;
+                    if (b == 0) {
+                        e2m1x8_to_f16x2x4(vlo[0][w], f[0]);
+                        e2m1x8_to_f16x2x4(vhi[0][w], f[1]);
+                        e2m1x8_to_f16x2x4(vlo[1][w], f[2]);
+                        e2m1x8_to_f16x2x4(vhi[1][w], f[3]);
+                    }
+                    a[0] = f[0][b];
+                    a[1] = f[1][b];
+                    a[2] = f[2][b];
+                    a[3] = f[3][b];
                 } else {
                     const uint32_t sel = (j & 1) ? 0x7362u : 0x5140u;  // bytes 2j%4, 2j%4+1 of two rows
-                    const uint32_t lo = byte_perm(vw[0][j >> 1], vw[1][j >> 1], sel);
-                    const uint32_t hi = byte_perm(vw[2][j >> 1], vw[3][j >> 1], sel);
-                    a[0] = e4m3x2_to_f16x2(lo);
-                    a[1] = e4m3x2_to_f16x2(lo >> 16);
-                    a[2] = e4m3x2_to_f16x2(hi);
-                    a[3] = e4m3x2_to_f16x2(hi >> 16);
+                    uint32_t x[2], y[2];
+                    e4m3x4_to_f16x2x2(byte_perm(vw[0][j >> 1], vw[1][j >> 1], sel), x);
+                    e4m3x4_to_f16x2x2(byte_perm(vw[2][j >> 1], vw[3][j >> 1], sel), y);
+                    a[0] = x[0];
+                    a[1] = x[1];
+                    a[2] = y[0];
+                    a[3] = y[1];
                 }
                 mma_f16(acc[j], a, bh0[n], bh1[n]);
             }

@@ -56,6 +56,25 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t x) {
     return r;
 }
 
+// The two E4M3 code pairs of x (bytes 0-1 -> r[0], bytes 2-3 -> r[1]) ->
+// f16x2, exactly; the halves feed the conversions as they are.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t* r) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(r[0]), "=r"(r[1])
+        : "r"(x));
+}
+
+// The four E2M1 code pairs of x (byte i -> r[i], low nibble -> low half) ->
+// f16x2, exactly; the bytes feed the conversions as they are.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t x, uint32_t* r) {
+    asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\tmov.b32 {c0, c1, c2, c3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, c0;\n\tcvt.rn.f16x2.e2m1x2 %1, c1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, c2;\n\tcvt.rn.f16x2.e2m1x2 %3, c3;\n\t}"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+        : "r"(x));
+}
+
 // Byte select of two words (prmt): result byte i = byte sel_i of {b:a}.
 __device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
