@@ -475,6 +475,39 @@ struct QuantMmaConsumer {
             vinv = pow2i(127 - es);
         }
 
+        // V codes of tokens 2tig, 2tig+1, 2tig+8, 2tig+9 of slab n: the lane's
+        // D/8 dims from byte (D/8)gid (E4M3) or (D/16)gid (E2M1); codes of
+        // invalid rows become 0 (NaN codes must not meet a 0 weight).  E4M3
+        // requests them before q.K^T (their shared loads then overlap it),
+        // E2M1 after the softmax (measured faster each way).
+        uint32_t vw[N][4][kVWords];
+        auto load_v = [&](int n) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int t = 2 * tig + (u & 1) + (u >> 1) * 8;
+                const unsigned char* vr = vb[n] + t * kRowBytes + 4 * kVWords * gid;
+                const bool ok = (vmask[n] >> t) & 1u;
+                if constexpr (kVWords == 4) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(vr);
+                    vw[n][u][0] = ok ? x.x : 0u;
+                    vw[n][u][1] = ok ? x.y : 0u;
+                    vw[n][u][2] = ok ? x.z : 0u;
+                    vw[n][u][3] = ok ? x.w : 0u;
+                } else if constexpr (kVWords == 2) {
+                    const uint2 x = *reinterpret_cast<const uint2*>(vr);
+                    vw[n][u][0] = ok ? x.x : 0u;
+                    vw[n][u][1] = ok ? x.y : 0u;
+                } else {
+                    const uint32_t x = *reinterpret_cast<const uint32_t*>(vr);
+                    vw[n][u][0] = ok ? x : 0u;
+                }
+            }
+        };
+        if constexpr (!kFp4) {
+#pragma unroll
+            for (int n = 0; n < N; ++n) load_v(n);
+        }
+
         // ---- q.K^T: tokens gid, gid + 8 of each slab
         float s[N][4];
 #pragma unroll
@@ -588,30 +621,7 @@ struct QuantMmaConsumer {
         }
 #pragma unroll
         for (int n = 0; n < N; ++n) {
-            // V codes of tokens 2tig, 2tig+1, 2tig+8, 2tig+9: the lane's D/8
-            // dims from byte (D/8)gid (E4M3) or (D/16)gid (E2M1); codes of
-            // invalid rows become 0 (NaN codes must not meet a 0 weight)
-            uint32_t vw[4][kVWords];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int t = 2 * tig + (u & 1) + (u >> 1) * 8;
-                const unsigned char* vr = vb[n] + t * kRowBytes + 4 * kVWords * gid;
-                const bool ok = (vmask[n] >> t) & 1u;
-                if constexpr (kVWords == 4) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(vr);
-                    vw[u][0] = ok ? x.x : 0u;
-                    vw[u][1] = ok ? x.y : 0u;
-                    vw[u][2] = ok ? x.z : 0u;
-                    vw[u][3] = ok ? x.w : 0u;
-                } else if constexpr (kVWords == 2) {
-                    const uint2 x = *reinterpret_cast<const uint2*>(vr);
-                    vw[u][0] = ok ? x.x : 0u;
-                    vw[u][1] = ok ? x.y : 0u;
-                } else {
-                    const uint32_t x = *reinterpret_cast<const uint32_t*>(vr);
-                    vw[u][0] = ok ? x : 0u;
-                }
-            }
+            if constexpr (kFp4) load_v(n);
             // FP4: byte j of the lane's range holds dims 2j (low nibble) and
             // 2j + 1 (high); pair the two tokens of a fragment register
             // nibble-wise, four bytes (blocks) per word: byte j of vlo[.]
@@ -623,7 +633,7 @@ struct QuantMmaConsumer {
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
                     for (int w = 0; w < kVWords; ++w) {
-                        const uint32_t x0 = vw[2 * h][w], x1 = vw[2 * h + 1][w];
+                        const uint32_t x0 = vw[n][2 * h][w], x1 = vw[n][2 * h + 1][w];
                         vlo[h][w] = (x0 & 0x0f0f0f0fu) | ((x1 << 4) & 0xf0f0f0f0u);
                         vhi[h][w] = ((x0 >> 4) & 0x0f0f0f0fu) | (x1 & 0xf0f0f0f0u);
                     }
@@ -647,8 +657,8 @@ struct QuantMmaConsumer {
                 } else {
                     const uint32_t sel = (j & 1) ? 0x7362u : 0x5140u;  // bytes 2j%4, 2j%4+1 of two rows
                     uint32_t x[2], y[2];
-                    e4m3x4_to_f16x2x2(byte_perm(vw[0][j >> 1], vw[1][j >> 1], sel), x);
-                    e4m3x4_to_f16x2x2(byte_perm(vw[2][j >> 1], vw[3][j >> 1], sel), y);
+                    e4m3x4_to_f16x2x2(byte_perm(vw[n][0][j >> 1], vw[n][1][j >> 1], sel), x);
+                    e4m3x4_to_f16x2x2(byte_perm(vw[n][2][j >> 1], vw[n][3][j >> 1], sel), y);
                     a[0] = x[0];
                     a[1] = x[1];
                     a[2] = y[0];
