@@ -27,6 +27,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -479,8 +480,11 @@ class MaskedBench:
 
     def kernel_name(self):
         g = self.Hq // self.Hkv
-        kind = "tensor-core" if g >= 4 else "CUDA-core"
-        return attention_kernel_name(kind, self.attention_plan(), g, fused=True)
+        plan = self.attention_plan()
+        # the one-launch kernel takes the tensor-core consumers for every bf16
+        # group width, the split kernel from 4 query heads per kv head
+        kind = "tensor-core" if (g >= 4 or plan.splits == 0) else "CUDA-core"
+        return attention_kernel_name(kind, plan, g, fused=True)
 
     def aux_ops(self):
         """The step's launches other than the attention kernel, per layer:
@@ -974,11 +978,14 @@ def measure_aux(b, torch, K):
     return out
 
 
-def measure_workload(b, torch, dist, K, W, peak, clocks=None):
+def measure_workload(b, torch, dist, K, W, peak, clocks=None, min_timed_ms=None):
     """Warm-up; the timed K steps (the step captured once as a CUDA graph and
     replayed K times); CUDA events around every kernel call of K more steps
     queued behind a spinning kernel (per-launch durations); K eager steps
-    through the binding (host launch overhead included)."""
+    through the binding (host launch overhead included).  With
+    `min_timed_ms`, K grows until the timed steps span at least that long
+    (short steps: one slow step would otherwise weigh on the mean), after
+    0.2 s of untimed replays."""
     res = {}
     b.reset_cycle()
     for j in range(W):
@@ -993,12 +1000,19 @@ def measure_workload(b, torch, dist, K, W, peak, clocks=None):
     b.reset_cycle()
     if clocks is not None:
         clocks.start()
-        soak_end, j = time.time() + 0.6, 0  # a few sampling intervals before the timed steps
+    if clocks is not None or min_timed_ms:
+        # a few sampling intervals before the timed steps
+        soak_end, j = time.time() + (0.6 if clocks is not None else 0.2), 0
         while time.time() < soak_end:
             b.graph_run(j)
             j += 1
             torch.cuda.synchronize()
         b.reset_cycle()
+    if min_timed_ms:
+        est = timed(torch, None, b.graph_run, 3) / 3
+        K = max(K, int(math.ceil(min_timed_ms / max(est, 1e-3))))
+        b.reset_cycle()
+    res["steps"] = K
     ms = timed(torch, dist, b.graph_run, K)
     if clocks is not None:
         res["clocks"] = clocks.stop()
@@ -1295,7 +1309,8 @@ def main():
         """One workload's figures: the step rate, the attention kernel's
         roofline, the end-to-end rate, the oracle beside it."""
         ent = {"value": res["gbs"], "unit": "GB/s", "frac_of_hbm_peak": res["gbs"] / peak,
-               "ms_per_step": res["ms_per_step"], "decode_tokens_per_s": res["tokens_per_s"],
+               "steps": res["steps"], "ms_per_step": res["ms_per_step"],
+               "decode_tokens_per_s": res["tokens_per_s"],
                "decode_tokens_per_s_eager":
                    b.tokens_per_step() / (res["eager"]["ms_per_step"] / 1e3),
                "attend_frac": res["op_gbs_in_step"] / peak,
@@ -1337,7 +1352,8 @@ def main():
                 continue
             log(f"workload {name}")
             ob = make_bench(name, torch, kvd, dev)
-            r = measure_workload(ob, torch, dist, max(5, min(args.steps, 20)), 3, peak)
+            r = measure_workload(ob, torch, dist, max(5, min(args.steps, 20)), 3, peak,
+                                 min_timed_ms=20.0)
             oe = measure_e2e(ob, torch, dist, max(5, min(args.steps, 20)))
             oc = measure_copy(ob, torch, 5)
             if int(ob.status.item()) != 0:
