@@ -45,6 +45,17 @@ struct CombineVec<2> {
         a.y = fmaf(a.y, c, e * x.y);
     }
 };
+template <>
+struct CombineVec<4> {
+    using T = float4;
+    __device__ static float4 zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+    __device__ static void fma(float4& a, float c, float e, float4 x) {
+        a.x = fmaf(a.x, c, e * x.x);
+        a.y = fmaf(a.y, c, e * x.y);
+        a.z = fmaf(a.z, c, e * x.z);
+        a.w = fmaf(a.w, c, e * x.w);
+    }
+};
 
 template <typename Out, int VPL>
 __global__ void __launch_bounds__(kCombineWarps * 32)
@@ -150,6 +161,11 @@ cudaError_t launch_combine(const float* part_o, const float* part_lse, void* out
     // two dims per lane once one dim per lane would need more than ~1024 items
     // (8-byte loads: every row of every split must start 8-byte aligned)
     const bool even = D % 2 == 0 && st.o_split % 2 == 0;
+    // four dims per lane (16-byte loads: every row of every split 16-byte
+    // aligned) on the same condition: half the warps, twice the bytes each
+    if (D % 4 == 0 && st.o_split % 4 == 0 && st.o_row % 4 == 0 && (long long)R * ((D + 31) / 32) >= 1024)
+        return launch_combine_vpl<4>(part_o, part_lse, out, lse_out, R, S, D, out_dt, wpi, st,
+                                     stream);
     if ((long long)R * ((D + 31) / 32) >= 1024 && even)
         return launch_combine_vpl<2>(part_o, part_lse, out, lse_out, R, S, D, out_dt, wpi, st,
                                      stream);
