@@ -671,7 +671,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
         // unit's first tiles were loaded speculatively) and takes no other
         // ring's units off the lookahead count until then.
         bool gated = !(MODE == kModeMasked && sw == 0 &&
-                       (p.units < n_sched || (int)blockIdx.x * kSchedN < p.units / p.S));
+                       (p.units < n_sched || (int)blockIdx.x * kSchedN < 2 * (p.units / p.S)));
         while (true) {
             const int slot = sw * kRingSlots + pos;
             if (!warp_wait(&ctl.qempty[slot], sphase ^ 1u, ctl.abort_flag)) {
@@ -836,8 +836,9 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
         };
         // Static buffer, scheduler 0's first unit on a leading split (a
         // launch with fewer units than scheduler warps, bounded by latency,
-        // or a split-0 unit of a larger one, which holds valid tokens unless
-        // its row is empty): its first tiles are loaded before its mask is
+        // or a split-0 or split-1 unit of a larger one, which holds valid
+        // tokens unless its row is empty or shorter than one split): its
+        // first tiles are loaded before its mask is
         // read (their addresses need no metadata) and delivered when that
         // unit's slot arrives -- as its tiles if the slot holds that unit,
         // else (the unit was empty) as empty tiles the consumers only
@@ -847,7 +848,7 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
         if constexpr (MODE == kModeMasked) {
             const int n_sched = kSchedN * (int)gridDim.x;
             const int u0 = p.units >= n_sched ? (int)blockIdx.x * kSchedN : (int)blockIdx.x;
-            if (u0 < p.units && (p.units < n_sched || u0 < p.units / p.S)) {
+            if (u0 < p.units && (p.units < n_sched || u0 < 2 * (p.units / p.S))) {
                 const Unit un0 = decode_unit(p, G, u0);
                 const SplitRange r = split_range<MODE>(p, un0.bz, un0.split, false);
                 spec_unit = u0;
