@@ -263,6 +263,56 @@ def test_leading_tiles_empty_or_valid(kvd, Hq, Hkv, start):
     assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
 
 
+@pytest.mark.parametrize("Hq,Hkv,fused", [(32, 8, False), (32, 8, True), (32, 32, True)])
+def test_large_launch_speculated_first_units(kvd, Hq, Hkv, fused):
+    """Large launches load the first tiles of a CTA's first unit before its
+    mask is read when that unit is a split-0 or split-1 unit.  Rows that are
+    empty, hold one slot, or end inside split 0 leave those speculated units
+    empty (delivered as empty tiles): every row still equals the oracle, in
+    the two-call and the fused append form."""
+    B, C, D = 16, 8192, 128
+    g = W.generator(1960 + Hq + int(fused))
+    q = W.randn(g, (B, Hq, D))
+    k = W.randn(g, (B, Hkv, C, D))
+    v = W.randn(g, (B, Hkv, C, D))
+    # lengths cycle through empty, 1, inside split 0, inside split 1, long
+    pattern = [0, 1, 100, 700, 5000, 8192, 37, 300]
+    lengths = [pattern[b % len(pattern)] for b in range(B)]
+    dev = "cuda"
+    plan = kvd.attend_masked_plan(B, Hq, Hkv, C, D)
+    assert plan.splits > 2 and plan.launches == 2  # the split kernel, many units
+    status = kvd.status_tensor(dev)
+    lse = torch.empty(B, Hq, device=dev)
+    if fused:
+        # the step appends at pos = length (the new slot), rows of length 0
+        # get their first slot
+        pos = torch.tensor([min(L, C - 1) for L in lengths], dtype=torch.int32)
+        mask = W.prefix_mask(lengths, C)
+        k_new = W.randn(g, (B, Hkv, D))
+        v_new = W.randn(g, (B, Hkv, D))
+        kh, vh, mh = k.view(torch.int16).numpy().copy(), v.view(torch.int16).numpy().copy(), \
+            mask.numpy().copy()
+        assert oracle.append(kh, vh, k_new, v_new, pos, mh) == 0
+        kd, vd, md = k.to(dev), v.to(dev), mask.to(dev)
+        out = kvd.append_attend_masked(q.to(dev), kd, vd, md, k_new.to(dev), v_new.to(dev),
+                                       pos.to(dev), 0.09, lse=lse, dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert np.array_equal(host(md).numpy(), mh)
+        ref, ref_lse = oracle.attend_masked(q, torch.from_numpy(kh).view(torch.bfloat16),
+                                            torch.from_numpy(vh).view(torch.bfloat16),
+                                            torch.from_numpy(mh), 0.09)
+    else:
+        mask = W.prefix_mask(lengths, C)
+        out = kvd.attend_masked(q.to(dev), k.to(dev), v.to(dev), mask.to(dev), 0.09, lse=lse,
+                                dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        ref, ref_lse = oracle.attend_masked(q, k, v, mask, 0.09)
+    assert_attention_close(out, ref, torch.bfloat16, "speculated first units")
+    assert_lse_close(lse, ref_lse, "speculated first units")
+
+
 @pytest.mark.parametrize("dtype,Hq,Hkv,D", [
     (torch.float32, 16, 4, 128), (torch.float32, 16, 2, 64), (torch.bfloat16, 8, 4, 64),
     (torch.bfloat16, 4, 4, 64), (torch.bfloat16, 32, 4, 64), (torch.bfloat16, 24, 1, 128)])
