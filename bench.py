@@ -48,14 +48,14 @@ L2_BYTES = 129 * 1024 * 1024
 # kernel sources it was taken on: reported only while the sources still hash
 # to that revision, else null.
 NCU_TRAFFIC = {
-    ("npuw", "cfb926f957cc9787"): 17890560,  # attend_small_kernel, tensor-core consumers, 1152-slot buffer
-    ("gqa", "cfb926f957cc9787"): 212896768,  # attend_kernel, tensor-core consumers, batched GQA
-    ("long", "cfb926f957cc9787"): 540574208,  # attend_kernel, CUDA-core consumers, 32768 slots
-    ("paged", "cfb926f957cc9787"): 521914368,  # attend_kernel, paged mode
-    ("indexed", "cfb926f957cc9787"): 122640640,  # attend_kernel, index-list mode, gather warp
-    ("window", "cfb926f957cc9787"): 68776704,  # attend_kernel, 4096-slot window
-    ("gqa_fp8", "cfb926f957cc9787"): 120613888,  # attend_kernel, E4M3 consumers
-    ("gqa_fp4", "cfb926f957cc9787"): 66410752,  # attend_kernel, E2M1 consumers
+    ("npuw", "791630c5b6deb48c"): 17890560,  # attend_small_kernel, tensor-core consumers, 1152-slot buffer
+    ("gqa", "791630c5b6deb48c"): 212764416,  # attend_kernel, tensor-core consumers, batched GQA
+    ("long", "791630c5b6deb48c"): 540828928,  # attend_kernel, CUDA-core consumers, 32768 slots
+    ("paged", "791630c5b6deb48c"): 522298368,  # attend_kernel, paged mode
+    ("indexed", "791630c5b6deb48c"): 122888960,  # attend_kernel, index-list mode, gather warp
+    ("window", "791630c5b6deb48c"): 69667840,  # attend_kernel, 4096-slot window
+    ("gqa_fp8", "791630c5b6deb48c"): 120518144,  # attend_kernel, E4M3 consumers
+    ("gqa_fp4", "791630c5b6deb48c"): 66514944,  # attend_kernel, E2M1 consumers
 }
 
 # ------------------------------------------------------------ byte accounting
