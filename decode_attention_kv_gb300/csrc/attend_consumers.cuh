@@ -29,14 +29,14 @@
 // inside fp32, and the result is the same up to rounding.  A warp rescales
 // only when one of its lanes needs it.
 //
-//  Fp8MmaConsumer: tensor cores over quantised K/V rows (E4M3 codes, the
-//    row's fp32 scale beside them; "FlashMLA на Huawei Ascend", "Ограничение
-//    по деквантованию" and "Оптимизация раскладки KV-кэша при decoding").
-//    The codes become f16 in registers (exactly), read with plain 16-byte
-//    shared loads in a dims-to-lanes order that both mma operands share;
-//    each row's scale multiplies its score (K) or its weight p (V), so no
-//    element is ever multiplied by its scale.  Any query head count up to 8
-//    per kv head.
+//  QuantMmaConsumer (Fp8MmaConsumer / Fp4MmaConsumer): tensor cores over
+//    quantised K/V rows (E4M3 codes, or E2M1 codes two per byte, the row's
+//    fp32 scale beside them; "FlashMLA на Huawei Ascend", "Ограничение по
+//    деквантованию" and "Оптимизация раскладки KV-кэша при decoding").  The
+//    codes become f16 in registers (exactly), read with plain shared loads
+//    in a dims-to-lanes order that both mma operands share; each row's scale
+//    multiplies its score (K) or its weight p (V), so no element is ever
+//    multiplied by its scale.  Any query head count up to 8 per kv head.
 //
 // finish() leaves each warp's state in shared memory as mo[w][h][d]
 // (unnormalised output) and ml[w][h] = (m, l) for the CTA-wide merge.

@@ -43,6 +43,8 @@
 //  * epilogue (warp NCW+5): merges the consumer warps' states of a unit and
 //    writes either the final rows (single split) or a normalised partial row
 //    and its log-sum-exp.
+//  * index-list mode only: the last scheduler warp gathers half of each
+//    tile's listed rows beside the loader (three warps schedule).
 // With more than one split the host launches the log-sum-exp combine kernel
 // right behind this one (programmatic dependent launch): it runs once the
 // partial rows are complete, without atomics or fences here.
@@ -50,9 +52,10 @@
 // Counters (unit counter, schedulers-done counter) live in the caller's
 // workspace: zero before the first call; the last scheduler warp to finish
 // taking units resets them.  The first unit of scheduler warp s (no atomic)
-// is blockIdx.x * 4 + s -- four consecutive rows of one split, which share a
-// mask row or a sequence -- or, with fewer units than scheduler warps,
-// s * gridDim.x + blockIdx.x; the counter hands out the rest.
+// is blockIdx.x * n + s (n scheduler warps) -- consecutive rows of one split,
+// which share a mask row or a sequence -- or, with fewer units than
+// scheduler warps, s * gridDim.x + blockIdx.x; the counter hands out the
+// rest.
 // All waits are bounded; a wait that runs out sets KVD_DEV_TIMEOUT, after
 // which the counters must be zeroed again.
 #pragma once
