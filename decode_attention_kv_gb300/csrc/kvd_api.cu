@@ -80,6 +80,7 @@ constexpr int kSmallSplits = 8;            // splits per row: the portable clust
 constexpr int kSmallTokens = 384;          // tokens per split, all resident
 constexpr int kSmallShared = 113 * 1024;   // shared memory per CTA: two CTAs per SM
 constexpr int kMinChunk = 128;
+constexpr long long kWideRows = 128;  // row units from which the tail splits are half a chunk
 
 struct Plan {
     int G, HG;      // compile-time group width, head groups per kv head
@@ -157,7 +158,13 @@ Plan plan_attention(int rows, int Hq, int Hkv, int cap, int D, kvd_dtype dt, int
     pl.chunk = pl.chunk2 = (int)chunk;
     pl.S = pl.Sb = (int)(((long long)cap + chunk - 1) / chunk);
     if (pl.S < 1) pl.S = pl.Sb = 1;
-    const long long small = ((chunk / 4) + unit - 1) / unit * unit;
+    // Tail splits: a quarter chunk, or half a chunk when there are enough
+    // rows (128 row units) to spread the late units over the grid by
+    // themselves (fewer partial rows to combine); a few long rows -- one
+    // sequence's heads -- keep the finer tail, where their valid slots may
+    // all sit (a window at the end of the buffer).
+    const long long small =
+        ((chunk / (row_units >= kWideRows ? 2 : 4)) + unit - 1) / unit * unit;
     // A launch whose units all fit the persistent grid at once (one unit per
     // CTA) keeps equal splits: small tail splits would only give some CTAs a
     // second unit.
