@@ -48,14 +48,14 @@ L2_BYTES = 129 * 1024 * 1024
 # kernel sources it was taken on: reported only while the sources still hash
 # to that revision, else null.
 NCU_TRAFFIC = {
-    ("npuw", "791630c5b6deb48c"): 17890560,  # attend_small_kernel, tensor-core consumers, 1152-slot buffer
-    ("gqa", "791630c5b6deb48c"): 212764416,  # attend_kernel, tensor-core consumers, batched GQA
-    ("long", "791630c5b6deb48c"): 540828928,  # attend_kernel, CUDA-core consumers, 32768 slots
-    ("paged", "791630c5b6deb48c"): 522298368,  # attend_kernel, paged mode
-    ("indexed", "791630c5b6deb48c"): 122888960,  # attend_kernel, index-list mode, gather warp
-    ("window", "791630c5b6deb48c"): 69667840,  # attend_kernel, 4096-slot window
-    ("gqa_fp8", "791630c5b6deb48c"): 120518144,  # attend_kernel, E4M3 consumers
-    ("gqa_fp4", "791630c5b6deb48c"): 66514944,  # attend_kernel, E2M1 consumers
+    ("npuw", "e75f907995f9d2d9"): 17890560,  # attend_small_kernel, tensor-core consumers, 1152-slot buffer
+    ("gqa", "e75f907995f9d2d9"): 212619264,  # attend_kernel, tensor-core consumers, batched GQA
+    ("long", "e75f907995f9d2d9"): 540581632,  # attend_kernel, CUDA-core consumers, 32768 slots
+    ("paged", "e75f907995f9d2d9"): 521597696,  # attend_kernel, paged mode
+    ("indexed", "e75f907995f9d2d9"): 122518016,  # attend_kernel, index-list mode, gather warp
+    ("window", "e75f907995f9d2d9"): 69692416,  # attend_kernel, 4096-slot window
+    ("gqa_fp8", "e75f907995f9d2d9"): 120531456,  # attend_kernel, E4M3 consumers
+    ("gqa_fp4", "e75f907995f9d2d9"): 66396672,  # attend_kernel, E2M1 consumers
 }
 
 # ------------------------------------------------------------ byte accounting
