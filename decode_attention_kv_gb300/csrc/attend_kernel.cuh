@@ -136,7 +136,7 @@ struct StageMeta {
     int unit;
     int tile;
     uint32_t flags;
-    uint32_t pad;
+    uint32_t pad;             // index-list mode: the unit's scheduler slot (for the gather warp)
     unsigned long long bits;  // validity of the tile's tokens
 };
 
