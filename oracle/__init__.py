@@ -11,6 +11,9 @@ Every function states what it computes and the page section it follows:
 * ``attend_masked`` -- "Intel NPU running LLMs" (OpenVINO community article
   882), Part 1 "解决方案：预分配 + Attention Mask" and Part 3 "Attention 在 NPU
   上的完整实现"; "FlashMLA на Huawei Ascend", "Математическая постановка".
+* ``attend_window`` -- ``attend_masked`` with every mask slot outside the
+  sliding window [last - W + 1, last] taken as 0 (Part 3's sliding-window
+  tile variant, expressed on Part 1's mask).
 * ``append`` -- same article, Part 2 "NPUW 的核心设计" (update_kvcache_for).
 * ``gather_paged`` -- "PyPTO 实现 AscendC GatherPaKvCache（Norm/ND 分支）",
   sections 3.1-3.3 and 7.
@@ -218,6 +221,29 @@ def attend_masked(q, k, v, mask, scale: float, nthreads: int = 0):
     if rc != 0:
         raise RuntimeError(f"oracle attend_masked failed ({rc})")
     return out, lse
+
+
+def attend_window(q, k, v, mask, last, W: int, scale: float, nthreads: int = 0):
+    """Sliding-window decode attention, fp64: row b attends to the slots j
+    with mask[b, j] != 0 and last[b] - W + 1 <= j <= last[b]; a row whose
+    last[b] is outside [0, C) attends to nothing.
+    Returns (out [B, Hq, D] float64, lse [B, Hq] float64, error bits: 1 when
+    some last[b] is outside [0, C))."""
+    ka, _ = _storage(k)
+    B, C = ka.shape[0], ka.shape[2]
+    m = _u8(mask).reshape(B, C).copy()
+    lst = _i32(last).reshape(B)
+    bad = 0
+    j = np.arange(C)
+    for b in range(B):
+        t = int(lst[b])
+        if t < 0 or t >= C:
+            bad = 1
+            m[b, :] = 0
+        else:
+            m[b, (j < t - int(W) + 1) | (j > t)] = 0
+    out, lse = attend_masked(q, k, v, m, scale, nthreads)
+    return out, lse, bad
 
 
 def attend_indexed(q, k, v, indices, scale: float, nthreads: int = 0):

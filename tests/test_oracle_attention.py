@@ -290,3 +290,39 @@ def test_sliding_window_is_attention_over_the_last_rows(oracle, L, Wn):
     assert np.array_equal(out, o2) and np.array_equal(lse, l2)
     if Wn >= L:
         assert np.array_equal(mask, W.prefix_mask([L], C))
+
+
+@pytest.mark.parametrize("Wn", [1, 5, 16, 33, 64, 200])
+def test_window_entry_is_attention_over_the_masked_window(oracle, Wn):
+    """The window entry's definition (cuTile on NPU, Part 1's sliding-window
+    variant over the mask contract): row b attends to the masked slots of
+    [last - Wn + 1, last].  Checked against float64 softmax written out over
+    the index set each row selects (a mask with holes, windows clipped at
+    slot 0, the newest slot at the buffer's end); W = 1 is the newest row's
+    value itself; a newest slot outside the buffer empties the row."""
+    g = W.generator(90 + Wn)
+    B, Hq, Hkv, C, D = 5, 4, 2, 96, 16
+    q = W.randn(g, (B, Hq, D), torch.bfloat16)
+    k = W.randn(g, (B, Hkv, C, D), torch.bfloat16)
+    v = W.randn(g, (B, Hkv, C, D), torch.bfloat16)
+    mask = (torch.rand(B, C, generator=g) < 0.7).to(torch.uint8)
+    last = torch.tensor([C - 1, 10, 0, 50, C], dtype=torch.int32)  # the last is outside
+    mask[torch.arange(4), last[:4].long()] = 1
+    out, lse, err = oracle.attend_window(q, k, v, mask, last, Wn, 0.3)
+    assert err == 1
+    for b in range(B):
+        t = int(last[b])
+        if not 0 <= t < C:
+            assert np.all(out[b] == 0) and np.all(np.isneginf(lse[b]))
+            continue
+        sel = [j for j in range(max(0, t - Wn + 1), t + 1) if mask[b, j]]
+        for h in range(Hq):
+            ks = k[b, h // (Hq // Hkv), sel].double()
+            vs = v[b, h // (Hq // Hkv), sel].double()
+            s = ks @ q[b, h].double() * 0.3
+            ref = torch.softmax(s, 0) @ vs
+            np.testing.assert_allclose(out[b, h], ref.numpy(), rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(lse[b, h], float(torch.logsumexp(s, 0)), rtol=1e-12)
+            if Wn == 1:
+                assert sel == [t]
+                np.testing.assert_allclose(out[b, h], vs[0].numpy(), rtol=0, atol=1e-15)
