@@ -225,6 +225,7 @@ def masked_config(name, w, layers, lengths0):
     if w.window:
         rows = layers * 2 * w.Hkv * sum(min(x, w.window) for x in L) * w.D * elem
         c.update({"window": w.window,
+                  "attention": "kvd_append_attend_window (splits over each row's window)",
                   "l2": f"inputs larger than L2: the windows' K/V rows of the {layers} layers "
                         f"read per step are {rows / 2**20:.0f} MiB vs {L2_BYTES // 2**20} MiB L2"})
     if name == "indexed":
@@ -324,7 +325,14 @@ class MaskedBench:
         # append slot of step j: base + (j mod cycle)
         self.pos_table = torch.stack([(base + i).to(torch.int32) for i in range(self.cycle)]).to(dev)
         self.gpos = self.pos_table[0].clone()
-        need = kvd.attend_masked_workspace_bytes(self.B, self.Hq, self.Hkv, self.C, self.D)
+        # the sliding window runs through the window entries (splits over each
+        # row's window only)
+        self.win = w.window
+        if self.win:
+            need = kvd.attend_window_workspace_bytes(self.B, self.Hq, self.Hkv, self.C, self.D,
+                                                     self.win)
+        else:
+            need = kvd.attend_masked_workspace_bytes(self.B, self.Hq, self.Hkv, self.C, self.D)
         self.ws = kvd.workspace(need, dev)
         self.out = [torch.empty_like(l.q) for l in w.layers]
         self.status = kvd.status_tensor(dev)
@@ -344,6 +352,11 @@ class MaskedBench:
     def _layer(self, li, lay, pos):
         """The layer's decode step: append + attention in one call (one
         launch and the combine)."""
+        if self.win:
+            self.kvd.append_attend_window(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.k_new,
+                                          lay.v_new, pos, self.win, lay.scale, out=self.out[li],
+                                          workspace=self.ws, dev_status=self.status)
+            return
         self.kvd.append_attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.k_new,
                                       lay.v_new, pos, lay.scale, out=self.out[li],
                                       workspace=self.ws, dev_status=self.status)
@@ -410,6 +423,8 @@ class MaskedBench:
     def launches_per_step(self):
         """One fused append + attention call per layer: one launch (the
         small-launch kernel) or two (the split kernel and the combine)."""
+        if self.win:
+            return self.layers * self.attention_plan().launches
         return self.layers * self.kvd.attend_masked_launches(self.B, self.Hq, self.Hkv, self.C,
                                                              self.D)
 
@@ -477,6 +492,8 @@ class MaskedBench:
         self.h_out.copy_(self.d_out, non_blocking=True)
 
     def attention_plan(self):
+        if self.win:
+            return self.kvd.attend_window_plan(self.B, self.Hq, self.Hkv, self.C, self.D, self.win)
         return self.kvd.attend_masked_plan(self.B, self.Hq, self.Hkv, self.C, self.D)
 
     def kernel_name(self):
@@ -485,7 +502,8 @@ class MaskedBench:
         # the one-launch kernel takes the tensor-core consumers for every bf16
         # group width, the split kernel from 4 query heads per kv head
         kind = "tensor-core" if (g >= 4 or plan.splits == 0) else "CUDA-core"
-        return attention_kernel_name(kind, plan, g, fused=True)
+        return attention_kernel_name(kind, plan, g, mode="window" if self.win else "masked",
+                                     fused=True)
 
     def aux_ops(self):
         """The step's launches other than the attention kernel, per layer:
@@ -1200,9 +1218,12 @@ def oracle_rate(name, seconds):
         lay = w.layers[li]
         kh, vh, mh = caches[li]
         oracle.append(kh, vh, lay.k_new, lay.v_new, lay.pos, mh)
-        oracle.attend_masked(lay.q, torch.from_numpy(kh).view(torch.bfloat16),
-                             torch.from_numpy(vh).view(torch.bfloat16), torch.from_numpy(mh),
-                             lay.scale)
+        kr = torch.from_numpy(kh).view(torch.bfloat16)
+        vr = torch.from_numpy(vh).view(torch.bfloat16)
+        if w.window:
+            oracle.attend_window(lay.q, kr, vr, torch.from_numpy(mh), lay.pos, w.window, lay.scale)
+        else:
+            oracle.attend_masked(lay.q, kr, vr, torch.from_numpy(mh), lay.scale)
     return run(step, per, "append + attention")
 
 

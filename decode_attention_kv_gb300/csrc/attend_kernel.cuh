@@ -18,7 +18,10 @@
 // group of <= G query heads sharing it), split = a chunk of `chunk` token
 // slots of that row.  Units are numbered split-major and handed out by a
 // global counter, so the grid is persistent (about one or two CTAs per SM)
-// and load-balances rows of any length.
+// and load-balances rows of any length.  With a sliding window (static
+// buffer) a row's splits count from the 64-slot boundary at or below its
+// window's first slot, so that they cover the window and nothing before it
+// ("Intel NPU running LLMs", Part 3, the sliding-window tile variant).
 //
 // CTA.  Four roles in warps:
 //  * schedulers (warps NCW+1 .. NCW+4): each takes units from the work counter,
@@ -110,6 +113,11 @@ struct AttendParams {
     int out_f32;                 // out is fp32 whatever the element type (a range's partial)
     int small_push;              // one-launch kernel: the splits push partials into split 0
     int small_nwg;               // one-launch kernel: consumer warp groups per CTA (1 or 2)
+    // sliding window (static buffer): row b attends to the masked slots of
+    // [win_last[b] - win + 1, win_last[b]] only; splits count their tokens
+    // from the 64-slot boundary at or below the window's first slot
+    int win;                     // window slots; 0: no window
+    const int32_t* win_last;     // [rows]: the window's newest slot (the step's pos when appending)
 };
 
 // Output rows: the element type of q, or fp32 for a token range's partial
@@ -249,6 +257,7 @@ struct KernelShape {
 // a constraint of the gather page become empty; `reporter` reports it.
 struct SplitRange {
     int t_begin, t_end, ntok, ntiles, first_col;
+    int t_lo;  // first slot that may count (> t_begin only where a window starts inside the split)
 };
 
 template <int MODE>
@@ -259,6 +268,7 @@ __device__ __forceinline__ SplitRange split_range(const AttendParams& p, int bz,
     r.t_begin = big ? split * p.chunk : p.Sb * p.chunk + (split - p.Sb) * p.chunk2;
     const int span = big ? p.chunk : p.chunk2;
     r.first_col = 0;
+    r.t_lo = r.t_begin;
     if constexpr (MODE == kModePaged) {
         const int s0 = p.seq_lens[bz], s1 = p.seq_lens[bz + 1];
         const int off = p.seq_offset ? p.seq_offset[bz] : 0;
@@ -285,6 +295,19 @@ __device__ __forceinline__ SplitRange split_range(const AttendParams& p, int bz,
         r.t_end = min(p.topk, r.t_begin + span);  // positions in the index list
     } else {
         r.t_end = min(p.C, r.t_begin + span);
+        if (p.win > 0) {
+            const int last = __ldg(p.win_last + bz);
+            if (last < 0 || last >= p.C) {  // no window: an empty row
+                if (reporter) report(p.dev_status, KVD_DEV_POS_RANGE);
+                r.t_end = r.t_begin;
+            } else {
+                const int lo = max(0, last - p.win + 1);
+                r.t_begin += lo & ~63;
+                r.t_lo = max(lo, r.t_begin);
+                r.t_end = min(last + 1, r.t_begin + span);
+                if (r.t_end <= r.t_lo) r.t_end = r.t_lo = r.t_begin;  // ends below the window
+            }
+        }
     }
     r.ntok = max(0, r.t_end - r.t_begin);
     r.ntiles = (r.ntok + p.tile - 1) / p.tile;
@@ -470,6 +493,13 @@ __device__ __forceinline__ int producer_scan(const AttendParams& p, const SplitR
                     if (lane == 0 && j0 + u < nwords) words[j0 + u] = w;
                 }
             }
+        }
+        if (r.t_lo > r.t_begin) {
+            // a window starting inside the split: its slots below the window
+            // do not count (fewer than 64, so words 0 and 1 at most)
+            __syncwarp();
+            const int skip = r.t_lo - r.t_begin - 32 * lane;
+            if (skip > 0) words[lane] &= skip >= 32 ? 0u : ~((1u << skip) - 1u);
         }
     }
     __syncwarp();

@@ -188,6 +188,29 @@ Plan plan_attention(int rows, int Hq, int Hkv, int cap, int D, kvd_dtype dt, int
     return pl;
 }
 
+// Slots a sliding window's splits span: from the 64-slot boundary at or below
+// the window's first slot to its last, at most W + 63 (and never beyond the
+// buffer); the whole buffer without a window.
+int window_span(int C, int W) {
+    if (W <= 0) return C;
+    const long long span = (long long)W + 63;
+    return span < C ? (int)span : C;
+}
+
+// Plan of a sliding-window call.  Every row of a window holds about W slots
+// (unlike the ragged lengths the general plan balances), so the default is
+// equal splits, as many as give each persistent CTA one unit (one split per
+// row from kGridUnitsHint rows on: no combine).
+Plan plan_window(int B, int Hq, int Hkv, int C, int W, int D, kvd_dtype dt, int num_splits) {
+    if (num_splits <= 0) {
+        const int g = Hq / Hkv, G = group_width(g);
+        const long long rows = (long long)B * Hkv * ((g + G - 1) / G);
+        const long long s = kGridUnitsHint / rows;
+        num_splits = s > 1 ? (int)s : 1;
+    }
+    return plan_attention(B, Hq, Hkv, window_span(C, W), D, dt, 0, num_splits);
+}
+
 // Small static-buffer launch (no caller split count; every split of every row
 // resident at once, a cluster of at most 8 CTAs per row that merges the row
 // itself).  Splits as equal as the copies allow: whole 64-row boxes for the
@@ -484,18 +507,21 @@ kvd_status attend_masked_impl(const char* fn, const void* q, const void* k_cache
                               kvd_dtype dtype, int num_splits, void* workspace,
                               size_t workspace_bytes, int32_t* dev_status, kvd_stream_t stream,
                               const void* k_new, const void* v_new, const int32_t* pos,
-                              bool out_f32 = false) {
+                              bool out_f32 = false, int win = 0,
+                              const int32_t* win_last = nullptr) {
     kvd_status st = check_attention_shape(Hq, Hkv, D, dtype);
     if (st != KVD_OK) return st;
     if (B < 0 || C < 1) return fail(KVD_ERR_INVALID_ARG, "%s: B >= 0 and C >= 1 required", fn);
+    if (win < 0) return fail(KVD_ERR_INVALID_ARG, "%s: W >= 1 required", fn);
     if (B == 0) return ok();
-    if (!q || !k_cache || !v_cache || !mask || !out)
+    if (!q || !k_cache || !v_cache || !mask || !out || (win > 0 && !win_last))
         return fail(KVD_ERR_INVALID_ARG, "%s: null pointer", fn);
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-        !aligned(lse_out, 4) || !aligned(dev_status, 4))
+        !aligned(lse_out, 4) || !aligned(dev_status, 4) || !aligned(win_last, 4))
         return fail(KVD_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
     if (num_splits < 0) return fail(KVD_ERR_INVALID_ARG, "%s: num_splits < 0", fn);
-    const Plan pl = plan_attention(B, Hq, Hkv, C, D, dtype, 0, num_splits);
+    const Plan pl = win > 0 ? plan_window(B, Hq, Hkv, C, win, D, dtype, num_splits)
+                            : plan_attention(B, Hq, Hkv, C, D, dtype, 0, num_splits);
     st = check_workspace(fn, pl, workspace, workspace_bytes);
     if (st != KVD_OK) return st;
     AttendParams p{};
@@ -517,11 +543,14 @@ kvd_status attend_masked_impl(const char* fn, const void* q, const void* k_cache
     p.pos = k_new ? pos : nullptr;
     p.mask_w = const_cast<uint8_t*>(mask);
     p.out_f32 = out_f32 ? 1 : 0;
+    p.win = win;
+    p.win_last = win > 0 ? win_last : nullptr;
     attach_workspace(p, pl, workspace);
     CUtensorMap kmap, vmap;
     std::memset(&kmap, 0, sizeof kmap);
     std::memset(&vmap, 0, sizeof vmap);
-    const SmallPlan sp = plan_small(B, Hkv, C, D, dtype, pl, num_splits);
+    // the one-launch kernel holds whole splits from slot 0: not for windows
+    const SmallPlan sp = win > 0 ? SmallPlan{} : plan_small(B, Hkv, C, D, dtype, pl, num_splits);
     if (sp.use ? small_uses_mma(dtype, pl.G) : attend_uses_mma(dtype, pl.G)) {
         // 128-byte-swizzled boxes of 64 dims x (tile rows) for the tensor-core consumers
         const long long rows = (long long)B * Hkv * C;
@@ -606,6 +635,63 @@ kvd_status kvd_append_attend_masked(const void* q, void* k_cache, void* v_cache,
     return attend_masked_impl(fn, q, k_cache, v_cache, mask, out, lse_out, B, Hq, Hkv, C, D, scale,
                               dtype, num_splits, workspace, workspace_bytes, dev_status, stream,
                               k_new, v_new, pos);
+}
+
+size_t kvd_attend_window_workspace_bytes(int B, int Hq, int Hkv, int C, int D, int W,
+                                         kvd_dtype dtype, int num_splits) {
+    if (B < 1 || C < 1 || W < 1 || check_attention_shape(Hq, Hkv, D, dtype) != KVD_OK) return 0;
+    return plan_window(B, Hq, Hkv, C, W, D, dtype, num_splits).ws;
+}
+
+kvd_status kvd_attend_window_plan(int B, int Hq, int Hkv, int C, int D, int W, kvd_dtype dtype,
+                                  int num_splits, kvd_plan* plan) {
+    if (!plan) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_window_plan: null pointer");
+    if (B < 1 || C < 1 || W < 1 || num_splits < 0)
+        return fail(KVD_ERR_INVALID_ARG,
+                    "kvd_attend_window_plan: B, C, W >= 1 and num_splits >= 0 required");
+    const kvd_status st = check_attention_shape(Hq, Hkv, D, dtype);
+    if (st != KVD_OK) return st;
+    put_plan(plan_window(B, Hq, Hkv, C, W, D, dtype, num_splits), false, plan);
+    return ok();
+}
+
+kvd_status kvd_attend_window(const void* q, const void* k_cache, const void* v_cache,
+                             const uint8_t* mask, const int32_t* last, void* out, float* lse_out,
+                             int B, int Hq, int Hkv, int C, int D, int W, float scale,
+                             kvd_dtype dtype, int num_splits, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_status, kvd_stream_t stream) {
+    if (W < 1) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_window: W >= 1 required");
+    return attend_masked_impl("kvd_attend_window", q, k_cache, v_cache, mask, out, lse_out, B, Hq,
+                              Hkv, C, D, scale, dtype, num_splits, workspace, workspace_bytes,
+                              dev_status, stream, nullptr, nullptr, nullptr, false, W, last);
+}
+
+kvd_status kvd_append_attend_window(const void* q, void* k_cache, void* v_cache, uint8_t* mask,
+                                    const void* k_new, const void* v_new, const int32_t* pos,
+                                    void* out, float* lse_out, int B, int Hq, int Hkv, int C,
+                                    int D, int W, float scale, kvd_dtype dtype, int num_splits,
+                                    void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                    kvd_stream_t stream) {
+    const char* fn = "kvd_append_attend_window";
+    if (W < 1) return fail(KVD_ERR_INVALID_ARG, "%s: W >= 1 required", fn);
+    if (B == 0) return ok();
+    if (!k_new || !v_new || !pos) return fail(KVD_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(pos, 4))
+        return fail(KVD_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+    const kvd_status st = check_attention_shape(Hq, Hkv, D, dtype);
+    if (st != KVD_OK) return st;
+    if (group_width(Hq / Hkv) < Hq / Hkv) {
+        // several head groups per kv head: the append first, then the attention
+        const kvd_status sa = kvd_append(k_cache, v_cache, k_new, v_new, pos, mask, B, Hkv, C, D,
+                                         dtype, dev_status, stream);
+        if (sa != KVD_OK) return sa;
+        return attend_masked_impl(fn, q, k_cache, v_cache, mask, out, lse_out, B, Hq, Hkv, C, D,
+                                  scale, dtype, num_splits, workspace, workspace_bytes, dev_status,
+                                  stream, nullptr, nullptr, nullptr, false, W, pos);
+    }
+    return attend_masked_impl(fn, q, k_cache, v_cache, mask, out, lse_out, B, Hq, Hkv, C, D, scale,
+                              dtype, num_splits, workspace, workspace_bytes, dev_status, stream,
+                              k_new, v_new, pos, false, W, pos);
 }
 
 }  // extern "C"

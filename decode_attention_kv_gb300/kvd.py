@@ -47,6 +47,10 @@ SIGNATURES = {
                                    _vp, _vp], _i),
     "kvd_append_attend_masked": ([_vp] * 7 + [_vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz,
                                   _vp, _vp], _i),
+    "kvd_attend_window_workspace_bytes": ([_i] * 8, _sz),
+    "kvd_attend_window_plan": ([_i] * 8 + [_vp], _i),
+    "kvd_attend_window": ([_vp] * 7 + [_i] * 6 + [_f, _i, _i, _vp, _sz, _vp, _vp], _i),
+    "kvd_append_attend_window": ([_vp] * 9 + [_i] * 6 + [_f, _i, _i, _vp, _sz, _vp, _vp], _i),
     "kvd_append_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp], _i),
     "kvd_attend_masked_fp8_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
     "kvd_attend_masked_fp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz,
@@ -523,6 +527,84 @@ def append_attend_masked(q, k_cache, v_cache, mask, k_new, v_new, pos, scale=Non
                                     D, float(scale), dt, num_splits, _ptr(ws), wsb,
                                     _ptr(dev_status), _stream(q.device))
     _check("kvd_append_attend_masked", st)
+    return out
+
+
+def attend_window_workspace_bytes(B, Hq, Hkv, C, D, W, dtype=torch.bfloat16, num_splits=0):
+    return load().kvd_attend_window_workspace_bytes(B, Hq, Hkv, C, D, W,
+                                                    BF16 if dtype == torch.bfloat16 else F32,
+                                                    num_splits)
+
+
+def attend_window_plan(B, Hq, Hkv, C, D, W, dtype=torch.bfloat16, num_splits=0):
+    return _plan("kvd_attend_window_plan", B, Hq, Hkv, C, D, W,
+                 BF16 if dtype == torch.bfloat16 else F32, num_splits)
+
+
+def _window_args(fn, q, k_cache, v_cache, mask, W, rows, extra):
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("mask", mask)) + extra:
+        _cuda_contig(n, t)
+    B, Hq, D = q.shape
+    Bk, Hkv, C, Dk = k_cache.shape
+    if Bk != B or Dk != D or v_cache.shape != k_cache.shape or mask.shape != (B, C):
+        raise ValueError(f"{fn}: shape mismatch")
+    if mask.dtype != torch.uint8 or rows.dtype != torch.int32 or rows.numel() != B:
+        raise ValueError(f"{fn}: mask uint8 [B, C], positions int32 [B]")
+    if int(W) < 1:
+        raise ValueError(f"{fn}: W >= 1 required")
+    return B, Hq, Hkv, C, D
+
+
+def attend_window(q, k_cache, v_cache, mask, last, W, scale=None, out=None, lse=None,
+                  num_splits=0, workspace=None, dev_status=None):
+    """kvd_attend_window: row b attends to the masked slots of
+    [last[b] - W + 1, last[b]].  Returns out [B, Hq, D]."""
+    B, Hq, Hkv, C, D = _window_args("attend_window", q, k_cache, v_cache, mask, W, last,
+                                    (("last", last),))
+    if not (q.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("attend_window: q and caches must share a dtype")
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is not None:
+        _cuda_contig("lse", lse)
+    L = load()
+    need = L.kvd_attend_window_workspace_bytes(B, Hq, Hkv, C, D, int(W), dt, num_splits)
+    ws, wsb = _workspace(need, q.device, workspace)
+    st = L.kvd_attend_window(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(mask), _ptr(last),
+                             _ptr(out), _ptr(lse), B, Hq, Hkv, C, D, int(W), float(scale), dt,
+                             num_splits, _ptr(ws), wsb, _ptr(dev_status), _stream(q.device))
+    _check("kvd_attend_window", st)
+    return out
+
+
+def append_attend_window(q, k_cache, v_cache, mask, k_new, v_new, pos, W, scale=None, out=None,
+                         lse=None, num_splits=0, workspace=None, dev_status=None):
+    """kvd_append_attend_window: kvd_append then kvd_attend_window with
+    last = pos, in one launch when Hq / Hkv <= 8.  Returns out [B, Hq, D]."""
+    B, Hq, Hkv, C, D = _window_args("append_attend_window", q, k_cache, v_cache, mask, W, pos,
+                                    (("k_new", k_new), ("v_new", v_new), ("pos", pos)))
+    if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D):
+        raise ValueError("append_attend_window: shape mismatch")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype == k_new.dtype == v_new.dtype):
+        raise TypeError("append_attend_window: q, caches and new rows must share a dtype")
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is not None:
+        _cuda_contig("lse", lse)
+    L = load()
+    need = L.kvd_attend_window_workspace_bytes(B, Hq, Hkv, C, D, int(W), dt, num_splits)
+    ws, wsb = _workspace(need, q.device, workspace)
+    st = L.kvd_append_attend_window(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(mask),
+                                    _ptr(k_new), _ptr(v_new), _ptr(pos), _ptr(out), _ptr(lse), B,
+                                    Hq, Hkv, C, D, int(W), float(scale), dt, num_splits, _ptr(ws),
+                                    wsb, _ptr(dev_status), _stream(q.device))
+    _check("kvd_append_attend_window", st)
     return out
 
 

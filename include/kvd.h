@@ -256,6 +256,51 @@ kvd_status kvd_append_attend_masked(const void* q, void* k_cache, void* v_cache,
                                     kvd_stream_t stream);
 
 /*
+ * kvd_attend_window -- sliding-window decode attention over the static
+ * buffer ([NPU] Part 3, the sliding-window tile variant; Part 1 for the
+ * mask): row b attends to the slots j with mask[b, j] != 0 and
+ *   last[b] - W + 1 <= j <= last[b],
+ * i.e. kvd_attend_masked with every mask slot outside the window taken as 0.
+ *   q [B, Hq, D]; k_cache, v_cache [B, Hkv, C, D]; mask [B, C] uint8;
+ *   last [B] int32, device (the window's newest slot, normally the slot the
+ *   step appended); W >= 1 window slots; out, lse_out, scale, dtype,
+ *   workspace, num_splits and dev_status as for kvd_attend_masked.
+ * The splits are laid over each row's window only (from the 64-slot boundary
+ * at or below last[b] - W + 1), so no slot outside it is scanned or read,
+ * whatever C is.  last[b] outside [0, C): row b is empty (out = 0,
+ * lse = -inf) and KVD_DEV_POS_RANGE is set.  Always the persistent split
+ * kernel (the one-launch cluster kernel holds whole buffers); 1 or 2
+ * launches (kvd_attend_window_plan).  Errors as for kvd_attend_masked, and
+ * KVD_ERR_INVALID_ARG for W < 1 or a null `last`.
+ */
+size_t kvd_attend_window_workspace_bytes(int B, int Hq, int Hkv, int C, int D, int W,
+                                         kvd_dtype dtype, int num_splits);
+/* As kvd_attend_masked_plan, for kvd_attend_window and
+ * kvd_append_attend_window (splits >= 1: never the one-launch kernel). */
+kvd_status kvd_attend_window_plan(int B, int Hq, int Hkv, int C, int D, int W, kvd_dtype dtype,
+                                  int num_splits, kvd_plan* plan);
+kvd_status kvd_attend_window(const void* q, const void* k_cache, const void* v_cache,
+                             const uint8_t* mask, const int32_t* last, void* out, float* lse_out,
+                             int B, int Hq, int Hkv, int C, int D, int W, float scale,
+                             kvd_dtype dtype, int num_splits, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_status, kvd_stream_t stream);
+/*
+ * kvd_append_attend_window -- one sliding-window decode step: the result of
+ * kvd_append(k_cache, v_cache, k_new, v_new, pos, mask) followed by
+ * kvd_attend_window(..., last = pos, W, ...), the append done inside the
+ * attention launch as in kvd_append_attend_masked (Hq / Hkv <= 8; larger
+ * groups run the append kernel first).  pos[b] outside [0, C): nothing is
+ * written for b, row b is empty, KVD_DEV_POS_RANGE is set.  Workspace:
+ * kvd_attend_window_workspace_bytes.
+ */
+kvd_status kvd_append_attend_window(const void* q, void* k_cache, void* v_cache, uint8_t* mask,
+                                    const void* k_new, const void* v_new, const int32_t* pos,
+                                    void* out, float* lse_out, int B, int Hq, int Hkv, int C,
+                                    int D, int W, float scale, kvd_dtype dtype, int num_splits,
+                                    void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                    kvd_stream_t stream);
+
+/*
  * kvd_attend_indexed -- decode attention over a list of cache slots per batch
  * entry ([FlashMLA] "Математическая постановка": the indexer's top-k indices
  * pick the KV rows, P = Q . gathered^T, S = softmax(P * sm_scale),

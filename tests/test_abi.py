@@ -143,3 +143,38 @@ def test_device_status_check():
     with pytest.raises(kvd.KvdDeviceError) as e:
         kvd.check(torch.tensor([1 | 32], dtype=torch.int32))
     assert e.value.names == ["KVD_DEV_POS_RANGE", "KVD_DEV_TIMEOUT"]
+
+
+def test_window_entry_points(lib):
+    """The window entries: the plan covers the window's span (W + 63 slots
+    at most, never beyond the buffer), never the one-launch kernel; W < 1, a
+    null newest-slot array and a short workspace are refused on the host."""
+    from decode_attention_kv_gb300 import kvd
+    P = lambda x: ctypes.c_void_p(x * 4096)  # noqa: E731
+    # the 32768-slot sequence, 32 heads, window 4096: equal splits over the
+    # window's span, as many as give each of the 304 persistent CTAs one unit
+    # (304 // 32 = 9), against 112 over the whole buffer
+    assert kvd.attend_masked_plan(1, 32, 32, 32768, 128).splits == 112
+    win = kvd.attend_window_plan(1, 32, 32, 32768, 128, 4096)
+    assert win.splits == 9 and win.launches == 2
+    R = 32
+    assert lib.kvd_attend_window_workspace_bytes(1, 32, 32, 32768, 128, 4096, 0, 0) == \
+        256 + (R * 9 * 4 + 255) // 256 * 256 + R * 9 * 128 * 4
+    # an explicit split count over the span: 4159 slots in splits of 1056
+    assert kvd.attend_window_plan(1, 32, 32, 32768, 128, 4096, num_splits=4).splits == 4
+    # 304 or more row units: one split per row, the rows written directly
+    pl = kvd.attend_window_plan(64, 32, 8, 8192, 128, 2048)
+    assert pl.splits == 1 and pl.launches == 1
+    assert lib.kvd_attend_window_workspace_bytes(64, 32, 8, 8192, 128, 2048, 0, 0) == 256
+    # a window at least as long as the buffer spans the buffer
+    assert kvd.attend_window_plan(1, 32, 32, 1152, 128, 5000).splits >= 1
+    assert lib.kvd_attend_window_workspace_bytes(1, 4, 4, 64, 64, 0, 0, 0) == 0  # W < 1
+    args = (P(1), P(1), P(1), P(1), P(1), P(1), None, 1, 4, 4, 4096, 128)
+    tail = (0.1, 0, 0, P(2), 1 << 20, None, None)
+    assert lib.kvd_attend_window(*args, 0, *tail) == 1                       # W < 1
+    assert lib.kvd_attend_window(*args[:4], None, *args[5:], 64, *tail) == 1  # no newest slots
+    assert lib.kvd_attend_window(*args, 64, 0.1, 0, 3, None, 0, None, None) == 3  # no workspace
+    fused = (P(1), P(1), P(1), P(1), P(1), P(1), P(1), P(1), None, 1, 4, 4, 4096, 128)
+    assert lib.kvd_append_attend_window(*fused, 0, *tail) == 1
+    assert lib.kvd_append_attend_window(*fused[:6], None, *fused[7:], 64, *tail) == 1
+    assert kvd.attend_window_plan(2, 8, 8, 1152, 128, 64).splits >= 1

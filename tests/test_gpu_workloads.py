@@ -32,8 +32,9 @@ def _bits(t):
     return host(t).view(torch.int16).numpy()
 
 
-def _masked_step_and_check(kvd, lay, what, fused):
-    """Append + attend one layer on the GPU (two calls, or the fused call);
+def _masked_step_and_check(kvd, lay, what, fused, window=0):
+    """Append + attend one layer on the GPU (two calls, or the fused call;
+    with ``window``, the sliding-window entries ending at the appended slot);
     the append compared byte for byte over the whole cache and mask, the
     attention over every (batch entry, head) against the oracle's append
     followed by its attention."""
@@ -43,22 +44,34 @@ def _masked_step_and_check(kvd, lay, what, fused):
     kh, vh, mh = _bits(lay.k_cache).copy(), _bits(lay.v_cache).copy(), host(lay.mask).numpy().copy()
     status = kvd.status_tensor(dev)
     lse = torch.empty(B, Hq, device=dev)
-    if fused:
+    if fused and window:
+        out = kvd.append_attend_window(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.k_new,
+                                       lay.v_new, lay.pos, window, lay.scale, lse=lse,
+                                       dev_status=status)
+    elif fused:
         out = kvd.append_attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.k_new,
                                        lay.v_new, lay.pos, lay.scale, lse=lse, dev_status=status)
     else:
         kvd.append(lay.k_cache, lay.v_cache, lay.k_new, lay.v_new, lay.pos, lay.mask, status)
-        out = kvd.attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale, lse=lse,
-                                dev_status=status)
+        if window:
+            out = kvd.attend_window(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.pos, window,
+                                    lay.scale, lse=lse, dev_status=status)
+        else:
+            out = kvd.attend_masked(lay.q, lay.k_cache, lay.v_cache, lay.mask, lay.scale,
+                                    lse=lse, dev_status=status)
     assert oracle.append(kh, vh, host(lay.k_new), host(lay.v_new), host(lay.pos), mh) == 0
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert np.array_equal(_bits(lay.k_cache), kh), f"{what}: append (K) not bit-exact"
     assert np.array_equal(_bits(lay.v_cache), vh), f"{what}: append (V) not bit-exact"
     assert np.array_equal(host(lay.mask).numpy(), mh), f"{what}: mask after the append"
-    ref, rl = oracle.attend_masked(host(lay.q), torch.from_numpy(kh).view(torch.bfloat16),
-                                   torch.from_numpy(vh).view(torch.bfloat16),
-                                   torch.from_numpy(mh), lay.scale)
+    kr, vr = torch.from_numpy(kh).view(torch.bfloat16), torch.from_numpy(vh).view(torch.bfloat16)
+    if window:
+        ref, rl, err = oracle.attend_window(host(lay.q), kr, vr, torch.from_numpy(mh),
+                                            host(lay.pos), window, lay.scale)
+        assert err == 0
+    else:
+        ref, rl = oracle.attend_masked(host(lay.q), kr, vr, torch.from_numpy(mh), lay.scale)
     assert_attention_close(out, ref, torch.bfloat16, what)
     assert_lse_close(lse, rl, what)
 
@@ -104,6 +117,20 @@ def test_window_full_size(kvd, fused):
     _masked_step_and_check(kvd, lay, "window", fused)
     mask = host(lay.mask)
     assert int(mask.sum()) == 4096 and int(mask[0, -1]) == 1 and int(mask[0, -4096]) == 1
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused"])
+@pytest.mark.parametrize("mask", ["window", "prefix"])
+def test_window_entry_full_size(kvd, fused, mask):
+    """The sliding-window entries on the 32768-slot sequence, window 4096
+    ending at the slot appended at C - 1: over the workload's own mask (the
+    benchmark's step), and over the whole prefix, where the window alone
+    selects the 4096 newest slots.  All 32 heads."""
+    w = W.window(device="cuda", layers=1)
+    lay = w.layers[0]
+    if mask == "prefix":
+        lay.mask = W.prefix_mask([w.C - 1], w.C, "cuda")
+    _masked_step_and_check(kvd, lay, f"window entry, {mask} mask", fused, window=w.window)
 
 
 def test_paged_full_size(kvd):
