@@ -34,6 +34,11 @@ Every function states what it computes and the page section it follows:
   absmax/6 scale per row after them, rows padded to D/2 + 16 bytes.
 * ``combine`` -- the log-sum-exp merge of disjoint key ranges (Part 3, "Flash
   SDPA 路径": tiles merged exactly through running max and sum).
+* ``append_paged_quant``, ``attend_paged_quant``, ``attend_indexed_quant`` --
+  the quantised rows above in the paged layout and through index lists (the
+  FlashMLA page motivates the value + scale layout on paged KV blocks):
+  compositions of the row quantisers, the paged append and gather (whole
+  rows as bytes) and the static-buffer attention over quantised rows.
 """
 from __future__ import annotations
 
@@ -593,3 +598,79 @@ def attend_masked_fp4(q, k_rows, v_rows, mask, scale: float, nthreads: int = 0):
     if rc != 0:
         raise RuntimeError(f"oracle attend_masked_fp4 failed ({rc})")
     return out, lse
+
+
+# ------------------------------------- quantised rows in the paged layout and
+# through index lists: compositions of the functions above (byte copies of
+# whole quantised rows, then the static-buffer attention over the copies)
+
+def _quant(fmt):
+    if fmt == "fp8":
+        return quantize_rows, attend_masked_fp8
+    if fmt == "fp4":
+        return quantize_rows_fp4, attend_masked_fp4
+    raise ValueError(f"oracle: unknown row format {fmt!r}")
+
+
+def append_paged_quant(key_rows, value_rows, block_tables, seq_offset, k_new, v_new, pos,
+                       fmt: str) -> int:
+    """Quantising paged append in place: the new rows k_new, v_new [Q, Hkv, D]
+    (bf16 or fp32) quantised row by row (``quantize_rows`` / ``_fp4``), then
+    written as whole rows through the paged gather's index mapping
+    (``append_paged``) into key_rows, value_rows uint8 [NB, BS, Hkv, RB].
+    Returns error bits."""
+    quantize, _ = _quant(fmt)
+    return append_paged(key_rows, value_rows, block_tables, seq_offset, quantize(k_new),
+                        quantize(v_new), pos)
+
+
+def attend_paged_quant(q, key_rows, value_rows, block_tables, seq_lens, seq_offset,
+                       scale: float, fmt: str, nthreads: int = 0):
+    """Paged decode attention over quantised rows, fp64: the paged gather of
+    whole rows (``gather_paged``), then per sequence the static-buffer
+    attention over quantised rows (``attend_masked_fp8`` / ``_fp4``) over its
+    gathered rows, every one valid.  q [Q, Hq, D]; key_rows, value_rows uint8
+    [NB, BS, Hkv, RB].  Returns (out [Q, Hq, D], lse [Q, Hq]); raises on the
+    gather's error bits (no result is defined then)."""
+    _, attend = _quant(fmt)
+    ko, vo, err = gather_paged(_u8(key_rows), _u8(value_rows), block_tables, seq_lens, seq_offset)
+    if err:
+        raise ValueError(f"oracle.attend_paged_quant: invalid paged inputs (error bits {err})")
+    qa, _ = _storage(q)
+    Q, Hq, D = qa.shape
+    sl = _i32(seq_lens)
+    out = np.zeros((Q, Hq, D), np.float64)
+    lse = np.full((Q, Hq), -np.inf)
+    for s in range(Q):
+        a, b = int(sl[s]), int(sl[s + 1])
+        if b <= a:
+            continue
+        kr = np.ascontiguousarray(ko[a:b].transpose(1, 0, 2)[None])  # [1, Hkv, n, RB]
+        vr = np.ascontiguousarray(vo[a:b].transpose(1, 0, 2)[None])
+        o, l = attend(q[s:s + 1], kr, vr, np.ones((1, b - a), np.uint8), scale, nthreads)
+        out[s], lse[s] = o[0], l[0]
+    return out, lse
+
+
+def attend_indexed_quant(q, k_rows, v_rows, indices, scale: float, fmt: str, nthreads: int = 0):
+    """Index-list decode attention over quantised rows, fp64: entry j of
+    batch entry b with 0 <= indices[b, j] < C contributes row indices[b, j]
+    of k_rows, v_rows uint8 [B, Hkv, C, RB] as one softmax term.  Written as
+    the copy of every entry's row into a [B, Hkv, topk, RB] buffer whose mask
+    marks the valid entries, then ``attend_masked_fp8`` / ``_fp4`` over it.
+    Returns (out, lse, error bits: 1 when an entry is outside [-1, C))."""
+    _, attend = _quant(fmt)
+    ka = np.ascontiguousarray(_u8(k_rows))
+    va = np.ascontiguousarray(_u8(v_rows))
+    B, Hkv, C, RB = ka.shape
+    idx = _i32(indices).reshape(B, -1)
+    topk = idx.shape[1]
+    err = ERR_POS if np.any((idx < -1) | (idx >= C)) else 0
+    valid = (idx >= 0) & (idx < C)
+    safe = np.where(valid, idx, 0)
+    kg = np.ascontiguousarray(ka[np.arange(B)[:, None, None], np.arange(Hkv)[None, :, None],
+                                 safe[:, None, :]])
+    vg = np.ascontiguousarray(va[np.arange(B)[:, None, None], np.arange(Hkv)[None, :, None],
+                                 safe[:, None, :]])
+    out, lse = attend(q, kg, vg, valid.astype(np.uint8), scale, nthreads)
+    return out, lse, err
