@@ -4,8 +4,10 @@
 
 namespace kvd {
 
-cudaError_t launch_attend_fp4(int D, int G, const AttendParams& p, cudaStream_t stream) {
-    return launch_attend_quant<true>(D, G, p, stream);
+cudaError_t launch_attend_fp4(int D, int G, int mode, const AttendParams& p,
+                               const CUtensorMap* kmap, const CUtensorMap* vmap,
+                               cudaStream_t stream) {
+    return launch_attend_quant<true>(D, G, mode, p, kmap, vmap, stream);
 }
 
 int small_shared_bytes_fp4(int D, int G, int chunk, int slots, int nwg) {

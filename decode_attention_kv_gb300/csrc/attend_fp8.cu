@@ -4,8 +4,10 @@
 
 namespace kvd {
 
-cudaError_t launch_attend_fp8(int D, int G, const AttendParams& p, cudaStream_t stream) {
-    return launch_attend_quant<false>(D, G, p, stream);
+cudaError_t launch_attend_fp8(int D, int G, int mode, const AttendParams& p,
+                               const CUtensorMap* kmap, const CUtensorMap* vmap,
+                               cudaStream_t stream) {
+    return launch_attend_quant<false>(D, G, mode, p, kmap, vmap, stream);
 }
 
 int small_shared_bytes_fp8(int D, int G, int chunk, int slots, int nwg) {

@@ -134,14 +134,13 @@ cudaError_t launch_mma(int mode, const AttendParams& p, const CUtensorMap* kmap,
     return launch_cfg<MmaCfg<D, G>>(mode, p, kmap, vmap, stream);
 }
 
-// Quantised rows: static-buffer mode only (no tensor maps: rows arrive by
-// bulk copies of whole tiles).
+// Quantised rows in every mode: the static buffer's tiles arrive by bulk
+// copies, the paged cache's by 3-D TMA boxes of whole rows (byte tensor
+// maps), index lists by cp.async row gathers.
 template <int D, int G, bool kFp4>
-cudaError_t launch_quant(const AttendParams& p, cudaStream_t stream) {
-    using C = QuantCfg<D, G, kFp4>;
-    CUtensorMap none;
-    std::memset(&none, 0, sizeof none);
-    return launch_kernel<typename C::Cons, C::STAGES, C::MB, kModeMasked>(p, &none, &none, stream);
+cudaError_t launch_quant(int mode, const AttendParams& p, const CUtensorMap* kmap,
+                         const CUtensorMap* vmap, cudaStream_t stream) {
+    return launch_cfg<QuantCfg<D, G, kFp4>>(mode, p, kmap, vmap, stream);
 }
 
 }  // namespace kvd

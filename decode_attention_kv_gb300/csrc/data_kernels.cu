@@ -361,12 +361,55 @@ cudaError_t launch_append_paged(void* key_cache, void* value_cache, const void* 
 __device__ __forceinline__ float as_float(float x) { return x; }
 __device__ __forceinline__ float as_float(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// Where a quantising append writes the row of (entry b, kv head h): slot
+// pos[b] of the static buffer [B, Hkv, C, RB], or, with block tables, token
+// pos[b] of sequence b in the paged cache [NB, BS, Hkv, RB] through the
+// gather's index mapping (the checks in the paged append's order).  Null when
+// the position is refused; `reporter` reports it.
+struct QuantDest {
+    const int32_t* block_tables;  // null: static buffer
+    const int32_t* seq_offset;
+    int NB, BS, cols;
+};
+
+__device__ __forceinline__ unsigned char* quant_row(unsigned char* cache, const QuantDest& pg,
+                                                    int b, int h, int Hkv, int C, int p, int RB,
+                                                    bool reporter, int32_t* dev_status) {
+    if (!pg.block_tables) {
+        if (p < 0 || p >= C) {
+            if (reporter) report(dev_status, KVD_DEV_POS_RANGE);
+            return nullptr;
+        }
+        return cache + (((size_t)b * Hkv + h) * C + p) * RB;
+    }
+    if (p < 0) {
+        if (reporter) report(dev_status, KVD_DEV_POS_RANGE);
+        return nullptr;
+    }
+    const long long off = pg.seq_offset ? pg.seq_offset[b] : 0;
+    if (off < 0 || off % pg.BS) {
+        if (reporter) report(dev_status, KVD_DEV_SEQ_OFFSET);
+        return nullptr;
+    }
+    const long long col = off / pg.BS + p / pg.BS;
+    if (col >= pg.cols) {
+        if (reporter) report(dev_status, KVD_DEV_TABLE_COLS);
+        return nullptr;
+    }
+    const long long phys = pg.block_tables[(size_t)b * pg.cols + col];
+    if (phys < 0 || phys >= pg.NB) {
+        if (reporter) report(dev_status, KVD_DEV_BLOCK_RANGE);
+        return nullptr;
+    }
+    return cache + (((size_t)phys * pg.BS + p % pg.BS) * Hkv + h) * RB;
+}
+
 template <typename In, int D>
 __global__ void __launch_bounds__(128)
 append_fp8_kernel(unsigned char* __restrict__ kc, unsigned char* __restrict__ vc,
                   const In* __restrict__ kn, const In* __restrict__ vn,
                   const int32_t* __restrict__ pos, uint8_t* __restrict__ mask, int B, int Hkv,
-                  int C, int32_t* dev_status) {
+                  int C, QuantDest pg, int32_t* dev_status) {
     pdl_launch_dependents();
     pdl_wait();
     constexpr int VPL = D / 32;
@@ -378,10 +421,9 @@ append_fp8_kernel(unsigned char* __restrict__ kc, unsigned char* __restrict__ vc
     const long long bh = job >> 1;
     const int b = (int)(bh / Hkv);
     const int p = pos[b];
-    if (p < 0 || p >= C) {
-        if (lane == 0 && kv == 0 && bh % Hkv == 0) report(dev_status, KVD_DEV_POS_RANGE);
-        return;
-    }
+    unsigned char* row = quant_row(kv ? vc : kc, pg, b, (int)(bh % Hkv), Hkv, C, p, RB,
+                                   lane == 0 && kv == 0 && bh % Hkv == 0, dev_status);
+    if (!row) return;
     const In* src = (kv ? vn : kn) + bh * D + VPL * lane;
     float x[VPL];
     float amax = 0.f;
@@ -401,7 +443,6 @@ append_fp8_kernel(unsigned char* __restrict__ kc, unsigned char* __restrict__ vc
                                        : 0u;
         codes |= c << (8 * i);
     }
-    unsigned char* row = (kv ? vc : kc) + ((size_t)bh * C + p) * RB;
     if constexpr (VPL == 4)
         *reinterpret_cast<uint32_t*>(row + 4 * lane) = codes;
     else
@@ -414,7 +455,10 @@ append_fp8_kernel(unsigned char* __restrict__ kc, unsigned char* __restrict__ vc
 
 cudaError_t launch_append_fp8(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                               const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
-                              kvd_dtype in_dt, int32_t* dev_status, cudaStream_t stream) {
+                              kvd_dtype in_dt, int32_t* dev_status, cudaStream_t stream,
+                              const int32_t* block_tables, const int32_t* seq_offset, int NB,
+                              int BS, int cols) {
+    const QuantDest pg{block_tables, seq_offset, NB, BS, cols};
     const long long jobs = 2ll * B * Hkv;
     const dim3 grid((unsigned)((jobs + 3) / 4));
     unsigned char* kc = static_cast<unsigned char*>(k_cache);
@@ -423,16 +467,16 @@ cudaError_t launch_append_fp8(void* k_cache, void* v_cache, const void* k_new, c
         const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(k_new);
         const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(v_new);
         return D == 128 ? launch_pdl(append_fp8_kernel<__nv_bfloat16, 128>, grid, dim3(128), 0, stream,
-                                     kc, vc, kn, vn, pos, mask, B, Hkv, C, dev_status)
+                                     kc, vc, kn, vn, pos, mask, B, Hkv, C, pg, dev_status)
                         : launch_pdl(append_fp8_kernel<__nv_bfloat16, 64>, grid, dim3(128), 0, stream,
-                                     kc, vc, kn, vn, pos, mask, B, Hkv, C, dev_status);
+                                     kc, vc, kn, vn, pos, mask, B, Hkv, C, pg, dev_status);
     }
     const float* kn = static_cast<const float*>(k_new);
     const float* vn = static_cast<const float*>(v_new);
     return D == 128 ? launch_pdl(append_fp8_kernel<float, 128>, grid, dim3(128), 0, stream, kc, vc,
-                                 kn, vn, pos, mask, B, Hkv, C, dev_status)
+                                 kn, vn, pos, mask, B, Hkv, C, pg, dev_status)
                     : launch_pdl(append_fp8_kernel<float, 64>, grid, dim3(128), 0, stream, kc, vc,
-                                 kn, vn, pos, mask, B, Hkv, C, dev_status);
+                                 kn, vn, pos, mask, B, Hkv, C, pg, dev_status);
 }
 
 // ------------------------------------------------------------- append_fp4
@@ -458,7 +502,7 @@ __global__ void __launch_bounds__(128)
 append_fp4_kernel(unsigned char* __restrict__ kc, unsigned char* __restrict__ vc,
                   const In* __restrict__ kn, const In* __restrict__ vn,
                   const int32_t* __restrict__ pos, uint8_t* __restrict__ mask, int B, int Hkv,
-                  int C, int32_t* dev_status) {
+                  int C, QuantDest pg, int32_t* dev_status) {
     pdl_launch_dependents();
     pdl_wait();
     constexpr int VPL = D / 32;  // elements per lane: 2 or 4, i.e. 1 or 2 code bytes
@@ -470,10 +514,9 @@ append_fp4_kernel(unsigned char* __restrict__ kc, unsigned char* __restrict__ vc
     const long long bh = job >> 1;
     const int b = (int)(bh / Hkv);
     const int p = pos[b];
-    if (p < 0 || p >= C) {
-        if (lane == 0 && kv == 0 && bh % Hkv == 0) report(dev_status, KVD_DEV_POS_RANGE);
-        return;
-    }
+    unsigned char* row = quant_row(kv ? vc : kc, pg, b, (int)(bh % Hkv), Hkv, C, p, RB,
+                                   lane == 0 && kv == 0 && bh % Hkv == 0, dev_status);
+    if (!row) return;
     const In* src = (kv ? vn : kn) + bh * D + VPL * lane;
     float x[VPL];
     float amax = 0.f;
@@ -491,7 +534,6 @@ append_fp4_kernel(unsigned char* __restrict__ kc, unsigned char* __restrict__ vc
         const uint32_t c = scale > 0.f ? e2m1_code(__fdiv_rn(x[i], scale)) : 0u;
         codes |= c << (4 * i);
     }
-    unsigned char* row = (kv ? vc : kc) + ((size_t)bh * C + p) * RB;
     if constexpr (VPL == 4)
         *reinterpret_cast<uint16_t*>(row + 2 * lane) = (uint16_t)codes;
     else
@@ -504,7 +546,10 @@ append_fp4_kernel(unsigned char* __restrict__ kc, unsigned char* __restrict__ vc
 
 cudaError_t launch_append_fp4(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                               const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
-                              kvd_dtype in_dt, int32_t* dev_status, cudaStream_t stream) {
+                              kvd_dtype in_dt, int32_t* dev_status, cudaStream_t stream,
+                              const int32_t* block_tables, const int32_t* seq_offset, int NB,
+                              int BS, int cols) {
+    const QuantDest pg{block_tables, seq_offset, NB, BS, cols};
     const long long jobs = 2ll * B * Hkv;
     const dim3 grid((unsigned)((jobs + 3) / 4));
     unsigned char* kc = static_cast<unsigned char*>(k_cache);
@@ -513,16 +558,16 @@ cudaError_t launch_append_fp4(void* k_cache, void* v_cache, const void* k_new, c
         const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(k_new);
         const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(v_new);
         return D == 128 ? launch_pdl(append_fp4_kernel<__nv_bfloat16, 128>, grid, dim3(128), 0, stream,
-                                     kc, vc, kn, vn, pos, mask, B, Hkv, C, dev_status)
+                                     kc, vc, kn, vn, pos, mask, B, Hkv, C, pg, dev_status)
                         : launch_pdl(append_fp4_kernel<__nv_bfloat16, 64>, grid, dim3(128), 0, stream,
-                                     kc, vc, kn, vn, pos, mask, B, Hkv, C, dev_status);
+                                     kc, vc, kn, vn, pos, mask, B, Hkv, C, pg, dev_status);
     }
     const float* kn = static_cast<const float*>(k_new);
     const float* vn = static_cast<const float*>(v_new);
     return D == 128 ? launch_pdl(append_fp4_kernel<float, 128>, grid, dim3(128), 0, stream, kc, vc,
-                                 kn, vn, pos, mask, B, Hkv, C, dev_status)
+                                 kn, vn, pos, mask, B, Hkv, C, pg, dev_status)
                     : launch_pdl(append_fp4_kernel<float, 64>, grid, dim3(128), 0, stream, kc, vc,
-                                 kn, vn, pos, mask, B, Hkv, C, dev_status);
+                                 kn, vn, pos, mask, B, Hkv, C, pg, dev_status);
 }
 
 // ------------------------------------------------------------------- gather

@@ -20,14 +20,18 @@ cudaError_t launch_attend_f32(int D, int G, int mode, const AttendParams& p,
                               cudaStream_t stream);
 AttendGeom attend_geom_bf16(int D, int G);
 AttendGeom attend_geom_f32(int D, int G);
-cudaError_t launch_attend_fp8(int D, int G, const AttendParams& p, cudaStream_t stream);
+cudaError_t launch_attend_fp8(int D, int G, int mode, const AttendParams& p,
+                               const CUtensorMap* kmap, const CUtensorMap* vmap,
+                               cudaStream_t stream);
 cudaError_t launch_attend_small(kvd_dtype dt, int D, int G, const AttendParams& p, int S, int rows,
                                 const CUtensorMap* kmap, const CUtensorMap* vmap,
                                 cudaStream_t stream);
 int small_shared_bytes(kvd_dtype dt, int D, int G, int chunk, int slots, int nwg);
 int small_shared_bytes_fp8(int D, int G, int chunk, int slots, int nwg);
 int small_shared_bytes_fp4(int D, int G, int chunk, int slots, int nwg);
-cudaError_t launch_attend_fp4(int D, int G, const AttendParams& p, cudaStream_t stream);
+cudaError_t launch_attend_fp4(int D, int G, int mode, const AttendParams& p,
+                               const CUtensorMap* kmap, const CUtensorMap* vmap,
+                               cudaStream_t stream);
 cudaError_t launch_attend_small_fp4(int D, int G, const AttendParams& p, int S, int rows,
                                     cudaStream_t stream);
 cudaError_t launch_attend_small_fp8(int D, int G, const AttendParams& p, int S, int rows,
@@ -781,8 +785,10 @@ kvd_status attend_quant(const char* fn, RowKind rk, const void* q, const void* k
         if (es != cudaSuccess) return cuda_fail(es, fn);
         return ok();
     }
-    cudaError_t e = fp4 ? launch_attend_fp4(D, pl.G, p, (cudaStream_t)stream)
-                        : launch_attend_fp8(D, pl.G, p, (cudaStream_t)stream);
+    CUtensorMap none;
+    std::memset(&none, 0, sizeof none);
+    cudaError_t e = fp4 ? launch_attend_fp4(D, pl.G, kModeMasked, p, &none, &none, (cudaStream_t)stream)
+                        : launch_attend_fp8(D, pl.G, kModeMasked, p, &none, &none, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, fn);
     if (pl.S > 1) {
         e = launch_combine(p.part_o, p.part_lse, out, lse_out, B * Hq, pl.S, D, KVD_BF16,
@@ -795,6 +801,167 @@ kvd_status attend_quant(const char* fn, RowKind rk, const void* q, const void* k
 size_t quant_workspace_bytes(int B, int Hq, int Hkv, int C, int D, int num_splits) {
     if (B < 1 || C < 1 || check_attention_shape(Hq, Hkv, D, KVD_BF16) != KVD_OK) return 0;
     return plan_attention(B, Hq, Hkv, C, D, KVD_BF16, 0, num_splits, false, kQuantTile).ws;
+}
+
+int quant_row_bytes(RowKind rk, int D) { return (rk == kRowsFp4 ? D / 2 : D) + 16; }
+
+// 3-D tensor map over the quantised rows of a paged cache [NB*BS, Hkv, RB]
+// (bytes): boxes of `tile` whole rows of one kv head, unswizzled.
+kvd_status make_row_map(CUtensorMap* map, const void* cache, long long rows, int Hkv, int RB,
+                        int tile) {
+    const cudaError_t e = get_encoder();
+    if (e != cudaSuccess || !g_encode) return cuda_fail(e, "cuTensorMapEncodeTiled lookup");
+    const cuuint64_t dims[3] = {(cuuint64_t)RB, (cuuint64_t)Hkv, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)RB, (cuuint64_t)Hkv * RB};
+    const cuuint32_t box[3] = {(cuuint32_t)RB, 1u, (cuuint32_t)tile};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(cache),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KVD_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return KVD_OK;
+}
+
+kvd_status append_paged_quant(const char* fn, bool fp4, void* key_cache, void* value_cache,
+                              const void* k_new, const void* v_new, const int32_t* block_tables,
+                              const int32_t* seq_offset, const int32_t* pos, int Q, int NB,
+                              int BS, int cols, int Hkv, int D, kvd_dtype new_dtype,
+                              int32_t* dev_status, kvd_stream_t stream) {
+    if (Q < 0 || NB < 1 || BS < 1 || cols < 1 || Hkv < 1)
+        return fail(KVD_ERR_INVALID_ARG, "%s: Q >= 0 and NB, BS, cols, Hkv >= 1 required", fn);
+    if (Q == 0) return ok();
+    if (!key_cache || !value_cache || !k_new || !v_new || !block_tables || !pos)
+        return fail(KVD_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!dtype_ok(new_dtype)) return fail(KVD_ERR_INVALID_ARG, "%s: unknown dtype", fn);
+    if (D != 64 && D != 128) return fail(KVD_ERR_UNSUPPORTED, "%s: head_dim %d (supported: 64, 128)", fn, D);
+    if (!aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(k_new, 16) ||
+        !aligned(v_new, 16) || !aligned(block_tables, 4) || !aligned(seq_offset, 4) ||
+        !aligned(pos, 4) || !aligned(dev_status, 4))
+        return fail(KVD_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+    if (2ll * Q * Hkv > (1ll << 33)) return fail(KVD_ERR_UNSUPPORTED, "%s: Q*Hkv too large", fn);
+    const cudaError_t e =
+        fp4 ? launch_append_fp4(key_cache, value_cache, k_new, v_new, pos, nullptr, Q, Hkv, 0, D,
+                                new_dtype, dev_status, (cudaStream_t)stream, block_tables,
+                                seq_offset, NB, BS, cols)
+            : launch_append_fp8(key_cache, value_cache, k_new, v_new, pos, nullptr, Q, Hkv, 0, D,
+                                new_dtype, dev_status, (cudaStream_t)stream, block_tables,
+                                seq_offset, NB, BS, cols);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return ok();
+}
+
+Plan paged_quant_plan(int Q, int Hq, int Hkv, int BS, int cols, int D, int num_splits) {
+    return plan_attention(Q, Hq, Hkv, cols * BS, D, KVD_BF16, BS, num_splits, false, kQuantTile);
+}
+
+kvd_status attend_paged_quant(const char* fn, RowKind rk, const void* q, const void* key_cache,
+                              const void* value_cache, const int32_t* block_tables,
+                              const int32_t* seq_lens, const int32_t* seq_offset, void* out,
+                              float* lse_out, int Q, int Hq, int Hkv, int NB, int BS, int cols,
+                              int D, float scale, int num_splits, void* workspace,
+                              size_t workspace_bytes, int32_t* dev_status, kvd_stream_t stream) {
+    kvd_status st = check_attention_shape(Hq, Hkv, D, KVD_BF16);
+    if (st != KVD_OK) return st;
+    if (Q < 0 || NB < 1 || BS < 1 || cols < 1)
+        return fail(KVD_ERR_INVALID_ARG, "%s: Q >= 0, NB, BS, cols >= 1 required", fn);
+    if (Q == 0) return ok();
+    if (!q || !key_cache || !value_cache || !block_tables || !seq_lens || !out)
+        return fail(KVD_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned(q, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+        !aligned(out, 16) || !aligned(lse_out, 4) || !aligned(block_tables, 4) ||
+        !aligned(seq_lens, 4) || !aligned(seq_offset, 4) || !aligned(dev_status, 4))
+        return fail(KVD_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+    if ((long long)NB * BS >= (1ll << 31)) return fail(KVD_ERR_UNSUPPORTED, "%s: NB*BS >= 2^31", fn);
+    if ((long long)cols * BS >= (1ll << 31)) return fail(KVD_ERR_UNSUPPORTED, "%s: cols*BS >= 2^31", fn);
+    if (num_splits < 0) return fail(KVD_ERR_INVALID_ARG, "%s: num_splits < 0", fn);
+    const Plan pl = paged_quant_plan(Q, Hq, Hkv, BS, cols, D, num_splits);
+    st = check_workspace(fn, pl, workspace, workspace_bytes);
+    if (st != KVD_OK) return st;
+    const int RB = quant_row_bytes(rk, D);
+    CUtensorMap kmap, vmap;
+    st = make_row_map(&kmap, key_cache, (long long)NB * BS, Hkv, RB, pl.tile);
+    if (st != KVD_OK) return st;
+    st = make_row_map(&vmap, value_cache, (long long)NB * BS, Hkv, RB, pl.tile);
+    if (st != KVD_OK) return st;
+    AttendParams p{};
+    p.q = q;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.seq_offset = seq_offset;
+    p.out = out;
+    p.lse_out = lse_out;
+    p.dev_status = dev_status;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.g = Hq / Hkv;
+    p.BS = BS;
+    p.cols = cols;
+    p.NB = NB;
+    p.qscale = scale * kLog2e;
+    attach_workspace(p, pl, workspace);
+    cudaError_t e = rk == kRowsFp4
+                        ? launch_attend_fp4(D, pl.G, kModePaged, p, &kmap, &vmap, (cudaStream_t)stream)
+                        : launch_attend_fp8(D, pl.G, kModePaged, p, &kmap, &vmap, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    if (pl.S > 1) {
+        e = launch_combine(p.part_o, p.part_lse, out, lse_out, Q * Hq, pl.S, D, KVD_BF16,
+                           (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    }
+    return ok();
+}
+
+Plan indexed_quant_plan(int B, int Hq, int Hkv, int topk, int D, int num_splits) {
+    return plan_attention(B, Hq, Hkv, topk, D, KVD_BF16, 0, num_splits, true, kQuantTile);
+}
+
+kvd_status attend_indexed_quant(const char* fn, RowKind rk, const void* q, const void* k_cache,
+                                const void* v_cache, const int32_t* indices, void* out,
+                                float* lse_out, int B, int Hq, int Hkv, int C, int topk, int D,
+                                float scale, int num_splits, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, kvd_stream_t stream) {
+    kvd_status st = check_attention_shape(Hq, Hkv, D, KVD_BF16);
+    if (st != KVD_OK) return st;
+    if (B < 0 || C < 1 || topk < 1)
+        return fail(KVD_ERR_INVALID_ARG, "%s: B >= 0, C >= 1 and topk >= 1 required", fn);
+    if (B == 0) return ok();
+    if (!q || !k_cache || !v_cache || !indices || !out)
+        return fail(KVD_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(indices, 4) || !aligned(lse_out, 4) || !aligned(dev_status, 4))
+        return fail(KVD_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+    if (num_splits < 0) return fail(KVD_ERR_INVALID_ARG, "%s: num_splits < 0", fn);
+    const Plan pl = indexed_quant_plan(B, Hq, Hkv, topk, D, num_splits);
+    st = check_workspace(fn, pl, workspace, workspace_bytes);
+    if (st != KVD_OK) return st;
+    AttendParams p{};
+    p.q = q;
+    p.k = k_cache;
+    p.v = v_cache;
+    p.indices = indices;
+    p.out = out;
+    p.lse_out = lse_out;
+    p.dev_status = dev_status;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.g = Hq / Hkv;
+    p.C = C;
+    p.topk = topk;
+    p.qscale = scale * kLog2e;
+    attach_workspace(p, pl, workspace);
+    CUtensorMap none;  // unused: the listed rows are gathered with cp.async
+    std::memset(&none, 0, sizeof none);
+    cudaError_t e = rk == kRowsFp4
+                        ? launch_attend_fp4(D, pl.G, kModeIndexed, p, &none, &none, (cudaStream_t)stream)
+                        : launch_attend_fp8(D, pl.G, kModeIndexed, p, &none, &none, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    if (pl.S > 1) {
+        e = launch_combine(p.part_o, p.part_lse, out, lse_out, B * Hq, pl.S, D, KVD_BF16,
+                           (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    }
+    return ok();
 }
 
 }  // namespace
@@ -851,6 +1018,142 @@ kvd_status kvd_attend_masked_fp4(const void* q, const void* k_cache, const void*
     return attend_quant("kvd_attend_masked_fp4", kRowsFp4, q, k_cache, v_cache, mask, out, lse_out,
                         B, Hq, Hkv, C, D, scale, num_splits, workspace, workspace_bytes,
                         dev_status, stream);
+}
+
+kvd_status kvd_append_paged_fp8(void* key_cache, void* value_cache, const void* k_new,
+                                const void* v_new, const int32_t* block_tables,
+                                const int32_t* seq_offset, const int32_t* pos, int Q, int NB,
+                                int BS, int cols, int Hkv, int D, kvd_dtype new_dtype,
+                                int32_t* dev_status, kvd_stream_t stream) {
+    return append_paged_quant("kvd_append_paged_fp8", false, key_cache, value_cache, k_new, v_new,
+                              block_tables, seq_offset, pos, Q, NB, BS, cols, Hkv, D, new_dtype,
+                              dev_status, stream);
+}
+
+size_t kvd_attend_paged_fp8_workspace_bytes(int Q, int Hq, int Hkv, int BS, int cols, int D,
+                                             int num_splits) {
+    if (Q < 1 || BS < 1 || cols < 1 || check_attention_shape(Hq, Hkv, D, KVD_BF16) != KVD_OK) return 0;
+    return paged_quant_plan(Q, Hq, Hkv, BS, cols, D, num_splits).ws;
+}
+
+kvd_status kvd_attend_paged_fp8_plan(int Q, int Hq, int Hkv, int BS, int cols, int D,
+                                      int num_splits, kvd_plan* plan) {
+    if (!plan) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_paged_fp8_plan: null pointer");
+    if (Q < 1 || BS < 1 || cols < 1 || num_splits < 0)
+        return fail(KVD_ERR_INVALID_ARG,
+                    "kvd_attend_paged_fp8_plan: Q, BS, cols >= 1 and num_splits >= 0 required");
+    const kvd_status st = check_attention_shape(Hq, Hkv, D, KVD_BF16);
+    if (st != KVD_OK) return st;
+    put_plan(paged_quant_plan(Q, Hq, Hkv, BS, cols, D, num_splits), false, plan);
+    return ok();
+}
+
+kvd_status kvd_attend_paged_fp8(const void* q, const void* key_cache, const void* value_cache,
+                                const int32_t* block_tables, const int32_t* seq_lens,
+                                const int32_t* seq_offset, void* out, float* lse_out, int Q,
+                                int Hq, int Hkv, int NB, int BS, int cols, int D, float scale,
+                                int num_splits, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_status, kvd_stream_t stream) {
+    return attend_paged_quant("kvd_attend_paged_fp8", kRowsFp8, q, key_cache, value_cache,
+                              block_tables, seq_lens, seq_offset, out, lse_out, Q, Hq, Hkv, NB,
+                              BS, cols, D, scale, num_splits, workspace, workspace_bytes,
+                              dev_status, stream);
+}
+
+size_t kvd_attend_indexed_fp8_workspace_bytes(int B, int Hq, int Hkv, int topk, int D,
+                                               int num_splits) {
+    if (B < 1 || topk < 1 || check_attention_shape(Hq, Hkv, D, KVD_BF16) != KVD_OK) return 0;
+    return indexed_quant_plan(B, Hq, Hkv, topk, D, num_splits).ws;
+}
+
+kvd_status kvd_attend_indexed_fp8_plan(int B, int Hq, int Hkv, int topk, int D, int num_splits,
+                                        kvd_plan* plan) {
+    if (!plan) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_indexed_fp8_plan: null pointer");
+    if (B < 1 || topk < 1 || num_splits < 0)
+        return fail(KVD_ERR_INVALID_ARG,
+                    "kvd_attend_indexed_fp8_plan: B, topk >= 1 and num_splits >= 0 required");
+    const kvd_status st = check_attention_shape(Hq, Hkv, D, KVD_BF16);
+    if (st != KVD_OK) return st;
+    put_plan(indexed_quant_plan(B, Hq, Hkv, topk, D, num_splits), false, plan);
+    return ok();
+}
+
+kvd_status kvd_attend_indexed_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* indices, void* out, float* lse_out, int B,
+                                  int Hq, int Hkv, int C, int topk, int D, float scale,
+                                  int num_splits, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, kvd_stream_t stream) {
+    return attend_indexed_quant("kvd_attend_indexed_fp8", kRowsFp8, q, k_cache, v_cache, indices,
+                                out, lse_out, B, Hq, Hkv, C, topk, D, scale, num_splits, workspace,
+                                workspace_bytes, dev_status, stream);
+}
+
+kvd_status kvd_append_paged_fp4(void* key_cache, void* value_cache, const void* k_new,
+                                const void* v_new, const int32_t* block_tables,
+                                const int32_t* seq_offset, const int32_t* pos, int Q, int NB,
+                                int BS, int cols, int Hkv, int D, kvd_dtype new_dtype,
+                                int32_t* dev_status, kvd_stream_t stream) {
+    return append_paged_quant("kvd_append_paged_fp4", true, key_cache, value_cache, k_new, v_new,
+                              block_tables, seq_offset, pos, Q, NB, BS, cols, Hkv, D, new_dtype,
+                              dev_status, stream);
+}
+
+size_t kvd_attend_paged_fp4_workspace_bytes(int Q, int Hq, int Hkv, int BS, int cols, int D,
+                                             int num_splits) {
+    if (Q < 1 || BS < 1 || cols < 1 || check_attention_shape(Hq, Hkv, D, KVD_BF16) != KVD_OK) return 0;
+    return paged_quant_plan(Q, Hq, Hkv, BS, cols, D, num_splits).ws;
+}
+
+kvd_status kvd_attend_paged_fp4_plan(int Q, int Hq, int Hkv, int BS, int cols, int D,
+                                      int num_splits, kvd_plan* plan) {
+    if (!plan) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_paged_fp4_plan: null pointer");
+    if (Q < 1 || BS < 1 || cols < 1 || num_splits < 0)
+        return fail(KVD_ERR_INVALID_ARG,
+                    "kvd_attend_paged_fp4_plan: Q, BS, cols >= 1 and num_splits >= 0 required");
+    const kvd_status st = check_attention_shape(Hq, Hkv, D, KVD_BF16);
+    if (st != KVD_OK) return st;
+    put_plan(paged_quant_plan(Q, Hq, Hkv, BS, cols, D, num_splits), false, plan);
+    return ok();
+}
+
+kvd_status kvd_attend_paged_fp4(const void* q, const void* key_cache, const void* value_cache,
+                                const int32_t* block_tables, const int32_t* seq_lens,
+                                const int32_t* seq_offset, void* out, float* lse_out, int Q,
+                                int Hq, int Hkv, int NB, int BS, int cols, int D, float scale,
+                                int num_splits, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_status, kvd_stream_t stream) {
+    return attend_paged_quant("kvd_attend_paged_fp4", kRowsFp4, q, key_cache, value_cache,
+                              block_tables, seq_lens, seq_offset, out, lse_out, Q, Hq, Hkv, NB,
+                              BS, cols, D, scale, num_splits, workspace, workspace_bytes,
+                              dev_status, stream);
+}
+
+size_t kvd_attend_indexed_fp4_workspace_bytes(int B, int Hq, int Hkv, int topk, int D,
+                                               int num_splits) {
+    if (B < 1 || topk < 1 || check_attention_shape(Hq, Hkv, D, KVD_BF16) != KVD_OK) return 0;
+    return indexed_quant_plan(B, Hq, Hkv, topk, D, num_splits).ws;
+}
+
+kvd_status kvd_attend_indexed_fp4_plan(int B, int Hq, int Hkv, int topk, int D, int num_splits,
+                                        kvd_plan* plan) {
+    if (!plan) return fail(KVD_ERR_INVALID_ARG, "kvd_attend_indexed_fp4_plan: null pointer");
+    if (B < 1 || topk < 1 || num_splits < 0)
+        return fail(KVD_ERR_INVALID_ARG,
+                    "kvd_attend_indexed_fp4_plan: B, topk >= 1 and num_splits >= 0 required");
+    const kvd_status st = check_attention_shape(Hq, Hkv, D, KVD_BF16);
+    if (st != KVD_OK) return st;
+    put_plan(indexed_quant_plan(B, Hq, Hkv, topk, D, num_splits), false, plan);
+    return ok();
+}
+
+kvd_status kvd_attend_indexed_fp4(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* indices, void* out, float* lse_out, int B,
+                                  int Hq, int Hkv, int C, int topk, int D, float scale,
+                                  int num_splits, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, kvd_stream_t stream) {
+    return attend_indexed_quant("kvd_attend_indexed_fp4", kRowsFp4, q, k_cache, v_cache, indices,
+                                out, lse_out, B, Hq, Hkv, C, topk, D, scale, num_splits, workspace,
+                                workspace_bytes, dev_status, stream);
 }
 
 size_t kvd_attend_indexed_workspace_bytes(int B, int Hq, int Hkv, int topk, int D,

@@ -75,13 +75,22 @@ cudaError_t launch_append_paged(void* key_cache, void* value_cache, const void* 
                                 int BS, int cols, int row_bytes, int32_t* dev_status,
                                 cudaStream_t stream);
 
+// Quantising appends: into the static buffer [B, Hkv, C, RB], or, with
+// block_tables, token pos[b] of sequence b of the paged cache [NB, BS, Hkv, RB]
+// (C unused then).
 cudaError_t launch_append_fp8(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                               const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
-                              kvd_dtype in_dt, int32_t* dev_status, cudaStream_t stream);
+                              kvd_dtype in_dt, int32_t* dev_status, cudaStream_t stream,
+                              const int32_t* block_tables = nullptr,
+                              const int32_t* seq_offset = nullptr, int NB = 0, int BS = 0,
+                              int cols = 0);
 
 cudaError_t launch_append_fp4(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                               const int32_t* pos, uint8_t* mask, int B, int Hkv, int C, int D,
-                              kvd_dtype in_dt, int32_t* dev_status, cudaStream_t stream);
+                              kvd_dtype in_dt, int32_t* dev_status, cudaStream_t stream,
+                              const int32_t* block_tables = nullptr,
+                              const int32_t* seq_offset = nullptr, int NB = 0, int BS = 0,
+                              int cols = 0);
 
 cudaError_t launch_gather(const void* key_cache, const void* value_cache,
                           const int32_t* block_tables, const int32_t* seq_lens,

@@ -59,6 +59,20 @@ SIGNATURES = {
     "kvd_attend_masked_fp4_workspace_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
     "kvd_attend_masked_fp4": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _sz,
                                _vp, _vp], _i),
+    "kvd_append_paged_fp8": ([_vp] * 7 + [_i] * 7 + [_vp, _vp], _i),
+    "kvd_attend_paged_fp8_workspace_bytes": ([_i] * 7, _sz),
+    "kvd_attend_paged_fp8_plan": ([_i] * 7 + [_vp], _i),
+    "kvd_attend_paged_fp8": ([_vp] * 8 + [_i] * 7 + [_f, _i, _vp, _sz, _vp, _vp], _i),
+    "kvd_attend_indexed_fp8_workspace_bytes": ([_i] * 6, _sz),
+    "kvd_attend_indexed_fp8_plan": ([_i] * 6 + [_vp], _i),
+    "kvd_attend_indexed_fp8": ([_vp] * 6 + [_i] * 6 + [_f, _i, _vp, _sz, _vp, _vp], _i),
+    "kvd_append_paged_fp4": ([_vp] * 7 + [_i] * 7 + [_vp, _vp], _i),
+    "kvd_attend_paged_fp4_workspace_bytes": ([_i] * 7, _sz),
+    "kvd_attend_paged_fp4_plan": ([_i] * 7 + [_vp], _i),
+    "kvd_attend_paged_fp4": ([_vp] * 8 + [_i] * 7 + [_f, _i, _vp, _sz, _vp, _vp], _i),
+    "kvd_attend_indexed_fp4_workspace_bytes": ([_i] * 6, _sz),
+    "kvd_attend_indexed_fp4_plan": ([_i] * 6 + [_vp], _i),
+    "kvd_attend_indexed_fp4": ([_vp] * 6 + [_i] * 6 + [_f, _i, _vp, _sz, _vp, _vp], _i),
     "kvd_attend_indexed_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i], _sz),
     "kvd_attend_indexed": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp,
                             _sz, _vp, _vp], _i),
@@ -282,6 +296,153 @@ def attend_masked_fp4(q, k_cache, v_cache, mask, scale=None, out=None, lse=None,
     [B, Hkv, C, D/2 + 16]); otherwise as attend_masked_fp8."""
     return _attend_quant("fp4", q, k_cache, v_cache, mask, scale, out, lse, num_splits,
                          workspace, dev_status)
+
+
+# ------------------------------- quantised rows: paged layout, index lists
+
+def _quant_row_d(fmt, RB, name):
+    D = _ROW_D[fmt](RB)
+    if D not in (64, 128):
+        raise ValueError(f"{name}: row bytes {RB} do not give head_dim 64 or 128")
+    return D
+
+
+def _append_paged_quant(fmt, key_cache, value_cache, block_tables, seq_offset, k_new, v_new, pos,
+                        dev_status):
+    name = f"append_paged_{fmt}"
+    for n, t in (("key_cache", key_cache), ("value_cache", value_cache), ("k_new", k_new),
+                 ("v_new", v_new), ("block_tables", block_tables), ("pos", pos)):
+        _cuda_contig(n, t)
+    NB, BS, Hkv, RB = key_cache.shape
+    D = _quant_row_d(fmt, RB, name)
+    Q, cols = block_tables.shape
+    if key_cache.dtype != torch.uint8 or value_cache.dtype != torch.uint8 or \
+            value_cache.shape != key_cache.shape:
+        raise ValueError(f"{name}: caches must be uint8 [NB, BS, Hkv, row bytes]")
+    if k_new.shape != (Q, Hkv, D) or v_new.shape != (Q, Hkv, D) or k_new.dtype != v_new.dtype \
+            or pos.numel() != Q:
+        raise ValueError(f"{name}: shape mismatch")
+    if block_tables.dtype != torch.int32 or pos.dtype != torch.int32 or \
+            (seq_offset is not None and seq_offset.dtype != torch.int32):
+        raise ValueError(f"{name}: int32 tables, offsets and positions")
+    fn = f"kvd_{name}"
+    st = getattr(load(), fn)(_ptr(key_cache), _ptr(value_cache), _ptr(k_new), _ptr(v_new),
+                             _ptr(block_tables), _ptr(seq_offset), _ptr(pos), Q, NB, BS, cols, Hkv,
+                             D, _dtype_code(k_new), _ptr(dev_status), _stream(key_cache.device))
+    _check(fn, st)
+
+
+def append_paged_fp8(key_cache, value_cache, block_tables, seq_offset, k_new, v_new, pos,
+                     dev_status=None):
+    """kvd_append_paged_fp8: the step's K/V rows (bf16 or fp32 [Q, Hkv, D])
+    quantised into token pos[q] of the paged E4M3 caches (uint8
+    [NB, BS, Hkv, D + 16])."""
+    _append_paged_quant("fp8", key_cache, value_cache, block_tables, seq_offset, k_new, v_new, pos,
+                        dev_status)
+
+
+def append_paged_fp4(key_cache, value_cache, block_tables, seq_offset, k_new, v_new, pos,
+                     dev_status=None):
+    """kvd_append_paged_fp4: as append_paged_fp8 into E2M1 caches (uint8
+    [NB, BS, Hkv, D/2 + 16])."""
+    _append_paged_quant("fp4", key_cache, value_cache, block_tables, seq_offset, k_new, v_new, pos,
+                        dev_status)
+
+
+def attend_paged_quant_workspace_bytes(fmt, Q, Hq, Hkv, BS, cols, D, num_splits=0):
+    return getattr(load(), f"kvd_attend_paged_{fmt}_workspace_bytes")(Q, Hq, Hkv, BS, cols, D,
+                                                                       num_splits)
+
+
+def attend_paged_quant_plan(fmt, Q, Hq, Hkv, BS, cols, D, num_splits=0):
+    return _plan(f"kvd_attend_paged_{fmt}_plan", Q, Hq, Hkv, BS, cols, D, num_splits)
+
+
+def attend_paged_quant(fmt, q, key_cache, value_cache, block_tables, seq_lens, seq_offset=None,
+                       scale=None, out=None, lse=None, num_splits=0, workspace=None,
+                       dev_status=None):
+    """kvd_attend_paged_fp8 / _fp4 (fmt "fp8" / "fp4"): paged decode attention
+    over quantised rows.  q [Q, Hq, D] bf16; caches uint8 [NB, BS, Hkv, RB];
+    block_tables [Q, cols], seq_lens [Q + 1], seq_offset [Q] or None, int32."""
+    name = f"attend_paged_{fmt}"
+    for n, t in (("q", q), ("key_cache", key_cache), ("value_cache", value_cache),
+                 ("block_tables", block_tables), ("seq_lens", seq_lens)):
+        _cuda_contig(n, t)
+    Q, Hq, D = q.shape
+    NB, BS, Hkv, RB = key_cache.shape
+    if _quant_row_d(fmt, RB, name) != D or value_cache.shape != key_cache.shape:
+        raise ValueError(f"{name}: shape mismatch")
+    if q.dtype != torch.bfloat16 or key_cache.dtype != torch.uint8 or \
+            value_cache.dtype != torch.uint8:
+        raise TypeError(f"{name}: q bf16, caches uint8")
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or block_tables.shape[0] != Q:
+        raise ValueError(f"{name}: block_tables must be int32 [Q, cols]")
+    if seq_lens.dtype != torch.int32 or seq_lens.shape != (Q + 1,):
+        raise ValueError(f"{name}: only cumsum seq_lens [Q+1] int32 is supported")
+    if seq_offset is not None:
+        _cuda_contig("seq_offset", seq_offset)
+        if seq_offset.dtype != torch.int32 or seq_offset.shape != (Q,):
+            raise ValueError(f"{name}: seq_offset must be int32 [Q]")
+    cols = block_tables.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is not None:
+        _cuda_contig("lse", lse)
+    L = load()
+    fn = f"kvd_{name}"
+    need = getattr(L, fn + "_workspace_bytes")(Q, Hq, Hkv, BS, cols, D, num_splits)
+    ws, wsb = _workspace(need, q.device, workspace)
+    st = getattr(L, fn)(_ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_tables),
+                        _ptr(seq_lens), _ptr(seq_offset), _ptr(out), _ptr(lse), Q, Hq, Hkv, NB,
+                        BS, cols, D, float(scale), num_splits, _ptr(ws), wsb, _ptr(dev_status),
+                        _stream(q.device))
+    _check(fn, st)
+    return out
+
+
+def attend_indexed_quant_workspace_bytes(fmt, B, Hq, Hkv, topk, D, num_splits=0):
+    return getattr(load(), f"kvd_attend_indexed_{fmt}_workspace_bytes")(B, Hq, Hkv, topk, D,
+                                                                         num_splits)
+
+
+def attend_indexed_quant_plan(fmt, B, Hq, Hkv, topk, D, num_splits=0):
+    return _plan(f"kvd_attend_indexed_{fmt}_plan", B, Hq, Hkv, topk, D, num_splits)
+
+
+def attend_indexed_quant(fmt, q, k_cache, v_cache, indices, scale=None, out=None, lse=None,
+                         num_splits=0, workspace=None, dev_status=None):
+    """kvd_attend_indexed_fp8 / _fp4 (fmt "fp8" / "fp4"): index-list decode
+    attention over quantised rows.  q [B, Hq, D] bf16; caches uint8
+    [B, Hkv, C, RB]; indices [B, topk] int32 (-1 = unused entry)."""
+    name = f"attend_indexed_{fmt}"
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("indices", indices)):
+        _cuda_contig(n, t)
+    B, Hq, D = q.shape
+    Bk, Hkv, C, RB = k_cache.shape
+    if Bk != B or _quant_row_d(fmt, RB, name) != D or v_cache.shape != k_cache.shape:
+        raise ValueError(f"{name}: shape mismatch")
+    if q.dtype != torch.bfloat16 or k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise TypeError(f"{name}: q bf16, caches uint8")
+    if indices.dtype != torch.int32 or indices.dim() != 2 or indices.shape[0] != B:
+        raise ValueError(f"{name}: indices must be int32 [B, topk]")
+    topk = indices.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is not None:
+        _cuda_contig("lse", lse)
+    L = load()
+    fn = f"kvd_{name}"
+    need = getattr(L, fn + "_workspace_bytes")(B, Hq, Hkv, topk, D, num_splits)
+    ws, wsb = _workspace(need, q.device, workspace)
+    st = getattr(L, fn)(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(indices), _ptr(out), _ptr(lse),
+                        B, Hq, Hkv, C, topk, D, float(scale), num_splits, _ptr(ws), wsb,
+                        _ptr(dev_status), _stream(q.device))
+    _check(fn, st)
+    return out
 
 
 def pointer_array(tensors, device):

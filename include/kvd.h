@@ -427,6 +427,91 @@ kvd_status kvd_attend_masked_fp4(const void* q, const void* k_cache, const void*
                                  kvd_stream_t stream);
 
 /*
+ * Quantised rows in the paged layout and through index lists ([FlashMLA-KV]
+ * "Оптимизация раскладки KV-кэша при decoding" keeps a token's quantised
+ * values and scale side by side, on paged KV blocks).  The rows are those of
+ * kvd_append_fp8 (RB = D + 16 bytes) and kvd_append_fp4 (RB = D/2 + 16); q
+ * and out are bf16; D in {64, 128}; Hq / Hkv <= 8 query heads per kv head
+ * share one tensor-core consumer pass, larger groups several.
+ *
+ * kvd_append_paged_fp8, kvd_append_paged_fp4 -- kvd_append_paged with the
+ * quantisation of kvd_append_fp8 / kvd_append_fp4: the new rows k_new, v_new
+ * [Q, Hkv, D] (new_dtype bf16 or fp32) quantised row by row and written as
+ * whole rows of key_cache, value_cache uint8 [NB, BS, Hkv, RB] at token pos[q]
+ * of sequence q, through the gather's index mapping ([PyPTO] 3.2).  Checks
+ * and their status bits in kvd_append_paged's order (a refused sequence
+ * writes nothing): pos[q] < 0 KVD_DEV_POS_RANGE, seq_offset[q] negative or
+ * not a multiple of BS KVD_DEV_SEQ_OFFSET, a column at or beyond cols
+ * KVD_DEV_TABLE_COLS, a block outside [0, NB) KVD_DEV_BLOCK_RANGE.
+ */
+kvd_status kvd_append_paged_fp8(void* key_cache, void* value_cache, const void* k_new,
+                                const void* v_new, const int32_t* block_tables,
+                                const int32_t* seq_offset, const int32_t* pos, int Q, int NB,
+                                int BS, int cols, int Hkv, int D, kvd_dtype new_dtype,
+                                int32_t* dev_status, kvd_stream_t stream);
+kvd_status kvd_append_paged_fp4(void* key_cache, void* value_cache, const void* k_new,
+                                const void* v_new, const int32_t* block_tables,
+                                const int32_t* seq_offset, const int32_t* pos, int Q, int NB,
+                                int BS, int cols, int Hkv, int D, kvd_dtype new_dtype,
+                                int32_t* dev_status, kvd_stream_t stream);
+/*
+ * kvd_attend_paged_fp8, kvd_attend_paged_fp4 -- kvd_attend_paged over
+ * quantised rows: key_cache, value_cache uint8 [NB, BS, Hkv, RB]; the same
+ * definition with every K/V element dequantised (scale * code value), the
+ * same sequence and block rules and status bits, and the precision rules of
+ * kvd_attend_masked_fp8 / _fp4.  Tiles are whole-row TMA boxes of the largest
+ * divisor of BS not above 64 rows; workspace and plan from the queries below
+ * (splits >= 1).
+ */
+size_t kvd_attend_paged_fp8_workspace_bytes(int Q, int Hq, int Hkv, int BS, int cols, int D,
+                                            int num_splits);
+size_t kvd_attend_paged_fp4_workspace_bytes(int Q, int Hq, int Hkv, int BS, int cols, int D,
+                                            int num_splits);
+kvd_status kvd_attend_paged_fp8_plan(int Q, int Hq, int Hkv, int BS, int cols, int D,
+                                     int num_splits, kvd_plan* plan);
+kvd_status kvd_attend_paged_fp4_plan(int Q, int Hq, int Hkv, int BS, int cols, int D,
+                                     int num_splits, kvd_plan* plan);
+kvd_status kvd_attend_paged_fp8(const void* q, const void* key_cache, const void* value_cache,
+                                const int32_t* block_tables, const int32_t* seq_lens,
+                                const int32_t* seq_offset, void* out, float* lse_out, int Q,
+                                int Hq, int Hkv, int NB, int BS, int cols, int D, float scale,
+                                int num_splits, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_status, kvd_stream_t stream);
+kvd_status kvd_attend_paged_fp4(const void* q, const void* key_cache, const void* value_cache,
+                                const int32_t* block_tables, const int32_t* seq_lens,
+                                const int32_t* seq_offset, void* out, float* lse_out, int Q,
+                                int Hq, int Hkv, int NB, int BS, int cols, int D, float scale,
+                                int num_splits, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_status, kvd_stream_t stream);
+/*
+ * kvd_attend_indexed_fp8, kvd_attend_indexed_fp4 -- kvd_attend_indexed over
+ * quantised rows: k_cache, v_cache uint8 [B, Hkv, C, RB]; the same definition
+ * (every entry with 0 <= indices[b, j] < C one softmax term, entries outside
+ * [-1, C) skipped and reported) with every K/V element dequantised; the
+ * listed rows are gathered whole (RB bytes) with 16-byte cp.async copies.
+ * Precision rules of kvd_attend_masked_fp8 / _fp4; workspace and plan from
+ * the queries below (splits of at most 128 entries).
+ */
+size_t kvd_attend_indexed_fp8_workspace_bytes(int B, int Hq, int Hkv, int topk, int D,
+                                              int num_splits);
+size_t kvd_attend_indexed_fp4_workspace_bytes(int B, int Hq, int Hkv, int topk, int D,
+                                              int num_splits);
+kvd_status kvd_attend_indexed_fp8_plan(int B, int Hq, int Hkv, int topk, int D, int num_splits,
+                                       kvd_plan* plan);
+kvd_status kvd_attend_indexed_fp4_plan(int B, int Hq, int Hkv, int topk, int D, int num_splits,
+                                       kvd_plan* plan);
+kvd_status kvd_attend_indexed_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* indices, void* out, float* lse_out, int B,
+                                  int Hq, int Hkv, int C, int topk, int D, float scale,
+                                  int num_splits, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, kvd_stream_t stream);
+kvd_status kvd_attend_indexed_fp4(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* indices, void* out, float* lse_out, int B,
+                                  int Hq, int Hkv, int C, int topk, int D, float scale,
+                                  int num_splits, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_status, kvd_stream_t stream);
+
+/*
  * kvd_attend_masked_noalloc -- the pages have no counterpart to this call; it
  * exists for callers that cannot allocate device memory.  Some host runtimes
  * own all device memory through their own allocator and hand a kernel library
