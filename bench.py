@@ -3,7 +3,8 @@
 decode tokens/s on GB300, through libkvd's C ABI.
 
     python bench.py [--gpus N] [--steps K] [--warmup W]
-                    [--workload gqa|long|paged|paged_gather|npuw|indexed|window|gqa_fp8|gqa_fp4]
+                    [--workload gqa|long|paged|paged_gather|npuw|indexed|window|gqa_fp8|gqa_fp4|
+                                paged_fp8|paged_fp4]
     python bench.py --impl reference ...     # the fp64 CPU oracle as the reference arm
 
 A step is one decode step of the workload: for the static-buffer workloads,
@@ -78,6 +79,15 @@ def paged_attend_bytes(lengths, Hq, Hkv, D, elem, BS):
     rows = sum(int(L) for L in lengths)
     entries = sum((int(L) + BS - 1) // BS for L in lengths)
     return rows * Hkv * D * 2 * elem + entries * 4 + (Q + 1) * 4 + 2 * Q * Hq * D * elem
+
+
+def paged_quant_attend_bytes(lengths, Hq, Hkv, D, row, BS):
+    """Valid quantised K and V rows (`row` bytes each), the block-table
+    entries the sequences use, the cumsum, bf16 q and out."""
+    Q = len(lengths)
+    rows = sum(int(L) for L in lengths)
+    entries = sum((int(L) + BS - 1) // BS for L in lengths)
+    return rows * Hkv * row * 2 + entries * 4 + (Q + 1) * 4 + 2 * Q * Hq * D * 2
 
 
 def gather_bytes(lengths, Hk, Dk, Hv, Dv, elem, BS):
@@ -244,16 +254,22 @@ def masked_config(name, w, layers, lengths0):
 
 
 def paged_config(pw, name="paged"):
-    NB, BS, Hkv, D = pw.key_cache.shape
-    Q, Hq, _ = pw.q.shape
+    NB, BS, Hkv, RB = pw.key_cache.shape
+    Q, Hq, D = pw.q.shape
     lengths = [int(x) for x in pw.lengths]
-    rows = 2 * sum(lengths) * Hkv * D * 2
-    return {"workload": name, "num_blocks": NB, "block_size": BS, "kv_heads": Hkv,
-            "q_heads": Hq, "head_dim": D, "sequences": Q, "dtype": "bf16",
-            "total_tokens": pw.total_tokens,
-            "l2": f"inputs larger than L2: {rows / 2**30:.2f} GiB of valid K/V rows per step "
-                  f"(of a {2 * pw.key_cache.numel() * 2 / 2**30:.0f} GiB cache) vs "
-                  f"{L2_BYTES // 2**20} MiB L2"}
+    row = pw.key_cache.element_size() * RB  # bytes of one K (or V) row of one kv head
+    rows = 2 * sum(lengths) * Hkv * row
+    cache = 2 * pw.key_cache.numel() * pw.key_cache.element_size()
+    c = {"workload": name, "num_blocks": NB, "block_size": BS, "kv_heads": Hkv,
+         "q_heads": Hq, "head_dim": D, "sequences": Q, "dtype": "bf16",
+         "total_tokens": pw.total_tokens,
+         "l2": f"inputs larger than L2: {rows / 2**30:.2f} GiB of valid K/V rows per step "
+               f"(of a {cache / 2**30:.1f} GiB cache) vs {L2_BYTES // 2**20} MiB L2"}
+    if name in PAGED_QUANT:
+        fmt = PAGED_QUANT[name]
+        c.update({"dtype": f"{fmt.lower()} K/V, bf16 q/out",
+                  "kv_format": f"{fmt} codes + fp32 row scale, {row}-byte rows"})
+    return c
 
 
 def workload_config(name):
@@ -262,6 +278,8 @@ def workload_config(name):
     import workloads
     if name in ("paged", "paged_gather"):
         return paged_config(workloads.paged(device="cpu"), name)
+    if name in PAGED_QUANT:
+        return paged_config(workloads.paged_quant(name[-3:], device="cpu"), name)
     gen = {"indexed": "gqa"}.get(name, name)
     w = getattr(workloads, gen)(device="cpu", layers=1)
     return masked_config(name, w, LAYERS[name], [int(x) for x in w.layers[0].lengths])
@@ -269,6 +287,9 @@ def workload_config(name):
 
 ROW_PAD = 16  # quantised rows: codes, fp32 scale, 12 zero bytes
 QUANT_FORMATS = {"gqa_fp8": "E4M3", "gqa_fp4": "E2M1"}
+# the paged workload over quantised rows
+PAGED_QUANT = {"paged_fp8": "E4M3", "paged_fp4": "E2M1"}
+KV_FORMATS = {**QUANT_FORMATS, **PAGED_QUANT}
 
 
 def quant_row_bytes(name, D):
@@ -692,6 +713,60 @@ class PagedBench:
         return paged_config(self.pw, self.name)
 
 
+class PagedQuantBench(PagedBench):
+    """The paged decode step over quantised caches: every sequence's new K/V
+    row quantised into its block (kvd_append_paged_fp8 / _fp4), then the
+    paged attention over the quantised rows (kvd_attend_paged_fp8 / _fp4);
+    the paged workload's sequences and tables."""
+
+    def __init__(self, name, torch, kvd, dev):
+        import workloads
+        self.torch, self.kvd, self.dev, self.name = torch, kvd, dev, name
+        self.fmt = name[-3:]
+        self.gather_mode = False
+        pw = workloads.paged_quant(self.fmt, device=dev)
+        self.pw = pw
+        self.Q, self.Hq, self.D = pw.q.shape
+        self.NB, self.BS, self.Hkv, self.row = pw.key_cache.shape
+        self.elem = 2
+        self.layers = 1
+        self.lengths = [int(x) for x in pw.lengths]
+        self.out = torch.empty_like(pw.q)
+        cols = pw.block_tables.shape[1]
+        need = kvd.attend_paged_quant_workspace_bytes(self.fmt, self.Q, self.Hq, self.Hkv,
+                                                      self.BS, cols, self.D)
+        self.ws = kvd.workspace(need, dev)
+        self.status = kvd.status_tensor(dev)
+        self.graph = None
+
+    def _attend(self):
+        pw = self.pw
+        self.kvd.attend_paged_quant(self.fmt, pw.q, pw.key_cache, pw.value_cache, pw.block_tables,
+                                    pw.seq_lens, pw.seq_offset, pw.scale, out=self.out,
+                                    workspace=self.ws, dev_status=self.status)
+
+    def _append(self):
+        pw = self.pw
+        append = self.kvd.append_paged_fp8 if self.fmt == "fp8" else self.kvd.append_paged_fp4
+        append(pw.key_cache, pw.value_cache, pw.block_tables, pw.seq_offset, pw.k_new, pw.v_new,
+               pw.pos, dev_status=self.status)
+
+    def attend_bytes(self, j):
+        return paged_quant_attend_bytes(self.lengths, self.Hq, self.Hkv, self.D, self.row, self.BS)
+
+    def step_bytes(self, j):
+        return self.attend_bytes(j) + quant_append_bytes(self.Q, self.Hkv, self.D, self.row)
+
+    def attention_plan(self):
+        cols = self.pw.block_tables.shape[1]
+        return self.kvd.attend_paged_quant_plan(self.fmt, self.Q, self.Hq, self.Hkv, self.BS,
+                                                cols, self.D)
+
+    def kernel_name(self):
+        return attention_kernel_name(f"{PAGED_QUANT[self.name]} tensor-core", self.attention_plan(),
+                                     self.Hq // self.Hkv, mode="paged")
+
+
 class IndexedBench(MaskedBench):
     """Top-k sparse decode on the batched-GQA caches: every layer appends the
     step's K/V row, then attends over 2048 slots per batch entry drawn once
@@ -850,6 +925,8 @@ class QuantBench(MaskedBench):
 def make_bench(name, torch, kvd, dev, layers=None):
     if name in ("paged", "paged_gather"):
         return PagedBench(torch, kvd, dev, name)
+    if name in PAGED_QUANT:
+        return PagedQuantBench(name, torch, kvd, dev)
     if name in QUANT_FORMATS:
         return QuantBench(name, torch, kvd, dev, layers)
     if name == "indexed":
@@ -1176,6 +1253,21 @@ def oracle_rate(name, seconds):
                                 pw.seq_offset, pw.scale)
         return run(step, paged_attend_bytes(lengths, 32, 8, 128, 2, 128) + append_bytes(64, 8, 128, 2),
                    "paged append + attention of all 64 sequences")
+    if name in PAGED_QUANT:
+        fmt = name[-3:]
+        pw = workloads.paged_quant(fmt, device="cpu")
+        lengths = [int(x) for x in pw.lengths]
+        kb, vb = pw.key_cache.numpy(), pw.value_cache.numpy()
+        row = kb.shape[-1]
+
+        def step(n):
+            oracle.append_paged_quant(kb, vb, pw.block_tables, pw.seq_offset, pw.k_new, pw.v_new,
+                                      pw.pos, fmt)
+            oracle.attend_paged_quant(pw.q, kb, vb, pw.block_tables, pw.seq_lens, pw.seq_offset,
+                                      pw.scale, fmt)
+        return run(step, paged_quant_attend_bytes(lengths, 32, 8, 128, row, 128)
+                   + quant_append_bytes(64, 8, 128, row),
+                   f"quantising paged append + {PAGED_QUANT[name]} paged attention of all 64 sequences")
     if name == "indexed":
         w = workloads.gqa(device="cpu", layers=1)
         lay = w.layers[0]
@@ -1268,7 +1360,7 @@ def main():
     ap.add_argument("--impl", default="kvd", choices=["kvd", "reference"])
     ap.add_argument("--workload", default="gqa",
                     choices=["gqa", "long", "paged", "paged_gather", "npuw", "indexed", "window",
-                             "gqa_fp8", "gqa_fp4"])
+                             "gqa_fp8", "gqa_fp4", "paged_fp8", "paged_fp4"])
     ap.add_argument("--no-others", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="oracle seconds for the main workload's CPU baseline")
@@ -1369,7 +1461,7 @@ def main():
     others = {}
     if not args.no_others:
         for name in ("long", "paged", "paged_gather", "npuw", "gqa", "indexed", "window",
-                     "gqa_fp8", "gqa_fp4"):
+                     "gqa_fp8", "gqa_fp4", "paged_fp8", "paged_fp4"):
             if name == args.workload:
                 continue
             log(f"workload {name}")
@@ -1396,8 +1488,8 @@ def main():
             "metric": METRIC, "value": res["gbs"], "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": ("bf16" if args.workload not in QUANT_FORMATS
-                      else f"{QUANT_FORMATS[args.workload].lower()} kv / bf16"),
+            "dtype": ("bf16" if args.workload not in KV_FORMATS
+                      else f"{KV_FORMATS[args.workload].lower()} kv / bf16"),
             "data": "synthetic", "config": b.config(),
             "peak_source": peak_src,
             "timing": "each timed step is one CUDA-graph replay of the decode step "

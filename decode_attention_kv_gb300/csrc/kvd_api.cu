@@ -851,8 +851,18 @@ kvd_status append_paged_quant(const char* fn, bool fp4, void* key_cache, void* v
     return ok();
 }
 
+// Paged caches of quantised rows: the tensor-core consumers' dependent chain,
+// not HBM, sets the tile rate (about 1.4 us per 64-row tile per CTA), so
+// long units leave a long tail; the default is equal splits of kQuantPagedChunk
+// slots (four tiles).  Measured on 64 sequences of 1..4096 tokens, 8 kv heads,
+// E4M3 rows: the general plan's 5 splits 110 us, 8: 101, 11: 92, 16: 84, 22:
+// 89, 32: 101 us per attention call; E2M1 rows 87, 77, 73, 76, 82, 95 us.
+constexpr int kQuantPagedChunk = 256;
+
 Plan paged_quant_plan(int Q, int Hq, int Hkv, int BS, int cols, int D, int num_splits) {
-    return plan_attention(Q, Hq, Hkv, cols * BS, D, KVD_BF16, BS, num_splits, false, kQuantTile);
+    const long long cap = (long long)cols * BS;
+    if (num_splits <= 0) num_splits = (int)((cap + kQuantPagedChunk - 1) / kQuantPagedChunk);
+    return plan_attention(Q, Hq, Hkv, (int)cap, D, KVD_BF16, BS, num_splits, false, kQuantTile);
 }
 
 kvd_status attend_paged_quant(const char* fn, RowKind rk, const void* q, const void* key_cache,

@@ -50,6 +50,20 @@ def test_quantised_accounting_row_formats():
         assert bench.quant_append_bytes(4, Hkv, D, row) == 4 * Hkv * 2 * (256 + row)
 
 
+def test_paged_quantised_accounting():
+    """The paged quantised step counts the valid quantised rows (144 or 80
+    bytes), the table entries, the cumsum and the bf16 q and out: a bf16-row
+    "quantised" row of 2 D bytes gives back the paged figure."""
+    lengths, Hq, Hkv, D, BS = [1, 128, 129, 4000], 32, 8, 128, 128
+    assert bench.paged_quant_attend_bytes(lengths, Hq, Hkv, D, 2 * D, BS) == \
+        bench.paged_attend_bytes(lengths, Hq, Hkv, D, 2, BS)
+    side = (1 + 1 + 2 + 32) * 4 + 5 * 4 + 2 * 4 * Hq * D * 2
+    for row in (144, 80):
+        assert bench.paged_quant_attend_bytes(lengths, Hq, Hkv, D, row, BS) == \
+            sum(lengths) * Hkv * row * 2 + side
+    assert bench.KV_FORMATS["paged_fp8"] == "E4M3" and bench.KV_FORMATS["gqa_fp4"] == "E2M1"
+
+
 def test_indexed_accounting_counts_listed_rows_and_whole_lists():
     """Only the listed rows are read; every query's list is read whole
     (topk int32 entries, padding included)."""

@@ -4,8 +4,8 @@ benchmark times (library-planned splits), every output element compared.
 Workloads (see workloads.py): the 1152-slot static buffer (MHA 32 x 128,
 bf16), batched GQA (16 x 32/8 heads, capacity 8192, lengths 512..8192), the
 paged cache (8192 blocks of 128 slots x 8 heads x 128, 64 sequences of
-1..4096 tokens), the 32768-token single sequence and its 4096-slot sliding
-window.  The static-buffer steps run both ways a caller can run them: the
+1..4096 tokens; also over E4M3 and E2M1 rows), the 32768-token single
+sequence and its 4096-slot sliding window.  The static-buffer steps run both ways a caller can run them: the
 append and the attention as two calls, and the fused call the benchmark
 times (the append inside the attention launch).  The fp64 oracle computes
 the whole layer (every batch entry, every head) on the host cores.
@@ -156,6 +156,33 @@ def test_paged_full_size(kvd):
     assert err == 0
     assert np.array_equal(_bits(ko), rk), "gather: key buffer not bit-exact"
     assert np.array_equal(_bits(vo), rv), "gather: value buffer not bit-exact"
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "fp4"])
+def test_paged_quant_full_size(kvd, fmt):
+    """The paged workload over E4M3 / E2M1 rows, as the benchmark's step
+    runs it: the quantising paged append of every sequence's last token
+    (both caches byte for byte), then the paged attention of all 64
+    sequences x 32 query heads."""
+    pw = W.paged_quant(fmt, device="cuda")
+    kh, vh = host(pw.key_cache).numpy().copy(), host(pw.value_cache).numpy().copy()
+    status = kvd.status_tensor()
+    append = kvd.append_paged_fp8 if fmt == "fp8" else kvd.append_paged_fp4
+    append(pw.key_cache, pw.value_cache, pw.block_tables, pw.seq_offset, pw.k_new, pw.v_new,
+           pw.pos, dev_status=status)
+    lse = torch.empty(pw.q.shape[:2], device="cuda")
+    out = kvd.attend_paged_quant(fmt, pw.q, pw.key_cache, pw.value_cache, pw.block_tables,
+                                 pw.seq_lens, pw.seq_offset, pw.scale, lse=lse, dev_status=status)
+    bt, sl, so = host(pw.block_tables), host(pw.seq_lens), host(pw.seq_offset)
+    assert oracle.append_paged_quant(kh, vh, bt, so, host(pw.k_new), host(pw.v_new),
+                                     host(pw.pos), fmt) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(host(pw.key_cache).numpy(), kh), f"paged {fmt} append (K)"
+    assert np.array_equal(host(pw.value_cache).numpy(), vh), f"paged {fmt} append (V)"
+    ref, rl = oracle.attend_paged_quant(host(pw.q), kh, vh, bt, sl, so, pw.scale, fmt)
+    assert_attention_close(out, ref, torch.bfloat16, f"paged {fmt} attention, all sequences")
+    assert_lse_close(lse, rl, f"paged {fmt} attention lse")
 
 
 @pytest.mark.parametrize("name", ["gqa", "long"])

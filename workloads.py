@@ -44,7 +44,7 @@ from dataclasses import dataclass, field
 import torch
 
 SEEDS = {"tiny": 1, "npuw": 2, "gqa": 3, "paged": 4, "long": 5, "window": 6, "gqa_fp8": 7,
-         "gqa_fp4": 8}
+         "gqa_fp4": 8, "paged_fp8": 9, "paged_fp4": 10}
 
 
 def generator(seed: int, device="cpu") -> torch.Generator:
@@ -358,18 +358,27 @@ class PagedWorkload:
 
 def paged(device="cpu", seed: int | None = None, NB: int = 8192, BS: int = 128,
           Hkv: int = 8, D: int = 128, Q: int = 64, cols: int = 32, Hq: int = 32,
-          lo: int = 1, hi: int = 4096, dtype=torch.bfloat16) -> PagedWorkload:
+          lo: int = 1, hi: int = 4096, dtype=torch.bfloat16, rows: str | None = None,
+          content_seed: int | None = None) -> PagedWorkload:
     """Paged cache addressed through a permuted block table.  Lengths, block
     tables and offsets are drawn on the CPU (small), caches and q on
-    ``device``."""
+    ``device``.  rows = "fp8" / "fp4": quantised K/V rows (``fp8_rows`` /
+    ``fp4_rows``, uint8 [NB, BS, Hkv, row bytes]) instead of `dtype` rows;
+    q and the new rows stay bf16."""
     s = SEEDS["paged"] if seed is None else seed
     gl = generator(s, "cpu")
     lengths = randint(gl, Q, lo, hi)
     bt = permuted_block_tables(gl, Q, cols, NB)
     sl = cumsum_lengths(lengths)
-    g = generator(s + 1000, device)
-    kc = randn(g, (NB, BS, Hkv, D), dtype, device)
-    vc = randn(g, (NB, BS, Hkv, D), dtype, device)
+    g = generator((s if content_seed is None else content_seed) + 1000, device)
+    if rows is None:
+        kc = randn(g, (NB, BS, Hkv, D), dtype, device)
+        vc = randn(g, (NB, BS, Hkv, D), dtype, device)
+    else:
+        make = {"fp8": fp8_rows, "fp4": fp4_rows}[rows]
+        kc = make(g, (NB, BS, Hkv), D, device=device)
+        vc = make(g, (NB, BS, Hkv), D, device=device)
+        dtype = torch.bfloat16
     q = randn(g, (Q, Hq, D), dtype, device)
     k_new = randn(g, (Q, Hkv, D), dtype, device)
     v_new = randn(g, (Q, Hkv, D), dtype, device)
@@ -379,3 +388,10 @@ def paged(device="cpu", seed: int | None = None, NB: int = 8192, BS: int = 128,
                          lengths=lengths, total_tokens=int(sl[-1]),
                          scale=1.0 / math.sqrt(D), k_new=k_new, v_new=v_new,
                          pos=(lengths - 1).to(torch.int32).to(device))
+
+
+def paged_quant(fmt: str, device="cpu") -> PagedWorkload:
+    """The paged workload's sequences, tables and offsets over quantised
+    caches (E4M3 rows for "fp8", E2M1 rows for "fp4"; the gqa_fp8 / gqa_fp4
+    row contents), bf16 q and new rows."""
+    return paged(device=device, rows=fmt, content_seed=SEEDS[f"paged_{fmt}"])
