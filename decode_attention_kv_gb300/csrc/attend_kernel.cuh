@@ -321,32 +321,54 @@ __device__ __forceinline__ SplitRange split_range(const AttendParams& p, int bz,
 // rows or quantised rows), each chunk landing where the consumer's layout
 // puts it.  (Per-row TMA boxes, four rows per box at best, issue too slowly
 // here: the tensor engine's per-copy cost bounds a 512-byte box.)
-template <class Cons, int D>
-__device__ __forceinline__ void gather_rows(unsigned char* gk, unsigned char* gv,
-                                            const unsigned char* k, const unsigned char* v,
-                                            size_t plane, int slot, int row0, int row1, int n,
-                                            int lane, uint64_t pol) {
+template <class Cons, typename Elem, int D>
+__device__ __forceinline__ void gather_rows(unsigned char* gk, unsigned char* gv, const void* k,
+                                            const void* v, size_t plane, int slot, int row0,
+                                            int row1, int n, int lane, uint64_t pol) {
     constexpr int kHalves = D / 64;
-    constexpr int kRB = Cons::kRowBytes;
-    static_assert(kRB % 16 == 0 && kRB <= 512, "rows of whole 16-byte chunks, one warp pass");
-    constexpr int cpr = kRB / 16, rpi = 32 / cpr;
-    const int c = lane % cpr;
-    const unsigned char* kb = k + plane * kRB + c * 16;
-    const unsigned char* vb = v + plane * kRB + c * 16;
     const int rows = min(n, row1) - row0;
+    if constexpr (Cons::kRowBytes == D * (int)sizeof(Elem)) {
+        // element rows: D * sizeof(Elem) = 128, 256 or 512 bytes, a power of
+        // two of chunks, so whole rows fill the warp
+        constexpr int cpr = D * (int)sizeof(Elem) / 16, rpi = 32 / cpr;
+        constexpr int epc = 16 / (int)sizeof(Elem);  // elements per chunk
+        const int c = lane % cpr;
+        const Elem* kb = static_cast<const Elem*>(k) + plane * D + c * epc;
+        const Elem* vb = static_cast<const Elem*>(v) + plane * D + c * epc;
 #pragma unroll 4
-    for (int rb = 0; rb < rows; rb += rpi) {
-        const int rr = rb + lane / cpr;
-        const int slot_row = __shfl_sync(0xffffffffu, slot, rr & 31);
-        if (lane < rpi * cpr && rr < rows && slot_row >= 0) {
-            const int row = row0 + rr;
-            uint32_t off;
-            if constexpr (Cons::kSwizzled)
-                off = (c >> 3) * (Cons::kTileBytes / kHalves) + swz128(row, c & 7);
-            else
-                off = row * kRB + c * 16;
-            cp_async16(gk + off, kb + (size_t)slot_row * kRB, pol);
-            cp_async16(gv + off, vb + (size_t)slot_row * kRB, pol);
+        for (int rb = 0; rb < rows; rb += rpi) {
+            const int rr = rb + lane / cpr;
+            const int slot_row = __shfl_sync(0xffffffffu, slot, rr & 31);
+            if (rr < rows && slot_row >= 0) {
+                const int row = row0 + rr;
+                uint32_t off;
+                if constexpr (Cons::kSwizzled)
+                    off = (c >> 3) * (Cons::kTileBytes / kHalves) + swz128(row, c & 7);
+                else
+                    off = row * D * (int)sizeof(Elem) + c * 16;
+                cp_async16(gk + off, kb + (size_t)slot_row * D, pol);
+                cp_async16(gv + off, vb + (size_t)slot_row * D, pol);
+            }
+        }
+    } else {
+        // quantised rows (D + 16 or D/2 + 16 bytes: 3 to 9 chunks): 32 / cpr
+        // whole rows per pass, the lanes past them idle
+        constexpr int kRB = Cons::kRowBytes;
+        static_assert(kRB % 16 == 0 && kRB <= 512, "rows of whole 16-byte chunks");
+        static_assert(!Cons::kSwizzled, "quantised rows land unswizzled");
+        constexpr int cpr = kRB / 16, rpi = 32 / cpr;
+        const int c = lane % cpr;
+        const unsigned char* kb = static_cast<const unsigned char*>(k) + plane * kRB + c * 16;
+        const unsigned char* vb = static_cast<const unsigned char*>(v) + plane * kRB + c * 16;
+#pragma unroll 4
+        for (int rb = 0; rb < rows; rb += rpi) {
+            const int rr = rb + lane / cpr;
+            const int slot_row = __shfl_sync(0xffffffffu, slot, rr & 31);
+            if (lane < rpi * cpr && rr < rows && slot_row >= 0) {
+                const uint32_t off = (row0 + rr) * kRB + c * 16;
+                cp_async16(gk + off, kb + (size_t)slot_row * kRB, pol);
+                cp_async16(gv + off, vb + (size_t)slot_row * kRB, pol);
+            }
         }
     }
 }
@@ -804,11 +826,9 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                                       ? sl.blocks[r0 + row] : -1;
                 if (n > row0) {
                     unsigned char* gk = smem + stage * Sh::kStageBytes;
-                    gather_rows<Cons, D>(gk, gk + Cons::kTileBytes,
-                                         static_cast<const unsigned char*>(p.k),
-                                         static_cast<const unsigned char*>(p.v),
-                                         ((size_t)un.bz * p.Hkv + un.kvh) * p.C, s_row, row0,
-                                         row1, n, lane, pol);
+                    gather_rows<Cons, Elem, D>(gk, gk + Cons::kTileBytes, p.k, p.v,
+                                               ((size_t)un.bz * p.Hkv + un.kvh) * p.C, s_row,
+                                               row0, row1, n, lane, pol);
                 }
                 cp_async_mbar_arrive(&ctl.full[stage]);
                 __syncwarp();
@@ -1040,11 +1060,9 @@ attend_kernel(const AttendParams p, const __grid_constant__ CUtensorMap kmap,
                     unsigned char* gk = smem + stage * Sh::kStageBytes;
                     const int g1 = gather_row(1);
                     const int s_lo = lane < min(n, g1) && ((bits >> lane) & 1ull) ? sl.blocks[r0 + lane] : -1;
-                    gather_rows<Cons, D>(gk, gk + Cons::kTileBytes,
-                                         static_cast<const unsigned char*>(p.k),
-                                         static_cast<const unsigned char*>(p.v),
-                                         ((size_t)un.bz * p.Hkv + un.kvh) * p.C, s_lo, 0, g1, n,
-                                         lane, pol);
+                    gather_rows<Cons, Elem, D>(gk, gk + Cons::kTileBytes, p.k, p.v,
+                                               ((size_t)un.bz * p.Hkv + un.kvh) * p.C, s_lo, 0, g1,
+                                               n, lane, pol);
                     cp_async_mbar_arrive(&ctl.full[stage]);
                     __syncwarp();
                 }
