@@ -49,16 +49,16 @@ L2_BYTES = 129 * 1024 * 1024
 # kernel sources it was taken on: reported only while the sources still hash
 # to that revision, else null.
 NCU_TRAFFIC = {
-    ("npuw", "57dbeb6034599648"): 17890560,  # attend_small_kernel, tensor-core consumers, 1152-slot buffer
-    ("gqa", "57dbeb6034599648"): 212783872,  # attend_kernel, tensor-core consumers, batched GQA
-    ("long", "57dbeb6034599648"): 540665600,  # attend_kernel, CUDA-core consumers, 32768 slots
-    ("paged", "57dbeb6034599648"): 521760512,  # attend_kernel, paged mode
-    ("indexed", "57dbeb6034599648"): 122495744,  # attend_kernel, index-list mode, gather warp
-    ("window", "57dbeb6034599648"): 67912704,  # attend_kernel, window entry, 4096-slot window
-    ("gqa_fp8", "57dbeb6034599648"): 120538112,  # attend_kernel, E4M3 consumers
-    ("gqa_fp4", "57dbeb6034599648"): 66420480,  # attend_kernel, E2M1 consumers
-    ("paged_fp8", "57dbeb6034599648"): 308373760,  # attend_kernel, paged mode, E4M3 rows
-    ("paged_fp4", "57dbeb6034599648"): 166990592,  # attend_kernel, paged mode, E2M1 rows
+    ("npuw", "f081e2091b51ce68"): 17892096,  # attend_small_kernel, tensor-core consumers, 1152-slot buffer
+    ("gqa", "f081e2091b51ce68"): 212512000,  # attend_kernel, tensor-core consumers, batched GQA
+    ("long", "f081e2091b51ce68"): 540379648,  # attend_kernel, CUDA-core consumers, 32768 slots
+    ("paged", "f081e2091b51ce68"): 521817088,  # attend_kernel, paged mode
+    ("indexed", "f081e2091b51ce68"): 122609408,  # attend_kernel, index-list mode, gather warp
+    ("window", "f081e2091b51ce68"): 67960832,  # attend_kernel, window entry, 4096-slot window
+    ("gqa_fp8", "f081e2091b51ce68"): 120547328,  # attend_kernel, E4M3 consumers
+    ("gqa_fp4", "f081e2091b51ce68"): 66348288,  # attend_kernel, E2M1 consumers
+    ("paged_fp8", "f081e2091b51ce68"): 308250880,  # attend_kernel, paged mode, E4M3 rows
+    ("paged_fp4", "f081e2091b51ce68"): 167010816,  # attend_kernel, paged mode, E2M1 rows
 }
 
 # ------------------------------------------------------------ byte accounting
