@@ -445,6 +445,69 @@ def attend_indexed_quant(fmt, q, k_cache, v_cache, indices, scale=None, out=None
     return out
 
 
+# the C entry points' own names
+def attend_paged_fp8_workspace_bytes(Q, Hq, Hkv, BS, cols, D, num_splits=0):
+    return attend_paged_quant_workspace_bytes("fp8", Q, Hq, Hkv, BS, cols, D, num_splits)
+
+
+def attend_paged_fp4_workspace_bytes(Q, Hq, Hkv, BS, cols, D, num_splits=0):
+    return attend_paged_quant_workspace_bytes("fp4", Q, Hq, Hkv, BS, cols, D, num_splits)
+
+
+def attend_paged_fp8_plan(Q, Hq, Hkv, BS, cols, D, num_splits=0):
+    return attend_paged_quant_plan("fp8", Q, Hq, Hkv, BS, cols, D, num_splits)
+
+
+def attend_paged_fp4_plan(Q, Hq, Hkv, BS, cols, D, num_splits=0):
+    return attend_paged_quant_plan("fp4", Q, Hq, Hkv, BS, cols, D, num_splits)
+
+
+def attend_paged_fp8(q, key_cache, value_cache, block_tables, seq_lens, seq_offset=None,
+                     scale=None, out=None, lse=None, num_splits=0, workspace=None,
+                     dev_status=None):
+    """kvd_attend_paged_fp8: paged decode attention over E4M3 rows."""
+    return attend_paged_quant("fp8", q, key_cache, value_cache, block_tables, seq_lens,
+                              seq_offset, scale, out, lse, num_splits, workspace, dev_status)
+
+
+def attend_paged_fp4(q, key_cache, value_cache, block_tables, seq_lens, seq_offset=None,
+                     scale=None, out=None, lse=None, num_splits=0, workspace=None,
+                     dev_status=None):
+    """kvd_attend_paged_fp4: paged decode attention over E2M1 rows."""
+    return attend_paged_quant("fp4", q, key_cache, value_cache, block_tables, seq_lens,
+                              seq_offset, scale, out, lse, num_splits, workspace, dev_status)
+
+
+def attend_indexed_fp8_workspace_bytes(B, Hq, Hkv, topk, D, num_splits=0):
+    return attend_indexed_quant_workspace_bytes("fp8", B, Hq, Hkv, topk, D, num_splits)
+
+
+def attend_indexed_fp4_workspace_bytes(B, Hq, Hkv, topk, D, num_splits=0):
+    return attend_indexed_quant_workspace_bytes("fp4", B, Hq, Hkv, topk, D, num_splits)
+
+
+def attend_indexed_fp8_plan(B, Hq, Hkv, topk, D, num_splits=0):
+    return attend_indexed_quant_plan("fp8", B, Hq, Hkv, topk, D, num_splits)
+
+
+def attend_indexed_fp4_plan(B, Hq, Hkv, topk, D, num_splits=0):
+    return attend_indexed_quant_plan("fp4", B, Hq, Hkv, topk, D, num_splits)
+
+
+def attend_indexed_fp8(q, k_cache, v_cache, indices, scale=None, out=None, lse=None,
+                       num_splits=0, workspace=None, dev_status=None):
+    """kvd_attend_indexed_fp8: index-list decode attention over E4M3 rows."""
+    return attend_indexed_quant("fp8", q, k_cache, v_cache, indices, scale, out, lse, num_splits,
+                                workspace, dev_status)
+
+
+def attend_indexed_fp4(q, k_cache, v_cache, indices, scale=None, out=None, lse=None,
+                       num_splits=0, workspace=None, dev_status=None):
+    """kvd_attend_indexed_fp4: index-list decode attention over E2M1 rows."""
+    return attend_indexed_quant("fp4", q, k_cache, v_cache, indices, scale, out, lse, num_splits,
+                                workspace, dev_status)
+
+
 def pointer_array(tensors, device):
     """A device int64 tensor holding the data pointers of `tensors` (the
     pointer arrays of kvd_copy_prefix).  Keep it alive until the call has run."""

@@ -178,3 +178,16 @@ def test_window_entry_points(lib):
     assert lib.kvd_append_attend_window(*fused, 0, *tail) == 1
     assert lib.kvd_append_attend_window(*fused[:6], None, *fused[7:], 64, *tail) == 1
     assert kvd.attend_window_plan(2, 8, 8, 1152, 128, 64).splits >= 1
+
+
+def test_binding_names_follow_the_c_entry_points():
+    """Every compute or query entry point of include/kvd.h has a binding
+    function of the same name without the kvd_ prefix (the diagnostics
+    kvd_status_string, kvd_last_error and kvd_version surface through the
+    binding's exceptions instead)."""
+    from decode_attention_kv_gb300 import kvd
+    header = open(os.path.join(ROOT, "include", "kvd.h")).read()
+    names = set(re.findall(r"\b(kvd_[a-z0-9_]+)\s*\(", header))
+    skip = {"kvd_status_string", "kvd_last_error", "kvd_version"}
+    missing = sorted(n for n in names - skip if not hasattr(kvd, n[len("kvd_"):]))
+    assert not missing, missing

@@ -213,3 +213,30 @@ def test_indexed_quant_bad_entries(kvd, fmt):
     assert torch.all(out[2] == 0) and torch.all(torch.isneginf(lse[2]))
     assert_attention_close(out, ref, torch.bfloat16, f"indexed {fmt}, bad entries")
     assert_lse_close(lse, ref_lse, f"indexed {fmt}, bad entries lse")
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "fp4"])
+def test_named_bindings_match_the_format_argument(kvd, fmt):
+    """kvd.attend_paged_fp8 / _fp4 and kvd.attend_indexed_fp8 / _fp4 (the C
+    entry points' names) give the same bytes as the format-argument forms."""
+    g = W.generator(990)
+    Q, Hq, Hkv, BS, cols, D, NB = 2, 8, 2, 32, 4, 128, 12
+    q = W.randn(g, (Q, Hq, D), torch.bfloat16).cuda()
+    kc = ROWS[fmt](g, (NB, BS, Hkv), D).cuda()
+    vc = ROWS[fmt](g, (NB, BS, Hkv), D).cuda()
+    bt = W.permuted_block_tables(g, Q, cols, NB).cuda()
+    sl = W.cumsum_lengths([100, 37]).cuda()
+    a = getattr(kvd, f"attend_paged_{fmt}")(q, kc, vc, bt, sl)
+    b = kvd.attend_paged_quant(fmt, q, kc, vc, bt, sl)
+    plan = getattr(kvd, f"attend_paged_{fmt}_plan")(Q, Hq, Hkv, BS, cols, D)
+    assert plan.splits == kvd.attend_paged_quant_plan(fmt, Q, Hq, Hkv, BS, cols, D).splits
+    k = ROWS[fmt](g, (Q, Hkv, 300), D).cuda()
+    v = ROWS[fmt](g, (Q, Hkv, 300), D).cuda()
+    idx = W.index_lists([300, 90], 128, seed=3).cuda()
+    c = getattr(kvd, f"attend_indexed_{fmt}")(q, k, v, idx)
+    d = kvd.attend_indexed_quant(fmt, q, k, v, idx)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(c.view(torch.int16), d.view(torch.int16))
+    assert getattr(kvd, f"attend_indexed_{fmt}_workspace_bytes")(Q, Hq, Hkv, 128, D) == \
+        kvd.attend_indexed_quant_workspace_bytes(fmt, Q, Hq, Hkv, 128, D)
